@@ -1,0 +1,179 @@
+"""CPU oracle for C = epi(A·B) — TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The library under test never imports,
+links or calls it; the two share no code.
+
+The arithmetic lives in ``tgemm_oracle.c`` (plain C, fp64 accumulation, one
+round-to-nearest-even to fp16).  This module builds it with gcc on first use
+and wraps it with ctypes.  See that file's header for the passages it follows
+and the readings it takes.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "tgemm_oracle.c")
+_LIB = os.path.join(_HERE, "_liboracle.so")
+_lock = threading.Lock()
+_default = None
+
+
+def compile_source(src: str, out: str) -> str:
+    """gcc-compile one C file into a shared library (OpenMP when available)."""
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", src, "-o", out + ".tmp", "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True, text=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True, text=True)
+    os.replace(out + ".tmp", out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle next to its source. Returns the .so path."""
+    with _lock:
+        if (not force and os.path.exists(_LIB)
+                and os.path.getmtime(_LIB) >= os.path.getmtime(SOURCE)):
+            return _LIB
+        return compile_source(SOURCE, _LIB)
+
+
+def _ptr(a, ct):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(ct))
+
+
+def _as_u16(x: np.ndarray) -> np.ndarray:
+    if x.dtype == np.float16:
+        x = x.view(np.uint16)
+    if x.dtype != np.uint16:
+        raise TypeError("expected float16 or uint16 bits")
+    return np.ascontiguousarray(x)
+
+
+class Oracle:
+    """ctypes view of one build of ``tgemm_oracle.c``."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        i64 = ctypes.c_int64
+        lib.oracle_gemm_f16.argtypes = [u16p, u16p, u16p, f64p, i64, i64, i64, i64, i64, i64,
+                                        ctypes.c_int]
+        lib.oracle_gemm_f16.restype = ctypes.c_int
+        lib.oracle_gemm_f16_at.argtypes = [u16p, u16p, i64, i64, i64, ctypes.c_int, i64p, i64p,
+                                           i64, u16p, f64p]
+        lib.oracle_gemm_f16_at.restype = ctypes.c_int
+        lib.oracle_f16_from_f64_array.argtypes = [f64p, u16p, i64]
+        lib.oracle_f64_from_f16_array.argtypes = [u16p, f64p, i64]
+        lib.oracle_num_threads.restype = ctypes.c_int
+        self.lib = lib
+        self.path = path
+
+    def num_threads(self) -> int:
+        return int(self.lib.oracle_num_threads())
+
+    def f16_from_f64(self, x) -> np.ndarray:
+        """Round float64 values to binary16 bits (RNE), element-wise."""
+        x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+        out = np.empty(x.shape, dtype=np.uint16)
+        self.lib.oracle_f16_from_f64_array(_ptr(x, ctypes.c_double),
+                                           _ptr(out, ctypes.c_uint16), x.size)
+        return out
+
+    def f64_from_f16(self, h) -> np.ndarray:
+        """Decode binary16 bits to float64, element-wise."""
+        h = _as_u16(np.asarray(h))
+        out = np.empty(h.shape, dtype=np.float64)
+        self.lib.oracle_f64_from_f16_array(_ptr(h, ctypes.c_uint16),
+                                           _ptr(out, ctypes.c_double), h.size)
+        return out
+
+    def gemm(self, A: np.ndarray, B: np.ndarray, M: int, N: int, K: int,
+             relu: bool = False, want_ref: bool = False):
+        """Full product of A (M×lda fp16, lda ≥ K) and B (K×ldb fp16, ldb ≥ N).
+
+        Returns C as float16 (M×N) and, if ``want_ref``, the fp64 values
+        epi(sum) before rounding (M×N).
+        """
+        A = _as_u16(A)
+        B = _as_u16(B)
+        lda = A.shape[1] if A.ndim == 2 else K
+        ldb = B.shape[1] if B.ndim == 2 else N
+        C = np.empty((M, N), dtype=np.uint16)
+        ref = np.empty((M, N), dtype=np.float64) if want_ref else None
+        rc = self.lib.oracle_gemm_f16(
+            _ptr(A, ctypes.c_uint16), _ptr(B, ctypes.c_uint16), _ptr(C, ctypes.c_uint16),
+            _ptr(ref, ctypes.c_double), M, N, K, lda, ldb, N, int(bool(relu)))
+        if rc != 0:
+            raise ValueError("oracle_gemm_f16 rejected its arguments")
+        C = C.view(np.float16)
+        return (C, ref) if want_ref else C
+
+    def gemm_at(self, A: np.ndarray, B: np.ndarray, K: int, rows, cols, relu: bool = False):
+        """Selected elements (rows[t], cols[t]) of the same product.
+
+        Returns (float16 values, float64 values before rounding).
+        """
+        A = _as_u16(A)
+        B = _as_u16(B)
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+        n = rows.size
+        out16 = np.empty(n, dtype=np.uint16)
+        out64 = np.empty(n, dtype=np.float64)
+        rc = self.lib.oracle_gemm_f16_at(
+            _ptr(A, ctypes.c_uint16), _ptr(B, ctypes.c_uint16), K, A.shape[1], B.shape[1],
+            int(bool(relu)), _ptr(rows, ctypes.c_int64), _ptr(cols, ctypes.c_int64), n,
+            _ptr(out16, ctypes.c_uint16), _ptr(out64, ctypes.c_double))
+        if rc != 0:
+            raise ValueError("oracle_gemm_f16_at rejected its arguments")
+        return out16.view(np.float16), out64
+
+
+def default() -> Oracle:
+    global _default
+    if _default is None:
+        _default = Oracle(build())
+    return _default
+
+
+def num_threads() -> int:
+    return default().num_threads()
+
+
+def f16_from_f64(x) -> np.ndarray:
+    return default().f16_from_f64(x)
+
+
+def f64_from_f16(h) -> np.ndarray:
+    return default().f64_from_f16(h)
+
+
+def gemm(A, B, M, N, K, relu=False, want_ref=False):
+    return default().gemm(A, B, M, N, K, relu, want_ref)
+
+
+def gemm_at(A, B, K, rows, cols, relu=False):
+    return default().gemm_at(A, B, K, rows, cols, relu)
+
+
+def ulp16(x) -> np.ndarray:
+    """Spacing of binary16 numbers at |x|: 2^(floor(log2|x|) - 10) for normal
+    magnitudes, 2^-24 below the smallest normal (and at zero)."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    out = np.full(a.shape, 2.0 ** -24)
+    nz = a >= 2.0 ** -14
+    e = np.floor(np.log2(np.where(nz, a, 1.0)))
+    out[nz] = np.exp2(e[nz] - 10.0)
+    return out

@@ -1,0 +1,193 @@
+/*
+ * CPU oracle for the tiled FP16 GEMM — TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the test suite, the package smoke check and the benchmark's CPU
+ * baseline may load this file's library.  The product path (libtgemm) never
+ * links, loads or calls it, and the two share no code.
+ *
+ * What it computes (the plain definition of the operation):
+ *
+ *   C[i][j] = fp16_rne( epi( sum_{k<K} (double)A[i][k] * (double)B[k][j] ) )
+ *
+ *   - "5分钟上手TileLang" (0539edu.com), section "安装与第一个内核": the
+ *     quickstart kernel computes C (M×N, fp16) from A (M×K, fp16) and
+ *     B (K×N, fp16), both row-major, with a float32 fragment accumulator.
+ *   - same page, section "避坑与调参": the accumulator stays in float32 and
+ *     the cast to fp16 happens once, at the final copy.
+ *   - "TileLang：比 Triton 低一层的 tile 语言" (anrans.github.io), section
+ *     "第一个 kernel：GEMM": the same kernel with block_K = 64.
+ *   - "TileLang：让GPU编程像Python一样简单的高性能计算新范式" (coreui.cn),
+ *     the ReLU epilogue: max(C_local, 0) is applied to the float32
+ *     accumulator before the copy to the fp16 output.
+ *
+ * Readings taken where the pages are silent:
+ *   - the reference sum is carried in fp64 (each fp16×fp16 product is exact
+ *     in fp64; the fp64 sum over K ≤ 8192 is far below one fp16 ulp off the
+ *     exact value), in k-ascending order;
+ *   - the rounding to fp16 is round-to-nearest, ties-to-even, done once from
+ *     fp64; overflow goes to ±inf; subnormals are kept;
+ *   - epi(x) = x > 0 ? x : +0 for ReLU (so -0 and NaN map to +0), epi(x) = x
+ *     otherwise.
+ *
+ * Loop order i-k-j with an fp64 row accumulator, OpenMP over rows (when the
+ * compiler offers it).  No blocking, no reordering of the k sum.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---- binary16 <-> binary64 (IEEE 754-2008 binary16 layout: 1|5|10, bias 15) */
+
+double oracle_f64_from_f16(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)m, -24); /* subnormal: m · 2^-24 */
+    } else if (e == 31) {
+        v = m ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + m), e - 25); /* (1.m) · 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* Round a non-negative double that is an exact multiple of 2^-k to the
+ * nearest integer, ties to even.  n is representable (|n| < 2^53). */
+static double round_half_even(double n)
+{
+    double fl = floor(n);
+    double frac = n - fl; /* exact */
+    if (frac > 0.5) return fl + 1.0;
+    if (frac < 0.5) return fl;
+    /* tie */
+    return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+}
+
+uint16_t oracle_f16_from_f64(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    if (isnan(x)) return (uint16_t)(sign | 0x7e00);
+    double a = fabs(x);
+    if (isinf(a)) return (uint16_t)(sign | 0x7c00);
+    if (a < ldexp(1.0, -14)) {
+        /* subnormal range: quantum 2^-24; n in [0, 1024] (1024 = min normal) */
+        double n = round_half_even(ldexp(a, 24));
+        return (uint16_t)(sign | (uint16_t)n);
+    }
+    int E;
+    frexp(a, &E);          /* a = f · 2^E, f in [0.5, 1) */
+    int e = E - 1;         /* a in [2^e, 2^(e+1)) */
+    double n = round_half_even(ldexp(a, 10 - e)); /* in [1024, 2048] */
+    if (n == 2048.0) {
+        n = 1024.0;
+        e += 1;
+    }
+    if (e > 15) return (uint16_t)(sign | 0x7c00); /* overflow -> inf */
+    return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)(n - 1024.0));
+}
+
+void oracle_f16_from_f64_array(const double* x, uint16_t* h, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) h[i] = oracle_f16_from_f64(x[i]);
+}
+
+void oracle_f64_from_f16_array(const uint16_t* h, double* x, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) x[i] = oracle_f64_from_f16(h[i]);
+}
+
+static double g_lut[65536];
+static int g_lut_ready = 0;
+
+static void lut_init(void)
+{
+    if (g_lut_ready) return;
+    for (int i = 0; i < 65536; ++i) g_lut[i] = oracle_f64_from_f16((uint16_t)i);
+    g_lut_ready = 1;
+}
+
+static double epi_apply(double v, int relu)
+{
+    if (relu) return v > 0.0 ? v : 0.0;
+    return v;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Full product.  A: M×K with row stride lda, B: K×N with row stride ldb,
+ * C: M×N with row stride ldc (fp16 bits).  If Cref is not NULL it receives the
+ * fp64 value epi(sum) before rounding, densely as M×N.
+ * Returns 0, or -1 on bad arguments / allocation failure.
+ */
+int oracle_gemm_f16(const uint16_t* A, const uint16_t* B, uint16_t* C, double* Cref,
+                    int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                    int relu)
+{
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < N || ldc < N) return -1;
+    lut_init();
+    int err = 0;
+#pragma omp parallel
+    {
+        double* acc = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+        if (!acc) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < M; ++i) {
+            if (!acc) continue;
+            for (int64_t j = 0; j < N; ++j) acc[j] = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double a = g_lut[A[i * lda + k]];
+                const uint16_t* brow = B + k * ldb;
+                for (int64_t j = 0; j < N; ++j) acc[j] += a * g_lut[brow[j]];
+            }
+            for (int64_t j = 0; j < N; ++j) {
+                double v = epi_apply(acc[j], relu);
+                C[i * ldc + j] = oracle_f16_from_f64(v);
+                if (Cref) Cref[i * N + j] = v;
+            }
+        }
+        free(acc);
+    }
+    return err ? -1 : 0;
+}
+
+/*
+ * Selected outputs only: for each t < n, the element (rows[t], cols[t]) of the
+ * same product, computed as one k-ascending fp64 dot product (the same order
+ * as the full routine, so the two agree bit for bit).
+ */
+int oracle_gemm_f16_at(const uint16_t* A, const uint16_t* B, int64_t K, int64_t lda,
+                       int64_t ldb, int relu, const int64_t* rows, const int64_t* cols,
+                       int64_t n, uint16_t* out16, double* out64)
+{
+    if (K < 0 || lda < K) return -1;
+    lut_init();
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) {
+        const uint16_t* arow = A + rows[t] * lda;
+        const uint16_t* bcol = B + cols[t];
+        double s = 0.0;
+        for (int64_t k = 0; k < K; ++k) s += g_lut[arow[k]] * g_lut[bcol[k * ldb]];
+        double v = epi_apply(s, relu);
+        if (out16) out16[t] = oracle_f16_from_f64(v);
+        if (out64) out64[t] = v;
+    }
+    return 0;
+}

@@ -1,0 +1,260 @@
+"""Pins for the CPU oracle: checks against facts fixed outside the oracle.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError when the
+oracle disagrees with:
+  * IEEE binary16 itself (numpy's float16 decoder, exact midpoints, the
+    overflow threshold 65520, subnormal spacing 2^-24);
+  * exact rational arithmetic (``exact.py``) on tiny products;
+  * closed forms: identity and permutation B, rank-1 A, A·1 row sums;
+  * integer products in {-1,0,1} against numpy's int64 matmul;
+  * torch's fp64 CPU matmul (a library routine);
+  * the ReLU rule (epi applied to the un-rounded sum; -0 becomes +0);
+  * the leading-dimension contract (padding is never read).
+
+The same pins run against deliberately broken builds of the oracle source in
+``test_oracle_mutants.py``; every plausible mistake listed there must trip at
+least one of them.
+"""
+
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+
+import numpy as np
+
+from exact import exact_gemm, rne_f16, frac_of_f16
+
+ALL16 = np.arange(65536, dtype=np.uint16)
+
+
+def _f16(x):
+    return np.asarray(x, dtype=np.float64).astype(np.float16)
+
+
+def _same_value(a, b):
+    """Equal by value (+0 == -0), NaN equal to NaN."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return np.all((a == b) | (np.isnan(a) & np.isnan(b)))
+
+
+# ---------------------------------------------------------------- binary16
+
+def pin_decode_matches_numpy(o):
+    mine = o.f64_from_f16(ALL16)
+    ref = ALL16.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan], ref[~nan])
+    # sign of zero too
+    assert np.signbit(mine[0x8000]) and not np.signbit(mine[0])
+
+
+def pin_roundtrip_all_halves(o):
+    vals = ALL16.view(np.float16).astype(np.float64)
+    keep = ~np.isnan(vals)
+    back = o.f16_from_f64(vals[keep])
+    assert np.array_equal(back, ALL16[keep])
+
+
+def pin_midpoints_tie_to_even(o):
+    pos = np.arange(0, 0x7bff, dtype=np.uint16)  # pairs (h, h+1), both finite, >= 0
+    lo = pos.view(np.float16).astype(np.float64)
+    hi = (pos + 1).view(np.float16).astype(np.float64)
+    mid = (lo + hi) / 2.0  # exact in fp64
+    got = o.f16_from_f64(mid)
+    even = np.where(pos % 2 == 0, pos, pos + 1).astype(np.uint16)
+    assert np.array_equal(got, even)
+    # a hair either side of the midpoint goes to the nearer neighbour
+    up = o.f16_from_f64(np.nextafter(mid, np.inf))
+    dn = o.f16_from_f64(np.nextafter(mid, -np.inf))
+    assert np.array_equal(up, pos + 1)
+    assert np.array_equal(dn, pos)
+    # negative side mirrors the positive side
+    gotn = o.f16_from_f64(-mid)
+    assert np.array_equal(gotn, even | 0x8000)
+
+
+def pin_overflow_and_specials(o):
+    cases = [
+        (65504.0, 0x7BFF), (65519.99, 0x7BFF), (65520.0, 0x7C00), (1e6, 0x7C00),
+        (-65520.0, 0xFC00), (math.inf, 0x7C00), (-math.inf, 0xFC00),
+        (2.0 ** -24, 0x0001), (2.0 ** -25, 0x0000), (1.5 * 2.0 ** -25, 0x0001),
+        (3 * 2.0 ** -25, 0x0002), (2.0 ** -14, 0x0400), (1.0, 0x3C00), (-2.0, 0xC000),
+        (0.0, 0x0000), (-0.0, 0x8000), (1.0 + 2.0 ** -11, 0x3C00),
+        (1.0 + 3 * 2.0 ** -11, 0x3C02),
+    ]
+    xs = np.array([c[0] for c in cases], dtype=np.float64)
+    want = np.array([c[1] for c in cases], dtype=np.uint16)
+    got = o.f16_from_f64(xs)
+    assert np.array_equal(got, want), [(x, hex(g), hex(w)) for x, g, w in zip(xs, got, want)
+                                       if g != w]
+    nanbits = o.f16_from_f64(np.array([np.nan]))
+    assert (nanbits[0] & 0x7C00) == 0x7C00 and (nanbits[0] & 0x3FF) != 0
+
+
+def pin_matches_numpy_cast(o):
+    rng = np.random.default_rng(123)
+    mant = rng.uniform(1.0, 2.0, 200_000)
+    expo = rng.integers(-30, 18, 200_000)
+    sign = np.where(rng.integers(0, 2, 200_000) == 1, -1.0, 1.0)
+    x = sign * np.ldexp(mant, expo)
+    got = o.f16_from_f64(x)
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+# ---------------------------------------------------------------- the product
+
+def pin_bruteforce_exact(o):
+    rng = np.random.default_rng(7)
+    shapes = [(1, 1, 1), (3, 5, 7), (7, 3, 16), (16, 16, 16), (5, 9, 13), (2, 11, 4)]
+    scales = [1.0, 1e-3, 64.0]  # 1e-3 puts products in the subnormal range
+    for (M, N, K) in shapes:
+        for sc in scales:
+            A = _f16(rng.normal(0, sc, (M, K)))
+            B = _f16(rng.normal(0, sc, (K, N)))
+            for relu in (False, True):
+                want, _ = exact_gemm(A, B, relu)
+                got = o.gemm(A, B, M, N, K, relu).astype(np.float64)
+                assert _same_value(got, want), (M, N, K, sc, relu, got, want)
+
+
+def pin_near_tie_rounding(o):
+    """Exact sums a hair off an fp16 midpoint must round from the exact value
+    (a single rounding): 1 + 2^-11 is the midpoint of 1 and 1 + 2^-10."""
+    t = 2.0 ** -15  # an fp16 subnormal; t*t = 2^-30
+    A = _f16([[1.0, 2.0 ** -11, t], [1.0, 2.0 ** -11, -t], [1.0, 3 * 2.0 ** -11, 0.0],
+              [1.0, 2.0 ** -11, 0.0]])
+    B = _f16([[1.0], [1.0], [t]])
+    got = o.gemm(A, B, 4, 1, 3).astype(np.float64)[:, 0]
+    want = np.array([1.0 + 2.0 ** -10, 1.0, 1.0 + 2.0 ** -9, 1.0])
+    assert np.array_equal(got, want), got
+
+
+def pin_identity_and_permutation(o):
+    rng = np.random.default_rng(11)
+    M, K = 37, 29
+    A = _f16(rng.uniform(-3, 3, (M, K)))
+    I = np.eye(K, dtype=np.float16)
+    C = o.gemm(A, I, M, K, K)
+    assert np.array_equal(C.view(np.uint16) & 0x7FFF, A.view(np.uint16) & 0x7FFF)
+    assert _same_value(C, A)
+    Cr = o.gemm(A, I, M, K, K, relu=True)
+    assert _same_value(Cr, np.maximum(A.astype(np.float64), 0.0))
+    p = rng.permutation(K)
+    P = np.zeros((K, K), dtype=np.float16)
+    P[p, np.arange(K)] = 1.0  # B[k, j] = 1 iff k == p[j]
+    Cp = o.gemm(A, P, M, K, K)
+    assert _same_value(Cp, A[:, p])
+
+
+def pin_rank1_and_row_sums(o):
+    rng = np.random.default_rng(12)
+    M, N, K = 19, 23, 41
+    u = _f16(rng.uniform(-2, 2, M))
+    A = np.repeat(u[:, None], K, axis=1)
+    Bi = rng.integers(-4, 5, (K, N))
+    B = Bi.astype(np.float16)
+    C = o.gemm(A, B, M, N, K).astype(np.float64)
+    colsum = Bi.sum(axis=0)
+    want = np.array([[rne_f16(frac_of_f16(u[i]) * int(colsum[j])) for j in range(N)]
+                     for i in range(M)])
+    assert _same_value(C, want)
+    # A·1: every column equals the (rounded) row sum of A
+    A2 = _f16(rng.uniform(-1, 1, (M, K)))
+    ones = np.ones((K, 5), dtype=np.float16)
+    C2 = o.gemm(A2, ones, M, 5, K).astype(np.float64)
+    rs = [rne_f16(sum((frac_of_f16(x) for x in A2[i]), Fraction(0))) for i in range(M)]
+    assert _same_value(C2, np.repeat(np.array(rs)[:, None], 5, axis=1))
+
+
+def pin_integer_product(o):
+    rng = np.random.default_rng(13)
+    M, N, K = 48, 40, 200
+    Ai = rng.integers(-1, 2, (M, K))
+    Bi = rng.integers(-1, 2, (K, N))
+    C = o.gemm(Ai.astype(np.float16), Bi.astype(np.float16), M, N, K).astype(np.float64)
+    assert np.array_equal(C, (Ai @ Bi).astype(np.float64))
+    Cr = o.gemm(Ai.astype(np.float16), Bi.astype(np.float16), M, N, K, relu=True)
+    assert np.array_equal(Cr.astype(np.float64), np.maximum(Ai @ Bi, 0).astype(np.float64))
+
+
+def pin_torch_fp64(o):
+    import torch
+    rng = np.random.default_rng(14)
+    M, N, K = 33, 45, 300
+    A = _f16(rng.uniform(-1, 1, (M, K)))
+    B = _f16(rng.uniform(-1, 1, (K, N)))
+    C, ref = o.gemm(A, B, M, N, K, want_ref=True)
+    t = (torch.from_numpy(A.astype(np.float64)) @ torch.from_numpy(B.astype(np.float64))).numpy()
+    assert np.max(np.abs(ref - t)) <= 1e-12 * K
+    assert np.mean(C.astype(np.float64) == t.astype(np.float16).astype(np.float64)) > 0.999
+
+
+def pin_relu_rule(o):
+    rng = np.random.default_rng(15)
+    M, N, K = 31, 27, 64
+    A = _f16(rng.uniform(-1, 1, (M, K)))
+    B = _f16(rng.uniform(-1, 1, (K, N)))
+    C0 = o.gemm(A, B, M, N, K).astype(np.float64)
+    C1 = o.gemm(A, B, M, N, K, relu=True)
+    assert not np.any(np.signbit(C1.astype(np.float64)))  # no negatives, no -0
+    assert _same_value(C1, np.maximum(C0, 0.0))
+    assert np.any(C0 < 0) and np.any(C0 > 0)
+    # all-zero rows: sum is exactly 0 -> +0 with ReLU
+    Z = np.zeros((2, K), dtype=np.float16)
+    Z[1] = -0.0
+    Cz = o.gemm(Z, B, 2, N, K, relu=True)
+    assert not np.any(np.signbit(Cz.astype(np.float64)))
+
+
+def pin_leading_dims(o):
+    rng = np.random.default_rng(16)
+    M, N, K = 9, 13, 21
+    A = _f16(rng.uniform(-1, 1, (M, K)))
+    B = _f16(rng.uniform(-1, 1, (K, N)))
+    base = o.gemm(A, B, M, N, K)
+    Ap = np.full((M, K + 11), np.nan, dtype=np.float16)
+    Ap[:, :K] = A
+    Bp = np.full((K, N + 3), np.inf, dtype=np.float16)
+    Bp[:, :N] = B
+    padded = o.gemm(Ap, Bp, M, N, K)
+    assert np.array_equal(base.view(np.uint16), padded.view(np.uint16))
+    want, _ = exact_gemm(A, B, False)
+    assert _same_value(base, want)
+
+
+def pin_sampled_matches_full(o):
+    rng = np.random.default_rng(17)
+    M, N, K = 70, 90, 130
+    A = _f16(rng.normal(0, 1, (M, K)))
+    B = _f16(rng.normal(0, 1, (K, N)))
+    for relu in (False, True):
+        C, ref = o.gemm(A, B, M, N, K, relu=relu, want_ref=True)
+        r = rng.integers(0, M, 500)
+        c = rng.integers(0, N, 500)
+        v16, v64 = o.gemm_at(A, B, K, r, c, relu=relu)
+        assert np.array_equal(v16.view(np.uint16), C.view(np.uint16)[r, c])
+        assert np.array_equal(v64, ref[r, c])
+        # and the sampled value itself is the exact sum rounded once
+        for t in range(8):
+            i, j = int(r[t]), int(c[t])
+            s = sum((frac_of_f16(A[i, k]) * frac_of_f16(B[k, j]) for k in range(K)), Fraction(0))
+            if relu and s < 0:
+                s = Fraction(0)
+            assert float(v16[t]) == rne_f16(s)
+
+
+def pin_zero_sizes(o):
+    A = np.zeros((3, 0), dtype=np.float16)
+    B = np.zeros((0, 4), dtype=np.float16)
+    C = o.gemm(A, B, 3, 4, 0)
+    assert C.shape == (3, 4) and np.all(C.astype(np.float64) == 0.0)
+    Cr = o.gemm(A, B, 3, 4, 0, relu=True)
+    assert not np.any(np.signbit(Cr.astype(np.float64)))
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

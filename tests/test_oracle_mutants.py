@@ -1,0 +1,62 @@
+"""Plant plausible mistakes in a copy of the oracle's C source and check that
+the pins catch every one of them (no GPU).
+
+Each mutant is a textual edit of ``oracle/tgemm_oracle.c`` compiled into a
+temporary library; the committed oracle is never modified.
+"""
+
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+# (name, original text, replacement) — each edit must apply at least once.
+# (A ReLU that lets -0 through is not listed: the fp64 sum starts at +0 and
+# IEEE addition never turns it into -0, so that mutant is equivalent.)
+MUTANTS = [
+    ("drop_last_term", "k < K; ++k)", "k < K - 1; ++k)"),
+    ("drop_first_term", "for (int64_t k = 0; k < K;", "for (int64_t k = 1; k < K;"),
+    ("wrong_sign_first_product", "acc[j] += a * g_lut[brow[j]];",
+     "acc[j] += (k == 0 ? -a : a) * g_lut[brow[j]];"),
+    ("wrong_b_row", "const uint16_t* brow = B + k * ldb;",
+     "const uint16_t* brow = B + ((k + 1) % K) * ldb;"),
+    ("transposed_a", "double a = g_lut[A[i * lda + k]];",
+     "double a = g_lut[A[(k % M) * lda + (i % K)]];"),
+    ("truncating_round", "double frac = n - fl; /* exact */", "double frac = 0.0;"),
+    ("ties_away", "return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;", "return fl + 1.0;"),
+    ("fp32_accumulator", "double* acc = (double*)malloc(sizeof(double)",
+     "float* acc = (float*)malloc(sizeof(float)"),
+    ("relu_as_abs", "if (relu) return v > 0.0 ? v : 0.0;", "if (relu) return fabs(v);"),
+    ("relu_ignored", "if (relu) return v > 0.0 ? v : 0.0;", "if (relu) return v;"),
+    ("flush_subnormals", "double n = round_half_even(ldexp(a, 24));", "double n = 0.0;"),
+    ("late_overflow", "if (e > 15) return", "if (e > 16) return"),
+    ("decode_bias", "e - 25);", "e - 24);"),
+    ("decode_subnormal", "v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
+    ("ldb_ignored", "g_lut[bcol[k * ldb]]", "g_lut[bcol[k * (ldb - (ldb > 1))]]"),
+]
+
+
+def _pin_catches(o):
+    failures = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(o)
+        except AssertionError:
+            failures.append(pin.__name__)
+        except (ValueError, FloatingPointError, OverflowError):
+            failures.append(pin.__name__ + "(raised)")
+    return failures
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new):
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    path = os.path.join(str(tmp_path), f"{name}.c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    lib = oracle.compile_source(path, os.path.join(str(tmp_path), f"lib{name}.so"))
+    caught = _pin_catches(oracle.Oracle(lib))
+    assert caught, f"mutant {name} passed every pin"
