@@ -1,0 +1,418 @@
+#!/usr/bin/env python3
+"""Benchmark libtgemm: FP16 GEMM TFLOP/s and fraction of the tensor roofline
+on the transformer-MLP workload (8192×28672×4096, fused ReLU), with the
+skinny weight-streaming workload (64×16384×8192) measured beside it in HBM
+GB/s.  Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one tg_gemm_f16 launch over one batch of synthetic input (the whole
+hot path: tensor maps, persistent tile schedule, TMA ring, tcgen05 MMA into
+TMEM, fused ReLU + fp16 epilogue with TMA stores).  Inputs are larger than L2,
+so no flush is needed between steps.  N > 1 runs N independent replicas (one
+per GPU, no collective on the data path); value = work of all ranks ÷ the
+slowest rank's time.
+
+--impl reference times the CPU oracle (oracle/) as it stands on this host's
+cores, on a bounded row slab of the same workload per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP16 GEMM TFLOP/s and % of dense tensor peak (HBM GB/s % for skinny M), 1 GB300"
+MAIN_WORKLOAD = "mlp_8192x28672x4096_relu"
+SKINNY_WORKLOAD = "skinny_64x16384x8192"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=MAIN_WORKLOAD)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-skinny", action="store_true")
+    a = p.parse_args(argv)
+    if a.warmup < 3:
+        p.error("--warmup must be at least 3")
+    return a
+
+
+# ------------------------------------------------------------------ helpers
+
+def rank_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def source_hash() -> str:
+    """Hash of the kernel sources, to tell whether stored ncu counters are stale."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tiled_fp16_gemm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_PEAKS["hbm_gbs"], FALLBACK_PEAKS["bf16_tflops"], "fallback"
+
+
+def stored_traffic(kernel_key: str):
+    """dram bytes per launch from a committed ncu capture, if taken on the
+    current kernel sources; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        e = d.get(kernel_key)
+        if e and e.get("source_hash") == source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while work runs."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 100):
+        self.index = index
+        self.period_ms = period_ms
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period_ms}", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.5)  # let the sampler come up before the timed region
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    rows.append((ts, float(parts[2]), float(parts[3]), float(parts[4]), parts[5:]))
+                except Exception:
+                    continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[4][1:5])
+                          if v.lower() == "active"})
+        return {
+            "sm_mhz": statistics.median(r[1] for r in inside) if inside else None,
+            "sm_max_mhz": max(r[2] for r in inside) if inside else None,
+            "power_w_max": max(r[3] for r in inside) if inside else None,
+            "samples": len(inside),
+            "reasons": reasons,
+        }
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ------------------------------------------------------------------ timing
+
+def time_launches(launch, stream, steps: int, world: int, device):
+    """Run `launch` steps times on `stream`; returns (total_ms, per_launch_ms list)."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(world, device)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_begin.record(stream)
+    for i in range(steps):
+        starts[i].record(stream)
+        launch()
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world, device)
+    wall1 = time.time()
+    total = t_begin.elapsed_time(t_end)
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return total, per, wall0, wall1
+
+
+def cpu_oracle_rate(A, B, w, seconds: float):
+    """Time the oracle on a row slab sized for about `seconds` of work.
+    Returns (tflops, rows, elapsed_s, threads)."""
+    import oracle
+    o = oracle.default()
+    th = o.num_threads()
+    rows = max(1, min(w.M, th))
+    t = time.perf_counter()
+    o.gemm(A[:rows], B, rows, w.N, w.K, relu=w.relu)
+    dt = time.perf_counter() - t
+    rows2 = int(max(rows, min(w.M, rows * seconds / max(dt, 1e-6))))
+    t = time.perf_counter()
+    o.gemm(A[:rows2], B, rows2, w.N, w.K, relu=w.relu)
+    dt2 = time.perf_counter() - t
+    return 2.0 * rows2 * w.N * w.K / dt2 / 1e12, rows2, dt2, th
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args, w):
+    """The CPU oracle as it stands, timed on this host's cores."""
+    import oracle
+    from tiled_fp16_gemm_gb300 import workloads as W
+    A, B = W.workload_inputs(w)
+    o = oracle.default()
+    th = o.num_threads()
+    rows = max(1, min(w.M, th))
+    t = time.perf_counter()
+    o.gemm(A[:rows], B, rows, w.N, w.K, relu=w.relu)
+    per_row = (time.perf_counter() - t) / rows
+    budget = 150.0 / (args.steps + args.warmup)
+    rows = int(max(1, min(w.M, budget / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        o.gemm(A[:rows], B, rows, w.N, w.K, relu=w.relu)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        o.gemm(A[:rows], B, rows, w.N, w.K, relu=w.relu)
+    dt = time.perf_counter() - t
+    flops = 2.0 * rows * w.N * w.K * args.steps
+    value = flops / dt / 1e12
+    sample = f"{rows} of {w.M} rows of {w.name} per step (full N and K)"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_block(w, args.gpus),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": th, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def config_block(w, gpus):
+    inb = 2 * (w.M * w.K + w.K * w.N)
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+            "epilogue": "relu" if w.relu else "none",
+            "inputs": f"A {w.dist_a}, B {w.dist_b}, seed {w.seed}",
+            "l2": f"inputs larger than L2 ({inb / 2**20:.0f} MiB of A+B vs {L2_BYTES // 2**20} MiB L2); no flush",
+            "parallelism": "replicas" if gpus > 1 else "single GPU"}
+
+
+def run_ours(args, w, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import tiled_fp16_gemm_gb300 as tg
+    from tiled_fp16_gemm_gb300 import workloads as W
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.current_stream(device)
+    nsm = torch.cuda.get_device_properties(device).multi_processor_count
+    hbm_peak, tf_peak, peak_src = load_peaks()
+
+    A, B = W.workload_inputs(w)
+    a = torch.from_numpy(A).to(device)
+    b = torch.from_numpy(B).to(device)
+    c = torch.empty((w.M, w.N), dtype=torch.float16, device=device)
+    epi = tg.TG_EPI_RELU if w.relu else tg.TG_EPI_NONE
+    plan = tg.tg_plan_f16(w.M, w.N, w.K, nsm)
+
+    def launch():
+        st = tg.tg_gemm_f16(a.data_ptr(), b.data_ptr(), c.data_ptr(), w.M, w.N, w.K, w.K, w.N,
+                            w.N, epi, stream.cuda_stream)
+        if st != tg.TG_OK:
+            raise tg.TgemmError(st)
+
+    for _ in range(args.warmup):
+        launch()
+    tg.sync_status(stream)
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    total_ms, per, wall0, wall1 = time_launches(launch, stream, args.steps, world, device)
+    clk = clocks.stop(wall0, wall1)
+    tg.sync_status(stream)
+    total_ms = max_over_ranks(total_ms, world, device)
+
+    flops = float(w.flops)
+    ms_step = total_ms / args.steps
+    value = world * flops * args.steps / (total_ms / 1e3) / 1e12
+    kernel_ms = statistics.mean(per)
+    achieved = flops / (kernel_ms / 1e3) / 1e12
+    kernel_key = f"persistent_bn{plan.bn}" if plan.kernel == tg.TG_KERNEL_PERSISTENT else "skinny"
+    traffic = stored_traffic(f"{kernel_key}:{w.name}")
+    out = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic", "config": config_block(w, world),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf_peak,
+                     "unit": "TFLOP/s", "frac": achieved / tf_peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} dense bf16 burst (fp16 dense rate is the same)",
+                     "kernel": f"tg_gemm_f16_persistent<{plan.bn},{plan.stages}>",
+                     "kernel_ms_mean": kernel_ms, "kernel_ms_min": min(per),
+                     "kernel_ms_median": statistics.median(per)},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+
+    # ---- skinny weight-streaming workload, same method
+    if not args.no_skinny and w.name != SKINNY_WORKLOAD:
+        ws = W.WORKLOADS[SKINNY_WORKLOAD]
+        As, Bs = W.workload_inputs(ws)
+        a2 = torch.from_numpy(As).to(device)
+        b2 = torch.from_numpy(Bs).to(device)
+        c2 = torch.empty((ws.M, ws.N), dtype=torch.float16, device=device)
+
+        def launch2():
+            st = tg.tg_gemm_f16(a2.data_ptr(), b2.data_ptr(), c2.data_ptr(), ws.M, ws.N, ws.K,
+                                ws.K, ws.N, ws.N, 0, stream.cuda_stream)
+            if st != tg.TG_OK:
+                raise tg.TgemmError(st)
+
+        for _ in range(args.warmup):
+            launch2()
+        tg.sync_status(stream)
+        n2 = max(50, args.steps)
+        tot2, per2, _, _ = time_launches(launch2, stream, n2, world, device)
+        tg.sync_status(stream)
+        k2 = statistics.mean(per2)
+        gbs = ws.min_bytes / (k2 / 1e3) / 1e9
+        out["skinny"] = {
+            "workload": ws.name, "launches": n2, "kernel_ms_mean": k2,
+            "kernel_ms_min": min(per2), "tflops": ws.flops / (k2 / 1e3) / 1e12,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": gbs / hbm_peak,
+                         "traffic": stored_traffic(f"skinny:{ws.name}"),
+                         "peak_source": f"{peak_src} copy bandwidth"},
+        }
+        del a2, b2, c2
+
+    # ---- end to end through the public API, host buffers in and out
+    if not args.no_e2e:
+        ha = torch.from_numpy(A).pin_memory()
+        hb = torch.from_numpy(B).pin_memory()
+        n3 = max(5, min(args.steps, 20))
+        tg.gemm_host(ha, hb, relu=w.relu, stream=stream)  # warm
+        barrier(world, device)
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        for _ in range(n3):
+            tg.gemm_host(ha, hb, relu=w.relu, stream=stream)
+        dt = max_over_ranks(time.perf_counter() - t, world, device)
+        out["e2e"] = {"value": world * flops * n3 / dt / 1e12, "unit": "TFLOP/s",
+                      "h2d_bytes_per_step": int(ha.numel() * 2 + hb.numel() * 2),
+                      "d2h_bytes_per_step": int(w.M * w.N * 2),
+                      "steps": n3, "call": "tiled_fp16_gemm_gb300.gemm_host"}
+
+    # ---- CPU oracle on this host (rank 0, N == 1 only)
+    if not args.no_cpu and rank == 0 and world == 1:
+        tfl, rows, secs, th = cpu_oracle_rate(A, B, w, 12.0)
+        out["cpu_baseline"] = {"value": tfl, "unit": "TFLOP/s", "cores": th, "kind": "oracle",
+                               "sample": f"{rows} of {w.M} rows of {w.name} (full N, K), "
+                                         f"{secs:.1f} s"}
+    return out
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local_rank = rank_info()
+    from tiled_fp16_gemm_gb300 import workloads as W
+    w = W.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, w)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    from tiled_fp16_gemm_gb300 import build
+    if rank == 0:
+        build.build()
+    if world > 1:
+        barrier(world, None)
+    out = run_ours(args, w, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

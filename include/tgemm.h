@@ -1,0 +1,167 @@
+/*
+ * libtgemm — dense FP16 GEMM for GB300 (sm_103a), C ABI.
+ *
+ *   C = epi(A · B)      A: M×K, B: K×N, C: M×N, all fp16, row-major,
+ *                       fp32 accumulation, one rounding to fp16 at the end,
+ *                       epi = identity or ReLU on the fp32 accumulator.
+ *
+ * The operation is the tiled GEMM of the TileLang pages:
+ *   - "5分钟上手TileLang" (0539edu.com), section "安装与第一个内核": A (M×K)
+ *     and B (K×N) fp16, a float32 accumulator fragment, C fp16; the official
+ *     quickstart carries a fused ReLU epilogue;
+ *   - same page, section "避坑与调参": the accumulator stays float32 and is
+ *     written back as fp16 only at the last copy;
+ *   - "TileLang：让GPU编程像Python一样简单的高性能计算新范式" (coreui.cn):
+ *     the ReLU epilogue takes max(C_local, 0) on the float32 accumulator
+ *     before the copy to C;
+ *   - "TileLang：比 Triton 低一层的 tile 语言" (anrans.github.io), sections
+ *     "第一个 kernel：GEMM" and "它生成了什么": one output tile per block,
+ *     TMA loads into a multi-stage shared-memory ring guarded by mbarriers,
+ *     warp-specialised producer and consumer.
+ *
+ * Threading: every entry point is thread-safe.  Calls on the same stream are
+ * ordered; calls on different streams may overlap (each stream gets its own
+ * split-K workspace).
+ */
+#ifndef TGEMM_H
+#define TGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TG_EPI_NONE = 0, /* C = fp16(acc)              */
+    TG_EPI_RELU = 1  /* C = fp16(acc > 0 ? acc : 0) (so -0 and NaN become +0) */
+} tg_epilogue_t;
+
+typedef enum {
+    TG_OK = 0,
+    TG_ERR_INVALID_VALUE = 1,      /* bad size, leading dimension, pointer or epilogue   */
+    TG_ERR_MISALIGNED = 2,         /* pointer not 16-byte aligned or ld not a multiple of 8 */
+    TG_ERR_UNSUPPORTED_DEVICE = 3, /* no CUDA device, or the current one is not sm_103     */
+    TG_ERR_LAUNCH = 4,             /* a CUDA launch or runtime call failed                 */
+    TG_ERR_NO_MEMORY = 5,          /* the library could not allocate its workspace         */
+    TG_ERR_TIMEOUT = 6             /* a kernel gave up on a wait and returned early        */
+} tg_status_t;
+
+/*
+ * tg_gemm_f16 — C = epi(A·B), asynchronous on `stream`.
+ *
+ * A   device pointer, fp16, row-major M×K, row stride lda elements (lda ≥ K).
+ * B   device pointer, fp16, row-major K×N, row stride ldb elements (ldb ≥ N).
+ * C   device pointer, fp16, row-major M×N, row stride ldc elements (ldc ≥ N).
+ *     Only the M×N elements are written; padding columns are left untouched.
+ * M, N, K   sizes, each in [0, 2^31 - 1].  M == 0 or N == 0: nothing is done
+ *     and TG_OK is returned.  K == 0: C is filled with epi(0) = +0 (A and B
+ *     may then be NULL and lda/ldb are ignored).
+ * epilogue  TG_EPI_NONE or TG_EPI_RELU.
+ * stream    a cudaStream_t (NULL = the legacy default stream) on the current
+ *     device.
+ *
+ * Alignment: A, B, C must be 16-byte aligned and lda, ldb, ldc multiples of 8
+ * (the tensor-memory-access unit copies rows with 16-byte strides); otherwise
+ * TG_ERR_MISALIGNED.  C must not overlap A or B (not checked).
+ * Ownership: the caller owns A, B and C; the library keeps no reference past
+ * the work it enqueued on `stream`.  The library owns a small split-K
+ * workspace per (device, stream), allocated on first use and kept until
+ * process exit.
+ * Errors: argument errors are returned before anything is enqueued.  Launch
+ * failures return TG_ERR_LAUNCH.  A kernel that gives up on a bounded wait
+ * records the fact on the device; tg_sync_status reports it.
+ * The current device must be compute capability 10.3 (sm_103).
+ * Kernel choice follows tg_plan_f16; the environment variable
+ * TGEMM_FORCE_CFG = persistent256 | persistent128 | skinny overrides it where
+ * the forced kernel applies (for tests and tile sweeps).
+ */
+tg_status_t tg_gemm_f16(const void* A, const void* B, void* C,
+                        int64_t M, int64_t N, int64_t K,
+                        int64_t lda, int64_t ldb, int64_t ldc,
+                        int epilogue, void* stream);
+
+/*
+ * tg_sync_status — wait for `stream`, then report (and clear) a device-side
+ * timeout recorded by any libtgemm kernel on the current device since the
+ * last call.  Returns TG_OK, TG_ERR_TIMEOUT, or TG_ERR_LAUNCH if the stream
+ * reports a CUDA error.
+ */
+tg_status_t tg_sync_status(void* stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* tg_status_string(tg_status_t status);
+
+/* Library version string, e.g. "libtgemm 0.1.0 (sm_103a)". */
+const char* tg_version(void);
+
+/* ------------------------------------------------------------------------
+ * Host-side planning (pure functions: no CUDA calls, usable without a GPU).
+ * ------------------------------------------------------------------------ */
+
+typedef enum {
+    TG_KERNEL_NONE = 0,       /* M == 0 or N == 0                                   */
+    TG_KERNEL_FILL = 1,       /* K == 0: C = 0                                      */
+    TG_KERNEL_PERSISTENT = 2, /* 128×BN tiles, persistent CTAs, TMEM accumulator    */
+    TG_KERNEL_SKINNY = 3      /* M ≤ 128: C^T = B^T·A^T tiles with split-K          */
+} tg_kernel_t;
+
+typedef struct {
+    int32_t kernel;       /* tg_kernel_t                                        */
+    int32_t bm, bn, bk;   /* output tile (rows of C, columns of C) and k step   */
+    int32_t stages;       /* shared-memory ring depth                           */
+    int32_t mma_m, mma_n; /* tensor-core instruction shape                      */
+    int64_t tiles_m, tiles_n, k_blocks;
+    int64_t num_tiles;
+    int64_t grid;         /* CTAs launched                                      */
+    int32_t threads;      /* threads per CTA                                    */
+    int32_t group_m;      /* raster: tiles_m blocks walked per group            */
+    int64_t smem_bytes;   /* dynamic shared memory per CTA                      */
+    int64_t ring_bytes;   /* of which the operand ring                          */
+    int64_t split_k;      /* k-ranges per output tile (skinny: maximum)         */
+    int64_t workspace_bytes; /* device scratch needed (skinny split-K)          */
+} tg_plan_t;
+
+/*
+ * tg_plan_f16 — the launch plan tg_gemm_f16 uses for these sizes on a device
+ * with `num_sms` multiprocessors.  Returns TG_ERR_INVALID_VALUE for negative
+ * or oversized dimensions or num_sms < 1.
+ */
+tg_status_t tg_plan_f16(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* plan);
+
+/*
+ * tg_tile_coord — which (m block, n block) tile number `tile` of a plan maps
+ * to; the persistent kernel walks tiles in this order (column-major inside
+ * groups of plan->group_m row blocks, so consecutive CTAs share B panels in
+ * L2).  Returns TG_ERR_INVALID_VALUE if `tile` is out of range.
+ */
+tg_status_t tg_tile_coord(const tg_plan_t* plan, int64_t tile, int64_t* m_blk, int64_t* n_blk);
+
+/*
+ * tg_ring_bytes — bytes of a shared-memory ring of `stages` stages, each
+ * holding one bm×bk tile of A and one bk×bn tile of B of `elem_bytes`-byte
+ * elements.  "TileLang：比 Triton 低一层的 tile 语言", section "练习",
+ * exercises 1–2 work this out for 128/128/64 fp16: 32 KB per stage, 96 KB
+ * for 3 stages.  Returns -1 for non-positive arguments.
+ */
+int64_t tg_ring_bytes(int32_t bm, int32_t bn, int32_t bk, int32_t stages, int32_t elem_bytes);
+
+/* ------------------------------------------------------------------------
+ * Fault-path hooks (for tests of the timeout path; they never fault a GPU).
+ * ------------------------------------------------------------------------ */
+
+/* Upper bound, in nanoseconds, on every wait inside libtgemm kernels launched
+ * after this call (default 2 000 000 000).  0 restores the default. */
+void tg_debug_set_wait_timeout_ns(uint64_t ns);
+
+/* mode 1: the next persistent/skinny launch withholds its first
+ * "accumulator ready" signal, so its epilogue waits out the timeout and the
+ * kernel returns early with TG_ERR_TIMEOUT recorded.  mode 0: off.  The
+ * setting applies to exactly one launch. */
+void tg_debug_inject(int32_t mode);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TGEMM_H */

@@ -1,0 +1,172 @@
+"""The C-ABI library loads, exports what include/tgemm.h declares, and its
+host-side logic (argument checks, planning) behaves — no GPU needed."""
+
+import json
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tgemm.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden", "page2_smem_exercises.json")
+
+
+@pytest.fixture(scope="module")
+def tg():
+    from tiled_fp16_gemm_gb300 import build
+    build.build()
+    import tiled_fp16_gemm_gb300 as t
+    t.library()
+    return t
+
+
+def _has_gpu():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+def header_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(tg_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_header_declares_expected_entry_points(tg):
+    assert set(header_functions()) == set(tg.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(tg):
+    lib = tg.library()
+    for name in header_functions():
+        assert hasattr(lib, name), name
+    nm = subprocess.run(["nm", "-D", "--defined-only", tg.LIB_PATH], capture_output=True,
+                        text=True)
+    if nm.returncode == 0:
+        exported = set(re.findall(r"\sT\s+(\S+)", nm.stdout))
+        for name in header_functions():
+            assert name in exported, name
+
+
+def test_version_and_status_strings(tg):
+    assert tg.tg_version().startswith("libtgemm ")
+    assert "sm_103a" in tg.tg_version()
+    for code in range(7):
+        assert tg.tg_status_string(code).startswith("TG_")
+    assert tg.tg_status_string(99) == "TG_ERR_UNKNOWN"
+
+
+GOOD = 1 << 20  # a 16-byte aligned fake address (never dereferenced on these paths)
+
+
+@pytest.mark.parametrize("args,want", [
+    # (A, B, C, M, N, K, lda, ldb, ldc, epi)
+    ((GOOD, GOOD, GOOD, 4, 4, 4, 8, 8, 8, 2), 1),          # bad epilogue
+    ((GOOD, GOOD, GOOD, -1, 4, 4, 8, 8, 8, 0), 1),         # negative M
+    ((GOOD, GOOD, GOOD, 4, 4, -4, 8, 8, 8, 0), 1),         # negative K
+    ((GOOD, GOOD, GOOD, 1 << 31, 4, 4, 8, 8, 8, 0), 1),    # M too large
+    ((0, GOOD, GOOD, 4, 4, 4, 8, 8, 8, 0), 1),             # null A
+    ((GOOD, 0, GOOD, 4, 4, 4, 8, 8, 8, 0), 1),             # null B
+    ((GOOD, GOOD, 0, 4, 4, 4, 8, 8, 8, 0), 1),             # null C
+    ((GOOD, GOOD, GOOD, 4, 4, 9, 8, 16, 8, 0), 1),         # lda < K
+    ((GOOD, GOOD, GOOD, 4, 12, 4, 8, 8, 16, 0), 1),        # ldb < N
+    ((GOOD, GOOD, GOOD, 4, 12, 4, 8, 16, 8, 0), 1),        # ldc < N
+    ((GOOD + 2, GOOD, GOOD, 4, 4, 4, 8, 8, 8, 0), 2),      # A misaligned
+    ((GOOD, GOOD + 8, GOOD, 4, 4, 4, 8, 8, 8, 0), 2),      # B misaligned
+    ((GOOD, GOOD, GOOD + 4, 4, 4, 4, 8, 8, 8, 0), 2),      # C misaligned
+    ((GOOD, GOOD, GOOD, 4, 4, 4, 12, 8, 8, 0), 2),         # lda not a multiple of 8
+    ((GOOD, GOOD, GOOD, 4, 4, 4, 8, 8, 12, 0), 2),         # ldc not a multiple of 8
+    ((GOOD, GOOD, GOOD, 0, 4, 4, 8, 8, 8, 0), 0),          # M == 0: no-op
+    ((0, 0, 0, 4, 0, 4, 8, 8, 8, 1), 0),                   # N == 0: no-op, nothing checked
+    ((0, 0, GOOD, 4, 4, 0, 0, 0, 8, 0), None),             # K == 0: A/B/lda/ldb ignored
+])
+def test_argument_checks_before_any_cuda_call(tg, args, want):
+    st = tg.tg_gemm_f16(*args, None)
+    if want is None:
+        # valid arguments: on a machine without an sm_103 device the call
+        # reaches the device check and stops there
+        if _has_gpu():
+            pytest.skip("valid call would launch")
+        assert st == tg.TG_ERR_UNSUPPORTED_DEVICE
+    else:
+        assert st == want, (args, tg.tg_status_string(st))
+
+
+def test_valid_call_without_gpu_reports_unsupported_device(tg):
+    if _has_gpu():
+        pytest.skip("a GPU is present")
+    assert tg.tg_gemm_f16(GOOD, GOOD, GOOD, 4, 4, 4, 8, 8, 8, 0, None) == tg.TG_ERR_UNSUPPORTED_DEVICE
+    assert tg.tg_sync_status(None) == tg.TG_ERR_UNSUPPORTED_DEVICE
+
+
+def test_ring_bytes_reproduces_page_exercises(tg):
+    g = json.load(open(GOLDEN))
+    for c in g["cases"]:
+        assert tg.tg_ring_bytes(c["block_M"], c["block_N"], c["block_K"], c["stages"],
+                                c["elem_bytes"]) == c["ring_bytes"]
+    # one A stage, and the B buffers following three A stages
+    assert tg.tg_ring_bytes(128, 128, 64, 1, 2) == 2 * g["a_stage_bytes"]
+    assert 3 * g["a_stage_bytes"] == g["b_buffer_offset_3_stages"]
+    assert (228 * 1024) // tg.tg_ring_bytes(128, 128, 64, 3, 2) == g["blocks_per_sm_in_228KB_3_stages"]
+    assert tg.tg_ring_bytes(0, 128, 64, 3, 2) == -1
+
+
+def test_plan_k_steps_and_grid_match_page_listing(tg):
+    g = json.load(open(GOLDEN))
+    p = tg.tg_plan_f16(1024, 1024, 1024, 152)
+    assert p.k_blocks == g["k_steps_for_K1024_BK64"]
+    assert p.bk == 64
+    # with 128×128 tiles the page's grid is (N/128, M/128)
+    assert (1024 // 128, 1024 // p.bm) == tuple(g["grid_for_M_N_1024_tile_128"])
+
+
+def test_plans(tg):
+    p = tg.tg_plan_f16(8192, 28672, 4096, 152)
+    assert p.kernel == tg.TG_KERNEL_PERSISTENT
+    assert (p.bm, p.bn, p.bk) == (128, 256, 64)
+    assert p.num_tiles == 64 * 112 and p.grid == 152 and p.k_blocks == 64
+    assert p.smem_bytes <= 232448  # 227 KB opt-in limit per CTA
+    assert p.ring_bytes == tg.tg_ring_bytes(128, 256, 64, p.stages, 2)
+    s = tg.tg_plan_f16(64, 16384, 8192, 152)
+    assert s.kernel == tg.TG_KERNEL_SKINNY
+    assert (s.mma_m, s.mma_n) == (128, 64) and s.tiles_n == 128 and s.k_blocks == 128
+    assert s.grid == 152 and s.workspace_bytes > 0 and s.smem_bytes <= 232448
+    small = tg.tg_plan_f16(7, 5, 3, 152)
+    assert small.kernel == tg.TG_KERNEL_SKINNY and small.mma_n == 16 and small.grid == 1
+    assert tg.tg_plan_f16(0, 5, 3, 152).kernel == tg.TG_KERNEL_NONE
+    assert tg.tg_plan_f16(5, 5, 0, 152).kernel == tg.TG_KERNEL_FILL
+    mid = tg.tg_plan_f16(1024, 1024, 1024, 152)
+    assert mid.kernel == tg.TG_KERNEL_PERSISTENT and mid.bn == 128 and mid.num_tiles == 64
+    with pytest.raises(tg.TgemmError):
+        tg.tg_plan_f16(-1, 5, 5, 152)
+    with pytest.raises(tg.TgemmError):
+        tg.tg_plan_f16(5, 5, 5, 0)
+
+
+def test_tile_order_is_a_bijection_and_grouped(tg):
+    p = tg.tg_plan_f16(8192, 28672, 4096, 152)
+    seen = set()
+    for t in range(p.num_tiles):
+        seen.add(tg.tg_tile_coord(p, t))
+    assert len(seen) == p.num_tiles
+    assert all(0 <= m < p.tiles_m and 0 <= n < p.tiles_n for m, n in seen)
+    # the first wave spans group_m row blocks and few column blocks
+    first = [tg.tg_tile_coord(p, t) for t in range(p.grid)]
+    assert len({m for m, _ in first}) == p.group_m
+    assert len({n for _, n in first}) <= -(-p.grid // p.group_m)
+    with pytest.raises(tg.TgemmError):
+        tg.tg_tile_coord(p, p.num_tiles)
+
+
+def test_schedule_bruteforce_cpp(tmp_path):
+    exe = os.path.join(str(tmp_path), "sched_check")
+    subprocess.run(["g++", "-std=c++17", "-O1", "-I",
+                    os.path.join(ROOT, "tiled_fp16_gemm_gb300", "csrc"),
+                    os.path.join(ROOT, "tests", "sched_check.cpp"), "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "OK", r.stdout

@@ -1,0 +1,234 @@
+"""Python binding for libtgemm (dense FP16 GEMM on GB300, sm_103a).
+
+Argument marshalling only: every step of C = epi(A·B) runs in the CUDA
+kernels of ``libtgemm.so``, called through its C ABI (``include/tgemm.h``).
+PyTorch is used for device memory and streams.  There is no fallback: if the
+shared library is missing, the first call raises ImportError.
+
+Build the library with ``tiled_fp16_gemm_gb300.build.build()`` (nvcc, sm_103a).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtgemm.so")
+
+TG_EPI_NONE = 0
+TG_EPI_RELU = 1
+
+TG_OK = 0
+TG_ERR_INVALID_VALUE = 1
+TG_ERR_MISALIGNED = 2
+TG_ERR_UNSUPPORTED_DEVICE = 3
+TG_ERR_LAUNCH = 4
+TG_ERR_NO_MEMORY = 5
+TG_ERR_TIMEOUT = 6
+
+TG_KERNEL_NONE = 0
+TG_KERNEL_FILL = 1
+TG_KERNEL_PERSISTENT = 2
+TG_KERNEL_SKINNY = 3
+
+#: every symbol include/tgemm.h declares
+EXPORTS = (
+    "tg_gemm_f16", "tg_sync_status", "tg_status_string", "tg_version", "tg_plan_f16",
+    "tg_tile_coord", "tg_ring_bytes", "tg_debug_set_wait_timeout_ns", "tg_debug_inject",
+)
+
+
+class tg_plan_t(ctypes.Structure):
+    _fields_ = [
+        ("kernel", ctypes.c_int32), ("bm", ctypes.c_int32), ("bn", ctypes.c_int32),
+        ("bk", ctypes.c_int32), ("stages", ctypes.c_int32), ("mma_m", ctypes.c_int32),
+        ("mma_n", ctypes.c_int32), ("tiles_m", ctypes.c_int64), ("tiles_n", ctypes.c_int64),
+        ("k_blocks", ctypes.c_int64), ("num_tiles", ctypes.c_int64), ("grid", ctypes.c_int64),
+        ("threads", ctypes.c_int32), ("group_m", ctypes.c_int32),
+        ("smem_bytes", ctypes.c_int64), ("ring_bytes", ctypes.c_int64),
+        ("split_k", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
+    ]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_i64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+_lib = None
+
+
+def _L():
+    """Load libtgemm.so on first use; there is no fallback if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libtgemm.so not found at {LIB_PATH}; build it with "
+            "`python -m tiled_fp16_gemm_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(LIB_PATH)
+    lib.tg_gemm_f16.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int,
+                                _vp]
+    lib.tg_gemm_f16.restype = ctypes.c_int
+    lib.tg_sync_status.argtypes = [_vp]
+    lib.tg_sync_status.restype = ctypes.c_int
+    lib.tg_status_string.argtypes = [ctypes.c_int]
+    lib.tg_status_string.restype = ctypes.c_char_p
+    lib.tg_version.restype = ctypes.c_char_p
+    lib.tg_plan_f16.argtypes = [_i64, _i64, _i64, ctypes.c_int32, ctypes.POINTER(tg_plan_t)]
+    lib.tg_plan_f16.restype = ctypes.c_int
+    lib.tg_tile_coord.argtypes = [ctypes.POINTER(tg_plan_t), _i64, ctypes.POINTER(_i64),
+                                  ctypes.POINTER(_i64)]
+    lib.tg_tile_coord.restype = ctypes.c_int
+    lib.tg_ring_bytes.argtypes = [ctypes.c_int32] * 5
+    lib.tg_ring_bytes.restype = _i64
+    lib.tg_debug_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    lib.tg_debug_set_wait_timeout_ns.restype = None
+    lib.tg_debug_inject.argtypes = [ctypes.c_int32]
+    lib.tg_debug_inject.restype = None
+    _lib = lib
+    return lib
+
+
+def library():
+    """The loaded ctypes.CDLL of libtgemm.so."""
+    return _L()
+
+
+class TgemmError(RuntimeError):
+    def __init__(self, status: int, what: str = "tg_gemm_f16"):
+        self.status = status
+        super().__init__(f"{what}: {tg_status_string(status)}")
+
+
+# ------------------------------------------------------------------ raw C ABI
+
+def tg_gemm_f16(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
+                epilogue: int, stream: int | None) -> int:
+    """The C entry point with integer device pointers; returns the status code."""
+    return _L().tg_gemm_f16(A, B, C, M, N, K, lda, ldb, ldc, epilogue, stream or None)
+
+
+def tg_sync_status(stream: int | None) -> int:
+    return _L().tg_sync_status(stream or None)
+
+
+def tg_status_string(status: int) -> str:
+    return _L().tg_status_string(status).decode()
+
+
+def tg_version() -> str:
+    return _L().tg_version().decode()
+
+
+def tg_plan_f16(M: int, N: int, K: int, num_sms: int) -> tg_plan_t:
+    plan = tg_plan_t()
+    st = _L().tg_plan_f16(M, N, K, num_sms, ctypes.byref(plan))
+    if st != TG_OK:
+        raise TgemmError(st, "tg_plan_f16")
+    return plan
+
+
+def tg_tile_coord(plan: tg_plan_t, tile: int) -> tuple[int, int]:
+    m, n = _i64(), _i64()
+    st = _L().tg_tile_coord(ctypes.byref(plan), tile, ctypes.byref(m), ctypes.byref(n))
+    if st != TG_OK:
+        raise TgemmError(st, "tg_tile_coord")
+    return m.value, n.value
+
+
+def tg_ring_bytes(bm: int, bn: int, bk: int, stages: int, elem_bytes: int) -> int:
+    return _L().tg_ring_bytes(bm, bn, bk, stages, elem_bytes)
+
+
+def tg_debug_set_wait_timeout_ns(ns: int) -> None:
+    _L().tg_debug_set_wait_timeout_ns(ns)
+
+
+def tg_debug_inject(mode: int) -> None:
+    _L().tg_debug_inject(mode)
+
+
+# ------------------------------------------------------------------ torch helpers
+
+def _check_operand(t, name: str):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.float16:
+        raise TypeError(f"{name} must be float16, got {t.dtype}")
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must be row-major (unit column stride)")
+
+
+def _ld(t) -> int:
+    if t.shape[0] > 1:
+        return int(t.stride(0))
+    # a single row: the row stride is never used, pass the 8-aligned width
+    return max(8, (int(t.shape[1]) + 7) // 8 * 8)
+
+
+def gemm(a, b, relu: bool = False, out=None, stream=None):
+    """C = epi(a @ b) for CUDA float16 tensors a (M×K) and b (K×N).
+
+    Row-major views with a row stride that is a multiple of 8 elements and
+    16-byte aligned storage are accepted; ``out`` (M×N, same rules) is written
+    in place when given.  Runs on ``stream`` (default: torch's current stream
+    of a's device).
+    """
+    import torch
+    _check_operand(a, "a")
+    _check_operand(b, "b")
+    M, K = a.shape
+    K2, N = b.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if not (a.is_cuda and b.is_cuda and a.device == b.device):
+        raise ValueError("a and b must be CUDA tensors on the same device")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=a.device)
+    else:
+        _check_operand(out, "out")
+        if tuple(out.shape) != (M, N) or out.device != a.device:
+            raise ValueError("out must be M×N on a's device")
+    with torch.cuda.device(a.device):
+        s = stream if stream is not None else torch.cuda.current_stream(a.device)
+        st = tg_gemm_f16(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K, _ld(a), _ld(b),
+                         _ld(out), TG_EPI_RELU if relu else TG_EPI_NONE, s.cuda_stream)
+    if st != TG_OK:
+        raise TgemmError(st)
+    return out
+
+
+def gemm_host(a, b, relu: bool = False, stream=None, device=None):
+    """End-to-end C = epi(a @ b) from host (CPU) float16 tensors.
+
+    Copies a and b to the device, runs tg_gemm_f16, copies C back into a
+    pinned host tensor and waits for it.  Inputs in pinned memory are copied
+    asynchronously.
+    """
+    import torch
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        with torch.cuda.stream(s):
+            da = a.to(dev, non_blocking=True)
+            db = b.to(dev, non_blocking=True)
+            dc = gemm(da, db, relu=relu, stream=s)
+            hc = torch.empty(dc.shape, dtype=dc.dtype, pin_memory=True)
+            hc.copy_(dc, non_blocking=True)
+        s.synchronize()
+    return hc
+
+
+def sync_status(stream=None) -> None:
+    """Wait for the stream and raise TgemmError if a kernel reported a timeout."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = tg_sync_status(s.cuda_stream)
+    if st != TG_OK:
+        raise TgemmError(st, "tg_sync_status")

@@ -1,0 +1,486 @@
+// Skinny FP16 GEMM (M ≤ 128) for sm_103a:  C = epi(A · B), bandwidth bound.
+//
+// With few rows of C the 128-row tensor-core tile would mostly multiply
+// padding, and ceil(N/BN) tiles leave most SMs idle while B (the large
+// operand) streams from HBM.  So this kernel computes the transposed product
+//     C^T (N×M) = B^T (N×K) · A^T (K×M)
+// with N as the 128-row MMA dimension and Mp = roundup(M, 16) as the MMA
+// N dimension:
+//   MMA A operand = B^T tile, 128 n × 64 k, read MN-major from row-major B;
+//   MMA B operand = A tile,   Mp m × 64 k, K-major from row-major A;
+//   D (TMEM)      = 128 lanes (n) × Mp columns (m), fp32.
+//
+// Split-K over "units" (tile, k-block), numbered tile-major.  CTA c of G owns
+// the contiguous unit range [U·c/G, U·(c+1)/G), so every SM streams the same
+// number of B bytes.  A range is cut at tile edges into segments:
+//   FULL     the whole k range of a tile: epilogue writes C directly;
+//   PARTIAL  starts inside a tile (only a CTA's first segment can): its fp32
+//            partial goes to workspace slot c; each epilogue warp then sets
+//            flag[4c + warp quarter] = epoch for the 32 columns it wrote;
+//   OWNER    starts at k = 0 but the range ends inside the tile (only a CTA's
+//            last segment can): each epilogue warp waits for its quarter's
+//            flags of CTAs c+1 .. c_last holding the rest of the tile, then
+//            adds their partials in that order (k order), applies the
+//            epilogue and writes C.  No barrier spans several warps.
+// The summation order is fixed by the sizes alone, so results are
+// deterministic.  Owners only wait on higher-numbered CTAs, which write their
+// partials from their first segment, so the waits form no cycle; the launch
+// is cooperative so all G ≤ #SM CTAs are resident together.  All waits are
+// bounded.
+//
+// The pages do not describe a split-K or swap-AB variant; this is the plain
+// reading of "measure the bandwidth and compute ceilings first"
+// ("TileLang：比 Triton 低一层的 tile 语言", section "工程上的几个注意点"):
+// a 64×16384×8192 product is bound by streaming B, so the kernel is shaped to
+// keep every SM's TMA unit busy on B.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "gemm_persistent.cuh"
+#include "sm103_ptx.cuh"
+#include "tile_schedule.h"
+#include "tgemm.h"
+
+namespace tg {
+
+constexpr int kSkStages = 6;
+constexpr uint32_t kSkBBytes = 128 * 64 * 2;  // B^T tile: two 64×64 boxes
+constexpr uint32_t kSkASlot = 128 * 64 * 2;   // A tile, room for Mp ≤ 128 rows
+constexpr uint32_t kSkStageBytes = kSkBBytes + kSkASlot;
+constexpr uint32_t kSkSmemBytes = 1024 + kSkStages * kSkStageBytes + 256;
+constexpr uint32_t kSkTmemCols = 256;        // two accumulators of up to 128 columns
+constexpr int64_t kSkSlotFloats = 128 * 128;  // one partial: Mp ≤ 128 rows × 128 n
+constexpr int kSkMinUnitsPerCta = 8;
+
+struct SkinnyParams {
+    int32_t M, N, K, Mp;
+    int32_t tiles_n, k_blocks;
+    int64_t total_units;
+    int32_t relu, inject;
+    uint64_t timeout_ns;
+    __half* C;
+    int64_t ldc;
+    float* ws;
+    uint32_t* flags;
+    uint32_t epoch;
+};
+
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(192, 1)
+    tg_gemm_f16_skinny(const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmA, const SkinnyParams p) {
+    constexpr int BK = 64;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const base_ptr = smem_raw + (base - raw);
+
+    const uint32_t sB = base;                             // [stages] B^T tiles
+    const uint32_t sA = sB + kSkStages * kSkBBytes;       // [stages] A tiles
+    const uint32_t sBar = sA + kSkStages * kSkASlot;
+    const uint32_t bar_full = sBar;
+    const uint32_t bar_empty = sBar + 8 * kSkStages;
+    const uint32_t bar_tfull = sBar + 16 * kSkStages;
+    const uint32_t bar_tempty = bar_tfull + 16;
+    const uint32_t bar_drain = bar_tempty + 16;
+    const uint32_t slot_tmem = bar_drain + 8;
+    uint32_t* const tmem_slot_ptr = reinterpret_cast<uint32_t*>(base_ptr + (slot_tmem - base));
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(tmem_slot_ptr + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t G = gridDim.x;
+    const int64_t U = p.total_units;
+    const int64_t KB = p.k_blocks;
+    const int64_t u_begin = unit_begin(blockIdx.x, G, U);
+    const int64_t u_end = unit_begin(blockIdx.x + 1, G, U);
+    const uint32_t a_bytes = static_cast<uint32_t>(p.Mp) * 128u;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSkStages; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar_tfull + 8 * a, 1);
+            mbar_init(bar_tempty + 8 * a, 4);
+        }
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(slot_tmem, kSkTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot_ptr;
+
+    auto fail = [&](unsigned int role) {
+        atomicOr(&g_wait_timeout_flags, role);
+        *abort_flag = 1;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t keep = policy_evict_last();   // A: reread by every CTA
+            const uint64_t stream = policy_evict_first(); // B: read exactly once
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_parity = 0;
+            for (int64_t u = u_begin; u < u_end; ++u) {
+                const int32_t t = static_cast<int32_t>(u / KB);
+                const int32_t kb = static_cast<int32_t>(u - t * KB);
+                if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.timeout_ns, abort_flag)) {
+                    fail(kRoleProducer);
+                    break;
+                }
+                const uint32_t full = bar_full + 8 * stage;
+                mbar_arrive_expect_tx(full, kSkBBytes + a_bytes);
+                const uint32_t b0 = sB + stage * kSkBBytes;
+                tma_load_2d_hint(b0, &tmB, full, t * 128, kb * BK, stream);
+                tma_load_2d_hint(b0 + 8192, &tmB, full, t * 128 + 64, kb * BK, stream);
+                tma_load_2d_hint(sA + stage * kSkASlot, &tmA, full, kb * BK, 0, keep);
+                issued_mask |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == kSkStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            for (int s = 0; s < kSkStages; ++s)
+                if (issued_mask & (1u << s))
+                    if (!mbar_wait(bar_full + 8 * s, (issued_parity >> s) & 1u, p.timeout_ns,
+                                   nullptr))
+                        atomicOr(&g_wait_timeout_flags, kRoleDrain);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16_f32(128, p.Mp, /*a_mn=*/true, /*b_mn=*/false);
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int64_t u = u_begin; ok && u < u_end; ++it) {
+                const int64_t t = u / KB;
+                const int64_t seg_end = (t + 1) * KB < u_end ? (t + 1) * KB : u_end;
+                const int acc = it & 1;
+                const uint32_t acc_phase = (it >> 1) & 1;
+                if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
+                    fail(kRoleMma);
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 128);
+                for (int64_t v = u; v < seg_end; ++v) {
+                    if (!mbar_wait(bar_full + 8 * stage, phase, p.timeout_ns, abort_flag)) {
+                        fail(kRoleMma);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t b0 = sB + stage * kSkBBytes;
+                    const uint32_t a0 = sA + stage * kSkASlot;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint64_t adesc = smem_desc_sw128(b0 + 2048 * k, 8192, 1024);
+                        const uint64_t bdesc = smem_desc_sw128(a0 + 32 * k, 16, 1024);
+                        mma_f16_ss(d_tmem, adesc, bdesc, idesc, (v != u || k != 0) ? 1u : 0u);
+                    }
+                    mma_commit(bar_empty + 8 * stage);
+                    if (++stage == kSkStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if (!(p.inject == 1 && it == 0)) mma_commit(bar_tfull + 8 * acc);
+                u = seg_end;
+            }
+            mma_commit(bar_drain);
+            if (!mbar_wait(bar_drain, 0, p.timeout_ns, nullptr))
+                atomicOr(&g_wait_timeout_flags, kRoleDrain);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int n_local = 32 * q + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+        const int nchunks = p.Mp / 16;
+        int it = 0;
+        for (int64_t u = u_begin; u < u_end; ++it) {
+            const int64_t t = u / KB;
+            const int64_t kb0 = u - t * KB;
+            const int64_t seg_end = (t + 1) * KB < u_end ? (t + 1) * KB : u_end;
+            const int64_t kb1 = seg_end - t * KB;
+            const int acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            const int64_t n = t * 128 + n_local;
+            int ok = 1;
+            if (lane == 0)
+                ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, p.timeout_ns, abort_flag) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) fail(kRoleEpilogue);
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * 128);
+
+            if (kb0 > 0) {
+                // PARTIAL: fp32 partial to this CTA's slot, layout [m][n_local].
+                float* slot = p.ws + static_cast<int64_t>(blockIdx.x) * kSkSlotFloats;
+                for (int c = 0; c < nchunks; ++c) {
+                    uint32_t r[16];
+                    tmem_ld_x16(tacc + 16 * c, r);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        __stcg(slot + (16 * c + i) * 128 + n_local, __uint_as_float(r[i]));
+                }
+                tc_fence_before_sync();
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar_tempty + 8 * acc);
+                    // this warp's 32 columns of the partial are published
+                    st_release_gpu(p.flags + 4 * static_cast<int64_t>(blockIdx.x) + q, p.epoch);
+                }
+            } else {
+                // FULL or OWNER.
+                int64_t c_first = 0, c_last = -1;
+                if (kb1 < KB) {  // OWNER: the rest of the tile lives in CTAs c+1 .. c_last
+                    c_first = blockIdx.x + 1;
+                    c_last = unit_owner((t + 1) * KB - 1, G, U);
+                    bool got = true;
+                    for (int64_t c = c_first; c <= c_last && got; ++c) {
+                        const uint32_t* f = p.flags + 4 * c + q;
+                        if (ld_acquire_gpu(f) != p.epoch) {
+                            const uint64_t t0 = globaltimer_ns();
+                            while (ld_acquire_gpu(f) != p.epoch) {
+                                if (*abort_flag || globaltimer_ns() - t0 > p.timeout_ns) {
+                                    got = false;
+                                    break;
+                                }
+                                __nanosleep(64);
+                            }
+                        }
+                    }
+                    if (__any_sync(0xffffffffu, !got)) {
+                        if (lane == 0) fail(kRoleEpilogue);
+                        break;
+                    }
+                }
+                for (int c = 0; c < nchunks; ++c) {
+                    uint32_t r[16];
+                    tmem_ld_x16(tacc + 16 * c, r);
+                    float v[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+                    for (int64_t cc = c_first; cc <= c_last; ++cc) {
+                        const float* slot = p.ws + cc * kSkSlotFloats;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[i] += __ldcg(slot + (16 * c + i) * 128 + n_local);
+                    }
+                    if (n < p.N) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int m = 16 * c + i;
+                            if (m < p.M) {
+                                const float x = p.relu ? relu_f32(v[i]) : v[i];
+                                p.C[static_cast<int64_t>(m) * p.ldc + n] = __float2half_rn(x);
+                            }
+                        }
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+            }
+            u = seg_end;
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, kSkTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+inline bool skinny_applies(int64_t M, int64_t N, int64_t K) {
+    (void)N;
+    (void)K;
+    return M >= 1 && M <= 128;
+}
+
+inline void skinny_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* pl) {
+    const int64_t Mp = (M + 15) / 16 * 16;
+    pl->kernel = TG_KERNEL_SKINNY;
+    pl->bm = static_cast<int32_t>(Mp);
+    pl->bn = 128;
+    pl->bk = 64;
+    pl->stages = kSkStages;
+    pl->mma_m = 128;
+    pl->mma_n = static_cast<int32_t>(Mp);
+    pl->tiles_m = 1;
+    pl->tiles_n = (N + 127) / 128;
+    pl->k_blocks = (K + 63) / 64;
+    pl->num_tiles = pl->tiles_n;
+    const int64_t U = pl->tiles_n * pl->k_blocks;
+    int64_t G = U / kSkMinUnitsPerCta;
+    if (G < 1) G = 1;
+    if (G > num_sms) G = num_sms;
+    pl->grid = G;
+    pl->threads = 192;
+    pl->group_m = 1;
+    pl->smem_bytes = kSkSmemBytes;
+    pl->ring_bytes = static_cast<int64_t>(kSkStages) * kSkStageBytes;
+    // most CTAs touching one tile: its k range over the shortest unit range, plus one
+    const int64_t shortest = U / G;
+    pl->split_k = shortest > 0 ? (pl->k_blocks + shortest - 1) / shortest + 1 : pl->k_blocks;
+    if (pl->split_k > G) pl->split_k = G;
+    pl->workspace_bytes = G * kSkSlotFloats * 4 + 4 * G * 4;
+}
+
+inline cudaError_t skinny_set_attributes() {
+    return cudaFuncSetAttribute(tg_gemm_f16_skinny, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSkSmemBytes);
+}
+
+struct SkinnyWorkspace {
+    float* partials = nullptr;
+    uint32_t* flags = nullptr;
+    int64_t slots = 0;
+    uint32_t epoch = 0;
+};
+
+inline std::mutex& skinny_ws_mutex() {
+    static std::mutex m;
+    return m;
+}
+
+inline std::map<std::pair<int, cudaStream_t>, SkinnyWorkspace>& skinny_ws_map() {
+    static std::map<std::pair<int, cudaStream_t>, SkinnyWorkspace> m;
+    return m;
+}
+
+using EncodeFn = bool (*)(CUtensorMap*, const void*, uint64_t, uint64_t, uint64_t, uint32_t,
+                          uint32_t);
+
+inline tg_status_t skinny_launch(const void* A, const void* B, void* C, const tg_plan_t& pl,
+                                 int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                 int64_t ldc, int epilogue, cudaStream_t stream, int dev,
+                                 uint64_t timeout_ns, int32_t inject, EncodeFn encode) {
+    const int64_t Mp = pl.mma_n;
+    CUtensorMap tmA, tmB;
+    if (!encode(&tmB, B, N, K, ldb * 2, 64, 64) ||
+        !encode(&tmA, A, K, M, lda * 2, 64, static_cast<uint32_t>(Mp)))
+        return TG_ERR_LAUNCH;
+
+    SkinnyParams prm;
+    {
+        std::lock_guard<std::mutex> lk(skinny_ws_mutex());
+        SkinnyWorkspace& ws = skinny_ws_map()[std::make_pair(dev, stream)];
+        if (ws.slots < pl.grid) {
+            // grow: ordered after all earlier work on this stream
+            if (ws.partials) {
+                cudaStreamSynchronize(stream);
+                cudaFree(ws.partials);
+                cudaFree(ws.flags);
+                ws.partials = nullptr;
+                ws.flags = nullptr;
+                ws.slots = 0;
+            }
+            const int64_t slots = pl.grid;
+            if (cudaMalloc(&ws.partials, slots * kSkSlotFloats * sizeof(float)) != cudaSuccess ||
+                cudaMalloc(&ws.flags, 4 * slots * sizeof(uint32_t)) != cudaSuccess) {
+                cudaGetLastError();
+                if (ws.partials) cudaFree(ws.partials);
+                ws.partials = nullptr;
+                ws.flags = nullptr;
+                return TG_ERR_NO_MEMORY;
+            }
+            if (cudaMemsetAsync(ws.flags, 0, 4 * slots * sizeof(uint32_t), stream) != cudaSuccess) {
+                cudaGetLastError();
+                return TG_ERR_LAUNCH;
+            }
+            ws.slots = slots;
+            ws.epoch = 0;
+        }
+        if (++ws.epoch == 0) ws.epoch = 1;
+        prm.ws = ws.partials;
+        prm.flags = ws.flags;
+        prm.epoch = ws.epoch;
+    }
+    prm.M = static_cast<int32_t>(M);
+    prm.N = static_cast<int32_t>(N);
+    prm.K = static_cast<int32_t>(K);
+    prm.Mp = static_cast<int32_t>(Mp);
+    prm.tiles_n = static_cast<int32_t>(pl.tiles_n);
+    prm.k_blocks = static_cast<int32_t>(pl.k_blocks);
+    prm.total_units = pl.tiles_n * pl.k_blocks;
+    prm.relu = epilogue == TG_EPI_RELU ? 1 : 0;
+    prm.inject = inject;
+    prm.timeout_ns = timeout_ns;
+    prm.C = static_cast<__half*>(C);
+    prm.ldc = ldc;
+
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = kSkSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, tg_gemm_f16_skinny, tmB, tmA, prm);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return TG_ERR_LAUNCH;
+    }
+    return TG_OK;
+}
+
+}  // namespace tg

@@ -1,0 +1,355 @@
+// libtgemm host side: argument validation, launch planning, tensor-map
+// encoding and kernel launch for C = epi(A·B) (fp16 in, fp32 accumulate,
+// fp16 out) on sm_103a.  The C ABI is declared in include/tgemm.h.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "tgemm.h"
+#include "gemm_persistent.cuh"
+#include "gemm_skinny.cuh"
+#include "tile_schedule.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxDim = 2147483647LL;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
+std::atomic<int32_t> g_inject{0};
+
+// ------------------------------------------------------------------ planning
+
+constexpr int kBigBN = 256, kBigStages = 4;
+constexpr int kMidBN = 128, kMidStages = 6;
+constexpr int kGroupM = 16;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+void plan_persistent(int64_t M, int64_t N, int64_t K, int32_t num_sms, int bn, int stages,
+                     int64_t smem, tg_plan_t* p) {
+    p->kernel = TG_KERNEL_PERSISTENT;
+    p->bm = 128;
+    p->bn = bn;
+    p->bk = 64;
+    p->stages = stages;
+    p->mma_m = 128;
+    p->mma_n = bn;
+    p->tiles_m = ceil_div(M, 128);
+    p->tiles_n = ceil_div(N, bn);
+    p->k_blocks = ceil_div(K, 64);
+    p->num_tiles = p->tiles_m * p->tiles_n;
+    p->grid = p->num_tiles < num_sms ? p->num_tiles : num_sms;
+    p->threads = 192;
+    p->group_m = static_cast<int32_t>(p->tiles_m < kGroupM ? p->tiles_m : kGroupM);
+    p->smem_bytes = smem;
+    p->ring_bytes = tg_ring_bytes(128, bn, 64, stages, 2);
+    p->split_k = 1;
+    p->workspace_bytes = 0;
+}
+
+// ------------------------------------------------------------------ device state
+
+struct DeviceState {
+    bool probed = false;
+    bool supported = false;
+    int num_sms = 0;
+    bool attrs_set = false;
+};
+
+std::mutex g_dev_mutex;
+DeviceState g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+// Returns TG_OK and fills *dev / *st for the current device, or an error.
+tg_status_t current_device(int* dev, DeviceState** st) {
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) {
+        cudaGetLastError();
+        return TG_ERR_UNSUPPORTED_DEVICE;
+    }
+    std::lock_guard<std::mutex> lk(g_dev_mutex);
+    DeviceState& s = g_dev[d];
+    if (!s.probed) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) {
+            cudaGetLastError();
+            return TG_ERR_UNSUPPORTED_DEVICE;
+        }
+        s.probed = true;
+        s.supported = (major == 10 && minor == 3);
+        s.num_sms = sms;
+    }
+    if (!s.supported) return TG_ERR_UNSUPPORTED_DEVICE;
+    if (!s.attrs_set) {
+        using C1 = tg::PersistentCfg<kBigBN, kBigStages>;
+        using C2 = tg::PersistentCfg<kMidBN, kMidStages>;
+        if (cudaFuncSetAttribute(tg::tg_gemm_f16_persistent<kBigBN, kBigStages>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C1::kSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(tg::tg_gemm_f16_persistent<kMidBN, kMidStages>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C2::kSmemBytes) != cudaSuccess ||
+            tg::skinny_set_attributes() != cudaSuccess) {
+            cudaGetLastError();
+            return TG_ERR_LAUNCH;
+        }
+        s.attrs_set = true;
+    }
+    *dev = d;
+    *st = &s;
+    return TG_OK;
+}
+
+// 2-D fp16 tensor map: inner (contiguous) extent, outer extent, row stride in
+// bytes, box, 128-byte swizzle, zero fill outside the tensor.
+bool encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES>
+tg_status_t launch_persistent(const void* A, const void* B, void* C, const tg_plan_t& pl,
+                              int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                              int64_t ldc, int epilogue, cudaStream_t stream) {
+    CUtensorMap tmA, tmB, tmC;
+    if (!encode_2d(&tmA, A, K, M, lda * 2, 64, 128) || !encode_2d(&tmB, B, N, K, ldb * 2, 64, 64) ||
+        !encode_2d(&tmC, C, N, M, ldc * 2, 64, 32))
+        return TG_ERR_LAUNCH;
+    tg::PersistentParams prm;
+    prm.M = static_cast<int32_t>(M);
+    prm.N = static_cast<int32_t>(N);
+    prm.K = static_cast<int32_t>(K);
+    prm.tiles_m = static_cast<int32_t>(pl.tiles_m);
+    prm.tiles_n = static_cast<int32_t>(pl.tiles_n);
+    prm.num_tiles = static_cast<int32_t>(pl.num_tiles);
+    prm.k_blocks = static_cast<int32_t>(pl.k_blocks);
+    prm.group_m = pl.group_m;
+    prm.relu = epilogue == TG_EPI_RELU ? 1 : 0;
+    prm.inject = g_inject.exchange(0);
+    prm.timeout_ns = g_timeout_ns.load();
+
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
+    cfg.blockDim = dim3(tg::PersistentCfg<BN, STAGES>::kThreads);
+    cfg.dynamicSmemBytes = tg::PersistentCfg<BN, STAGES>::kSmemBytes;
+    cfg.stream = stream;
+    cudaError_t e =
+        cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_persistent<BN, STAGES>, tmA, tmB, tmC, prm);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return TG_ERR_LAUNCH;
+    }
+    return TG_OK;
+}
+
+// TGEMM_FORCE_CFG = persistent256 | persistent128 | skinny overrides the
+// planner's kernel choice (used by tests and tile sweeps); ignored where the
+// forced kernel does not apply (skinny needs M <= 128; K == 0 always fills).
+void apply_forced_config(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* pl) {
+    const char* f = std::getenv("TGEMM_FORCE_CFG");
+    if (f == nullptr || *f == 0 || pl->kernel == TG_KERNEL_NONE || pl->kernel == TG_KERNEL_FILL)
+        return;
+    if (std::strcmp(f, "persistent256") == 0)
+        plan_persistent(M, N, K, num_sms, kBigBN, kBigStages,
+                        tg::PersistentCfg<kBigBN, kBigStages>::kSmemBytes, pl);
+    else if (std::strcmp(f, "persistent128") == 0)
+        plan_persistent(M, N, K, num_sms, kMidBN, kMidStages,
+                        tg::PersistentCfg<kMidBN, kMidStages>::kSmemBytes, pl);
+    else if (std::strcmp(f, "skinny") == 0 && tg::skinny_applies(M, N, K))
+        tg::skinny_plan(M, N, K, num_sms, pl);
+}
+
+tg_status_t validate(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
+                     int64_t lda, int64_t ldb, int64_t ldc, int epilogue) {
+    if (epilogue != TG_EPI_NONE && epilogue != TG_EPI_RELU) return TG_ERR_INVALID_VALUE;
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return TG_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return TG_OK;
+    if (C == nullptr || ldc < N) return TG_ERR_INVALID_VALUE;
+    if (K > 0 && (A == nullptr || B == nullptr || lda < K || ldb < N)) return TG_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(C) & 15u) != 0 || (ldc & 7) != 0) return TG_ERR_MISALIGNED;
+    if (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15u) != 0 ||
+                  (reinterpret_cast<uintptr_t>(B) & 15u) != 0 || (lda & 7) != 0 ||
+                  (ldb & 7) != 0))
+        return TG_ERR_MISALIGNED;
+    return TG_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+int64_t tg_ring_bytes(int32_t bm, int32_t bn, int32_t bk, int32_t stages, int32_t elem_bytes) {
+    if (bm <= 0 || bn <= 0 || bk <= 0 || stages <= 0 || elem_bytes <= 0) return -1;
+    const int64_t per_stage = (static_cast<int64_t>(bm) * bk + static_cast<int64_t>(bk) * bn) *
+                              elem_bytes;
+    return per_stage * stages;
+}
+
+tg_status_t tg_plan_f16(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* plan) {
+    if (plan == nullptr || num_sms < 1) return TG_ERR_INVALID_VALUE;
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return TG_ERR_INVALID_VALUE;
+    std::memset(plan, 0, sizeof(*plan));
+    if (M == 0 || N == 0) {
+        plan->kernel = TG_KERNEL_NONE;
+        return TG_OK;
+    }
+    if (K == 0) {
+        plan->kernel = TG_KERNEL_FILL;
+        plan->threads = 256;
+        int64_t blocks = ceil_div(M * N, 256);
+        plan->grid = blocks < 4 * num_sms ? blocks : 4 * num_sms;
+        return TG_OK;
+    }
+    if (tg::skinny_applies(M, N, K)) {
+        tg::skinny_plan(M, N, K, num_sms, plan);
+        return TG_OK;
+    }
+    const int64_t tiles256 = ceil_div(M, 128) * ceil_div(N, kBigBN);
+    if (tiles256 >= num_sms || N <= kMidBN) {
+        if (N <= kMidBN)
+            plan_persistent(M, N, K, num_sms, kMidBN, kMidStages,
+                            tg::PersistentCfg<kMidBN, kMidStages>::kSmemBytes, plan);
+        else
+            plan_persistent(M, N, K, num_sms, kBigBN, kBigStages,
+                            tg::PersistentCfg<kBigBN, kBigStages>::kSmemBytes, plan);
+    } else {
+        plan_persistent(M, N, K, num_sms, kMidBN, kMidStages,
+                        tg::PersistentCfg<kMidBN, kMidStages>::kSmemBytes, plan);
+    }
+    return TG_OK;
+}
+
+tg_status_t tg_tile_coord(const tg_plan_t* plan, int64_t tile, int64_t* m_blk, int64_t* n_blk) {
+    if (plan == nullptr || m_blk == nullptr || n_blk == nullptr) return TG_ERR_INVALID_VALUE;
+    if (plan->kernel != TG_KERNEL_PERSISTENT || tile < 0 || tile >= plan->num_tiles)
+        return TG_ERR_INVALID_VALUE;
+    const tg::TileCoord c =
+        tg::tile_coord(static_cast<int32_t>(tile), static_cast<int32_t>(plan->tiles_m),
+                       static_cast<int32_t>(plan->tiles_n), plan->group_m);
+    *m_blk = c.m_blk;
+    *n_blk = c.n_blk;
+    return TG_OK;
+}
+
+void tg_debug_set_wait_timeout_ns(uint64_t ns) {
+    g_timeout_ns.store(ns == 0 ? kDefaultTimeoutNs : ns);
+}
+
+void tg_debug_inject(int32_t mode) { g_inject.store(mode); }
+
+const char* tg_status_string(tg_status_t s) {
+    switch (s) {
+        case TG_OK: return "TG_OK";
+        case TG_ERR_INVALID_VALUE: return "TG_ERR_INVALID_VALUE";
+        case TG_ERR_MISALIGNED: return "TG_ERR_MISALIGNED";
+        case TG_ERR_UNSUPPORTED_DEVICE: return "TG_ERR_UNSUPPORTED_DEVICE";
+        case TG_ERR_LAUNCH: return "TG_ERR_LAUNCH";
+        case TG_ERR_NO_MEMORY: return "TG_ERR_NO_MEMORY";
+        case TG_ERR_TIMEOUT: return "TG_ERR_TIMEOUT";
+    }
+    return "TG_ERR_UNKNOWN";
+}
+
+const char* tg_version(void) { return "libtgemm 0.1.0 (sm_103a)"; }
+
+tg_status_t tg_gemm_f16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                        int64_t lda, int64_t ldb, int64_t ldc, int epilogue, void* stream) {
+    tg_status_t st = validate(A, B, C, M, N, K, lda, ldb, ldc, epilogue);
+    if (st != TG_OK || M == 0 || N == 0) return st;
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    st = current_device(&dev, &ds);
+    if (st != TG_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    tg_plan_t pl;
+    st = tg_plan_f16(M, N, K, ds->num_sms, &pl);
+    if (st != TG_OK) return st;
+    apply_forced_config(M, N, K, ds->num_sms, &pl);
+
+    switch (pl.kernel) {
+        case TG_KERNEL_FILL: {
+            tg::tg_fill_zero_f16<<<static_cast<unsigned>(pl.grid), 256, 0, s>>>(
+                static_cast<__half*>(C), M, N, ldc);
+            if (cudaGetLastError() != cudaSuccess) return TG_ERR_LAUNCH;
+            return TG_OK;
+        }
+        case TG_KERNEL_PERSISTENT:
+            if (pl.bn == kBigBN)
+                return launch_persistent<kBigBN, kBigStages>(A, B, C, pl, M, N, K, lda, ldb, ldc,
+                                                            epilogue, s);
+            return launch_persistent<kMidBN, kMidStages>(A, B, C, pl, M, N, K, lda, ldb, ldc,
+                                                        epilogue, s);
+        case TG_KERNEL_SKINNY: {
+            const uint64_t timeout = g_timeout_ns.load();
+            const int32_t inject = g_inject.exchange(0);
+            return tg::skinny_launch(A, B, C, pl, M, N, K, lda, ldb, ldc, epilogue, s, dev,
+                                     timeout, inject, encode_2d);
+        }
+        default:
+            return TG_ERR_INVALID_VALUE;
+    }
+}
+
+tg_status_t tg_sync_status(void* stream) {
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    tg_status_t st = current_device(&dev, &ds);
+    if (st != TG_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return TG_ERR_LAUNCH;
+    }
+    unsigned int flags = 0;
+    if (cudaMemcpyFromSymbol(&flags, tg::g_wait_timeout_flags, sizeof(flags)) != cudaSuccess) {
+        cudaGetLastError();
+        return TG_ERR_LAUNCH;
+    }
+    if (flags != 0) {
+        const unsigned int zero = 0;
+        cudaMemcpyToSymbol(tg::g_wait_timeout_flags, &zero, sizeof(zero));
+        return TG_ERR_TIMEOUT;
+    }
+    return TG_OK;
+}
+
+}  // extern "C"
