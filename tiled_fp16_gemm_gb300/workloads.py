@@ -68,6 +68,10 @@ WORKLOADS = {
         Workload("skinny_64x16384x8192", 64, 16384, 8192, False,
                  ("normal", 0.0, 1.0), ("normal", 0.0, 1.0 / float(np.sqrt(8192.0))), 5,
                  "weight streaming, HBM bound (B is 256 MiB)"),
+        Workload("profile_8192x8192x4096_relu", 8192, 8192, 4096, True,
+                 ("normal", 0.0, 1.0 / 64.0), ("normal", 0.0, 1.0 / 64.0), 6,
+                 "profiling case for the persistent kernel: the MLP shape with N cut to "
+                 "8192 (256 MiB of A, B and C, twice L2)"),
     ]
 }
 
