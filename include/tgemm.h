@@ -160,6 +160,47 @@ void tg_debug_set_wait_timeout_ns(uint64_t ns);
  * setting applies to exactly one launch. */
 void tg_debug_inject(int32_t mode);
 
+/* ------------------------------------------------------------------------
+ * Entry point that allocates nothing.
+ * ------------------------------------------------------------------------ */
+
+/* Size of the scratch array inside the library that tg_gemm_f16_noalloc uses. */
+#define TG_NOALLOC_SCRATCH_BYTES ((int64_t)12 * 1024 * 1024)
+
+/*
+ * tg_gemm_f16_noalloc — C = epi(A·B) for 1 ≤ M ≤ 128 without allocating any
+ * device memory.  The pages have no counterpart for this entry point: it
+ * exists for callers that cannot allocate device memory at call time, e.g. a
+ * service that handed all device memory to its own pool allocator at
+ * start-up (a late cudaMalloc would fail or fragment that pool), or code in a
+ * phase where a cudaMalloc, which may synchronise the whole device, must not
+ * stall other streams.
+ *
+ * It runs the same split-K kernel that tg_gemm_f16 uses for M ≤ 128, with its
+ * scratch (fp32 partial sums and ready flags) in a fixed array of
+ * TG_NOALLOC_SCRATCH_BYTES (12 MiB) inside the library; every device that
+ * loads the library holds that array until the process exits.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Arguments, alignment rules, ownership of A, B and C, and argument errors are
+ * those of tg_gemm_f16.  Additionally:
+ *   - M > 128 returns TG_ERR_INVALID_VALUE (the split-K kernel covers
+ *     M ≤ 128 only); so does a problem whose split needs more scratch than the
+ *     array holds (more than 191 CTAs, i.e. a device with more than 191 SMs).
+ *   - K == 0 fills C with +0 and uses no scratch; M == 0 or N == 0 is a no-op.
+ *   - Set-up: the first call on each device (with that device current) looks
+ *     up the array's device address and clears its flag words on `stream`.
+ *     Make that first call before any stream capture begins.
+ *   - Every call shares the one array, which keeps what the last call left in
+ *     it.  Calls whose kernels overlap on the GPU (e.g. on two streams with no
+ *     ordering between them) race on it and give wrong results: order them on
+ *     one stream or with events.
+ */
+tg_status_t tg_gemm_f16_noalloc(const void* A, const void* B, void* C,
+                                int64_t M, int64_t N, int64_t K,
+                                int64_t lda, int64_t ldb, int64_t ldc,
+                                int epilogue, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

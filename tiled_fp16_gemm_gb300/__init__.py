@@ -36,7 +36,11 @@ TG_KERNEL_SKINNY = 3
 EXPORTS = (
     "tg_gemm_f16", "tg_sync_status", "tg_status_string", "tg_version", "tg_plan_f16",
     "tg_tile_coord", "tg_ring_bytes", "tg_debug_set_wait_timeout_ns", "tg_debug_inject",
+    "tg_gemm_f16_noalloc",
 )
+
+#: bytes of the library's fixed scratch array used by tg_gemm_f16_noalloc
+TG_NOALLOC_SCRATCH_BYTES = 12 * 1024 * 1024
 
 
 class tg_plan_t(ctypes.Structure):
@@ -149,6 +153,21 @@ def tg_debug_set_wait_timeout_ns(ns: int) -> None:
 
 def tg_debug_inject(mode: int) -> None:
     _L().tg_debug_inject(mode)
+
+
+def tg_gemm_f16_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+                        ldc: int, epilogue: int, stream: int | None) -> int:
+    """C = epi(A·B) for M <= 128 with no device allocation: the split-K
+    scratch lives in a fixed 12 MiB array inside the library.  For callers
+    that cannot allocate device memory at call time.  Calls that overlap on
+    the GPU share that array and race; the first call on a device does a
+    one-time set-up and should come before any stream capture.  Returns the
+    status code."""
+    lib = _L()
+    fn = lib.tg_gemm_f16_noalloc
+    fn.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _vp]
+    fn.restype = ctypes.c_int
+    return fn(A, B, C, M, N, K, lda, ldb, ldc, epilogue, stream or None)
 
 
 # ------------------------------------------------------------------ torch helpers

@@ -353,3 +353,132 @@ tg_status_t tg_sync_status(void* stream) {
 }
 
 }  // extern "C"
+
+// ====================================================================== no-allocation variant
+//
+// tg_gemm_f16_noalloc runs the skinny split-K kernel with its scratch (fp32
+// partial sums and the per-warp ready flags) in the file-scope array below
+// instead of a workspace obtained from cudaMalloc.  It serves callers that
+// cannot allocate device memory at call time.  The array is a fixed
+// TG_NOALLOC_SCRATCH_BYTES; every device that loads this library holds it
+// until the process exits.
+//
+// In host code `g_noalloc_scratch` only names the variable: it is not a
+// device address.  Its device address is looked up once per device with
+// cudaGetSymbolAddress (with that device current) and passed to the kernel.
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[TG_NOALLOC_SCRATCH_BYTES];
+
+// Flag words first (4 per CTA, 16 bytes), then the fp32 partial slots.
+constexpr int64_t kNoallocFlagBytes = 64 * 1024;
+constexpr int64_t kNoallocMaxCtas = kNoallocFlagBytes / 16;
+
+struct NoallocDeviceState {
+    bool ready = false;
+    unsigned char* base = nullptr;  // device address of g_noalloc_scratch
+    uint32_t epoch = 0;
+};
+
+std::mutex g_noalloc_mutex;
+NoallocDeviceState g_noalloc[kMaxDevices];
+
+}  // namespace
+
+extern "C" tg_status_t tg_gemm_f16_noalloc(const void* A, const void* B, void* C, int64_t M,
+                                           int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                           int64_t ldc, int epilogue, void* stream) {
+    tg_status_t st = validate(A, B, C, M, N, K, lda, ldb, ldc, epilogue);
+    if (st != TG_OK || M == 0 || N == 0) return st;
+    if (M > 128) return TG_ERR_INVALID_VALUE;  // the split-K kernel covers M <= 128 only
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    st = current_device(&dev, &ds);
+    if (st != TG_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (K == 0) {  // C = epi(0): no scratch involved
+        tg_plan_t pf;
+        tg_plan_f16(M, N, K, ds->num_sms, &pf);
+        tg::tg_fill_zero_f16<<<static_cast<unsigned>(pf.grid), 256, 0, s>>>(
+            static_cast<__half*>(C), M, N, ldc);
+        return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_LAUNCH;
+    }
+
+    tg_plan_t pl;
+    std::memset(&pl, 0, sizeof(pl));
+    tg::skinny_plan(M, N, K, ds->num_sms, &pl);
+    if (pl.grid > kNoallocMaxCtas ||
+        kNoallocFlagBytes + pl.grid * tg::kSkSlotFloats * 4 > TG_NOALLOC_SCRATCH_BYTES)
+        return TG_ERR_INVALID_VALUE;  // would need more scratch than the array holds
+
+    tg::SkinnyParams prm;
+    {
+        std::lock_guard<std::mutex> lk(g_noalloc_mutex);
+        NoallocDeviceState& ns = g_noalloc[dev];
+        if (!ns.ready) {
+            // Once per device, with that device current: the array's device
+            // address, and the flag words cleared so no stale value can equal
+            // an epoch handed out below.
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+                cudaGetLastError();
+                return TG_ERR_LAUNCH;
+            }
+            if (cudaMemsetAsync(p, 0, kNoallocFlagBytes, s) != cudaSuccess) {
+                cudaGetLastError();
+                return TG_ERR_LAUNCH;
+            }
+            ns.base = static_cast<unsigned char*>(p);
+            ns.epoch = 0;
+            ns.ready = true;
+        }
+        if (++ns.epoch == 0) {
+            // 2^32 calls later: clear the flags again before reusing epochs
+            if (cudaMemsetAsync(ns.base, 0, kNoallocFlagBytes, s) != cudaSuccess) {
+                cudaGetLastError();
+                return TG_ERR_LAUNCH;
+            }
+            ns.epoch = 1;
+        }
+        prm.flags = reinterpret_cast<uint32_t*>(ns.base);
+        prm.ws = reinterpret_cast<float*>(ns.base + kNoallocFlagBytes);
+        prm.epoch = ns.epoch;
+    }
+
+    const int64_t Mp = pl.mma_n;
+    CUtensorMap tmA, tmB;
+    if (!encode_2d(&tmB, B, N, K, ldb * 2, 64, 64) ||
+        !encode_2d(&tmA, A, K, M, lda * 2, 64, static_cast<uint32_t>(Mp)))
+        return TG_ERR_LAUNCH;
+    prm.M = static_cast<int32_t>(M);
+    prm.N = static_cast<int32_t>(N);
+    prm.K = static_cast<int32_t>(K);
+    prm.Mp = static_cast<int32_t>(Mp);
+    prm.tiles_n = static_cast<int32_t>(pl.tiles_n);
+    prm.k_blocks = static_cast<int32_t>(pl.k_blocks);
+    prm.total_units = pl.tiles_n * pl.k_blocks;
+    prm.relu = epilogue == TG_EPI_RELU ? 1 : 0;
+    prm.inject = 0;
+    prm.timeout_ns = g_timeout_ns.load();
+    prm.C = static_cast<__half*>(C);
+    prm.ldc = ldc;
+
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = tg::kSkSmemBytes;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_skinny, tmB, tmA, prm) != cudaSuccess) {
+        cudaGetLastError();
+        return TG_ERR_LAUNCH;
+    }
+    return TG_OK;
+}
