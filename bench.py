@@ -312,8 +312,12 @@ def run_ours(args, w, rank, world, local_rank):
     kernel_ms = statistics.mean(per)
     achieved = flops / (kernel_ms / 1e3) / 1e12
     if plan.kernel == tg.TG_KERNEL_PERSISTENT:
-        kernel_key = f"persistent_bn{plan.bn}"
-        kname = f"tg_gemm_f16_persistent<{plan.bn},{plan.stages}>"
+        if plan.cluster == 2:
+            kernel_key = "pair256"
+            kname = f"tg_gemm_f16_pair<{plan.stages}> (CTA pairs, 256x256 tiles)"
+        else:
+            kernel_key = f"persistent_bn{plan.bn}"
+            kname = f"tg_gemm_f16_persistent<{plan.bn},{plan.stages}>"
         roof = {"bound": "tensor", "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
                 "frac": achieved / tf_peak,
                 "peak_source": f"{peak_src} dense bf16 burst (fp16 dense rate is the same)"}

@@ -120,6 +120,8 @@ typedef struct {
     int64_t ring_bytes;   /* of which the operand ring                          */
     int64_t split_k;      /* k-ranges per output tile (skinny: maximum)         */
     int64_t workspace_bytes; /* device scratch needed (skinny split-K)          */
+    int32_t cluster;      /* CTAs per cluster: 2 = tcgen05 CTA pair (256-row MMA) */
+    int32_t reserved;
 } tg_plan_t;
 
 /*

@@ -127,11 +127,15 @@ def test_plan_k_steps_and_grid_match_page_listing(tg):
 
 def test_plans(tg):
     p = tg.tg_plan_f16(8192, 28672, 4096, 152)
-    assert p.kernel == tg.TG_KERNEL_PERSISTENT
-    assert (p.bm, p.bn, p.bk) == (128, 256, 64)
-    assert p.num_tiles == 64 * 112 and p.grid == 152 and p.k_blocks == 64
+    assert p.kernel == tg.TG_KERNEL_PERSISTENT and p.cluster == 2
+    assert (p.bm, p.bn, p.bk, p.mma_m, p.mma_n) == (256, 256, 64, 256, 256)
+    assert p.num_tiles == 32 * 112 and p.grid == 152 and p.k_blocks == 64
     assert p.smem_bytes <= 232448  # 227 KB opt-in limit per CTA
-    assert p.ring_bytes == tg.tg_ring_bytes(128, 256, 64, p.stages, 2)
+    assert p.ring_bytes == 2 * tg.tg_ring_bytes(128, 128, 64, p.stages, 2)
+    one = tg.tg_plan_f16(2048, 2048, 4096, 152)  # 64 pair tiles < 76 pairs: one-CTA tiles
+    assert one.cluster == 1 and (one.bm, one.bn) == (128, 128) and one.grid == 152
+    pair = tg.tg_plan_f16(2048, 4864, 4096, 152)  # 8 x 19 = 152 pair tiles: two waves of pairs
+    assert pair.cluster == 2 and pair.num_tiles == 152 and pair.grid == 152
     s = tg.tg_plan_f16(64, 16384, 8192, 152)
     assert s.kernel == tg.TG_KERNEL_SKINNY
     assert (s.mma_m, s.mma_n) == (128, 64) and s.tiles_n == 128 and s.k_blocks == 128
@@ -155,10 +159,11 @@ def test_tile_order_is_a_bijection_and_grouped(tg):
         seen.add(tg.tg_tile_coord(p, t))
     assert len(seen) == p.num_tiles
     assert all(0 <= m < p.tiles_m and 0 <= n < p.tiles_n for m, n in seen)
-    # the first wave spans group_m row blocks and few column blocks
-    first = [tg.tg_tile_coord(p, t) for t in range(p.grid)]
+    # the first wave (one tile per CTA pair) spans group_m row blocks and few column blocks
+    wave = p.grid // p.cluster
+    first = [tg.tg_tile_coord(p, t) for t in range(wave)]
     assert len({m for m, _ in first}) == p.group_m
-    assert len({n for _, n in first}) <= -(-p.grid // p.group_m)
+    assert len({n for _, n in first}) <= -(-wave // p.group_m)
     with pytest.raises(tg.TgemmError):
         tg.tg_tile_coord(p, p.num_tiles)
 

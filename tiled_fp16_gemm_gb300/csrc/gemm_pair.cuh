@@ -1,0 +1,292 @@
+// Persistent FP16 GEMM on CTA pairs (tcgen05 cta_group::2) for sm_103a:
+//   C = epi(A · B), 256×256 output tiles per cluster of two CTAs.
+//
+// Each CTA of the pair (rank r = 0, 1) owns, in its own shared memory:
+//   A rows  [m0 + 128 r, m0 + 128 r + 128)  × 64 k   (K-major, one 16 KB box)
+//   B cols  [n0 + 128 r, n0 + 128 r + 128)  × 64 k   (MN-major, two 8 KB boxes)
+// at identical offsets.  The even CTA's single MMA thread issues
+// 256×256×16 tcgen05.mma over the pair; result rows 128 r .. 128 r + 127 land
+// in CTA r's TMEM (two 256-column fp32 accumulators per CTA).  Per SM this
+// halves the operand bytes loaded per MMA cycle compared with a one-CTA
+// 128×256 tile, so a 6-stage ring of 32 KB stages covers ~3000 MMA cycles.
+//
+// Synchronisation (all waits bounded):
+//   full[s]     in the even CTA only: its producer arms it with the bytes of
+//               both CTAs; both CTAs' TMA loads count their bytes on it.
+//   empty[s]    in each CTA: the MMA thread's commit is multicast to both.
+//   tmem_full   in each CTA: multicast commit at the end of a tile.
+//   tmem_empty  in the even CTA: all 8 epilogue warps of the pair arrive.
+// A cluster barrier after set-up (barriers initialised, TMEM allocated) and
+// before exit (no peer still reads or signals this CTA) brackets the work.
+//
+// Structure: producer warp / MMA warp / four epilogue warps as in the
+// one-CTA kernel (gemm_persistent.cuh), which follows the warp-specialised
+// TMA + mbarrier ring of "TileLang：比 Triton 低一层的 tile 语言", section
+// "它生成了什么", re-designed around TMEM and CTA pairs.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "gemm_persistent.cuh"
+#include "sm103_ptx.cuh"
+#include "tile_schedule.h"
+
+namespace tg {
+
+template <int STAGES>
+struct PairCfg {
+    static constexpr int BM = 256;  // rows of C per cluster tile (128 per CTA)
+    static constexpr int BN = 256;  // columns of C per cluster tile
+    static constexpr int BK = 64;
+    static constexpr int kThreads = 192;
+    static constexpr uint32_t kABytes = 128 * BK * 2;  // this CTA's A half
+    static constexpr uint32_t kBBytes = 128 * BK * 2;  // this CTA's B half
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    static constexpr uint32_t kCBuf = 32 * 64 * 2;
+    static constexpr uint32_t kCBytes = 4 * 2 * kCBuf;
+    static constexpr uint32_t kBarBytes = 256;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kSmemBytes =
+        1024 + STAGES * kStageBytes + kCBytes + kBarBytes;
+};
+
+template <int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    tg_gemm_f16_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmC, const PersistentParams p) {
+    using Cfg = PairCfg<STAGES>;
+    constexpr int BK = Cfg::BK;
+    constexpr uint32_t kABytes = Cfg::kABytes;
+    constexpr uint32_t kBBytes = Cfg::kBBytes;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const base_ptr = smem_raw + (base - raw);
+
+    const uint32_t sA = base;
+    const uint32_t sB = sA + STAGES * kABytes;
+    const uint32_t sC = sB + STAGES * kBBytes;
+    const uint32_t sBar = sC + Cfg::kCBytes;
+    const uint32_t bar_full = sBar;
+    const uint32_t bar_empty = sBar + 8 * STAGES;
+    const uint32_t bar_tfull = sBar + 16 * STAGES;
+    const uint32_t bar_tempty = bar_tfull + 16;
+    const uint32_t bar_drain = bar_tempty + 16;
+    const uint32_t slot_tmem = bar_drain + 8;
+    uint32_t* const tmem_slot_ptr = reinterpret_cast<uint32_t*>(base_ptr + (slot_tmem - base));
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(tmem_slot_ptr + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int cluster_id = static_cast<int>(blockIdx.x >> 1);
+    const int nclusters = static_cast<int>(gridDim.x >> 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar_tfull + 8 * a, 1);
+            mbar_init(bar_tempty + 8 * a, 8);
+        }
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(slot_tmem, Cfg::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // the peer's barriers exist and its TMEM is allocated
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot_ptr;
+
+    auto fail = [&](unsigned int role) {
+        atomicOr(&g_wait_timeout_flags, role);
+        *abort_flag = 1;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer (both CTAs)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_parity = 0;
+            bool ok = true;
+            uint64_t last_issue = 0;
+            for (int tile = cluster_id; ok && tile < p.num_tiles; tile += nclusters) {
+                const TileCoord tc = tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m);
+                const int ma = tc.m_blk * 256 + static_cast<int>(rank) * 128;
+                const int nb = tc.n_blk * 256 + static_cast<int>(rank) * 128;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.timeout_ns, abort_flag)) {
+                        fail(kRoleProducer);
+                        ok = false;
+                        break;
+                    }
+                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * Cfg::kStageBytes);
+                    const uint32_t fb = mapa_shared(bar_full + 8 * stage, 0);
+                    tma_load_2d_pair(sA + stage * kABytes, &tmA, fb, kb * BK, ma);
+                    tma_load_2d_pair(sB + stage * kBBytes, &tmB, fb, nb, kb * BK);
+                    tma_load_2d_pair(sB + stage * kBBytes + 8192, &tmB, fb, nb + 64, kb * BK);
+                    issued_mask |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (ok && leader) {
+                // Normal exit: every phase armed here completed (the MMA
+                // thread consumed it), so these waits return at once.
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued_mask & (1u << s))
+                        if (!mbar_wait(bar_full + 8 * s, (issued_parity >> s) & 1u, p.timeout_ns,
+                                       nullptr))
+                            atomicOr(&g_wait_timeout_flags, kRoleDrain);
+            } else if (!ok && issued_mask != 0) {
+                // Abort: completion of this CTA's last loads may be counted on
+                // a phase the pair never finishes, so give them a fixed,
+                // bounded grace period (far above a TMA round trip) to land.
+                last_issue = globaltimer_ns();
+                while (globaltimer_ns() - last_issue < 1000000ull) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (even CTA)
+        if (leader && lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(256, 256, /*a_mn=*/false, /*b_mn=*/true);
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int tile = cluster_id; ok && tile < p.num_tiles; tile += nclusters, ++it) {
+                const int acc = it & 1;
+                const uint32_t acc_phase = (it >> 1) & 1;
+                if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
+                    fail(kRoleMma);
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 256);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(bar_full + 8 * stage, phase, p.timeout_ns, abort_flag)) {
+                        fail(kRoleMma);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a0 = sA + stage * kABytes;
+                    const uint32_t b0 = sB + stage * kBBytes;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint64_t adesc = smem_desc_sw128(a0 + 32 * k, 16, 1024);
+                        const uint64_t bdesc = smem_desc_sw128(b0 + 2048 * k, 8192, 1024);
+                        mma_f16_ss_pair(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    mma_commit_pair_mc(bar_empty + 8 * stage, 0x3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if (!(p.inject == 1 && it == 0)) mma_commit_pair_mc(bar_tfull + 8 * acc, 0x3);
+            }
+            mma_commit_pair_mc(bar_drain, 0x1);
+            if (!mbar_wait(bar_drain, 0, p.timeout_ns, nullptr))
+                atomicOr(&g_wait_timeout_flags, kRoleDrain);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        const uint32_t cbuf = sC + static_cast<uint32_t>((warp - 2) * 2) * Cfg::kCBuf;
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+        int buf = 0;
+        int it = 0;
+        for (int tile = cluster_id; tile < p.num_tiles; tile += nclusters, ++it) {
+            const TileCoord tc = tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m);
+            const int row0 = tc.m_blk * 256 + static_cast<int>(rank) * 128 + 32 * q;
+            const int n0 = tc.n_blk * 256;
+            const int acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            int ok = 1;
+            if (lane == 0)
+                ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, p.timeout_ns, abort_flag) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) fail(kRoleEpilogue);
+                break;
+            }
+            tc_fence_after_sync();
+#pragma unroll 1
+            for (int j = 0; j < 4; ++j) {
+                uint32_t v0[32], v1[32];
+                const uint32_t taddr =
+                    tmem_base + lane_addr + static_cast<uint32_t>(acc * 256 + j * 64);
+                tmem_ld_x32(taddr, v0);
+                tmem_ld_x32(taddr + 32, v1);
+                if (j == 3) {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * acc, 0));
+                }
+                uint32_t h[32];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    float x0 = __uint_as_float(v0[2 * t]), x1 = __uint_as_float(v0[2 * t + 1]);
+                    float y0 = __uint_as_float(v1[2 * t]), y1 = __uint_as_float(v1[2 * t + 1]);
+                    if (p.relu) {
+                        x0 = relu_f32(x0);
+                        x1 = relu_f32(x1);
+                        y0 = relu_f32(y0);
+                        y1 = relu_f32(y1);
+                    }
+                    h[t] = pack_half2(x0, x1);
+                    h[16 + t] = pack_half2(y0, y1);
+                }
+                if (lane == 0) bulk_wait_group_read<1>();
+                __syncwarp();
+                const uint32_t cb = cbuf + static_cast<uint32_t>(buf) * Cfg::kCBuf;
+                const uint32_t row_addr = cb + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(row_addr + ((static_cast<uint32_t>(c) ^ (lane & 7u)) << 4),
+                                 h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (row0 < p.M && n0 + 64 * j < p.N) tma_store_2d(&tmC, cb, n0 + 64 * j, row0);
+                    bulk_commit_group();
+                }
+                buf ^= 1;
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // the peer no longer reads this CTA's smem or signals its barriers
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+}  // namespace tg

@@ -379,6 +379,7 @@ inline void skinny_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_pla
     pl->split_k = shortest > 0 ? (pl->k_blocks + shortest - 1) / shortest + 1 : pl->k_blocks;
     if (pl->split_k > G) pl->split_k = G;
     pl->workspace_bytes = G * kSkSlotFloats * 4 + 4 * G * 4;
+    pl->cluster = 1;
 }
 
 inline cudaError_t skinny_set_attributes() {

@@ -14,6 +14,7 @@
 
 #include "tgemm.h"
 #include "gemm_persistent.cuh"
+#include "gemm_pair.cuh"
 #include "gemm_skinny.cuh"
 #include "tile_schedule.h"
 
@@ -54,6 +55,34 @@ void plan_persistent(int64_t M, int64_t N, int64_t K, int32_t num_sms, int bn, i
     p->ring_bytes = tg_ring_bytes(128, bn, 64, stages, 2);
     p->split_k = 1;
     p->workspace_bytes = 0;
+    p->cluster = 1;
+}
+
+constexpr int kPairStages = 6;
+constexpr int kPairGroupM = 8;  // 8 blocks of 256 rows = 2048 rows per raster group
+
+// 256×256 tiles on CTA pairs; grid = two CTAs per tile, at most num_sms.
+void plan_pair(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* p) {
+    p->kernel = TG_KERNEL_PERSISTENT;
+    p->bm = 256;
+    p->bn = 256;
+    p->bk = 64;
+    p->stages = kPairStages;
+    p->mma_m = 256;
+    p->mma_n = 256;
+    p->tiles_m = ceil_div(M, 256);
+    p->tiles_n = ceil_div(N, 256);
+    p->k_blocks = ceil_div(K, 64);
+    p->num_tiles = p->tiles_m * p->tiles_n;
+    const int64_t pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
+    p->grid = 2 * (p->num_tiles < pairs ? p->num_tiles : pairs);
+    p->threads = 192;
+    p->group_m = static_cast<int32_t>(p->tiles_m < kPairGroupM ? p->tiles_m : kPairGroupM);
+    p->smem_bytes = tg::PairCfg<kPairStages>::kSmemBytes;
+    p->ring_bytes = 2 * tg_ring_bytes(128, 128, 64, kPairStages, 2);  // both CTAs
+    p->split_k = 1;
+    p->workspace_bytes = 0;
+    p->cluster = 2;
 }
 
 // ------------------------------------------------------------------ device state
@@ -63,6 +92,7 @@ struct DeviceState {
     bool supported = false;
     int num_sms = 0;
     bool attrs_set = false;
+    int max_pairs = 0;  // CTA pairs of the pair kernel that fit on the device at once
 };
 
 std::mutex g_dev_mutex;
@@ -114,10 +144,34 @@ tg_status_t current_device(int* dev, DeviceState** st) {
             cudaFuncSetAttribute(tg::tg_gemm_f16_persistent<kMidBN, kMidStages>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C2::kSmemBytes) != cudaSuccess ||
-            tg::skinny_set_attributes() != cudaSuccess) {
+            tg::skinny_set_attributes() != cudaSuccess ||
+            cudaFuncSetAttribute(tg::tg_gemm_f16_pair<kPairStages>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tg::PairCfg<kPairStages>::kSmemBytes) != cudaSuccess) {
             cudaGetLastError();
             return TG_ERR_LAUNCH;
         }
+        // How many CTA pairs can be resident together (clusters must sit
+        // inside one GPC, so this can be below num_sms / 2).
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3(static_cast<unsigned>(2 * (s.num_sms / 2)));
+        cfg.blockDim = dim3(tg::PairCfg<kPairStages>::kThreads);
+        cfg.dynamicSmemBytes = tg::PairCfg<kPairStages>::kSmemBytes;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, tg::tg_gemm_f16_pair<kPairStages>, &cfg) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            clusters = 0;
+        }
+        s.max_pairs = clusters;
         s.attrs_set = true;
     }
     *dev = d;
@@ -177,14 +231,62 @@ tg_status_t launch_persistent(const void* A, const void* B, void* C, const tg_pl
     return TG_OK;
 }
 
-// TGEMM_FORCE_CFG = persistent256 | persistent128 | skinny overrides the
-// planner's kernel choice (used by tests and tile sweeps); ignored where the
-// forced kernel does not apply (skinny needs M <= 128; K == 0 always fills).
+// The pair kernel: clusters of two CTAs, at most as many pairs as the device
+// holds at once (the launch is persistent, so no pair waits for another).
+tg_status_t launch_pair(const void* A, const void* B, void* C, const tg_plan_t& pl, int64_t M,
+                        int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int epilogue,
+                        cudaStream_t stream, int max_pairs) {
+    CUtensorMap tmA, tmB, tmC;
+    if (!encode_2d(&tmA, A, K, M, lda * 2, 64, 128) || !encode_2d(&tmB, B, N, K, ldb * 2, 64, 64) ||
+        !encode_2d(&tmC, C, N, M, ldc * 2, 64, 32))
+        return TG_ERR_LAUNCH;
+    tg::PersistentParams prm;
+    prm.M = static_cast<int32_t>(M);
+    prm.N = static_cast<int32_t>(N);
+    prm.K = static_cast<int32_t>(K);
+    prm.tiles_m = static_cast<int32_t>(pl.tiles_m);
+    prm.tiles_n = static_cast<int32_t>(pl.tiles_n);
+    prm.num_tiles = static_cast<int32_t>(pl.num_tiles);
+    prm.k_blocks = static_cast<int32_t>(pl.k_blocks);
+    prm.group_m = pl.group_m;
+    prm.relu = epilogue == TG_EPI_RELU ? 1 : 0;
+    prm.inject = g_inject.exchange(0);
+    prm.timeout_ns = g_timeout_ns.load();
+
+    int64_t pairs = pl.grid / 2;
+    if (pairs > max_pairs) pairs = max_pairs;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+    cfg.blockDim = dim3(tg::PairCfg<kPairStages>::kThreads);
+    cfg.dynamicSmemBytes = tg::PairCfg<kPairStages>::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_pair<kPairStages>, tmA, tmB, tmC, prm);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return TG_ERR_LAUNCH;
+    }
+    return TG_OK;
+}
+
+// TGEMM_FORCE_CFG = pair256 | persistent256 | persistent128 | skinny
+// overrides the planner's kernel choice (used by tests and tile sweeps);
+// ignored where the forced kernel does not apply (skinny needs M <= 128;
+// K == 0 always fills).
 void apply_forced_config(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* pl) {
     const char* f = std::getenv("TGEMM_FORCE_CFG");
     if (f == nullptr || *f == 0 || pl->kernel == TG_KERNEL_NONE || pl->kernel == TG_KERNEL_FILL)
         return;
-    if (std::strcmp(f, "persistent256") == 0)
+    if (std::strcmp(f, "pair256") == 0)
+        plan_pair(M, N, K, num_sms, pl);
+    else if (std::strcmp(f, "persistent256") == 0)
         plan_persistent(M, N, K, num_sms, kBigBN, kBigStages,
                         tg::PersistentCfg<kBigBN, kBigStages>::kSmemBytes, pl);
     else if (std::strcmp(f, "persistent128") == 0)
@@ -241,6 +343,12 @@ tg_status_t tg_plan_f16(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_pla
     }
     if (tg::skinny_applies(M, N, K)) {
         tg::skinny_plan(M, N, K, num_sms, plan);
+        return TG_OK;
+    }
+    // At least one full wave of 256×256 tiles on CTA pairs: the pair kernel.
+    const int64_t tiles_pair = ceil_div(M, 256) * ceil_div(N, 256);
+    if (num_sms >= 2 && tiles_pair >= num_sms / 2) {
+        plan_pair(M, N, K, num_sms, plan);
         return TG_OK;
     }
     const int64_t tiles256 = ceil_div(M, 128) * ceil_div(N, kBigBN);
@@ -314,6 +422,15 @@ tg_status_t tg_gemm_f16(const void* A, const void* B, void* C, int64_t M, int64_
             return TG_OK;
         }
         case TG_KERNEL_PERSISTENT:
+            if (pl.cluster == 2) {
+                if (ds->max_pairs < 1) {  // cannot place a pair: one-CTA tiles instead
+                    plan_persistent(M, N, K, ds->num_sms, kBigBN, kBigStages,
+                                    tg::PersistentCfg<kBigBN, kBigStages>::kSmemBytes, &pl);
+                } else {
+                    return launch_pair(A, B, C, pl, M, N, K, lda, ldb, ldc, epilogue, s,
+                                       ds->max_pairs);
+                }
+            }
             if (pl.bn == kBigBN)
                 return launch_persistent<kBigBN, kBigStages>(A, B, C, pl, M, N, K, lda, ldb, ldc,
                                                             epilogue, s);
