@@ -215,6 +215,7 @@ __global__ void __launch_bounds__(192, 1)
         const int q = warp & 3;
         const uint32_t cbuf = sC + static_cast<uint32_t>((warp - 2) * 2) * Cfg::kCBuf;
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+        const uint64_t c_policy = policy_evict_first();  // C is written once, never reread
         int buf = 0;
         int it = 0;
         for (int tile = cluster_id; tile < p.num_tiles; tile += nclusters, ++it) {
@@ -269,7 +270,8 @@ __global__ void __launch_bounds__(192, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    if (row0 < p.M && n0 + 64 * j < p.N) tma_store_2d(&tmC, cb, n0 + 64 * j, row0);
+                    if (row0 < p.M && n0 + 64 * j < p.N)
+                        tma_store_2d_hint(&tmC, cb, n0 + 64 * j, row0, c_policy);
                     bulk_commit_group();
                 }
                 buf ^= 1;

@@ -123,6 +123,16 @@ __device__ __forceinline__ void tma_store_2d(const void* desc, uint32_t src, int
         : "memory");
 }
 
+// Same, with an L2 eviction-priority hint for the written lines.
+__device__ __forceinline__ void tma_store_2d_hint(const void* desc, uint32_t src, int32_t x,
+                                                  int32_t y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+        " [%0, {%1, %2}], [%3], %4;" ::"l"(reinterpret_cast<uint64_t>(desc)),
+        "r"(x), "r"(y), "r"(src), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
