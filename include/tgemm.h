@@ -73,8 +73,14 @@ typedef enum {
  * records the fact on the device; tg_sync_status reports it.
  * The current device must be compute capability 10.3 (sm_103).
  * Kernel choice follows tg_plan_f16; the environment variable
- * TGEMM_FORCE_CFG = persistent256 | persistent128 | skinny overrides it where
- * the forced kernel applies (for tests and tile sweeps).
+ * TGEMM_FORCE_CFG = pair256 | persistent256 | persistent128 | skinny
+ * overrides it where the forced kernel applies, and TGEMM_GROUP_M sets the
+ * raster group height (both for tests and tile sweeps).
+ * CUDA graphs: once one call has run on a stream outside capture (the first
+ * call per stream allocates that stream's split-K workspace), calls on that
+ * stream can be captured; a graph holding an M <= 128 call uses the capturing
+ * stream's workspace, so it must not run concurrently with other libtgemm
+ * work on that stream.
  */
 tg_status_t tg_gemm_f16(const void* A, const void* B, void* C,
                         int64_t M, int64_t N, int64_t K,

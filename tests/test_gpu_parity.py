@@ -220,6 +220,33 @@ def test_streams_repeat_and_determinism(tg):
               what=f"streams {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(2048, 9728, 1024), (64, 8192, 4096), (300, 496, 200)],
+                         ids=["pair", "skinny", "small"])
+def test_cuda_graph_capture_and_replay(tg, M, N, K):
+    """tg_gemm_f16 captured in a CUDA graph (after one call on the stream
+    outside capture) replays to the same bits as the eager call."""
+    A, B = W.draw_inputs(M, N, K, ("normal", 0, 1), ("normal", 0, 1 / np.sqrt(K)), 61 + M)
+    a = torch.from_numpy(A).cuda()
+    b = torch.from_numpy(B).cuda()
+    s = torch.cuda.Stream()
+    eager = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    graphed = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+    with torch.cuda.stream(s):
+        tg.gemm(a, b, relu=True, out=eager, stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        tg.gemm(a, b, relu=True, out=graphed, stream=torch.cuda.current_stream())
+    for _ in range(3):
+        graphed.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(graphed.view(torch.int16), eager.view(torch.int16))
+    assert tg.tg_sync_status(s.cuda_stream) == tg.TG_OK
+    check(eager.cpu().numpy(), oracle.gemm(A, B, M, N, K, relu=True), K, relu=True,
+          what="graph")
+
+
 def test_torch_matmul_sanity(tg):
     """Secondary check (never the product path): agrees with torch's fp16 matmul."""
     M, N, K = 1024, 1536, 768

@@ -16,7 +16,9 @@
 //   FULL     the whole k range of a tile: epilogue writes C directly;
 //   PARTIAL  starts inside a tile (only a CTA's first segment can): its fp32
 //            partial goes to workspace slot c; each epilogue warp then sets
-//            flag[4c + warp quarter] = epoch for the 32 columns it wrote;
+//            flag[4c + warp quarter] = 1 for the 32 columns it wrote (the
+//            owner warp that reads it sets it back to 0, so flags are zero
+//            between launches);
 //   OWNER    starts at k = 0 but the range ends inside the tile (only a CTA's
 //            last segment can): each epilogue warp waits for its quarter's
 //            flags of CTAs c+1 .. c_last holding the rest of the tile, then
@@ -49,11 +51,20 @@
 
 namespace tg {
 
-constexpr int kSkStages = 6;
 constexpr uint32_t kSkBBytes = 128 * 64 * 2;  // B^T tile: two 64×64 boxes
-constexpr uint32_t kSkASlot = 128 * 64 * 2;   // A tile, room for Mp ≤ 128 rows
-constexpr uint32_t kSkStageBytes = kSkBBytes + kSkASlot;
-constexpr uint32_t kSkSmemBytes = 1024 + kSkStages * kSkStageBytes + 256;
+
+// Two ring shapes, both about 220 KB of shared memory: A slots sized for
+// Mp ≤ 64 (24 KB stages, 9 deep: 144 KB of B in flight per SM) or for
+// Mp ≤ 128 (32 KB stages, 6 deep).
+template <int STAGES, int MP_MAX>
+struct SkinnyCfg {
+    static constexpr int kStages = STAGES;
+    static constexpr uint32_t kASlot = MP_MAX * 64 * 2;
+    static constexpr uint32_t kStageBytes = kSkBBytes + kASlot;
+    static constexpr uint32_t kSmemBytes = 1024 + STAGES * kStageBytes + 256;
+};
+using SkinnyNarrow = SkinnyCfg<9, 64>;
+using SkinnyWide = SkinnyCfg<6, 128>;
 constexpr uint32_t kSkTmemCols = 256;        // two accumulators of up to 128 columns
 constexpr int64_t kSkSlotFloats = 128 * 128;  // one partial: Mp ≤ 128 rows × 128 n
 constexpr int kSkMinUnitsPerCta = 8;
@@ -93,10 +104,13 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+template <int STAGES, int MP_MAX>
 __global__ void __launch_bounds__(192, 1)
     tg_gemm_f16_skinny(const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmA, const SkinnyParams p) {
     constexpr int BK = 64;
+    constexpr int kSkStages = STAGES;
+    constexpr uint32_t kSkASlot = SkinnyCfg<STAGES, MP_MAX>::kASlot;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -329,7 +343,13 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+                if (lane == 0) {
+                    mbar_arrive(bar_tempty + 8 * acc);
+                    // Each flag has this warp as its only reader: clear the
+                    // ones consumed, so every launch leaves the flags at zero
+                    // (a replayed graph finds them clean).
+                    for (int64_t cc = c_first; cc <= c_last; ++cc) p.flags[4 * cc + q] = 0u;
+                }
             }
             u = seg_end;
         }
@@ -354,11 +374,12 @@ inline bool skinny_applies(int64_t M, int64_t N, int64_t K) {
 
 inline void skinny_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* pl) {
     const int64_t Mp = (M + 15) / 16 * 16;
+    const bool narrow = Mp <= 64;
     pl->kernel = TG_KERNEL_SKINNY;
     pl->bm = static_cast<int32_t>(Mp);
     pl->bn = 128;
     pl->bk = 64;
-    pl->stages = kSkStages;
+    pl->stages = narrow ? SkinnyNarrow::kStages : SkinnyWide::kStages;
     pl->mma_m = 128;
     pl->mma_n = static_cast<int32_t>(Mp);
     pl->tiles_m = 1;
@@ -372,8 +393,9 @@ inline void skinny_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_pla
     pl->grid = G;
     pl->threads = 192;
     pl->group_m = 1;
-    pl->smem_bytes = kSkSmemBytes;
-    pl->ring_bytes = static_cast<int64_t>(kSkStages) * kSkStageBytes;
+    pl->smem_bytes = narrow ? SkinnyNarrow::kSmemBytes : SkinnyWide::kSmemBytes;
+    pl->ring_bytes = narrow ? int64_t{SkinnyNarrow::kStages} * SkinnyNarrow::kStageBytes
+                            : int64_t{SkinnyWide::kStages} * SkinnyWide::kStageBytes;
     // most CTAs touching one tile: its k range over the shortest unit range, plus one
     const int64_t shortest = U / G;
     pl->split_k = shortest > 0 ? (pl->k_blocks + shortest - 1) / shortest + 1 : pl->k_blocks;
@@ -383,15 +405,41 @@ inline void skinny_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_pla
 }
 
 inline cudaError_t skinny_set_attributes() {
-    return cudaFuncSetAttribute(tg_gemm_f16_skinny, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kSkSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(tg_gemm_f16_skinny<9, 64>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SkinnyNarrow::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(tg_gemm_f16_skinny<6, 128>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                SkinnyWide::kSmemBytes);
+}
+
+// Cooperative launch of the instantiation whose A slots fit prm.Mp.
+inline cudaError_t skinny_launch_kernel(const CUtensorMap& tmB, const CUtensorMap& tmA,
+                                        const SkinnyParams& prm, int64_t grid,
+                                        cudaStream_t stream) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(192);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (prm.Mp <= 64) {
+        cfg.dynamicSmemBytes = SkinnyNarrow::kSmemBytes;
+        return cudaLaunchKernelEx(&cfg, tg_gemm_f16_skinny<9, 64>, tmB, tmA, prm);
+    }
+    cfg.dynamicSmemBytes = SkinnyWide::kSmemBytes;
+    return cudaLaunchKernelEx(&cfg, tg_gemm_f16_skinny<6, 128>, tmB, tmA, prm);
 }
 
 struct SkinnyWorkspace {
     float* partials = nullptr;
     uint32_t* flags = nullptr;
     int64_t slots = 0;
-    uint32_t epoch = 0;
 };
 
 inline std::mutex& skinny_ws_mutex() {
@@ -404,13 +452,23 @@ inline std::map<std::pair<int, cudaStream_t>, SkinnyWorkspace>& skinny_ws_map() 
     return m;
 }
 
+// After a launch gave up on a wait, flags it raised may never have been
+// consumed: reset every workspace's flags on this device (the device is idle).
+inline void skinny_reset_flags(int dev) {
+    std::lock_guard<std::mutex> lk(skinny_ws_mutex());
+    for (auto& kv : skinny_ws_map())
+        if (kv.first.first == dev && kv.second.flags != nullptr)
+            cudaMemset(kv.second.flags, 0, 4 * kv.second.slots * sizeof(uint32_t));
+}
+
 using EncodeFn = bool (*)(CUtensorMap*, const void*, uint64_t, uint64_t, uint64_t, uint32_t,
                           uint32_t);
 
 inline tg_status_t skinny_launch(const void* A, const void* B, void* C, const tg_plan_t& pl,
                                  int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                                  int64_t ldc, int epilogue, cudaStream_t stream, int dev,
-                                 uint64_t timeout_ns, int32_t inject, EncodeFn encode) {
+                                 int64_t max_ctas, uint64_t timeout_ns, int32_t inject,
+                                 EncodeFn encode) {
     const int64_t Mp = pl.mma_n;
     CUtensorMap tmA, tmB;
     if (!encode(&tmB, B, N, K, ldb * 2, 64, 64) ||
@@ -422,7 +480,8 @@ inline tg_status_t skinny_launch(const void* A, const void* B, void* C, const tg
         std::lock_guard<std::mutex> lk(skinny_ws_mutex());
         SkinnyWorkspace& ws = skinny_ws_map()[std::make_pair(dev, stream)];
         if (ws.slots < pl.grid) {
-            // grow: ordered after all earlier work on this stream
+            // First use on this stream: room for the largest grid (one CTA
+            // per SM), so later calls, graph captures included, never grow it.
             if (ws.partials) {
                 cudaStreamSynchronize(stream);
                 cudaFree(ws.partials);
@@ -431,7 +490,7 @@ inline tg_status_t skinny_launch(const void* A, const void* B, void* C, const tg
                 ws.flags = nullptr;
                 ws.slots = 0;
             }
-            const int64_t slots = pl.grid;
+            const int64_t slots = pl.grid > max_ctas ? pl.grid : max_ctas;
             if (cudaMalloc(&ws.partials, slots * kSkSlotFloats * sizeof(float)) != cudaSuccess ||
                 cudaMalloc(&ws.flags, 4 * slots * sizeof(uint32_t)) != cudaSuccess) {
                 cudaGetLastError();
@@ -445,12 +504,10 @@ inline tg_status_t skinny_launch(const void* A, const void* B, void* C, const tg
                 return TG_ERR_LAUNCH;
             }
             ws.slots = slots;
-            ws.epoch = 0;
         }
-        if (++ws.epoch == 0) ws.epoch = 1;
         prm.ws = ws.partials;
         prm.flags = ws.flags;
-        prm.epoch = ws.epoch;
+        prm.epoch = 1;  // flags are zero between launches (owners clear them)
     }
     prm.M = static_cast<int32_t>(M);
     prm.N = static_cast<int32_t>(N);
@@ -465,19 +522,7 @@ inline tg_status_t skinny_launch(const void* A, const void* B, void* C, const tg
     prm.C = static_cast<__half*>(C);
     prm.ldc = ldc;
 
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
-    cfg.blockDim = dim3(192);
-    cfg.dynamicSmemBytes = kSkSmemBytes;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, tg_gemm_f16_skinny, tmB, tmA, prm);
-    if (e != cudaSuccess) {
+    if (skinny_launch_kernel(tmB, tmA, prm, pl.grid, stream) != cudaSuccess) {
         cudaGetLastError();
         return TG_ERR_LAUNCH;
     }

@@ -27,6 +27,8 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
 std::atomic<int32_t> g_inject{0};
 
+void noalloc_reset_flags(int dev);  // defined with the no-allocation entry point below
+
 // ------------------------------------------------------------------ planning
 
 constexpr int kBigBN = 256, kBigStages = 4;
@@ -452,7 +454,7 @@ tg_status_t tg_gemm_f16(const void* A, const void* B, void* C, int64_t M, int64_
             const uint64_t timeout = g_timeout_ns.load();
             const int32_t inject = g_inject.exchange(0);
             return tg::skinny_launch(A, B, C, pl, M, N, K, lda, ldb, ldc, epilogue, s, dev,
-                                     timeout, inject, encode_2d);
+                                     ds->num_sms, timeout, inject, encode_2d);
         }
         default:
             return TG_ERR_INVALID_VALUE;
@@ -474,8 +476,14 @@ tg_status_t tg_sync_status(void* stream) {
         return TG_ERR_LAUNCH;
     }
     if (flags != 0) {
+        // A kernel gave up early: let every queued kernel finish, then clear
+        // the split-K flags it may have left raised before anything reuses them.
+        cudaDeviceSynchronize();
         const unsigned int zero = 0;
         cudaMemcpyToSymbol(tg::g_wait_timeout_flags, &zero, sizeof(zero));
+        tg::skinny_reset_flags(dev);
+        noalloc_reset_flags(dev);
+        cudaGetLastError();
         return TG_ERR_TIMEOUT;
     }
     return TG_OK;
@@ -507,11 +515,17 @@ constexpr int64_t kNoallocMaxCtas = kNoallocFlagBytes / 16;
 struct NoallocDeviceState {
     bool ready = false;
     unsigned char* base = nullptr;  // device address of g_noalloc_scratch
-    uint32_t epoch = 0;
 };
 
 std::mutex g_noalloc_mutex;
 NoallocDeviceState g_noalloc[kMaxDevices];
+
+// After a timed-out launch: clear the flag words (the device is idle).
+void noalloc_reset_flags(int dev) {
+    std::lock_guard<std::mutex> lk(g_noalloc_mutex);
+    if (dev >= 0 && dev < kMaxDevices && g_noalloc[dev].ready)
+        cudaMemset(g_noalloc[dev].base, 0, kNoallocFlagBytes);
+}
 
 }  // namespace
 
@@ -548,8 +562,8 @@ extern "C" tg_status_t tg_gemm_f16_noalloc(const void* A, const void* B, void* C
         NoallocDeviceState& ns = g_noalloc[dev];
         if (!ns.ready) {
             // Once per device, with that device current: the array's device
-            // address, and the flag words cleared so no stale value can equal
-            // an epoch handed out below.
+            // address, and the flag words cleared (each launch then leaves
+            // them at zero: the kernel's owners clear what they consume).
             void* p = nullptr;
             if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
                 cudaGetLastError();
@@ -560,20 +574,11 @@ extern "C" tg_status_t tg_gemm_f16_noalloc(const void* A, const void* B, void* C
                 return TG_ERR_LAUNCH;
             }
             ns.base = static_cast<unsigned char*>(p);
-            ns.epoch = 0;
             ns.ready = true;
-        }
-        if (++ns.epoch == 0) {
-            // 2^32 calls later: clear the flags again before reusing epochs
-            if (cudaMemsetAsync(ns.base, 0, kNoallocFlagBytes, s) != cudaSuccess) {
-                cudaGetLastError();
-                return TG_ERR_LAUNCH;
-            }
-            ns.epoch = 1;
         }
         prm.flags = reinterpret_cast<uint32_t*>(ns.base);
         prm.ws = reinterpret_cast<float*>(ns.base + kNoallocFlagBytes);
-        prm.epoch = ns.epoch;
+        prm.epoch = 1;
     }
 
     const int64_t Mp = pl.mma_n;
@@ -594,18 +599,7 @@ extern "C" tg_status_t tg_gemm_f16_noalloc(const void* A, const void* B, void* C
     prm.C = static_cast<__half*>(C);
     prm.ldc = ldc;
 
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
-    cfg.blockDim = dim3(192);
-    cfg.dynamicSmemBytes = tg::kSkSmemBytes;
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_skinny, tmB, tmA, prm) != cudaSuccess) {
+    if (tg::skinny_launch_kernel(tmB, tmA, prm, pl.grid, s) != cudaSuccess) {
         cudaGetLastError();
         return TG_ERR_LAUNCH;
     }
