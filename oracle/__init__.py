@@ -77,6 +77,12 @@ class Oracle:
         lib.oracle_f16_from_f64_array.argtypes = [f64p, u16p, i64]
         lib.oracle_f64_from_f16_array.argtypes = [u16p, f64p, i64]
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_gemm_bf16.argtypes = lib.oracle_gemm_f16.argtypes
+        lib.oracle_gemm_bf16.restype = ctypes.c_int
+        lib.oracle_gemm_bf16_at.argtypes = lib.oracle_gemm_f16_at.argtypes
+        lib.oracle_gemm_bf16_at.restype = ctypes.c_int
+        lib.oracle_bf16_from_f64_array.argtypes = [f64p, u16p, i64]
+        lib.oracle_f64_from_bf16_array.argtypes = [u16p, f64p, i64]
         self.lib = lib
         self.path = path
 
@@ -99,11 +105,29 @@ class Oracle:
                                            _ptr(out, ctypes.c_double), h.size)
         return out
 
-    def gemm(self, A: np.ndarray, B: np.ndarray, M: int, N: int, K: int,
-             relu: bool = False, want_ref: bool = False):
-        """Full product of A (M×lda fp16, lda ≥ K) and B (K×ldb fp16, ldb ≥ N).
+    def bf16_from_f64(self, x) -> np.ndarray:
+        """Round float64 values to bfloat16 bits (RNE), element-wise."""
+        x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+        out = np.empty(x.shape, dtype=np.uint16)
+        self.lib.oracle_bf16_from_f64_array(_ptr(x, ctypes.c_double),
+                                            _ptr(out, ctypes.c_uint16), x.size)
+        return out
 
-        Returns C as float16 (M×N) and, if ``want_ref``, the fp64 values
+    def f64_from_bf16(self, h) -> np.ndarray:
+        """Decode bfloat16 bits (uint16) to float64, element-wise."""
+        h = np.ascontiguousarray(np.asarray(h, dtype=np.uint16))
+        out = np.empty(h.shape, dtype=np.float64)
+        self.lib.oracle_f64_from_bf16_array(_ptr(h, ctypes.c_uint16),
+                                            _ptr(out, ctypes.c_double), h.size)
+        return out
+
+    def gemm(self, A: np.ndarray, B: np.ndarray, M: int, N: int, K: int,
+             relu: bool = False, want_ref: bool = False, dtype: str = "f16"):
+        """Full product of A (M×lda, lda ≥ K) and B (K×ldb, ldb ≥ N).
+
+        dtype "f16": A and B are float16 (or their bits); returns C as float16.
+        dtype "bf16": A and B are bfloat16 bit patterns (uint16); returns C as
+        bfloat16 bits (uint16).  With ``want_ref`` also returns the fp64 values
         epi(sum) before rounding (M×N).
         """
         A = _as_u16(A)
@@ -112,18 +136,21 @@ class Oracle:
         ldb = B.shape[1] if B.ndim == 2 else N
         C = np.empty((M, N), dtype=np.uint16)
         ref = np.empty((M, N), dtype=np.float64) if want_ref else None
-        rc = self.lib.oracle_gemm_f16(
-            _ptr(A, ctypes.c_uint16), _ptr(B, ctypes.c_uint16), _ptr(C, ctypes.c_uint16),
-            _ptr(ref, ctypes.c_double), M, N, K, lda, ldb, N, int(bool(relu)))
+        fn = self.lib.oracle_gemm_bf16 if dtype == "bf16" else self.lib.oracle_gemm_f16
+        rc = fn(_ptr(A, ctypes.c_uint16), _ptr(B, ctypes.c_uint16), _ptr(C, ctypes.c_uint16),
+                _ptr(ref, ctypes.c_double), M, N, K, lda, ldb, N, int(bool(relu)))
         if rc != 0:
-            raise ValueError("oracle_gemm_f16 rejected its arguments")
-        C = C.view(np.float16)
+            raise ValueError("oracle gemm rejected its arguments")
+        if dtype != "bf16":
+            C = C.view(np.float16)
         return (C, ref) if want_ref else C
 
-    def gemm_at(self, A: np.ndarray, B: np.ndarray, K: int, rows, cols, relu: bool = False):
+    def gemm_at(self, A: np.ndarray, B: np.ndarray, K: int, rows, cols, relu: bool = False,
+                dtype: str = "f16"):
         """Selected elements (rows[t], cols[t]) of the same product.
 
-        Returns (float16 values, float64 values before rounding).
+        Returns (rounded values: float16, or bfloat16 bits for dtype "bf16";
+        float64 values before rounding).
         """
         A = _as_u16(A)
         B = _as_u16(B)
@@ -132,13 +159,13 @@ class Oracle:
         n = rows.size
         out16 = np.empty(n, dtype=np.uint16)
         out64 = np.empty(n, dtype=np.float64)
-        rc = self.lib.oracle_gemm_f16_at(
-            _ptr(A, ctypes.c_uint16), _ptr(B, ctypes.c_uint16), K, A.shape[1], B.shape[1],
-            int(bool(relu)), _ptr(rows, ctypes.c_int64), _ptr(cols, ctypes.c_int64), n,
-            _ptr(out16, ctypes.c_uint16), _ptr(out64, ctypes.c_double))
+        fn = self.lib.oracle_gemm_bf16_at if dtype == "bf16" else self.lib.oracle_gemm_f16_at
+        rc = fn(_ptr(A, ctypes.c_uint16), _ptr(B, ctypes.c_uint16), K, A.shape[1], B.shape[1],
+                int(bool(relu)), _ptr(rows, ctypes.c_int64), _ptr(cols, ctypes.c_int64), n,
+                _ptr(out16, ctypes.c_uint16), _ptr(out64, ctypes.c_double))
         if rc != 0:
-            raise ValueError("oracle_gemm_f16_at rejected its arguments")
-        return out16.view(np.float16), out64
+            raise ValueError("oracle gemm_at rejected its arguments")
+        return (out16 if dtype == "bf16" else out16.view(np.float16)), out64
 
 
 def default() -> Oracle:
@@ -160,12 +187,31 @@ def f64_from_f16(h) -> np.ndarray:
     return default().f64_from_f16(h)
 
 
-def gemm(A, B, M, N, K, relu=False, want_ref=False):
-    return default().gemm(A, B, M, N, K, relu, want_ref)
+def bf16_from_f64(x) -> np.ndarray:
+    return default().bf16_from_f64(x)
 
 
-def gemm_at(A, B, K, rows, cols, relu=False):
-    return default().gemm_at(A, B, K, rows, cols, relu)
+def f64_from_bf16(h) -> np.ndarray:
+    return default().f64_from_bf16(h)
+
+
+def gemm(A, B, M, N, K, relu=False, want_ref=False, dtype="f16"):
+    return default().gemm(A, B, M, N, K, relu, want_ref, dtype)
+
+
+def gemm_at(A, B, K, rows, cols, relu=False, dtype="f16"):
+    return default().gemm_at(A, B, K, rows, cols, relu, dtype)
+
+
+def ulp_bf16(x) -> np.ndarray:
+    """Spacing of bfloat16 numbers at |x|: 2^(floor(log2|x|) - 7) for normal
+    magnitudes, 2^-133 below the smallest normal (and at zero)."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    out = np.full(a.shape, 2.0 ** -133)
+    nz = a >= 2.0 ** -126
+    e = np.floor(np.log2(np.where(nz, a, 1.0)))
+    out[nz] = np.exp2(e[nz] - 7.0)
+    return out
 
 
 def ulp16(x) -> np.ndarray:

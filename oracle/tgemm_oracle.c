@@ -191,3 +191,126 @@ int oracle_gemm_f16_at(const uint16_t* A, const uint16_t* B, int64_t K, int64_t 
     }
     return 0;
 }
+
+/* ========================================================================
+ * bfloat16 variant.  The pages define the GEMM for fp16 storage only; the
+ * bf16 variant applies the same definition with bfloat16 storage of A, B and
+ * C:  C[i][j] = bf16_rne( epi( sum_k (double)A[i][k] * (double)B[k][j] ) ).
+ * bfloat16 is the upper half of an IEEE binary32: 1 sign bit, 8 exponent
+ * bits (bias 127), 7 fraction bits; subnormal spacing 2^-133; largest finite
+ * value (2 - 2^-7) * 2^127.  Rounding is once, from fp64, ties to even.
+ * ======================================================================== */
+
+double oracle_f64_from_bf16(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 7) & 0xff;
+    int m = h & 0x7f;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)m, -133); /* subnormal: m · 2^-133 */
+    } else if (e == 255) {
+        v = m ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(128 + m), e - 134); /* (1.m) · 2^(e-127) */
+    }
+    return sign ? -v : v;
+}
+
+uint16_t oracle_bf16_from_f64(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    if (isnan(x)) return (uint16_t)(sign | 0x7fc0);
+    double a = fabs(x);
+    if (isinf(a)) return (uint16_t)(sign | 0x7f80);
+    if (a < ldexp(1.0, -126)) {
+        /* subnormal range: quantum 2^-133; n in [0, 128] (128 = min normal) */
+        double n = round_half_even(ldexp(a, 133));
+        return (uint16_t)(sign | (uint16_t)n);
+    }
+    int E;
+    frexp(a, &E);
+    int e = E - 1; /* a in [2^e, 2^(e+1)) */
+    double n = round_half_even(ldexp(a, 7 - e)); /* in [128, 256] */
+    if (n == 256.0) {
+        n = 128.0;
+        e += 1;
+    }
+    if (e > 127) return (uint16_t)(sign | 0x7f80); /* overflow -> inf */
+    return (uint16_t)(sign | (uint16_t)((e + 127) << 7) | (uint16_t)(n - 128.0));
+}
+
+void oracle_bf16_from_f64_array(const double* x, uint16_t* h, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) h[i] = oracle_bf16_from_f64(x[i]);
+}
+
+void oracle_f64_from_bf16_array(const uint16_t* h, double* x, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) x[i] = oracle_f64_from_bf16(h[i]);
+}
+
+static double g_lut_bf16[65536];
+static int g_lut_bf16_ready = 0;
+
+static void lut_bf16_init(void)
+{
+    if (g_lut_bf16_ready) return;
+    for (int i = 0; i < 65536; ++i) g_lut_bf16[i] = oracle_f64_from_bf16((uint16_t)i);
+    g_lut_bf16_ready = 1;
+}
+
+/* Full product, bf16 storage; arguments as oracle_gemm_f16. */
+int oracle_gemm_bf16(const uint16_t* A, const uint16_t* B, uint16_t* C, double* Cref,
+                     int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                     int relu)
+{
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < N || ldc < N) return -1;
+    lut_bf16_init();
+    int err = 0;
+#pragma omp parallel
+    {
+        double* acc = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+        if (!acc) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < M; ++i) {
+            if (!acc) continue;
+            for (int64_t j = 0; j < N; ++j) acc[j] = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double a = g_lut_bf16[A[i * lda + k]];
+                const uint16_t* brow = B + k * ldb;
+                for (int64_t j = 0; j < N; ++j) acc[j] += a * g_lut_bf16[brow[j]];
+            }
+            for (int64_t j = 0; j < N; ++j) {
+                double v = epi_apply(acc[j], relu);
+                C[i * ldc + j] = oracle_bf16_from_f64(v);
+                if (Cref) Cref[i * N + j] = v;
+            }
+        }
+        free(acc);
+    }
+    return err ? -1 : 0;
+}
+
+/* Selected outputs, bf16 storage; arguments as oracle_gemm_f16_at. */
+int oracle_gemm_bf16_at(const uint16_t* A, const uint16_t* B, int64_t K, int64_t lda,
+                        int64_t ldb, int relu, const int64_t* rows, const int64_t* cols,
+                        int64_t n, uint16_t* out16, double* out64)
+{
+    if (K < 0 || lda < K) return -1;
+    lut_bf16_init();
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) {
+        const uint16_t* arow = A + rows[t] * lda;
+        const uint16_t* bcol = B + cols[t];
+        double s = 0.0;
+        for (int64_t k = 0; k < K; ++k) s += g_lut_bf16[arow[k]] * g_lut_bf16[bcol[k * ldb]];
+        double v = epi_apply(s, relu);
+        if (out16) out16[t] = oracle_bf16_from_f64(v);
+        if (out64) out64[t] = v;
+    }
+    return 0;
+}

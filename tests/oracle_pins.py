@@ -23,7 +23,7 @@ from fractions import Fraction
 
 import numpy as np
 
-from exact import exact_gemm, rne_f16, frac_of_f16
+from exact import BF16_MAX, bf16_bits_to_float, exact_gemm, frac_of_f16, rne_bf16, rne_f16
 
 ALL16 = np.arange(65536, dtype=np.uint16)
 
@@ -255,6 +255,107 @@ def pin_zero_sizes(o):
     assert C.shape == (3, 4) and np.all(C.astype(np.float64) == 0.0)
     Cr = o.gemm(A, B, 3, 4, 0, relu=True)
     assert not np.any(np.signbit(Cr.astype(np.float64)))
+
+
+# ---------------------------------------------------------------- bfloat16 variant
+
+def _bf16_bits(x):
+    """Round float64 values to bfloat16 bits exactly (single rounding), via
+    exact rationals — independent of the oracle."""
+    return np.array([_float_to_bf16_bits(rne_bf16(Fraction(float(v)))) for v in np.ravel(x)],
+                    dtype=np.uint16).reshape(np.shape(x))
+
+
+def _float_to_bf16_bits(v: float) -> int:
+    f32 = np.array([v], dtype=np.float32)  # exact: v is a bf16 value
+    return int(f32.view(np.uint32)[0] >> 16)
+
+
+def pin_bf16_decode_matches_binary32(o):
+    mine = o.f64_from_bf16(ALL16)
+    ref = bf16_bits_to_float(ALL16)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan], ref[~nan])
+    assert np.signbit(mine[0x8000]) and not np.signbit(mine[0])
+
+
+def pin_bf16_roundtrip_and_midpoints(o):
+    vals = bf16_bits_to_float(ALL16)
+    keep = ~np.isnan(vals)
+    assert np.array_equal(o.bf16_from_f64(vals[keep]), ALL16[keep])
+    pos = np.arange(0, 0x7f7f, dtype=np.uint16)  # adjacent finite pairs (h, h+1)
+    lo = bf16_bits_to_float(pos)
+    hi = bf16_bits_to_float(pos + 1)
+    mid = (lo + hi) / 2.0
+    even = np.where(pos % 2 == 0, pos, pos + 1).astype(np.uint16)
+    assert np.array_equal(o.bf16_from_f64(mid), even)
+    assert np.array_equal(o.bf16_from_f64(np.nextafter(mid, np.inf)), pos + 1)
+    assert np.array_equal(o.bf16_from_f64(np.nextafter(mid, -np.inf)), pos)
+    assert np.array_equal(o.bf16_from_f64(-mid), even | 0x8000)
+
+
+def pin_bf16_overflow_and_specials(o):
+    mx = float(BF16_MAX)
+    half_ulp = 2.0 ** (127 - 8)
+    cases = [(mx, 0x7F7F), (mx + half_ulp * 0.99, 0x7F7F), (mx + half_ulp, 0x7F80),
+             (1.5 * 2.0 ** 128, 0x7F80), (1e300, 0x7F80),
+             (-(mx + half_ulp), 0xFF80), (math.inf, 0x7F80), (2.0 ** -133, 0x0001),
+             (2.0 ** -134, 0x0000), (1.5 * 2.0 ** -134, 0x0001), (2.0 ** -126, 0x0080),
+             (1.0, 0x3F80), (-2.0, 0xC000), (0.0, 0x0000), (-0.0, 0x8000),
+             (1.0 + 2.0 ** -8, 0x3F80), (1.0 + 3 * 2.0 ** -8, 0x3F82)]
+    got = o.bf16_from_f64(np.array([c[0] for c in cases]))
+    want = np.array([c[1] for c in cases], dtype=np.uint16)
+    assert np.array_equal(got, want), [(c[0], hex(g), hex(w)) for c, g, w in zip(cases, got, want)
+                                       if g != w]
+
+
+def pin_bf16_matches_exact_rounding(o):
+    rng = np.random.default_rng(321)
+    x = np.ldexp(rng.uniform(1.0, 2.0, 3000), rng.integers(-140, 128, 3000))
+    x *= np.where(rng.integers(0, 2, 3000) == 1, -1.0, 1.0)
+    assert np.array_equal(o.bf16_from_f64(x), _bf16_bits(x))
+
+
+def pin_bf16_bruteforce_exact(o):
+    rng = np.random.default_rng(8)
+    for (M, N, K) in [(1, 1, 1), (3, 5, 7), (7, 3, 16), (5, 9, 13)]:
+        for sc in (1.0, 1e-30, 1e20):
+            A = _bf16_bits(rng.normal(0, sc, (M, K)))
+            B = _bf16_bits(rng.normal(0, sc, (K, N)))
+            for relu in (False, True):
+                want, _ = exact_gemm(A, B, relu, dtype="bf16")
+                got = bf16_bits_to_float(o.gemm(A, B, M, N, K, relu, dtype="bf16"))
+                assert _same_value(got, want), (M, N, K, sc, relu)
+
+
+def pin_bf16_integer_product(o):
+    """{-1,0,1} products: the sum is an exact integer; bf16 then rounds it once
+    (integers above 256 are not all representable)."""
+    rng = np.random.default_rng(18)
+    M, N, K = 24, 20, 1500
+    Ai = rng.integers(-1, 2, (M, K))
+    Ai[0] = 1  # row 0 against the all-ones columns sums to K = 1500
+    Bi = np.ones((K, N), dtype=np.int64)
+    Bi[:, ::2] = rng.integers(-1, 2, (K, (N + 1) // 2))
+    A = _bf16_bits(Ai.astype(np.float64))
+    B = _bf16_bits(Bi.astype(np.float64))
+    got = bf16_bits_to_float(o.gemm(A, B, M, N, K, dtype="bf16"))
+    want = np.array([[rne_bf16(Fraction(int(v))) for v in row] for row in Ai @ Bi])
+    assert np.array_equal(got, want)
+    assert np.any(np.abs(Ai @ Bi) > 256)  # the rounding is exercised
+
+
+def pin_bf16_sampled_matches_full(o):
+    rng = np.random.default_rng(19)
+    M, N, K = 40, 50, 90
+    A = _bf16_bits(rng.normal(0, 1, (M, K)))
+    B = _bf16_bits(rng.normal(0, 1, (K, N)))
+    C, ref = o.gemm(A, B, M, N, K, relu=True, want_ref=True, dtype="bf16")
+    r = rng.integers(0, M, 300)
+    c = rng.integers(0, N, 300)
+    v16, v64 = o.gemm_at(A, B, K, r, c, relu=True, dtype="bf16")
+    assert np.array_equal(v16, C[r, c]) and np.array_equal(v64, ref[r, c])
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -35,6 +35,16 @@ MUTANTS = [
     ("decode_bias", "e - 25);", "e - 24);"),
     ("decode_subnormal", "v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
     ("ldb_ignored", "g_lut[bcol[k * ldb]]", "g_lut[bcol[k * (ldb - (ldb > 1))]]"),
+    # bfloat16 variant
+    ("bf16_decode_bias", "e - 134);", "e - 133);"),
+    ("bf16_decode_subnormal", "v = ldexp((double)m, -133);", "v = ldexp((double)m, -134);"),
+    ("bf16_flush_subnormals", "double n = round_half_even(ldexp(a, 133));", "double n = 0.0;"),
+    ("bf16_late_overflow", "if (e > 127) return", "if (e > 128) return"),
+    ("bf16_fp16_lut", "acc[j] += a * g_lut_bf16[brow[j]];", "acc[j] += a * g_lut[brow[j]];"),
+    ("bf16_rounds_as_fp16", "C[i * ldc + j] = oracle_bf16_from_f64(v);",
+     "C[i * ldc + j] = oracle_f16_from_f64(v);"),
+    ("bf16_truncating_round", "double n = round_half_even(ldexp(a, 7 - e));",
+     "double n = floor(ldexp(a, 7 - e));"),
 ]
 
 
