@@ -51,6 +51,7 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-skinny", action="store_true")
+    p.add_argument("--no-bf16", action="store_true")
     a = p.parse_args(argv)
     if a.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -371,6 +372,38 @@ def run_ours(args, w, rank, world, local_rank):
                          "peak_source": f"{peak_src} copy bandwidth"},
         }
         del a2, b2, c2
+
+    # ---- bfloat16 variant on the same shape, same method
+    if not args.no_bf16:
+        ab = a.to(torch.bfloat16)
+        bb = b.to(torch.bfloat16)
+        cb = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
+
+        def launch3():
+            st = tg.tg_gemm_bf16(ab.data_ptr(), bb.data_ptr(), cb.data_ptr(), w.M, w.N, w.K,
+                                 w.K, w.N, w.N, epi, stream.cuda_stream)
+            if st != tg.TG_OK:
+                raise tg.TgemmError(st)
+
+        for _ in range(args.warmup):
+            launch3()
+        tg.sync_status(stream)
+        n4 = max(50, args.steps // 2)
+        _, per4, _, _ = time_launches(launch3, stream, n4, world, device)
+        tg.sync_status(stream)
+        k4 = statistics.mean(per4)
+        if plan.kernel == tg.TG_KERNEL_PERSISTENT:
+            ach = flops / (k4 / 1e3) / 1e12
+            roof4 = {"bound": "tensor", "achieved": ach, "peak": tf_peak, "unit": "TFLOP/s",
+                     "frac": ach / tf_peak}
+        else:
+            ach = w.min_bytes / (k4 / 1e3) / 1e9
+            roof4 = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": ach / hbm_peak}
+        out["bf16"] = {"workload": w.name, "entry": "tg_gemm_bf16", "launches": n4,
+                       "kernel_ms_mean": k4, "kernel_ms_min": min(per4),
+                       "tflops": flops / (k4 / 1e3) / 1e12, "roofline": roof4}
+        del ab, bb, cb
 
     # ---- end to end through the public API, host buffers in and out
     if not args.no_e2e:

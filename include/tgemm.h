@@ -88,6 +88,19 @@ tg_status_t tg_gemm_f16(const void* A, const void* B, void* C,
                         int epilogue, void* stream);
 
 /*
+ * tg_gemm_bf16 — the same operation with bfloat16 storage of A, B and C:
+ * C = bf16_rne(epi(A·B)), fp32 accumulation.  The pages define the GEMM for
+ * fp16 only ("5分钟上手TileLang", section "安装与第一个内核"); bf16 runs on the
+ * same tensor-core instruction kind (operand format bf16 instead of f16)
+ * through the same kernels, so arguments, layouts, alignment, ownership,
+ * errors and kernel choice are exactly those of tg_gemm_f16.
+ */
+tg_status_t tg_gemm_bf16(const void* A, const void* B, void* C,
+                         int64_t M, int64_t N, int64_t K,
+                         int64_t lda, int64_t ldb, int64_t ldc,
+                         int epilogue, void* stream);
+
+/*
  * tg_sync_status — wait for `stream`, then report (and clear) a device-side
  * timeout recorded by any libtgemm kernel on the current device since the
  * last call.  Returns TG_OK, TG_ERR_TIMEOUT, or TG_ERR_LAUNCH if the stream

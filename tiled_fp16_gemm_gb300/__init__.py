@@ -36,7 +36,7 @@ TG_KERNEL_SKINNY = 3
 EXPORTS = (
     "tg_gemm_f16", "tg_sync_status", "tg_status_string", "tg_version", "tg_plan_f16",
     "tg_tile_coord", "tg_ring_bytes", "tg_debug_set_wait_timeout_ns", "tg_debug_inject",
-    "tg_gemm_f16_noalloc",
+    "tg_gemm_f16_noalloc", "tg_gemm_bf16",
 )
 
 #: bytes of the library's fixed scratch array used by tg_gemm_f16_noalloc
@@ -77,6 +77,8 @@ def _L():
     lib.tg_gemm_f16.argtypes = [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int,
                                 _vp]
     lib.tg_gemm_f16.restype = ctypes.c_int
+    lib.tg_gemm_bf16.argtypes = lib.tg_gemm_f16.argtypes
+    lib.tg_gemm_bf16.restype = ctypes.c_int
     lib.tg_sync_status.argtypes = [_vp]
     lib.tg_sync_status.restype = ctypes.c_int
     lib.tg_status_string.argtypes = [ctypes.c_int]
@@ -114,6 +116,12 @@ def tg_gemm_f16(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: i
                 epilogue: int, stream: int | None) -> int:
     """The C entry point with integer device pointers; returns the status code."""
     return _L().tg_gemm_f16(A, B, C, M, N, K, lda, ldb, ldc, epilogue, stream or None)
+
+
+def tg_gemm_bf16(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
+                 epilogue: int, stream: int | None) -> int:
+    """The bfloat16 entry point with integer device pointers; returns the status code."""
+    return _L().tg_gemm_bf16(A, B, C, M, N, K, lda, ldb, ldc, epilogue, stream or None)
 
 
 def tg_sync_status(stream: int | None) -> int:
@@ -177,8 +185,8 @@ def _check_operand(t, name: str):
     import torch
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.dtype != torch.float16:
-        raise TypeError(f"{name} must be float16, got {t.dtype}")
+    if t.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError(f"{name} must be float16 or bfloat16, got {t.dtype}")
     if t.dim() != 2:
         raise ValueError(f"{name} must be 2-D")
     if t.shape[1] > 1 and t.stride(1) != 1:
@@ -193,7 +201,7 @@ def _ld(t) -> int:
 
 
 def gemm(a, b, relu: bool = False, out=None, stream=None):
-    """C = epi(a @ b) for CUDA float16 tensors a (M×K) and b (K×N).
+    """C = epi(a @ b) for CUDA float16 (or bfloat16) tensors a (M×K) and b (K×N).
 
     Row-major views with a row stride that is a multiple of 8 elements and
     16-byte aligned storage are accepted; ``out`` (M×N, same rules) is written
@@ -209,16 +217,19 @@ def gemm(a, b, relu: bool = False, out=None, stream=None):
         raise ValueError(f"inner dimensions differ: {K} vs {K2}")
     if not (a.is_cuda and b.is_cuda and a.device == b.device):
         raise ValueError("a and b must be CUDA tensors on the same device")
+    if a.dtype != b.dtype:
+        raise TypeError(f"a and b must share a dtype, got {a.dtype} and {b.dtype}")
     if out is None:
-        out = torch.empty((M, N), dtype=torch.float16, device=a.device)
+        out = torch.empty((M, N), dtype=a.dtype, device=a.device)
     else:
         _check_operand(out, "out")
-        if tuple(out.shape) != (M, N) or out.device != a.device:
-            raise ValueError("out must be M×N on a's device")
+        if tuple(out.shape) != (M, N) or out.device != a.device or out.dtype != a.dtype:
+            raise ValueError("out must be M×N on a's device with a's dtype")
+    entry = tg_gemm_bf16 if a.dtype == torch.bfloat16 else tg_gemm_f16
     with torch.cuda.device(a.device):
         s = stream if stream is not None else torch.cuda.current_stream(a.device)
-        st = tg_gemm_f16(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K, _ld(a), _ld(b),
-                         _ld(out), TG_EPI_RELU if relu else TG_EPI_NONE, s.cuda_stream)
+        st = entry(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K, _ld(a), _ld(b),
+                   _ld(out), TG_EPI_RELU if relu else TG_EPI_NONE, s.cuda_stream)
     if st != TG_OK:
         raise TgemmError(st)
     return out

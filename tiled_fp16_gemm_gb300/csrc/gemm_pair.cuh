@@ -50,7 +50,7 @@ struct PairCfg {
         1024 + STAGES * kStageBytes + kCBytes + kBarBytes;
 };
 
-template <int STAGES>
+template <int STAGES, typename T = __half>
 __global__ void __launch_bounds__(192, 1)
     tg_gemm_f16_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const PersistentParams p) {
@@ -168,7 +168,8 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (even CTA)
         if (leader && lane == 0) {
-            constexpr uint32_t idesc = idesc_f16_f32(256, 256, /*a_mn=*/false, /*b_mn=*/true);
+            constexpr uint32_t idesc =
+                idesc_f16_f32(256, 256, /*a_mn=*/false, /*b_mn=*/true, Elem16<T>::kFmt);
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
@@ -256,8 +257,8 @@ __global__ void __launch_bounds__(192, 1)
                         y0 = relu_f32(y0);
                         y1 = relu_f32(y1);
                     }
-                    h[t] = pack_half2(x0, x1);
-                    h[16 + t] = pack_half2(y0, y1);
+                    h[t] = Elem16<T>::pack2(x0, x1);
+                    h[16 + t] = Elem16<T>::pack2(y0, y1);
                 }
                 if (lane == 0) bulk_wait_group_read<1>();
                 __syncwarp();

@@ -67,7 +67,7 @@ struct PersistentCfg {
                   "TMEM columns must be a power of two in [32, 512]");
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, typename T = __half>
 __global__ void __launch_bounds__(192, 1)
     tg_gemm_f16_persistent(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
@@ -175,7 +175,8 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16_f32(BM, BN, /*a_mn=*/false, /*b_mn=*/true);
+            constexpr uint32_t idesc =
+                idesc_f16_f32(BM, BN, /*a_mn=*/false, /*b_mn=*/true, Elem16<T>::kFmt);
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
@@ -267,8 +268,8 @@ __global__ void __launch_bounds__(192, 1)
                         y0 = relu_f32(y0);
                         y1 = relu_f32(y1);
                     }
-                    h[t] = pack_half2(x0, x1);
-                    h[16 + t] = pack_half2(y0, y1);
+                    h[t] = Elem16<T>::pack2(x0, x1);
+                    h[16 + t] = Elem16<T>::pack2(y0, y1);
                 }
                 // the buffer written two stores ago must have been read out
                 if (lane == 0) bulk_wait_group_read<1>();

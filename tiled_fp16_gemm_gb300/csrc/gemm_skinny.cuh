@@ -75,7 +75,7 @@ struct SkinnyParams {
     int64_t total_units;
     int32_t relu, inject;
     uint64_t timeout_ns;
-    __half* C;
+    void* C;  // T*: the kernel's element type
     int64_t ldc;
     float* ws;
     uint32_t* flags;
@@ -104,7 +104,7 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-template <int STAGES, int MP_MAX>
+template <int STAGES, int MP_MAX, typename T = __half>
 __global__ void __launch_bounds__(192, 1)
     tg_gemm_f16_skinny(const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmA, const SkinnyParams p) {
@@ -205,7 +205,8 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = idesc_f16_f32(128, p.Mp, /*a_mn=*/true, /*b_mn=*/false);
+            const uint32_t idesc =
+                idesc_f16_f32(128, p.Mp, /*a_mn=*/true, /*b_mn=*/false, Elem16<T>::kFmt);
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
@@ -336,7 +337,7 @@ __global__ void __launch_bounds__(192, 1)
                             const int m = 16 * c + i;
                             if (m < p.M) {
                                 const float x = p.relu ? relu_f32(v[i]) : v[i];
-                                p.C[static_cast<int64_t>(m) * p.ldc + n] = __float2half_rn(x);
+                                static_cast<T*>(p.C)[static_cast<int64_t>(m) * p.ldc + n] = Elem16<T>::from_float(x);
                             }
                         }
                     }
@@ -404,17 +405,19 @@ inline void skinny_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_pla
     pl->cluster = 1;
 }
 
+template <typename T>
 inline cudaError_t skinny_set_attributes() {
-    cudaError_t e = cudaFuncSetAttribute(tg_gemm_f16_skinny<9, 64>,
+    cudaError_t e = cudaFuncSetAttribute(tg_gemm_f16_skinny<9, 64, T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SkinnyNarrow::kSmemBytes);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(tg_gemm_f16_skinny<6, 128>,
+    return cudaFuncSetAttribute(tg_gemm_f16_skinny<6, 128, T>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 SkinnyWide::kSmemBytes);
 }
 
 // Cooperative launch of the instantiation whose A slots fit prm.Mp.
+template <typename T>
 inline cudaError_t skinny_launch_kernel(const CUtensorMap& tmB, const CUtensorMap& tmA,
                                         const SkinnyParams& prm, int64_t grid,
                                         cudaStream_t stream) {
@@ -430,10 +433,10 @@ inline cudaError_t skinny_launch_kernel(const CUtensorMap& tmB, const CUtensorMa
     cfg.numAttrs = 1;
     if (prm.Mp <= 64) {
         cfg.dynamicSmemBytes = SkinnyNarrow::kSmemBytes;
-        return cudaLaunchKernelEx(&cfg, tg_gemm_f16_skinny<9, 64>, tmB, tmA, prm);
+        return cudaLaunchKernelEx(&cfg, tg_gemm_f16_skinny<9, 64, T>, tmB, tmA, prm);
     }
     cfg.dynamicSmemBytes = SkinnyWide::kSmemBytes;
-    return cudaLaunchKernelEx(&cfg, tg_gemm_f16_skinny<6, 128>, tmB, tmA, prm);
+    return cudaLaunchKernelEx(&cfg, tg_gemm_f16_skinny<6, 128, T>, tmB, tmA, prm);
 }
 
 struct SkinnyWorkspace {
@@ -462,8 +465,9 @@ inline void skinny_reset_flags(int dev) {
 }
 
 using EncodeFn = bool (*)(CUtensorMap*, const void*, uint64_t, uint64_t, uint64_t, uint32_t,
-                          uint32_t);
+                          uint32_t, CUtensorMapDataType);
 
+template <typename T>
 inline tg_status_t skinny_launch(const void* A, const void* B, void* C, const tg_plan_t& pl,
                                  int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                                  int64_t ldc, int epilogue, cudaStream_t stream, int dev,
@@ -471,8 +475,10 @@ inline tg_status_t skinny_launch(const void* A, const void* B, void* C, const tg
                                  EncodeFn encode) {
     const int64_t Mp = pl.mma_n;
     CUtensorMap tmA, tmB;
-    if (!encode(&tmB, B, N, K, ldb * 2, 64, 64) ||
-        !encode(&tmA, A, K, M, lda * 2, 64, static_cast<uint32_t>(Mp)))
+    const CUtensorMapDataType dt = Elem16<T>::kFmt == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (!encode(&tmB, B, N, K, ldb * 2, 64, 64, dt) ||
+        !encode(&tmA, A, K, M, lda * 2, 64, static_cast<uint32_t>(Mp), dt))
         return TG_ERR_LAUNCH;
 
     SkinnyParams prm;
@@ -519,10 +525,10 @@ inline tg_status_t skinny_launch(const void* A, const void* B, void* C, const tg
     prm.relu = epilogue == TG_EPI_RELU ? 1 : 0;
     prm.inject = inject;
     prm.timeout_ns = timeout_ns;
-    prm.C = static_cast<__half*>(C);
+    prm.C = C;
     prm.ldc = ldc;
 
-    if (skinny_launch_kernel(tmB, tmA, prm, pl.grid, stream) != cudaSuccess) {
+    if (skinny_launch_kernel<T>(tmB, tmA, prm, pl.grid, stream) != cudaSuccess) {
         cudaGetLastError();
         return TG_ERR_LAUNCH;
     }

@@ -9,6 +9,8 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace tg {
 
@@ -244,15 +246,45 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
            (2ull << 61);   // swizzle mode: 128 B
 }
 
-// Instruction descriptor for tcgen05.mma kind::f16 with fp16 A and B and an
-// fp32 accumulator.  a_mn / b_mn select MN-major (transposed) operands.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n, bool a_mn, bool b_mn) {
+// Instruction descriptor for tcgen05.mma kind::f16 with 16-bit A and B of
+// format `ab_fmt` (0 = f16, 1 = bf16; A and B always share it) and an fp32
+// accumulator.  a_mn / b_mn select MN-major (transposed) operands.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n, bool a_mn, bool b_mn,
+                                                     uint32_t ab_fmt = 0) {
     return (1u << 4)                                  // D format: f32
-           | (0u << 7) | (0u << 10)                   // A, B format: f16
+           | (ab_fmt << 7) | (ab_fmt << 10)           // A, B format
            | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16)
            | (static_cast<uint32_t>(n >> 3) << 17)    // N / 8
            | (static_cast<uint32_t>(m >> 4) << 24);   // M / 16
 }
+
+// The two 16-bit element types: operand format code for the instruction
+// descriptor, and the epilogue's fp32 → storage rounding (nearest, ties to
+// even), two values packed per 32-bit word (first in the low half).
+template <typename T>
+struct Elem16;
+
+template <>
+struct Elem16<__half> {
+    static constexpr uint32_t kFmt = 0;
+    __device__ static __forceinline__ uint32_t pack2(float lo, float hi) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __device__ static __forceinline__ __half from_float(float x) { return __float2half_rn(x); }
+};
+
+template <>
+struct Elem16<__nv_bfloat16> {
+    static constexpr uint32_t kFmt = 1;
+    __device__ static __forceinline__ uint32_t pack2(float lo, float hi) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __device__ static __forceinline__ __nv_bfloat16 from_float(float x) {
+        return __float2bfloat16_rn(x);
+    }
+};
 
 // ------------------------------------------------------------------ CTA pairs (cta_group::2)
 //
@@ -333,11 +365,6 @@ __device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_ma
 }
 
 // ------------------------------------------------------------------ misc
-
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
 
 __device__ __forceinline__ float relu_f32(float x) { return x > 0.0f ? x : 0.0f; }
 

@@ -119,6 +119,24 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return g_encode;
 }
 
+// Opt every kernel instantiation of element type T into its shared memory.
+template <typename T>
+cudaError_t set_kernel_attributes() {
+    cudaError_t e = cudaFuncSetAttribute(tg::tg_gemm_f16_persistent<kBigBN, kBigStages, T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         tg::PersistentCfg<kBigBN, kBigStages>::kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tg::tg_gemm_f16_persistent<kMidBN, kMidStages, T>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tg::PersistentCfg<kMidBN, kMidStages>::kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tg::tg_gemm_f16_pair<kPairStages, T>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tg::PairCfg<kPairStages>::kSmemBytes);
+    if (e == cudaSuccess) e = tg::skinny_set_attributes<T>();
+    return e;
+}
+
 // Returns TG_OK and fills *dev / *st for the current device, or an error.
 tg_status_t current_device(int* dev, DeviceState** st) {
     int d = -1;
@@ -142,18 +160,8 @@ tg_status_t current_device(int* dev, DeviceState** st) {
     }
     if (!s.supported) return TG_ERR_UNSUPPORTED_DEVICE;
     if (!s.attrs_set) {
-        using C1 = tg::PersistentCfg<kBigBN, kBigStages>;
-        using C2 = tg::PersistentCfg<kMidBN, kMidStages>;
-        if (cudaFuncSetAttribute(tg::tg_gemm_f16_persistent<kBigBN, kBigStages>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C1::kSmemBytes) != cudaSuccess ||
-            cudaFuncSetAttribute(tg::tg_gemm_f16_persistent<kMidBN, kMidStages>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C2::kSmemBytes) != cudaSuccess ||
-            tg::skinny_set_attributes() != cudaSuccess ||
-            cudaFuncSetAttribute(tg::tg_gemm_f16_pair<kPairStages>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 tg::PairCfg<kPairStages>::kSmemBytes) != cudaSuccess) {
+        if (set_kernel_attributes<__half>() != cudaSuccess ||
+            set_kernel_attributes<__nv_bfloat16>() != cudaSuccess) {
             cudaGetLastError();
             return TG_ERR_LAUNCH;
         }
@@ -172,8 +180,8 @@ tg_status_t current_device(int* dev, DeviceState** st) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, tg::tg_gemm_f16_pair<kPairStages>, &cfg) !=
-            cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&clusters, tg::tg_gemm_f16_pair<kPairStages, __half>,
+                                           &cfg) != cudaSuccess) {
             cudaGetLastError();
             clusters = 0;
         }
@@ -185,30 +193,42 @@ tg_status_t current_device(int* dev, DeviceState** st) {
     return TG_OK;
 }
 
-// 2-D fp16 tensor map: inner (contiguous) extent, outer extent, row stride in
-// bytes, box, 128-byte swizzle, zero fill outside the tensor.
+template <typename T>
+constexpr CUtensorMapDataType tensor_map_type() {
+    return tg::Elem16<T>::kFmt == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+// 2-D 16-bit tensor map: inner (contiguous) extent, outer extent, row stride
+// in bytes, box, 128-byte swizzle, zero fill outside the tensor.
 bool encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
-               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapDataType dtype) {
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {row_bytes};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r = enc(map, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES>
-tg_status_t launch_persistent(const void* A, const void* B, void* C, const tg_plan_t& pl,
-                              int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
-                              int64_t ldc, int epilogue, cudaStream_t stream) {
-    CUtensorMap tmA, tmB, tmC;
-    if (!encode_2d(&tmA, A, K, M, lda * 2, 64, 128) || !encode_2d(&tmB, B, N, K, ldb * 2, 64, 64) ||
-        !encode_2d(&tmC, C, N, M, ldc * 2, 64, 32))
-        return TG_ERR_LAUNCH;
+// A, B and C maps of the pair / one-CTA kernels.
+template <typename T>
+bool encode_abc(CUtensorMap* tmA, CUtensorMap* tmB, CUtensorMap* tmC, const void* A,
+                const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                int64_t ldc) {
+    constexpr CUtensorMapDataType dt = tensor_map_type<T>();
+    return encode_2d(tmA, A, K, M, lda * 2, 64, 128, dt) &&
+           encode_2d(tmB, B, N, K, ldb * 2, 64, 64, dt) &&
+           encode_2d(tmC, C, N, M, ldc * 2, 64, 32, dt);
+}
+
+tg::PersistentParams persistent_params(const tg_plan_t& pl, int64_t M, int64_t N, int64_t K,
+                                       int epilogue) {
     tg::PersistentParams prm;
     prm.M = static_cast<int32_t>(M);
     prm.N = static_cast<int32_t>(N);
@@ -221,7 +241,16 @@ tg_status_t launch_persistent(const void* A, const void* B, void* C, const tg_pl
     prm.relu = epilogue == TG_EPI_RELU ? 1 : 0;
     prm.inject = g_inject.exchange(0);
     prm.timeout_ns = g_timeout_ns.load();
+    return prm;
+}
 
+template <int BN, int STAGES, typename T>
+tg_status_t launch_persistent(const void* A, const void* B, void* C, const tg_plan_t& pl,
+                              int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                              int64_t ldc, int epilogue, cudaStream_t stream) {
+    CUtensorMap tmA, tmB, tmC;
+    if (!encode_abc<T>(&tmA, &tmB, &tmC, A, B, C, M, N, K, lda, ldb, ldc)) return TG_ERR_LAUNCH;
+    const tg::PersistentParams prm = persistent_params(pl, M, N, K, epilogue);
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
@@ -229,7 +258,7 @@ tg_status_t launch_persistent(const void* A, const void* B, void* C, const tg_pl
     cfg.dynamicSmemBytes = tg::PersistentCfg<BN, STAGES>::kSmemBytes;
     cfg.stream = stream;
     cudaError_t e =
-        cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_persistent<BN, STAGES>, tmA, tmB, tmC, prm);
+        cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_persistent<BN, STAGES, T>, tmA, tmB, tmC, prm);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return TG_ERR_LAUNCH;
@@ -239,26 +268,13 @@ tg_status_t launch_persistent(const void* A, const void* B, void* C, const tg_pl
 
 // The pair kernel: clusters of two CTAs, at most as many pairs as the device
 // holds at once (the launch is persistent, so no pair waits for another).
+template <typename T>
 tg_status_t launch_pair(const void* A, const void* B, void* C, const tg_plan_t& pl, int64_t M,
                         int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int epilogue,
                         cudaStream_t stream, int max_pairs) {
     CUtensorMap tmA, tmB, tmC;
-    if (!encode_2d(&tmA, A, K, M, lda * 2, 64, 128) || !encode_2d(&tmB, B, N, K, ldb * 2, 64, 64) ||
-        !encode_2d(&tmC, C, N, M, ldc * 2, 64, 32))
-        return TG_ERR_LAUNCH;
-    tg::PersistentParams prm;
-    prm.M = static_cast<int32_t>(M);
-    prm.N = static_cast<int32_t>(N);
-    prm.K = static_cast<int32_t>(K);
-    prm.tiles_m = static_cast<int32_t>(pl.tiles_m);
-    prm.tiles_n = static_cast<int32_t>(pl.tiles_n);
-    prm.num_tiles = static_cast<int32_t>(pl.num_tiles);
-    prm.k_blocks = static_cast<int32_t>(pl.k_blocks);
-    prm.group_m = pl.group_m;
-    prm.relu = epilogue == TG_EPI_RELU ? 1 : 0;
-    prm.inject = g_inject.exchange(0);
-    prm.timeout_ns = g_timeout_ns.load();
-
+    if (!encode_abc<T>(&tmA, &tmB, &tmC, A, B, C, M, N, K, lda, ldb, ldc)) return TG_ERR_LAUNCH;
+    const tg::PersistentParams prm = persistent_params(pl, M, N, K, epilogue);
     int64_t pairs = pl.grid / 2;
     if (pairs > max_pairs) pairs = max_pairs;
     cudaLaunchAttribute attr[1];
@@ -274,7 +290,8 @@ tg_status_t launch_pair(const void* A, const void* B, void* C, const tg_plan_t& 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_pair<kPairStages>, tmA, tmB, tmC, prm);
+    cudaError_t e =
+        cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_pair<kPairStages, T>, tmA, tmB, tmC, prm);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return TG_ERR_LAUNCH;
@@ -324,6 +341,58 @@ tg_status_t validate(const void* A, const void* B, const void* C, int64_t M, int
                   (ldb & 7) != 0))
         return TG_ERR_MISALIGNED;
     return TG_OK;
+}
+
+// C = epi(A·B) for 16-bit element type T (__half or __nv_bfloat16): plan,
+// then launch the planned kernel on `stream`.
+template <typename T>
+tg_status_t gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                      int64_t lda, int64_t ldb, int64_t ldc, int epilogue, void* stream) {
+    tg_status_t st = validate(A, B, C, M, N, K, lda, ldb, ldc, epilogue);
+    if (st != TG_OK || M == 0 || N == 0) return st;
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    st = current_device(&dev, &ds);
+    if (st != TG_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    tg_plan_t pl;
+    st = tg_plan_f16(M, N, K, ds->num_sms, &pl);
+    if (st != TG_OK) return st;
+    apply_forced_config(M, N, K, ds->num_sms, &pl);
+
+    switch (pl.kernel) {
+        case TG_KERNEL_FILL: {
+            // +0 has the same (all-zero) bits in fp16 and bf16
+            tg::tg_fill_zero_f16<<<static_cast<unsigned>(pl.grid), 256, 0, s>>>(
+                static_cast<__half*>(C), M, N, ldc);
+            if (cudaGetLastError() != cudaSuccess) return TG_ERR_LAUNCH;
+            return TG_OK;
+        }
+        case TG_KERNEL_PERSISTENT:
+            if (pl.cluster == 2) {
+                if (ds->max_pairs < 1) {  // cannot place a pair: one-CTA tiles instead
+                    plan_persistent(M, N, K, ds->num_sms, kBigBN, kBigStages,
+                                    tg::PersistentCfg<kBigBN, kBigStages>::kSmemBytes, &pl);
+                } else {
+                    return launch_pair<T>(A, B, C, pl, M, N, K, lda, ldb, ldc, epilogue, s,
+                                       ds->max_pairs);
+                }
+            }
+            if (pl.bn == kBigBN)
+                return launch_persistent<kBigBN, kBigStages, T>(A, B, C, pl, M, N, K, lda, ldb, ldc,
+                                                            epilogue, s);
+            return launch_persistent<kMidBN, kMidStages, T>(A, B, C, pl, M, N, K, lda, ldb, ldc,
+                                                        epilogue, s);
+        case TG_KERNEL_SKINNY: {
+            const uint64_t timeout = g_timeout_ns.load();
+            const int32_t inject = g_inject.exchange(0);
+            return tg::skinny_launch<T>(A, B, C, pl, M, N, K, lda, ldb, ldc, epilogue, s, dev,
+                                     ds->num_sms, timeout, inject, encode_2d);
+        }
+        default:
+            return TG_ERR_INVALID_VALUE;
+    }
 }
 
 }  // namespace
@@ -415,50 +484,12 @@ const char* tg_version(void) { return "libtgemm 0.1.0 (sm_103a)"; }
 
 tg_status_t tg_gemm_f16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                         int64_t lda, int64_t ldb, int64_t ldc, int epilogue, void* stream) {
-    tg_status_t st = validate(A, B, C, M, N, K, lda, ldb, ldc, epilogue);
-    if (st != TG_OK || M == 0 || N == 0) return st;
-    int dev = 0;
-    DeviceState* ds = nullptr;
-    st = current_device(&dev, &ds);
-    if (st != TG_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return gemm_impl<__half>(A, B, C, M, N, K, lda, ldb, ldc, epilogue, stream);
+}
 
-    tg_plan_t pl;
-    st = tg_plan_f16(M, N, K, ds->num_sms, &pl);
-    if (st != TG_OK) return st;
-    apply_forced_config(M, N, K, ds->num_sms, &pl);
-
-    switch (pl.kernel) {
-        case TG_KERNEL_FILL: {
-            tg::tg_fill_zero_f16<<<static_cast<unsigned>(pl.grid), 256, 0, s>>>(
-                static_cast<__half*>(C), M, N, ldc);
-            if (cudaGetLastError() != cudaSuccess) return TG_ERR_LAUNCH;
-            return TG_OK;
-        }
-        case TG_KERNEL_PERSISTENT:
-            if (pl.cluster == 2) {
-                if (ds->max_pairs < 1) {  // cannot place a pair: one-CTA tiles instead
-                    plan_persistent(M, N, K, ds->num_sms, kBigBN, kBigStages,
-                                    tg::PersistentCfg<kBigBN, kBigStages>::kSmemBytes, &pl);
-                } else {
-                    return launch_pair(A, B, C, pl, M, N, K, lda, ldb, ldc, epilogue, s,
-                                       ds->max_pairs);
-                }
-            }
-            if (pl.bn == kBigBN)
-                return launch_persistent<kBigBN, kBigStages>(A, B, C, pl, M, N, K, lda, ldb, ldc,
-                                                            epilogue, s);
-            return launch_persistent<kMidBN, kMidStages>(A, B, C, pl, M, N, K, lda, ldb, ldc,
-                                                        epilogue, s);
-        case TG_KERNEL_SKINNY: {
-            const uint64_t timeout = g_timeout_ns.load();
-            const int32_t inject = g_inject.exchange(0);
-            return tg::skinny_launch(A, B, C, pl, M, N, K, lda, ldb, ldc, epilogue, s, dev,
-                                     ds->num_sms, timeout, inject, encode_2d);
-        }
-        default:
-            return TG_ERR_INVALID_VALUE;
-    }
+tg_status_t tg_gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                         int64_t lda, int64_t ldb, int64_t ldc, int epilogue, void* stream) {
+    return gemm_impl<__nv_bfloat16>(A, B, C, M, N, K, lda, ldb, ldc, epilogue, stream);
 }
 
 tg_status_t tg_sync_status(void* stream) {
@@ -583,8 +614,9 @@ extern "C" tg_status_t tg_gemm_f16_noalloc(const void* A, const void* B, void* C
 
     const int64_t Mp = pl.mma_n;
     CUtensorMap tmA, tmB;
-    if (!encode_2d(&tmB, B, N, K, ldb * 2, 64, 64) ||
-        !encode_2d(&tmA, A, K, M, lda * 2, 64, static_cast<uint32_t>(Mp)))
+    if (!encode_2d(&tmB, B, N, K, ldb * 2, 64, 64, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) ||
+        !encode_2d(&tmA, A, K, M, lda * 2, 64, static_cast<uint32_t>(Mp),
+                   CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
         return TG_ERR_LAUNCH;
     prm.M = static_cast<int32_t>(M);
     prm.N = static_cast<int32_t>(N);
@@ -596,10 +628,10 @@ extern "C" tg_status_t tg_gemm_f16_noalloc(const void* A, const void* B, void* C
     prm.relu = epilogue == TG_EPI_RELU ? 1 : 0;
     prm.inject = 0;
     prm.timeout_ns = g_timeout_ns.load();
-    prm.C = static_cast<__half*>(C);
+    prm.C = C;
     prm.ldc = ldc;
 
-    if (tg::skinny_launch_kernel(tmB, tmA, prm, pl.grid, s) != cudaSuccess) {
+    if (tg::skinny_launch_kernel<__half>(tmB, tmA, prm, pl.grid, s) != cudaSuccess) {
         cudaGetLastError();
         return TG_ERR_LAUNCH;
     }
