@@ -61,9 +61,15 @@ typedef enum {
  * stream    a cudaStream_t (NULL = the legacy default stream) on the current
  *     device.
  *
- * Alignment: A, B, C must be 16-byte aligned and lda, ldb, ldc multiples of 8
- * (the tensor-memory-access unit copies rows with 16-byte strides); otherwise
- * TG_ERR_MISALIGNED.  C must not overlap A or B (not checked).
+ * Layout: A, B and C need only be aligned to their 2-byte elements (else
+ * TG_ERR_MISALIGNED); any lda ≥ K, ldb ≥ N, ldc ≥ N is accepted.  The kernels
+ * read and write through the tensor memory-access unit, which needs 16-byte
+ * aligned rows: an operand whose pointer is not 16-byte aligned or whose
+ * leading dimension is not a multiple of 8 is first copied into an aligned
+ * staging buffer (per device and stream, grown on demand; growth waits for
+ * the stream), and a C in such a layout is computed there and copied back.
+ * That costs one extra read and write of the staged matrices.  C must not
+ * overlap A or B (not checked).
  * Ownership: the caller owns A, B and C; the library keeps no reference past
  * the work it enqueued on `stream`.  The library owns a small split-K
  * workspace per (device, stream), allocated on first use and kept until
@@ -203,8 +209,10 @@ void tg_debug_inject(int32_t mode);
  * loads the library holds that array until the process exits.  It calls no
  * cudaMalloc, cudaFree or other allocating routine.
  *
- * Arguments, alignment rules, ownership of A, B and C, and argument errors are
- * those of tg_gemm_f16.  Additionally:
+ * Arguments, ownership of A, B and C, and argument errors are those of
+ * tg_gemm_f16, except that it has no staging buffer: A, B, C must be 16-byte
+ * aligned and lda, ldb, ldc multiples of 8 (else TG_ERR_MISALIGNED).
+ * Additionally:
  *   - M > 128 returns TG_ERR_INVALID_VALUE (the split-K kernel covers
  *     M ≤ 128 only); so does a problem whose split needs more scratch than the
  *     array holds (more than 191 CTAs, i.e. a device with more than 191 SMs).

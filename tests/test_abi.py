@@ -76,11 +76,13 @@ GOOD = 1 << 20  # a 16-byte aligned fake address (never dereferenced on these pa
     ((GOOD, GOOD, GOOD, 4, 4, 9, 8, 16, 8, 0), 1),         # lda < K
     ((GOOD, GOOD, GOOD, 4, 12, 4, 8, 8, 16, 0), 1),        # ldb < N
     ((GOOD, GOOD, GOOD, 4, 12, 4, 8, 16, 8, 0), 1),        # ldc < N
-    ((GOOD + 2, GOOD, GOOD, 4, 4, 4, 8, 8, 8, 0), 2),      # A misaligned
-    ((GOOD, GOOD + 8, GOOD, 4, 4, 4, 8, 8, 8, 0), 2),      # B misaligned
-    ((GOOD, GOOD, GOOD + 4, 4, 4, 4, 8, 8, 8, 0), 2),      # C misaligned
-    ((GOOD, GOOD, GOOD, 4, 4, 4, 12, 8, 8, 0), 2),         # lda not a multiple of 8
-    ((GOOD, GOOD, GOOD, 4, 4, 4, 8, 8, 12, 0), 2),         # ldc not a multiple of 8
+    ((GOOD + 1, GOOD, GOOD, 4, 4, 4, 8, 8, 8, 0), 2),      # A not even element-aligned
+    ((GOOD, GOOD + 3, GOOD, 4, 4, 4, 8, 8, 8, 0), 2),      # B not even element-aligned
+    ((GOOD, GOOD, GOOD + 5, 4, 4, 4, 8, 8, 8, 0), 2),      # C not even element-aligned
+    ((GOOD + 2, GOOD, GOOD, 4, 4, 4, 8, 8, 8, 0), None),   # A off 16 B: staged, accepted
+    ((GOOD, GOOD, GOOD + 4, 4, 4, 4, 8, 8, 8, 0), None),   # C off 16 B: staged, accepted
+    ((GOOD, GOOD, GOOD, 4, 4, 9, 7, 8, 8, 0), 1),          # odd lda < K still rejected
+    ((GOOD, GOOD, GOOD, 4, 4, 4, 12, 9, 11, 0), None),     # odd leading dimensions accepted
     ((GOOD, GOOD, GOOD, 0, 4, 4, 8, 8, 8, 0), 0),          # M == 0: no-op
     ((0, 0, 0, 4, 0, 4, 8, 8, 8, 1), 0),                   # N == 0: no-op, nothing checked
     ((0, 0, GOOD, 4, 4, 0, 0, 0, 8, 0), None),             # K == 0: A/B/lda/ldb ignored
@@ -95,6 +97,14 @@ def test_argument_checks_before_any_cuda_call(tg, args, want):
         assert st == tg.TG_ERR_UNSUPPORTED_DEVICE
     else:
         assert st == want, (args, tg.tg_status_string(st))
+
+
+def test_noalloc_keeps_the_tma_layout_rule(tg):
+    # the entry point without allocation has no staging buffer
+    st = tg.tg_gemm_f16_noalloc(GOOD, GOOD, GOOD, 4, 4, 4, 12, 8, 8, 0, None)
+    assert st == tg.TG_ERR_MISALIGNED
+    st = tg.tg_gemm_f16_noalloc(GOOD + 2, GOOD, GOOD, 4, 4, 4, 8, 8, 8, 0, None)
+    assert st == tg.TG_ERR_MISALIGNED
 
 
 def test_valid_call_without_gpu_reports_unsupported_device(tg):

@@ -7,6 +7,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <map>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -327,28 +328,116 @@ void apply_forced_config(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_pl
     }
 }
 
+// Argument checks shared by every entry point: sizes, null pointers, leading
+// dimensions, element (2-byte) alignment.  With `tma_layout` also the layout
+// the tensor memory-access unit addresses directly: 16-byte aligned pointers
+// and leading dimensions that are multiples of 8 elements.
 tg_status_t validate(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
-                     int64_t lda, int64_t ldb, int64_t ldc, int epilogue) {
+                     int64_t lda, int64_t ldb, int64_t ldc, int epilogue, bool tma_layout = true) {
     if (epilogue != TG_EPI_NONE && epilogue != TG_EPI_RELU) return TG_ERR_INVALID_VALUE;
     if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
         return TG_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return TG_OK;
     if (C == nullptr || ldc < N) return TG_ERR_INVALID_VALUE;
     if (K > 0 && (A == nullptr || B == nullptr || lda < K || ldb < N)) return TG_ERR_INVALID_VALUE;
-    if ((reinterpret_cast<uintptr_t>(C) & 15u) != 0 || (ldc & 7) != 0) return TG_ERR_MISALIGNED;
-    if (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15u) != 0 ||
-                  (reinterpret_cast<uintptr_t>(B) & 15u) != 0 || (lda & 7) != 0 ||
-                  (ldb & 7) != 0))
+    const unsigned mask = tma_layout ? 15u : 1u;
+    if ((reinterpret_cast<uintptr_t>(C) & mask) != 0) return TG_ERR_MISALIGNED;
+    if (K > 0 && ((reinterpret_cast<uintptr_t>(A) & mask) != 0 ||
+                  (reinterpret_cast<uintptr_t>(B) & mask) != 0))
+        return TG_ERR_MISALIGNED;
+    if (tma_layout && ((ldc & 7) != 0 || (K > 0 && ((lda & 7) != 0 || (ldb & 7) != 0))))
         return TG_ERR_MISALIGNED;
     return TG_OK;
 }
 
+bool tma_layout_ok(const void* p, int64_t ld) {
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0 && (ld & 7) == 0;
+}
+
+int64_t round_up8(int64_t x) { return (x + 7) / 8 * 8; }
+
+// Per-(device, stream) staging buffer for operands in layouts the tensor
+// memory-access unit cannot address; grown on demand (growth waits for the
+// stream, so it cannot happen inside a stream capture).
+struct Staging {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_staging_mutex;
+std::map<std::pair<int, cudaStream_t>, Staging> g_staging;
+
+tg_status_t staging_buffer(int dev, cudaStream_t s, size_t bytes, void** out) {
+    std::lock_guard<std::mutex> lk(g_staging_mutex);
+    Staging& st = g_staging[std::make_pair(dev, s)];
+    if (st.bytes < bytes) {
+        if (st.ptr) {
+            if (cudaStreamSynchronize(s) != cudaSuccess || cudaFree(st.ptr) != cudaSuccess) {
+                cudaGetLastError();
+                return TG_ERR_LAUNCH;
+            }
+            st.ptr = nullptr;
+            st.bytes = 0;
+        }
+        if (cudaMalloc(&st.ptr, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            st.ptr = nullptr;
+            return TG_ERR_NO_MEMORY;
+        }
+        st.bytes = bytes;
+    }
+    *out = st.ptr;
+    return TG_OK;
+}
+
+tg_status_t copy_matrix16(const void* src, int64_t ld_src, void* dst, int64_t ld_dst,
+                          int64_t rows, int64_t cols, int num_sms, cudaStream_t s) {
+    const int64_t chunks = rows * ((cols + 7) / 8);
+    const int64_t blocks = (chunks + 255) / 256;
+    const unsigned grid = static_cast<unsigned>(blocks < 8 * num_sms ? blocks : 8 * num_sms);
+    tg::tg_copy_matrix16<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(src), ld_src,
+                                              static_cast<uint16_t*>(dst), ld_dst, rows, cols);
+    return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_LAUNCH;
+}
+
+// Launch the planned kernel for operands in the tensor memory-access layout.
+template <typename T>
+tg_status_t launch_planned(tg_plan_t pl, const void* A, const void* B, void* C, int64_t M,
+                           int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                           int epilogue, cudaStream_t s, int dev, DeviceState* ds) {
+    switch (pl.kernel) {
+        case TG_KERNEL_PERSISTENT:
+            if (pl.cluster == 2) {
+                if (ds->max_pairs < 1) {  // cannot place a pair: one-CTA tiles instead
+                    plan_persistent(M, N, K, ds->num_sms, kBigBN, kBigStages,
+                                    tg::PersistentCfg<kBigBN, kBigStages>::kSmemBytes, &pl);
+                } else {
+                    return launch_pair<T>(A, B, C, pl, M, N, K, lda, ldb, ldc, epilogue, s,
+                                          ds->max_pairs);
+                }
+            }
+            if (pl.bn == kBigBN)
+                return launch_persistent<kBigBN, kBigStages, T>(A, B, C, pl, M, N, K, lda, ldb,
+                                                               ldc, epilogue, s);
+            return launch_persistent<kMidBN, kMidStages, T>(A, B, C, pl, M, N, K, lda, ldb, ldc,
+                                                           epilogue, s);
+        case TG_KERNEL_SKINNY: {
+            const uint64_t timeout = g_timeout_ns.load();
+            const int32_t inject = g_inject.exchange(0);
+            return tg::skinny_launch<T>(A, B, C, pl, M, N, K, lda, ldb, ldc, epilogue, s, dev,
+                                        ds->num_sms, timeout, inject, encode_2d);
+        }
+        default:
+            return TG_ERR_INVALID_VALUE;
+    }
+}
+
 // C = epi(A·B) for 16-bit element type T (__half or __nv_bfloat16): plan,
-// then launch the planned kernel on `stream`.
+// stage operands the tensor memory-access unit cannot address, launch the
+// planned kernel on `stream`, and copy a staged C back.
 template <typename T>
 tg_status_t gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                       int64_t lda, int64_t ldb, int64_t ldc, int epilogue, void* stream) {
-    tg_status_t st = validate(A, B, C, M, N, K, lda, ldb, ldc, epilogue);
+    tg_status_t st = validate(A, B, C, M, N, K, lda, ldb, ldc, epilogue, /*tma_layout=*/false);
     if (st != TG_OK || M == 0 || N == 0) return st;
     int dev = 0;
     DeviceState* ds = nullptr;
@@ -361,38 +450,37 @@ tg_status_t gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t 
     if (st != TG_OK) return st;
     apply_forced_config(M, N, K, ds->num_sms, &pl);
 
-    switch (pl.kernel) {
-        case TG_KERNEL_FILL: {
-            // +0 has the same (all-zero) bits in fp16 and bf16
-            tg::tg_fill_zero_f16<<<static_cast<unsigned>(pl.grid), 256, 0, s>>>(
-                static_cast<__half*>(C), M, N, ldc);
-            if (cudaGetLastError() != cudaSuccess) return TG_ERR_LAUNCH;
-            return TG_OK;
-        }
-        case TG_KERNEL_PERSISTENT:
-            if (pl.cluster == 2) {
-                if (ds->max_pairs < 1) {  // cannot place a pair: one-CTA tiles instead
-                    plan_persistent(M, N, K, ds->num_sms, kBigBN, kBigStages,
-                                    tg::PersistentCfg<kBigBN, kBigStages>::kSmemBytes, &pl);
-                } else {
-                    return launch_pair<T>(A, B, C, pl, M, N, K, lda, ldb, ldc, epilogue, s,
-                                       ds->max_pairs);
-                }
-            }
-            if (pl.bn == kBigBN)
-                return launch_persistent<kBigBN, kBigStages, T>(A, B, C, pl, M, N, K, lda, ldb, ldc,
-                                                            epilogue, s);
-            return launch_persistent<kMidBN, kMidStages, T>(A, B, C, pl, M, N, K, lda, ldb, ldc,
-                                                        epilogue, s);
-        case TG_KERNEL_SKINNY: {
-            const uint64_t timeout = g_timeout_ns.load();
-            const int32_t inject = g_inject.exchange(0);
-            return tg::skinny_launch<T>(A, B, C, pl, M, N, K, lda, ldb, ldc, epilogue, s, dev,
-                                     ds->num_sms, timeout, inject, encode_2d);
-        }
-        default:
-            return TG_ERR_INVALID_VALUE;
+    if (pl.kernel == TG_KERNEL_FILL) {
+        // +0 has the same (all-zero) bits in fp16 and bf16; any ldc works
+        tg::tg_fill_zero_f16<<<static_cast<unsigned>(pl.grid), 256, 0, s>>>(
+            static_cast<__half*>(C), M, N, ldc);
+        return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_LAUNCH;
     }
+    const bool a_ok = tma_layout_ok(A, lda), b_ok = tma_layout_ok(B, ldb);
+    const bool c_ok = tma_layout_ok(C, ldc);
+    if (a_ok && b_ok && c_ok)
+        return launch_planned<T>(pl, A, B, C, M, N, K, lda, ldb, ldc, epilogue, s, dev, ds);
+
+    // Staging: aligned copies with leading dimensions rounded up to 8.
+    const int64_t lda2 = a_ok ? lda : round_up8(K), ldb2 = b_ok ? ldb : round_up8(N);
+    const int64_t ldc2 = c_ok ? ldc : round_up8(N);
+    auto align256 = [](int64_t b) { return (b + 255) / 256 * 256; };
+    const int64_t bytes_a = a_ok ? 0 : align256(M * lda2 * 2);
+    const int64_t bytes_b = b_ok ? 0 : align256(K * ldb2 * 2);
+    const int64_t bytes_c = c_ok ? 0 : align256(M * ldc2 * 2);
+    void* buf = nullptr;
+    st = staging_buffer(dev, s, static_cast<size_t>(bytes_a + bytes_b + bytes_c), &buf);
+    if (st != TG_OK) return st;
+    char* p = static_cast<char*>(buf);
+    const void* A2 = a_ok ? A : p;
+    const void* B2 = b_ok ? B : p + bytes_a;
+    void* C2 = c_ok ? C : p + bytes_a + bytes_b;
+    if (!a_ok && (st = copy_matrix16(A, lda, p, lda2, M, K, ds->num_sms, s)) != TG_OK) return st;
+    if (!b_ok && (st = copy_matrix16(B, ldb, p + bytes_a, ldb2, K, N, ds->num_sms, s)) != TG_OK)
+        return st;
+    st = launch_planned<T>(pl, A2, B2, C2, M, N, K, lda2, ldb2, ldc2, epilogue, s, dev, ds);
+    if (st != TG_OK || c_ok) return st;
+    return copy_matrix16(C2, ldc2, C, ldc, M, N, ds->num_sms, s);
 }
 
 }  // namespace
