@@ -83,6 +83,15 @@ class Oracle:
         lib.oracle_gemm_bf16_at.restype = ctypes.c_int
         lib.oracle_bf16_from_f64_array.argtypes = [f64p, u16p, i64]
         lib.oracle_f64_from_bf16_array.argtypes = [u16p, f64p, i64]
+        f32p = ctypes.POINTER(ctypes.c_float)
+        vp = ctypes.c_void_p
+        lib.oracle_gemm_ex.argtypes = [ctypes.c_int, ctypes.c_int, u16p, u16p, vp, f64p, i64, i64,
+                                       i64, i64, i64, i64, ctypes.c_int, f32p, u16p, i64]
+        lib.oracle_gemm_ex.restype = ctypes.c_int
+        lib.oracle_gemm_ex_at.argtypes = [ctypes.c_int, ctypes.c_int, u16p, u16p, i64, i64, i64,
+                                          ctypes.c_int, f32p, u16p, i64, i64p, i64p, i64, vp,
+                                          f64p]
+        lib.oracle_gemm_ex_at.restype = ctypes.c_int
         self.lib = lib
         self.path = path
 
@@ -166,6 +175,83 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle gemm_at rejected its arguments")
         return (out16 if dtype == "bf16" else out16.view(np.float16)), out64
+
+
+_FMT = {"f16": 0, "bf16": 1, "f32": 2}
+
+
+def _ex_outputs(out_dtype: str, shape):
+    if out_dtype == "f32":
+        return np.empty(shape, dtype=np.float32)
+    return np.empty(shape, dtype=np.uint16)
+
+
+def _ex_view(C, out_dtype: str):
+    return C.view(np.float16) if out_dtype == "f16" else C
+
+
+def _gemm_ex(self, A, B, M, N, K, relu=False, bias=None, R=None, in_dtype="f16",
+             out_dtype="f16", want_ref=False):
+    """C = out_round(act(A·B + bias[j]) + R[i][j]) (see tgemm_oracle.c).
+
+    A, B, R: float16 arrays or 16-bit patterns of ``in_dtype`` ("f16"/"bf16");
+    bias: float32 vector of N or None; R: M×ldr or None.  Returns C as
+    float16 (out "f16"), bfloat16 bits (out "bf16") or float32 (out "f32").
+    """
+    A = _as_u16(A)
+    B = _as_u16(B)
+    lda = A.shape[1] if A.ndim == 2 else K
+    ldb = B.shape[1] if B.ndim == 2 else N
+    bias_a = None if bias is None else np.ascontiguousarray(np.asarray(bias, dtype=np.float32))
+    R_a = None if R is None else _as_u16(np.asarray(R))
+    ldr = 0 if R_a is None else R_a.shape[1]
+    C = _ex_outputs(out_dtype, (M, N))
+    ref = np.empty((M, N), dtype=np.float64) if want_ref else None
+    rc = self.lib.oracle_gemm_ex(_FMT[in_dtype], _FMT[out_dtype], _ptr(A, ctypes.c_uint16),
+                                 _ptr(B, ctypes.c_uint16), C.ctypes.data_as(ctypes.c_void_p),
+                                 _ptr(ref, ctypes.c_double), M, N, K, lda, ldb, N,
+                                 int(bool(relu)), _ptr(bias_a, ctypes.c_float),
+                                 _ptr(R_a, ctypes.c_uint16), ldr)
+    if rc != 0:
+        raise ValueError("oracle_gemm_ex rejected its arguments")
+    C = _ex_view(C, out_dtype)
+    return (C, ref) if want_ref else C
+
+
+def _gemm_ex_at(self, A, B, K, rows, cols, relu=False, bias=None, R=None, in_dtype="f16",
+                out_dtype="f16"):
+    """Selected elements of gemm_ex; returns (rounded values, fp64 values)."""
+    A = _as_u16(A)
+    B = _as_u16(B)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+    bias_a = None if bias is None else np.ascontiguousarray(np.asarray(bias, dtype=np.float32))
+    R_a = None if R is None else _as_u16(np.asarray(R))
+    ldr = 0 if R_a is None else R_a.shape[1]
+    out = _ex_outputs(out_dtype, rows.size)
+    out64 = np.empty(rows.size, dtype=np.float64)
+    rc = self.lib.oracle_gemm_ex_at(_FMT[in_dtype], _FMT[out_dtype], _ptr(A, ctypes.c_uint16),
+                                    _ptr(B, ctypes.c_uint16), K, A.shape[1], B.shape[1],
+                                    int(bool(relu)), _ptr(bias_a, ctypes.c_float),
+                                    _ptr(R_a, ctypes.c_uint16), ldr, _ptr(rows, ctypes.c_int64),
+                                    _ptr(cols, ctypes.c_int64), rows.size,
+                                    out.ctypes.data_as(ctypes.c_void_p),
+                                    _ptr(out64, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle_gemm_ex_at rejected its arguments")
+    return _ex_view(out, out_dtype), out64
+
+
+Oracle.gemm_ex = _gemm_ex
+Oracle.gemm_ex_at = _gemm_ex_at
+
+
+def gemm_ex(*args, **kw):
+    return default().gemm_ex(*args, **kw)
+
+
+def gemm_ex_at(*args, **kw):
+    return default().gemm_ex_at(*args, **kw)
 
 
 def default() -> Oracle:

@@ -314,3 +314,98 @@ int oracle_gemm_bf16_at(const uint16_t* A, const uint16_t* B, int64_t K, int64_t
     }
     return 0;
 }
+
+/* ========================================================================
+ * Extended epilogue.  The pages show the ReLU epilogue as an element-wise
+ * step on the fp32 accumulator before the final copy ("TileLang：让GPU编程像
+ * Python一样简单的高性能计算新范式", T.Parallel over C_local); the same step
+ * here also adds a per-column bias and a residual matrix and may keep the
+ * result in fp32.  Reading taken (stated in the design notes):
+ *
+ *   C[i][j] = out_round( act( sum_k A[i][k]·B[k][j] + bias[j] ) + R[i][j] )
+ *
+ * with the sum in fp64 (k ascending), bias an fp32 vector over columns (or
+ * absent), R a matrix in the input storage type with row stride ldr (or
+ * absent), act = ReLU or identity, and out_round one rounding to fp16, bf16
+ * or binary32.
+ *   in_fmt:  0 = fp16 inputs (A, B, R), 1 = bf16
+ *   out_fmt: 0 = fp16, 1 = bf16, 2 = fp32 (C is float*)
+ * ======================================================================== */
+
+static double decode16(uint16_t h, int fmt) { return fmt ? g_lut_bf16[h] : g_lut[h]; }
+
+static double ex_value(double s, int64_t i, int64_t j, int relu, const float* bias,
+                       const uint16_t* R, int64_t ldr, int in_fmt)
+{
+    double v = s;
+    if (bias) v += (double)bias[j];
+    v = epi_apply(v, relu);
+    if (R) v += decode16(R[i * ldr + j], in_fmt);
+    return v;
+}
+
+static void ex_store(void* C, int64_t idx, double v, int out_fmt)
+{
+    if (out_fmt == 2) ((float*)C)[idx] = (float)v; /* IEEE binary32, round to nearest even */
+    else if (out_fmt == 1) ((uint16_t*)C)[idx] = oracle_bf16_from_f64(v);
+    else ((uint16_t*)C)[idx] = oracle_f16_from_f64(v);
+}
+
+int oracle_gemm_ex(int in_fmt, int out_fmt, const uint16_t* A, const uint16_t* B, void* C,
+                   double* Cref, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                   int64_t ldc, int relu, const float* bias, const uint16_t* R, int64_t ldr)
+{
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < N || ldc < N) return -1;
+    if (R && ldr < N) return -1;
+    if (in_fmt < 0 || in_fmt > 1 || out_fmt < 0 || out_fmt > 2) return -1;
+    lut_init();
+    lut_bf16_init();
+    int err = 0;
+#pragma omp parallel
+    {
+        double* acc = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+        if (!acc) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < M; ++i) {
+            if (!acc) continue;
+            for (int64_t j = 0; j < N; ++j) acc[j] = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double a = decode16(A[i * lda + k], in_fmt);
+                const uint16_t* brow = B + k * ldb;
+                for (int64_t j = 0; j < N; ++j) acc[j] += a * decode16(brow[j], in_fmt);
+            }
+            for (int64_t j = 0; j < N; ++j) {
+                double v = ex_value(acc[j], i, j, relu, bias, R, ldr, in_fmt);
+                ex_store(C, i * ldc + j, v, out_fmt);
+                if (Cref) Cref[i * N + j] = v;
+            }
+        }
+        free(acc);
+    }
+    return err ? -1 : 0;
+}
+
+int oracle_gemm_ex_at(int in_fmt, int out_fmt, const uint16_t* A, const uint16_t* B, int64_t K,
+                      int64_t lda, int64_t ldb, int relu, const float* bias, const uint16_t* R,
+                      int64_t ldr, const int64_t* rows, const int64_t* cols, int64_t n,
+                      void* out, double* out64)
+{
+    if (K < 0 || lda < K || in_fmt < 0 || in_fmt > 1 || out_fmt < 0 || out_fmt > 2) return -1;
+    lut_init();
+    lut_bf16_init();
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) {
+        const uint16_t* arow = A + rows[t] * lda;
+        const uint16_t* bcol = B + cols[t];
+        double s = 0.0;
+        for (int64_t k = 0; k < K; ++k)
+            s += decode16(arow[k], in_fmt) * decode16(bcol[k * ldb], in_fmt);
+        double v = ex_value(s, rows[t], cols[t], relu, bias, R, ldr, in_fmt);
+        if (out) ex_store(out, t, v, out_fmt);
+        if (out64) out64[t] = v;
+    }
+    return 0;
+}

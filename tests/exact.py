@@ -62,6 +62,14 @@ def rne_bf16(q: Fraction) -> float:
     return rne_binary(q, 8, -126, BF16_MAX)
 
 
+F32_MAX = (Fraction(2) - Fraction(1, 2 ** 23)) * Fraction(2) ** 127
+
+
+def rne_f32(q: Fraction) -> float:
+    """binary32: 24 significant bits, smallest normal 2^-126, largest (2-2^-23)·2^127."""
+    return rne_binary(q, 24, -126, F32_MAX)
+
+
 def bf16_bits_to_float(bits) -> np.ndarray:
     """Decode bfloat16 bit patterns through numpy's binary32 (bf16 is its top half)."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16

@@ -23,7 +23,8 @@ from fractions import Fraction
 
 import numpy as np
 
-from exact import BF16_MAX, bf16_bits_to_float, exact_gemm, frac_of_f16, rne_bf16, rne_f16
+from exact import (BF16_MAX, bf16_bits_to_float, exact_gemm, frac_of_f16, rne_bf16, rne_f16,
+                   rne_f32)
 
 ALL16 = np.arange(65536, dtype=np.uint16)
 
@@ -356,6 +357,99 @@ def pin_bf16_sampled_matches_full(o):
     c = rng.integers(0, N, 300)
     v16, v64 = o.gemm_at(A, B, K, r, c, relu=True, dtype="bf16")
     assert np.array_equal(v16, C[r, c]) and np.array_equal(v64, ref[r, c])
+
+
+# ---------------------------------------------------------------- extended epilogue
+
+def _exact_ex(A, B, relu, bias, R, in_dtype, out_dtype):
+    """Exact rational out_round(act(A·B + bias[j]) + R[i][j]) for tiny inputs."""
+    dec = bf16_bits_to_float if in_dtype == "bf16" else (lambda x: np.asarray(x).astype(np.float64))
+    Ad, Bd = dec(A), dec(B)
+    Rd = None if R is None else dec(R)
+    rne = {"f16": rne_f16, "bf16": rne_bf16, "f32": rne_f32}[out_dtype]
+    M, K = Ad.shape
+    N = Bd.shape[1]
+    out = np.empty((M, N))
+    for i in range(M):
+        for j in range(N):
+            q = sum((Fraction(float(Ad[i, k])) * Fraction(float(Bd[k, j])) for k in range(K)),
+                    Fraction(0))
+            if bias is not None:
+                q += Fraction(float(np.float32(bias[j])))
+            if relu and q < 0:
+                q = Fraction(0)
+            if Rd is not None:
+                q += Fraction(float(Rd[i, j]))
+            out[i, j] = rne(q)
+    return out
+
+
+def _ex_values(C, out_dtype):
+    if out_dtype == "bf16":
+        return bf16_bits_to_float(C)
+    return np.asarray(C).astype(np.float64)
+
+
+def pin_ex_exact_bruteforce(o):
+    rng = np.random.default_rng(41)
+    for in_dtype in ("f16", "bf16"):
+        conv = _f16 if in_dtype == "f16" else _bf16_bits
+        for (M, N, K) in [(3, 5, 7), (4, 4, 16), (1, 6, 2)]:
+            A = conv(rng.normal(0, 1, (M, K)))
+            B = conv(rng.normal(0, 1, (K, N)))
+            R = conv(rng.normal(0, 2, (M, N + 3)))  # ldr = N + 3
+            bias = rng.normal(0, 2, N).astype(np.float32)
+            for out_dtype in ("f16", "bf16", "f32"):
+                for relu in (False, True):
+                    for bb, rr in ((None, None), (bias, None), (None, R), (bias, R)):
+                        want = _exact_ex(A, B, relu, bb, None if rr is None else rr[:, :N],
+                                         in_dtype, out_dtype)
+                        got = _ex_values(o.gemm_ex(A, B, M, N, K, relu=relu, bias=bb, R=rr,
+                                                   in_dtype=in_dtype, out_dtype=out_dtype),
+                                         out_dtype)
+                        assert _same_value(got, want), (in_dtype, out_dtype, relu, bb is None,
+                                                        rr is None)
+
+
+def pin_ex_closed_forms(o):
+    rng = np.random.default_rng(42)
+    M, N = 9, 11
+    bias = rng.normal(0, 3, N).astype(np.float32)
+    R = _f16(rng.normal(0, 3, (M, N)))
+    # K = 0: C = round(act(bias) + R)
+    C0 = o.gemm_ex(np.zeros((M, 0), np.float16), np.zeros((0, N), np.float16), M, N, 0,
+                   relu=True, bias=bias, R=R, out_dtype="f32")
+    want0 = np.maximum(bias.astype(np.float64), 0.0)[None, :] + R.astype(np.float64)
+    assert np.array_equal(C0.astype(np.float64), want0.astype(np.float32).astype(np.float64))
+    # identity B: C = round(A + bias) exactly representable when all are small integers
+    Ai = rng.integers(-8, 9, (M, N))
+    bi = rng.integers(-8, 9, N).astype(np.float32)
+    Ri = rng.integers(-8, 9, (M, N))
+    C1 = o.gemm_ex(Ai.astype(np.float16), np.eye(N, dtype=np.float16), M, N, N, relu=True,
+                   bias=bi, R=Ri.astype(np.float16))
+    assert np.array_equal(C1.astype(np.float64), np.maximum(Ai + bi, 0) + Ri)
+    # no bias, no residual, same output type: the plain product
+    A = _f16(rng.normal(0, 1, (M, 20)))
+    B = _f16(rng.normal(0, 1, (20, N)))
+    assert np.array_equal(o.gemm_ex(A, B, M, N, 20, relu=True).view(np.uint16),
+                          o.gemm(A, B, M, N, 20, relu=True).view(np.uint16))
+
+
+def pin_ex_sampled_matches_full(o):
+    rng = np.random.default_rng(43)
+    M, N, K = 30, 40, 70
+    A = _bf16_bits(rng.normal(0, 1, (M, K)))
+    B = _bf16_bits(rng.normal(0, 1, (K, N)))
+    R = _bf16_bits(rng.normal(0, 1, (M, N + 8)))
+    bias = rng.normal(0, 1, N).astype(np.float32)
+    for out_dtype in ("bf16", "f32"):
+        C, ref = o.gemm_ex(A, B, M, N, K, relu=True, bias=bias, R=R, in_dtype="bf16",
+                           out_dtype=out_dtype, want_ref=True)
+        r = rng.integers(0, M, 200)
+        c = rng.integers(0, N, 200)
+        v, v64 = o.gemm_ex_at(A, B, K, r, c, relu=True, bias=bias, R=R, in_dtype="bf16",
+                              out_dtype=out_dtype)
+        assert np.array_equal(np.asarray(v), np.asarray(C)[r, c]) and np.array_equal(v64, ref[r, c])
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

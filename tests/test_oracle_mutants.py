@@ -45,6 +45,18 @@ MUTANTS = [
      "C[i * ldc + j] = oracle_f16_from_f64(v);"),
     ("bf16_truncating_round", "double n = round_half_even(ldexp(a, 7 - e));",
      "double n = floor(ldexp(a, 7 - e));"),
+    # extended epilogue
+    ("ex_bias_after_relu", "    if (bias) v += (double)bias[j];\n    v = epi_apply(v, relu);",
+     "    v = epi_apply(v, relu);\n    if (bias) v += (double)bias[j];"),
+    ("ex_residual_before_relu",
+     "    v = epi_apply(v, relu);\n    if (R) v += decode16(R[i * ldr + j], in_fmt);",
+     "    if (R) v += decode16(R[i * ldr + j], in_fmt);\n    v = epi_apply(v, relu);"),
+    ("ex_bias_by_row", "if (bias) v += (double)bias[j];", "if (bias) v += (double)bias[i];"),
+    ("ex_residual_ignored", "if (R) v += decode16(R[i * ldr + j], in_fmt);", "(void)R;"),
+    ("ex_residual_row_ignored", "decode16(R[i * ldr + j], in_fmt)",
+     "decode16(R[(i % 1) * ldr + j], in_fmt)"),
+    ("ex_f32_through_f16", "if (out_fmt == 2) ((float*)C)[idx] = (float)v;",
+     "if (out_fmt == 2) ((float*)C)[idx] = (float)oracle_f64_from_f16(oracle_f16_from_f64(v));"),
 ]
 
 
