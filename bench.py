@@ -52,6 +52,7 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-skinny", action="store_true")
     p.add_argument("--no-bf16", action="store_true")
+    p.add_argument("--no-epilogue", action="store_true")
     a = p.parse_args(argv)
     if a.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -404,6 +405,51 @@ def run_ours(args, w, rank, world, local_rank):
                        "kernel_ms_mean": k4, "kernel_ms_min": min(per4),
                        "tflops": flops / (k4 / 1e3) / 1e12, "roofline": roof4}
         del ab, bb, cb
+
+    # ---- extended epilogue on the same shape: bias + ReLU + residual (16-bit
+    # out) and bias + ReLU with fp32 out, through tg_gemm_ex, same method
+    if not args.no_epilogue:
+        rng = np.random.default_rng(w.seed + 101)
+        bias = torch.from_numpy(rng.normal(0.0, 0.5, size=w.N).astype(np.float32)).to(device)
+        resid = torch.empty((w.M, w.N), dtype=torch.float16, device=device).normal_()
+        variants = {"bias_relu_residual_f16": (resid, tg.TG_DTYPE_F16, torch.float16),
+                    "bias_relu_f32": (None, tg.TG_DTYPE_F32, torch.float32)}
+        out["epilogue"] = {"workload": w.name, "entry": "tg_gemm_ex"}
+        for name, (r, odt, tdt) in variants.items():
+            ce = torch.empty((w.M, w.N), dtype=tdt, device=device)
+            ex = tg.tg_epilogue_ex_t(epi, odt, bias.data_ptr(),
+                                     r.data_ptr() if r is not None else None,
+                                     w.N if r is not None else 0)
+
+            def launch5(ce=ce, ex=ex):
+                st = tg.tg_gemm_ex(tg.TG_DTYPE_F16, a.data_ptr(), b.data_ptr(), ce.data_ptr(),
+                                   w.M, w.N, w.K, w.K, w.N, w.N, ex, stream.cuda_stream)
+                if st != tg.TG_OK:
+                    raise tg.TgemmError(st, "tg_gemm_ex")
+
+            for _ in range(args.warmup):
+                launch5()
+            tg.sync_status(stream)
+            n5 = max(50, args.steps // 2)
+            _, per5, _, _ = time_launches(launch5, stream, n5, world, device)
+            tg.sync_status(stream)
+            k5 = statistics.mean(per5)
+            # bytes the epilogue adds: the residual read, the wider output
+            extra = (w.M * w.N * 2 if r is not None else 0) + w.N * 4 + \
+                (w.M * w.N * 2 if odt == tg.TG_DTYPE_F32 else 0)
+            ent = {"launches": n5, "kernel_ms_mean": k5, "kernel_ms_min": min(per5),
+                   "extra_bytes": extra, "vs_plain": kernel_ms / k5}
+            if plan.kernel == tg.TG_KERNEL_PERSISTENT:
+                ach = flops / (k5 / 1e3) / 1e12
+                ent["roofline"] = {"bound": "tensor", "achieved": ach, "peak": tf_peak,
+                                   "unit": "TFLOP/s", "frac": ach / tf_peak}
+            else:
+                ach = (w.min_bytes + extra) / (k5 / 1e3) / 1e9
+                ent["roofline"] = {"bound": "hbm", "achieved": ach, "peak": hbm_peak,
+                                   "unit": "GB/s", "frac": ach / hbm_peak}
+            out["epilogue"][name] = ent
+            del ce
+        del bias, resid
 
     # ---- end to end through the public API, host buffers in and out
     if not args.no_e2e:

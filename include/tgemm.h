@@ -106,6 +106,64 @@ tg_status_t tg_gemm_bf16(const void* A, const void* B, void* C,
                          int64_t lda, int64_t ldb, int64_t ldc,
                          int epilogue, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Extended epilogue: bias, residual, fp32 output.
+ * ------------------------------------------------------------------------ */
+
+typedef enum {
+    TG_DTYPE_F16 = 0,  /* IEEE binary16               */
+    TG_DTYPE_BF16 = 1, /* bfloat16                    */
+    TG_DTYPE_F32 = 2   /* IEEE binary32 (output only) */
+} tg_dtype_t;
+
+typedef struct {
+    int32_t activation;   /* tg_epilogue_t: TG_EPI_NONE or TG_EPI_RELU              */
+    int32_t out_dtype;    /* tg_dtype_t of C: the input type, or TG_DTYPE_F32       */
+    const float* bias;    /* device, N fp32 values (one per column of C), or NULL  */
+    const void* residual; /* device, M×N of the input type, row stride ldr, or NULL */
+    int64_t ldr;          /* row stride of residual in elements (≥ N when present) */
+} tg_epilogue_ex_t;
+
+/*
+ * tg_gemm_ex — C = out( act( A·B + bias ) + R ), asynchronous on `stream`:
+ *
+ *   C[i][j] = out( act( sum_k A[i][k]·B[k][j] + bias[j] ) + R[i][j] )
+ *
+ * with the sum accumulated in fp32, bias (if given) added to the fp32
+ * accumulator, act = identity or ReLU, the residual R (if given, stored in
+ * the input type) added after the activation in fp32, and one rounding at
+ * the end: round-to-nearest-even to the input type, or none for fp32 output.
+ * It widens the element-wise epilogue of the pages — the ReLU taken on the
+ * float32 accumulator before the final copy ("TileLang：让GPU编程像Python一样
+ * 简单的高性能计算新范式", the T.Parallel loop over C_local; "5分钟上手TileLang",
+ * section "安装与第一个内核", whose quickstart carries a fused epilogue) — to
+ * the bias, residual and output-type variants a layer's GEMM needs; the pages
+ * define none of the three, so their placement (bias before, residual after
+ * the activation) is this library's reading.
+ *
+ * in_dtype  TG_DTYPE_F16 or TG_DTYPE_BF16: the type of A, B and R.
+ * A, B, M, N, K, lda, ldb, stream  as for tg_gemm_f16 (any row-major layout;
+ *     operands the tensor memory-access unit cannot address are staged).
+ * C   device pointer of type epi->out_dtype, row-major M×N, row stride ldc
+ *     elements (ldc ≥ N); aligned to its element size.  An fp32 C not
+ *     16-byte aligned or with ldc not a multiple of 4 is computed in the
+ *     staging buffer and copied back.
+ * epi NULL means { TG_EPI_NONE, in_dtype, NULL, NULL, 0 } (plain GEMM).
+ *     bias must be 4-byte aligned, residual aligned to its element.  R may be
+ *     the same buffer as C (same pointer, ldr == ldc, same 16-bit type): each
+ *     element is read before it is overwritten.  Any other overlap of R or
+ *     bias with C is undefined.
+ * K == 0: C = out(act(bias) + R) (the product is +0).
+ * Errors: TG_ERR_INVALID_VALUE for an unknown dtype or activation, an output
+ * type that is neither the input type nor fp32, ldr < N, or a NULL C, A or B
+ * where needed; TG_ERR_MISALIGNED for a pointer not aligned to its element;
+ * otherwise as tg_gemm_f16.
+ */
+tg_status_t tg_gemm_ex(int32_t in_dtype, const void* A, const void* B, void* C,
+                       int64_t M, int64_t N, int64_t K,
+                       int64_t lda, int64_t ldb, int64_t ldc,
+                       const tg_epilogue_ex_t* epi, void* stream);
+
 /*
  * tg_sync_status — wait for `stream`, then report (and clear) a device-side
  * timeout recorded by any libtgemm kernel on the current device since the

@@ -99,6 +99,43 @@ def test_argument_checks_before_any_cuda_call(tg, args, want):
         assert st == want, (args, tg.tg_status_string(st))
 
 
+@pytest.mark.parametrize("in_dt,out_dt,bias,resid,ldr,K,want", [
+    # (input type, output type, bias address, residual address, ldr, K, status)
+    (3, 0, 0, 0, 0, 4, 1),                  # unknown input type
+    (2, 2, 0, 0, 0, 4, 1),                  # fp32 is an output type only
+    (0, 1, 0, 0, 0, 4, 1),                  # fp16 in, bf16 out: not offered
+    (1, 0, 0, 0, 0, 4, 1),                  # bf16 in, fp16 out: not offered
+    (0, 0, 0, GOOD, 3, 4, 1),               # ldr < N
+    (0, 0, GOOD + 2, 0, 0, 4, 2),           # bias not 4-byte aligned
+    (0, 0, 0, GOOD + 1, 8, 4, 2),           # residual not element-aligned
+    (0, 0, GOOD + 4, GOOD + 2, 9, 4, None),  # scalar-path bias and residual: accepted
+    (1, 2, GOOD, GOOD, 8, 4, None),         # bf16 in, fp32 out
+    (0, 2, GOOD, GOOD, 8, 0, None),         # K == 0 with bias and residual
+])
+def test_gemm_ex_argument_checks(tg, in_dt, out_dt, bias, resid, ldr, K, want):
+    epi = tg.tg_epilogue_ex_t(0, out_dt, bias or None, resid or None, ldr)
+    st = tg.tg_gemm_ex(in_dt, GOOD, GOOD, GOOD, 4, 4, K, 8, 8, 8, epi, None)
+    if want is None:
+        if _has_gpu():
+            pytest.skip("valid call would launch")
+        assert st == tg.TG_ERR_UNSUPPORTED_DEVICE
+    else:
+        assert st == want, tg.tg_status_string(st)
+
+
+def test_gemm_ex_fp32_output_alignment(tg):
+    # an fp32 C must be aligned to its 4-byte element; a 2-byte offset is not
+    epi = tg.tg_epilogue_ex_t(0, tg.TG_DTYPE_F32, None, None, 0)
+    assert tg.tg_gemm_ex(0, GOOD, GOOD, GOOD + 2, 4, 4, 4, 8, 8, 8, epi, None) == \
+        tg.TG_ERR_MISALIGNED
+    # bad activation and a NULL epilogue (plain GEMM) take the usual checks
+    epi = tg.tg_epilogue_ex_t(5, 0, None, None, 0)
+    assert tg.tg_gemm_ex(0, GOOD, GOOD, GOOD, 4, 4, 4, 8, 8, 8, epi, None) == \
+        tg.TG_ERR_INVALID_VALUE
+    assert tg.tg_gemm_ex(0, GOOD, GOOD, 0, 4, 4, 4, 8, 8, 8, None, None) == \
+        tg.TG_ERR_INVALID_VALUE
+
+
 def test_noalloc_keeps_the_tma_layout_rule(tg):
     # the entry point without allocation has no staging buffer
     st = tg.tg_gemm_f16_noalloc(GOOD, GOOD, GOOD, 4, 4, 4, 12, 8, 8, 0, None)

@@ -27,6 +27,10 @@ TG_ERR_LAUNCH = 4
 TG_ERR_NO_MEMORY = 5
 TG_ERR_TIMEOUT = 6
 
+TG_DTYPE_F16 = 0
+TG_DTYPE_BF16 = 1
+TG_DTYPE_F32 = 2
+
 TG_KERNEL_NONE = 0
 TG_KERNEL_FILL = 1
 TG_KERNEL_PERSISTENT = 2
@@ -36,7 +40,7 @@ TG_KERNEL_SKINNY = 3
 EXPORTS = (
     "tg_gemm_f16", "tg_sync_status", "tg_status_string", "tg_version", "tg_plan_f16",
     "tg_tile_coord", "tg_ring_bytes", "tg_debug_set_wait_timeout_ns", "tg_debug_inject",
-    "tg_gemm_f16_noalloc", "tg_gemm_bf16",
+    "tg_gemm_f16_noalloc", "tg_gemm_bf16", "tg_gemm_ex",
 )
 
 #: bytes of the library's fixed scratch array used by tg_gemm_f16_noalloc
@@ -59,6 +63,13 @@ class tg_plan_t(ctypes.Structure):
         return {name: getattr(self, name) for name, _ in self._fields_}
 
 
+class tg_epilogue_ex_t(ctypes.Structure):
+    _fields_ = [
+        ("activation", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
+        ("bias", ctypes.c_void_p), ("residual", ctypes.c_void_p), ("ldr", ctypes.c_int64),
+    ]
+
+
 _i64 = ctypes.c_int64
 _vp = ctypes.c_void_p
 _lib = None
@@ -79,6 +90,9 @@ def _L():
     lib.tg_gemm_f16.restype = ctypes.c_int
     lib.tg_gemm_bf16.argtypes = lib.tg_gemm_f16.argtypes
     lib.tg_gemm_bf16.restype = ctypes.c_int
+    lib.tg_gemm_ex.argtypes = [ctypes.c_int32, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64,
+                               ctypes.POINTER(tg_epilogue_ex_t), _vp]
+    lib.tg_gemm_ex.restype = ctypes.c_int
     lib.tg_sync_status.argtypes = [_vp]
     lib.tg_sync_status.restype = ctypes.c_int
     lib.tg_status_string.argtypes = [ctypes.c_int]
@@ -122,6 +136,13 @@ def tg_gemm_bf16(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: 
                  epilogue: int, stream: int | None) -> int:
     """The bfloat16 entry point with integer device pointers; returns the status code."""
     return _L().tg_gemm_bf16(A, B, C, M, N, K, lda, ldb, ldc, epilogue, stream or None)
+
+
+def tg_gemm_ex(in_dtype: int, A: int, B: int, C: int, M: int, N: int, K: int, lda: int,
+               ldb: int, ldc: int, epi: tg_epilogue_ex_t | None, stream: int | None) -> int:
+    """C = out(act(A·B + bias) + R) with integer device pointers; returns the status code."""
+    return _L().tg_gemm_ex(in_dtype, A, B, C, M, N, K, lda, ldb, ldc,
+                           ctypes.byref(epi) if epi is not None else None, stream or None)
 
 
 def tg_sync_status(stream: int | None) -> int:
@@ -200,13 +221,17 @@ def _ld(t) -> int:
     return max(8, (int(t.shape[1]) + 7) // 8 * 8)
 
 
-def gemm(a, b, relu: bool = False, out=None, stream=None):
-    """C = epi(a @ b) for CUDA float16 (or bfloat16) tensors a (M×K) and b (K×N).
+def gemm(a, b, relu: bool = False, out=None, stream=None, *, bias=None, residual=None,
+         out_dtype=None):
+    """C = out(act(a @ b + bias) + residual) for CUDA float16 (or bfloat16)
+    tensors a (M×K) and b (K×N); act = ReLU if ``relu`` else identity.
 
-    Row-major views with a row stride that is a multiple of 8 elements and
-    16-byte aligned storage are accepted; ``out`` (M×N, same rules) is written
-    in place when given.  Runs on ``stream`` (default: torch's current stream
-    of a's device).
+    bias: optional float32 tensor of N elements (added to the fp32
+    accumulator before the activation).  residual: optional M×N tensor of a's
+    dtype (added after the activation; may be ``out`` itself).  out_dtype:
+    a's dtype (default) or torch.float32.  Any row-major 2-D views are
+    accepted (unit column stride); ``out`` (M×N) is written in place when
+    given.  Runs on ``stream`` (default: torch's current stream of a's device).
     """
     import torch
     _check_operand(a, "a")
@@ -219,19 +244,49 @@ def gemm(a, b, relu: bool = False, out=None, stream=None):
         raise ValueError("a and b must be CUDA tensors on the same device")
     if a.dtype != b.dtype:
         raise TypeError(f"a and b must share a dtype, got {a.dtype} and {b.dtype}")
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else a.dtype
+    if out_dtype not in (a.dtype, torch.float32):
+        raise TypeError(f"out_dtype must be {a.dtype} or torch.float32, got {out_dtype}")
     if out is None:
-        out = torch.empty((M, N), dtype=a.dtype, device=a.device)
+        out = torch.empty((M, N), dtype=out_dtype, device=a.device)
     else:
-        _check_operand(out, "out")
-        if tuple(out.shape) != (M, N) or out.device != a.device or out.dtype != a.dtype:
-            raise ValueError("out must be M×N on a's device with a's dtype")
-    entry = tg_gemm_bf16 if a.dtype == torch.bfloat16 else tg_gemm_f16
+        if out.dtype != out_dtype or out.dim() != 2 or tuple(out.shape) != (M, N) \
+                or out.device != a.device:
+            raise ValueError("out must be M×N on a's device with dtype out_dtype")
+        if N > 1 and out.stride(1) != 1:
+            raise ValueError("out must be row-major (unit column stride)")
+    extended = bias is not None or residual is not None or out_dtype == torch.float32
+    if bias is not None:
+        if not isinstance(bias, torch.Tensor) or bias.dtype != torch.float32 \
+                or bias.device != a.device or bias.numel() != N or bias.dim() != 1 \
+                or (N > 1 and bias.stride(0) != 1):
+            raise ValueError("bias must be a contiguous float32 CUDA tensor of N elements")
+    if residual is not None:
+        _check_operand(residual, "residual")
+        if residual.dtype != a.dtype or tuple(residual.shape) != (M, N) \
+                or residual.device != a.device:
+            raise ValueError("residual must be M×N on a's device with a's dtype")
+    in_code = TG_DTYPE_BF16 if a.dtype == torch.bfloat16 else TG_DTYPE_F16
     with torch.cuda.device(a.device):
         s = stream if stream is not None else torch.cuda.current_stream(a.device)
-        st = entry(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K, _ld(a), _ld(b),
-                   _ld(out), TG_EPI_RELU if relu else TG_EPI_NONE, s.cuda_stream)
+        if extended:
+            epi = tg_epilogue_ex_t(
+                TG_EPI_RELU if relu else TG_EPI_NONE,
+                TG_DTYPE_F32 if out_dtype == torch.float32 else in_code,
+                bias.data_ptr() if bias is not None else None,
+                residual.data_ptr() if residual is not None else None,
+                _ld(residual) if residual is not None else 0)
+            st = tg_gemm_ex(in_code, a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K,
+                            _ld(a), _ld(b), _ld(out), epi, s.cuda_stream)
+            what = "tg_gemm_ex"
+        else:
+            entry = tg_gemm_bf16 if in_code == TG_DTYPE_BF16 else tg_gemm_f16
+            st = entry(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K, _ld(a), _ld(b),
+                       _ld(out), TG_EPI_RELU if relu else TG_EPI_NONE, s.cuda_stream)
+            what = entry.__name__
     if st != TG_OK:
-        raise TgemmError(st)
+        raise TgemmError(st, what)
     return out
 
 

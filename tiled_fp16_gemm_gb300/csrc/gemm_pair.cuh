@@ -27,6 +27,7 @@
 
 #include <cuda_fp16.h>
 
+#include "epilogue.cuh"
 #include "gemm_persistent.cuh"
 #include "sm103_ptx.cuh"
 #include "tile_schedule.h"
@@ -246,36 +247,15 @@ __global__ void __launch_bounds__(192, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * acc, 0));
                 }
-                uint32_t h[32];
+                float x[64];
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    float x0 = __uint_as_float(v0[2 * t]), x1 = __uint_as_float(v0[2 * t + 1]);
-                    float y0 = __uint_as_float(v1[2 * t]), y1 = __uint_as_float(v1[2 * t + 1]);
-                    if (p.relu) {
-                        x0 = relu_f32(x0);
-                        x1 = relu_f32(x1);
-                        y0 = relu_f32(y0);
-                        y1 = relu_f32(y1);
-                    }
-                    h[t] = Elem16<T>::pack2(x0, x1);
-                    h[16 + t] = Elem16<T>::pack2(y0, y1);
+                for (int t = 0; t < 32; ++t) {
+                    x[t] = __uint_as_float(v0[t]);
+                    x[32 + t] = __uint_as_float(v1[t]);
                 }
-                if (lane == 0) bulk_wait_group_read<1>();
-                __syncwarp();
-                const uint32_t cb = cbuf + static_cast<uint32_t>(buf) * Cfg::kCBuf;
-                const uint32_t row_addr = cb + static_cast<uint32_t>(lane) * 128u;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st_shared_v4(row_addr + ((static_cast<uint32_t>(c) ^ (lane & 7u)) << 4),
-                                 h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (row0 < p.M && n0 + 64 * j < p.N)
-                        tma_store_2d_hint(&tmC, cb, n0 + 64 * j, row0, c_policy);
-                    bulk_commit_group();
-                }
-                buf ^= 1;
+                epilogue_math<T>(x, p.e, p.relu, row0 + lane, n0 + 64 * j, p.M, p.N);
+                epilogue_store<T>(x, cbuf, buf, &tmC, c_policy, row0, n0 + 64 * j, p.M, p.N, lane,
+                                  p.out_f32 != 0);
             }
         }
         if (lane == 0) bulk_wait_group<0>();

@@ -13,8 +13,9 @@
 //               releases ring slots with tcgen05.commit -> empty[s] and hands a
 //               finished accumulator to the epilogue via tmem_full[a].
 //   warps 2..5  epilogue: tcgen05.ld of 32 rows each (TMEM lane quarter =
-//               warp % 4), ReLU on the fp32 value, round to fp16, stage in a
-//               128-byte-swizzled shared buffer, TMA store; tmem_empty[a]
+//               warp % 4), bias / ReLU / residual on the fp32 value, round
+//               to the output type, stage in a 128-byte-swizzled shared
+//               buffer, TMA store (epilogue.cuh); tmem_empty[a]
 //               returns the accumulator to the MMA warp, so the epilogue of
 //               tile t overlaps the main loop of tile t+1.
 //
@@ -28,6 +29,7 @@
 
 #include <cuda_fp16.h>
 
+#include "epilogue.cuh"
 #include "sm103_ptx.cuh"
 #include "tile_schedule.h"
 
@@ -44,6 +46,8 @@ struct PersistentParams {
     int32_t relu;
     int32_t inject;  // 1: withhold the first tmem_full signal (fault-path test)
     uint64_t timeout_ns;
+    EpilogueArgs e;       // bias / residual (null: none)
+    int32_t out_f32 = 0;  // 1: C is fp32 (tensor map with 32×32 boxes)
 };
 
 enum : unsigned int { kRoleProducer = 1u, kRoleMma = 2u, kRoleEpilogue = 4u, kRoleDrain = 8u };
@@ -257,37 +261,15 @@ __global__ void __launch_bounds__(192, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
                 }
-                uint32_t h[32];
+                float x[64];
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    float x0 = __uint_as_float(v0[2 * t]), x1 = __uint_as_float(v0[2 * t + 1]);
-                    float y0 = __uint_as_float(v1[2 * t]), y1 = __uint_as_float(v1[2 * t + 1]);
-                    if (p.relu) {
-                        x0 = relu_f32(x0);
-                        x1 = relu_f32(x1);
-                        y0 = relu_f32(y0);
-                        y1 = relu_f32(y1);
-                    }
-                    h[t] = Elem16<T>::pack2(x0, x1);
-                    h[16 + t] = Elem16<T>::pack2(y0, y1);
+                for (int t = 0; t < 32; ++t) {
+                    x[t] = __uint_as_float(v0[t]);
+                    x[32 + t] = __uint_as_float(v1[t]);
                 }
-                // the buffer written two stores ago must have been read out
-                if (lane == 0) bulk_wait_group_read<1>();
-                __syncwarp();
-                const uint32_t cb = cbuf + static_cast<uint32_t>(buf) * Cfg::kCBuf;
-                const uint32_t row_addr = cb + static_cast<uint32_t>(lane) * 128u;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    st_shared_v4(row_addr + ((static_cast<uint32_t>(c) ^ (lane & 7u)) << 4),
-                                 h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (row0 < p.M && n0 + 64 * j < p.N)
-                        tma_store_2d_hint(&tmC, cb, n0 + 64 * j, row0, c_policy);
-                    bulk_commit_group();
-                }
-                buf ^= 1;
+                epilogue_math<T>(x, p.e, p.relu, row0 + lane, n0 + 64 * j, p.M, p.N);
+                epilogue_store<T>(x, cbuf, buf, &tmC, c_policy, row0, n0 + 64 * j, p.M, p.N, lane,
+                                  p.out_f32 != 0);
             }
         }
         if (lane == 0) bulk_wait_group<0>();
@@ -313,23 +295,44 @@ __global__ void tg_fill_zero_f16(__half* C, int64_t M, int64_t N, int64_t ldc) {
     }
 }
 
-// Copy a rows×cols matrix of 16-bit elements between two row-major layouts
-// with any leading dimensions (used to move operands whose layout the tensor
-// memory-access unit cannot address into an aligned staging buffer, and a
-// result back out of one).  Each thread moves 8 consecutive elements of a row
-// with 2-byte accesses; consecutive threads take consecutive chunks, so every
-// warp reads and writes contiguous runs.
-__global__ void tg_copy_matrix16(const uint16_t* __restrict__ src, int64_t ld_src,
-                                 uint16_t* __restrict__ dst, int64_t ld_dst, int64_t rows,
-                                 int64_t cols) {
+// K == 0 with a bias, a residual or an fp32 output: the product is the empty
+// sum (+0), so C = out(act(+0 + bias[j]) + R[i][j]) element by element.
+template <typename T>
+__global__ void tg_epilogue_only(void* C, int64_t ldc, int32_t out_f32, EpilogueArgs e,
+                                 int32_t relu, int64_t M, int64_t N) {
+    const int64_t total = M * N;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / N, c = i - r * N;
+        float v = 0.0f;
+        if (e.bias != nullptr) v += e.bias[c];
+        if (relu) v = relu_f32(v);
+        if (e.resid != nullptr)
+            v += Elem16<T>::to_float(static_cast<const T*>(e.resid)[r * e.ldr + c]);
+        if (out_f32)
+            static_cast<float*>(C)[r * ldc + c] = v;
+        else
+            static_cast<T*>(C)[r * ldc + c] = Elem16<T>::from_float(v);
+    }
+}
+
+// Copy a rows×cols matrix of 2- or 4-byte elements between two row-major
+// layouts with any leading dimensions (used to move operands whose layout the
+// tensor memory-access unit cannot address into an aligned staging buffer,
+// and a result back out of one).  Each thread moves 8 consecutive elements
+// of a row with element-sized accesses; consecutive threads take consecutive
+// chunks, so every warp reads and writes contiguous runs.
+template <typename E>
+__global__ void tg_copy_matrix(const E* __restrict__ src, int64_t ld_src, E* __restrict__ dst,
+                               int64_t ld_dst, int64_t rows, int64_t cols) {
     const int64_t chunks_per_row = (cols + 7) / 8;
     const int64_t total = rows * chunks_per_row;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t r = i / chunks_per_row;
         const int64_t c0 = (i - r * chunks_per_row) * 8;
-        const uint16_t* s = src + r * ld_src + c0;
-        uint16_t* d = dst + r * ld_dst + c0;
+        const E* s = src + r * ld_src + c0;
+        E* d = dst + r * ld_dst + c0;
         const int n = cols - c0 < 8 ? static_cast<int>(cols - c0) : 8;
 #pragma unroll
         for (int j = 0; j < 8; ++j)

@@ -24,6 +24,9 @@
 //            flags of CTAs c+1 .. c_last holding the rest of the tile, then
 //            adds their partials in that order (k order), applies the
 //            epilogue and writes C.  No barrier spans several warps.
+// The epilogue (bias, ReLU, residual, output type) is applied per element by
+// the thread holding column n: C[m][n] = out(act(acc + bias[n]) + R[m][n]),
+// with plain stores (consecutive threads write consecutive n).
 // The summation order is fixed by the sizes alone, so results are
 // deterministic.  Owners only wait on higher-numbered CTAs, which write their
 // partials from their first segment, so the waits form no cycle; the launch
@@ -80,6 +83,8 @@ struct SkinnyParams {
     float* ws;
     uint32_t* flags;
     uint32_t epoch;
+    EpilogueArgs e;       // bias / residual (null: none)
+    int32_t out_f32 = 0;  // 1: C is fp32
 };
 
 __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -332,12 +337,24 @@ __global__ void __launch_bounds__(192, 1)
                         for (int i = 0; i < 16; ++i) v[i] += __ldcg(slot + (16 * c + i) * 128 + n_local);
                     }
                     if (n < p.N) {
+                        // C[m][n] = out(act(acc + bias[n]) + R[m][n]): this
+                        // thread holds column n of rows 16c .. 16c + 15.
+                        const float bias_n = p.e.bias != nullptr ? __ldg(p.e.bias + n) : 0.0f;
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const int m = 16 * c + i;
                             if (m < p.M) {
-                                const float x = p.relu ? relu_f32(v[i]) : v[i];
-                                static_cast<T*>(p.C)[static_cast<int64_t>(m) * p.ldc + n] = Elem16<T>::from_float(x);
+                                float x = v[i];
+                                if (p.e.bias != nullptr) x += bias_n;
+                                if (p.relu) x = relu_f32(x);
+                                if (p.e.resid != nullptr)
+                                    x += Elem16<T>::to_float(static_cast<const T*>(
+                                        p.e.resid)[static_cast<int64_t>(m) * p.e.ldr + n]);
+                                const int64_t off = static_cast<int64_t>(m) * p.ldc + n;
+                                if (p.out_f32)
+                                    static_cast<float*>(p.C)[off] = x;
+                                else
+                                    static_cast<T*>(p.C)[off] = Elem16<T>::from_float(x);
                             }
                         }
                     }
@@ -470,7 +487,7 @@ using EncodeFn = bool (*)(CUtensorMap*, const void*, uint64_t, uint64_t, uint64_
 template <typename T>
 inline tg_status_t skinny_launch(const void* A, const void* B, void* C, const tg_plan_t& pl,
                                  int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
-                                 int64_t ldc, int epilogue, cudaStream_t stream, int dev,
+                                 int64_t ldc, const EpilogueSpec& ep, cudaStream_t stream, int dev,
                                  int64_t max_ctas, uint64_t timeout_ns, int32_t inject,
                                  EncodeFn encode) {
     const int64_t Mp = pl.mma_n;
@@ -522,7 +539,9 @@ inline tg_status_t skinny_launch(const void* A, const void* B, void* C, const tg
     prm.tiles_n = static_cast<int32_t>(pl.tiles_n);
     prm.k_blocks = static_cast<int32_t>(pl.k_blocks);
     prm.total_units = pl.tiles_n * pl.k_blocks;
-    prm.relu = epilogue == TG_EPI_RELU ? 1 : 0;
+    prm.relu = ep.relu;
+    prm.e = ep.e;
+    prm.out_f32 = ep.out_f32;
     prm.inject = inject;
     prm.timeout_ns = timeout_ns;
     prm.C = C;

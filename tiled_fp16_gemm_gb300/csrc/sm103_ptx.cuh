@@ -272,6 +272,7 @@ struct Elem16<__half> {
         return *reinterpret_cast<uint32_t*>(&h);
     }
     __device__ static __forceinline__ __half from_float(float x) { return __float2half_rn(x); }
+    __device__ static __forceinline__ float to_float(__half x) { return __half2float(x); }
 };
 
 template <>
@@ -283,6 +284,9 @@ struct Elem16<__nv_bfloat16> {
     }
     __device__ static __forceinline__ __nv_bfloat16 from_float(float x) {
         return __float2bfloat16_rn(x);
+    }
+    __device__ static __forceinline__ float to_float(__nv_bfloat16 x) {
+        return __bfloat162float(x);
     }
 };
 

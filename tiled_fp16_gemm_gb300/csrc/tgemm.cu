@@ -217,19 +217,21 @@ bool encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer
     return r == CUDA_SUCCESS;
 }
 
-// A, B and C maps of the pair / one-CTA kernels.
+// A, B and C maps of the pair / one-CTA kernels.  C: 32 rows × 128 bytes per
+// box (64 16-bit or 32 fp32 elements).
 template <typename T>
 bool encode_abc(CUtensorMap* tmA, CUtensorMap* tmB, CUtensorMap* tmC, const void* A,
                 const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
-                int64_t ldc) {
+                int64_t ldc, bool out_f32) {
     constexpr CUtensorMapDataType dt = tensor_map_type<T>();
     return encode_2d(tmA, A, K, M, lda * 2, 64, 128, dt) &&
            encode_2d(tmB, B, N, K, ldb * 2, 64, 64, dt) &&
-           encode_2d(tmC, C, N, M, ldc * 2, 64, 32, dt);
+           (out_f32 ? encode_2d(tmC, C, N, M, ldc * 4, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)
+                    : encode_2d(tmC, C, N, M, ldc * 2, 64, 32, dt));
 }
 
 tg::PersistentParams persistent_params(const tg_plan_t& pl, int64_t M, int64_t N, int64_t K,
-                                       int epilogue) {
+                                       const tg::EpilogueSpec& ep) {
     tg::PersistentParams prm;
     prm.M = static_cast<int32_t>(M);
     prm.N = static_cast<int32_t>(N);
@@ -239,19 +241,22 @@ tg::PersistentParams persistent_params(const tg_plan_t& pl, int64_t M, int64_t N
     prm.num_tiles = static_cast<int32_t>(pl.num_tiles);
     prm.k_blocks = static_cast<int32_t>(pl.k_blocks);
     prm.group_m = pl.group_m;
-    prm.relu = epilogue == TG_EPI_RELU ? 1 : 0;
+    prm.relu = ep.relu;
     prm.inject = g_inject.exchange(0);
     prm.timeout_ns = g_timeout_ns.load();
+    prm.e = ep.e;
+    prm.out_f32 = ep.out_f32;
     return prm;
 }
 
 template <int BN, int STAGES, typename T>
 tg_status_t launch_persistent(const void* A, const void* B, void* C, const tg_plan_t& pl,
                               int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
-                              int64_t ldc, int epilogue, cudaStream_t stream) {
+                              int64_t ldc, const tg::EpilogueSpec& ep, cudaStream_t stream) {
     CUtensorMap tmA, tmB, tmC;
-    if (!encode_abc<T>(&tmA, &tmB, &tmC, A, B, C, M, N, K, lda, ldb, ldc)) return TG_ERR_LAUNCH;
-    const tg::PersistentParams prm = persistent_params(pl, M, N, K, epilogue);
+    if (!encode_abc<T>(&tmA, &tmB, &tmC, A, B, C, M, N, K, lda, ldb, ldc, ep.out_f32 != 0))
+        return TG_ERR_LAUNCH;
+    const tg::PersistentParams prm = persistent_params(pl, M, N, K, ep);
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
@@ -271,11 +276,12 @@ tg_status_t launch_persistent(const void* A, const void* B, void* C, const tg_pl
 // holds at once (the launch is persistent, so no pair waits for another).
 template <typename T>
 tg_status_t launch_pair(const void* A, const void* B, void* C, const tg_plan_t& pl, int64_t M,
-                        int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int epilogue,
-                        cudaStream_t stream, int max_pairs) {
+                        int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                        const tg::EpilogueSpec& ep, cudaStream_t stream, int max_pairs) {
     CUtensorMap tmA, tmB, tmC;
-    if (!encode_abc<T>(&tmA, &tmB, &tmC, A, B, C, M, N, K, lda, ldb, ldc)) return TG_ERR_LAUNCH;
-    const tg::PersistentParams prm = persistent_params(pl, M, N, K, epilogue);
+    if (!encode_abc<T>(&tmA, &tmB, &tmC, A, B, C, M, N, K, lda, ldb, ldc, ep.out_f32 != 0))
+        return TG_ERR_LAUNCH;
+    const tg::PersistentParams prm = persistent_params(pl, M, N, K, ep);
     int64_t pairs = pl.grid / 2;
     if (pairs > max_pairs) pairs = max_pairs;
     cudaLaunchAttribute attr[1];
@@ -389,13 +395,20 @@ tg_status_t staging_buffer(int dev, cudaStream_t s, size_t bytes, void** out) {
     return TG_OK;
 }
 
-tg_status_t copy_matrix16(const void* src, int64_t ld_src, void* dst, int64_t ld_dst,
-                          int64_t rows, int64_t cols, int num_sms, cudaStream_t s) {
+// Copy a rows×cols matrix of `elem_bytes` (2 or 4) byte elements.
+tg_status_t copy_matrix(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows,
+                        int64_t cols, int elem_bytes, int num_sms, cudaStream_t s) {
     const int64_t chunks = rows * ((cols + 7) / 8);
     const int64_t blocks = (chunks + 255) / 256;
     const unsigned grid = static_cast<unsigned>(blocks < 8 * num_sms ? blocks : 8 * num_sms);
-    tg::tg_copy_matrix16<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(src), ld_src,
-                                              static_cast<uint16_t*>(dst), ld_dst, rows, cols);
+    if (elem_bytes == 4)
+        tg::tg_copy_matrix<uint32_t><<<grid, 256, 0, s>>>(static_cast<const uint32_t*>(src),
+                                                          ld_src, static_cast<uint32_t*>(dst),
+                                                          ld_dst, rows, cols);
+    else
+        tg::tg_copy_matrix<uint16_t><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(src),
+                                                          ld_src, static_cast<uint16_t*>(dst),
+                                                          ld_dst, rows, cols);
     return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_LAUNCH;
 }
 
@@ -403,7 +416,7 @@ tg_status_t copy_matrix16(const void* src, int64_t ld_src, void* dst, int64_t ld
 template <typename T>
 tg_status_t launch_planned(tg_plan_t pl, const void* A, const void* B, void* C, int64_t M,
                            int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
-                           int epilogue, cudaStream_t s, int dev, DeviceState* ds) {
+                           const tg::EpilogueSpec& ep, cudaStream_t s, int dev, DeviceState* ds) {
     switch (pl.kernel) {
         case TG_KERNEL_PERSISTENT:
             if (pl.cluster == 2) {
@@ -411,19 +424,19 @@ tg_status_t launch_planned(tg_plan_t pl, const void* A, const void* B, void* C, 
                     plan_persistent(M, N, K, ds->num_sms, kBigBN, kBigStages,
                                     tg::PersistentCfg<kBigBN, kBigStages>::kSmemBytes, &pl);
                 } else {
-                    return launch_pair<T>(A, B, C, pl, M, N, K, lda, ldb, ldc, epilogue, s,
+                    return launch_pair<T>(A, B, C, pl, M, N, K, lda, ldb, ldc, ep, s,
                                           ds->max_pairs);
                 }
             }
             if (pl.bn == kBigBN)
                 return launch_persistent<kBigBN, kBigStages, T>(A, B, C, pl, M, N, K, lda, ldb,
-                                                               ldc, epilogue, s);
+                                                               ldc, ep, s);
             return launch_persistent<kMidBN, kMidStages, T>(A, B, C, pl, M, N, K, lda, ldb, ldc,
-                                                           epilogue, s);
+                                                           ep, s);
         case TG_KERNEL_SKINNY: {
             const uint64_t timeout = g_timeout_ns.load();
             const int32_t inject = g_inject.exchange(0);
-            return tg::skinny_launch<T>(A, B, C, pl, M, N, K, lda, ldb, ldc, epilogue, s, dev,
+            return tg::skinny_launch<T>(A, B, C, pl, M, N, K, lda, ldb, ldc, ep, s, dev,
                                         ds->num_sms, timeout, inject, encode_2d);
         }
         default:
@@ -431,17 +444,18 @@ tg_status_t launch_planned(tg_plan_t pl, const void* A, const void* B, void* C, 
     }
 }
 
-// C = epi(A·B) for 16-bit element type T (__half or __nv_bfloat16): plan,
-// stage operands the tensor memory-access unit cannot address, launch the
-// planned kernel on `stream`, and copy a staged C back.
+// C = out(act(A·B + bias) + R) for 16-bit input type T (__half or
+// __nv_bfloat16): plan, stage operands the tensor memory-access unit cannot
+// address, launch the planned kernel on `stream`, and copy a staged C back.
+// Arguments were validated by the caller.
 template <typename T>
 tg_status_t gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
-                      int64_t lda, int64_t ldb, int64_t ldc, int epilogue, void* stream) {
-    tg_status_t st = validate(A, B, C, M, N, K, lda, ldb, ldc, epilogue, /*tma_layout=*/false);
-    if (st != TG_OK || M == 0 || N == 0) return st;
+                      int64_t lda, int64_t ldb, int64_t ldc, const tg::EpilogueSpec& ep,
+                      void* stream) {
+    if (M == 0 || N == 0) return TG_OK;
     int dev = 0;
     DeviceState* ds = nullptr;
-    st = current_device(&dev, &ds);
+    tg_status_t st = current_device(&dev, &ds);
     if (st != TG_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -451,15 +465,23 @@ tg_status_t gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t 
     apply_forced_config(M, N, K, ds->num_sms, &pl);
 
     if (pl.kernel == TG_KERNEL_FILL) {
-        // +0 has the same (all-zero) bits in fp16 and bf16; any ldc works
-        tg::tg_fill_zero_f16<<<static_cast<unsigned>(pl.grid), 256, 0, s>>>(
-            static_cast<__half*>(C), M, N, ldc);
+        if (ep.e.bias == nullptr && ep.e.resid == nullptr && !ep.out_f32) {
+            // +0 has the same (all-zero) bits in fp16 and bf16; any ldc works
+            tg::tg_fill_zero_f16<<<static_cast<unsigned>(pl.grid), 256, 0, s>>>(
+                static_cast<__half*>(C), M, N, ldc);
+        } else {
+            tg::tg_epilogue_only<T><<<static_cast<unsigned>(pl.grid), 256, 0, s>>>(
+                C, ldc, ep.out_f32, ep.e, ep.relu, M, N);
+        }
         return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_LAUNCH;
     }
+    // C's element size and the tensor memory-access layout rule for it:
+    // 16-byte aligned rows, i.e. ldc a multiple of 16 / elem_c.
+    const int elem_c = ep.out_f32 ? 4 : 2;
     const bool a_ok = tma_layout_ok(A, lda), b_ok = tma_layout_ok(B, ldb);
-    const bool c_ok = tma_layout_ok(C, ldc);
+    const bool c_ok = (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && (ldc * elem_c) % 16 == 0;
     if (a_ok && b_ok && c_ok)
-        return launch_planned<T>(pl, A, B, C, M, N, K, lda, ldb, ldc, epilogue, s, dev, ds);
+        return launch_planned<T>(pl, A, B, C, M, N, K, lda, ldb, ldc, ep, s, dev, ds);
 
     // Staging: aligned copies with leading dimensions rounded up to 8.
     const int64_t lda2 = a_ok ? lda : round_up8(K), ldb2 = b_ok ? ldb : round_up8(N);
@@ -467,7 +489,7 @@ tg_status_t gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t 
     auto align256 = [](int64_t b) { return (b + 255) / 256 * 256; };
     const int64_t bytes_a = a_ok ? 0 : align256(M * lda2 * 2);
     const int64_t bytes_b = b_ok ? 0 : align256(K * ldb2 * 2);
-    const int64_t bytes_c = c_ok ? 0 : align256(M * ldc2 * 2);
+    const int64_t bytes_c = c_ok ? 0 : align256(M * ldc2 * elem_c);
     void* buf = nullptr;
     st = staging_buffer(dev, s, static_cast<size_t>(bytes_a + bytes_b + bytes_c), &buf);
     if (st != TG_OK) return st;
@@ -475,12 +497,35 @@ tg_status_t gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t 
     const void* A2 = a_ok ? A : p;
     const void* B2 = b_ok ? B : p + bytes_a;
     void* C2 = c_ok ? C : p + bytes_a + bytes_b;
-    if (!a_ok && (st = copy_matrix16(A, lda, p, lda2, M, K, ds->num_sms, s)) != TG_OK) return st;
-    if (!b_ok && (st = copy_matrix16(B, ldb, p + bytes_a, ldb2, K, N, ds->num_sms, s)) != TG_OK)
+    if (!a_ok && (st = copy_matrix(A, lda, p, lda2, M, K, 2, ds->num_sms, s)) != TG_OK) return st;
+    if (!b_ok && (st = copy_matrix(B, ldb, p + bytes_a, ldb2, K, N, 2, ds->num_sms, s)) != TG_OK)
         return st;
-    st = launch_planned<T>(pl, A2, B2, C2, M, N, K, lda2, ldb2, ldc2, epilogue, s, dev, ds);
+    st = launch_planned<T>(pl, A2, B2, C2, M, N, K, lda2, ldb2, ldc2, ep, s, dev, ds);
     if (st != TG_OK || c_ok) return st;
-    return copy_matrix16(C2, ldc2, C, ldc, M, N, ds->num_sms, s);
+    return copy_matrix(C2, ldc2, C, ldc, M, N, elem_c, ds->num_sms, s);
+}
+
+tg::EpilogueSpec plain_epilogue(int epilogue) {
+    tg::EpilogueSpec ep;
+    ep.relu = epilogue == TG_EPI_RELU ? 1 : 0;
+    return ep;
+}
+
+// tg_gemm_ex's own argument checks (beyond validate): types, the residual's
+// stride and the alignment of bias, residual and an fp32 C.
+tg_status_t validate_ex(int32_t in_dtype, const void* C, int64_t M, int64_t N,
+                        const tg_epilogue_ex_t& x) {
+    if (in_dtype != TG_DTYPE_F16 && in_dtype != TG_DTYPE_BF16) return TG_ERR_INVALID_VALUE;
+    if (x.out_dtype != in_dtype && x.out_dtype != TG_DTYPE_F32) return TG_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return TG_OK;
+    if (x.residual != nullptr && x.ldr < N) return TG_ERR_INVALID_VALUE;
+    if (x.bias != nullptr && (reinterpret_cast<uintptr_t>(x.bias) & 3u) != 0)
+        return TG_ERR_MISALIGNED;
+    if (x.residual != nullptr && (reinterpret_cast<uintptr_t>(x.residual) & 1u) != 0)
+        return TG_ERR_MISALIGNED;
+    if (x.out_dtype == TG_DTYPE_F32 && (reinterpret_cast<uintptr_t>(C) & 3u) != 0)
+        return TG_ERR_MISALIGNED;
+    return TG_OK;
 }
 
 }  // namespace
@@ -572,12 +617,45 @@ const char* tg_version(void) { return "libtgemm 0.1.0 (sm_103a)"; }
 
 tg_status_t tg_gemm_f16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                         int64_t lda, int64_t ldb, int64_t ldc, int epilogue, void* stream) {
-    return gemm_impl<__half>(A, B, C, M, N, K, lda, ldb, ldc, epilogue, stream);
+    const tg_status_t st = validate(A, B, C, M, N, K, lda, ldb, ldc, epilogue, false);
+    if (st != TG_OK) return st;
+    return gemm_impl<__half>(A, B, C, M, N, K, lda, ldb, ldc, plain_epilogue(epilogue), stream);
 }
 
 tg_status_t tg_gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                          int64_t lda, int64_t ldb, int64_t ldc, int epilogue, void* stream) {
-    return gemm_impl<__nv_bfloat16>(A, B, C, M, N, K, lda, ldb, ldc, epilogue, stream);
+    const tg_status_t st = validate(A, B, C, M, N, K, lda, ldb, ldc, epilogue, false);
+    if (st != TG_OK) return st;
+    return gemm_impl<__nv_bfloat16>(A, B, C, M, N, K, lda, ldb, ldc, plain_epilogue(epilogue),
+                                    stream);
+}
+
+tg_status_t tg_gemm_ex(int32_t in_dtype, const void* A, const void* B, void* C, int64_t M,
+                       int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                       const tg_epilogue_ex_t* epi, void* stream) {
+    tg_epilogue_ex_t x;
+    if (epi != nullptr) {
+        x = *epi;
+    } else {
+        std::memset(&x, 0, sizeof(x));
+        x.activation = TG_EPI_NONE;
+        x.out_dtype = in_dtype;
+    }
+    tg_status_t st = validate(A, B, C, M, N, K, lda, ldb, ldc, x.activation, false);
+    if (st != TG_OK) return st;
+    st = validate_ex(in_dtype, C, M, N, x);
+    if (st != TG_OK) return st;
+    tg::EpilogueSpec ep = plain_epilogue(x.activation);
+    ep.out_f32 = x.out_dtype == TG_DTYPE_F32 ? 1 : 0;
+    ep.e.bias = x.bias;
+    ep.e.resid = x.residual;
+    ep.e.ldr = x.residual != nullptr ? x.ldr : 0;
+    ep.e.bias_vec = (reinterpret_cast<uintptr_t>(x.bias) & 15u) == 0 ? 1 : 0;
+    ep.e.resid_vec =
+        (reinterpret_cast<uintptr_t>(x.residual) & 15u) == 0 && (x.ldr & 7) == 0 ? 1 : 0;
+    if (in_dtype == TG_DTYPE_BF16)
+        return gemm_impl<__nv_bfloat16>(A, B, C, M, N, K, lda, ldb, ldc, ep, stream);
+    return gemm_impl<__half>(A, B, C, M, N, K, lda, ldb, ldc, ep, stream);
 }
 
 tg_status_t tg_sync_status(void* stream) {
