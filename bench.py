@@ -66,11 +66,12 @@ def rank_info():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
-def source_hash() -> str:
-    """Hash of the kernel sources, to tell whether stored ncu counters are stale."""
+def source_hash(files=None) -> str:
+    """Hash of kernel sources (the given csrc file names, else all of csrc),
+    to tell whether stored ncu counters are stale."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tiled_fp16_gemm_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(files if files is not None else os.listdir(csrc)):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
@@ -93,7 +94,7 @@ def stored_traffic(kernel_key: str):
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
         e = d.get(kernel_key)
-        if e and e.get("source_hash") == source_hash():
+        if e and e.get("source_hash") == source_hash(e.get("sources")):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass

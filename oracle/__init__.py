@@ -92,6 +92,13 @@ class Oracle:
                                           ctypes.c_int, f32p, u16p, i64, i64p, i64p, i64, vp,
                                           f64p]
         lib.oracle_gemm_ex_at.restype = ctypes.c_int
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        lib.oracle_f64_from_e2m1.argtypes = [ctypes.c_uint8]
+        lib.oracle_f64_from_e2m1.restype = ctypes.c_double
+        lib.oracle_f64_from_e8m0.argtypes = [ctypes.c_uint8]
+        lib.oracle_f64_from_e8m0.restype = ctypes.c_double
+        lib.oracle_mxfp4_dequant_f16.argtypes = [u8p, i64, u8p, i64, i64, i64, u16p, i64]
+        lib.oracle_mxfp4_dequant_f16.restype = ctypes.c_int
         self.lib = lib
         self.path = path
 
@@ -309,3 +316,68 @@ def ulp16(x) -> np.ndarray:
     e = np.floor(np.log2(np.where(nz, a, 1.0)))
     out[nz] = np.exp2(e[nz] - 10.0)
     return out
+
+
+# ------------------------------------------------------------------ MXFP4 weights
+
+def _mx_e2m1(self, code: int) -> float:
+    """Value of one 4-bit FP4 E2M1 code."""
+    return float(self.lib.oracle_f64_from_e2m1(int(code) & 15))
+
+
+def _mx_e8m0(self, x: int) -> float:
+    """Value of one E8M0 scale byte: 2^(x - 127), NaN for 255."""
+    return float(self.lib.oracle_f64_from_e8m0(int(x) & 255))
+
+
+def _mxfp4_dequant(self, Bq, S, K, N):
+    """Bdeq = fp16_rne(e2m1(code) * 2^(X - 127)) as a K×N float16 array.
+
+    Bq: uint8, K rows of packed codes (row stride Bq.shape[1] >= ceil(N/2));
+    S: uint8 E8M0 scales, ceil(K/32) rows (row stride S.shape[1] >= N)."""
+    Bq = np.ascontiguousarray(np.asarray(Bq, dtype=np.uint8))
+    S = np.ascontiguousarray(np.asarray(S, dtype=np.uint8))
+    out = np.empty((K, N), dtype=np.uint16)
+    ldbq = Bq.shape[1] if Bq.ndim == 2 else (N + 1) // 2
+    lds = S.shape[1] if S.ndim == 2 else N
+    rc = self.lib.oracle_mxfp4_dequant_f16(_ptr(Bq, ctypes.c_uint8), ldbq,
+                                          _ptr(S, ctypes.c_uint8), lds, K, N,
+                                          _ptr(out, ctypes.c_uint16), N)
+    if rc != 0:
+        raise ValueError("oracle_mxfp4_dequant_f16 rejected its arguments")
+    return out.view(np.float16)
+
+
+def _gemm_mxfp4(self, A, Bq, S, M, N, K, relu=False, bias=None, R=None, out_dtype="f16"):
+    """C = out(act(A·Bdeq + bias) + R) with Bdeq the dequantised MXFP4 weights
+    (see tgemm_oracle.c); A and R fp16."""
+    Bd = self.mxfp4_dequant(Bq, S, K, N)
+    return self.gemm_ex(A, Bd, M, N, K, relu=relu, bias=bias, R=R, in_dtype="f16",
+                        out_dtype=out_dtype)
+
+
+def _gemm_mxfp4_at(self, A, Bq, S, K, N, rows, cols, relu=False, bias=None, R=None,
+                   out_dtype="f16"):
+    """Selected outputs of gemm_mxfp4; returns (rounded values, fp64 values)."""
+    Bd = self.mxfp4_dequant(Bq, S, K, N)
+    return self.gemm_ex_at(A, Bd, K, rows, cols, relu=relu, bias=bias, R=R, in_dtype="f16",
+                           out_dtype=out_dtype)
+
+
+Oracle.e2m1 = _mx_e2m1
+Oracle.e8m0 = _mx_e8m0
+Oracle.mxfp4_dequant = _mxfp4_dequant
+Oracle.gemm_mxfp4 = _gemm_mxfp4
+Oracle.gemm_mxfp4_at = _gemm_mxfp4_at
+
+
+def mxfp4_dequant(*args, **kw):
+    return default().mxfp4_dequant(*args, **kw)
+
+
+def gemm_mxfp4(*args, **kw):
+    return default().gemm_mxfp4(*args, **kw)
+
+
+def gemm_mxfp4_at(*args, **kw):
+    return default().gemm_mxfp4_at(*args, **kw)

@@ -409,3 +409,56 @@ int oracle_gemm_ex_at(int in_fmt, int out_fmt, const uint16_t* A, const uint16_t
     }
     return 0;
 }
+
+/* ========================================================================
+ * MXFP4 weight GEMM.  The pages name low-bit weight GEMMs as the largest
+ * mixed-precision win ("5分钟上手TileLang", section "H100 实测": WFP4 mixed
+ * precision; section "进阶方向": dequantize_gemm with W4A8 and MXFP4;
+ * "TileLang：让GPU编程像Python一样简单的高性能计算新范式": WINT2AFP16) but
+ * define no format.  Reading taken: B is stored in the OCP Microscaling
+ * MXFP4 format and dequantised to fp16 before an fp16 GEMM:
+ *
+ *   code(k, n) = 4-bit FP4 E2M1 element: byte Bq[k*ldbq + n/2], low nibble
+ *                for even n, high nibble for odd n;
+ *   X(k, n)    = 8-bit E8M0 scale shared by the 32 k of a block:
+ *                S[(k/32)*lds + n];
+ *   Bdeq[k][n] = fp16_rne( e2m1(code) * 2^(X - 127) )   (X = 255: NaN)
+ *   C          = the fp16 GEMM of A and Bdeq (oracle_gemm_ex, in_fmt 0).
+ *
+ * E2M1: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa; exponent
+ * 0 is subnormal (0 or 0.5); no infinities or NaNs.  E8M0: an unsigned
+ * power-of-two exponent with bias 127, 255 encoding NaN.
+ * ======================================================================== */
+
+double oracle_f64_from_e2m1(uint8_t code)
+{
+    const int s = (code >> 3) & 1;
+    const int e = (code >> 1) & 3;
+    const int m = code & 1;
+    double mag = (e == 0) ? ldexp((double)m, -1) : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -mag : mag;
+}
+
+double oracle_f64_from_e8m0(uint8_t x)
+{
+    if (x == 255) return NAN;
+    return ldexp(1.0, (int)x - 127);
+}
+
+/* Bdeq (K×N fp16 bits, row stride ldb) from the packed codes and scales.
+ * Returns 0, or -1 on bad arguments. */
+int oracle_mxfp4_dequant_f16(const uint8_t* Bq, int64_t ldbq, const uint8_t* S, int64_t lds,
+                             int64_t K, int64_t N, uint16_t* Bdeq, int64_t ldb)
+{
+    if (K < 0 || N < 0 || ldbq < (N + 1) / 2 || lds < N || ldb < N) return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t k = 0; k < K; ++k) {
+        for (int64_t n = 0; n < N; ++n) {
+            uint8_t byte = Bq[k * ldbq + n / 2];
+            uint8_t code = (n & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+            double v = oracle_f64_from_e2m1(code) * oracle_f64_from_e8m0(S[(k / 32) * lds + n]);
+            Bdeq[k * ldb + n] = oracle_f16_from_f64(v);
+        }
+    }
+    return 0;
+}

@@ -452,4 +452,130 @@ def pin_ex_sampled_matches_full(o):
         assert np.array_equal(np.asarray(v), np.asarray(C)[r, c]) and np.array_equal(v64, ref[r, c])
 
 
+
+
+# ---------------------------------------------------------------- MXFP4 weights
+#
+# Facts from the OCP Microscaling (MX) format specification, not from the
+# oracle: the FP4 E2M1 element values for codes 0..15 (sign-magnitude, codes
+# 8..15 negative, code 8 is -0) and the E8M0 scale 2^(X-127) with 0xFF = NaN.
+
+E2M1_SPEC = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+             -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def _pack_codes(codes: np.ndarray, ld_bytes: int | None = None) -> np.ndarray:
+    """K×N codes (0..15) into K×ceil(N/2) bytes: low nibble = even column."""
+    K, N = codes.shape
+    ld = (N + 1) // 2 if ld_bytes is None else ld_bytes
+    out = np.zeros((K, ld), dtype=np.uint8)
+    for n in range(N):
+        out[:, n // 2] |= (codes[:, n].astype(np.uint8) << (4 * (n % 2))).astype(np.uint8)
+    return out
+
+
+def _exact_deq(code: int, x: int) -> Fraction:
+    return Fraction(E2M1_SPEC[code]) * (Fraction(2) ** (int(x) - 127))
+
+
+def pin_mx_e2m1_table(o):
+    for code, want in enumerate(E2M1_SPEC):
+        got = o.e2m1(code)
+        assert got == want and math.copysign(1.0, got) == math.copysign(1.0, want), (code, got)
+
+
+def pin_mx_e8m0(o):
+    assert o.e8m0(127) == 1.0
+    assert o.e8m0(128) == 2.0 and o.e8m0(126) == 0.5
+    assert o.e8m0(0) == float(Fraction(1, 2 ** 127))
+    assert o.e8m0(254) == float(2 ** 127)
+    assert math.isnan(o.e8m0(255))
+
+
+def pin_mx_dequant_exact(o):
+    """Every (code, scale) pair over a scale range that covers underflow to
+    zero, fp16 subnormals, normals and overflow to inf, against exact
+    rational rounding; also fixes the nibble order and the scale indexing."""
+    rng = np.random.default_rng(51)
+    K, N = 70, 37  # ragged: three scale rows, odd N (a padding nibble)
+    codes = rng.integers(0, 16, (K, N))
+    X = rng.integers(95, 146, ((K + 31) // 32, N)).astype(np.uint8)
+    Bq = _pack_codes(codes, ld_bytes=21)
+    got = o.mxfp4_dequant(Bq, X, K, N).astype(np.float64)
+    for k in range(K):
+        for n in range(N):
+            want = rne_f16(_exact_deq(int(codes[k, n]), int(X[k // 32, n])))
+            if want == 0.0:  # a zero result keeps the element's sign (code bit 3)
+                want = math.copysign(0.0, -1.0 if codes[k, n] >= 8 else 1.0)
+            g = got[k, n]
+            assert (g == want and math.copysign(1, g) == math.copysign(1, want)), \
+                (k, n, int(codes[k, n]), int(X[k // 32, n]), g, want)
+    # NaN scale: every element of that block is NaN
+    X2 = X.copy()
+    X2[1, 3] = 255
+    d2 = o.mxfp4_dequant(Bq, X2, K, N).astype(np.float64)
+    assert np.all(np.isnan(d2[32:64, 3])) and not np.any(np.isnan(d2[:32, 3]))
+
+
+def pin_mx_padding_ignored(o):
+    """Bytes past ceil(N/2), the spare high nibble of an odd N, and scale
+    columns past N are never read."""
+    rng = np.random.default_rng(52)
+    K, N = 40, 9
+    codes = rng.integers(0, 16, (K, N))
+    X = rng.integers(120, 130, ((K + 31) // 32, N + 4)).astype(np.uint8)
+    Bq = _pack_codes(codes, ld_bytes=8)
+    ref = o.mxfp4_dequant(Bq, X, K, N).view(np.uint16).copy()
+    Bq2 = Bq.copy()
+    Bq2[:, 5:] = 0xEE
+    Bq2[:, 4] |= 0xF0  # high nibble of byte 4 is column 9: padding for N = 9
+    X2 = X.copy()
+    X2[:, N:] = 255
+    assert np.array_equal(o.mxfp4_dequant(Bq2, X2, K, N).view(np.uint16), ref)
+
+
+def pin_mx_gemm_exact(o):
+    """C = out(act(A·Bdeq + bias) + R) against exact rationals, with scales
+    where every dequantised weight is an fp16 number (so no intermediate
+    rounding is involved)."""
+    rng = np.random.default_rng(53)
+    M, N, K = 3, 5, 70
+    A = _f16(rng.normal(0, 1, (M, K)))
+    codes = rng.integers(0, 16, (K, N))
+    X = rng.integers(115, 130, ((K + 31) // 32, N)).astype(np.uint8)
+    Bq = _pack_codes(codes)
+    bias = rng.normal(0, 1, N).astype(np.float32)
+    R = _f16(rng.normal(0, 1, (M, N)))
+    Ad = A.astype(np.float64)
+    for relu in (False, True):
+        for out_dtype in ("f16", "f32"):
+            got = np.asarray(o.gemm_mxfp4(A, Bq, X, M, N, K, relu=relu, bias=bias, R=R,
+                                          out_dtype=out_dtype), dtype=np.float64)
+            rne = rne_f16 if out_dtype == "f16" else rne_f32
+            for i in range(M):
+                for j in range(N):
+                    q = sum((Fraction(float(Ad[i, k])) * _exact_deq(int(codes[k, j]),
+                                                                    int(X[k // 32, j]))
+                             for k in range(K)), Fraction(0))
+                    q += Fraction(float(bias[j]))
+                    if relu and q < 0:
+                        q = Fraction(0)
+                    q += Fraction(float(R[i, j]))
+                    assert got[i, j] == rne(q), (relu, out_dtype, i, j)
+
+
+def pin_mx_gemm_integer_closed_form(o):
+    """Codes ±1 (2, 10) with scale 2^0 make Bdeq a ±1 matrix: C equals
+    numpy's int64 product of the integer A with that sign matrix."""
+    rng = np.random.default_rng(54)
+    M, N, K = 6, 10, 96
+    Ai = rng.integers(-3, 4, (M, K))
+    sign = rng.integers(0, 2, (K, N))
+    codes = np.where(sign == 1, 10, 2)  # 2 -> +1.0, 10 -> -1.0
+    X = np.full(((K + 31) // 32, N), 127, dtype=np.uint8)
+    C = o.gemm_mxfp4(Ai.astype(np.float16), _pack_codes(codes), X, M, N, K)
+    want = Ai @ np.where(sign == 1, -1, 1)
+    assert np.array_equal(C.astype(np.float64), want.astype(np.float64))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

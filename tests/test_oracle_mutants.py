@@ -57,6 +57,18 @@ MUTANTS = [
      "decode16(R[(i % 1) * ldr + j], in_fmt)"),
     ("ex_f32_through_f16", "if (out_fmt == 2) ((float*)C)[idx] = (float)v;",
      "if (out_fmt == 2) ((float*)C)[idx] = (float)oracle_f64_from_f16(oracle_f16_from_f64(v));"),
+    # MXFP4 weights
+    ("mx_nibbles_swapped", "(n & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15)",
+     "(n & 1) ? (uint8_t)(byte & 15) : (uint8_t)(byte >> 4)"),
+    ("mx_scale_block_16", "S[(k / 32) * lds + n]", "S[(k / 16) * lds + n]"),
+    ("mx_scale_by_row", "S[(k / 32) * lds + n]", "S[(n / 32) * lds + k % lds]"),
+    ("mx_e2m1_bias_2", "ldexp(1.0 + 0.5 * m, e - 1)", "ldexp(1.0 + 0.5 * m, e - 2)"),
+    ("mx_e2m1_no_subnormal", "(e == 0) ? ldexp((double)m, -1)", "(e == 0) ? ldexp(1.0 + 0.5 * m, -1)"),
+    ("mx_e2m1_sign_ignored", "return s ? -mag : mag;", "return mag;"),
+    ("mx_e8m0_bias_128", "return ldexp(1.0, (int)x - 127);", "return ldexp(1.0, (int)x - 128);"),
+    ("mx_e8m0_nan_ignored", "if (x == 255) return NAN;", "if (x == 256) return NAN;"),
+    ("mx_deq_no_rounding", "Bdeq[k * ldb + n] = oracle_f16_from_f64(v);",
+     "Bdeq[k * ldb + n] = oracle_f16_from_f64(v) & 0xFFFE;"),
 ]
 
 
