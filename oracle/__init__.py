@@ -333,12 +333,13 @@ def _mx_e8m0(self, x: int) -> float:
 def _mxfp4_dequant(self, Bq, S, K, N):
     """Bdeq = fp16_rne(e2m1(code) * 2^(X - 127)) as a K×N float16 array.
 
-    Bq: uint8, K rows of packed codes (row stride Bq.shape[1] >= ceil(N/2));
-    S: uint8 E8M0 scales, ceil(K/32) rows (row stride S.shape[1] >= N)."""
+    Bq: uint8, N rows of packed codes along k (row stride Bq.shape[1] >=
+    ceil(K/2)); S: uint8 E8M0 scales, ceil(K/32) rows (row stride S.shape[1]
+    >= N)."""
     Bq = np.ascontiguousarray(np.asarray(Bq, dtype=np.uint8))
     S = np.ascontiguousarray(np.asarray(S, dtype=np.uint8))
     out = np.empty((K, N), dtype=np.uint16)
-    ldbq = Bq.shape[1] if Bq.ndim == 2 else (N + 1) // 2
+    ldbq = Bq.shape[1] if Bq.ndim == 2 else (K + 1) // 2
     lds = S.shape[1] if S.ndim == 2 else N
     rc = self.lib.oracle_mxfp4_dequant_f16(_ptr(Bq, ctypes.c_uint8), ldbq,
                                           _ptr(S, ctypes.c_uint8), lds, K, N,

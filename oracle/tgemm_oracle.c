@@ -418,10 +418,13 @@ int oracle_gemm_ex_at(int in_fmt, int out_fmt, const uint16_t* A, const uint16_t
  * define no format.  Reading taken: B is stored in the OCP Microscaling
  * MXFP4 format and dequantised to fp16 before an fp16 GEMM:
  *
- *   code(k, n) = 4-bit FP4 E2M1 element: byte Bq[k*ldbq + n/2], low nibble
- *                for even n, high nibble for odd n;
+ *   code(k, n) = 4-bit FP4 E2M1 element: byte Bq[n*ldbq + k/2], low nibble
+ *                for even k, high nibble for odd k (B is stored in the
+ *                [out][in] orientation of a linear layer's weight: each
+ *                column's k run is contiguous, so a 32-element MX block is 16
+ *                bytes);
  *   X(k, n)    = 8-bit E8M0 scale shared by the 32 k of a block:
- *                S[(k/32)*lds + n];
+ *                S[(k/32)*lds + n] (block-major, n contiguous);
  *   Bdeq[k][n] = fp16_rne( e2m1(code) * 2^(X - 127) )   (X = 255: NaN)
  *   C          = the fp16 GEMM of A and Bdeq (oracle_gemm_ex, in_fmt 0).
  *
@@ -445,17 +448,17 @@ double oracle_f64_from_e8m0(uint8_t x)
     return ldexp(1.0, (int)x - 127);
 }
 
-/* Bdeq (K×N fp16 bits, row stride ldb) from the packed codes and scales.
- * Returns 0, or -1 on bad arguments. */
+/* Bdeq (K×N fp16 bits, row stride ldb) from the packed codes (N rows of
+ * ldbq bytes) and scales.  Returns 0, or -1 on bad arguments. */
 int oracle_mxfp4_dequant_f16(const uint8_t* Bq, int64_t ldbq, const uint8_t* S, int64_t lds,
                              int64_t K, int64_t N, uint16_t* Bdeq, int64_t ldb)
 {
-    if (K < 0 || N < 0 || ldbq < (N + 1) / 2 || lds < N || ldb < N) return -1;
+    if (K < 0 || N < 0 || ldbq < (K + 1) / 2 || lds < N || ldb < N) return -1;
 #pragma omp parallel for schedule(static)
     for (int64_t k = 0; k < K; ++k) {
         for (int64_t n = 0; n < N; ++n) {
-            uint8_t byte = Bq[k * ldbq + n / 2];
-            uint8_t code = (n & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+            uint8_t byte = Bq[n * ldbq + k / 2];
+            uint8_t code = (k & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
             double v = oracle_f64_from_e2m1(code) * oracle_f64_from_e8m0(S[(k / 32) * lds + n]);
             Bdeq[k * ldb + n] = oracle_f16_from_f64(v);
         }

@@ -465,12 +465,13 @@ E2M1_SPEC = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
 
 
 def _pack_codes(codes: np.ndarray, ld_bytes: int | None = None) -> np.ndarray:
-    """K×N codes (0..15) into K×ceil(N/2) bytes: low nibble = even column."""
+    """K×N codes (0..15) into N rows of ceil(K/2) bytes: row n holds column n's
+    codes along k, low nibble = even k."""
     K, N = codes.shape
-    ld = (N + 1) // 2 if ld_bytes is None else ld_bytes
-    out = np.zeros((K, ld), dtype=np.uint8)
-    for n in range(N):
-        out[:, n // 2] |= (codes[:, n].astype(np.uint8) << (4 * (n % 2))).astype(np.uint8)
+    ld = (K + 1) // 2 if ld_bytes is None else ld_bytes
+    out = np.zeros((N, ld), dtype=np.uint8)
+    for k in range(K):
+        out[:, k // 2] |= (codes[k, :].astype(np.uint8) << (4 * (k % 2))).astype(np.uint8)
     return out
 
 
@@ -497,10 +498,10 @@ def pin_mx_dequant_exact(o):
     zero, fp16 subnormals, normals and overflow to inf, against exact
     rational rounding; also fixes the nibble order and the scale indexing."""
     rng = np.random.default_rng(51)
-    K, N = 70, 37  # ragged: three scale rows, odd N (a padding nibble)
+    K, N = 71, 37  # ragged: three scale rows, odd K (a padding nibble)
     codes = rng.integers(0, 16, (K, N))
     X = rng.integers(95, 146, ((K + 31) // 32, N)).astype(np.uint8)
-    Bq = _pack_codes(codes, ld_bytes=21)
+    Bq = _pack_codes(codes, ld_bytes=40)
     got = o.mxfp4_dequant(Bq, X, K, N).astype(np.float64)
     for k in range(K):
         for n in range(N):
@@ -518,17 +519,17 @@ def pin_mx_dequant_exact(o):
 
 
 def pin_mx_padding_ignored(o):
-    """Bytes past ceil(N/2), the spare high nibble of an odd N, and scale
+    """Bytes past ceil(K/2), the spare high nibble of an odd K, and scale
     columns past N are never read."""
     rng = np.random.default_rng(52)
-    K, N = 40, 9
+    K, N = 41, 9
     codes = rng.integers(0, 16, (K, N))
     X = rng.integers(120, 130, ((K + 31) // 32, N + 4)).astype(np.uint8)
-    Bq = _pack_codes(codes, ld_bytes=8)
+    Bq = _pack_codes(codes, ld_bytes=24)
     ref = o.mxfp4_dequant(Bq, X, K, N).view(np.uint16).copy()
     Bq2 = Bq.copy()
-    Bq2[:, 5:] = 0xEE
-    Bq2[:, 4] |= 0xF0  # high nibble of byte 4 is column 9: padding for N = 9
+    Bq2[:, 21:] = 0xEE
+    Bq2[:, 20] |= 0xF0  # high nibble of byte 20 is k = 41: padding for K = 41
     X2 = X.copy()
     X2[:, N:] = 255
     assert np.array_equal(o.mxfp4_dequant(Bq2, X2, K, N).view(np.uint16), ref)

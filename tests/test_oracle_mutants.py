@@ -58,8 +58,8 @@ MUTANTS = [
     ("ex_f32_through_f16", "if (out_fmt == 2) ((float*)C)[idx] = (float)v;",
      "if (out_fmt == 2) ((float*)C)[idx] = (float)oracle_f64_from_f16(oracle_f16_from_f64(v));"),
     # MXFP4 weights
-    ("mx_nibbles_swapped", "(n & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15)",
-     "(n & 1) ? (uint8_t)(byte & 15) : (uint8_t)(byte >> 4)"),
+    ("mx_nibbles_swapped", "(k & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15)",
+     "(k & 1) ? (uint8_t)(byte & 15) : (uint8_t)(byte >> 4)"),
     ("mx_scale_block_16", "S[(k / 32) * lds + n]", "S[(k / 16) * lds + n]"),
     ("mx_scale_by_row", "S[(k / 32) * lds + n]", "S[(n / 32) * lds + k % lds]"),
     ("mx_e2m1_bias_2", "ldexp(1.0 + 0.5 * m, e - 1)", "ldexp(1.0 + 0.5 * m, e - 2)"),
