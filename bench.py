@@ -53,6 +53,7 @@ def parse_args(argv=None):
     p.add_argument("--no-skinny", action="store_true")
     p.add_argument("--no-bf16", action="store_true")
     p.add_argument("--no-epilogue", action="store_true")
+    p.add_argument("--no-mxfp4", action="store_true")
     a = p.parse_args(argv)
     if a.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -451,6 +452,53 @@ def run_ours(args, w, rank, world, local_rank):
             out["epilogue"][name] = ent
             del ce
         del bias, resid
+
+    # ---- MXFP4 weights (tg_gemm_mxfp4): weight streaming through the fused
+    # split-K kernel, and the MLP shape through dequantise-then-GEMM
+    if not args.no_mxfp4 and world == 1:
+        out["mxfp4"] = {"entry": "tg_gemm_mxfp4"}
+        for mname in ("mxfp4_skinny_64x16384x8192", "mxfp4_mlp_8192x28672x4096_relu"):
+            mw = W.MX_WORKLOADS[mname]
+            Am, Bqm, Sm = W.mx_workload_inputs(mw)
+            am = torch.from_numpy(Am).to(device)
+            bqm = torch.from_numpy(Bqm).to(device)
+            sm = torch.from_numpy(Sm).to(device)
+            cm = torch.empty((mw.M, mw.N), dtype=torch.float16, device=device)
+            ex_m = tg.tg_epilogue_ex_t(tg.TG_EPI_RELU if mw.relu else tg.TG_EPI_NONE,
+                                       tg.TG_DTYPE_F16, None, None, 0)
+
+            def launch6(am=am, bqm=bqm, sm=sm, cm=cm, mw=mw, ex_m=ex_m):
+                st = tg.tg_gemm_mxfp4(am.data_ptr(), bqm.data_ptr(), sm.data_ptr(), cm.data_ptr(),
+                                      mw.M, mw.N, mw.K, mw.K, bqm.shape[1], sm.shape[1], mw.N,
+                                      ex_m, stream.cuda_stream)
+                if st != tg.TG_OK:
+                    raise tg.TgemmError(st, "tg_gemm_mxfp4")
+
+            for _ in range(args.warmup):
+                launch6()
+            tg.sync_status(stream)
+            n6 = max(50, args.steps // 2) if mw.M <= 128 else max(20, args.steps // 10)
+            _, per6, _, _ = time_launches(launch6, stream, n6, world, device)
+            tg.sync_status(stream)
+            k6 = statistics.mean(per6)
+            ent = {"workload": mname, "launches": n6, "kernel_ms_mean": k6,
+                   "kernel_ms_min": min(per6), "tflops": mw.flops / (k6 / 1e3) / 1e12}
+            if mw.M <= 128:
+                gbs = mw.min_bytes / (k6 / 1e3) / 1e9
+                ent["kernel"] = "tg_gemm_mxfp4_skinny (codes decoded in shared memory)"
+                ent["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak,
+                                   "unit": "GB/s", "frac": gbs / hbm_peak,
+                                   "traffic": stored_traffic(f"mxfp4_skinny:{mname}"),
+                                   "peak_source": f"{peak_src} copy bandwidth"}
+                if "skinny" in out:
+                    ent["vs_fp16_skinny"] = out["skinny"]["kernel_ms_mean"] / k6
+            else:
+                tf = mw.flops / (k6 / 1e3) / 1e12
+                ent["kernel"] = "tg_mxfp4_dequant_f16 + tg_gemm_f16_pair<6>"
+                ent["roofline"] = {"bound": "tensor", "achieved": tf, "peak": tf_peak,
+                                   "unit": "TFLOP/s", "frac": tf / tf_peak}
+            out["mxfp4"][mname] = ent
+            del am, bqm, sm, cm
 
     # ---- end to end through the public API, host buffers in and out
     if not args.no_e2e:

@@ -164,6 +164,56 @@ tg_status_t tg_gemm_ex(int32_t in_dtype, const void* A, const void* B, void* C,
                        int64_t lda, int64_t ldb, int64_t ldc,
                        const tg_epilogue_ex_t* epi, void* stream);
 
+/* ------------------------------------------------------------------------
+ * MXFP4 weights: C = out(act(A · Bdeq + bias) + R), A fp16, B in MXFP4.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * tg_gemm_mxfp4 — the GEMM with B stored in the OCP Microscaling MXFP4
+ * format and dequantised to fp16 inside the library, asynchronous on
+ * `stream`:
+ *
+ *   code(k, n)  4-bit FP4 E2M1 element: byte Bq[n*ldbq + k/2], low nibble for
+ *               even k, high nibble for odd k (sign bit, 2 exponent bits with
+ *               bias 1, 1 mantissa bit; values 0, ±0.5, ±1, ±1.5, ±2, ±3, ±4, ±6).
+ *               B is stored in the [out][in] orientation of a linear layer's
+ *               weight: one row of packed codes per column n, k contiguous;
+ *   X(k, n)     8-bit E8M0 scale of the block of 32 k holding k:
+ *               Bscale[(k/32)*ldbs + n]; its value is 2^(X-127), X = 255 NaN;
+ *   Bdeq[k][n]  = fp16_rne(e2m1(code) * 2^(X-127));
+ *   C           = out(act(A·Bdeq + bias) + R) exactly as tg_gemm_ex with
+ *                 in_dtype TG_DTYPE_F16 (fp32 accumulation, one rounding).
+ *
+ * The pages name low-bit weight GEMMs as the largest mixed-precision gain
+ * ("5分钟上手TileLang", section "H100 实测": WFP4; section "进阶方向":
+ * dequantize_gemm with W4A8 and MXFP4; "TileLang：让GPU编程像Python一样
+ * 简单的高性能计算新范式": WINT2AFP16) but define no format; MXFP4 as
+ * specified by OCP, with fp16 activations, is this library's reading.
+ *
+ * A        device, fp16, row-major M×K, row stride lda ≥ K, 2-byte aligned
+ *          (other layouts than 16-byte aligned rows are staged).
+ * Bq       device, N rows of ceil(K/2) bytes, row stride ldbq ≥ ceil(K/2);
+ *          Bq 16-byte aligned and ldbq a multiple of 16 (else
+ *          TG_ERR_MISALIGNED).  A spare high nibble (odd K) is ignored.
+ * Bscale   device, ceil(K/32) rows of N bytes, row stride ldbs ≥ N; 16-byte
+ *          aligned, ldbs a multiple of 16 (else TG_ERR_MISALIGNED).
+ * C, ldc, epi, stream  as tg_gemm_ex with in_dtype TG_DTYPE_F16 (epi NULL =
+ *          plain fp16 output; the residual, if any, is fp16).
+ * M ≤ 128: a split-K kernel streams Bq and Bscale once and decodes them
+ *          into tensor memory (about 0.53 bytes per weight instead of 2).
+ * M > 128: Bq is dequantised once into a per-(device, stream) fp16 buffer of
+ *          K × roundup(N, 8) elements (grown on demand; growth waits for the
+ *          stream), then the fp16 GEMM runs on it.  TGEMM_FORCE_CFG =
+ *          pair256 | persistent256 | persistent128 takes this path for any M.
+ * K == 0:  C = out(act(bias) + R); A, Bq and Bscale may be NULL.
+ * Errors: as tg_gemm_ex, plus TG_ERR_INVALID_VALUE for ldbq < ceil(K/2) or
+ * ldbs < N, and TG_ERR_MISALIGNED for the Bq / Bscale alignment rules above.
+ */
+tg_status_t tg_gemm_mxfp4(const void* A, const void* Bq, const void* Bscale, void* C,
+                          int64_t M, int64_t N, int64_t K,
+                          int64_t lda, int64_t ldbq, int64_t ldbs, int64_t ldc,
+                          const tg_epilogue_ex_t* epi, void* stream);
+
 /*
  * tg_sync_status — wait for `stream`, then report (and clear) a device-side
  * timeout recorded by any libtgemm kernel on the current device since the

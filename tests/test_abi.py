@@ -136,6 +136,43 @@ def test_gemm_ex_fp32_output_alignment(tg):
         tg.TG_ERR_INVALID_VALUE
 
 
+@pytest.mark.parametrize("A,Bq,S,N,K,lda,ldbq,ldbs,want", [
+    # M = 4 throughout; C = GOOD with ldc = N; K = 64 needs ldbq >= 32
+    (GOOD, GOOD, GOOD, 32, 64, 64, 32, 32, None),        # valid
+    (GOOD + 2, GOOD, GOOD, 32, 64, 67, 32, 32, None),    # A off 16 bytes, odd lda: staged
+    (GOOD, GOOD + 8, GOOD, 32, 64, 64, 32, 32, 2),       # Bq not 16-byte aligned
+    (GOOD, GOOD, GOOD + 4, 32, 64, 64, 32, 32, 2),       # scales not 16-byte aligned
+    (GOOD, GOOD, GOOD, 32, 64, 64, 40, 32, 2),           # ldbq not a multiple of 16
+    (GOOD, GOOD, GOOD, 32, 64, 64, 32, 40, 2),           # ldbs not a multiple of 16
+    (GOOD, GOOD, GOOD, 32, 80, 80, 32, 32, 1),           # ldbq < ceil(K/2) = 40
+    (GOOD, GOOD, GOOD, 40, 64, 64, 32, 32, 1),           # ldbs < N
+    (GOOD, 0, GOOD, 32, 64, 64, 32, 32, 1),              # null Bq
+    (GOOD, GOOD, 0, 32, 64, 64, 32, 32, 1),              # null scales
+    (GOOD + 1, GOOD, GOOD, 32, 64, 64, 32, 32, 2),       # A not element-aligned
+    (0, 0, 0, 32, 0, 0, 0, 0, None),                     # K == 0: operands ignored
+])
+def test_gemm_mxfp4_argument_checks(tg, A, Bq, S, N, K, lda, ldbq, ldbs, want):
+    st = tg.tg_gemm_mxfp4(A, Bq, S, GOOD, 4, N, K, lda, ldbq, ldbs, N, None, None)
+    if want is None:
+        if _has_gpu():
+            pytest.skip("valid call would launch")
+        assert st == tg.TG_ERR_UNSUPPORTED_DEVICE
+    else:
+        assert st == want, tg.tg_status_string(st)
+
+
+def test_gemm_mxfp4_epilogue_checks(tg):
+    bf16_out = tg.tg_epilogue_ex_t(0, tg.TG_DTYPE_BF16, None, None, 0)  # input is fp16
+    assert tg.tg_gemm_mxfp4(GOOD, GOOD, GOOD, GOOD, 4, 32, 64, 64, 32, 32, 32, bf16_out,
+                            None) == tg.TG_ERR_INVALID_VALUE
+    bad_act = tg.tg_epilogue_ex_t(3, tg.TG_DTYPE_F16, None, None, 0)
+    assert tg.tg_gemm_mxfp4(GOOD, GOOD, GOOD, GOOD, 4, 32, 64, 64, 32, 32, 32, bad_act,
+                            None) == tg.TG_ERR_INVALID_VALUE
+    short_r = tg.tg_epilogue_ex_t(0, tg.TG_DTYPE_F16, None, GOOD, 16)  # ldr < N
+    assert tg.tg_gemm_mxfp4(GOOD, GOOD, GOOD, GOOD, 4, 32, 64, 64, 32, 32, 32, short_r,
+                            None) == tg.TG_ERR_INVALID_VALUE
+
+
 def test_noalloc_keeps_the_tma_layout_rule(tg):
     # the entry point without allocation has no staging buffer
     st = tg.tg_gemm_f16_noalloc(GOOD, GOOD, GOOD, 4, 4, 4, 12, 8, 8, 0, None)

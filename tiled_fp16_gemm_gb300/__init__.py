@@ -40,7 +40,7 @@ TG_KERNEL_SKINNY = 3
 EXPORTS = (
     "tg_gemm_f16", "tg_sync_status", "tg_status_string", "tg_version", "tg_plan_f16",
     "tg_tile_coord", "tg_ring_bytes", "tg_debug_set_wait_timeout_ns", "tg_debug_inject",
-    "tg_gemm_f16_noalloc", "tg_gemm_bf16", "tg_gemm_ex",
+    "tg_gemm_f16_noalloc", "tg_gemm_bf16", "tg_gemm_ex", "tg_gemm_mxfp4",
 )
 
 #: bytes of the library's fixed scratch array used by tg_gemm_f16_noalloc
@@ -93,6 +93,9 @@ def _L():
     lib.tg_gemm_ex.argtypes = [ctypes.c_int32, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64,
                                ctypes.POINTER(tg_epilogue_ex_t), _vp]
     lib.tg_gemm_ex.restype = ctypes.c_int
+    lib.tg_gemm_mxfp4.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, _i64,
+                                  ctypes.POINTER(tg_epilogue_ex_t), _vp]
+    lib.tg_gemm_mxfp4.restype = ctypes.c_int
     lib.tg_sync_status.argtypes = [_vp]
     lib.tg_sync_status.restype = ctypes.c_int
     lib.tg_status_string.argtypes = [ctypes.c_int]
@@ -143,6 +146,15 @@ def tg_gemm_ex(in_dtype: int, A: int, B: int, C: int, M: int, N: int, K: int, ld
     """C = out(act(A·B + bias) + R) with integer device pointers; returns the status code."""
     return _L().tg_gemm_ex(in_dtype, A, B, C, M, N, K, lda, ldb, ldc,
                            ctypes.byref(epi) if epi is not None else None, stream or None)
+
+
+def tg_gemm_mxfp4(A: int, Bq: int, Bscale: int, C: int, M: int, N: int, K: int, lda: int,
+                  ldbq: int, ldbs: int, ldc: int, epi: tg_epilogue_ex_t | None,
+                  stream: int | None) -> int:
+    """C = out(act(A·Bdeq + bias) + R) with B in MXFP4 (packed E2M1 codes and
+    E8M0 scales per 32 k), integer device pointers; returns the status code."""
+    return _L().tg_gemm_mxfp4(A, Bq, Bscale, C, M, N, K, lda, ldbq, ldbs, ldc,
+                              ctypes.byref(epi) if epi is not None else None, stream or None)
 
 
 def tg_sync_status(stream: int | None) -> int:
@@ -287,6 +299,60 @@ def gemm(a, b, relu: bool = False, out=None, stream=None, *, bias=None, residual
             what = entry.__name__
     if st != TG_OK:
         raise TgemmError(st, what)
+    return out
+
+
+def gemm_mxfp4(a, bq, bscale, N: int, relu: bool = False, out=None, stream=None, *, bias=None,
+               residual=None, out_dtype=None):
+    """C = out(act(a @ Bdeq + bias) + residual) with the weight in MXFP4.
+
+    a: CUDA float16 tensor M×K (row-major).  bq: CUDA uint8 tensor of N rows
+    (one per weight column, the [out][in] orientation) of packed E2M1 codes
+    along k, low nibble first (row stride a multiple of 16 bytes, at least
+    ceil(K/2)); bscale: CUDA uint8 tensor of ceil(K/32) rows of E8M0 scales
+    (row stride a multiple of 16, at least N).  N is the number of weight
+    columns.  bias, residual, out_dtype, out and stream as for ``gemm``.
+    """
+    import torch
+    _check_operand(a, "a")
+    if a.dtype != torch.float16:
+        raise TypeError("a must be float16 for the MXFP4 GEMM")
+    M, K = a.shape
+    for t, name, rows, width in ((bq, "bq", N, (K + 1) // 2), (bscale, "bscale", (K + 31) // 32, N)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.uint8 or t.dim() != 2:
+            raise TypeError(f"{name} must be a 2-D uint8 tensor")
+        if t.shape[0] != rows or t.shape[1] < width or (t.shape[1] > 1 and t.stride(1) != 1):
+            raise ValueError(f"{name} must be {rows} rows of at least {width} bytes, row-major")
+        if t.device != a.device:
+            raise ValueError(f"{name} must be on a's device")
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else torch.float16
+    if out_dtype not in (torch.float16, torch.float32):
+        raise TypeError("out_dtype must be torch.float16 or torch.float32")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    elif out.dtype != out_dtype or tuple(out.shape) != (M, N) or out.device != a.device:
+        raise ValueError("out must be M×N on a's device with dtype out_dtype")
+    if bias is not None and (bias.dtype != torch.float32 or bias.numel() != N or bias.dim() != 1
+                             or bias.device != a.device or (N > 1 and bias.stride(0) != 1)):
+        raise ValueError("bias must be a contiguous float32 CUDA tensor of N elements")
+    if residual is not None:
+        _check_operand(residual, "residual")
+        if residual.dtype != torch.float16 or tuple(residual.shape) != (M, N) \
+                or residual.device != a.device:
+            raise ValueError("residual must be M×N float16 on a's device")
+    epi = tg_epilogue_ex_t(TG_EPI_RELU if relu else TG_EPI_NONE,
+                           TG_DTYPE_F32 if out_dtype == torch.float32 else TG_DTYPE_F16,
+                           bias.data_ptr() if bias is not None else None,
+                           residual.data_ptr() if residual is not None else None,
+                           _ld(residual) if residual is not None else 0)
+    ldb = lambda t: int(t.stride(0)) if t.shape[0] > 1 else (int(t.shape[1]) + 15) // 16 * 16  # noqa
+    with torch.cuda.device(a.device):
+        s = stream if stream is not None else torch.cuda.current_stream(a.device)
+        st = tg_gemm_mxfp4(a.data_ptr(), bq.data_ptr(), bscale.data_ptr(), out.data_ptr(), M, N,
+                           K, _ld(a), ldb(bq), ldb(bscale), _ld(out), epi, s.cuda_stream)
+    if st != TG_OK:
+        raise TgemmError(st, "tg_gemm_mxfp4")
     return out
 
 

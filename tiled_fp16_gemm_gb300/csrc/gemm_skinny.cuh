@@ -48,6 +48,7 @@
 #include <utility>
 
 #include "gemm_persistent.cuh"
+#include "mxfp4.cuh"
 #include "sm103_ptx.cuh"
 #include "tile_schedule.h"
 #include "tgemm.h"
@@ -68,6 +69,38 @@ struct SkinnyCfg {
 };
 using SkinnyNarrow = SkinnyCfg<9, 64>;
 using SkinnyWide = SkinnyCfg<6, 128>;
+// MXFP4 B (M ≤ 128 weight streaming).  Per unit, one 128 n × 64 k tile of
+// packed codes (128 rows × 32 bytes, TMA 32-byte swizzle), its scales (2
+// rows × 128 bytes) and the A tile land in a deep raw ring.  Converter
+// threads each own one column n of the tile: they decode its 64 k into fp16
+// and write them with tcgen05.st straight into the tensor memory holding the
+// MMA's A operand (the weight tile is the A operand of the swapped product),
+// so decoded weights never pass through shared memory.  Tensor memory holds
+// the two accumulators (256 columns) and kStages operand stages of 32
+// columns.  Two converter groups of four warps (one per tensor-memory lane
+// quarter) take alternate units.  A raw stage is free once its group has read
+// it and the MMAs that read its A tile have completed.
+constexpr uint32_t kMxRawBytes = 128 * 32;
+constexpr uint32_t kMxScaleBytes = 2 * 128;
+constexpr int kMxConvWarps = 8;
+constexpr int kMxGroups = kMxConvWarps / 4;
+constexpr uint32_t kMxTmemCols = 512;
+constexpr uint32_t kMxOpCol0 = 256;  // first tensor-memory column of the operand stages
+// Raw ring depth for A slots of MP_MAX rows (as deep as shared memory allows).
+__host__ __device__ constexpr int mx_raw_stages(int mp_max) { return mp_max <= 64 ? 16 : 10; }
+template <int STAGES, int MP_MAX>
+struct SkinnyMxCfg {
+    static constexpr int kStages = STAGES;  // tensor-memory operand stages
+    static constexpr int kRawStages = mx_raw_stages(MP_MAX);
+    static constexpr uint32_t kASlot = MP_MAX * 64 * 2;
+    static constexpr uint32_t kStageBytes = 0;  // no shared-memory operand ring
+    static constexpr uint32_t kRawStageBytes = kASlot + kMxRawBytes + kMxScaleBytes;
+    static constexpr uint32_t kSmemBytes = 1024 + kRawStages * kRawStageBytes + 512;
+    static_assert(kMxOpCol0 + 32 * STAGES <= kMxTmemCols, "operand stages exceed tensor memory");
+};
+using SkinnyMxNarrow = SkinnyMxCfg<4, 64>;
+using SkinnyMxWide = SkinnyMxCfg<4, 128>;
+constexpr unsigned int kRoleConvert = 16u;
 constexpr uint32_t kSkTmemCols = 256;        // two accumulators of up to 128 columns
 constexpr int64_t kSkSlotFloats = 128 * 128;  // one partial: Mp ≤ 128 rows × 128 n
 constexpr int kSkMinUnitsPerCta = 8;
@@ -109,24 +142,34 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-template <int STAGES, int MP_MAX, typename T = __half>
-__global__ void __launch_bounds__(192, 1)
-    tg_gemm_f16_skinny(const __grid_constant__ CUtensorMap tmB,
-                       const __grid_constant__ CUtensorMap tmA, const SkinnyParams p) {
+// The kernel body shared by the fp16/bf16 kernel (QB = false: B^T tiles by
+// TMA) and the MXFP4 kernel (QB = true: B^T tiles decoded by warps 6..13).
+template <int STAGES, int MP_MAX, typename T, bool QB>
+__device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtensorMap* tmA,
+                                            const CUtensorMap* tmS, const SkinnyParams& p) {
     constexpr int BK = 64;
     constexpr int kSkStages = STAGES;
-    constexpr uint32_t kSkASlot = SkinnyCfg<STAGES, MP_MAX>::kASlot;
+    constexpr uint32_t kSkASlot = MP_MAX * 64 * 2;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* const base_ptr = smem_raw + (base - raw);
 
-    const uint32_t sB = base;                             // [stages] B^T tiles
-    const uint32_t sA = sB + kSkStages * kSkBBytes;       // [stages] A tiles
-    const uint32_t sBar = sA + kSkStages * kSkASlot;
-    const uint32_t bar_full = sBar;
-    const uint32_t bar_empty = sBar + 8 * kSkStages;
-    const uint32_t bar_tfull = sBar + 16 * kSkStages;
+    constexpr int kRaw = QB ? mx_raw_stages(MP_MAX) : 0;  // raw ring depth (QB)
+    constexpr int kARing = QB ? kRaw : kSkStages;         // A slots ride with B or raw
+    constexpr int kBRing = QB ? 0 : kSkStages;            // B^T tiles in shared memory
+    const uint32_t sB = base;                             // [kBRing] B^T tiles
+    const uint32_t sA = sB + kBRing * kSkBBytes;          // [kARing] A tiles
+    // QB only: [raw stages] packed codes, [raw stages] scales
+    const uint32_t sRaw = sA + kARing * kSkASlot;
+    const uint32_t sScl = sRaw + kRaw * kMxRawBytes;
+    const uint32_t sBar = sScl + kRaw * kMxScaleBytes;
+    const uint32_t bar_full = sBar;                       // [stages] A and B landed (fp16 B)
+    const uint32_t bar_empty = sBar + 8 * kSkStages;      // [stages] MMA done with the stage
+    const uint32_t bar_dec = sBar + 16 * kSkStages;       // QB: [stages] B^T decoded
+    const uint32_t bar_rfull = bar_dec + (QB ? 8 * kSkStages : 0);  // QB: [raw] landed
+    const uint32_t bar_rempty = bar_rfull + 8 * kRaw;     // QB: [raw] read and consumed
+    const uint32_t bar_tfull = bar_rempty + 8 * kRaw;
     const uint32_t bar_tempty = bar_tfull + 16;
     const uint32_t bar_drain = bar_tempty + 16;
     const uint32_t slot_tmem = bar_drain + 8;
@@ -146,6 +189,13 @@ __global__ void __launch_bounds__(192, 1)
         for (int s = 0; s < kSkStages; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
+            if (QB) mbar_init(bar_dec + 8 * s, 4);  // the four warps of one group
+        }
+        if (QB) {
+            for (int r = 0; r < kRaw; ++r) {
+                mbar_init(bar_rfull + 8 * r, 1);
+                mbar_init(bar_rempty + 8 * r, 5);  // the group's four warps + the MMA commit
+            }
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar_tfull + 8 * a, 1);
@@ -156,11 +206,13 @@ __global__ void __launch_bounds__(192, 1)
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(tmA);
+        tma_prefetch_desc(tmB);
+        if (QB) tma_prefetch_desc(tmS);
     }
+    constexpr uint32_t kTmemCols = QB ? kMxTmemCols : kSkTmemCols;
     if (warp == 1) {
-        tmem_alloc(slot_tmem, kSkTmemCols);
+        tmem_alloc(slot_tmem, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -178,42 +230,63 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             const uint64_t keep = policy_evict_last();   // A: reread by every CTA
             const uint64_t stream = policy_evict_first(); // B: read exactly once
+            // fp16 B: the operand ring (B^T + A per stage).  QB: the raw ring
+            // (codes + scales + A).
+            constexpr int kRing = QB ? kRaw : kSkStages;
+            const uint32_t ring_full = QB ? bar_rfull : bar_full;
+            const uint32_t ring_empty = QB ? bar_rempty : bar_empty;
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
+            // (tile, k block) of unit u, advanced incrementally (no division per unit)
+            int32_t t = static_cast<int32_t>(u_begin / KB);
+            int32_t kb = static_cast<int32_t>(u_begin - static_cast<int64_t>(t) * KB);
             for (int64_t u = u_begin; u < u_end; ++u) {
-                const int32_t t = static_cast<int32_t>(u / KB);
-                const int32_t kb = static_cast<int32_t>(u - t * KB);
-                if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.timeout_ns, abort_flag)) {
+                if (!mbar_wait(ring_empty + 8 * stage, phase ^ 1u, p.timeout_ns, abort_flag)) {
                     fail(kRoleProducer);
                     break;
                 }
-                const uint32_t full = bar_full + 8 * stage;
-                mbar_arrive_expect_tx(full, kSkBBytes + a_bytes);
-                const uint32_t b0 = sB + stage * kSkBBytes;
-                tma_load_2d_hint(b0, &tmB, full, t * 128, kb * BK, stream);
-                tma_load_2d_hint(b0 + 8192, &tmB, full, t * 128 + 64, kb * BK, stream);
-                tma_load_2d_hint(sA + stage * kSkASlot, &tmA, full, kb * BK, 0, keep);
+                const uint32_t full = ring_full + 8 * stage;
+                if constexpr (QB) {
+                    mbar_arrive_expect_tx(full, kMxRawBytes + kMxScaleBytes + a_bytes);
+                    tma_load_2d_hint(sRaw + stage * kMxRawBytes, tmB, full, kb * 32, t * 128,
+                                     stream);
+                    tma_load_2d_hint(sScl + stage * kMxScaleBytes, tmS, full, t * 128, kb * 2,
+                                     stream);
+                    tma_load_2d_hint(sA + stage * kSkASlot, tmA, full, kb * BK, 0, keep);
+                } else {
+                    mbar_arrive_expect_tx(full, kSkBBytes + a_bytes);
+                    const uint32_t b0 = sB + stage * kSkBBytes;
+                    tma_load_2d_hint(b0, tmB, full, t * 128, kb * BK, stream);
+                    tma_load_2d_hint(b0 + 8192, tmB, full, t * 128 + 64, kb * BK, stream);
+                    tma_load_2d_hint(sA + stage * kSkASlot, tmA, full, kb * BK, 0, keep);
+                }
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                if (++stage == kSkStages) {
+                if (++stage == kRing) {
                     stage = 0;
                     phase ^= 1u;
                 }
+                if (++kb == KB) {
+                    kb = 0;
+                    ++t;
+                }
             }
-            for (int s = 0; s < kSkStages; ++s)
+            for (int s = 0; s < kRing; ++s)
                 if (issued_mask & (1u << s))
-                    if (!mbar_wait(bar_full + 8 * s, (issued_parity >> s) & 1u, p.timeout_ns,
+                    if (!mbar_wait(ring_full + 8 * s, (issued_parity >> s) & 1u, p.timeout_ns,
                                    nullptr))
                         atomicOr(&g_wait_timeout_flags, kRoleDrain);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
+            // fp16 B: A operand = B^T tile, MN-major in shared memory.  QB: A
+            // operand = decoded weights in tensor memory (K-major).
             const uint32_t idesc =
-                idesc_f16_f32(128, p.Mp, /*a_mn=*/true, /*b_mn=*/false, Elem16<T>::kFmt);
-            int stage = 0;
-            uint32_t phase = 0;
+                idesc_f16_f32(128, p.Mp, /*a_mn=*/!QB, /*b_mn=*/false, Elem16<T>::kFmt);
+            int stage = 0, rstage = 0;
+            uint32_t phase = 0, rphase = 0;
             int it = 0;
             bool ok = true;
             for (int64_t u = u_begin; ok && u < u_end; ++it) {
@@ -228,24 +301,44 @@ __global__ void __launch_bounds__(192, 1)
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 128);
                 for (int64_t v = u; v < seg_end; ++v) {
-                    if (!mbar_wait(bar_full + 8 * stage, phase, p.timeout_ns, abort_flag)) {
+                    // QB: A (raw ring) landed and B^T (operand ring) decoded
+                    const bool got =
+                        QB ? mbar_wait(bar_rfull + 8 * rstage, rphase, p.timeout_ns, abort_flag) &&
+                                 mbar_wait(bar_dec + 8 * stage, phase, p.timeout_ns, abort_flag)
+                           : mbar_wait(bar_full + 8 * stage, phase, p.timeout_ns, abort_flag);
+                    if (!got) {
                         fail(kRoleMma);
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
                     const uint32_t b0 = sB + stage * kSkBBytes;
-                    const uint32_t a0 = sA + stage * kSkASlot;
+                    const uint32_t a0 = sA + (QB ? rstage : stage) * kSkASlot;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        const uint64_t adesc = smem_desc_sw128(b0 + 2048 * k, 8192, 1024);
                         const uint64_t bdesc = smem_desc_sw128(a0 + 32 * k, 16, 1024);
-                        mma_f16_ss(d_tmem, adesc, bdesc, idesc, (v != u || k != 0) ? 1u : 0u);
+                        const uint32_t acc_in = (v != u || k != 0) ? 1u : 0u;
+                        if constexpr (QB) {
+                            // 16 k = 8 columns of the operand stage
+                            const uint32_t a_tmem = tmem_base + kMxOpCol0 +
+                                                    static_cast<uint32_t>(32 * stage + 8 * k);
+                            mx_mma_f16_ts(d_tmem, a_tmem, bdesc, idesc, acc_in);
+                        } else {
+                            const uint64_t adesc = smem_desc_sw128(b0 + 2048 * k, 8192, 1024);
+                            mma_f16_ss(d_tmem, adesc, bdesc, idesc, acc_in);
+                        }
                     }
                     mma_commit(bar_empty + 8 * stage);
                     if (++stage == kSkStages) {
                         stage = 0;
                         phase ^= 1u;
+                    }
+                    if (QB) {
+                        mma_commit(bar_rempty + 8 * rstage);  // its A tile is consumed
+                        if (++rstage == kRaw) {
+                            rstage = 0;
+                            rphase ^= 1u;
+                        }
                     }
                 }
                 if (!ok) break;
@@ -256,7 +349,7 @@ __global__ void __launch_bounds__(192, 1)
             if (!mbar_wait(bar_drain, 0, p.timeout_ns, nullptr))
                 atomicOr(&g_wait_timeout_flags, kRoleDrain);
         }
-    } else {
+    } else if (warp < 6) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
         const int n_local = 32 * q + lane;
@@ -371,6 +464,83 @@ __global__ void __launch_bounds__(192, 1)
             }
             u = seg_end;
         }
+    } else if constexpr (QB) {
+        // ------------------------------------------------------------ converters (QB)
+        // Warp cw = warp - 6 is in group g = cw / 4 and owns tensor-memory
+        // lane quarter q = warp % 4.  For each unit of local index i ≡ g (mod
+        // kMxGroups), thread l decodes column n = 32 q + l of the tile: its 64
+        // k codes (32 bytes: row n of the codes tile, 32-byte swizzle) with the
+        // two block scales of the unit, into 32 columns of fp16 pairs (lower k
+        // in the low half), stored to its lane of the unit's operand stage.
+        const int cw = warp - 6;
+        const int g = cw / 4;
+        const uint32_t q = static_cast<uint32_t>(warp & 3);
+        const uint32_t n_local = 32u * q + static_cast<uint32_t>(lane);
+        const uint32_t swz32 = (n_local >> 2) & 1u;
+        const uint32_t lane_addr = (32u * q) << 16;
+        for (int64_t i = g; u_begin + i < u_end; i += kMxGroups) {
+            const int stage = static_cast<int>(i % kSkStages);
+            const uint32_t phase = static_cast<uint32_t>((i / kSkStages) & 1);
+            const int rstage = static_cast<int>(i % kRaw);
+            const uint32_t rphase = static_cast<uint32_t>((i / kRaw) & 1);
+            int ok = 1;
+            if (lane == 0) {
+                ok = mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.timeout_ns, abort_flag) ? 1
+                                                                                            : 0;
+                if (ok)
+                    ok = mbar_wait(bar_rfull + 8 * rstage, rphase, p.timeout_ns, abort_flag) ? 1
+                                                                                             : 0;
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) fail(kRoleConvert);
+                break;
+            }
+            tc_fence_after_sync();  // the MMAs that read this operand stage have completed
+            const uint32_t row = sRaw + static_cast<uint32_t>(rstage) * kMxRawBytes + 32u * n_local;
+            const uint4 c0 = mx_ld_shared_v4(row + (swz32 << 4));
+            const uint4 c1 = mx_ld_shared_v4(row + ((swz32 ^ 1u) << 4));
+            const uint32_t scl = sScl + static_cast<uint32_t>(rstage) * kMxScaleBytes + n_local;
+            const uint32_t X0 = mx_ld_shared_u8(scl);
+            const uint32_t X1 = mx_ld_shared_u8(scl + 128u);
+            const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            uint32_t d[32];
+            if (mx_fast_scale(X0) && mx_fast_scale(X1)) {
+                const uint32_t f0 = mx_factor_bits(X0) * 0x10001u;  // both halves
+                const uint32_t f1 = mx_factor_bits(X1) * 0x10001u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t f = j < 4 ? f0 : f1;  // words 0..3: k 0..31
+                    const uint32_t fj[4] = {f, f, f, f};
+                    const uint4 o = mx_decode8_fast(w[j], fj);
+                    d[4 * j] = o.x;
+                    d[4 * j + 1] = o.y;
+                    d[4 * j + 2] = o.z;
+                    d[4 * j + 3] = o.w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t xb = j < 4 ? X0 : X1;
+                    const uint32_t x[8] = {xb, xb, xb, xb, xb, xb, xb, xb};
+                    const uint4 o = mx_decode8_exact(w[j], x);
+                    d[4 * j] = o.x;
+                    d[4 * j + 1] = o.y;
+                    d[4 * j + 2] = o.z;
+                    d[4 * j + 3] = o.w;
+                }
+            }
+            __syncwarp();
+            mx_tmem_st_x32(tmem_base + lane_addr + kMxOpCol0 + static_cast<uint32_t>(32 * stage),
+                           d);
+            mx_tmem_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar_rempty + 8 * rstage);
+                mbar_arrive(bar_dec + 8 * stage);
+            }
+        }
     }
 
     tc_fence_before_sync();
@@ -378,8 +548,24 @@ __global__ void __launch_bounds__(192, 1)
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, kSkTmemCols);
+        tmem_dealloc(tmem_base, kTmemCols);
     }
+}
+
+template <int STAGES, int MP_MAX, typename T = __half>
+__global__ void __launch_bounds__(192, 1)
+    tg_gemm_f16_skinny(const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmA, const SkinnyParams p) {
+    skinny_body<STAGES, MP_MAX, T, false>(&tmB, &tmA, nullptr, p);
+}
+
+// C = epi(A · Bdeq) with B in MXFP4 (mxfp4.cuh), M ≤ 128, A fp16.
+template <int STAGES, int MP_MAX>
+__global__ void __launch_bounds__(192 + 32 * kMxConvWarps, 1)
+    tg_gemm_mxfp4_skinny(const __grid_constant__ CUtensorMap tmBq,
+                         const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmS, const SkinnyParams p) {
+    skinny_body<STAGES, MP_MAX, __half, true>(&tmBq, &tmA, &tmS, p);
 }
 
 // ------------------------------------------------------------------ host side
@@ -422,6 +608,30 @@ inline void skinny_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_pla
     pl->cluster = 1;
 }
 
+// The MXFP4 kernel: the same units and split, its own rings and 448 threads.
+inline void skinny_mx_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* pl) {
+    skinny_plan(M, N, K, num_sms, pl);
+    const bool narrow = pl->bm <= 64;
+    pl->stages = narrow ? SkinnyMxNarrow::kStages : SkinnyMxWide::kStages;
+    pl->threads = 192 + 32 * kMxConvWarps;
+    pl->smem_bytes = narrow ? SkinnyMxNarrow::kSmemBytes : SkinnyMxWide::kSmemBytes;
+    pl->ring_bytes = narrow ? int64_t{SkinnyMxNarrow::kStages} * SkinnyMxNarrow::kStageBytes +
+                                  int64_t{SkinnyMxNarrow::kRawStages} *
+                                      SkinnyMxNarrow::kRawStageBytes
+                            : int64_t{SkinnyMxWide::kStages} * SkinnyMxWide::kStageBytes +
+                                  int64_t{SkinnyMxWide::kRawStages} * SkinnyMxWide::kRawStageBytes;
+}
+
+inline cudaError_t skinny_mx_set_attributes() {
+    cudaError_t e = cudaFuncSetAttribute(tg_gemm_mxfp4_skinny<SkinnyMxNarrow::kStages, 64>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SkinnyMxNarrow::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(tg_gemm_mxfp4_skinny<SkinnyMxWide::kStages, 128>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                SkinnyMxWide::kSmemBytes);
+}
+
 template <typename T>
 inline cudaError_t skinny_set_attributes() {
     cudaError_t e = cudaFuncSetAttribute(tg_gemm_f16_skinny<9, 64, T>,
@@ -456,6 +666,30 @@ inline cudaError_t skinny_launch_kernel(const CUtensorMap& tmB, const CUtensorMa
     return cudaLaunchKernelEx(&cfg, tg_gemm_f16_skinny<6, 128, T>, tmB, tmA, prm);
 }
 
+// Cooperative launch of the MXFP4 instantiation whose A slots fit prm.Mp.
+inline cudaError_t skinny_mx_launch_kernel(const CUtensorMap& tmBq, const CUtensorMap& tmA,
+                                           const CUtensorMap& tmS, const SkinnyParams& prm,
+                                           int64_t grid, cudaStream_t stream) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(192 + 32 * kMxConvWarps);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (prm.Mp <= 64) {
+        cfg.dynamicSmemBytes = SkinnyMxNarrow::kSmemBytes;
+        return cudaLaunchKernelEx(&cfg, tg_gemm_mxfp4_skinny<SkinnyMxNarrow::kStages, 64>, tmBq,
+                                  tmA, tmS, prm);
+    }
+    cfg.dynamicSmemBytes = SkinnyMxWide::kSmemBytes;
+    return cudaLaunchKernelEx(&cfg, tg_gemm_mxfp4_skinny<SkinnyMxWide::kStages, 128>, tmBq, tmA,
+                              tmS, prm);
+}
+
 struct SkinnyWorkspace {
     float* partials = nullptr;
     uint32_t* flags = nullptr;
@@ -481,6 +715,46 @@ inline void skinny_reset_flags(int dev) {
             cudaMemset(kv.second.flags, 0, 4 * kv.second.slots * sizeof(uint32_t));
 }
 
+// The split-K workspace of (dev, stream) into prm (ws, flags, epoch); sized on
+// first use for the largest grid, so later calls never grow it.
+inline tg_status_t skinny_workspace(int dev, cudaStream_t stream, int64_t grid, int64_t max_ctas,
+                                    SkinnyParams* prm) {
+    {
+        std::lock_guard<std::mutex> lk(skinny_ws_mutex());
+        SkinnyWorkspace& ws = skinny_ws_map()[std::make_pair(dev, stream)];
+        if (ws.slots < grid) {
+            // First use on this stream: room for the largest grid (one CTA
+            // per SM), so later calls, graph captures included, never grow it.
+            if (ws.partials) {
+                cudaStreamSynchronize(stream);
+                cudaFree(ws.partials);
+                cudaFree(ws.flags);
+                ws.partials = nullptr;
+                ws.flags = nullptr;
+                ws.slots = 0;
+            }
+            const int64_t slots = grid > max_ctas ? grid : max_ctas;
+            if (cudaMalloc(&ws.partials, slots * kSkSlotFloats * sizeof(float)) != cudaSuccess ||
+                cudaMalloc(&ws.flags, 4 * slots * sizeof(uint32_t)) != cudaSuccess) {
+                cudaGetLastError();
+                if (ws.partials) cudaFree(ws.partials);
+                ws.partials = nullptr;
+                ws.flags = nullptr;
+                return TG_ERR_NO_MEMORY;
+            }
+            if (cudaMemsetAsync(ws.flags, 0, 4 * slots * sizeof(uint32_t), stream) != cudaSuccess) {
+                cudaGetLastError();
+                return TG_ERR_LAUNCH;
+            }
+            ws.slots = slots;
+        }
+        prm->ws = ws.partials;
+        prm->flags = ws.flags;
+        prm->epoch = 1;  // flags are zero between launches (owners clear them)
+    }
+    return TG_OK;
+}
+
 using EncodeFn = bool (*)(CUtensorMap*, const void*, uint64_t, uint64_t, uint64_t, uint32_t,
                           uint32_t, CUtensorMapDataType);
 
@@ -499,39 +773,8 @@ inline tg_status_t skinny_launch(const void* A, const void* B, void* C, const tg
         return TG_ERR_LAUNCH;
 
     SkinnyParams prm;
-    {
-        std::lock_guard<std::mutex> lk(skinny_ws_mutex());
-        SkinnyWorkspace& ws = skinny_ws_map()[std::make_pair(dev, stream)];
-        if (ws.slots < pl.grid) {
-            // First use on this stream: room for the largest grid (one CTA
-            // per SM), so later calls, graph captures included, never grow it.
-            if (ws.partials) {
-                cudaStreamSynchronize(stream);
-                cudaFree(ws.partials);
-                cudaFree(ws.flags);
-                ws.partials = nullptr;
-                ws.flags = nullptr;
-                ws.slots = 0;
-            }
-            const int64_t slots = pl.grid > max_ctas ? pl.grid : max_ctas;
-            if (cudaMalloc(&ws.partials, slots * kSkSlotFloats * sizeof(float)) != cudaSuccess ||
-                cudaMalloc(&ws.flags, 4 * slots * sizeof(uint32_t)) != cudaSuccess) {
-                cudaGetLastError();
-                if (ws.partials) cudaFree(ws.partials);
-                ws.partials = nullptr;
-                ws.flags = nullptr;
-                return TG_ERR_NO_MEMORY;
-            }
-            if (cudaMemsetAsync(ws.flags, 0, 4 * slots * sizeof(uint32_t), stream) != cudaSuccess) {
-                cudaGetLastError();
-                return TG_ERR_LAUNCH;
-            }
-            ws.slots = slots;
-        }
-        prm.ws = ws.partials;
-        prm.flags = ws.flags;
-        prm.epoch = 1;  // flags are zero between launches (owners clear them)
-    }
+    const tg_status_t wst = skinny_workspace(dev, stream, pl.grid, max_ctas, &prm);
+    if (wst != TG_OK) return wst;
     prm.M = static_cast<int32_t>(M);
     prm.N = static_cast<int32_t>(N);
     prm.K = static_cast<int32_t>(K);
@@ -548,6 +791,51 @@ inline tg_status_t skinny_launch(const void* A, const void* B, void* C, const tg
     prm.ldc = ldc;
 
     if (skinny_launch_kernel<T>(tmB, tmA, prm, pl.grid, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return TG_ERR_LAUNCH;
+    }
+    return TG_OK;
+}
+
+using EncodeSwFn = bool (*)(CUtensorMap*, const void*, uint64_t, uint64_t, uint64_t, uint32_t,
+                            uint32_t, CUtensorMapDataType, CUtensorMapSwizzle);
+
+// MXFP4 B: Bq (N rows of ceil(K/2) packed bytes along k, stride ldbq) and S
+// (ceil(K/32) rows of N scale bytes, stride lds); A fp16.  Pointers 16-byte
+// aligned and ldbq, lds multiples of 16, lda of 8 (checked by the caller).
+inline tg_status_t skinny_mx_launch(const void* A, const void* Bq, const void* S, void* C,
+                                    const tg_plan_t& pl, int64_t M, int64_t N, int64_t K,
+                                    int64_t lda, int64_t ldbq, int64_t lds, int64_t ldc,
+                                    const EpilogueSpec& ep, cudaStream_t stream, int dev,
+                                    int64_t max_ctas, uint64_t timeout_ns, int32_t inject,
+                                    EncodeSwFn encode) {
+    const int64_t Mp = pl.mma_n;
+    CUtensorMap tmBq, tmA, tmS;
+    if (!encode(&tmBq, Bq, static_cast<uint64_t>((K + 1) / 2), N, ldbq, 32, 128,
+                CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !encode(&tmS, S, N, (K + 31) / 32, lds, 128, 2, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode(&tmA, A, K, M, lda * 2, 64, static_cast<uint32_t>(Mp),
+                CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CU_TENSOR_MAP_SWIZZLE_128B))
+        return TG_ERR_LAUNCH;
+    SkinnyParams prm;
+    const tg_status_t wst = skinny_workspace(dev, stream, pl.grid, max_ctas, &prm);
+    if (wst != TG_OK) return wst;
+    prm.M = static_cast<int32_t>(M);
+    prm.N = static_cast<int32_t>(N);
+    prm.K = static_cast<int32_t>(K);
+    prm.Mp = static_cast<int32_t>(Mp);
+    prm.tiles_n = static_cast<int32_t>(pl.tiles_n);
+    prm.k_blocks = static_cast<int32_t>(pl.k_blocks);
+    prm.total_units = pl.tiles_n * pl.k_blocks;
+    prm.relu = ep.relu;
+    prm.e = ep.e;
+    prm.out_f32 = ep.out_f32;
+    prm.inject = inject;
+    prm.timeout_ns = timeout_ns;
+    prm.C = C;
+    prm.ldc = ldc;
+    if (skinny_mx_launch_kernel(tmBq, tmA, tmS, prm, pl.grid, stream) != cudaSuccess) {
         cudaGetLastError();
         return TG_ERR_LAUNCH;
     }

@@ -162,7 +162,8 @@ tg_status_t current_device(int* dev, DeviceState** st) {
     if (!s.supported) return TG_ERR_UNSUPPORTED_DEVICE;
     if (!s.attrs_set) {
         if (set_kernel_attributes<__half>() != cudaSuccess ||
-            set_kernel_attributes<__nv_bfloat16>() != cudaSuccess) {
+            set_kernel_attributes<__nv_bfloat16>() != cudaSuccess ||
+            tg::skinny_mx_set_attributes() != cudaSuccess) {
             cudaGetLastError();
             return TG_ERR_LAUNCH;
         }
@@ -200,11 +201,11 @@ constexpr CUtensorMapDataType tensor_map_type() {
                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
-// 2-D 16-bit tensor map: inner (contiguous) extent, outer extent, row stride
-// in bytes, box, 128-byte swizzle, zero fill outside the tensor.
-bool encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
-               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-               CUtensorMapDataType dtype) {
+// 2-D tensor map: inner (contiguous) extent, outer extent, row stride in
+// bytes, box, swizzle, zero fill outside the tensor.
+bool encode_2d_sw(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                  CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle) {
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[2] = {inner, outer};
@@ -212,9 +213,17 @@ bool encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// The same with the 128-byte swizzle of every 16-bit operand tile.
+bool encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapDataType dtype) {
+    return encode_2d_sw(map, ptr, inner, outer, row_bytes, box_inner, box_outer, dtype,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // A, B and C maps of the pair / one-CTA kernels.  C: 32 rows × 128 bytes per
@@ -528,6 +537,43 @@ tg_status_t validate_ex(int32_t in_dtype, const void* C, int64_t M, int64_t N,
     return TG_OK;
 }
 
+// Per-(device, stream) fp16 buffer for dequantised MXFP4 weights (M > 128
+// path); grown on demand like the staging buffer.
+std::mutex g_deq_mutex;
+std::map<std::pair<int, cudaStream_t>, Staging> g_deq;
+
+tg_status_t dequant_buffer(int dev, cudaStream_t s, size_t bytes, void** out) {
+    std::lock_guard<std::mutex> lk(g_deq_mutex);
+    Staging& st = g_deq[std::make_pair(dev, s)];
+    if (st.bytes < bytes) {
+        if (st.ptr) {
+            if (cudaStreamSynchronize(s) != cudaSuccess || cudaFree(st.ptr) != cudaSuccess) {
+                cudaGetLastError();
+                return TG_ERR_LAUNCH;
+            }
+            st.ptr = nullptr;
+            st.bytes = 0;
+        }
+        if (cudaMalloc(&st.ptr, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            st.ptr = nullptr;
+            return TG_ERR_NO_MEMORY;
+        }
+        st.bytes = bytes;
+    }
+    *out = st.ptr;
+    return TG_OK;
+}
+
+// Whether TGEMM_FORCE_CFG names one of the dense tile kernels (the MXFP4
+// entry point then takes its dequantise-then-GEMM path even for M <= 128).
+bool forced_dense_kernel() {
+    const char* f = std::getenv("TGEMM_FORCE_CFG");
+    return f != nullptr && (std::strcmp(f, "pair256") == 0 ||
+                            std::strcmp(f, "persistent256") == 0 ||
+                            std::strcmp(f, "persistent128") == 0);
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -656,6 +702,83 @@ tg_status_t tg_gemm_ex(int32_t in_dtype, const void* A, const void* B, void* C, 
     if (in_dtype == TG_DTYPE_BF16)
         return gemm_impl<__nv_bfloat16>(A, B, C, M, N, K, lda, ldb, ldc, ep, stream);
     return gemm_impl<__half>(A, B, C, M, N, K, lda, ldb, ldc, ep, stream);
+}
+
+tg_status_t tg_gemm_mxfp4(const void* A, const void* Bq, const void* Bscale, void* C, int64_t M,
+                          int64_t N, int64_t K, int64_t lda, int64_t ldbq, int64_t ldbs,
+                          int64_t ldc, const tg_epilogue_ex_t* epi, void* stream) {
+    tg_epilogue_ex_t x;
+    if (epi != nullptr) {
+        x = *epi;
+    } else {
+        std::memset(&x, 0, sizeof(x));
+        x.activation = TG_EPI_NONE;
+        x.out_dtype = TG_DTYPE_F16;
+    }
+    if (x.activation != TG_EPI_NONE && x.activation != TG_EPI_RELU) return TG_ERR_INVALID_VALUE;
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return TG_ERR_INVALID_VALUE;
+    tg_status_t st = validate_ex(TG_DTYPE_F16, C, M, N, x);
+    if (st != TG_OK || M == 0 || N == 0) return st;
+    if (C == nullptr || ldc < N) return TG_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(C) & 1u) != 0) return TG_ERR_MISALIGNED;
+    if (K > 0) {
+        if (A == nullptr || Bq == nullptr || Bscale == nullptr || lda < K ||
+            ldbq < (K + 1) / 2 || ldbs < N)
+            return TG_ERR_INVALID_VALUE;
+        if ((reinterpret_cast<uintptr_t>(A) & 1u) != 0 ||
+            (reinterpret_cast<uintptr_t>(Bq) & 15u) != 0 ||
+            (reinterpret_cast<uintptr_t>(Bscale) & 15u) != 0 || (ldbq & 15) != 0 ||
+            (ldbs & 15) != 0)
+            return TG_ERR_MISALIGNED;
+    }
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    st = current_device(&dev, &ds);
+    if (st != TG_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    tg::EpilogueSpec ep = plain_epilogue(x.activation);
+    ep.out_f32 = x.out_dtype == TG_DTYPE_F32 ? 1 : 0;
+    ep.e.bias = x.bias;
+    ep.e.resid = x.residual;
+    ep.e.ldr = x.residual != nullptr ? x.ldr : 0;
+    ep.e.bias_vec = (reinterpret_cast<uintptr_t>(x.bias) & 15u) == 0 ? 1 : 0;
+    ep.e.resid_vec =
+        (reinterpret_cast<uintptr_t>(x.residual) & 15u) == 0 && (x.ldr & 7) == 0 ? 1 : 0;
+    if (K == 0)  // the product is +0: only the epilogue remains
+        return gemm_impl<__half>(nullptr, nullptr, C, M, N, 0, 0, 0, ldc, ep, stream);
+
+    if (M <= 128 && !forced_dense_kernel()) {
+        // Weight streaming: decode inside the split-K kernel.
+        tg_plan_t pl;
+        std::memset(&pl, 0, sizeof(pl));
+        tg::skinny_mx_plan(M, N, K, ds->num_sms, &pl);
+        const void* A2 = A;
+        int64_t lda2 = lda;
+        if (!tma_layout_ok(A, lda)) {  // A in the staging buffer, rows 16-byte aligned
+            lda2 = round_up8(K);
+            void* buf = nullptr;
+            st = staging_buffer(dev, s, static_cast<size_t>(M * lda2 * 2), &buf);
+            if (st != TG_OK) return st;
+            if ((st = copy_matrix(A, lda, buf, lda2, M, K, 2, ds->num_sms, s)) != TG_OK) return st;
+            A2 = buf;
+        }
+        return tg::skinny_mx_launch(A2, Bq, Bscale, C, pl, M, N, K, lda2, ldbq, ldbs, ldc, ep,
+                                    s, dev, ds->num_sms, g_timeout_ns.load(),
+                                    g_inject.exchange(0), encode_2d_sw);
+    }
+    // Compute-bound sizes: dequantise once to fp16, then the dense GEMM.
+    const int64_t ldd = round_up8(N);
+    void* deq = nullptr;
+    st = dequant_buffer(dev, s, static_cast<size_t>(K * ldd * 2), &deq);
+    if (st != TG_OK) return st;
+    const int64_t tiles = ((K + 63) / 64) * ((N + 63) / 64);  // 64 × 64 per block iteration
+    const unsigned grid = static_cast<unsigned>(tiles < 8 * ds->num_sms ? tiles : 8 * ds->num_sms);
+    tg::tg_mxfp4_dequant_f16<<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(Bq), ldbq,
+                                                  static_cast<const uint8_t*>(Bscale), ldbs, K, N,
+                                                  static_cast<uint16_t*>(deq), ldd);
+    if (cudaGetLastError() != cudaSuccess) return TG_ERR_LAUNCH;
+    return gemm_impl<__half>(A, deq, C, M, N, K, lda, ldd, ldc, ep, stream);
 }
 
 tg_status_t tg_sync_status(void* stream) {

@@ -137,3 +137,71 @@ def sample_positions(M: int, N: int, BM: int, BN: int, seed: int, n_random: int 
         rows.append(np.arange(M, dtype=np.int64))
         cols.append(np.full(M, c, dtype=np.int64))
     return (np.concatenate(rows).astype(np.int64), np.concatenate(cols).astype(np.int64))
+
+
+# ------------------------------------------------------------------ MXFP4 weights
+
+@dataclasses.dataclass(frozen=True)
+class MxWorkload:
+    """A fp16 (M×K) times an MXFP4 weight (K×N): packed E2M1 codes and E8M0
+    scales, both drawn as plain random bytes (no encoder involved)."""
+    name: str
+    M: int
+    N: int
+    K: int
+    relu: bool
+    dist_a: tuple
+    scale_lo: int  # E8M0 scale bytes drawn uniformly from [scale_lo, scale_hi]
+    scale_hi: int
+    seed: int
+    note: str = ""
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def min_bytes(self) -> int:
+        """A read once, packed codes (K/2 bytes per weight column) and scales
+        (N per 32 k) read once, C written once (fp16)."""
+        return (2 * self.M * self.K + self.N * ((self.K + 1) // 2)
+                + ((self.K + 31) // 32) * self.N + 2 * self.M * self.N)
+
+
+MX_WORKLOADS = {
+    w.name: w
+    for w in [
+        MxWorkload("mxfp4_skinny_64x16384x8192", 64, 16384, 8192, False, ("normal", 0.0, 1.0),
+                   118, 122, 7,
+                   "weight streaming with MXFP4 weights: the skinny shape's B at 0.53 bytes "
+                   "per weight (64 MiB of codes + 4 MiB of scales)"),
+        MxWorkload("mxfp4_mlp_8192x28672x4096_relu", 8192, 28672, 4096, True,
+                   ("normal", 0.0, 1.0 / 64.0), 118, 122, 8,
+                   "the MLP shape with MXFP4 weights (dequantise-then-GEMM path)"),
+    ]
+}
+
+
+def round16(x: int) -> int:
+    return (x + 15) // 16 * 16
+
+
+def draw_mxfp4(rng: np.random.Generator, K: int, N: int, scale_lo: int, scale_hi: int,
+               ldbq: int | None = None, lds: int | None = None):
+    """(Bq, S): N × ldbq random bytes (a weight column's codes along k, two
+    4-bit codes per byte; every code value equally likely) and ceil(K/32) ×
+    lds scale bytes uniform in [scale_lo, scale_hi].  Default row strides are
+    rounded up to 16 bytes.  Padding bytes are random too (a correct GEMM
+    never decodes them)."""
+    ldbq = round16((K + 1) // 2) if ldbq is None else ldbq
+    lds = round16(N) if lds is None else lds
+    Bq = rng.integers(0, 256, size=(N, ldbq), dtype=np.uint8)
+    S = rng.integers(scale_lo, scale_hi + 1, size=((K + 31) // 32, lds), dtype=np.uint8)
+    return Bq, S
+
+
+def mx_workload_inputs(w: MxWorkload):
+    """(A float16 M×K, Bq, S) for an MXFP4 workload."""
+    A = draw(np.random.default_rng([w.seed, 0]), w.dist_a, w.M, w.K).astype(np.float16)
+    Bq, S = draw_mxfp4(np.random.default_rng([w.seed, 1]), w.K, w.N, w.scale_lo, w.scale_hi)
+    return A, Bq, S
