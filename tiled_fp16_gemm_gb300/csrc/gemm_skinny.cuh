@@ -87,7 +87,7 @@ constexpr int kMxGroups = kMxConvWarps / 4;
 constexpr uint32_t kMxTmemCols = 512;
 constexpr uint32_t kMxOpCol0 = 256;  // first tensor-memory column of the operand stages
 // Raw ring depth for A slots of MP_MAX rows (as deep as shared memory allows).
-__host__ __device__ constexpr int mx_raw_stages(int mp_max) { return mp_max <= 64 ? 16 : 10; }
+__host__ __device__ constexpr int mx_raw_stages(int mp_max) { return mp_max <= 64 ? 16 : 8; }
 template <int STAGES, int MP_MAX>
 struct SkinnyMxCfg {
     static constexpr int kStages = STAGES;  // tensor-memory operand stages
@@ -101,6 +101,22 @@ struct SkinnyMxCfg {
 using SkinnyMxNarrow = SkinnyMxCfg<4, 64>;
 using SkinnyMxWide = SkinnyMxCfg<4, 128>;
 constexpr unsigned int kRoleConvert = 16u;
+
+// Load issue is split over several producer threads (one per warp): one
+// thread's loop of slot wait, transaction arming and TMA issue costs a few
+// hundred cycles per unit whatever the box size, which alone would cap a
+// skinny kernel far below HBM bandwidth.  Producer p takes the units of local
+// index i ≡ p (mod count); the count divides the ring depth, so each ring
+// stage always belongs to the same producer.
+__host__ __device__ constexpr int skinny_producers(int ring) {
+    return ring % 4 == 0 ? 4 : (ring % 3 == 0 ? 3 : (ring % 2 == 0 ? 2 : 1));
+}
+// Threads of a skinny kernel: producer 0, MMA, 4 epilogue warps, the
+// converter warps (MXFP4), then producers 1 .. count - 1.
+__host__ __device__ constexpr int skinny_threads(int stages, int mp_max, bool qb) {
+    return 32 * (6 + (qb ? kMxConvWarps : 0) +
+                 skinny_producers(qb ? mx_raw_stages(mp_max) : stages) - 1);
+}
 constexpr uint32_t kSkTmemCols = 256;        // two accumulators of up to 128 columns
 constexpr int64_t kSkSlotFloats = 128 * 128;  // one partial: Mp ≤ 128 rows × 128 n
 constexpr int kSkMinUnitsPerCta = 8;
@@ -225,23 +241,28 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
         *abort_flag = 1;
     };
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    // fp16 B: the operand ring (B^T + A per stage).  QB: the raw ring (codes +
+    // scales + A).
+    constexpr int kRing = QB ? kRaw : kSkStages;
+    constexpr int kProd = skinny_producers(kRing);
+    constexpr int kProdWarp1 = 6 + (QB ? kMxConvWarps : 0);  // warp of producer 1
+    const int prod = warp == 0 ? 0 : (warp >= kProdWarp1 ? warp - kProdWarp1 + 1 : -1);
+    if (prod >= 0) {
+        // ------------------------------------------------------------ producers
         if (lane == 0) {
             const uint64_t keep = policy_evict_last();   // A: reread by every CTA
             const uint64_t stream = policy_evict_first(); // B: read exactly once
-            // fp16 B: the operand ring (B^T + A per stage).  QB: the raw ring
-            // (codes + scales + A).
-            constexpr int kRing = QB ? kRaw : kSkStages;
             const uint32_t ring_full = QB ? bar_rfull : bar_full;
             const uint32_t ring_empty = QB ? bar_rempty : bar_empty;
-            int stage = 0;
-            uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
-            // (tile, k block) of unit u, advanced incrementally (no division per unit)
-            int32_t t = static_cast<int32_t>(u_begin / KB);
-            int32_t kb = static_cast<int32_t>(u_begin - static_cast<int64_t>(t) * KB);
-            for (int64_t u = u_begin; u < u_end; ++u) {
+            // (tile, k block) of this producer's next unit, advanced by kProd
+            // units per step (no division per unit)
+            const int64_t u0 = u_begin + prod;
+            int32_t t = static_cast<int32_t>(u0 / KB);
+            int32_t kb = static_cast<int32_t>(u0 - static_cast<int64_t>(t) * KB);
+            for (int64_t i = prod; u_begin + i < u_end; i += kProd) {
+                const int stage = static_cast<int>(i % kRing);
+                const uint32_t phase = static_cast<uint32_t>((i / kRing) & 1);
                 if (!mbar_wait(ring_empty + 8 * stage, phase ^ 1u, p.timeout_ns, abort_flag)) {
                     fail(kRoleProducer);
                     break;
@@ -263,12 +284,9 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                 }
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                if (++stage == kRing) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-                if (++kb == KB) {
-                    kb = 0;
+                kb += kProd;
+                while (kb >= KB) {
+                    kb -= static_cast<int32_t>(KB);
                     ++t;
                 }
             }
@@ -349,7 +367,7 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
             if (!mbar_wait(bar_drain, 0, p.timeout_ns, nullptr))
                 atomicOr(&g_wait_timeout_flags, kRoleDrain);
         }
-    } else if (warp < 6) {
+    } else if (warp >= 2 && warp < 6) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
         const int n_local = 32 * q + lane;
@@ -466,6 +484,7 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
         }
     } else if constexpr (QB) {
         // ------------------------------------------------------------ converters (QB)
+        // (warps 6 .. 6 + kMxConvWarps - 1)
         // Warp cw = warp - 6 is in group g = cw / 4 and owns tensor-memory
         // lane quarter q = warp % 4.  For each unit of local index i ≡ g (mod
         // kMxGroups), thread l decodes column n = 32 q + l of the tile: its 64
@@ -553,7 +572,7 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
 }
 
 template <int STAGES, int MP_MAX, typename T = __half>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(skinny_threads(STAGES, MP_MAX, false), 1)
     tg_gemm_f16_skinny(const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmA, const SkinnyParams p) {
     skinny_body<STAGES, MP_MAX, T, false>(&tmB, &tmA, nullptr, p);
@@ -561,7 +580,7 @@ __global__ void __launch_bounds__(192, 1)
 
 // C = epi(A · Bdeq) with B in MXFP4 (mxfp4.cuh), M ≤ 128, A fp16.
 template <int STAGES, int MP_MAX>
-__global__ void __launch_bounds__(192 + 32 * kMxConvWarps, 1)
+__global__ void __launch_bounds__(skinny_threads(STAGES, MP_MAX, true), 1)
     tg_gemm_mxfp4_skinny(const __grid_constant__ CUtensorMap tmBq,
                          const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmS, const SkinnyParams p) {
@@ -595,7 +614,8 @@ inline void skinny_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_pla
     if (G < 1) G = 1;
     if (G > num_sms) G = num_sms;
     pl->grid = G;
-    pl->threads = 192;
+    pl->threads = narrow ? skinny_threads(SkinnyNarrow::kStages, 64, false)
+                         : skinny_threads(SkinnyWide::kStages, 128, false);
     pl->group_m = 1;
     pl->smem_bytes = narrow ? SkinnyNarrow::kSmemBytes : SkinnyWide::kSmemBytes;
     pl->ring_bytes = narrow ? int64_t{SkinnyNarrow::kStages} * SkinnyNarrow::kStageBytes
@@ -613,7 +633,8 @@ inline void skinny_mx_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_
     skinny_plan(M, N, K, num_sms, pl);
     const bool narrow = pl->bm <= 64;
     pl->stages = narrow ? SkinnyMxNarrow::kStages : SkinnyMxWide::kStages;
-    pl->threads = 192 + 32 * kMxConvWarps;
+    pl->threads = narrow ? skinny_threads(SkinnyMxNarrow::kStages, 64, true)
+                         : skinny_threads(SkinnyMxWide::kStages, 128, true);
     pl->smem_bytes = narrow ? SkinnyMxNarrow::kSmemBytes : SkinnyMxWide::kSmemBytes;
     pl->ring_bytes = narrow ? int64_t{SkinnyMxNarrow::kStages} * SkinnyMxNarrow::kStageBytes +
                                   int64_t{SkinnyMxNarrow::kRawStages} *
@@ -654,7 +675,8 @@ inline cudaError_t skinny_launch_kernel(const CUtensorMap& tmB, const CUtensorMa
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(192);
+    cfg.blockDim = dim3(prm.Mp <= 64 ? skinny_threads(SkinnyNarrow::kStages, 64, false)
+                                     : skinny_threads(SkinnyWide::kStages, 128, false));
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -676,7 +698,8 @@ inline cudaError_t skinny_mx_launch_kernel(const CUtensorMap& tmBq, const CUtens
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(192 + 32 * kMxConvWarps);
+    cfg.blockDim = dim3(prm.Mp <= 64 ? skinny_threads(SkinnyMxNarrow::kStages, 64, true)
+                                     : skinny_threads(SkinnyMxWide::kStages, 128, true));
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
