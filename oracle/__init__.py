@@ -99,6 +99,9 @@ class Oracle:
         lib.oracle_f64_from_e8m0.restype = ctypes.c_double
         lib.oracle_mxfp4_dequant_f16.argtypes = [u8p, i64, u8p, i64, i64, i64, u16p, i64]
         lib.oracle_mxfp4_dequant_f16.restype = ctypes.c_int
+        u32p = ctypes.POINTER(ctypes.c_uint32)
+        lib.oracle_sp24_decompress.argtypes = [u16p, i64, u32p, i64, i64, i64, u16p, i64]
+        lib.oracle_sp24_decompress.restype = ctypes.c_int
         self.lib = lib
         self.path = path
 
@@ -382,3 +385,59 @@ def gemm_mxfp4(*args, **kw):
 
 def gemm_mxfp4_at(*args, **kw):
     return default().gemm_mxfp4_at(*args, **kw)
+
+
+# ------------------------------------------------------------------ 2:4 sparse A
+
+def _sp24_decompress(self, Ac, E, M, K):
+    """Dense A (M×K 16-bit patterns) from compressed values Ac (M rows of >= K/2
+    16-bit patterns) and metadata E (M rows of >= K/32 uint32 words); see
+    tgemm_oracle.c for the format.  Raises ValueError on invalid metadata."""
+    Ac = _as_u16(np.asarray(Ac)) if np.asarray(Ac).dtype != np.uint16 else np.ascontiguousarray(Ac)
+    E = np.ascontiguousarray(np.asarray(E, dtype=np.uint32))
+    A = np.full((M, K), 0x7E00, dtype=np.uint16)  # NaN pattern: every element must be written
+    rc = self.lib.oracle_sp24_decompress(_ptr(Ac, ctypes.c_uint16), Ac.shape[1],
+                                        _ptr(E, ctypes.c_uint32), E.shape[1], M, K,
+                                        _ptr(A, ctypes.c_uint16), K)
+    if rc == -2:
+        raise ValueError("sp24 metadata: a group's positions are not first < second")
+    if rc != 0:
+        raise ValueError("oracle_sp24_decompress rejected its arguments")
+    return A
+
+
+def _gemm_sp24(self, Ac, E, B, M, N, K, relu=False, bias=None, R=None, in_dtype="f16",
+               out_dtype=None):
+    """C = out(act(A·B + bias) + R) with A the 2:4 sparse matrix (Ac, E)."""
+    A = self.sp24_decompress(Ac, E, M, K)
+    return self.gemm_ex(A, B, M, N, K, relu=relu, bias=bias, R=R, in_dtype=in_dtype,
+                        out_dtype=out_dtype or in_dtype)
+
+
+def _gemm_sp24_at(self, Ac, E, B, K, rows, cols, relu=False, bias=None, R=None,
+                  in_dtype="f16", out_dtype=None):
+    """Selected outputs of gemm_sp24 (decompresses only the rows needed)."""
+    rows = np.asarray(rows, dtype=np.int64)
+    uniq, inv = np.unique(rows, return_inverse=True)
+    Ac = np.asarray(Ac)
+    A = self.sp24_decompress(Ac[uniq], np.asarray(E)[uniq], uniq.size, K)
+    Rsub = None if R is None else np.asarray(R)[uniq]
+    return self.gemm_ex_at(A, B, K, inv, cols, relu=relu, bias=bias, R=Rsub,
+                           in_dtype=in_dtype, out_dtype=out_dtype or in_dtype)
+
+
+Oracle.sp24_decompress = _sp24_decompress
+Oracle.gemm_sp24 = _gemm_sp24
+Oracle.gemm_sp24_at = _gemm_sp24_at
+
+
+def sp24_decompress(*args, **kw):
+    return default().sp24_decompress(*args, **kw)
+
+
+def gemm_sp24(*args, **kw):
+    return default().gemm_sp24(*args, **kw)
+
+
+def gemm_sp24_at(*args, **kw):
+    return default().gemm_sp24_at(*args, **kw)

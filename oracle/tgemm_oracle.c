@@ -465,3 +465,40 @@ int oracle_mxfp4_dequant_f16(const uint8_t* Bq, int64_t ldbq, const uint8_t* S, 
     }
     return 0;
 }
+
+/* ========================================================================
+ * 2:4 structured-sparse A.  The pages name a sparse GEMM on 2:4 sparse tensor
+ * cores ("TileLang：让GPU编程像Python一样简单的高性能计算新范式", T.gemm_sp(A_sparse,
+ * B, C)) without fixing a storage format.  Reading taken: A (M×K, K a
+ * multiple of 32) has at most two nonzeros in every aligned group of four
+ * consecutive k; it is stored as
+ *   Ac[i][2*G + h]   the h-th kept value (h = 0, 1; increasing k) of group G
+ *                    (G = k/4), fp16, row stride ldac (>= K/2);
+ *   E[i][w]          32-bit metadata word w (row stride lde >= K/32 words):
+ *                    group G = 8w + g sits in bits 4g .. 4g+3, low two bits
+ *                    = position (0..3) of the first kept value, high two bits
+ *                    = position of the second, first < second.
+ * Dense A: A[i][4G + pos_h] = Ac[i][2G + h], every other element +0.
+ * C is then the GEMM of the dense A and B (oracle_gemm_ex with fp16 or bf16
+ * inputs).
+ * ======================================================================== */
+
+/* Dense A (M×K 16-bit patterns, row stride lda) from Ac and E.  Returns 0, -1
+ * on bad sizes, -2 if any group's positions are not first < second. */
+int oracle_sp24_decompress(const uint16_t* Ac, int64_t ldac, const uint32_t* E, int64_t lde,
+                           int64_t M, int64_t K, uint16_t* A, int64_t lda)
+{
+    if (M < 0 || K < 0 || (K % 32) != 0 || ldac < K / 2 || lde < K / 32 || lda < K) return -1;
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t k = 0; k < K; ++k) A[i * lda + k] = 0;  /* +0 in fp16 and bf16 */
+        for (int64_t G = 0; G < K / 4; ++G) {
+            uint32_t word = E[i * lde + G / 8];
+            uint32_t nib = (word >> (4 * (G % 8))) & 15u;
+            uint32_t p0 = nib & 3u, p1 = (nib >> 2) & 3u;
+            if (p0 >= p1) return -2;
+            A[i * lda + 4 * G + p0] = Ac[i * ldac + 2 * G];
+            A[i * lda + 4 * G + p1] = Ac[i * ldac + 2 * G + 1];
+        }
+    }
+    return 0;
+}

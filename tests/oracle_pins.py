@@ -579,4 +579,94 @@ def pin_mx_gemm_integer_closed_form(o):
     assert np.array_equal(C.astype(np.float64), want.astype(np.float64))
 
 
+# ---------------------------------------------------------------- 2:4 sparse A
+#
+# The format is fixed by its definition (tgemm_oracle.c): each group of four k
+# keeps two values; a 4-bit field per group holds the first kept position in
+# its low two bits and the second in its high two bits, eight groups per
+# 32-bit word, group 0 in the lowest bits.  The helpers below restate that
+# encoding independently (compression, not decompression).
+
+SP24_PATTERNS = [(0, 1), (0, 2), (0, 3), (1, 2), (1, 3), (2, 3)]
+
+
+def sp24_random(rng, M, K, values):
+    """A dense 2:4 matrix (float64) with kept positions drawn per group, its
+    compressed values (M × K/2) and metadata words (M × K/32 uint32)."""
+    A = np.zeros((M, K))
+    Ac = np.zeros((M, K // 2))
+    E = np.zeros((M, K // 32), dtype=np.uint64)
+    for i in range(M):
+        for G in range(K // 4):
+            p0, p1 = SP24_PATTERNS[rng.integers(0, 6)]
+            v0, v1 = values(rng), values(rng)
+            A[i, 4 * G + p0], A[i, 4 * G + p1] = v0, v1
+            Ac[i, 2 * G], Ac[i, 2 * G + 1] = v0, v1
+            E[i, G // 8] |= np.uint64((p0 | (p1 << 2)) << (4 * (G % 8)))
+    return A, Ac, E.astype(np.uint32)
+
+
+def pin_sp24_hand_example(o):
+    """Two rows worked by hand from the format definition."""
+    Ac = _f16(np.arange(1, 33).reshape(2, 16))
+    E = np.array([[0xE4E4E4E4], [0x98DC4C4C]], dtype=np.uint32)
+    A = o.sp24_decompress(Ac, E, 2, 32).view(np.float16).astype(np.float64)
+    want = np.zeros((2, 32))
+    # row 0: groups alternate positions (0,1) [nibble 4] and (2,3) [nibble E]
+    for G in range(8):
+        p = (0, 1) if G % 2 == 0 else (2, 3)
+        want[0, 4 * G + p[0]], want[0, 4 * G + p[1]] = 2 * G + 1, 2 * G + 2
+    # row 1: nibbles from group 0 up: C 4 C 4 C D 8 9
+    for G, p in enumerate([(0, 3), (0, 1), (0, 3), (0, 1), (0, 3), (1, 3), (0, 2), (1, 2)]):
+        want[1, 4 * G + p[0]], want[1, 4 * G + p[1]] = 17 + 2 * G, 18 + 2 * G
+    assert np.array_equal(A, want)
+
+
+def pin_sp24_roundtrip_and_exact_gemm(o):
+    rng = np.random.default_rng(61)
+    for (M, N, K) in [(3, 5, 32), (4, 3, 64), (1, 7, 96)]:
+        A, Ac, E = sp24_random(rng, M, K, lambda r: float(np.float16(r.normal(0, 1))))
+        Ac16 = _f16(Ac)
+        assert np.array_equal(o.sp24_decompress(Ac16, E, M, K).view(np.float16).astype(np.float64),
+                              A)
+        B = _f16(rng.normal(0, 1, (K, N)))
+        for relu in (False, True):
+            got = o.gemm_sp24(Ac16, E, B, M, N, K, relu=relu).astype(np.float64)
+            want, _ = exact_gemm(_f16(A), B, relu)
+            assert _same_value(got, want), (M, N, K, relu)
+
+
+def pin_sp24_invalid_metadata_rejected(o):
+    Ac = _f16(np.ones((1, 16)))
+    for nib in (0x0, 0x5, 0xA, 0xF, 0x1, 0x6, 0xB):  # first >= second
+        E = np.array([[0xE4E4E4E0 | nib]], dtype=np.uint32)
+        try:
+            o.sp24_decompress(Ac, E, 1, 32)
+        except ValueError:
+            continue
+        raise AssertionError(f"nibble {nib:#x} accepted")
+
+
+def pin_sp24_padding_ignored(o):
+    """Ac entries past K/2 and metadata words past K/32 are never read."""
+    rng = np.random.default_rng(62)
+    M, K = 3, 64
+    A, Ac, E = sp24_random(rng, M, K, lambda r: float(r.integers(1, 9)))
+    Acp = np.full((M, 40), np.float16(np.nan), dtype=np.float16)
+    Acp[:, :32] = _f16(Ac)
+    Ep = np.full((M, 5), 0xFFFFFFFF, dtype=np.uint32)  # invalid if read
+    Ep[:, :2] = E
+    assert np.array_equal(o.sp24_decompress(Acp, Ep, M, K).view(np.float16).astype(np.float64), A)
+
+
+def pin_sp24_integer_closed_form(o):
+    """Integer values: C equals numpy's int64 product of the dense A with B."""
+    rng = np.random.default_rng(63)
+    M, N, K = 8, 9, 128
+    A, Ac, E = sp24_random(rng, M, K, lambda r: float(r.integers(-3, 4)))
+    Bi = rng.integers(-2, 3, (K, N))
+    C = o.gemm_sp24(_f16(Ac), E, Bi.astype(np.float16), M, N, K)
+    assert np.array_equal(C.astype(np.float64), (A.astype(np.int64) @ Bi).astype(np.float64))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -69,6 +69,15 @@ MUTANTS = [
     ("mx_e8m0_nan_ignored", "if (x == 255) return NAN;", "if (x == 256) return NAN;"),
     ("mx_deq_no_rounding", "Bdeq[k * ldb + n] = oracle_f16_from_f64(v);",
      "Bdeq[k * ldb + n] = oracle_f16_from_f64(v) & 0xFFFE;"),
+    # 2:4 sparse A
+    ("sp24_position_fields_swapped", "uint32_t p0 = nib & 3u, p1 = (nib >> 2) & 3u;",
+     "uint32_t p1 = nib & 3u, p0 = (nib >> 2) & 3u;"),
+    ("sp24_group_order_reversed", "(word >> (4 * (G % 8))) & 15u", "(word >> (4 * (7 - G % 8))) & 15u"),
+    ("sp24_values_swapped", "A[i * lda + 4 * G + p0] = Ac[i * ldac + 2 * G];",
+     "A[i * lda + 4 * G + p0] = Ac[i * ldac + 2 * G + 1];"),
+    ("sp24_word_per_16k", "E[i * lde + G / 8]", "E[i * lde + G / 16]"),
+    ("sp24_no_zero_fill", "for (int64_t k = 0; k < K; ++k) A[i * lda + k] = 0;", "(void)0;"),
+    ("sp24_order_unchecked", "if (p0 >= p1) return -2;", "(void)0;"),
 ]
 
 
