@@ -54,6 +54,7 @@ def parse_args(argv=None):
     p.add_argument("--no-bf16", action="store_true")
     p.add_argument("--no-epilogue", action="store_true")
     p.add_argument("--no-mxfp4", action="store_true")
+    p.add_argument("--no-sp24", action="store_true")
     a = p.parse_args(argv)
     if a.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -499,6 +500,45 @@ def run_ours(args, w, rank, world, local_rank):
                                    "unit": "TFLOP/s", "frac": tf / tf_peak}
             out["mxfp4"][mname] = ent
             del am, bqm, sm, cm
+
+    # ---- 2:4 structured-sparse A (tg_gemm_sp24) on the MLP shape
+    if not args.no_sp24 and world == 1:
+        sw = W.SP24_WORKLOADS["sp24_mlp_8192x28672x4096_relu"]
+        Acs, Es, Bs = W.sp24_workload_inputs(sw)
+        acs = torch.from_numpy(Acs).to(device)
+        es = torch.from_numpy(Es.view(np.int32)).to(device)
+        bs = torch.from_numpy(Bs).to(device)
+        cs = torch.empty((sw.M, sw.N), dtype=torch.float16, device=device)
+        ex_s = tg.tg_epilogue_ex_t(tg.TG_EPI_RELU if sw.relu else tg.TG_EPI_NONE,
+                                   tg.TG_DTYPE_F16, None, None, 0)
+
+        def launch7():
+            st = tg.tg_gemm_sp24(tg.TG_DTYPE_F16, acs.data_ptr(), es.data_ptr(), bs.data_ptr(),
+                                 cs.data_ptr(), sw.M, sw.N, sw.K, sw.K // 2, sw.K // 32, sw.N,
+                                 sw.N, ex_s, stream.cuda_stream)
+            if st != tg.TG_OK:
+                raise tg.TgemmError(st, "tg_gemm_sp24")
+
+        for _ in range(args.warmup):
+            launch7()
+        tg.sync_status(stream)
+        n7 = max(20, args.steps // 10)
+        _, per7, _, _ = time_launches(launch7, stream, n7, world, device)
+        tg.sync_status(stream)
+        k7 = statistics.mean(per7)
+        tf7 = sw.flops / (k7 / 1e3) / 1e12
+        sp_peak = 2.0 * tf_peak
+        out["sp24"] = {
+            "workload": sw.name, "entry": "tg_gemm_sp24", "launches": n7,
+            "kernel": "tg_gemm_sp24 (tcgen05.mma.sp, 128x128 tiles)",
+            "kernel_ms_mean": k7, "kernel_ms_min": min(per7),
+            "tflops_dense_equivalent": tf7, "vs_dense_pair": kernel_ms / k7,
+            "roofline": {"bound": "tensor", "achieved": tf7, "peak": sp_peak, "unit": "TFLOP/s",
+                         "frac": tf7 / sp_peak,
+                         "peak_source": f"2 x {peak_src} dense bf16 burst (nominal 2:4 "
+                                        "sparse-to-dense ratio)"},
+        }
+        del acs, es, bs, cs
 
     # ---- end to end through the public API, host buffers in and out
     if not args.no_e2e:

@@ -214,6 +214,45 @@ tg_status_t tg_gemm_mxfp4(const void* A, const void* Bq, const void* Bscale, voi
                           int64_t lda, int64_t ldbq, int64_t ldbs, int64_t ldc,
                           const tg_epilogue_ex_t* epi, void* stream);
 
+/* ------------------------------------------------------------------------
+ * 2:4 structured-sparse A: C = out(act(A · B + bias) + R).
+ * ------------------------------------------------------------------------ */
+
+/*
+ * tg_gemm_sp24 — the GEMM with A 2:4 structured-sparse, on the sparse tensor
+ * cores (tcgen05.mma.sp), asynchronous on `stream`.  A (M×K) has at most two
+ * nonzeros in every aligned group of four k and is passed compressed:
+ *
+ *   Ac[i][2G + h]  the h-th kept value (h = 0, 1; increasing k) of group G
+ *                  (k = 4G .. 4G+3), of type in_dtype, row stride ldac;
+ *   E[i][w]        32-bit metadata word w (k = 32w .. 32w+31), row stride lde
+ *                  words: group g of the word in bits 4g .. 4g+3, the low two
+ *                  bits the position (0..3) of the first kept value, the high
+ *                  two the second; first < second in every group.
+ *
+ * The dense A (kept values at their positions, +0 elsewhere) then enters
+ *   C[i][j] = out( act( sum_k A[i][k]·B[k][j] + bias[j] ) + R[i][j] )
+ * exactly as in tg_gemm_ex (fp32 accumulation, one rounding).  The pages name
+ * the operation — T.gemm_sp on 2:4 sparse tensor cores ("TileLang：让GPU编程像
+ * Python一样简单的高性能计算新范式") — without a storage format; this packing of
+ * positions is the library's reading (the form the tensor core consumes).
+ *
+ * in_dtype  TG_DTYPE_F16 or TG_DTYPE_BF16 (Ac, B, R).
+ * K         a multiple of 32 (else TG_ERR_INVALID_VALUE).
+ * Ac, E, B  device; 16-byte aligned with ldac and ldb multiples of 8 elements
+ *           and lde a multiple of 4 words (else TG_ERR_MISALIGNED); ldac ≥
+ *           K/2, lde ≥ K/32, ldb ≥ N.
+ * C         of epi->out_dtype, 16-byte aligned with 16-byte aligned rows (else
+ *           TG_ERR_MISALIGNED); no staging on this entry point.
+ * epi       as tg_gemm_ex (NULL: plain output in the input type).
+ * Metadata that breaks first < second gives undefined values in its row of
+ * C (it is not checked on the device).  K == 0: C = out(act(bias) + R).
+ */
+tg_status_t tg_gemm_sp24(int32_t in_dtype, const void* Ac, const void* E, const void* B,
+                         void* C, int64_t M, int64_t N, int64_t K,
+                         int64_t ldac, int64_t lde, int64_t ldb, int64_t ldc,
+                         const tg_epilogue_ex_t* epi, void* stream);
+
 /*
  * tg_sync_status — wait for `stream`, then report (and clear) a device-side
  * timeout recorded by any libtgemm kernel on the current device since the

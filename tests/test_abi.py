@@ -173,6 +173,30 @@ def test_gemm_mxfp4_epilogue_checks(tg):
                             None) == tg.TG_ERR_INVALID_VALUE
 
 
+@pytest.mark.parametrize("args,want", [
+    # (in_dtype, Ac, E, B, C, M, N, K, ldac, lde, ldb, ldc)
+    ((0, GOOD, GOOD, GOOD, GOOD, 4, 16, 64, 32, 4, 16, 16), None),    # valid
+    ((0, GOOD, GOOD, GOOD, GOOD, 4, 16, 48, 24, 4, 16, 16), 1),       # K not a multiple of 32
+    ((0, GOOD, GOOD, GOOD, GOOD, 4, 16, 64, 24, 4, 16, 16), 1),       # ldac < K/2
+    ((0, GOOD, GOOD, GOOD, GOOD, 4, 16, 64, 32, 1, 16, 16), 1),       # lde < K/32
+    ((0, GOOD, GOOD, GOOD, GOOD, 4, 16, 64, 40, 6, 16, 16), 2),       # lde not a multiple of 4
+    ((0, GOOD, GOOD, GOOD, GOOD, 4, 16, 64, 36, 4, 16, 16), 2),       # ldac not a multiple of 8
+    ((0, GOOD + 8, GOOD, GOOD, GOOD, 4, 16, 64, 32, 4, 16, 16), 2),   # Ac not 16-byte aligned
+    ((0, GOOD, GOOD, GOOD, GOOD + 2, 4, 16, 64, 32, 4, 16, 16), 2),   # C not 16-byte aligned
+    ((0, GOOD, 0, GOOD, GOOD, 4, 16, 64, 32, 4, 16, 16), 1),          # null metadata
+    ((3, GOOD, GOOD, GOOD, GOOD, 4, 16, 64, 32, 4, 16, 16), 1),       # unknown type
+    ((1, 0, 0, 0, GOOD, 4, 16, 0, 0, 0, 0, 16), None),                # K == 0, bf16
+])
+def test_gemm_sp24_argument_checks(tg, args, want):
+    st = tg.tg_gemm_sp24(*args, None, None)
+    if want is None:
+        if _has_gpu():
+            pytest.skip("valid call would launch")
+        assert st == tg.TG_ERR_UNSUPPORTED_DEVICE
+    else:
+        assert st == want, tg.tg_status_string(st)
+
+
 def test_noalloc_keeps_the_tma_layout_rule(tg):
     # the entry point without allocation has no staging buffer
     st = tg.tg_gemm_f16_noalloc(GOOD, GOOD, GOOD, 4, 4, 4, 12, 8, 8, 0, None)

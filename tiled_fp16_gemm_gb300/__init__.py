@@ -40,7 +40,7 @@ TG_KERNEL_SKINNY = 3
 EXPORTS = (
     "tg_gemm_f16", "tg_sync_status", "tg_status_string", "tg_version", "tg_plan_f16",
     "tg_tile_coord", "tg_ring_bytes", "tg_debug_set_wait_timeout_ns", "tg_debug_inject",
-    "tg_gemm_f16_noalloc", "tg_gemm_bf16", "tg_gemm_ex", "tg_gemm_mxfp4",
+    "tg_gemm_f16_noalloc", "tg_gemm_bf16", "tg_gemm_ex", "tg_gemm_mxfp4", "tg_gemm_sp24",
 )
 
 #: bytes of the library's fixed scratch array used by tg_gemm_f16_noalloc
@@ -96,6 +96,9 @@ def _L():
     lib.tg_gemm_mxfp4.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, _i64,
                                   ctypes.POINTER(tg_epilogue_ex_t), _vp]
     lib.tg_gemm_mxfp4.restype = ctypes.c_int
+    lib.tg_gemm_sp24.argtypes = [ctypes.c_int32, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                                 _i64, _i64, _i64, ctypes.POINTER(tg_epilogue_ex_t), _vp]
+    lib.tg_gemm_sp24.restype = ctypes.c_int
     lib.tg_sync_status.argtypes = [_vp]
     lib.tg_sync_status.restype = ctypes.c_int
     lib.tg_status_string.argtypes = [ctypes.c_int]
@@ -155,6 +158,15 @@ def tg_gemm_mxfp4(A: int, Bq: int, Bscale: int, C: int, M: int, N: int, K: int, 
     E8M0 scales per 32 k), integer device pointers; returns the status code."""
     return _L().tg_gemm_mxfp4(A, Bq, Bscale, C, M, N, K, lda, ldbq, ldbs, ldc,
                               ctypes.byref(epi) if epi is not None else None, stream or None)
+
+
+def tg_gemm_sp24(in_dtype: int, Ac: int, E: int, B: int, C: int, M: int, N: int, K: int,
+                 ldac: int, lde: int, ldb: int, ldc: int, epi: tg_epilogue_ex_t | None,
+                 stream: int | None) -> int:
+    """C = out(act(A·B + bias) + R) with A 2:4 sparse (compressed values Ac and
+    metadata words E), integer device pointers; returns the status code."""
+    return _L().tg_gemm_sp24(in_dtype, Ac, E, B, C, M, N, K, ldac, lde, ldb, ldc,
+                             ctypes.byref(epi) if epi is not None else None, stream or None)
 
 
 def tg_sync_status(stream: int | None) -> int:
@@ -353,6 +365,49 @@ def gemm_mxfp4(a, bq, bscale, N: int, relu: bool = False, out=None, stream=None,
                            K, _ld(a), ldb(bq), ldb(bscale), _ld(out), epi, s.cuda_stream)
     if st != TG_OK:
         raise TgemmError(st, "tg_gemm_mxfp4")
+    return out
+
+
+def gemm_sp24(ac, e, b, relu: bool = False, out=None, stream=None, *, bias=None, residual=None,
+              out_dtype=None):
+    """C = out(act(A @ b + bias) + residual) with A 2:4 structured-sparse.
+
+    ac: CUDA float16/bfloat16 tensor M × K/2 of kept values; e: CUDA int32 (or
+    uint32 bits in int32) tensor M × K/32 of metadata words; b: K × N of ac's
+    dtype.  Rows 16-byte aligned (row strides multiples of 8 elements, 4 words).
+    bias, residual, out_dtype, out and stream as for ``gemm``.
+    """
+    import torch
+    _check_operand(ac, "ac")
+    _check_operand(b, "b")
+    M, half = ac.shape
+    K, N = b.shape
+    if half * 2 != K or K % 32 != 0:
+        raise ValueError("ac must be M × K/2 for b of K rows, K a multiple of 32")
+    if ac.dtype != b.dtype:
+        raise TypeError("ac and b must share a dtype")
+    if not isinstance(e, torch.Tensor) or e.dtype != torch.int32 or e.dim() != 2 \
+            or tuple(e.shape) != (M, K // 32) or (K > 32 and e.stride(1) != 1):
+        raise ValueError("e must be an int32 tensor of M × K/32 metadata words")
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else ac.dtype
+    if out_dtype not in (ac.dtype, torch.float32):
+        raise TypeError(f"out_dtype must be {ac.dtype} or torch.float32")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=ac.device)
+    in_code = TG_DTYPE_BF16 if ac.dtype == torch.bfloat16 else TG_DTYPE_F16
+    epi = tg_epilogue_ex_t(TG_EPI_RELU if relu else TG_EPI_NONE,
+                           TG_DTYPE_F32 if out_dtype == torch.float32 else in_code,
+                           bias.data_ptr() if bias is not None else None,
+                           residual.data_ptr() if residual is not None else None,
+                           _ld(residual) if residual is not None else 0)
+    lde = int(e.stride(0)) if M > 1 else max(4, (K // 32 + 3) // 4 * 4)
+    with torch.cuda.device(ac.device):
+        s = stream if stream is not None else torch.cuda.current_stream(ac.device)
+        st = tg_gemm_sp24(in_code, ac.data_ptr(), e.data_ptr(), b.data_ptr(), out.data_ptr(), M,
+                          N, K, _ld(ac), lde, _ld(b), _ld(out), epi, s.cuda_stream)
+    if st != TG_OK:
+        raise TgemmError(st, "tg_gemm_sp24")
     return out
 
 

@@ -17,6 +17,7 @@
 #include "gemm_persistent.cuh"
 #include "gemm_pair.cuh"
 #include "gemm_skinny.cuh"
+#include "gemm_sparse.cuh"
 #include "tile_schedule.h"
 
 namespace {
@@ -135,6 +136,9 @@ cudaError_t set_kernel_attributes() {
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  tg::PairCfg<kPairStages>::kSmemBytes);
     if (e == cudaSuccess) e = tg::skinny_set_attributes<T>();
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tg::tg_gemm_sp24<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tg::SparseCfg::kSmemBytes);
     return e;
 }
 
@@ -574,6 +578,53 @@ bool forced_dense_kernel() {
                             std::strcmp(f, "persistent128") == 0);
 }
 
+// 2:4 sparse A: tensor maps, tile plan and launch (operands in the tensor
+// memory-access layout, checked by the caller).
+template <typename T>
+tg_status_t launch_sp24(const void* Ac, const void* E, const void* B, void* C, int64_t M,
+                        int64_t N, int64_t K, int64_t ldac, int64_t lde, int64_t ldb,
+                        int64_t ldc, const tg::EpilogueSpec& ep, cudaStream_t s,
+                        DeviceState* ds) {
+    using Cfg = tg::SparseCfg;
+    constexpr CUtensorMapDataType dt = tensor_map_type<T>();
+    CUtensorMap tmA, tmB, tmE, tmC;
+    if (!encode_2d(&tmA, Ac, K / 2, M, ldac * 2, 64, Cfg::BM, dt) ||
+        !encode_2d(&tmB, B, N, K, ldb * 2, 64, Cfg::BK, dt) ||
+        !encode_2d_sw(&tmE, E, K / 32, M, lde * 4, Cfg::BK / 32, Cfg::BM,
+                      CU_TENSOR_MAP_DATA_TYPE_UINT32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !(ep.out_f32 ? encode_2d(&tmC, C, N, M, ldc * 4, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)
+                     : encode_2d(&tmC, C, N, M, ldc * 2, 64, 32, dt)))
+        return TG_ERR_LAUNCH;
+    tg::SparseParams sp;
+    tg::PersistentParams& prm = sp.base;
+    prm.M = static_cast<int32_t>(M);
+    prm.N = static_cast<int32_t>(N);
+    prm.K = static_cast<int32_t>(K);
+    prm.tiles_m = static_cast<int32_t>(ceil_div(M, Cfg::BM));
+    prm.tiles_n = static_cast<int32_t>(ceil_div(N, Cfg::BN));
+    prm.num_tiles = prm.tiles_m * prm.tiles_n;
+    prm.k_blocks = static_cast<int32_t>(ceil_div(K, Cfg::BK));
+    prm.group_m = prm.tiles_m < 16 ? prm.tiles_m : 16;
+    prm.relu = ep.relu;
+    prm.inject = g_inject.exchange(0);
+    prm.timeout_ns = g_timeout_ns.load();
+    prm.e = ep.e;
+    prm.out_f32 = ep.out_f32;
+    sp.words = static_cast<int32_t>(K / 32);
+    const int64_t grid = prm.num_tiles < ds->num_sms ? prm.num_tiles : ds->num_sms;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(Cfg::kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = s;
+    if (cudaLaunchKernelEx(&cfg, tg::tg_gemm_sp24<T>, tmA, tmB, tmE, tmC, sp) != cudaSuccess) {
+        cudaGetLastError();
+        return TG_ERR_LAUNCH;
+    }
+    return TG_OK;
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -779,6 +830,59 @@ tg_status_t tg_gemm_mxfp4(const void* A, const void* Bq, const void* Bscale, voi
                                                   static_cast<uint16_t*>(deq), ldd);
     if (cudaGetLastError() != cudaSuccess) return TG_ERR_LAUNCH;
     return gemm_impl<__half>(A, deq, C, M, N, K, lda, ldd, ldc, ep, stream);
+}
+
+tg_status_t tg_gemm_sp24(int32_t in_dtype, const void* Ac, const void* E, const void* B, void* C,
+                         int64_t M, int64_t N, int64_t K, int64_t ldac, int64_t lde, int64_t ldb,
+                         int64_t ldc, const tg_epilogue_ex_t* epi, void* stream) {
+    tg_epilogue_ex_t x;
+    if (epi != nullptr) {
+        x = *epi;
+    } else {
+        std::memset(&x, 0, sizeof(x));
+        x.activation = TG_EPI_NONE;
+        x.out_dtype = in_dtype;
+    }
+    if (x.activation != TG_EPI_NONE && x.activation != TG_EPI_RELU) return TG_ERR_INVALID_VALUE;
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim || (K % 32) != 0)
+        return TG_ERR_INVALID_VALUE;
+    tg_status_t st = validate_ex(in_dtype, C, M, N, x);
+    if (st != TG_OK || M == 0 || N == 0) return st;
+    if (C == nullptr || ldc < N) return TG_ERR_INVALID_VALUE;
+    const int elem_c = x.out_dtype == TG_DTYPE_F32 ? 4 : 2;
+    if ((reinterpret_cast<uintptr_t>(C) & 15u) != 0 || (ldc * elem_c) % 16 != 0)
+        return TG_ERR_MISALIGNED;
+    if (K > 0) {
+        if (Ac == nullptr || E == nullptr || B == nullptr || ldac < K / 2 || lde < K / 32 ||
+            ldb < N)
+            return TG_ERR_INVALID_VALUE;
+        if ((reinterpret_cast<uintptr_t>(Ac) & 15u) != 0 ||
+            (reinterpret_cast<uintptr_t>(E) & 15u) != 0 ||
+            (reinterpret_cast<uintptr_t>(B) & 15u) != 0 || (ldac & 7) != 0 || (lde & 3) != 0 ||
+            (ldb & 7) != 0)
+            return TG_ERR_MISALIGNED;
+    }
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    st = current_device(&dev, &ds);
+    if (st != TG_OK) return st;
+    tg::EpilogueSpec ep = plain_epilogue(x.activation);
+    ep.out_f32 = x.out_dtype == TG_DTYPE_F32 ? 1 : 0;
+    ep.e.bias = x.bias;
+    ep.e.resid = x.residual;
+    ep.e.ldr = x.residual != nullptr ? x.ldr : 0;
+    ep.e.bias_vec = (reinterpret_cast<uintptr_t>(x.bias) & 15u) == 0 ? 1 : 0;
+    ep.e.resid_vec =
+        (reinterpret_cast<uintptr_t>(x.residual) & 15u) == 0 && (x.ldr & 7) == 0 ? 1 : 0;
+    if (K == 0) {
+        if (in_dtype == TG_DTYPE_BF16)
+            return gemm_impl<__nv_bfloat16>(nullptr, nullptr, C, M, N, 0, 0, 0, ldc, ep, stream);
+        return gemm_impl<__half>(nullptr, nullptr, C, M, N, 0, 0, 0, ldc, ep, stream);
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (in_dtype == TG_DTYPE_BF16)
+        return launch_sp24<__nv_bfloat16>(Ac, E, B, C, M, N, K, ldac, lde, ldb, ldc, ep, s, ds);
+    return launch_sp24<__half>(Ac, E, B, C, M, N, K, ldac, lde, ldb, ldc, ep, s, ds);
 }
 
 tg_status_t tg_sync_status(void* stream) {

@@ -205,3 +205,61 @@ def mx_workload_inputs(w: MxWorkload):
     A = draw(np.random.default_rng([w.seed, 0]), w.dist_a, w.M, w.K).astype(np.float16)
     Bq, S = draw_mxfp4(np.random.default_rng([w.seed, 1]), w.K, w.N, w.scale_lo, w.scale_hi)
     return A, Bq, S
+
+
+# ------------------------------------------------------------------ 2:4 sparse A
+
+SP24_PATTERN_CODES = np.array([0x4, 0x8, 0xC, 0x9, 0xD, 0xE], dtype=np.uint32)
+"""The six valid 4-bit group codes of the 2:4 metadata format (positions
+(0,1), (0,2), (0,3), (1,2), (1,3), (2,3): first in the low two bits)."""
+
+
+def draw_sp24(rng: np.random.Generator, M: int, K: int, dist: tuple, lde: int | None = None):
+    """A random 2:4 sparse M×K matrix drawn directly in its stored form:
+    kept values Ac (float16, M × K/2) from ``dist`` and metadata words E
+    (uint32, M × lde, lde >= K/32) whose group codes are drawn uniformly from
+    the six valid ones.  No dense matrix is formed."""
+    Ac = draw(rng, dist, M, K // 2).astype(np.float16)
+    codes = SP24_PATTERN_CODES[rng.integers(0, 6, size=(M, K // 4))]
+    words = np.zeros((M, K // 32), dtype=np.uint32)
+    for g in range(8):
+        words |= codes[:, g::8] << np.uint32(4 * g)
+    lde = K // 32 if lde is None else lde
+    E = np.zeros((M, lde), dtype=np.uint32)
+    E[:, :K // 32] = words
+    return Ac, E
+
+
+@dataclasses.dataclass(frozen=True)
+class Sp24Workload:
+    name: str
+    M: int
+    N: int
+    K: int
+    relu: bool
+    dist_a: tuple
+    dist_b: tuple
+    seed: int
+    note: str = ""
+
+    @property
+    def flops(self) -> int:
+        """Dense-equivalent: 2·M·N·K (the skipped zeros counted as work)."""
+        return 2 * self.M * self.N * self.K
+
+
+SP24_WORKLOADS = {
+    w.name: w
+    for w in [
+        Sp24Workload("sp24_mlp_8192x28672x4096_relu", 8192, 28672, 4096, True,
+                     ("normal", 0.0, 1.0 / 64.0), ("normal", 0.0, 1.0 / 64.0), 9,
+                     "the MLP shape with a 2:4 sparse A (half of A's weights pruned)"),
+    ]
+}
+
+
+def sp24_workload_inputs(w: Sp24Workload):
+    """(Ac, E, B) for a 2:4 workload."""
+    Ac, E = draw_sp24(np.random.default_rng([w.seed, 0]), w.M, w.K, w.dist_a)
+    B = draw(np.random.default_rng([w.seed, 1]), w.dist_b, w.K, w.N).astype(np.float16)
+    return Ac, E, B
