@@ -534,7 +534,7 @@ def run_ours(args, w, rank, world, local_rank):
             "kernel_ms_mean": k7, "kernel_ms_min": min(per7),
             "tflops_dense_equivalent": tf7, "vs_dense_pair": kernel_ms / k7,
             "roofline": {"bound": "tensor", "achieved": tf7, "peak": sp_peak, "unit": "TFLOP/s",
-                         "frac": tf7 / sp_peak,
+                         "frac": tf7 / sp_peak, "traffic": stored_traffic(f"sp24:{sw.name}"),
                          "peak_source": f"2 x {peak_src} dense bf16 burst (nominal 2:4 "
                                         "sparse-to-dense ratio)"},
         }
