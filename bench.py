@@ -42,6 +42,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
 def parse_args(argv=None):
+    from tiled_fp16_gemm_gb300 import workloads as W
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=500)
@@ -55,6 +56,8 @@ def parse_args(argv=None):
     p.add_argument("--no-epilogue", action="store_true")
     p.add_argument("--no-mxfp4", action="store_true")
     p.add_argument("--no-sp24", action="store_true")
+    p.add_argument("--sp24-workload", default="sp24_mlp_8192x28672x4096_relu",
+                   choices=sorted(W.SP24_WORKLOADS))
     a = p.parse_args(argv)
     if a.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -503,7 +506,7 @@ def run_ours(args, w, rank, world, local_rank):
 
     # ---- 2:4 structured-sparse A (tg_gemm_sp24) on the MLP shape
     if not args.no_sp24 and world == 1:
-        sw = W.SP24_WORKLOADS["sp24_mlp_8192x28672x4096_relu"]
+        sw = W.SP24_WORKLOADS[args.sp24_workload]
         Acs, Es, Bs = W.sp24_workload_inputs(sw)
         acs = torch.from_numpy(Acs).to(device)
         es = torch.from_numpy(Es.view(np.int32)).to(device)
@@ -519,24 +522,45 @@ def run_ours(args, w, rank, world, local_rank):
             if st != tg.TG_OK:
                 raise tg.TgemmError(st, "tg_gemm_sp24")
 
-        for _ in range(args.warmup):
-            launch7()
-        tg.sync_status(stream)
+        def time_sp24(force):
+            """Mean / min ms of launch7 with TGEMM_FORCE_SP24 = force (None: the
+            library's own choice, the CTA-pair kernel at this shape)."""
+            prev = os.environ.pop("TGEMM_FORCE_SP24", None)
+            if force is not None:
+                os.environ["TGEMM_FORCE_SP24"] = force
+            try:
+                for _ in range(args.warmup):
+                    launch7()
+                tg.sync_status(stream)
+                _, per, _, _ = time_launches(launch7, stream, n7, world, device)
+                tg.sync_status(stream)
+            finally:
+                os.environ.pop("TGEMM_FORCE_SP24", None)
+                if prev is not None:
+                    os.environ["TGEMM_FORCE_SP24"] = prev
+            return statistics.mean(per), min(per)
+
         n7 = max(20, args.steps // 10)
-        _, per7, _, _ = time_launches(launch7, stream, n7, world, device)
-        tg.sync_status(stream)
-        k7 = statistics.mean(per7)
+        k7, min7 = time_sp24(None)
+        k7c, min7c = time_sp24("cta")
         tf7 = sw.flops / (k7 / 1e3) / 1e12
         sp_peak = 2.0 * tf_peak
         out["sp24"] = {
             "workload": sw.name, "entry": "tg_gemm_sp24", "launches": n7,
-            "kernel": "tg_gemm_sp24 (tcgen05.mma.sp, 128x128 tiles)",
-            "kernel_ms_mean": k7, "kernel_ms_min": min(per7),
-            "tflops_dense_equivalent": tf7, "vs_dense_pair": kernel_ms / k7,
+            "kernel": "tg_gemm_sp24_pair<3> (tcgen05.mma.sp cta_group::2, 256x256 tiles)",
+            "kernel_ms_mean": k7, "kernel_ms_min": min7,
+            "tflops_dense_equivalent": tf7,
+            "vs_dense_pair": kernel_ms / k7 if (sw.M, sw.N, sw.K) == (w.M, w.N, w.K) else None,
             "roofline": {"bound": "tensor", "achieved": tf7, "peak": sp_peak, "unit": "TFLOP/s",
-                         "frac": tf7 / sp_peak, "traffic": stored_traffic(f"sp24:{sw.name}"),
+                         "frac": tf7 / sp_peak,
+                         "traffic": stored_traffic(f"sp24_pair:{sw.name}"),
                          "peak_source": f"2 x {peak_src} dense bf16 burst (nominal 2:4 "
                                         "sparse-to-dense ratio)"},
+            "one_cta_kernel": {
+                "kernel": "tg_gemm_sp24 (tcgen05.mma.sp, 128x128 tiles)", "launches": n7,
+                "kernel_ms_mean": k7c, "kernel_ms_min": min7c,
+                "tflops_dense_equivalent": sw.flops / (k7c / 1e3) / 1e12,
+                "traffic": stored_traffic(f"sp24:{sw.name}")},
         }
         del acs, es, bs, cs
 

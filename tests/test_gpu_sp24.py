@@ -1,8 +1,10 @@
 """Parity of the 2:4 structured-sparse GEMM (tg_gemm_sp24, through the C ABI)
-against the oracle on a GB300: ragged shapes (M, N off the 128 tile, K not a
-multiple of the 128-k stage), fp16 and bf16, the extended epilogue, integer
-inputs (exact), the bounded-wait fault path and sampled outputs at the MLP
-layer's full size.  Tolerances are those of parity.py and test_gpu_epilogue.py:
+against the oracle on a GB300, for both of its kernels (one CTA with 128×128
+tiles, and CTA pairs with 256×256 tiles, forced through TGEMM_FORCE_SP24):
+ragged shapes (M, N off the tile, K not a multiple of the 128-k stage, a pair
+whose second CTA lies wholly past M), fp16 and bf16, the extended epilogue,
+integer inputs (exact), the bounded-wait fault path and sampled outputs at the
+MLP layer's full size.  Tolerances are those of parity.py and test_gpu_epilogue.py:
 the kept values enter the same fp32 accumulation as the dense GEMM."""
 
 import numpy as np
@@ -28,6 +30,14 @@ def tg():
 
 
 TDT = {"f16": torch.float16, "bf16": torch.bfloat16}
+KERNELS = ["cta", "pair"]
+
+
+@pytest.fixture(params=KERNELS)
+def kern(request, monkeypatch):
+    """Selects the sparse kernel for the calls of one test."""
+    monkeypatch.setenv("TGEMM_FORCE_SP24", request.param)
+    return request.param
 
 
 def to16(x64, fmt):
@@ -99,7 +109,7 @@ SHAPES = [(128, 128, 128), (1, 64, 32), (129, 200, 96), (300, 1000, 512), (257, 
 
 @pytest.mark.parametrize("fmt", ["f16", "bf16"])
 @pytest.mark.parametrize("M,N,K", SHAPES, ids=[f"{m}x{n}x{k}" for m, n, k in SHAPES])
-def test_sp24_parity(tg, M, N, K, fmt):
+def test_sp24_parity(tg, kern, M, N, K, fmt):
     Ac, E, B = case(M, N, K, fmt, 1000 + M + N + K)
     for relu in (False, True):
         got = run(tg, fmt, Ac, E, B, M, N, K, relu=relu)
@@ -109,7 +119,7 @@ def test_sp24_parity(tg, M, N, K, fmt):
 
 
 @pytest.mark.parametrize("fmt", ["f16", "bf16"])
-def test_sp24_epilogue(tg, fmt):
+def test_sp24_epilogue(tg, kern, fmt):
     M, N, K = 200, 300, 256
     Ac, E, B = case(M, N, K, fmt, 7)
     rng = np.random.default_rng(8)
@@ -127,18 +137,19 @@ def test_sp24_epilogue(tg, fmt):
     assert np.all(np.abs(got - want.astype(np.float64)) <= tol), "sp24 f32 out"
 
 
-def test_sp24_integers_exact(tg):
+@pytest.mark.parametrize("M,N,K", [(256, 384, 1024), (512, 512, 512)])
+def test_sp24_integers_exact(tg, kern, M, N, K):
     """Integer kept values and B: every partial sum is an exact integer in fp32,
     so the result equals the oracle exactly (this pins the metadata layout in
-    tensor memory: a wrong position would change some sum)."""
-    M, N, K = 256, 384, 1024
+    tensor memory, for the pair kernel in both CTAs: a wrong position would
+    change some sum)."""
     Ac, E, B = case(M, N, K, "f16", 11, integer=True)
     got = run(tg, "f16", Ac, E, B, M, N, K)
     want = oracle.gemm_sp24(Ac, E, B, M, N, K).astype(np.float64)
     assert np.array_equal(got, want)
 
 
-def test_sp24_metadata_padding(tg):
+def test_sp24_metadata_padding(tg, kern):
     """Metadata words past K/32 in a padded row stride are never used."""
     M, N, K = 64, 128, 96
     Ac, E, B = case(M, N, K, "f16", 12)
@@ -148,7 +159,7 @@ def test_sp24_metadata_padding(tg):
     check(got, oracle.gemm_sp24(Ac, E, B, M, N, K), K, what="sp24 padded metadata")
 
 
-def test_sp24_withheld_signal_times_out_and_recovers(tg):
+def test_sp24_withheld_signal_times_out_and_recovers(tg, kern):
     M, N, K = 256, 256, 256
     Ac, E, B = case(M, N, K, "f16", 13)
     s = torch.cuda.current_stream().cuda_stream
@@ -186,8 +197,9 @@ def test_sp24_python_api(tg):
         tg.gemm_sp24(ac[:, :-8], e, b)
 
 
-def test_sp24_mlp_full_size_sampled(tg):
-    """8192×28672×4096 with a 2:4 A, as the benchmark runs it: sampled outputs."""
+def test_sp24_mlp_full_size_sampled(tg, kern):
+    """8192×28672×4096 with a 2:4 A, as the benchmark runs it (the pair
+    kernel) and on the one-CTA kernel: sampled outputs."""
     w = W.SP24_WORKLOADS["sp24_mlp_8192x28672x4096_relu"]
     Ac, E, B = W.sp24_workload_inputs(w)
     ac = torch.from_numpy(Ac).cuda()

@@ -1,0 +1,409 @@
+// 2:4 structured-sparse GEMM on CTA pairs (tcgen05.mma.sp cta_group::2) for
+// sm_103a:  C = epi(A · B) with A sparse, 256×256 output tiles per cluster.
+//
+// Same operation and operand formats as the one-CTA kernel (gemm_sparse.cuh:
+// Ac = the kept values, E = 32-bit metadata words), the operation of "TileLang：
+// 让GPU编程像Python一样简单的高性能计算新范式", section on sparse computation.
+// What changes is the tile: each CTA of the pair (rank r) holds, per 128-k
+// stage,
+//   Ac rows [m0 + 128 r, +128) × 64 kept values   (one 16 KB box)
+//   B cols  [n0 + 128 r, +128) × 128 k             (two 16 KB boxes)
+//   E rows  [m0 + 128 r, +128) × 4 words           (one 2 KB box)
+// and the even CTA issues 256×256×32 sparse MMAs over the pair.  Per SM this
+// halves the operand bytes per MMA cycle of the 128×128 one-CTA tile, whose
+// speed the L2 → SM bandwidth sets.
+//
+// Tensor memory (512 columns per CTA): one 256-column fp32 accumulator and,
+// from column 256, the metadata ring — each MMA's metadata column on a
+// 16-column boundary, 64 columns per stage.  Each CTA's tensor memory holds
+// the metadata of its own 128 rows at the same column, in the lane layout of
+// the one-CTA kernel.  With one accumulator the epilogue's tensor-memory
+// reads of a tile are not overlapped with the next tile's MMAs (its global
+// stores are).
+//
+// Synchronisation (all waits bounded):
+//   full[s]    even CTA: Ac and B bytes of both CTAs (pair TMA loads);
+//   efull[s]   each CTA: its own E box (plain TMA load);
+//   meta[s]    even CTA: the 8 metadata warps of the pair wrote stage s;
+//   empty[s]   each CTA: multicast commit after the MMAs of stage s;
+//   tfull      each CTA: multicast commit at the end of a tile;
+//   tempty     even CTA: the 8 epilogue warps of the pair read the tile.
+// A cluster barrier after set-up and before exit brackets the work.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "epilogue.cuh"
+#include "gemm_persistent.cuh"
+#include "gemm_sparse.cuh"
+#include "sm103_ptx.cuh"
+#include "tile_schedule.h"
+
+namespace tg {
+
+template <int STAGES_>
+struct SparsePairCfg {
+    static constexpr int STAGES = STAGES_;
+    static constexpr int BM = 256;      // rows of C per cluster tile (128 per CTA)
+    static constexpr int BN = 256;      // columns of C per cluster tile (B: 128 per CTA)
+    static constexpr int BK = 128;      // dense-equivalent k per stage
+    static constexpr int kThreads = 320;
+    static constexpr uint32_t kABytes = 128 * (BK / 2) * 2;  // 16 KB of kept values
+    static constexpr uint32_t kBBytes = BK * 128 * 2;        // 32 KB: two 64-column boxes
+    static constexpr uint32_t kEBytes = 128 * (BK / 32) * 4; // 2 KB of metadata
+    static constexpr uint32_t kCBuf = 32 * 64 * 2;
+    static constexpr uint32_t kCBytes = 4 * 2 * kCBuf;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kMetaCol0 = BN;
+    static constexpr uint32_t kMetaStageCols = 64;
+    static constexpr uint32_t kMetaSliceCols = 16;
+    static constexpr uint32_t kBarBytes = 256;
+    static constexpr uint32_t kSmemBytes =
+        1024 + STAGES * (kABytes + kBBytes + kEBytes) + kCBytes + kBarBytes;
+    static_assert(kMetaCol0 + kMetaStageCols * STAGES <= kTmemCols,
+                  "metadata columns exceed tensor memory");
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeded");
+};
+
+// mbar_wait for a barrier that threads of the peer CTA arrive on (release at
+// cluster scope): the successful wait acquires at cluster scope.
+__device__ __forceinline__ uint32_t mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  uint64_t timeout_ns,
+                                                  const volatile int* abort_flag) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (abort_flag != nullptr && *abort_flag) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
+__device__ __forceinline__ void mma_f16_sp_pair(uint32_t d_tmem, uint64_t a_desc,
+                                                uint64_t b_desc, uint32_t meta_tmem,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.sp.cta_group::2.kind::f16 [%0], %1, %2, [%3], %4, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(meta_tmem), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+template <int STAGES, typename T>
+__global__ void __launch_bounds__(320, 1)
+    tg_gemm_sp24_pair(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmE,
+                      const __grid_constant__ CUtensorMap tmC, const SparseParams sp) {
+    using Cfg = SparsePairCfg<STAGES>;
+    constexpr int S = STAGES;
+    const PersistentParams& p = sp.base;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const base_ptr = smem_raw + (base - raw);
+
+    const uint32_t sA = base;
+    const uint32_t sB = sA + S * Cfg::kABytes;
+    const uint32_t sE = sB + S * Cfg::kBBytes;
+    const uint32_t sC = sE + S * Cfg::kEBytes;
+    const uint32_t sBar = sC + Cfg::kCBytes;
+    const uint32_t bar_full = sBar;              // [S]
+    const uint32_t bar_efull = sBar + 8 * S;     // [S]
+    const uint32_t bar_meta = sBar + 16 * S;     // [S]
+    const uint32_t bar_empty = sBar + 24 * S;    // [S]
+    const uint32_t bar_tfull = sBar + 32 * S;
+    const uint32_t bar_tempty = bar_tfull + 8;
+    const uint32_t bar_drain = bar_tempty + 8;
+    const uint32_t slot_tmem = bar_drain + 8;
+    static_assert(32 * S + 24 + 8 <= Cfg::kBarBytes, "barrier area too small");
+    uint32_t* const tmem_slot_ptr = reinterpret_cast<uint32_t*>(base_ptr + (slot_tmem - base));
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(tmem_slot_ptr + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int cluster_id = static_cast<int>(blockIdx.x >> 1);
+    const int nclusters = static_cast<int>(gridDim.x >> 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_efull + 8 * s, 1);
+            mbar_init(bar_meta + 8 * s, 8);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        mbar_init(bar_tfull, 1);
+        mbar_init(bar_tempty, 8);
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmE);
+        tma_prefetch_desc(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(slot_tmem, Cfg::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // the peer's barriers exist and its tensor memory is allocated
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot_ptr;
+
+    auto fail = [&](unsigned int role) {
+        atomicOr(&g_wait_timeout_flags, role);
+        *abort_flag = 1;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer (both CTAs)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_parity = 0;
+            bool ok = true;
+            for (int tile = cluster_id; ok && tile < p.num_tiles; tile += nclusters) {
+                const TileCoord tc = tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m);
+                const int ma = tc.m_blk * Cfg::BM + static_cast<int>(rank) * 128;
+                const int nb = tc.n_blk * Cfg::BN + static_cast<int>(rank) * 128;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.timeout_ns, abort_flag)) {
+                        fail(kRoleProducer);
+                        ok = false;
+                        break;
+                    }
+                    if (leader)
+                        mbar_arrive_expect_tx(bar_full + 8 * stage,
+                                              2 * (Cfg::kABytes + Cfg::kBBytes));
+                    const uint32_t fb = mapa_shared(bar_full + 8 * stage, 0);
+                    tma_load_2d_pair(sA + stage * Cfg::kABytes, &tmA, fb, kb * (Cfg::BK / 2), ma);
+                    tma_load_2d_pair(sB + stage * Cfg::kBBytes, &tmB, fb, nb, kb * Cfg::BK);
+                    tma_load_2d_pair(sB + stage * Cfg::kBBytes + Cfg::kBBytes / 2, &tmB, fb,
+                                     nb + 64, kb * Cfg::BK);
+                    const uint32_t eb = bar_efull + 8 * stage;
+                    mbar_arrive_expect_tx(eb, Cfg::kEBytes);
+                    tma_load_2d(sE + stage * Cfg::kEBytes, &tmE, eb, kb * (Cfg::BK / 32), ma);
+                    issued_mask |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (ok) {
+                // Normal exit: every phase armed here was consumed (by the MMA
+                // thread, and by this CTA's metadata warps), so these return at once.
+                for (int s = 0; s < S; ++s)
+                    if (issued_mask & (1u << s)) {
+                        const uint32_t par = (issued_parity >> s) & 1u;
+                        if ((leader && !mbar_wait(bar_full + 8 * s, par, p.timeout_ns, nullptr)) ||
+                            !mbar_wait(bar_efull + 8 * s, par, p.timeout_ns, nullptr))
+                            atomicOr(&g_wait_timeout_flags, kRoleDrain);
+                    }
+            } else if (issued_mask != 0) {
+                // Abort: this CTA's last loads may be counted on a phase the
+                // pair never finishes; give them a fixed, bounded grace period
+                // (far above a TMA round trip) to land.
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 1000000ull) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (even CTA)
+        if (leader && lane == 0) {
+            // sparse (bit 2), selector 0; A K-major, B MN-major; 256 × 256 over the pair
+            constexpr uint32_t idesc =
+                idesc_f16_f32(Cfg::BM, Cfg::BN, /*a_mn=*/false, /*b_mn=*/true,
+                              Elem16<T>::kFmt) |
+                (1u << 2);
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int tile = cluster_id; ok && tile < p.num_tiles; tile += nclusters, ++it) {
+                if (!mbar_wait_cluster(bar_tempty, (static_cast<uint32_t>(it) & 1u) ^ 1u,
+                                       p.timeout_ns, abort_flag)) {
+                    fail(kRoleMma);
+                    break;
+                }
+                tc_fence_after_sync();
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(bar_full + 8 * stage, phase, p.timeout_ns, abort_flag) ||
+                        !mbar_wait_cluster(bar_meta + 8 * stage, phase, p.timeout_ns,
+                                           abort_flag)) {
+                        fail(kRoleMma);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a0 = sA + stage * Cfg::kABytes;
+                    const uint32_t b0 = sB + stage * Cfg::kBBytes;
+#pragma unroll
+                    for (int k = 0; k < Cfg::BK / 32; ++k) {
+                        const uint64_t adesc = smem_desc_sw128(a0 + 32 * k, 16, 1024);
+                        const uint64_t bdesc = smem_desc_sw128(b0 + 4096 * k, 16384, 1024);
+                        const uint32_t meta = tmem_base + Cfg::kMetaCol0 +
+                                              static_cast<uint32_t>(stage) * Cfg::kMetaStageCols +
+                                              static_cast<uint32_t>(k) * Cfg::kMetaSliceCols;
+                        mma_f16_sp_pair(tmem_base, adesc, bdesc, meta, idesc,
+                                        (kb | k) != 0 ? 1u : 0u);
+                    }
+                    mma_commit_pair_mc(bar_empty + 8 * stage, 0x3);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if (!(p.inject == 1 && it == 0)) mma_commit_pair_mc(bar_tfull, 0x3);
+            }
+            mma_commit_pair_mc(bar_drain, 0x1);
+            if (!mbar_wait(bar_drain, 0, p.timeout_ns, nullptr))
+                atomicOr(&g_wait_timeout_flags, kRoleDrain);
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        const uint32_t cbuf = sC + static_cast<uint32_t>((warp - 2) * 2) * Cfg::kCBuf;
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+        const uint64_t c_policy = policy_evict_first();
+        const uint32_t tempty_leader = mapa_shared(bar_tempty, 0);
+        int buf = 0;
+        int it = 0;
+        for (int tile = cluster_id; tile < p.num_tiles; tile += nclusters, ++it) {
+            const TileCoord tc = tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m);
+            const int row0 = tc.m_blk * Cfg::BM + static_cast<int>(rank) * 128 + 32 * q;
+            const int n0 = tc.n_blk * Cfg::BN;
+            int ok = 1;
+            if (lane == 0)
+                ok = mbar_wait(bar_tfull, static_cast<uint32_t>(it) & 1u, p.timeout_ns,
+                               abort_flag) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) fail(kRoleEpilogue);
+                break;
+            }
+            tc_fence_after_sync();
+#pragma unroll 1
+            for (int j = 0; j < Cfg::BN / 64; ++j) {
+                uint32_t v0[32], v1[32];
+                const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(j * 64);
+                tmem_ld_x32(taddr, v0);
+                tmem_ld_x32(taddr + 32, v1);
+                if (j == Cfg::BN / 64 - 1) {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(tempty_leader);
+                }
+                float x[64];
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    x[t] = __uint_as_float(v0[t]);
+                    x[32 + t] = __uint_as_float(v1[t]);
+                }
+                epilogue_math<T>(x, p.e, p.relu, row0 + lane, n0 + 64 * j, p.M, p.N);
+                epilogue_store<T>(x, cbuf, buf, &tmC, c_policy, row0, n0 + 64 * j, p.M, p.N, lane,
+                                  p.out_f32 != 0);
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ metadata (warps 6..9, both CTAs)
+        // Lane L of this CTA's tensor memory (quarter warp % 4) takes rows
+        // r0 = (L & ~15) | (L & 7) and r1 = r0 + 8 of the CTA's 128, k half
+        // h = (L >> 3) & 1 of each of the stage's four 32-k words.
+        const uint32_t L = 32u * static_cast<uint32_t>(warp & 3) + static_cast<uint32_t>(lane);
+        const uint32_t r0 = (L & ~15u) | (L & 7u);
+        const uint32_t r1 = r0 + 8u;
+        const uint32_t h = (L >> 3) & 1u;
+        const uint32_t lane_addr = (32u * static_cast<uint32_t>(warp & 3)) << 16;
+        const uint32_t meta_leader = mapa_shared(bar_meta, 0);
+        constexpr uint32_t kNeutral = 0x4444u;  // positions (0, 1) in every group of a half
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int tile = cluster_id; ok && tile < p.num_tiles; tile += nclusters) {
+            const TileCoord tc = tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m);
+            const int m0 = tc.m_blk * Cfg::BM + static_cast<int>(rank) * 128;
+            const bool row0_in = m0 + static_cast<int>(r0) < p.M;
+            const bool row1_in = m0 + static_cast<int>(r1) < p.M;
+            for (int kb = 0; kb < p.k_blocks; ++kb) {
+                int got = 1;
+                if (lane == 0)
+                    got = mbar_wait(bar_efull + 8 * stage, phase, p.timeout_ns, abort_flag) ? 1
+                                                                                             : 0;
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!got) {
+                    if (lane == 0) fail(kRoleMeta);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();  // the MMAs that read this stage's columns completed
+                const uint32_t e = sE + stage * Cfg::kEBytes;
+                const uint4 w0 = ld_shared_v4_u32(e + 16u * r0);
+                const uint4 w1 = ld_shared_v4_u32(e + 16u * r1);
+                const uint32_t a[4] = {w0.x, w0.y, w0.z, w0.w};
+                const uint32_t b[4] = {w1.x, w1.y, w1.z, w1.w};
+                uint32_t t[4];
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const bool word_in = kb * 4 + w < sp.words;
+                    const uint32_t lo =
+                        (row0_in && word_in) ? (a[w] >> (16 * h)) & 0xFFFFu : kNeutral;
+                    const uint32_t hi =
+                        (row1_in && word_in) ? (b[w] >> (16 * h)) & 0xFFFFu : kNeutral;
+                    t[w] = lo | (hi << 16);
+                }
+                const uint32_t col = tmem_base + lane_addr + Cfg::kMetaCol0 +
+                                     static_cast<uint32_t>(stage) * Cfg::kMetaStageCols;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) tmem_st_x1(col + w * Cfg::kMetaSliceCols, t[w]);
+                tmem_wait_st();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(meta_leader + 8u * static_cast<uint32_t>(stage));
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // the peer no longer reads this CTA's memory or signals its barriers
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+}  // namespace tg

@@ -16,6 +16,7 @@
 #include "tgemm.h"
 #include "gemm_persistent.cuh"
 #include "gemm_pair.cuh"
+#include "gemm_sparse_pair.cuh"
 #include "gemm_skinny.cuh"
 #include "gemm_sparse.cuh"
 #include "tile_schedule.h"
@@ -69,6 +70,10 @@ constexpr int kPairStages = 6;
 // 16: 1629, 32: 1552 TFLOP/s.
 constexpr int kPairGroupM = 16;
 
+// 2:4 sparse pair kernel: 3 stages of 50 KB per CTA (a fourth does not fit
+// beside the epilogue's staging buffers).
+constexpr int kSpPairStages = 3;
+
 // 256×256 tiles on CTA pairs; grid = two CTAs per tile, at most num_sms.
 void plan_pair(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* p) {
     p->kernel = TG_KERNEL_PERSISTENT;
@@ -101,6 +106,7 @@ struct DeviceState {
     int num_sms = 0;
     bool attrs_set = false;
     int max_pairs = 0;  // CTA pairs of the pair kernel that fit on the device at once
+    int max_sp_pairs = 0;  // the same for the 2:4 sparse pair kernel
 };
 
 std::mutex g_dev_mutex;
@@ -139,7 +145,36 @@ cudaError_t set_kernel_attributes() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(tg::tg_gemm_sp24<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  tg::SparseCfg::kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tg::tg_gemm_sp24_pair<kSpPairStages, T>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tg::SparsePairCfg<kSpPairStages>::kSmemBytes);
     return e;
+}
+
+// How many clusters of two CTAs of `kernel` can be resident together
+// (clusters must sit inside one GPC, so this can be below num_sms / 2);
+// 0 if the query fails.
+template <typename Kernel>
+int max_active_pairs(Kernel kernel, int threads, uint32_t smem, int num_sms) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * (num_sms / 2)));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        clusters = 0;
+    }
+    return clusters;
 }
 
 // Returns TG_OK and fills *dev / *st for the current device, or an error.
@@ -171,27 +206,12 @@ tg_status_t current_device(int* dev, DeviceState** st) {
             cudaGetLastError();
             return TG_ERR_LAUNCH;
         }
-        // How many CTA pairs can be resident together (clusters must sit
-        // inside one GPC, so this can be below num_sms / 2).
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cudaLaunchConfig_t cfg;
-        std::memset(&cfg, 0, sizeof(cfg));
-        cfg.gridDim = dim3(static_cast<unsigned>(2 * (s.num_sms / 2)));
-        cfg.blockDim = dim3(tg::PairCfg<kPairStages>::kThreads);
-        cfg.dynamicSmemBytes = tg::PairCfg<kPairStages>::kSmemBytes;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, tg::tg_gemm_f16_pair<kPairStages, __half>,
-                                           &cfg) != cudaSuccess) {
-            cudaGetLastError();
-            clusters = 0;
-        }
-        s.max_pairs = clusters;
+        s.max_pairs = max_active_pairs(tg::tg_gemm_f16_pair<kPairStages, __half>,
+                                       tg::PairCfg<kPairStages>::kThreads,
+                                       tg::PairCfg<kPairStages>::kSmemBytes, s.num_sms);
+        s.max_sp_pairs = max_active_pairs(tg::tg_gemm_sp24_pair<kSpPairStages, __half>,
+                                          tg::SparsePairCfg<kSpPairStages>::kThreads,
+                                          tg::SparsePairCfg<kSpPairStages>::kSmemBytes, s.num_sms);
         s.attrs_set = true;
     }
     *dev = d;
@@ -578,14 +598,22 @@ bool forced_dense_kernel() {
                             std::strcmp(f, "persistent128") == 0);
 }
 
-// 2:4 sparse A: tensor maps, tile plan and launch (operands in the tensor
-// memory-access layout, checked by the caller).
+// 2:4 sparse A: tensor maps, kernel choice, tile plan and launch (operands in
+// the tensor memory-access layout, checked by the caller).  The CTA-pair
+// kernel (256×256 tiles) runs once its tiles fill every resident pair at least
+// once; smaller problems take the one-CTA kernel (128×128 tiles, twice the
+// CTAs in flight).  TGEMM_FORCE_SP24 = pair | cta overrides the choice (tests
+// and sweeps).  Both kernels take the same tensor maps: per CTA 128 rows of
+// Ac and E and 128 k of B per stage.
 template <typename T>
 tg_status_t launch_sp24(const void* Ac, const void* E, const void* B, void* C, int64_t M,
                         int64_t N, int64_t K, int64_t ldac, int64_t lde, int64_t ldb,
                         int64_t ldc, const tg::EpilogueSpec& ep, cudaStream_t s,
                         DeviceState* ds) {
     using Cfg = tg::SparseCfg;
+    using PairCfg = tg::SparsePairCfg<kSpPairStages>;
+    static_assert(PairCfg::BK == Cfg::BK && PairCfg::BM == 2 * Cfg::BM,
+                  "the two sparse kernels share their tensor maps");
     constexpr CUtensorMapDataType dt = tensor_map_type<T>();
     CUtensorMap tmA, tmB, tmE, tmC;
     if (!encode_2d(&tmA, Ac, K / 2, M, ldac * 2, 64, Cfg::BM, dt) ||
@@ -595,13 +623,21 @@ tg_status_t launch_sp24(const void* Ac, const void* E, const void* B, void* C, i
         !(ep.out_f32 ? encode_2d(&tmC, C, N, M, ldc * 4, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)
                      : encode_2d(&tmC, C, N, M, ldc * 2, 64, 32, dt)))
         return TG_ERR_LAUNCH;
+    const int64_t pair_tiles = ceil_div(M, PairCfg::BM) * ceil_div(N, PairCfg::BN);
+    bool pair = ds->max_sp_pairs >= 1 && pair_tiles >= ds->max_sp_pairs;
+    if (const char* f = std::getenv("TGEMM_FORCE_SP24")) {
+        if (std::strcmp(f, "pair") == 0) pair = ds->max_sp_pairs >= 1;
+        if (std::strcmp(f, "cta") == 0) pair = false;
+    }
+    const int64_t bm = pair ? PairCfg::BM : Cfg::BM;
+    const int64_t bn = pair ? PairCfg::BN : Cfg::BN;
     tg::SparseParams sp;
     tg::PersistentParams& prm = sp.base;
     prm.M = static_cast<int32_t>(M);
     prm.N = static_cast<int32_t>(N);
     prm.K = static_cast<int32_t>(K);
-    prm.tiles_m = static_cast<int32_t>(ceil_div(M, Cfg::BM));
-    prm.tiles_n = static_cast<int32_t>(ceil_div(N, Cfg::BN));
+    prm.tiles_m = static_cast<int32_t>(ceil_div(M, bm));
+    prm.tiles_n = static_cast<int32_t>(ceil_div(N, bn));
     prm.num_tiles = prm.tiles_m * prm.tiles_n;
     prm.k_blocks = static_cast<int32_t>(ceil_div(K, Cfg::BK));
     prm.group_m = prm.tiles_m < 16 ? prm.tiles_m : 16;
@@ -611,14 +647,32 @@ tg_status_t launch_sp24(const void* Ac, const void* E, const void* B, void* C, i
     prm.e = ep.e;
     prm.out_f32 = ep.out_f32;
     sp.words = static_cast<int32_t>(K / 32);
-    const int64_t grid = prm.num_tiles < ds->num_sms ? prm.num_tiles : ds->num_sms;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(Cfg::kThreads);
-    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cfg.stream = s;
-    if (cudaLaunchKernelEx(&cfg, tg::tg_gemm_sp24<T>, tmA, tmB, tmE, tmC, sp) != cudaSuccess) {
+    cudaError_t e;
+    if (pair) {
+        const int64_t pairs = prm.num_tiles < ds->max_sp_pairs ? prm.num_tiles : ds->max_sp_pairs;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+        cfg.blockDim = dim3(PairCfg::kThreads);
+        cfg.dynamicSmemBytes = PairCfg::kSmemBytes;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, tg::tg_gemm_sp24_pair<kSpPairStages, T>, tmA, tmB, tmE, tmC,
+                               sp);
+    } else {
+        const int64_t grid = prm.num_tiles < ds->num_sms ? prm.num_tiles : ds->num_sms;
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(Cfg::kThreads);
+        cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+        e = cudaLaunchKernelEx(&cfg, tg::tg_gemm_sp24<T>, tmA, tmB, tmE, tmC, sp);
+    }
+    if (e != cudaSuccess) {
         cudaGetLastError();
         return TG_ERR_LAUNCH;
     }

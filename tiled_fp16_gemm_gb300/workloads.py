@@ -254,6 +254,10 @@ SP24_WORKLOADS = {
         Sp24Workload("sp24_mlp_8192x28672x4096_relu", 8192, 28672, 4096, True,
                      ("normal", 0.0, 1.0 / 64.0), ("normal", 0.0, 1.0 / 64.0), 9,
                      "the MLP shape with a 2:4 sparse A (half of A's weights pruned)"),
+        Sp24Workload("sp24_8192x8192x4096_relu", 8192, 8192, 4096, True,
+                     ("normal", 0.0, 1.0 / 64.0), ("normal", 0.0, 1.0 / 64.0), 10,
+                     "a smaller square case for profiling captures: 228 MB of operands "
+                     "and output, above the L2's 129 MB"),
     ]
 }
 
