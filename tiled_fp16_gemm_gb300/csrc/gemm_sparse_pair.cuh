@@ -14,18 +14,35 @@
 // speed the L2 → SM bandwidth sets.
 //
 // Tensor memory (512 columns per CTA): one 256-column fp32 accumulator and,
-// from column 256, the metadata ring — each MMA's metadata column on a
-// 16-column boundary, 64 columns per stage.  Each CTA's tensor memory holds
+// from column 256, a ring of four metadata slots of 64 columns — each MMA's
+// metadata column on a 16-column boundary.  Each CTA's tensor memory holds
 // the metadata of its own 128 rows at the same column, in the lane layout of
 // the one-CTA kernel.  With one accumulator the epilogue's tensor-memory
 // reads of a tile are not overlapped with the next tile's MMAs (its global
 // stores are).
 //
+// The metadata path is kept off the operand ring's critical path and needs
+// no signal between the CTAs:
+//   * E boxes are loaded (plain TMA, local barrier) three stages ahead of
+//     the operands into their own 4-slot ring;
+//   * each CTA's metadata warps write stage u's words into metadata slot
+//     u % 4 once the MMAs of stage u - 4 have completed, then arrive on a
+//     local barrier;
+//   * each CTA's producer issues stage u's Ac load only after that local
+//     barrier, so the even CTA's full barrier — which counts both CTAs'
+//     bytes — completes only once both CTAs' metadata for the stage is in
+//     tensor memory.
+// A single thread issuing every TMA copy of a stage would take longer than
+// the stage's MMAs, so two threads (warps 0 and 10) share them: warp 0 the
+// Ac box and the E box kEAhead stages ahead, warp 10 the two B boxes (which
+// wait only for the stage's slot to be free).
+//
 // Synchronisation (all waits bounded):
 //   full[s]    even CTA: Ac and B bytes of both CTAs (pair TMA loads);
-//   efull[s]   each CTA: its own E box (plain TMA load);
-//   meta[s]    even CTA: the 8 metadata warps of the pair wrote stage s;
 //   empty[s]   each CTA: multicast commit after the MMAs of stage s;
+//   efull[e]   each CTA: its own E box;
+//   mready[m]  each CTA: its 4 metadata warps wrote slot m;
+//   mfree[m]   each CTA: multicast commit after the MMAs that read slot m;
 //   tfull      each CTA: multicast commit at the end of a tile;
 //   tempty     even CTA: the 8 epilogue warps of the pair read the tile.
 // A cluster barrier after set-up and before exit brackets the work.
@@ -48,7 +65,10 @@ struct SparsePairCfg {
     static constexpr int BM = 256;      // rows of C per cluster tile (128 per CTA)
     static constexpr int BN = 256;      // columns of C per cluster tile (B: 128 per CTA)
     static constexpr int BK = 128;      // dense-equivalent k per stage
-    static constexpr int kThreads = 320;
+    static constexpr int kThreads = 352;
+    static constexpr int kESlots = 4;   // E ring
+    static constexpr int kEAhead = 3;   // E boxes issued this many stages ahead
+    static constexpr int kMSlots = 4;   // metadata ring in tensor memory
     static constexpr uint32_t kABytes = 128 * (BK / 2) * 2;  // 16 KB of kept values
     static constexpr uint32_t kBBytes = BK * 128 * 2;        // 32 KB: two 64-column boxes
     static constexpr uint32_t kEBytes = 128 * (BK / 32) * 4; // 2 KB of metadata
@@ -56,13 +76,18 @@ struct SparsePairCfg {
     static constexpr uint32_t kCBytes = 4 * 2 * kCBuf;
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kMetaCol0 = BN;
-    static constexpr uint32_t kMetaStageCols = 64;
+    static constexpr uint32_t kMetaSlotCols = 64;
     static constexpr uint32_t kMetaSliceCols = 16;
     static constexpr uint32_t kBarBytes = 256;
-    static constexpr uint32_t kSmemBytes =
-        1024 + STAGES * (kABytes + kBBytes + kEBytes) + kCBytes + kBarBytes;
-    static_assert(kMetaCol0 + kMetaStageCols * STAGES <= kTmemCols,
+    static constexpr uint32_t kSmemBytes = 1024 + STAGES * (kABytes + kBBytes) +
+                                           kESlots * kEBytes + kCBytes + kBarBytes;
+    static_assert(kMetaCol0 + kMetaSlotCols * kMSlots <= kTmemCols,
                   "metadata columns exceed tensor memory");
+    // E slot (u + kEAhead) % kESlots was last read for stage u + kEAhead -
+    // kESlots <= u - 1, whose metadata the producer waited for at stage u - 1.
+    static_assert(kEAhead < kESlots, "E ring too shallow for the look-ahead");
+    static_assert(8 * (2 * STAGES + kESlots + 2 * kMSlots) + 32 <= kBarBytes,
+                  "barrier area too small");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeded");
 };
 
@@ -105,14 +130,45 @@ __device__ __forceinline__ void mma_f16_sp_pair(uint32_t d_tmem, uint64_t a_desc
         : "memory");
 }
 
+// Walks this cluster's (tile, k block) sequence: stage u is k block u % kb of
+// the cluster's tile u / kb (tiles cluster_id, cluster_id + nclusters, ...).
+// The tile's block coordinates (three integer divisions) are computed once
+// per tile, not per stage: the producer issues a stage every few hundred
+// cycles.
+struct StageIter {
+    int tile, kb, m_blk, n_blk;
+    const PersistentParams& p;
+    int step;
+    __device__ StageIter(int first_tile, const PersistentParams& p_, int step_)
+        : tile(first_tile), kb(0), m_blk(0), n_blk(0), p(p_), step(step_) {
+        coords();
+    }
+    __device__ void coords() {
+        if (tile < p.num_tiles) {
+            const TileCoord c = tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m);
+            m_blk = c.m_blk;
+            n_blk = c.n_blk;
+        }
+    }
+    __device__ void next() {
+        if (++kb == p.k_blocks) {
+            kb = 0;
+            tile += step;
+            coords();
+        }
+    }
+};
+
 template <int STAGES, typename T>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     tg_gemm_sp24_pair(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmE,
                       const __grid_constant__ CUtensorMap tmC, const SparseParams sp) {
     using Cfg = SparsePairCfg<STAGES>;
     constexpr int S = STAGES;
+    constexpr int SE = Cfg::kESlots;
+    constexpr int SM = Cfg::kMSlots;
     const PersistentParams& p = sp.base;
 
     extern __shared__ uint8_t smem_raw[];
@@ -123,17 +179,17 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t sA = base;
     const uint32_t sB = sA + S * Cfg::kABytes;
     const uint32_t sE = sB + S * Cfg::kBBytes;
-    const uint32_t sC = sE + S * Cfg::kEBytes;
+    const uint32_t sC = sE + SE * Cfg::kEBytes;
     const uint32_t sBar = sC + Cfg::kCBytes;
-    const uint32_t bar_full = sBar;              // [S]
-    const uint32_t bar_efull = sBar + 8 * S;     // [S]
-    const uint32_t bar_meta = sBar + 16 * S;     // [S]
-    const uint32_t bar_empty = sBar + 24 * S;    // [S]
-    const uint32_t bar_tfull = sBar + 32 * S;
+    const uint32_t bar_full = sBar;                  // [S]
+    const uint32_t bar_empty = bar_full + 8 * S;     // [S]
+    const uint32_t bar_efull = bar_empty + 8 * S;    // [SE]
+    const uint32_t bar_mready = bar_efull + 8 * SE;  // [SM]
+    const uint32_t bar_mfree = bar_mready + 8 * SM;  // [SM]
+    const uint32_t bar_tfull = bar_mfree + 8 * SM;
     const uint32_t bar_tempty = bar_tfull + 8;
     const uint32_t bar_drain = bar_tempty + 8;
     const uint32_t slot_tmem = bar_drain + 8;
-    static_assert(32 * S + 24 + 8 <= Cfg::kBarBytes, "barrier area too small");
     uint32_t* const tmem_slot_ptr = reinterpret_cast<uint32_t*>(base_ptr + (slot_tmem - base));
     volatile int* const abort_flag = reinterpret_cast<volatile int*>(tmem_slot_ptr + 1);
 
@@ -143,13 +199,20 @@ __global__ void __launch_bounds__(320, 1)
     const bool leader = rank == 0;
     const int cluster_id = static_cast<int>(blockIdx.x >> 1);
     const int nclusters = static_cast<int>(gridDim.x >> 1);
+    // stages this cluster runs: its tiles × k blocks
+    const int my_tiles =
+        cluster_id < p.num_tiles ? (p.num_tiles - cluster_id + nclusters - 1) / nclusters : 0;
+    const int U = my_tiles * p.k_blocks;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_efull + 8 * s, 1);
-            mbar_init(bar_meta + 8 * s, 8);
             mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int e = 0; e < SE; ++e) mbar_init(bar_efull + 8 * e, 1);
+        for (int m = 0; m < SM; ++m) {
+            mbar_init(bar_mready + 8 * m, 4);
+            mbar_init(bar_mfree + 8 * m, 1);
         }
         mbar_init(bar_tfull, 1);
         mbar_init(bar_tempty, 8);
@@ -179,52 +242,69 @@ __global__ void __launch_bounds__(320, 1)
     };
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer (both CTAs)
+        // ------------------------------------------------------------ producer of Ac and E (both CTAs)
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t issued_mask = 0, issued_parity = 0;
+            uint32_t issued_mask = 0, issued_parity = 0;      // full[] phases armed here
+            uint32_t e_issued_mask = 0, e_issued_parity = 0;  // efull[] phases armed here
+            StageIter e_it(cluster_id, p, nclusters);
+            int e_next = 0;  // next stage whose E box is issued
+            auto issue_e = [&]() {
+                const int ma = e_it.m_blk * Cfg::BM + static_cast<int>(rank) * 128;
+                const int slot = e_next % SE;
+                const uint32_t par = static_cast<uint32_t>(e_next / SE) & 1u;
+                const uint32_t eb = bar_efull + 8 * slot;
+                mbar_arrive_expect_tx(eb, Cfg::kEBytes);
+                tma_load_2d(sE + slot * Cfg::kEBytes, &tmE, eb, e_it.kb * (Cfg::BK / 32), ma);
+                e_issued_mask |= 1u << slot;
+                e_issued_parity = (e_issued_parity & ~(1u << slot)) | (par << slot);
+                e_it.next();
+                ++e_next;
+            };
+            while (e_next < U && e_next < Cfg::kEAhead) issue_e();
             bool ok = true;
-            for (int tile = cluster_id; ok && tile < p.num_tiles; tile += nclusters) {
-                const TileCoord tc = tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m);
-                const int ma = tc.m_blk * Cfg::BM + static_cast<int>(rank) * 128;
-                const int nb = tc.n_blk * Cfg::BN + static_cast<int>(rank) * 128;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.timeout_ns, abort_flag)) {
-                        fail(kRoleProducer);
-                        ok = false;
-                        break;
-                    }
-                    if (leader)
-                        mbar_arrive_expect_tx(bar_full + 8 * stage,
-                                              2 * (Cfg::kABytes + Cfg::kBBytes));
-                    const uint32_t fb = mapa_shared(bar_full + 8 * stage, 0);
-                    tma_load_2d_pair(sA + stage * Cfg::kABytes, &tmA, fb, kb * (Cfg::BK / 2), ma);
-                    tma_load_2d_pair(sB + stage * Cfg::kBBytes, &tmB, fb, nb, kb * Cfg::BK);
-                    tma_load_2d_pair(sB + stage * Cfg::kBBytes + Cfg::kBBytes / 2, &tmB, fb,
-                                     nb + 64, kb * Cfg::BK);
-                    const uint32_t eb = bar_efull + 8 * stage;
-                    mbar_arrive_expect_tx(eb, Cfg::kEBytes);
-                    tma_load_2d(sE + stage * Cfg::kEBytes, &tmE, eb, kb * (Cfg::BK / 32), ma);
-                    issued_mask |= 1u << stage;
-                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+            StageIter it(cluster_id, p, nclusters);
+            int stage = 0, mslot = 0;
+            uint32_t phase = 0, mphase = 0;
+            for (int u = 0; u < U; ++u, it.next()) {
+                if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.timeout_ns, abort_flag) ||
+                    !mbar_wait(bar_mready + 8 * mslot, mphase, p.timeout_ns, abort_flag)) {
+                    fail(kRoleProducer);
+                    ok = false;
+                    break;
+                }
+                // This CTA's metadata for stage u is in tensor memory: the
+                // loads below complete full[stage] only after it.
+                const int ma = it.m_blk * Cfg::BM + static_cast<int>(rank) * 128;
+                if (leader)
+                    mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * (Cfg::kABytes + Cfg::kBBytes));
+                const uint32_t fb = mapa_shared(bar_full + 8 * stage, 0);
+                tma_load_2d_pair(sA + stage * Cfg::kABytes, &tmA, fb, it.kb * (Cfg::BK / 2), ma);
+                issued_mask |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (e_next < U) issue_e();
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                if (++mslot == SM) {
+                    mslot = 0;
+                    mphase ^= 1u;
                 }
             }
             if (ok) {
                 // Normal exit: every phase armed here was consumed (by the MMA
                 // thread, and by this CTA's metadata warps), so these return at once.
                 for (int s = 0; s < S; ++s)
-                    if (issued_mask & (1u << s)) {
-                        const uint32_t par = (issued_parity >> s) & 1u;
-                        if ((leader && !mbar_wait(bar_full + 8 * s, par, p.timeout_ns, nullptr)) ||
-                            !mbar_wait(bar_efull + 8 * s, par, p.timeout_ns, nullptr))
+                    if (leader && (issued_mask & (1u << s)))
+                        if (!mbar_wait(bar_full + 8 * s, (issued_parity >> s) & 1u, p.timeout_ns,
+                                       nullptr))
                             atomicOr(&g_wait_timeout_flags, kRoleDrain);
-                    }
-            } else if (issued_mask != 0) {
+                for (int e = 0; e < SE; ++e)
+                    if (e_issued_mask & (1u << e))
+                        if (!mbar_wait(bar_efull + 8 * e, (e_issued_parity >> e) & 1u,
+                                       p.timeout_ns, nullptr))
+                            atomicOr(&g_wait_timeout_flags, kRoleDrain);
+            } else if ((issued_mask | e_issued_mask) != 0) {
                 // Abort: this CTA's last loads may be counted on a phase the
                 // pair never finishes; give them a fixed, bounded grace period
                 // (far above a TMA round trip) to land.
@@ -241,7 +321,7 @@ __global__ void __launch_bounds__(320, 1)
                 idesc_f16_f32(Cfg::BM, Cfg::BN, /*a_mn=*/false, /*b_mn=*/true,
                               Elem16<T>::kFmt) |
                 (1u << 2);
-            int stage = 0;
+            int stage = 0, mslot = 0;
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
@@ -253,9 +333,7 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 tc_fence_after_sync();
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait(bar_full + 8 * stage, phase, p.timeout_ns, abort_flag) ||
-                        !mbar_wait_cluster(bar_meta + 8 * stage, phase, p.timeout_ns,
-                                           abort_flag)) {
+                    if (!mbar_wait(bar_full + 8 * stage, phase, p.timeout_ns, abort_flag)) {
                         fail(kRoleMma);
                         ok = false;
                         break;
@@ -263,21 +341,23 @@ __global__ void __launch_bounds__(320, 1)
                     tc_fence_after_sync();
                     const uint32_t a0 = sA + stage * Cfg::kABytes;
                     const uint32_t b0 = sB + stage * Cfg::kBBytes;
+                    const uint32_t meta0 = tmem_base + Cfg::kMetaCol0 +
+                                           static_cast<uint32_t>(mslot) * Cfg::kMetaSlotCols;
 #pragma unroll
                     for (int k = 0; k < Cfg::BK / 32; ++k) {
                         const uint64_t adesc = smem_desc_sw128(a0 + 32 * k, 16, 1024);
                         const uint64_t bdesc = smem_desc_sw128(b0 + 4096 * k, 16384, 1024);
-                        const uint32_t meta = tmem_base + Cfg::kMetaCol0 +
-                                              static_cast<uint32_t>(stage) * Cfg::kMetaStageCols +
-                                              static_cast<uint32_t>(k) * Cfg::kMetaSliceCols;
-                        mma_f16_sp_pair(tmem_base, adesc, bdesc, meta, idesc,
-                                        (kb | k) != 0 ? 1u : 0u);
+                        mma_f16_sp_pair(tmem_base, adesc, bdesc,
+                                        meta0 + static_cast<uint32_t>(k) * Cfg::kMetaSliceCols,
+                                        idesc, (kb | k) != 0 ? 1u : 0u);
                     }
                     mma_commit_pair_mc(bar_empty + 8 * stage, 0x3);
+                    mma_commit_pair_mc(bar_mfree + 8 * mslot, 0x3);
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
+                    if (++mslot == SM) mslot = 0;
                 }
                 if (!ok) break;
                 if (!(p.inject == 1 && it == 0)) mma_commit_pair_mc(bar_tfull, 0x3);
@@ -285,6 +365,40 @@ __global__ void __launch_bounds__(320, 1)
             mma_commit_pair_mc(bar_drain, 0x1);
             if (!mbar_wait(bar_drain, 0, p.timeout_ns, nullptr))
                 atomicOr(&g_wait_timeout_flags, kRoleDrain);
+        }
+    } else if (warp == 10) {
+        // ------------------------------------------------------------ producer of B (both CTAs)
+        if (lane == 0) {
+            StageIter it(cluster_id, p, nclusters);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            bool issued = false;
+            for (int u = 0; u < U; ++u, it.next()) {
+                if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.timeout_ns, abort_flag)) {
+                    fail(kRoleProducer);
+                    ok = false;
+                    break;
+                }
+                // Counted on the even CTA's full barrier like the Ac box; the
+                // phase completes only when warp 0 of the even CTA has armed it.
+                const int nb = it.n_blk * Cfg::BN + static_cast<int>(rank) * 128;
+                const uint32_t fb = mapa_shared(bar_full + 8 * stage, 0);
+                tma_load_2d_pair(sB + stage * Cfg::kBBytes, &tmB, fb, nb, it.kb * Cfg::BK);
+                tma_load_2d_pair(sB + stage * Cfg::kBBytes + Cfg::kBBytes / 2, &tmB, fb, nb + 64,
+                                 it.kb * Cfg::BK);
+                issued = true;
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok && issued) {
+                // Abort: bounded grace period for the last loads to land.
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 1000000ull) {
+                }
+            }
         }
     } else if (warp < 6) {
         // ------------------------------------------------------------ epilogue (both CTAs)
@@ -335,6 +449,7 @@ __global__ void __launch_bounds__(320, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ metadata (warps 6..9, both CTAs)
+        static_assert(Cfg::kThreads == 11 * 32, "warp roles: 0, 1, 2-5, 6-9, 10");
         // Lane L of this CTA's tensor memory (quarter warp % 4) takes rows
         // r0 = (L & ~15) | (L & 7) and r1 = r0 + 8 of the CTA's 128, k half
         // h = (L >> 3) & 1 of each of the stage's four 32-k words.
@@ -343,55 +458,53 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t r1 = r0 + 8u;
         const uint32_t h = (L >> 3) & 1u;
         const uint32_t lane_addr = (32u * static_cast<uint32_t>(warp & 3)) << 16;
-        const uint32_t meta_leader = mapa_shared(bar_meta, 0);
         constexpr uint32_t kNeutral = 0x4444u;  // positions (0, 1) in every group of a half
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        for (int tile = cluster_id; ok && tile < p.num_tiles; tile += nclusters) {
-            const TileCoord tc = tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m);
-            const int m0 = tc.m_blk * Cfg::BM + static_cast<int>(rank) * 128;
+        StageIter it(cluster_id, p, nclusters);
+        int eslot = 0, mslot = 0;
+        uint32_t ephase = 0, mphase = 0;
+        for (int u = 0; u < U; ++u, it.next()) {
+            int got = 1;
+            if (lane == 0)
+                got = (mbar_wait(bar_efull + 8 * eslot, ephase, p.timeout_ns, abort_flag) &&
+                       mbar_wait(bar_mfree + 8 * mslot, mphase ^ 1u, p.timeout_ns, abort_flag))
+                          ? 1 : 0;
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) {
+                if (lane == 0) fail(kRoleMeta);
+                break;
+            }
+            tc_fence_after_sync();  // the MMAs that read this slot completed
+            const int m0 = it.m_blk * Cfg::BM + static_cast<int>(rank) * 128;
             const bool row0_in = m0 + static_cast<int>(r0) < p.M;
             const bool row1_in = m0 + static_cast<int>(r1) < p.M;
-            for (int kb = 0; kb < p.k_blocks; ++kb) {
-                int got = 1;
-                if (lane == 0)
-                    got = mbar_wait(bar_efull + 8 * stage, phase, p.timeout_ns, abort_flag) ? 1
-                                                                                             : 0;
-                got = __shfl_sync(0xffffffffu, got, 0);
-                if (!got) {
-                    if (lane == 0) fail(kRoleMeta);
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();  // the MMAs that read this stage's columns completed
-                const uint32_t e = sE + stage * Cfg::kEBytes;
-                const uint4 w0 = ld_shared_v4_u32(e + 16u * r0);
-                const uint4 w1 = ld_shared_v4_u32(e + 16u * r1);
-                const uint32_t a[4] = {w0.x, w0.y, w0.z, w0.w};
-                const uint32_t b[4] = {w1.x, w1.y, w1.z, w1.w};
-                uint32_t t[4];
+            const uint32_t e = sE + static_cast<uint32_t>(eslot) * Cfg::kEBytes;
+            const uint4 w0 = ld_shared_v4_u32(e + 16u * r0);
+            const uint4 w1 = ld_shared_v4_u32(e + 16u * r1);
+            const uint32_t a[4] = {w0.x, w0.y, w0.z, w0.w};
+            const uint32_t b[4] = {w1.x, w1.y, w1.z, w1.w};
+            uint32_t t[4];
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const bool word_in = kb * 4 + w < sp.words;
-                    const uint32_t lo =
-                        (row0_in && word_in) ? (a[w] >> (16 * h)) & 0xFFFFu : kNeutral;
-                    const uint32_t hi =
-                        (row1_in && word_in) ? (b[w] >> (16 * h)) & 0xFFFFu : kNeutral;
-                    t[w] = lo | (hi << 16);
-                }
-                const uint32_t col = tmem_base + lane_addr + Cfg::kMetaCol0 +
-                                     static_cast<uint32_t>(stage) * Cfg::kMetaStageCols;
+            for (int w = 0; w < 4; ++w) {
+                const bool word_in = it.kb * 4 + w < sp.words;
+                const uint32_t lo = (row0_in && word_in) ? (a[w] >> (16 * h)) & 0xFFFFu : kNeutral;
+                const uint32_t hi = (row1_in && word_in) ? (b[w] >> (16 * h)) & 0xFFFFu : kNeutral;
+                t[w] = lo | (hi << 16);
+            }
+            const uint32_t col = tmem_base + lane_addr + Cfg::kMetaCol0 +
+                                 static_cast<uint32_t>(mslot) * Cfg::kMetaSlotCols;
 #pragma unroll
-                for (int w = 0; w < 4; ++w) tmem_st_x1(col + w * Cfg::kMetaSliceCols, t[w]);
-                tmem_wait_st();
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(meta_leader + 8u * static_cast<uint32_t>(stage));
-                if (++stage == S) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+            for (int w = 0; w < 4; ++w) tmem_st_x1(col + w * Cfg::kMetaSliceCols, t[w]);
+            tmem_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_mready + 8 * mslot);
+            if (++eslot == SE) {
+                eslot = 0;
+                ephase ^= 1u;
+            }
+            if (++mslot == SM) {
+                mslot = 0;
+                mphase ^= 1u;
             }
         }
     }
