@@ -88,6 +88,29 @@ __device__ __forceinline__ void epilogue_math(float (&x)[64], const EpilogueArgs
     }
 }
 
+// Stage and store one chunk of 64 columns already rounded to the 16-bit type
+// (h[t] holds columns 2t and 2t + 1, the first in the low half).  cbuf: this
+// warp's two 4 KB staging buffers; buf: which one is used next (toggled).
+__device__ __forceinline__ void epilogue_store_packed(const uint32_t (&h)[32], uint32_t cbuf,
+                                                      int& buf, const void* tmC, uint64_t policy,
+                                                      int row0, int col0, int M, int N, int lane) {
+    if (lane == 0) bulk_wait_group_read<1>();  // the buffer used two chunks ago is free
+    __syncwarp();
+    const uint32_t cb = cbuf + static_cast<uint32_t>(buf) * 4096u;
+    const uint32_t row_addr = cb + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        st_shared_v4(row_addr + ((static_cast<uint32_t>(c) ^ (lane & 7u)) << 4), h[4 * c],
+                     h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (row0 < M && col0 < N) tma_store_2d_hint(tmC, cb, col0, row0, policy);
+        bulk_commit_group();
+    }
+    buf ^= 1;
+}
+
 // Stage and store one chunk.  cbuf: this warp's two 4 KB staging buffers;
 // buf: which one the 16-bit path uses next (toggled).  row0: the warp's first
 // row (stores are clipped at M and N by the tensor map).  out_f32 (uniform
@@ -100,21 +123,7 @@ __device__ __forceinline__ void epilogue_store(const float (&x)[64], uint32_t cb
         uint32_t h[32];
 #pragma unroll
         for (int t = 0; t < 32; ++t) h[t] = Elem16<T>::pack2(x[2 * t], x[2 * t + 1]);
-        if (lane == 0) bulk_wait_group_read<1>();  // the buffer used two chunks ago is free
-        __syncwarp();
-        const uint32_t cb = cbuf + static_cast<uint32_t>(buf) * 4096u;
-        const uint32_t row_addr = cb + static_cast<uint32_t>(lane) * 128u;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-            st_shared_v4(row_addr + ((static_cast<uint32_t>(c) ^ (lane & 7u)) << 4), h[4 * c],
-                         h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            if (row0 < M && col0 < N) tma_store_2d_hint(tmC, cb, col0, row0, policy);
-            bulk_commit_group();
-        }
-        buf ^= 1;
+        epilogue_store_packed(h, cbuf, buf, tmC, policy, row0, col0, M, N, lane);
     } else {
         // fp32: 256 bytes per row, two 32-column boxes, one per buffer.
         if (lane == 0) bulk_wait_group_read<0>();

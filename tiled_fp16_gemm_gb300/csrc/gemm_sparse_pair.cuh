@@ -119,6 +119,50 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
     }
 }
 
+// Arrive on an mbarrier of the peer CTA without release semantics (no memory
+// barrier): used where the signal only says "this thread has finished reading
+// tensor memory" — tcgen05.wait::ld completed those reads before the arrive
+// issues, and there are no writes whose visibility it would have to order.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
+// Early-release epilogue step: 64 accumulator columns of this thread's row
+// (tensor memory at taddr, one load) → bias, activation → 32 packed 16-bit
+// pairs (h[t]: columns 2t, 2t + 1).
+template <typename T>
+__device__ __forceinline__ void epilogue_pack64(uint32_t taddr, const EpilogueArgs& e, int relu,
+                                                int col0, int N, uint32_t (&h)[32]) {
+    uint32_t v[64];
+    tmem_ld_x64(taddr, v);
+    float x[64];
+#pragma unroll
+    for (int t = 0; t < 64; ++t) x[t] = __uint_as_float(v[t]);
+    if (e.bias != nullptr) {
+        if (e.bias_vec && col0 + 64 <= N) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                const float4 b = __ldg(reinterpret_cast<const float4*>(e.bias + col0) + t);
+                x[4 * t] += b.x;
+                x[4 * t + 1] += b.y;
+                x[4 * t + 2] += b.z;
+                x[4 * t + 3] += b.w;
+            }
+        } else {
+#pragma unroll
+            for (int t = 0; t < 64; ++t)
+                if (col0 + t < N) x[t] += __ldg(e.bias + col0 + t);
+        }
+    }
+    if (relu) {
+#pragma unroll
+        for (int t = 0; t < 64; ++t) x[t] = relu_f32(x[t]);
+    }
+#pragma unroll
+    for (int t = 0; t < 32; ++t) h[t] = Elem16<T>::pack2(x[2 * t], x[2 * t + 1]);
+}
+
 __device__ __forceinline__ void mma_f16_sp_pair(uint32_t d_tmem, uint64_t a_desc,
                                                 uint64_t b_desc, uint32_t meta_tmem,
                                                 uint32_t idesc, uint32_t accumulate) {
@@ -321,6 +365,12 @@ __global__ void __launch_bounds__(352, 1)
                 idesc_f16_f32(Cfg::BM, Cfg::BN, /*a_mn=*/false, /*b_mn=*/true,
                               Elem16<T>::kFmt) |
                 (1u << 2);
+            // Descriptors of stage 0; a stage or k step only moves the start
+            // address, the descriptor's low 14 bits (address / 16, and every
+            // address here is below 256 KB), so it is a plain add.
+            const uint64_t adesc0 = smem_desc_sw128(sA, 16, 1024);
+            const uint64_t bdesc0 = smem_desc_sw128(sB, 16384, 1024);
+            constexpr uint64_t kAStep = Cfg::kABytes >> 4, kBStep = Cfg::kBBytes >> 4;
             int stage = 0, mslot = 0;
             uint32_t phase = 0;
             int it = 0;
@@ -339,15 +389,14 @@ __global__ void __launch_bounds__(352, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a0 = sA + stage * Cfg::kABytes;
-                    const uint32_t b0 = sB + stage * Cfg::kBBytes;
+                    const uint64_t ad = adesc0 + static_cast<uint64_t>(stage) * kAStep;
+                    const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage) * kBStep;
                     const uint32_t meta0 = tmem_base + Cfg::kMetaCol0 +
                                            static_cast<uint32_t>(mslot) * Cfg::kMetaSlotCols;
 #pragma unroll
                     for (int k = 0; k < Cfg::BK / 32; ++k) {
-                        const uint64_t adesc = smem_desc_sw128(a0 + 32 * k, 16, 1024);
-                        const uint64_t bdesc = smem_desc_sw128(b0 + 4096 * k, 16384, 1024);
-                        mma_f16_sp_pair(tmem_base, adesc, bdesc,
+                        // A: 16 kept values (32 B) per MMA; B: 32 k rows (4 KB)
+                        mma_f16_sp_pair(tmem_base, ad + 2 * k, bd + 256 * k,
                                         meta0 + static_cast<uint32_t>(k) * Cfg::kMetaSliceCols,
                                         idesc, (kb | k) != 0 ? 1u : 0u);
                     }
@@ -407,6 +456,7 @@ __global__ void __launch_bounds__(352, 1)
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
         const uint64_t c_policy = policy_evict_first();
         const uint32_t tempty_leader = mapa_shared(bar_tempty, 0);
+        const bool early_release = p.out_f32 == 0 && p.e.resid == nullptr;
         int buf = 0;
         int it = 0;
         for (int tile = cluster_id; tile < p.num_tiles; tile += nclusters, ++it) {
@@ -423,6 +473,50 @@ __global__ void __launch_bounds__(352, 1)
                 break;
             }
             tc_fence_after_sync();
+            if (early_release) {
+                // 16-bit C without a residual: the row's 256 columns are read,
+                // finished and rounded before anything is stored — columns
+                // 0..127 straight into the two staging buffers (swizzled as
+                // epilogue_store_packed lays them out), 128..255 into
+                // registers — so the accumulator is released first.
+                if (lane == 0) bulk_wait_group_read<0>();  // both buffers free
+                __syncwarp();
+                const uint32_t row_off = static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    uint32_t hp[32];
+                    epilogue_pack64<T>(tmem_base + lane_addr + static_cast<uint32_t>(64 * j), p.e,
+                                       p.relu, n0 + 64 * j, p.N, hp);
+                    const uint32_t rb = cbuf + static_cast<uint32_t>(j) * 4096u + row_off;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        st_shared_v4(rb + ((static_cast<uint32_t>(u) ^ (lane & 7u)) << 4),
+                                     hp[4 * u], hp[4 * u + 1], hp[4 * u + 2], hp[4 * u + 3]);
+                }
+                uint32_t h2[32], h3[32];
+                epilogue_pack64<T>(tmem_base + lane_addr + 128u, p.e, p.relu, n0 + 128, p.N, h2);
+                epilogue_pack64<T>(tmem_base + lane_addr + 192u, p.e, p.relu, n0 + 192, p.N, h3);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        if (row0 < p.M && n0 + 64 * j < p.N)
+                            tma_store_2d_hint(&tmC, cbuf + static_cast<uint32_t>(j) * 4096u,
+                                              n0 + 64 * j, row0, c_policy);
+                        bulk_commit_group();
+                    }
+                }
+                buf = 0;
+                epilogue_store_packed(h2, cbuf, buf, &tmC, c_policy, row0, n0 + 128, p.M, p.N,
+                                      lane);
+                epilogue_store_packed(h3, cbuf, buf, &tmC, c_policy, row0, n0 + 192, p.M, p.N,
+                                      lane);
+                continue;
+            }
 #pragma unroll 1
             for (int j = 0; j < Cfg::BN / 64; ++j) {
                 uint32_t v0[32], v1[32];
@@ -432,7 +526,7 @@ __global__ void __launch_bounds__(352, 1)
                 if (j == Cfg::BN / 64 - 1) {
                     tc_fence_before_sync();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(tempty_leader);
+                    if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
                 }
                 float x[64];
 #pragma unroll
