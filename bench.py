@@ -322,7 +322,8 @@ def run_ours(args, w, rank, world, local_rank):
     if plan.kernel == tg.TG_KERNEL_PERSISTENT:
         if plan.cluster == 2:
             kernel_key = "pair256"
-            kname = f"tg_gemm_f16_pair<{plan.stages}> (CTA pairs, 256x256 tiles)"
+            kname = (f"tg_gemm_f16_pair<{plan.stages} stages of {plan.bk} k> "
+                     "(CTA pairs, 256x256 tiles)")
         else:
             kernel_key = f"persistent_bn{plan.bn}"
             kname = f"tg_gemm_f16_persistent<{plan.bn},{plan.stages}>"
@@ -498,7 +499,7 @@ def run_ours(args, w, rank, world, local_rank):
                     ent["vs_fp16_skinny"] = out["skinny"]["kernel_ms_mean"] / k6
             else:
                 tf = mw.flops / (k6 / 1e3) / 1e12
-                ent["kernel"] = "tg_mxfp4_dequant_f16 + tg_gemm_f16_pair<6>"
+                ent["kernel"] = "tg_mxfp4_dequant_f16 + tg_gemm_f16_pair (256x256 tiles)"
                 ent["roofline"] = {"bound": "tensor", "achieved": tf, "peak": tf_peak,
                                    "unit": "TFLOP/s", "frac": tf / tf_peak}
             out["mxfp4"][mname] = ent

@@ -236,10 +236,10 @@ def test_plan_k_steps_and_grid_match_page_listing(tg):
 def test_plans(tg):
     p = tg.tg_plan_f16(8192, 28672, 4096, 152)
     assert p.kernel == tg.TG_KERNEL_PERSISTENT and p.cluster == 2
-    assert (p.bm, p.bn, p.bk, p.mma_m, p.mma_n) == (256, 256, 64, 256, 256)
-    assert p.num_tiles == 32 * 112 and p.grid == 152 and p.k_blocks == 64
+    assert (p.bm, p.bn, p.bk, p.mma_m, p.mma_n) == (256, 256, 128, 256, 256)
+    assert p.num_tiles == 32 * 112 and p.grid == 152 and p.k_blocks == 32 and p.stages == 3
     assert p.smem_bytes <= 232448  # 227 KB opt-in limit per CTA
-    assert p.ring_bytes == 2 * tg.tg_ring_bytes(128, 128, 64, p.stages, 2)
+    assert p.ring_bytes == 2 * tg.tg_ring_bytes(128, 128, 128, p.stages, 2)
     one = tg.tg_plan_f16(2048, 2048, 4096, 152)  # 64 pair tiles < 76 pairs: one-CTA tiles
     assert one.cluster == 1 and (one.bm, one.bn) == (128, 128) and one.grid == 152
     pair = tg.tg_plan_f16(2048, 4864, 4096, 152)  # 8 x 19 = 152 pair tiles: two waves of pairs

@@ -1,14 +1,17 @@
 // Persistent FP16 GEMM on CTA pairs (tcgen05 cta_group::2) for sm_103a:
 //   C = epi(A · B), 256×256 output tiles per cluster of two CTAs.
 //
-// Each CTA of the pair (rank r = 0, 1) owns, in its own shared memory:
-//   A rows  [m0 + 128 r, m0 + 128 r + 128)  × 64 k   (K-major, one 16 KB box)
-//   B cols  [n0 + 128 r, n0 + 128 r + 128)  × 64 k   (MN-major, two 8 KB boxes)
+// Each CTA of the pair (rank r = 0, 1) owns, per stage of BK k, in its own
+// shared memory:
+//   A rows  [m0 + 128 r, m0 + 128 r + 128)  × BK k  (K-major, BK/64 boxes of 16 KB)
+//   B cols  [n0 + 128 r, n0 + 128 r + 128)  × BK k  (MN-major, two boxes of 64 columns)
 // at identical offsets.  The even CTA's single MMA thread issues
 // 256×256×16 tcgen05.mma over the pair; result rows 128 r .. 128 r + 127 land
 // in CTA r's TMEM (two 256-column fp32 accumulators per CTA).  Per SM this
 // halves the operand bytes loaded per MMA cycle compared with a one-CTA
-// 128×256 tile, so a 6-stage ring of 32 KB stages covers ~3000 MMA cycles.
+// 128×256 tile.  One MMA covers 128 tensor cycles of the SM, and each issue
+// costs the MMA thread a large part of that, so the per-stage work of that
+// thread (barrier wait, fence, commit) is spread over BK/16 MMAs.
 //
 // Synchronisation (all waits bounded):
 //   full[s]     in the even CTA only: its producer arms it with the bytes of
@@ -34,11 +37,12 @@
 
 namespace tg {
 
-template <int STAGES>
+template <int STAGES, int BK_ = 64>
 struct PairCfg {
     static constexpr int BM = 256;  // rows of C per cluster tile (128 per CTA)
     static constexpr int BN = 256;  // columns of C per cluster tile
-    static constexpr int BK = 64;
+    static constexpr int BK = BK_;
+    static_assert(BK % 64 == 0, "A arrives in 64-k boxes");
     static constexpr int kThreads = 192;
     static constexpr uint32_t kABytes = 128 * BK * 2;  // this CTA's A half
     static constexpr uint32_t kBBytes = 128 * BK * 2;  // this CTA's B half
@@ -49,13 +53,14 @@ struct PairCfg {
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kSmemBytes =
         1024 + STAGES * kStageBytes + kCBytes + kBarBytes;
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeded");
 };
 
-template <int STAGES, typename T = __half>
+template <int STAGES, typename T = __half, int BK_ = 64>
 __global__ void __launch_bounds__(192, 1)
     tg_gemm_f16_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const PersistentParams p) {
-    using Cfg = PairCfg<STAGES>;
+    using Cfg = PairCfg<STAGES, BK_>;
     constexpr int BK = Cfg::BK;
     constexpr uint32_t kABytes = Cfg::kABytes;
     constexpr uint32_t kBBytes = Cfg::kBBytes;
@@ -138,9 +143,13 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * Cfg::kStageBytes);
                     const uint32_t fb = mapa_shared(bar_full + 8 * stage, 0);
-                    tma_load_2d_pair(sA + stage * kABytes, &tmA, fb, kb * BK, ma);
+#pragma unroll
+                    for (int i = 0; i < BK / 64; ++i)
+                        tma_load_2d_pair(sA + stage * kABytes + 16384 * i, &tmA, fb,
+                                         kb * BK + 64 * i, ma);
                     tma_load_2d_pair(sB + stage * kBBytes, &tmB, fb, nb, kb * BK);
-                    tma_load_2d_pair(sB + stage * kBBytes + 8192, &tmB, fb, nb + 64, kb * BK);
+                    tma_load_2d_pair(sB + stage * kBBytes + kBBytes / 2, &tmB, fb, nb + 64,
+                                     kb * BK);
                     issued_mask |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -195,8 +204,11 @@ __global__ void __launch_bounds__(192, 1)
                     const uint32_t b0 = sB + stage * kBBytes;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        const uint64_t adesc = smem_desc_sw128(a0 + 32 * k, 16, 1024);
-                        const uint64_t bdesc = smem_desc_sw128(b0 + 2048 * k, 8192, 1024);
+                        // A: 64-k boxes of 16 KB, 32 B per k16 inside one; B: 16
+                        // k rows (2 KB) per k16, the two column boxes kBBytes/2 apart
+                        const uint64_t adesc =
+                            smem_desc_sw128(a0 + 16384 * (k / 4) + 32 * (k % 4), 16, 1024);
+                        const uint64_t bdesc = smem_desc_sw128(b0 + 2048 * k, kBBytes / 2, 1024);
                         mma_f16_ss_pair(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
                     }
                     mma_commit_pair_mc(bar_empty + 8 * stage, 0x3);

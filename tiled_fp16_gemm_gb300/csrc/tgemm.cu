@@ -63,7 +63,13 @@ void plan_persistent(int64_t M, int64_t N, int64_t K, int32_t num_sms, int bn, i
     p->cluster = 1;
 }
 
-constexpr int kPairStages = 6;
+// Pair kernel ring: 3 stages of 128 k (64 KB per CTA each).  The MMA thread
+// waits and commits once per stage, so 8 MMAs per stage instead of 4 leave it
+// more of each stage's 1024 tensor cycles; measured on the 8192×28672×4096
+// workload against 6 stages of 64 k: 1.144 ms vs 1.171 ms, same result bits.
+constexpr int kPairStages = 3;
+constexpr int kPairBK = 128;  // k per ring stage of the pair kernel
+using PairCfgT = tg::PairCfg<kPairStages, kPairBK>;
 // 16 blocks of 256 rows = 4096 rows per raster group: a wave of 76 pair tiles
 // then spans 16 × ~5 tiles (A 32 MB + B 10 MB in L2) and B is reread M/4096
 // times.  Swept on the 8192×28672×4096 workload: 2: 1450, 4: 1528, 8: 1589,
@@ -79,20 +85,20 @@ void plan_pair(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* p) {
     p->kernel = TG_KERNEL_PERSISTENT;
     p->bm = 256;
     p->bn = 256;
-    p->bk = 64;
+    p->bk = kPairBK;
     p->stages = kPairStages;
     p->mma_m = 256;
     p->mma_n = 256;
     p->tiles_m = ceil_div(M, 256);
     p->tiles_n = ceil_div(N, 256);
-    p->k_blocks = ceil_div(K, 64);
+    p->k_blocks = ceil_div(K, kPairBK);
     p->num_tiles = p->tiles_m * p->tiles_n;
     const int64_t pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
     p->grid = 2 * (p->num_tiles < pairs ? p->num_tiles : pairs);
     p->threads = 192;
     p->group_m = static_cast<int32_t>(p->tiles_m < kPairGroupM ? p->tiles_m : kPairGroupM);
-    p->smem_bytes = tg::PairCfg<kPairStages>::kSmemBytes;
-    p->ring_bytes = 2 * tg_ring_bytes(128, 128, 64, kPairStages, 2);  // both CTAs
+    p->smem_bytes = PairCfgT::kSmemBytes;
+    p->ring_bytes = 2 * tg_ring_bytes(128, 128, kPairBK, kPairStages, 2);  // both CTAs
     p->split_k = 1;
     p->workspace_bytes = 0;
     p->cluster = 2;
@@ -138,9 +144,9 @@ cudaError_t set_kernel_attributes() {
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  tg::PersistentCfg<kMidBN, kMidStages>::kSmemBytes);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(tg::tg_gemm_f16_pair<kPairStages, T>,
+        e = cudaFuncSetAttribute(tg::tg_gemm_f16_pair<kPairStages, T, kPairBK>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 tg::PairCfg<kPairStages>::kSmemBytes);
+                                 PairCfgT::kSmemBytes);
     if (e == cudaSuccess) e = tg::skinny_set_attributes<T>();
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(tg::tg_gemm_sp24<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -206,9 +212,8 @@ tg_status_t current_device(int* dev, DeviceState** st) {
             cudaGetLastError();
             return TG_ERR_LAUNCH;
         }
-        s.max_pairs = max_active_pairs(tg::tg_gemm_f16_pair<kPairStages, __half>,
-                                       tg::PairCfg<kPairStages>::kThreads,
-                                       tg::PairCfg<kPairStages>::kSmemBytes, s.num_sms);
+        s.max_pairs = max_active_pairs(tg::tg_gemm_f16_pair<kPairStages, __half, kPairBK>,
+                                       PairCfgT::kThreads, PairCfgT::kSmemBytes, s.num_sms);
         s.max_sp_pairs = max_active_pairs(tg::tg_gemm_sp24_pair<kSpPairStages, __half>,
                                           tg::SparsePairCfg<kSpPairStages>::kThreads,
                                           tg::SparsePairCfg<kSpPairStages>::kSmemBytes, s.num_sms);
@@ -250,15 +255,16 @@ bool encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer
                         CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// A, B and C maps of the pair / one-CTA kernels.  C: 32 rows × 128 bytes per
-// box (64 16-bit or 32 fp32 elements).
+// A, B and C maps of the pair / one-CTA kernels.  A: 64 k × 128 rows per box;
+// B: 64 columns × b_box_k k rows per box (the kernel's k per stage); C: 32
+// rows × 128 bytes per box (64 16-bit or 32 fp32 elements).
 template <typename T>
 bool encode_abc(CUtensorMap* tmA, CUtensorMap* tmB, CUtensorMap* tmC, const void* A,
                 const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
-                int64_t ldc, bool out_f32) {
+                int64_t ldc, bool out_f32, uint32_t b_box_k = 64) {
     constexpr CUtensorMapDataType dt = tensor_map_type<T>();
     return encode_2d(tmA, A, K, M, lda * 2, 64, 128, dt) &&
-           encode_2d(tmB, B, N, K, ldb * 2, 64, 64, dt) &&
+           encode_2d(tmB, B, N, K, ldb * 2, 64, b_box_k, dt) &&
            (out_f32 ? encode_2d(tmC, C, N, M, ldc * 4, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)
                     : encode_2d(tmC, C, N, M, ldc * 2, 64, 32, dt));
 }
@@ -312,7 +318,8 @@ tg_status_t launch_pair(const void* A, const void* B, void* C, const tg_plan_t& 
                         int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                         const tg::EpilogueSpec& ep, cudaStream_t stream, int max_pairs) {
     CUtensorMap tmA, tmB, tmC;
-    if (!encode_abc<T>(&tmA, &tmB, &tmC, A, B, C, M, N, K, lda, ldb, ldc, ep.out_f32 != 0))
+    if (!encode_abc<T>(&tmA, &tmB, &tmC, A, B, C, M, N, K, lda, ldb, ldc, ep.out_f32 != 0,
+                       kPairBK))
         return TG_ERR_LAUNCH;
     const tg::PersistentParams prm = persistent_params(pl, M, N, K, ep);
     int64_t pairs = pl.grid / 2;
@@ -325,13 +332,14 @@ tg_status_t launch_pair(const void* A, const void* B, void* C, const tg_plan_t& 
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-    cfg.blockDim = dim3(tg::PairCfg<kPairStages>::kThreads);
-    cfg.dynamicSmemBytes = tg::PairCfg<kPairStages>::kSmemBytes;
+    cfg.blockDim = dim3(PairCfgT::kThreads);
+    cfg.dynamicSmemBytes = PairCfgT::kSmemBytes;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e =
-        cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_pair<kPairStages, T>, tmA, tmB, tmC, prm);
+        cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_pair<kPairStages, T, kPairBK>, tmA, tmB, tmC,
+                           prm);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return TG_ERR_LAUNCH;
