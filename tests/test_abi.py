@@ -246,8 +246,12 @@ def test_plans(tg):
     assert pair.cluster == 2 and pair.num_tiles == 152 and pair.grid == 152
     s = tg.tg_plan_f16(64, 16384, 8192, 152)
     assert s.kernel == tg.TG_KERNEL_SKINNY
-    assert (s.mma_m, s.mma_n) == (128, 64) and s.tiles_n == 128 and s.k_blocks == 128
+    assert (s.mma_m, s.mma_n) == (128, 64) and s.tiles_n == 128
+    assert (s.bk, s.k_blocks, s.stages) == (64, 128, 9)
     assert s.grid == 152 and s.workspace_bytes > 0 and s.smem_bytes <= 232448
+    w = tg.tg_plan_f16(128, 16384, 8192, 152)  # Mp = 128: 64-k units, 6 stages
+    assert w.kernel == tg.TG_KERNEL_SKINNY and (w.bk, w.k_blocks, w.stages) == (64, 128, 6)
+    assert w.smem_bytes <= 232448
     small = tg.tg_plan_f16(7, 5, 3, 152)
     assert small.kernel == tg.TG_KERNEL_SKINNY and small.mma_n == 16 and small.grid == 1
     assert tg.tg_plan_f16(0, 5, 3, 152).kernel == tg.TG_KERNEL_NONE

@@ -6,9 +6,13 @@
 //     C^T (N×M) = B^T (N×K) · A^T (K×M)
 // with N as the 128-row MMA dimension and Mp = roundup(M, 16) as the MMA
 // N dimension:
-//   MMA A operand = B^T tile, 128 n × 64 k, read MN-major from row-major B;
-//   MMA B operand = A tile,   Mp m × 64 k, K-major from row-major A;
+//   MMA A operand = B^T tile, 128 n × BK k, read MN-major from row-major B;
+//   MMA B operand = A tile,   Mp m × BK k, K-major from row-major A;
 //   D (TMEM)      = 128 lanes (n) × Mp columns (m), fp32.
+// BK (k per unit) is a parameter of the ring shape; both shapes use 64.  On
+// the 64×16384×8192 workload, units of 128 k (4 stages of 48 KB) and of 256
+// k (2 stages of 96 KB: B in 32 KB boxes) measured 52.5 and 53.3 µs against
+// 51.7 µs for 64 k (9 stages of 24 KB).
 //
 // Split-K over "units" (tile, k-block), numbered tile-major.  CTA c of G owns
 // the contiguous unit range [U·c/G, U·(c+1)/G), so every SM streams the same
@@ -55,20 +59,26 @@
 
 namespace tg {
 
-constexpr uint32_t kSkBBytes = 128 * 64 * 2;  // B^T tile: two 64×64 boxes
+// B^T tile of one unit: two boxes of 64 columns × BK k.
+__host__ __device__ constexpr uint32_t skinny_b_bytes(int bk) {
+    return 128u * static_cast<uint32_t>(bk) * 2u;
+}
 
 // Two ring shapes, both about 220 KB of shared memory: A slots sized for
 // Mp ≤ 64 (24 KB stages, 9 deep: 144 KB of B in flight per SM) or for
-// Mp ≤ 128 (32 KB stages, 6 deep).
-template <int STAGES, int MP_MAX>
+// Mp ≤ 128 (32 KB stages, 6 deep).  A stage of BK k holds B^T as two boxes
+// of 64 columns × BK k and the A tile as BK/64 boxes of 64 k.
+template <int STAGES, int MP_MAX, int BK_>
 struct SkinnyCfg {
     static constexpr int kStages = STAGES;
-    static constexpr uint32_t kASlot = MP_MAX * 64 * 2;
-    static constexpr uint32_t kStageBytes = kSkBBytes + kASlot;
+    static constexpr int kBK = BK_;
+    static constexpr uint32_t kASlot = MP_MAX * BK_ * 2;
+    static constexpr uint32_t kStageBytes = skinny_b_bytes(BK_) + kASlot;
     static constexpr uint32_t kSmemBytes = 1024 + STAGES * kStageBytes + 256;
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeded");
 };
-using SkinnyNarrow = SkinnyCfg<9, 64>;
-using SkinnyWide = SkinnyCfg<6, 128>;
+using SkinnyNarrow = SkinnyCfg<9, 64, 64>;
+using SkinnyWide = SkinnyCfg<6, 128, 64>;
 // MXFP4 B (M ≤ 128 weight streaming).  Per unit, one 128 n × 64 k tile of
 // packed codes (128 rows × 32 bytes, TMA 32-byte swizzle), its scales (2
 // rows × 128 bytes) and the A tile land in a deep raw ring.  Converter
@@ -160,12 +170,14 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
 
 // The kernel body shared by the fp16/bf16 kernel (QB = false: B^T tiles by
 // TMA) and the MXFP4 kernel (QB = true: B^T tiles decoded by warps 6..13).
-template <int STAGES, int MP_MAX, typename T, bool QB>
+template <int STAGES, int MP_MAX, typename T, bool QB, int BK = 64>
 __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtensorMap* tmA,
                                             const CUtensorMap* tmS, const SkinnyParams& p) {
-    constexpr int BK = 64;
+    static_assert(BK % 64 == 0 && (!QB || BK == 64), "MXFP4 units are 64 k");
     constexpr int kSkStages = STAGES;
-    constexpr uint32_t kSkASlot = MP_MAX * 64 * 2;
+    constexpr uint32_t kSkBBytes = skinny_b_bytes(BK);
+    constexpr uint32_t kABox = MP_MAX * 64 * 2;   // one 64-k box of the A tile (≤ MP_MAX rows)
+    constexpr uint32_t kSkASlot = kABox * (BK / 64);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -245,6 +257,7 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
     // scales + A).
     constexpr int kRing = QB ? kRaw : kSkStages;
     constexpr int kProd = skinny_producers(kRing);
+    static_assert(kRing % kProd == 0, "each ring stage must belong to one producer thread");
     constexpr int kProdWarp1 = 6 + (QB ? kMxConvWarps : 0);  // warp of producer 1
     const int prod = warp == 0 ? 0 : (warp >= kProdWarp1 ? warp - kProdWarp1 + 1 : -1);
     if (prod >= 0) {
@@ -276,11 +289,14 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                                      stream);
                     tma_load_2d_hint(sA + stage * kSkASlot, tmA, full, kb * BK, 0, keep);
                 } else {
-                    mbar_arrive_expect_tx(full, kSkBBytes + a_bytes);
+                    mbar_arrive_expect_tx(full, kSkBBytes + (BK / 64) * a_bytes);
                     const uint32_t b0 = sB + stage * kSkBBytes;
                     tma_load_2d_hint(b0, tmB, full, t * 128, kb * BK, stream);
-                    tma_load_2d_hint(b0 + 8192, tmB, full, t * 128 + 64, kb * BK, stream);
-                    tma_load_2d_hint(sA + stage * kSkASlot, tmA, full, kb * BK, 0, keep);
+                    tma_load_2d_hint(b0 + kSkBBytes / 2, tmB, full, t * 128 + 64, kb * BK, stream);
+#pragma unroll
+                    for (int i = 0; i < BK / 64; ++i)
+                        tma_load_2d_hint(sA + stage * kSkASlot + kABox * i, tmA, full,
+                                         kb * BK + 64 * i, 0, keep);
                 }
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -334,7 +350,9 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                     const uint32_t a0 = sA + (QB ? rstage : stage) * kSkASlot;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        const uint64_t bdesc = smem_desc_sw128(a0 + 32 * k, 16, 1024);
+                        // A tile: 64-k boxes kABox apart, 32 B per 16 k inside one
+                        const uint64_t bdesc =
+                            smem_desc_sw128(a0 + kABox * (k / 4) + 32 * (k % 4), 16, 1024);
                         const uint32_t acc_in = (v != u || k != 0) ? 1u : 0u;
                         if constexpr (QB) {
                             // 16 k = 8 columns of the operand stage
@@ -342,7 +360,10 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                                                     static_cast<uint32_t>(32 * stage + 8 * k);
                             mx_mma_f16_ts(d_tmem, a_tmem, bdesc, idesc, acc_in);
                         } else {
-                            const uint64_t adesc = smem_desc_sw128(b0 + 2048 * k, 8192, 1024);
+                            // B^T: 16 k rows (2 KB) per step; the two 64-column
+                            // boxes kSkBBytes / 2 apart
+                            const uint64_t adesc =
+                                smem_desc_sw128(b0 + 2048 * k, kSkBBytes / 2, 1024);
                             mma_f16_ss(d_tmem, adesc, bdesc, idesc, acc_in);
                         }
                     }
@@ -571,11 +592,11 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
     }
 }
 
-template <int STAGES, int MP_MAX, typename T = __half>
+template <int STAGES, int MP_MAX, typename T = __half, int BK = 64>
 __global__ void __launch_bounds__(skinny_threads(STAGES, MP_MAX, false), 1)
     tg_gemm_f16_skinny(const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmA, const SkinnyParams p) {
-    skinny_body<STAGES, MP_MAX, T, false>(&tmB, &tmA, nullptr, p);
+    skinny_body<STAGES, MP_MAX, T, false, BK>(&tmB, &tmA, nullptr, p);
 }
 
 // C = epi(A · Bdeq) with B in MXFP4 (mxfp4.cuh), M ≤ 128, A fp16.
@@ -595,19 +616,21 @@ inline bool skinny_applies(int64_t M, int64_t N, int64_t K) {
     return M >= 1 && M <= 128;
 }
 
-inline void skinny_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* pl) {
+// Units of bk k (the fp16/bf16 kernel: SkinnyNarrow/Wide::kBK; MXFP4: 64).
+inline void skinny_plan_bk(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t bk,
+                           tg_plan_t* pl) {
     const int64_t Mp = (M + 15) / 16 * 16;
     const bool narrow = Mp <= 64;
     pl->kernel = TG_KERNEL_SKINNY;
     pl->bm = static_cast<int32_t>(Mp);
     pl->bn = 128;
-    pl->bk = 64;
+    pl->bk = bk;
     pl->stages = narrow ? SkinnyNarrow::kStages : SkinnyWide::kStages;
     pl->mma_m = 128;
     pl->mma_n = static_cast<int32_t>(Mp);
     pl->tiles_m = 1;
     pl->tiles_n = (N + 127) / 128;
-    pl->k_blocks = (K + 63) / 64;
+    pl->k_blocks = (K + bk - 1) / bk;
     pl->num_tiles = pl->tiles_n;
     const int64_t U = pl->tiles_n * pl->k_blocks;
     int64_t G = U / kSkMinUnitsPerCta;
@@ -628,9 +651,14 @@ inline void skinny_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_pla
     pl->cluster = 1;
 }
 
+inline void skinny_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* pl) {
+    const bool narrow = (M + 15) / 16 * 16 <= 64;
+    skinny_plan_bk(M, N, K, num_sms, narrow ? SkinnyNarrow::kBK : SkinnyWide::kBK, pl);
+}
+
 // The MXFP4 kernel: the same units and split, its own rings and 448 threads.
 inline void skinny_mx_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* pl) {
-    skinny_plan(M, N, K, num_sms, pl);
+    skinny_plan_bk(M, N, K, num_sms, 64, pl);
     const bool narrow = pl->bm <= 64;
     pl->stages = narrow ? SkinnyMxNarrow::kStages : SkinnyMxWide::kStages;
     pl->threads = narrow ? skinny_threads(SkinnyMxNarrow::kStages, 64, true)
@@ -655,11 +683,11 @@ inline cudaError_t skinny_mx_set_attributes() {
 
 template <typename T>
 inline cudaError_t skinny_set_attributes() {
-    cudaError_t e = cudaFuncSetAttribute(tg_gemm_f16_skinny<9, 64, T>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SkinnyNarrow::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(
+        tg_gemm_f16_skinny<SkinnyNarrow::kStages, 64, T, SkinnyNarrow::kBK>,
+        cudaFuncAttributeMaxDynamicSharedMemorySize, SkinnyNarrow::kSmemBytes);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(tg_gemm_f16_skinny<6, 128, T>,
+    return cudaFuncSetAttribute(tg_gemm_f16_skinny<SkinnyWide::kStages, 128, T, SkinnyWide::kBK>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 SkinnyWide::kSmemBytes);
 }
@@ -682,10 +710,13 @@ inline cudaError_t skinny_launch_kernel(const CUtensorMap& tmB, const CUtensorMa
     cfg.numAttrs = 1;
     if (prm.Mp <= 64) {
         cfg.dynamicSmemBytes = SkinnyNarrow::kSmemBytes;
-        return cudaLaunchKernelEx(&cfg, tg_gemm_f16_skinny<9, 64, T>, tmB, tmA, prm);
+        return cudaLaunchKernelEx(
+            &cfg, tg_gemm_f16_skinny<SkinnyNarrow::kStages, 64, T, SkinnyNarrow::kBK>, tmB, tmA,
+            prm);
     }
     cfg.dynamicSmemBytes = SkinnyWide::kSmemBytes;
-    return cudaLaunchKernelEx(&cfg, tg_gemm_f16_skinny<6, 128, T>, tmB, tmA, prm);
+    return cudaLaunchKernelEx(
+        &cfg, tg_gemm_f16_skinny<SkinnyWide::kStages, 128, T, SkinnyWide::kBK>, tmB, tmA, prm);
 }
 
 // Cooperative launch of the MXFP4 instantiation whose A slots fit prm.Mp.
@@ -791,7 +822,8 @@ inline tg_status_t skinny_launch(const void* A, const void* B, void* C, const tg
     CUtensorMap tmA, tmB;
     const CUtensorMapDataType dt = Elem16<T>::kFmt == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    if (!encode(&tmB, B, N, K, ldb * 2, 64, 64, dt) ||
+    // B: boxes of 64 columns × (the unit's k) rows; A: 64-k boxes of Mp rows
+    if (!encode(&tmB, B, N, K, ldb * 2, 64, static_cast<uint32_t>(pl.bk), dt) ||
         !encode(&tmA, A, K, M, lda * 2, 64, static_cast<uint32_t>(Mp), dt))
         return TG_ERR_LAUNCH;
 

@@ -1069,7 +1069,10 @@ extern "C" tg_status_t tg_gemm_f16_noalloc(const void* A, const void* B, void* C
 
     const int64_t Mp = pl.mma_n;
     CUtensorMap tmA, tmB;
-    if (!encode_2d(&tmB, B, N, K, ldb * 2, 64, 64, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) ||
+    // B boxes: 64 columns × the plan's k per unit (the kernel arms its
+    // barriers for that many rows)
+    if (!encode_2d(&tmB, B, N, K, ldb * 2, 64, static_cast<uint32_t>(pl.bk),
+                   CU_TENSOR_MAP_DATA_TYPE_FLOAT16) ||
         !encode_2d(&tmA, A, K, M, lda * 2, 64, static_cast<uint32_t>(Mp),
                    CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
         return TG_ERR_LAUNCH;
