@@ -335,6 +335,44 @@ void tg_debug_set_wait_timeout_ns(uint64_t ns);
 void tg_debug_inject(int32_t mode);
 
 /* ------------------------------------------------------------------------
+ * Host buffers in and out.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * tg_gemm_f16_host — C = epi(A·B) with A, B and C in host memory,
+ * asynchronous on `stream`.  The pages' GEMM (the tiled fp16 product with
+ * the ReLU epilogue: "TileLang：让GPU编程像Python一样简单的高性能计算新范式",
+ * the GEMM example) run end to end: the copies to and from the device are
+ * part of the call.
+ *
+ * A, B, C   HOST pointers, fp16, row-major, with row strides lda ≥ K,
+ *     ldb ≥ N, ldc ≥ N elements, 2-byte aligned (else TG_ERR_MISALIGNED).
+ *     Page-locked (pinned) memory lets the copies overlap the computation;
+ *     pageable memory works but each copy then waits for the host.
+ * M, N, K, epilogue, stream   as for tg_gemm_f16.
+ *
+ * The call uploads A, then walks N in blocks of columns (at most 8 blocks,
+ * each a multiple of 256 columns): for each block the library copies that
+ * block of B up on a copy stream of its own, runs the GEMM of the block on
+ * `stream`, and copies that block of C down on a second copy stream, ordered
+ * by events, so uploads, products and downloads of different blocks overlap.
+ * `stream` waits for the last download: once `stream` completes (e.g.
+ * cudaStreamSynchronize), C holds the result.  Work already enqueued on
+ * `stream` completes before the call's first copy starts.
+ * Ownership: the caller owns A, B and C and must keep them alive and
+ * unmodified (C unread) until `stream` completes.  The library owns device
+ * copies of A, B and C and the two copy streams, per (device, stream), grown
+ * on demand (growth waits for earlier calls on that stream) and kept until
+ * process exit.
+ * Errors: as tg_gemm_f16; TG_ERR_NO_MEMORY if the device copies cannot be
+ * allocated; TG_ERR_LAUNCH if a copy or launch cannot be enqueued.
+ */
+tg_status_t tg_gemm_f16_host(const void* A, const void* B, void* C,
+                             int64_t M, int64_t N, int64_t K,
+                             int64_t lda, int64_t ldb, int64_t ldc,
+                             int epilogue, void* stream);
+
+/* ------------------------------------------------------------------------
  * Entry point that allocates nothing.
  * ------------------------------------------------------------------------ */
 

@@ -87,8 +87,10 @@ GOOD = 1 << 20  # a 16-byte aligned fake address (never dereferenced on these pa
     ((0, 0, 0, 4, 0, 4, 8, 8, 8, 1), 0),                   # N == 0: no-op, nothing checked
     ((0, 0, GOOD, 4, 4, 0, 0, 0, 8, 0), None),             # K == 0: A/B/lda/ldb ignored
 ])
-def test_argument_checks_before_any_cuda_call(tg, args, want):
-    st = tg.tg_gemm_f16(*args, None)
+@pytest.mark.parametrize("entry", ["tg_gemm_f16", "tg_gemm_f16_host"])
+def test_argument_checks_before_any_cuda_call(tg, entry, args, want):
+    """The device entry point and the host-buffer one share these checks."""
+    st = getattr(tg, entry)(*args, None)
     if want is None:
         # valid arguments: on a machine without an sm_103 device the call
         # reaches the device check and stops there

@@ -41,6 +41,7 @@ EXPORTS = (
     "tg_gemm_f16", "tg_sync_status", "tg_status_string", "tg_version", "tg_plan_f16",
     "tg_tile_coord", "tg_ring_bytes", "tg_debug_set_wait_timeout_ns", "tg_debug_inject",
     "tg_gemm_f16_noalloc", "tg_gemm_bf16", "tg_gemm_ex", "tg_gemm_mxfp4", "tg_gemm_sp24",
+    "tg_gemm_f16_host",
 )
 
 #: bytes of the library's fixed scratch array used by tg_gemm_f16_noalloc
@@ -90,6 +91,8 @@ def _L():
     lib.tg_gemm_f16.restype = ctypes.c_int
     lib.tg_gemm_bf16.argtypes = lib.tg_gemm_f16.argtypes
     lib.tg_gemm_bf16.restype = ctypes.c_int
+    lib.tg_gemm_f16_host.argtypes = lib.tg_gemm_f16.argtypes
+    lib.tg_gemm_f16_host.restype = ctypes.c_int
     lib.tg_gemm_ex.argtypes = [ctypes.c_int32, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64,
                                ctypes.POINTER(tg_epilogue_ex_t), _vp]
     lib.tg_gemm_ex.restype = ctypes.c_int
@@ -142,6 +145,12 @@ def tg_gemm_bf16(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: 
                  epilogue: int, stream: int | None) -> int:
     """The bfloat16 entry point with integer device pointers; returns the status code."""
     return _L().tg_gemm_bf16(A, B, C, M, N, K, lda, ldb, ldc, epilogue, stream or None)
+
+
+def tg_gemm_f16_host(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+                     ldc: int, epilogue: int, stream: int | None) -> int:
+    """The C entry point with integer HOST pointers; returns the status code."""
+    return _L().tg_gemm_f16_host(A, B, C, M, N, K, lda, ldb, ldc, epilogue, stream or None)
 
 
 def tg_gemm_ex(in_dtype: int, A: int, B: int, C: int, M: int, N: int, K: int, lda: int,
@@ -412,23 +421,34 @@ def gemm_sp24(ac, e, b, relu: bool = False, out=None, stream=None, *, bias=None,
 
 
 def gemm_host(a, b, relu: bool = False, stream=None, device=None):
-    """End-to-end C = epi(a @ b) from host (CPU) float16 tensors.
-
-    Copies a and b to the device, runs tg_gemm_f16, copies C back into a
-    pinned host tensor and waits for it.  Inputs in pinned memory are copied
-    asynchronously.
+    """End-to-end C = epi(a @ b) from host (CPU) float16 tensors, through
+    tg_gemm_f16_host: the library uploads a and B and downloads C block by
+    block on its own copy streams, overlapped with the products.  Returns C
+    in a pinned host tensor once it is complete.  Pinned a and b let the
+    copies overlap; pageable ones work, without overlap.
     """
     import torch
+    for t, name in ((a, "a"), (b, "b")):
+        if t.device.type != "cpu" or t.dtype != torch.float16 or t.dim() != 2:
+            raise ValueError(f"{name} must be a 2-D float16 CPU tensor")
+        if t.stride(1) != 1:
+            raise ValueError(f"{name} must have unit column stride")
+    M, K = a.shape
+    if b.shape[0] != K:
+        raise ValueError(f"inner sizes differ: a is {tuple(a.shape)}, b is {tuple(b.shape)}")
+    N = b.shape[1]
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    hc = torch.empty((M, N), dtype=torch.float16, pin_memory=True)
     with torch.cuda.device(dev):
         s = stream if stream is not None else torch.cuda.current_stream(dev)
-        with torch.cuda.stream(s):
-            da = a.to(dev, non_blocking=True)
-            db = b.to(dev, non_blocking=True)
-            dc = gemm(da, db, relu=relu, stream=s)
-            hc = torch.empty(dc.shape, dtype=dc.dtype, pin_memory=True)
-            hc.copy_(dc, non_blocking=True)
-        s.synchronize()
+        st = tg_gemm_f16_host(a.data_ptr(), b.data_ptr(), hc.data_ptr(), M, N, K,
+                              max(a.stride(0), 1), max(b.stride(0), 1), max(N, 1),
+                              TG_EPI_RELU if relu else TG_EPI_NONE, s.cuda_stream)
+        if st != TG_OK:
+            raise TgemmError(st, "tg_gemm_f16_host")
+        st = tg_sync_status(s.cuda_stream)
+        if st != TG_OK:
+            raise TgemmError(st, "tg_sync_status")
     return hc
 
 

@@ -977,6 +977,145 @@ tg_status_t tg_sync_status(void* stream) {
 
 }  // extern "C"
 
+// ====================================================================== host buffers in and out
+//
+// tg_gemm_f16_host: device copies of A, B and C plus two copy streams per
+// (device, stream); see include/tgemm.h for the overlap scheme.
+
+namespace {
+
+constexpr int kHostMaxBlocks = 8;        // column blocks per call
+constexpr int64_t kHostMinBlockCols = 2048;
+
+struct HostPipeline {
+    void* dA = nullptr;
+    void* dB = nullptr;
+    void* dC = nullptr;
+    size_t bytes_a = 0, bytes_b = 0, bytes_c = 0;
+    cudaStream_t up = nullptr, down = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t uploaded[kHostMaxBlocks] = {};
+    cudaEvent_t computed[kHostMaxBlocks] = {};
+    bool ready = false;
+};
+
+std::mutex g_host_mutex;
+std::map<std::pair<int, cudaStream_t>, HostPipeline> g_host;
+
+// Grow one device copy to `need` bytes.  Earlier calls on this pipeline may
+// still read or write the old buffer: `stream` (which every call leaves
+// waiting for its last download) is synchronised first.
+tg_status_t host_buffer(void** p, size_t* have, size_t need, cudaStream_t stream) {
+    if (*have >= need) return TG_OK;
+    if (*p != nullptr) {
+        if (cudaStreamSynchronize(stream) != cudaSuccess || cudaFree(*p) != cudaSuccess) {
+            cudaGetLastError();
+            return TG_ERR_LAUNCH;
+        }
+        *p = nullptr;
+        *have = 0;
+    }
+    if (cudaMalloc(p, need) != cudaSuccess) {
+        cudaGetLastError();
+        *p = nullptr;
+        return TG_ERR_NO_MEMORY;
+    }
+    *have = need;
+    return TG_OK;
+}
+
+tg_status_t host_pipeline_init(HostPipeline& hp) {
+    if (hp.ready) return TG_OK;
+    bool ok = cudaStreamCreateWithFlags(&hp.up, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&hp.down, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < kHostMaxBlocks; ++i)
+        ok = cudaEventCreateWithFlags(&hp.uploaded[i], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&hp.computed[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        return TG_ERR_LAUNCH;
+    }
+    hp.ready = true;
+    return TG_OK;
+}
+
+}  // namespace
+
+extern "C" tg_status_t tg_gemm_f16_host(const void* A, const void* B, void* C, int64_t M,
+                                        int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                        int64_t ldc, int epilogue, void* stream) {
+    tg_status_t st = validate(A, B, C, M, N, K, lda, ldb, ldc, epilogue, false);
+    if (st != TG_OK || M == 0 || N == 0) return st;
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    st = current_device(&dev, &ds);
+    if (st != TG_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    std::lock_guard<std::mutex> lk(g_host_mutex);
+    HostPipeline& hp = g_host[std::make_pair(dev, s)];
+    if ((st = host_pipeline_init(hp)) != TG_OK) return st;
+    // Device copies: row strides rounded up to 8 elements (16-byte rows).
+    const int64_t Kp = round_up8(K), Np = round_up8(N);
+    if ((st = host_buffer(&hp.dA, &hp.bytes_a, static_cast<size_t>(M * Kp * 2) + 16, s)) != TG_OK ||
+        (st = host_buffer(&hp.dB, &hp.bytes_b, static_cast<size_t>(K * Np * 2) + 16, s)) != TG_OK ||
+        (st = host_buffer(&hp.dC, &hp.bytes_c, static_cast<size_t>(M * Np * 2) + 16, s)) != TG_OK)
+        return st;
+
+    // Column blocks: at most kHostMaxBlocks, each at least kHostMinBlockCols
+    // wide (a full wave of tiles) and a multiple of 256 columns.
+    int64_t blocks = (N + kHostMinBlockCols - 1) / kHostMinBlockCols;
+    if (blocks > kHostMaxBlocks) blocks = kHostMaxBlocks;
+    int64_t width = (N + blocks - 1) / blocks;
+    width = (width + 255) / 256 * 256;
+    blocks = (N + width - 1) / width;
+
+    const char* hA = static_cast<const char*>(A);
+    const char* hB = static_cast<const char*>(B);
+    char* hC = static_cast<char*>(C);
+    char* dA = static_cast<char*>(hp.dA);
+    char* dB = static_cast<char*>(hp.dB);
+    char* dC = static_cast<char*>(hp.dC);
+    const tg::EpilogueSpec ep = plain_epilogue(epilogue);
+    auto fail = [] {
+        cudaGetLastError();
+        return TG_ERR_LAUNCH;
+    };
+
+    // Everything already on `stream` (earlier calls' products included)
+    // comes before this call's uploads overwrite the device copies.
+    if (cudaEventRecord(hp.start, s) != cudaSuccess ||
+        cudaStreamWaitEvent(hp.up, hp.start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(hp.down, hp.start, 0) != cudaSuccess)
+        return fail();
+    if (K > 0 && cudaMemcpy2DAsync(dA, Kp * 2, hA, lda * 2, K * 2, M, cudaMemcpyHostToDevice,
+                                   hp.up) != cudaSuccess)
+        return fail();
+    for (int64_t j = 0; j < blocks; ++j) {
+        const int64_t c0 = j * width;
+        const int64_t w = N - c0 < width ? N - c0 : width;
+        if (K > 0 && cudaMemcpy2DAsync(dB + c0 * 2, Np * 2, hB + c0 * 2, ldb * 2, w * 2, K,
+                                       cudaMemcpyHostToDevice, hp.up) != cudaSuccess)
+            return fail();
+        if (cudaEventRecord(hp.uploaded[j], hp.up) != cudaSuccess ||
+            cudaStreamWaitEvent(s, hp.uploaded[j], 0) != cudaSuccess)
+            return fail();
+        st = gemm_impl<__half>(dA, dB + c0 * 2, dC + c0 * 2, M, w, K, Kp, Np, Np, ep, s);
+        if (st != TG_OK) return st;
+        if (cudaEventRecord(hp.computed[j], s) != cudaSuccess ||
+            cudaStreamWaitEvent(hp.down, hp.computed[j], 0) != cudaSuccess ||
+            cudaMemcpy2DAsync(hC + c0 * 2, ldc * 2, dC + c0 * 2, Np * 2, w * 2, M,
+                              cudaMemcpyDeviceToHost, hp.down) != cudaSuccess)
+            return fail();
+    }
+    if (cudaEventRecord(hp.done, hp.down) != cudaSuccess ||
+        cudaStreamWaitEvent(s, hp.done, 0) != cudaSuccess)
+        return fail();
+    return TG_OK;
+}
+
 // ====================================================================== no-allocation variant
 //
 // tg_gemm_f16_noalloc runs the skinny split-K kernel with its scratch (fp32
