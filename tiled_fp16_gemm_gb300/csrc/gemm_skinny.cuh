@@ -80,36 +80,55 @@ struct SkinnyCfg {
 using SkinnyNarrow = SkinnyCfg<9, 64, 64>;
 using SkinnyWide = SkinnyCfg<6, 128, 64>;
 // MXFP4 B (M ≤ 128 weight streaming).  Per unit, one 128 n × 64 k tile of
-// packed codes (128 rows × 32 bytes, TMA 32-byte swizzle), its scales (2
-// rows × 128 bytes) and the A tile land in a deep raw ring.  Converter
+// packed codes (128 rows × 32 bytes, TMA 32-byte swizzle) and its scales (2
+// rows × 128 bytes) land in a deep raw ring: the codes are the HBM stream,
+// and keeping ~130 KB of them in flight per SM takes about 30 stages.  The A
+// tile (from L2, re-read by every CTA) has a shallow ring of its own with its
+// own producer thread; were it in the raw ring it would take most of each
+// stage (8 KB against 4.25 KB) and cap the codes in flight.  The A ring is
+// indexed like the tensor-memory operand stages (8 of each), so one MMA
+// commit per unit frees both, and the converters wait for a unit's A tile
+// before they report its operand decoded: the MMA thread, the pipeline's
+// slowest member (four MMA issues per unit), waits once and commits once per
+// unit.  Converter
 // threads each own one column n of the tile: they decode its 64 k into fp16
 // and write them with tcgen05.st straight into the tensor memory holding the
 // MMA's A operand (the weight tile is the A operand of the swapped product),
 // so decoded weights never pass through shared memory.  Tensor memory holds
 // the two accumulators (256 columns) and kStages operand stages of 32
 // columns.  Two converter groups of four warps (one per tensor-memory lane
-// quarter) take alternate units.  A raw stage is free once its group has read
-// it and the MMAs that read its A tile have completed.
+// quarter) take alternate units.  A raw stage is free once its group has
+// decoded it; an operand stage and its A stage once the MMAs that read them
+// have completed.
 constexpr uint32_t kMxRawBytes = 128 * 32;
 constexpr uint32_t kMxScaleBytes = 2 * 128;
 constexpr int kMxConvWarps = 8;
 constexpr int kMxGroups = kMxConvWarps / 4;
 constexpr uint32_t kMxTmemCols = 512;
 constexpr uint32_t kMxOpCol0 = 256;  // first tensor-memory column of the operand stages
-// Raw ring depth for A slots of MP_MAX rows (as deep as shared memory allows).
-__host__ __device__ constexpr int mx_raw_stages(int mp_max) { return mp_max <= 64 ? 16 : 8; }
+// Raw ring depth (codes + scales; as deep as shared memory allows beside 8
+// A stages of MP_MAX rows).
+__host__ __device__ constexpr int mx_raw_stages(int mp_max) { return mp_max <= 64 ? 32 : 20; }
+constexpr uint32_t kMxBarBytes = 1024;
 template <int STAGES, int MP_MAX>
 struct SkinnyMxCfg {
-    static constexpr int kStages = STAGES;  // tensor-memory operand stages
+    static constexpr int kStages = STAGES;  // tensor-memory operand stages = A stages
     static constexpr int kRawStages = mx_raw_stages(MP_MAX);
+    static constexpr int kAStages = STAGES;
     static constexpr uint32_t kASlot = MP_MAX * 64 * 2;
     static constexpr uint32_t kStageBytes = 0;  // no shared-memory operand ring
-    static constexpr uint32_t kRawStageBytes = kASlot + kMxRawBytes + kMxScaleBytes;
-    static constexpr uint32_t kSmemBytes = 1024 + kRawStages * kRawStageBytes + 512;
+    static constexpr uint32_t kRawStageBytes = kMxRawBytes + kMxScaleBytes;
+    static constexpr uint32_t kSmemBytes =
+        1024 + kRawStages * kRawStageBytes + kAStages * kASlot + kMxBarBytes;
     static_assert(kMxOpCol0 + 32 * STAGES <= kMxTmemCols, "operand stages exceed tensor memory");
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeded");
+    // barriers: full/empty/dec per operand stage, rfull/rempty per raw stage,
+    // afull per A stage, two tfull, two tempty, drain, TMEM slot + flag
+    static_assert(8 * (3 * STAGES + 2 * kRawStages + kAStages) + 48 <= kMxBarBytes,
+                  "barrier area too small");
 };
-using SkinnyMxNarrow = SkinnyMxCfg<4, 64>;
-using SkinnyMxWide = SkinnyMxCfg<4, 128>;
+using SkinnyMxNarrow = SkinnyMxCfg<8, 64>;
+using SkinnyMxWide = SkinnyMxCfg<8, 128>;
 constexpr unsigned int kRoleConvert = 16u;
 
 // Load issue is split over several producer threads (one per warp): one
@@ -122,9 +141,10 @@ __host__ __device__ constexpr int skinny_producers(int ring) {
     return ring % 4 == 0 ? 4 : (ring % 3 == 0 ? 3 : (ring % 2 == 0 ? 2 : 1));
 }
 // Threads of a skinny kernel: producer 0, MMA, 4 epilogue warps, the
-// converter warps (MXFP4), then producers 1 .. count - 1.
+// converter warps (MXFP4), producers 1 .. count - 1, then (MXFP4) the
+// producer of the A ring.
 __host__ __device__ constexpr int skinny_threads(int stages, int mp_max, bool qb) {
-    return 32 * (6 + (qb ? kMxConvWarps : 0) +
+    return 32 * (6 + (qb ? kMxConvWarps + 1 : 0) +
                  skinny_producers(qb ? mx_raw_stages(mp_max) : stages) - 1);
 }
 constexpr uint32_t kSkTmemCols = 256;        // two accumulators of up to 128 columns
@@ -184,7 +204,8 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
     uint8_t* const base_ptr = smem_raw + (base - raw);
 
     constexpr int kRaw = QB ? mx_raw_stages(MP_MAX) : 0;  // raw ring depth (QB)
-    constexpr int kARing = QB ? kRaw : kSkStages;         // A slots ride with B or raw
+    constexpr int kAS = QB ? kSkStages : 0;               // A ring depth (QB): the operand stages
+    constexpr int kARing = QB ? kAS : kSkStages;          // A slots: own ring, or with B
     constexpr int kBRing = QB ? 0 : kSkStages;            // B^T tiles in shared memory
     const uint32_t sB = base;                             // [kBRing] B^T tiles
     const uint32_t sA = sB + kBRing * kSkBBytes;          // [kARing] A tiles
@@ -196,8 +217,9 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
     const uint32_t bar_empty = sBar + 8 * kSkStages;      // [stages] MMA done with the stage
     const uint32_t bar_dec = sBar + 16 * kSkStages;       // QB: [stages] B^T decoded
     const uint32_t bar_rfull = bar_dec + (QB ? 8 * kSkStages : 0);  // QB: [raw] landed
-    const uint32_t bar_rempty = bar_rfull + 8 * kRaw;     // QB: [raw] read and consumed
-    const uint32_t bar_tfull = bar_rempty + 8 * kRaw;
+    const uint32_t bar_rempty = bar_rfull + 8 * kRaw;     // QB: [raw] decoded
+    const uint32_t bar_afull = bar_rempty + 8 * kRaw;     // QB: [A stages] landed
+    const uint32_t bar_tfull = bar_afull + 8 * kAS;
     const uint32_t bar_tempty = bar_tfull + 16;
     const uint32_t bar_drain = bar_tempty + 16;
     const uint32_t slot_tmem = bar_drain + 8;
@@ -222,8 +244,9 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
         if (QB) {
             for (int r = 0; r < kRaw; ++r) {
                 mbar_init(bar_rfull + 8 * r, 1);
-                mbar_init(bar_rempty + 8 * r, 5);  // the group's four warps + the MMA commit
+                mbar_init(bar_rempty + 8 * r, 4);  // the group's four warps
             }
+            for (int a = 0; a < kAS; ++a) mbar_init(bar_afull + 8 * a, 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar_tfull + 8 * a, 1);
@@ -259,7 +282,10 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
     constexpr int kProd = skinny_producers(kRing);
     static_assert(kRing % kProd == 0, "each ring stage must belong to one producer thread");
     constexpr int kProdWarp1 = 6 + (QB ? kMxConvWarps : 0);  // warp of producer 1
-    const int prod = warp == 0 ? 0 : (warp >= kProdWarp1 ? warp - kProdWarp1 + 1 : -1);
+    constexpr int kAProdWarp = QB ? kProdWarp1 + kProd - 1 : -1;  // QB: A ring producer
+    const int prod = warp == 0 ? 0
+                     : (warp >= kProdWarp1 && warp < kProdWarp1 + kProd - 1 ? warp - kProdWarp1 + 1
+                                                                             : -1);
     if (prod >= 0) {
         // ------------------------------------------------------------ producers
         if (lane == 0) {
@@ -282,12 +308,11 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                 }
                 const uint32_t full = ring_full + 8 * stage;
                 if constexpr (QB) {
-                    mbar_arrive_expect_tx(full, kMxRawBytes + kMxScaleBytes + a_bytes);
+                    mbar_arrive_expect_tx(full, kMxRawBytes + kMxScaleBytes);
                     tma_load_2d_hint(sRaw + stage * kMxRawBytes, tmB, full, kb * 32, t * 128,
                                      stream);
                     tma_load_2d_hint(sScl + stage * kMxScaleBytes, tmS, full, t * 128, kb * 2,
                                      stream);
-                    tma_load_2d_hint(sA + stage * kSkASlot, tmA, full, kb * BK, 0, keep);
                 } else {
                     mbar_arrive_expect_tx(full, kSkBBytes + (BK / 64) * a_bytes);
                     const uint32_t b0 = sB + stage * kSkBBytes;
@@ -312,6 +337,33 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                                    nullptr))
                         atomicOr(&g_wait_timeout_flags, kRoleDrain);
         }
+    } else if (warp == kAProdWarp) {
+        // ------------------------------------------------------------ A ring producer (QB)
+        if constexpr (QB) if (lane == 0) {
+            const uint64_t keep = policy_evict_last();  // A: reread by every CTA
+            uint32_t issued_mask = 0, issued_parity = 0;
+            int32_t kb = static_cast<int32_t>(u_begin % KB);
+            for (int64_t i = 0; u_begin + i < u_end; ++i) {
+                const int stage = static_cast<int>(i % kAS);
+                const uint32_t phase = static_cast<uint32_t>((i / kAS) & 1);
+                // the MMAs of the unit kAS earlier (same operand stage) are done
+                if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.timeout_ns, abort_flag)) {
+                    fail(kRoleProducer);
+                    break;
+                }
+                const uint32_t full = bar_afull + 8 * stage;
+                mbar_arrive_expect_tx(full, a_bytes);
+                tma_load_2d_hint(sA + stage * kSkASlot, tmA, full, kb * BK, 0, keep);
+                issued_mask |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++kb == KB) kb = 0;
+            }
+            for (int a = 0; a < kAS; ++a)
+                if (issued_mask & (1u << a))
+                    if (!mbar_wait(bar_afull + 8 * a, (issued_parity >> a) & 1u, p.timeout_ns,
+                                   nullptr))
+                        atomicOr(&g_wait_timeout_flags, kRoleDrain);
+        }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -319,8 +371,8 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
             // operand = decoded weights in tensor memory (K-major).
             const uint32_t idesc =
                 idesc_f16_f32(128, p.Mp, /*a_mn=*/!QB, /*b_mn=*/false, Elem16<T>::kFmt);
-            int stage = 0, rstage = 0;
-            uint32_t phase = 0, rphase = 0;
+            int stage = 0;
+            uint32_t phase = 0;
             int it = 0;
             bool ok = true;
             for (int64_t u = u_begin; ok && u < u_end; ++it) {
@@ -335,10 +387,10 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 128);
                 for (int64_t v = u; v < seg_end; ++v) {
-                    // QB: A (raw ring) landed and B^T (operand ring) decoded
+                    // QB: B^T decoded into the operand stage, and (the
+                    // converters waited for it) that stage's A tile landed
                     const bool got =
-                        QB ? mbar_wait(bar_rfull + 8 * rstage, rphase, p.timeout_ns, abort_flag) &&
-                                 mbar_wait(bar_dec + 8 * stage, phase, p.timeout_ns, abort_flag)
+                        QB ? mbar_wait(bar_dec + 8 * stage, phase, p.timeout_ns, abort_flag)
                            : mbar_wait(bar_full + 8 * stage, phase, p.timeout_ns, abort_flag);
                     if (!got) {
                         fail(kRoleMma);
@@ -347,7 +399,7 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                     }
                     tc_fence_after_sync();
                     const uint32_t b0 = sB + stage * kSkBBytes;
-                    const uint32_t a0 = sA + (QB ? rstage : stage) * kSkASlot;
+                    const uint32_t a0 = sA + stage * kSkASlot;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
                         // A tile: 64-k boxes kABox apart, 32 B per 16 k inside one
@@ -367,17 +419,10 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                             mma_f16_ss(d_tmem, adesc, bdesc, idesc, acc_in);
                         }
                     }
-                    mma_commit(bar_empty + 8 * stage);
+                    mma_commit(bar_empty + 8 * stage);  // QB: the operand and A stages
                     if (++stage == kSkStages) {
                         stage = 0;
                         phase ^= 1u;
-                    }
-                    if (QB) {
-                        mma_commit(bar_rempty + 8 * rstage);  // its A tile is consumed
-                        if (++rstage == kRaw) {
-                            rstage = 0;
-                            rphase ^= 1u;
-                        }
                     }
                 }
                 if (!ok) break;
@@ -530,6 +575,9 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                 if (ok)
                     ok = mbar_wait(bar_rfull + 8 * rstage, rphase, p.timeout_ns, abort_flag) ? 1
                                                                                              : 0;
+                // the unit's A tile: the MMA thread waits only for this warp's report
+                if (ok)
+                    ok = mbar_wait(bar_afull + 8 * stage, phase, p.timeout_ns, abort_flag) ? 1 : 0;
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
@@ -664,11 +712,11 @@ inline void skinny_mx_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_
     pl->threads = narrow ? skinny_threads(SkinnyMxNarrow::kStages, 64, true)
                          : skinny_threads(SkinnyMxWide::kStages, 128, true);
     pl->smem_bytes = narrow ? SkinnyMxNarrow::kSmemBytes : SkinnyMxWide::kSmemBytes;
-    pl->ring_bytes = narrow ? int64_t{SkinnyMxNarrow::kStages} * SkinnyMxNarrow::kStageBytes +
-                                  int64_t{SkinnyMxNarrow::kRawStages} *
-                                      SkinnyMxNarrow::kRawStageBytes
-                            : int64_t{SkinnyMxWide::kStages} * SkinnyMxWide::kStageBytes +
-                                  int64_t{SkinnyMxWide::kRawStages} * SkinnyMxWide::kRawStageBytes;
+    pl->ring_bytes =
+        narrow ? int64_t{SkinnyMxNarrow::kRawStages} * SkinnyMxNarrow::kRawStageBytes +
+                     int64_t{SkinnyMxNarrow::kAStages} * SkinnyMxNarrow::kASlot
+               : int64_t{SkinnyMxWide::kRawStages} * SkinnyMxWide::kRawStageBytes +
+                     int64_t{SkinnyMxWide::kAStages} * SkinnyMxWide::kASlot;
 }
 
 inline cudaError_t skinny_mx_set_attributes() {
