@@ -79,10 +79,13 @@ struct SkinnyCfg {
 };
 using SkinnyNarrow = SkinnyCfg<9, 64, 64>;
 using SkinnyWide = SkinnyCfg<6, 128, 64>;
-// MXFP4 B (M ≤ 128 weight streaming).  Per unit, one 128 n × 64 k tile of
-// packed codes (128 rows × 32 bytes, TMA 32-byte swizzle) and its scales (2
-// rows × 128 bytes) land in a deep raw ring: the codes are the HBM stream,
-// and keeping ~130 KB of them in flight per SM takes about 30 stages.  The A
+// MXFP4 B (M ≤ 128 weight streaming).  Units of 128 k: per unit, two 128 n ×
+// 64 k tiles of packed codes (128 rows × 32 bytes each, TMA 32-byte swizzle)
+// and their scales (4 rows × 128 bytes) land in a deep raw ring: the codes
+// are the HBM stream, and ~130 KB of them in flight per SM takes 16 stages.
+// 128 k per unit spreads the MMA thread's per-unit barrier wait, fence and
+// commit over 8 MMAs: that thread sets the pace (about 820 cycles per 64-k
+// unit of four MMAs, measured with clock stamps).  The A
 // tile (from L2, re-read by every CTA) has a shallow ring of its own with its
 // own producer thread; were it in the raw ring it would take most of each
 // stage (8 KB against 4.25 KB) and cap the codes in flight.  The A ring is
@@ -100,35 +103,39 @@ using SkinnyWide = SkinnyCfg<6, 128, 64>;
 // quarter) take alternate units.  A raw stage is free once its group has
 // decoded it; an operand stage and its A stage once the MMAs that read them
 // have completed.
-constexpr uint32_t kMxRawBytes = 128 * 32;
-constexpr uint32_t kMxScaleBytes = 2 * 128;
+constexpr int kMxBK = 128;                       // k per MXFP4 unit
+constexpr uint32_t kMxCodeBox = 128 * 32;        // one 64-k tile of codes
+constexpr uint32_t kMxRawBytes = (kMxBK / 64) * kMxCodeBox;
+constexpr uint32_t kMxScaleBytes = (kMxBK / 32) * 128;
+constexpr uint32_t kMxOpCols = kMxBK / 2;        // tensor-memory columns per operand stage
 constexpr int kMxConvWarps = 8;
 constexpr int kMxGroups = kMxConvWarps / 4;
 constexpr uint32_t kMxTmemCols = 512;
 constexpr uint32_t kMxOpCol0 = 256;  // first tensor-memory column of the operand stages
 // Raw ring depth (codes + scales; as deep as shared memory allows beside 8
 // A stages of MP_MAX rows).
-__host__ __device__ constexpr int mx_raw_stages(int mp_max) { return mp_max <= 64 ? 32 : 20; }
+__host__ __device__ constexpr int mx_raw_stages(int mp_max) { return mp_max <= 64 ? 16 : 8; }
 constexpr uint32_t kMxBarBytes = 1024;
 template <int STAGES, int MP_MAX>
 struct SkinnyMxCfg {
     static constexpr int kStages = STAGES;  // tensor-memory operand stages = A stages
     static constexpr int kRawStages = mx_raw_stages(MP_MAX);
     static constexpr int kAStages = STAGES;
-    static constexpr uint32_t kASlot = MP_MAX * 64 * 2;
+    static constexpr uint32_t kASlot = MP_MAX * kMxBK * 2;
     static constexpr uint32_t kStageBytes = 0;  // no shared-memory operand ring
     static constexpr uint32_t kRawStageBytes = kMxRawBytes + kMxScaleBytes;
     static constexpr uint32_t kSmemBytes =
         1024 + kRawStages * kRawStageBytes + kAStages * kASlot + kMxBarBytes;
-    static_assert(kMxOpCol0 + 32 * STAGES <= kMxTmemCols, "operand stages exceed tensor memory");
+    static_assert(kMxOpCol0 + kMxOpCols * STAGES <= kMxTmemCols,
+                  "operand stages exceed tensor memory");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeded");
     // barriers: full/empty/dec per operand stage, rfull/rempty per raw stage,
     // afull per A stage, two tfull, two tempty, drain, TMEM slot + flag
     static_assert(8 * (3 * STAGES + 2 * kRawStages + kAStages) + 48 <= kMxBarBytes,
                   "barrier area too small");
 };
-using SkinnyMxNarrow = SkinnyMxCfg<8, 64>;
-using SkinnyMxWide = SkinnyMxCfg<8, 128>;
+using SkinnyMxNarrow = SkinnyMxCfg<4, 64>;
+using SkinnyMxWide = SkinnyMxCfg<4, 128>;
 constexpr unsigned int kRoleConvert = 16u;
 
 // Load issue is split over several producer threads (one per warp): one
@@ -193,7 +200,7 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
 template <int STAGES, int MP_MAX, typename T, bool QB, int BK = 64>
 __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtensorMap* tmA,
                                             const CUtensorMap* tmS, const SkinnyParams& p) {
-    static_assert(BK % 64 == 0 && (!QB || BK == 64), "MXFP4 units are 64 k");
+    static_assert(BK % 64 == 0 && (!QB || BK == kMxBK), "MXFP4 units are kMxBK");
     constexpr int kSkStages = STAGES;
     constexpr uint32_t kSkBBytes = skinny_b_bytes(BK);
     constexpr uint32_t kABox = MP_MAX * 64 * 2;   // one 64-k box of the A tile (≤ MP_MAX rows)
@@ -309,10 +316,12 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                 const uint32_t full = ring_full + 8 * stage;
                 if constexpr (QB) {
                     mbar_arrive_expect_tx(full, kMxRawBytes + kMxScaleBytes);
-                    tma_load_2d_hint(sRaw + stage * kMxRawBytes, tmB, full, kb * 32, t * 128,
-                                     stream);
-                    tma_load_2d_hint(sScl + stage * kMxScaleBytes, tmS, full, t * 128, kb * 2,
-                                     stream);
+#pragma unroll
+                    for (int h = 0; h < BK / 64; ++h)  // codes: BK / 2 bytes of k per column
+                        tma_load_2d_hint(sRaw + stage * kMxRawBytes + kMxCodeBox * h, tmB, full,
+                                         kb * (BK / 2) + 32 * h, t * 128, stream);
+                    tma_load_2d_hint(sScl + stage * kMxScaleBytes, tmS, full, t * 128,
+                                     kb * (BK / 32), stream);
                 } else {
                     mbar_arrive_expect_tx(full, kSkBBytes + (BK / 64) * a_bytes);
                     const uint32_t b0 = sB + stage * kSkBBytes;
@@ -352,8 +361,11 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                     break;
                 }
                 const uint32_t full = bar_afull + 8 * stage;
-                mbar_arrive_expect_tx(full, a_bytes);
-                tma_load_2d_hint(sA + stage * kSkASlot, tmA, full, kb * BK, 0, keep);
+                mbar_arrive_expect_tx(full, (BK / 64) * a_bytes);
+#pragma unroll
+                for (int h = 0; h < BK / 64; ++h)
+                    tma_load_2d_hint(sA + stage * kSkASlot + kABox * h, tmA, full,
+                                     kb * BK + 64 * h, 0, keep);
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                 if (++kb == KB) kb = 0;
@@ -408,8 +420,9 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                         const uint32_t acc_in = (v != u || k != 0) ? 1u : 0u;
                         if constexpr (QB) {
                             // 16 k = 8 columns of the operand stage
-                            const uint32_t a_tmem = tmem_base + kMxOpCol0 +
-                                                    static_cast<uint32_t>(32 * stage + 8 * k);
+                            const uint32_t a_tmem =
+                                tmem_base + kMxOpCol0 +
+                                static_cast<uint32_t>(kMxOpCols * stage + 8 * k);
                             mx_mma_f16_ts(d_tmem, a_tmem, bdesc, idesc, acc_in);
                         } else {
                             // B^T: 16 k rows (2 KB) per step; the two 64-column
@@ -585,42 +598,48 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                 break;
             }
             tc_fence_after_sync();  // the MMAs that read this operand stage have completed
-            const uint32_t row = sRaw + static_cast<uint32_t>(rstage) * kMxRawBytes + 32u * n_local;
-            const uint4 c0 = mx_ld_shared_v4(row + (swz32 << 4));
-            const uint4 c1 = mx_ld_shared_v4(row + ((swz32 ^ 1u) << 4));
-            const uint32_t scl = sScl + static_cast<uint32_t>(rstage) * kMxScaleBytes + n_local;
-            const uint32_t X0 = mx_ld_shared_u8(scl);
-            const uint32_t X1 = mx_ld_shared_u8(scl + 128u);
-            const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-            uint32_t d[32];
-            if (mx_fast_scale(X0) && mx_fast_scale(X1)) {
-                const uint32_t f0 = mx_factor_bits(X0) * 0x10001u;  // both halves
-                const uint32_t f1 = mx_factor_bits(X1) * 0x10001u;
+#pragma unroll 1
+            for (int h = 0; h < BK / 64; ++h) {  // the unit's 64-k halves
+                const uint32_t row = sRaw + static_cast<uint32_t>(rstage) * kMxRawBytes +
+                                     kMxCodeBox * static_cast<uint32_t>(h) + 32u * n_local;
+                const uint4 c0 = mx_ld_shared_v4(row + (swz32 << 4));
+                const uint4 c1 = mx_ld_shared_v4(row + ((swz32 ^ 1u) << 4));
+                const uint32_t scl = sScl + static_cast<uint32_t>(rstage) * kMxScaleBytes +
+                                     256u * static_cast<uint32_t>(h) + n_local;
+                const uint32_t X0 = mx_ld_shared_u8(scl);
+                const uint32_t X1 = mx_ld_shared_u8(scl + 128u);
+                const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                uint32_t d[32];
+                if (mx_fast_scale(X0) && mx_fast_scale(X1)) {
+                    const uint32_t f0 = mx_factor_bits(X0) * 0x10001u;  // both halves
+                    const uint32_t f1 = mx_factor_bits(X1) * 0x10001u;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t f = j < 4 ? f0 : f1;  // words 0..3: k 0..31
-                    const uint32_t fj[4] = {f, f, f, f};
-                    const uint4 o = mx_decode8_fast(w[j], fj);
-                    d[4 * j] = o.x;
-                    d[4 * j + 1] = o.y;
-                    d[4 * j + 2] = o.z;
-                    d[4 * j + 3] = o.w;
-                }
-            } else {
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t f = j < 4 ? f0 : f1;  // words 0..3: k 0..31
+                        const uint32_t fj[4] = {f, f, f, f};
+                        const uint4 o = mx_decode8_fast(w[j], fj);
+                        d[4 * j] = o.x;
+                        d[4 * j + 1] = o.y;
+                        d[4 * j + 2] = o.z;
+                        d[4 * j + 3] = o.w;
+                    }
+                } else {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t xb = j < 4 ? X0 : X1;
-                    const uint32_t x[8] = {xb, xb, xb, xb, xb, xb, xb, xb};
-                    const uint4 o = mx_decode8_exact(w[j], x);
-                    d[4 * j] = o.x;
-                    d[4 * j + 1] = o.y;
-                    d[4 * j + 2] = o.z;
-                    d[4 * j + 3] = o.w;
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t xb = j < 4 ? X0 : X1;
+                        const uint32_t x[8] = {xb, xb, xb, xb, xb, xb, xb, xb};
+                        const uint4 o = mx_decode8_exact(w[j], x);
+                        d[4 * j] = o.x;
+                        d[4 * j + 1] = o.y;
+                        d[4 * j + 2] = o.z;
+                        d[4 * j + 3] = o.w;
+                    }
                 }
+                __syncwarp();
+                mx_tmem_st_x32(tmem_base + lane_addr + kMxOpCol0 +
+                                   static_cast<uint32_t>(kMxOpCols * stage + 32 * h),
+                               d);
             }
-            __syncwarp();
-            mx_tmem_st_x32(tmem_base + lane_addr + kMxOpCol0 + static_cast<uint32_t>(32 * stage),
-                           d);
             mx_tmem_wait_st();
             tc_fence_before_sync();
             __syncwarp();
@@ -653,7 +672,7 @@ __global__ void __launch_bounds__(skinny_threads(STAGES, MP_MAX, true), 1)
     tg_gemm_mxfp4_skinny(const __grid_constant__ CUtensorMap tmBq,
                          const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmS, const SkinnyParams p) {
-    skinny_body<STAGES, MP_MAX, __half, true>(&tmBq, &tmA, &tmS, p);
+    skinny_body<STAGES, MP_MAX, __half, true, kMxBK>(&tmBq, &tmA, &tmS, p);
 }
 
 // ------------------------------------------------------------------ host side
@@ -664,7 +683,7 @@ inline bool skinny_applies(int64_t M, int64_t N, int64_t K) {
     return M >= 1 && M <= 128;
 }
 
-// Units of bk k (the fp16/bf16 kernel: SkinnyNarrow/Wide::kBK; MXFP4: 64).
+// Units of bk k (the fp16/bf16 kernel: SkinnyNarrow/Wide::kBK; MXFP4: kMxBK).
 inline void skinny_plan_bk(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t bk,
                            tg_plan_t* pl) {
     const int64_t Mp = (M + 15) / 16 * 16;
@@ -706,7 +725,7 @@ inline void skinny_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_pla
 
 // The MXFP4 kernel: the same units and split, its own rings and 448 threads.
 inline void skinny_mx_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* pl) {
-    skinny_plan_bk(M, N, K, num_sms, 64, pl);
+    skinny_plan_bk(M, N, K, num_sms, kMxBK, pl);
     const bool narrow = pl->bm <= 64;
     pl->stages = narrow ? SkinnyMxNarrow::kStages : SkinnyMxWide::kStages;
     pl->threads = narrow ? skinny_threads(SkinnyMxNarrow::kStages, 64, true)
@@ -916,7 +935,7 @@ inline tg_status_t skinny_mx_launch(const void* A, const void* Bq, const void* S
     CUtensorMap tmBq, tmA, tmS;
     if (!encode(&tmBq, Bq, static_cast<uint64_t>((K + 1) / 2), N, ldbq, 32, 128,
                 CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_32B) ||
-        !encode(&tmS, S, N, (K + 31) / 32, lds, 128, 2, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+        !encode(&tmS, S, N, (K + 31) / 32, lds, 128, kMxBK / 32, CU_TENSOR_MAP_DATA_TYPE_UINT8,
                 CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode(&tmA, A, K, M, lda * 2, 64, static_cast<uint32_t>(Mp),
                 CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CU_TENSOR_MAP_SWIZZLE_128B))
