@@ -9,7 +9,11 @@ GB/s.  Prints one JSON line (rank 0).
 One step = one tg_gemm_f16 launch over one batch of synthetic input (the whole
 hot path: tensor maps, persistent tile schedule, TMA ring, tcgen05 MMA into
 TMEM, fused ReLU + fp16 epilogue with TMA stores).  Inputs are larger than L2,
-so no flush is needed between steps.  N > 1 runs N independent replicas (one
+so no flush is needed between steps.  Every leg times its launches back to
+back between two CUDA events on the launching stream (no event between
+launches) and divides by their number; 20 further launches, each between its
+own events, give the min / median of an isolated launch as context.  N > 1
+runs N independent replicas (one
 per GPU, no collective on the data path); value = work of all ranks ÷ the
 slowest rank's time.
 
@@ -191,28 +195,40 @@ def barrier(world: int, device=None):
 
 # ------------------------------------------------------------------ timing
 
+PER_LAUNCH_SAMPLES = 20
+
+
 def time_launches(launch, stream, steps: int, world: int, device):
-    """Run `launch` steps times on `stream`; returns (total_ms, per_launch_ms list)."""
+    """Time `steps` back-to-back launches on `stream` between two CUDA events,
+    with no event between launches: consecutive launches overlap their
+    start-up with the previous launch's tail, as in any stream of kernels.
+    Returns (total_ms, mean_ms = total_ms / steps, per_ms, wall0, wall1).
+    per_ms holds PER_LAUNCH_SAMPLES further launches, each bracketed by its
+    own events; those events serialise the launches, so per_ms is context
+    (min / median of an isolated launch), not the throughput."""
     import torch
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier(world, device)
     torch.cuda.synchronize()
     wall0 = time.time()
     t_begin.record(stream)
-    for i in range(steps):
-        starts[i].record(stream)
+    for _ in range(steps):
         launch()
-        ends[i].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world, device)
     wall1 = time.time()
     total = t_begin.elapsed_time(t_end)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(PER_LAUNCH_SAMPLES)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(PER_LAUNCH_SAMPLES)]
+    for i in range(PER_LAUNCH_SAMPLES):
+        starts[i].record(stream)
+        launch()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
     per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    return total, per, wall0, wall1
+    return total, total / steps, per, wall0, wall1
 
 
 def cpu_oracle_rate(A, B, w, seconds: float):
@@ -309,7 +325,7 @@ def run_ours(args, w, rank, world, local_rank):
 
     clocks = ClockSampler(local_rank)
     clocks.start()
-    total_ms, per, wall0, wall1 = time_launches(launch, stream, args.steps, world, device)
+    total_ms, _, per, wall0, wall1 = time_launches(launch, stream, args.steps, world, device)
     clk = clocks.stop(wall0, wall1)
     tg.sync_status(stream)
     total_ms = max_over_ranks(total_ms, world, device)
@@ -317,7 +333,7 @@ def run_ours(args, w, rank, world, local_rank):
     flops = float(w.flops)
     ms_step = total_ms / args.steps
     value = world * flops * args.steps / (total_ms / 1e3) / 1e12
-    kernel_ms = statistics.mean(per)
+    kernel_ms = ms_step
     achieved = flops / (kernel_ms / 1e3) / 1e12
     if plan.kernel == tg.TG_KERNEL_PERSISTENT:
         if plan.cluster == 2:
@@ -337,8 +353,9 @@ def run_ours(args, w, rank, world, local_rank):
         roof = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                 "frac": gbs / hbm_peak, "peak_source": f"{peak_src} copy bandwidth"}
     roof["traffic"] = stored_traffic(f"{kernel_key}:{w.name}")
-    roof.update({"kernel": kname, "kernel_ms_mean": kernel_ms, "kernel_ms_min": min(per),
-                 "kernel_ms_median": statistics.median(per)})
+    roof.update({"kernel": kname, "kernel_ms_mean": kernel_ms,
+                 "isolated_launch_ms_min": min(per),
+                 "isolated_launch_ms_median": statistics.median(per)})
     out = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -367,13 +384,13 @@ def run_ours(args, w, rank, world, local_rank):
             launch2()
         tg.sync_status(stream)
         n2 = max(50, args.steps)
-        tot2, per2, _, _ = time_launches(launch2, stream, n2, world, device)
+        _, k2, per2, _, _ = time_launches(launch2, stream, n2, world, device)
         tg.sync_status(stream)
-        k2 = statistics.mean(per2)
         gbs = ws.min_bytes / (k2 / 1e3) / 1e9
         out["skinny"] = {
             "workload": ws.name, "launches": n2, "kernel_ms_mean": k2,
-            "kernel_ms_min": min(per2), "tflops": ws.flops / (k2 / 1e3) / 1e12,
+            "isolated_launch_ms_min": min(per2), "isolated_launch_ms_median": statistics.median(per2),
+            "tflops": ws.flops / (k2 / 1e3) / 1e12,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": gbs / hbm_peak,
                          "traffic": stored_traffic(f"skinny:{ws.name}"),
@@ -397,9 +414,8 @@ def run_ours(args, w, rank, world, local_rank):
             launch3()
         tg.sync_status(stream)
         n4 = max(50, args.steps // 2)
-        _, per4, _, _ = time_launches(launch3, stream, n4, world, device)
+        _, k4, per4, _, _ = time_launches(launch3, stream, n4, world, device)
         tg.sync_status(stream)
-        k4 = statistics.mean(per4)
         if plan.kernel == tg.TG_KERNEL_PERSISTENT:
             ach = flops / (k4 / 1e3) / 1e12
             roof4 = {"bound": "tensor", "achieved": ach, "peak": tf_peak, "unit": "TFLOP/s",
@@ -409,7 +425,7 @@ def run_ours(args, w, rank, world, local_rank):
             roof4 = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
                      "frac": ach / hbm_peak}
         out["bf16"] = {"workload": w.name, "entry": "tg_gemm_bf16", "launches": n4,
-                       "kernel_ms_mean": k4, "kernel_ms_min": min(per4),
+                       "kernel_ms_mean": k4, "isolated_launch_ms_min": min(per4),
                        "tflops": flops / (k4 / 1e3) / 1e12, "roofline": roof4}
         del ab, bb, cb
 
@@ -438,13 +454,12 @@ def run_ours(args, w, rank, world, local_rank):
                 launch5()
             tg.sync_status(stream)
             n5 = max(50, args.steps // 2)
-            _, per5, _, _ = time_launches(launch5, stream, n5, world, device)
+            _, k5, per5, _, _ = time_launches(launch5, stream, n5, world, device)
             tg.sync_status(stream)
-            k5 = statistics.mean(per5)
             # bytes the epilogue adds: the residual read, the wider output
             extra = (w.M * w.N * 2 if r is not None else 0) + w.N * 4 + \
                 (w.M * w.N * 2 if odt == tg.TG_DTYPE_F32 else 0)
-            ent = {"launches": n5, "kernel_ms_mean": k5, "kernel_ms_min": min(per5),
+            ent = {"launches": n5, "kernel_ms_mean": k5, "isolated_launch_ms_min": min(per5),
                    "extra_bytes": extra, "vs_plain": kernel_ms / k5}
             if plan.kernel == tg.TG_KERNEL_PERSISTENT:
                 ach = flops / (k5 / 1e3) / 1e12
@@ -483,11 +498,10 @@ def run_ours(args, w, rank, world, local_rank):
                 launch6()
             tg.sync_status(stream)
             n6 = max(50, args.steps // 2) if mw.M <= 128 else max(20, args.steps // 10)
-            _, per6, _, _ = time_launches(launch6, stream, n6, world, device)
+            _, k6, per6, _, _ = time_launches(launch6, stream, n6, world, device)
             tg.sync_status(stream)
-            k6 = statistics.mean(per6)
             ent = {"workload": mname, "launches": n6, "kernel_ms_mean": k6,
-                   "kernel_ms_min": min(per6), "tflops": mw.flops / (k6 / 1e3) / 1e12}
+                   "isolated_launch_ms_min": min(per6), "tflops": mw.flops / (k6 / 1e3) / 1e12}
             if mw.M <= 128:
                 gbs = mw.min_bytes / (k6 / 1e3) / 1e9
                 ent["kernel"] = "tg_gemm_mxfp4_skinny (codes decoded in shared memory)"
@@ -533,13 +547,13 @@ def run_ours(args, w, rank, world, local_rank):
                 for _ in range(args.warmup):
                     launch7()
                 tg.sync_status(stream)
-                _, per, _, _ = time_launches(launch7, stream, n7, world, device)
+                _, mean, per, _, _ = time_launches(launch7, stream, n7, world, device)
                 tg.sync_status(stream)
             finally:
                 os.environ.pop("TGEMM_FORCE_SP24", None)
                 if prev is not None:
                     os.environ["TGEMM_FORCE_SP24"] = prev
-            return statistics.mean(per), min(per)
+            return mean, min(per)
 
         n7 = max(20, args.steps // 10)
         k7, min7 = time_sp24(None)
@@ -549,7 +563,7 @@ def run_ours(args, w, rank, world, local_rank):
         out["sp24"] = {
             "workload": sw.name, "entry": "tg_gemm_sp24", "launches": n7,
             "kernel": "tg_gemm_sp24_pair<3> (tcgen05.mma.sp cta_group::2, 256x256 tiles)",
-            "kernel_ms_mean": k7, "kernel_ms_min": min7,
+            "kernel_ms_mean": k7, "isolated_launch_ms_min": min7,
             "tflops_dense_equivalent": tf7,
             "vs_dense_pair": kernel_ms / k7 if (sw.M, sw.N, sw.K) == (w.M, w.N, w.K) else None,
             "roofline": {"bound": "tensor", "achieved": tf7, "peak": sp_peak, "unit": "TFLOP/s",
@@ -559,7 +573,7 @@ def run_ours(args, w, rank, world, local_rank):
                                         "sparse-to-dense ratio)"},
             "one_cta_kernel": {
                 "kernel": "tg_gemm_sp24 (tcgen05.mma.sp, 128x128 tiles)", "launches": n7,
-                "kernel_ms_mean": k7c, "kernel_ms_min": min7c,
+                "kernel_ms_mean": k7c, "isolated_launch_ms_min": min7c,
                 "tflops_dense_equivalent": sw.flops / (k7c / 1e3) / 1e12,
                 "traffic": stored_traffic(f"sp24:{sw.name}")},
         }
