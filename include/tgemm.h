@@ -351,8 +351,9 @@ void tg_debug_inject(int32_t mode);
  *     pageable memory works but each copy then waits for the host.
  * M, N, K, epilogue, stream   as for tg_gemm_f16.
  *
- * The call uploads A, then walks N in blocks of columns (at most 8 blocks,
- * each a multiple of 256 columns): for each block the library copies that
+ * The call uploads A, then walks N in blocks of columns (at most 8: 1024
+ * columns, then doubling up to 8192, the last taking the rest): for each
+ * block the library copies that
  * block of B up on a copy stream of its own, runs the GEMM of the block on
  * `stream`, and copies that block of C down on a second copy stream, ordered
  * by events, so uploads, products and downloads of different blocks overlap.

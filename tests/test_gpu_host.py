@@ -58,7 +58,7 @@ def run(tg, M, N, K, relu, pads=(0, 0, 0), pinned=True, seed=0):
 
 CASES = [  # M, N, K, relu, (pad lda, pad ldb, pad ldc)
     (300, 1000, 200, True, (0, 0, 0)),       # one column block
-    (512, 9000, 320, False, (0, 0, 0)),      # five blocks of 2048, the last 808 wide
+    (512, 9000, 320, False, (0, 0, 0)),      # blocks of 1024, 2048, 4096 and 1832 columns
     (257, 4100, 96, True, (5, 3, 7)),        # odd host strides, ragged everything
     (64, 6000, 512, False, (8, 0, 16)),      # M <= 128: split-K kernel in every block
     (1, 2500, 33, True, (1, 1, 1)),

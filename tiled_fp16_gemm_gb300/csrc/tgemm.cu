@@ -984,8 +984,9 @@ tg_status_t tg_sync_status(void* stream) {
 
 namespace {
 
-constexpr int kHostMaxBlocks = 8;        // column blocks per call
-constexpr int64_t kHostMinBlockCols = 2048;
+constexpr int kHostMaxBlocks = 8;           // column blocks per call
+constexpr int64_t kHostFirstBlockCols = 1024;  // then doubling, up to kHostMaxBlockCols
+constexpr int64_t kHostMaxBlockCols = 8192;
 
 struct HostPipeline {
     void* dA = nullptr;
@@ -1064,13 +1065,23 @@ extern "C" tg_status_t tg_gemm_f16_host(const void* A, const void* B, void* C, i
         (st = host_buffer(&hp.dC, &hp.bytes_c, static_cast<size_t>(M * Np * 2) + 16, s)) != TG_OK)
         return st;
 
-    // Column blocks: at most kHostMaxBlocks, each at least kHostMinBlockCols
-    // wide (a full wave of tiles) and a multiple of 256 columns.
-    int64_t blocks = (N + kHostMinBlockCols - 1) / kHostMinBlockCols;
-    if (blocks > kHostMaxBlocks) blocks = kHostMaxBlocks;
-    int64_t width = (N + blocks - 1) / blocks;
-    width = (width + 255) / 256 * 256;
-    blocks = (N + width - 1) / width;
+    // Column blocks: a narrow first one, so that downloads start early, then
+    // doubling widths (wider rows copy faster) up to kHostMaxBlockCols; the
+    // last of at most kHostMaxBlocks takes the rest.  Every block but the
+    // last is a multiple of 256 columns, so each block's device pointers stay
+    // 16-byte aligned.
+    int64_t c0s[kHostMaxBlocks + 1];
+    int blocks = 0;
+    {
+        int64_t c = 0, w = kHostFirstBlockCols;
+        while (c < N) {
+            if (blocks == kHostMaxBlocks - 1 || w > N - c) w = N - c;
+            c0s[blocks++] = c;
+            c += w;
+            w = w * 2 < kHostMaxBlockCols ? w * 2 : kHostMaxBlockCols;
+        }
+        c0s[blocks] = N;
+    }
 
     const char* hA = static_cast<const char*>(A);
     const char* hB = static_cast<const char*>(B);
@@ -1093,9 +1104,9 @@ extern "C" tg_status_t tg_gemm_f16_host(const void* A, const void* B, void* C, i
     if (K > 0 && cudaMemcpy2DAsync(dA, Kp * 2, hA, lda * 2, K * 2, M, cudaMemcpyHostToDevice,
                                    hp.up) != cudaSuccess)
         return fail();
-    for (int64_t j = 0; j < blocks; ++j) {
-        const int64_t c0 = j * width;
-        const int64_t w = N - c0 < width ? N - c0 : width;
+    for (int j = 0; j < blocks; ++j) {
+        const int64_t c0 = c0s[j];
+        const int64_t w = c0s[j + 1] - c0;
         if (K > 0 && cudaMemcpy2DAsync(dB + c0 * 2, Np * 2, hB + c0 * 2, ldb * 2, w * 2, K,
                                        cudaMemcpyHostToDevice, hp.up) != cudaSuccess)
             return fail();
