@@ -242,8 +242,13 @@ def test_plans(tg):
     assert p.num_tiles == 32 * 112 and p.grid == 152 and p.k_blocks == 32 and p.stages == 3
     assert p.smem_bytes <= 232448  # 227 KB opt-in limit per CTA
     assert p.ring_bytes == 2 * tg.tg_ring_bytes(128, 128, 128, p.stages, 2)
-    one = tg.tg_plan_f16(2048, 2048, 4096, 152)  # 64 pair tiles < 76 pairs: one-CTA tiles
-    assert one.cluster == 1 and (one.bm, one.bn) == (128, 128) and one.grid == 152
+    one = tg.tg_plan_f16(1536, 1536, 4096, 152)  # 144 tiles of 128x128 fit one wave
+    assert one.cluster == 1 and (one.bm, one.bn) == (128, 128) and one.grid == 144
+    # 64 pair tiles (< 76 pairs) but 256 tiles of 128x128 (> 152 SMs), K >= 1024: pairs
+    sub = tg.tg_plan_f16(2048, 2048, 4096, 152)
+    assert sub.cluster == 2 and sub.num_tiles == 64 and sub.grid == 128
+    short = tg.tg_plan_f16(2048, 2048, 512, 152)  # short K: one-CTA 128x128 tiles
+    assert short.cluster == 1 and (short.bm, short.bn) == (128, 128)
     pair = tg.tg_plan_f16(2048, 4864, 4096, 152)  # 8 x 19 = 152 pair tiles: two waves of pairs
     assert pair.cluster == 2 and pair.num_tiles == 152 and pair.grid == 152
     s = tg.tg_plan_f16(64, 16384, 8192, 152)

@@ -726,6 +726,18 @@ tg_status_t tg_plan_f16(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_pla
         plan_pair(M, N, K, num_sms, plan);
         return TG_OK;
     }
+    // Less than a wave of pair tiles, but more 128×128 tiles than SMs (one-CTA
+    // tiles would take two or more rounds) and K of at least 1024: one round of
+    // pair tiles on part of the GPU still wins, since one-CTA 128×128 tiles run
+    // at about 0.6 of the pair kernel's rate per SM.  Measured on GB300:
+    // 2048×2048×8192 47 µs against 84 µs, 2048×1536×4096 26 µs against 42 µs,
+    // 2048×2048×1024 14.1 µs against 16.4 µs.  With shorter K the pair kernel's
+    // longer pipeline fill loses (2048×2048×256: 10.3 µs against 8.3 µs).
+    const int64_t tiles128 = ceil_div(M, 128) * ceil_div(N, 128);
+    if (num_sms >= 2 && tiles128 > num_sms && K >= 1024) {
+        plan_pair(M, N, K, num_sms, plan);
+        return TG_OK;
+    }
     const int64_t tiles256 = ceil_div(M, 128) * ceil_div(N, kBigBN);
     if (tiles256 >= num_sms || N <= kMidBN) {
         if (N <= kMidBN)
