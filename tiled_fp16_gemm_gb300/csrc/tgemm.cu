@@ -608,10 +608,13 @@ bool forced_dense_kernel() {
 
 // 2:4 sparse A: tensor maps, kernel choice, tile plan and launch (operands in
 // the tensor memory-access layout, checked by the caller).  The CTA-pair
-// kernel (256×256 tiles) runs once its tiles fill every resident pair at least
-// once; smaller problems take the one-CTA kernel (128×128 tiles, twice the
-// CTAs in flight).  TGEMM_FORCE_SP24 = pair | cta overrides the choice (tests
-// and sweeps).  Both kernels take the same tensor maps: per CTA 128 rows of
+// kernel (256×256 tiles) runs once its tiles fill every resident pair at
+// least once, and also below that when K ≥ 1024 and one-CTA tiles would
+// occupy more than half the SMs (measured on GB300: 2048×2048×4096 22.7 µs
+// against 37.8 µs, 1536×1536×4096 20.8 against 22.7 µs, 2048×2048×1024 12.4
+// against 14.5 µs; a tie at K = 512).  Smaller problems take the one-CTA
+// kernel (128×128 tiles, four times the tiles in flight).
+// TGEMM_FORCE_SP24 = pair | cta overrides the choice (tests and sweeps).  Both kernels take the same tensor maps: per CTA 128 rows of
 // Ac and E and 128 k of B per stage.
 template <typename T>
 tg_status_t launch_sp24(const void* Ac, const void* E, const void* B, void* C, int64_t M,
@@ -632,7 +635,9 @@ tg_status_t launch_sp24(const void* Ac, const void* E, const void* B, void* C, i
                      : encode_2d(&tmC, C, N, M, ldc * 2, 64, 32, dt)))
         return TG_ERR_LAUNCH;
     const int64_t pair_tiles = ceil_div(M, PairCfg::BM) * ceil_div(N, PairCfg::BN);
-    bool pair = ds->max_sp_pairs >= 1 && pair_tiles >= ds->max_sp_pairs;
+    const int64_t cta_tiles = ceil_div(M, Cfg::BM) * ceil_div(N, Cfg::BN);
+    bool pair = ds->max_sp_pairs >= 1 &&
+                (pair_tiles >= ds->max_sp_pairs || (K >= 1024 && 2 * cta_tiles > ds->num_sms));
     if (const char* f = std::getenv("TGEMM_FORCE_SP24")) {
         if (std::strcmp(f, "pair") == 0) pair = ds->max_sp_pairs >= 1;
         if (std::strcmp(f, "cta") == 0) pair = false;
