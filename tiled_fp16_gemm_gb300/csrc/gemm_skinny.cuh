@@ -79,30 +79,29 @@ struct SkinnyCfg {
 };
 using SkinnyNarrow = SkinnyCfg<9, 64, 64>;
 using SkinnyWide = SkinnyCfg<6, 128, 64>;
-// MXFP4 B (M ≤ 128 weight streaming).  Units of 128 k: per unit, two 128 n ×
-// 64 k tiles of packed codes (128 rows × 32 bytes each, TMA 32-byte swizzle)
-// and their scales (4 rows × 128 bytes) land in a deep raw ring: the codes
-// are the HBM stream, and ~130 KB of them in flight per SM takes 16 stages.
-// 128 k per unit spreads the MMA thread's per-unit barrier wait, fence and
-// commit over 8 MMAs: that thread sets the pace (about 820 cycles per 64-k
-// unit of four MMAs, measured with clock stamps).  The A
-// tile (from L2, re-read by every CTA) has a shallow ring of its own with its
-// own producer thread; were it in the raw ring it would take most of each
-// stage (8 KB against 4.25 KB) and cap the codes in flight.  The A ring is
-// indexed like the tensor-memory operand stages (8 of each), so one MMA
-// commit per unit frees both, and the converters wait for a unit's A tile
-// before they report its operand decoded: the MMA thread, the pipeline's
-// slowest member (four MMA issues per unit), waits once and commits once per
-// unit.  Converter
-// threads each own one column n of the tile: they decode its 64 k into fp16
-// and write them with tcgen05.st straight into the tensor memory holding the
-// MMA's A operand (the weight tile is the A operand of the swapped product),
-// so decoded weights never pass through shared memory.  Tensor memory holds
-// the two accumulators (256 columns) and kStages operand stages of 32
-// columns.  Two converter groups of four warps (one per tensor-memory lane
-// quarter) take alternate units.  A raw stage is free once its group has
-// decoded it; an operand stage and its A stage once the MMAs that read them
-// have completed.
+// MXFP4 B (M ≤ 128 weight streaming), units of kMxBK = 128 k.
+//   Raw ring (deep, four producer threads): per unit, two 128 n × 64 k tiles
+//     of packed codes (128 rows × 32 bytes each, TMA 32-byte swizzle) and
+//     their scales (4 rows × 128 bytes).  The codes are the HBM stream; ~130
+//     KB of them in flight per SM takes 16 stages.
+//   A ring (one producer thread): the unit's activation tile (from L2,
+//     re-read by every CTA).  Were it in the raw ring it would take most of
+//     each stage (16 KB against 8.5 KB) and cap the codes in flight.  It is
+//     indexed like the tensor-memory operand stages (4 of each), so the one
+//     MMA commit per unit frees both.
+//   Converters (two groups of four warps, one per tensor-memory lane
+//     quarter, alternate units): thread n owns weight column n of the tile,
+//     decodes its 128 k into fp16 and writes them with tcgen05.st straight
+//     into the operand stage (the weight tile is the A operand of the swapped
+//     product), so decoded weights never pass through shared memory.  A
+//     group also waits for the unit's A tile before it reports the operand
+//     decoded, so the MMA thread waits on one barrier per unit.
+//   Tensor memory: two accumulators (256 columns) and 4 operand stages of 64
+//     columns.
+// The MMA thread sets the pace (about 80 cycles per MMA issue, measured with
+// clock stamps); 128 k per unit spreads its per-unit wait, fence and commit
+// over 8 MMAs.  A raw stage is free once its group has decoded it; an
+// operand stage and its A stage once the MMAs that read them have completed.
 constexpr int kMxBK = 128;                       // k per MXFP4 unit
 constexpr uint32_t kMxCodeBox = 128 * 32;        // one 64-k tile of codes
 constexpr uint32_t kMxRawBytes = (kMxBK / 64) * kMxCodeBox;
