@@ -378,7 +378,7 @@ tg_status_t tg_gemm_f16_host(const void* A, const void* B, void* C,
  * ------------------------------------------------------------------------ */
 
 /* Size of the scratch array inside the library that tg_gemm_f16_noalloc uses. */
-#define TG_NOALLOC_SCRATCH_BYTES ((int64_t)12 * 1024 * 1024)
+#define TG_NOALLOC_SCRATCH_BYTES ((int64_t)24 * 1024 * 1024)
 
 /*
  * tg_gemm_f16_noalloc — C = epi(A·B) for 1 ≤ M ≤ 128 without allocating any
@@ -390,8 +390,8 @@ tg_status_t tg_gemm_f16_host(const void* A, const void* B, void* C,
  * stall other streams.
  *
  * It runs the same split-K kernel that tg_gemm_f16 uses for M ≤ 128, with its
- * scratch (fp32 partial sums and ready flags) in a fixed array of
- * TG_NOALLOC_SCRATCH_BYTES (12 MiB) inside the library; every device that
+ * scratch (fp32 partial sums and piece counters) in a fixed array of
+ * TG_NOALLOC_SCRATCH_BYTES (24 MiB) inside the library; every device that
  * loads the library holds that array until the process exits.  It calls no
  * cudaMalloc, cudaFree or other allocating routine.
  *
@@ -404,7 +404,7 @@ tg_status_t tg_gemm_f16_host(const void* A, const void* B, void* C,
  *     array holds (more than 191 CTAs, i.e. a device with more than 191 SMs).
  *   - K == 0 fills C with +0 and uses no scratch; M == 0 or N == 0 is a no-op.
  *   - Set-up: the first call on each device (with that device current) looks
- *     up the array's device address and clears its flag words on `stream`.
+ *     up the array's device address and clears its counter words on `stream`.
  *     Make that first call before any stream capture begins.
  *   - Every call shares the one array, which keeps what the last call left in
  *     it.  Calls whose kernels overlap on the GPU (e.g. on two streams with no

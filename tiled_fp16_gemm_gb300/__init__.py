@@ -45,7 +45,7 @@ EXPORTS = (
 )
 
 #: bytes of the library's fixed scratch array used by tg_gemm_f16_noalloc
-TG_NOALLOC_SCRATCH_BYTES = 12 * 1024 * 1024
+TG_NOALLOC_SCRATCH_BYTES = 24 * 1024 * 1024
 
 
 class tg_plan_t(ctypes.Structure):
@@ -221,7 +221,7 @@ def tg_debug_inject(mode: int) -> None:
 def tg_gemm_f16_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
                         ldc: int, epilogue: int, stream: int | None) -> int:
     """C = epi(A·B) for M <= 128 with no device allocation: the split-K
-    scratch lives in a fixed 12 MiB array inside the library.  For callers
+    scratch lives in a fixed 24 MiB array inside the library.  For callers
     that cannot allocate device memory at call time.  Calls that overlap on
     the GPU share that array and race; the first call on a device does a
     one-time set-up and should come before any stream capture.  Returns the

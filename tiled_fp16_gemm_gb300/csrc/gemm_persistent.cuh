@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot_ptr;
+    grid_dependency_wait();  // the previous kernel's writes are visible from here on
+    grid_launch_dependents();
 
     auto fail = [&](unsigned int role) {
         atomicOr(&g_wait_timeout_flags, role);

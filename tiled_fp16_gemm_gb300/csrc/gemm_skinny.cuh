@@ -17,25 +17,23 @@
 // Split-K over "units" (tile, k-block), numbered tile-major.  CTA c of G owns
 // the contiguous unit range [U·c/G, U·(c+1)/G), so every SM streams the same
 // number of B bytes.  A range is cut at tile edges into segments:
-//   FULL     the whole k range of a tile: epilogue writes C directly;
-//   PARTIAL  starts inside a tile (only a CTA's first segment can): its fp32
-//            partial goes to workspace slot c; each epilogue warp then sets
-//            flag[4c + warp quarter] = 1 for the 32 columns it wrote (the
-//            owner warp that reads it sets it back to 0, so flags are zero
-//            between launches);
-//   OWNER    starts at k = 0 but the range ends inside the tile (only a CTA's
-//            last segment can): each epilogue warp waits for its quarter's
-//            flags of CTAs c+1 .. c_last holding the rest of the tile, then
-//            adds their partials in that order (k order), applies the
-//            epilogue and writes C.  No barrier spans several warps.
+//   FULL     the whole k range of a tile: the epilogue writes C directly;
+//   piece    a segment that starts or ends inside its tile.  The tile's
+//            pieces lie in CTAs c_head .. c_tail in k order: the head's is its
+//            last segment (k = 0 onwards), every other one is its CTA's first
+//            segment.  Each epilogue warp writes its 32 columns of the fp32
+//            partial to its CTA's slot for it (first segment: slot 2c; head:
+//            slot 2c + 1), then adds one to counter[4 c_head + warp quarter].
+//            The warp that brings the counter to the number of pieces adds the
+//            slots in k order (head first), applies the epilogue, writes C and
+//            zeroes the counter, so counters are zero between launches.
 // The epilogue (bias, ReLU, residual, output type) is applied per element by
 // the thread holding column n: C[m][n] = out(act(acc + bias[n]) + R[m][n]),
 // with plain stores (consecutive threads write consecutive n).
-// The summation order is fixed by the sizes alone, so results are
-// deterministic.  Owners only wait on higher-numbered CTAs, which write their
-// partials from their first segment, so the waits form no cycle; the launch
-// is cooperative so all G ≤ #SM CTAs are resident together.  All waits are
-// bounded.
+// The summation order is fixed by the sizes alone, whichever piece finishes
+// last, so results are deterministic.  No CTA waits for another, so the
+// launch needs no co-residency guarantee (and no cooperative launch); the
+// waits inside a CTA are bounded.
 //
 // The pages do not describe a split-K or swap-AB variant; this is the plain
 // reading of "measure the bandwidth and compute ceilings first"
@@ -165,9 +163,8 @@ struct SkinnyParams {
     uint64_t timeout_ns;
     void* C;  // T*: the kernel's element type
     int64_t ldc;
-    float* ws;
-    uint32_t* flags;
-    uint32_t epoch;
+    float* ws;            // two partial slots per CTA
+    uint32_t* counters;   // four piece counters per CTA (zero between launches)
     EpilogueArgs e;       // bias / residual (null: none)
     int32_t out_f32 = 0;  // 1: C is fp32
 };
@@ -184,14 +181,15 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
         : "memory");
 }
 
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+// Returns the old value; orders this thread's earlier writes before the add
+// and its later reads after it, at GPU scope.
+__device__ __forceinline__ uint32_t atomic_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
 }
 
 // The kernel body shared by the fp16/bf16 kernel (QB = false: B^T tiles by
@@ -276,6 +274,8 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot_ptr;
+    grid_dependency_wait();  // the previous kernel's writes are visible from here on
+    grid_launch_dependents();
 
     auto fail = [&](unsigned int role) {
         atomicOr(&g_wait_timeout_flags, role);
@@ -471,9 +471,14 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
             tc_fence_after_sync();
             const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * 128);
 
-            if (kb0 > 0) {
-                // PARTIAL: fp32 partial to this CTA's slot, layout [m][n_local].
-                float* slot = p.ws + static_cast<int64_t>(blockIdx.x) * kSkSlotFloats;
+            // The slots this warp sums, in k order (none: a FULL segment,
+            // summed from tensor memory alone).
+            int64_t c_head = 0, c_last = -1;
+            if (kb0 > 0 || kb1 < KB) {
+                // A piece of a split tile: its fp32 partial to this CTA's
+                // slot for it, layout [m][n_local].
+                const int64_t my_slot = 2 * static_cast<int64_t>(blockIdx.x) + (kb0 > 0 ? 0 : 1);
+                float* slot = p.ws + my_slot * kSkSlotFloats;
                 for (int c = 0; c < nchunks; ++c) {
                     uint32_t r[16];
                     tmem_ld_x16(tacc + 16 * c, r);
@@ -484,79 +489,73 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                 tc_fence_before_sync();
                 __threadfence();
                 __syncwarp();
+                // The accumulator is free.  Count this piece in; the warp
+                // that brings the count to the tile's number of pieces sums
+                // them all.
+                c_head = unit_owner(t * KB, G, U);
+                const int64_t c_tail = unit_owner((t + 1) * KB - 1, G, U);
+                int last = 0;
                 if (lane == 0) {
                     mbar_arrive(bar_tempty + 8 * acc);
-                    // this warp's 32 columns of the partial are published
-                    st_release_gpu(p.flags + 4 * static_cast<int64_t>(blockIdx.x) + q, p.epoch);
+                    uint32_t* cnt = p.counters + 4 * c_head + q;
+                    const uint32_t before = atomic_add_acq_rel_gpu(cnt, 1u);
+                    last = before + 1 == static_cast<uint32_t>(c_tail - c_head + 1) ? 1 : 0;
+                    if (last) *cnt = 0u;  // zero again for the next launch
                 }
-            } else {
-                // FULL or OWNER.
-                int64_t c_first = 0, c_last = -1;
-                if (kb1 < KB) {  // OWNER: the rest of the tile lives in CTAs c+1 .. c_last
-                    c_first = blockIdx.x + 1;
-                    c_last = unit_owner((t + 1) * KB - 1, G, U);
-                    bool got = true;
-                    for (int64_t c = c_first; c <= c_last && got; ++c) {
-                        const uint32_t* f = p.flags + 4 * c + q;
-                        if (ld_acquire_gpu(f) != p.epoch) {
-                            const uint64_t t0 = globaltimer_ns();
-                            while (ld_acquire_gpu(f) != p.epoch) {
-                                if (*abort_flag || globaltimer_ns() - t0 > p.timeout_ns) {
-                                    got = false;
-                                    break;
-                                }
-                                __nanosleep(64);
-                            }
-                        }
-                    }
-                    if (__any_sync(0xffffffffu, !got)) {
-                        if (lane == 0) fail(kRoleEpilogue);
-                        break;
-                    }
+                if (!__shfl_sync(0xffffffffu, last, 0)) {
+                    u = seg_end;
+                    continue;
                 }
-                for (int c = 0; c < nchunks; ++c) {
+                __threadfence();
+                c_last = c_tail;
+            }
+            // FULL, or the last piece of a split tile in: C[m][n] =
+            // out(act(sum + bias[n]) + R[m][n]); this thread holds column n.
+            for (int c = 0; c < nchunks; ++c) {
+                float v[16];
+                if (c_last < 0) {
                     uint32_t r[16];
                     tmem_ld_x16(tacc + 16 * c, r);
-                    float v[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-                    for (int64_t cc = c_first; cc <= c_last; ++cc) {
-                        const float* slot = p.ws + cc * kSkSlotFloats;
+                } else {
+                    // the head's piece (its second slot), then the first
+                    // pieces of CTAs c_head + 1 .. c_last: k order
+                    const float* h = p.ws + (2 * c_head + 1) * kSkSlotFloats;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) v[i] += __ldcg(slot + (16 * c + i) * 128 + n_local);
+                    for (int i = 0; i < 16; ++i) v[i] = __ldcg(h + (16 * c + i) * 128 + n_local);
+                    for (int64_t cc = c_head + 1; cc <= c_last; ++cc) {
+                        const float* slot = p.ws + 2 * cc * kSkSlotFloats;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            v[i] += __ldcg(slot + (16 * c + i) * 128 + n_local);
                     }
-                    if (n < p.N) {
-                        // C[m][n] = out(act(acc + bias[n]) + R[m][n]): this
-                        // thread holds column n of rows 16c .. 16c + 15.
-                        const float bias_n = p.e.bias != nullptr ? __ldg(p.e.bias + n) : 0.0f;
+                }
+                if (n < p.N) {
+                    const float bias_n = p.e.bias != nullptr ? __ldg(p.e.bias + n) : 0.0f;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int m = 16 * c + i;
-                            if (m < p.M) {
-                                float x = v[i];
-                                if (p.e.bias != nullptr) x += bias_n;
-                                if (p.relu) x = relu_f32(x);
-                                if (p.e.resid != nullptr)
-                                    x += Elem16<T>::to_float(static_cast<const T*>(
-                                        p.e.resid)[static_cast<int64_t>(m) * p.e.ldr + n]);
-                                const int64_t off = static_cast<int64_t>(m) * p.ldc + n;
-                                if (p.out_f32)
-                                    static_cast<float*>(p.C)[off] = x;
-                                else
-                                    static_cast<T*>(p.C)[off] = Elem16<T>::from_float(x);
-                            }
+                    for (int i = 0; i < 16; ++i) {
+                        const int m = 16 * c + i;
+                        if (m < p.M) {
+                            float x = v[i];
+                            if (p.e.bias != nullptr) x += bias_n;
+                            if (p.relu) x = relu_f32(x);
+                            if (p.e.resid != nullptr)
+                                x += Elem16<T>::to_float(static_cast<const T*>(
+                                    p.e.resid)[static_cast<int64_t>(m) * p.e.ldr + n]);
+                            const int64_t off = static_cast<int64_t>(m) * p.ldc + n;
+                            if (p.out_f32)
+                                static_cast<float*>(p.C)[off] = x;
+                            else
+                                static_cast<T*>(p.C)[off] = Elem16<T>::from_float(x);
                         }
                     }
                 }
+            }
+            if (c_last < 0) {
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bar_tempty + 8 * acc);
-                    // Each flag has this warp as its only reader: clear the
-                    // ones consumed, so every launch leaves the flags at zero
-                    // (a replayed graph finds them clean).
-                    for (int64_t cc = c_first; cc <= c_last; ++cc) p.flags[4 * cc + q] = 0u;
-                }
+                if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
             }
             u = seg_end;
         }
@@ -713,7 +712,7 @@ inline void skinny_plan_bk(int64_t M, int64_t N, int64_t K, int32_t num_sms, int
     const int64_t shortest = U / G;
     pl->split_k = shortest > 0 ? (pl->k_blocks + shortest - 1) / shortest + 1 : pl->k_blocks;
     if (pl->split_k > G) pl->split_k = G;
-    pl->workspace_bytes = G * kSkSlotFloats * 4 + 4 * G * 4;
+    pl->workspace_bytes = 2 * G * kSkSlotFloats * 4 + 4 * G * 4;
     pl->cluster = 1;
 }
 
@@ -758,14 +757,13 @@ inline cudaError_t skinny_set_attributes() {
                                 SkinnyWide::kSmemBytes);
 }
 
-// Cooperative launch of the instantiation whose A slots fit prm.Mp.
+// Launch of the instantiation whose A slots fit prm.Mp.
 template <typename T>
 inline cudaError_t skinny_launch_kernel(const CUtensorMap& tmB, const CUtensorMap& tmA,
                                         const SkinnyParams& prm, int64_t grid,
                                         cudaStream_t stream) {
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    set_dependent_launch(attr[0]);
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -785,13 +783,12 @@ inline cudaError_t skinny_launch_kernel(const CUtensorMap& tmB, const CUtensorMa
         &cfg, tg_gemm_f16_skinny<SkinnyWide::kStages, 128, T, SkinnyWide::kBK>, tmB, tmA, prm);
 }
 
-// Cooperative launch of the MXFP4 instantiation whose A slots fit prm.Mp.
+// Launch of the MXFP4 instantiation whose A slots fit prm.Mp.
 inline cudaError_t skinny_mx_launch_kernel(const CUtensorMap& tmBq, const CUtensorMap& tmA,
                                            const CUtensorMap& tmS, const SkinnyParams& prm,
                                            int64_t grid, cudaStream_t stream) {
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    set_dependent_launch(attr[0]);
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -811,9 +808,9 @@ inline cudaError_t skinny_mx_launch_kernel(const CUtensorMap& tmBq, const CUtens
 }
 
 struct SkinnyWorkspace {
-    float* partials = nullptr;
-    uint32_t* flags = nullptr;
-    int64_t slots = 0;
+    float* partials = nullptr;    // two slots per CTA
+    uint32_t* counters = nullptr;  // four per CTA
+    int64_t ctas = 0;
 };
 
 inline std::mutex& skinny_ws_mutex() {
@@ -826,51 +823,53 @@ inline std::map<std::pair<int, cudaStream_t>, SkinnyWorkspace>& skinny_ws_map() 
     return m;
 }
 
-// After a launch gave up on a wait, flags it raised may never have been
-// consumed: reset every workspace's flags on this device (the device is idle).
-inline void skinny_reset_flags(int dev) {
+// After a launch gave up on a wait, some tiles' counters may never have
+// reached their piece count (and been zeroed): reset every workspace's
+// counters on this device (the device is idle).
+inline void skinny_reset_counters(int dev) {
     std::lock_guard<std::mutex> lk(skinny_ws_mutex());
     for (auto& kv : skinny_ws_map())
-        if (kv.first.first == dev && kv.second.flags != nullptr)
-            cudaMemset(kv.second.flags, 0, 4 * kv.second.slots * sizeof(uint32_t));
+        if (kv.first.first == dev && kv.second.counters != nullptr)
+            cudaMemset(kv.second.counters, 0, 4 * kv.second.ctas * sizeof(uint32_t));
 }
 
-// The split-K workspace of (dev, stream) into prm (ws, flags, epoch); sized on
+// The split-K workspace of (dev, stream) into prm (ws, counters); sized on
 // first use for the largest grid, so later calls never grow it.
 inline tg_status_t skinny_workspace(int dev, cudaStream_t stream, int64_t grid, int64_t max_ctas,
                                     SkinnyParams* prm) {
     {
         std::lock_guard<std::mutex> lk(skinny_ws_mutex());
         SkinnyWorkspace& ws = skinny_ws_map()[std::make_pair(dev, stream)];
-        if (ws.slots < grid) {
+        if (ws.ctas < grid) {
             // First use on this stream: room for the largest grid (one CTA
             // per SM), so later calls, graph captures included, never grow it.
             if (ws.partials) {
                 cudaStreamSynchronize(stream);
                 cudaFree(ws.partials);
-                cudaFree(ws.flags);
+                cudaFree(ws.counters);
                 ws.partials = nullptr;
-                ws.flags = nullptr;
-                ws.slots = 0;
+                ws.counters = nullptr;
+                ws.ctas = 0;
             }
-            const int64_t slots = grid > max_ctas ? grid : max_ctas;
-            if (cudaMalloc(&ws.partials, slots * kSkSlotFloats * sizeof(float)) != cudaSuccess ||
-                cudaMalloc(&ws.flags, 4 * slots * sizeof(uint32_t)) != cudaSuccess) {
+            const int64_t ctas = grid > max_ctas ? grid : max_ctas;
+            if (cudaMalloc(&ws.partials, 2 * ctas * kSkSlotFloats * sizeof(float)) !=
+                    cudaSuccess ||
+                cudaMalloc(&ws.counters, 4 * ctas * sizeof(uint32_t)) != cudaSuccess) {
                 cudaGetLastError();
                 if (ws.partials) cudaFree(ws.partials);
                 ws.partials = nullptr;
-                ws.flags = nullptr;
+                ws.counters = nullptr;
                 return TG_ERR_NO_MEMORY;
             }
-            if (cudaMemsetAsync(ws.flags, 0, 4 * slots * sizeof(uint32_t), stream) != cudaSuccess) {
+            if (cudaMemsetAsync(ws.counters, 0, 4 * ctas * sizeof(uint32_t), stream) !=
+                cudaSuccess) {
                 cudaGetLastError();
                 return TG_ERR_LAUNCH;
             }
-            ws.slots = slots;
+            ws.ctas = ctas;
         }
         prm->ws = ws.partials;
-        prm->flags = ws.flags;
-        prm->epoch = 1;  // flags are zero between launches (owners clear them)
+        prm->counters = ws.counters;  // zero between launches (the last piece zeroes them)
     }
     return TG_OK;
 }

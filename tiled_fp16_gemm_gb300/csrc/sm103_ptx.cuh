@@ -11,6 +11,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_runtime.h>
 
 namespace tg {
 
@@ -22,6 +23,33 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// ------------------------------------------------------------------ dependent launch
+//
+// Every kernel of this library is launched with programmatic stream
+// serialisation allowed: its CTAs may be placed on SMs that the previous
+// kernel in the stream has already left, and run their set-up (barrier
+// initialisation, tensor-memory allocation, descriptor prefetch) while that
+// kernel's last CTAs finish.  grid_dependency_wait() then blocks until the
+// previous kernel has completed and its memory writes are visible, so nothing
+// before it may touch global memory that another kernel writes.  Where the
+// previous work is not a kernel (a copy, an event wait) it is a plain stream
+// dependency and the wait returns at once.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel in the stream be scheduled onto SMs as they free up.
+// It cannot start before this one's CTAs are all placed, and it reads
+// nothing this one writes before its own grid_dependency_wait().
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+inline void set_dependent_launch(cudaLaunchAttribute& a) {
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
 }
 
 // ------------------------------------------------------------------ mbarrier

@@ -30,7 +30,7 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
 std::atomic<int32_t> g_inject{0};
 
-void noalloc_reset_flags(int dev);  // defined with the no-allocation entry point below
+void noalloc_reset_counters(int dev);  // defined with the no-allocation entry point below
 
 // ------------------------------------------------------------------ planning
 
@@ -302,6 +302,10 @@ tg_status_t launch_persistent(const void* A, const void* B, void* C, const tg_pl
     cfg.blockDim = dim3(tg::PersistentCfg<BN, STAGES>::kThreads);
     cfg.dynamicSmemBytes = tg::PersistentCfg<BN, STAGES>::kSmemBytes;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    tg::set_dependent_launch(attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     cudaError_t e =
         cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_persistent<BN, STAGES, T>, tmA, tmB, tmC, prm);
     if (e != cudaSuccess) {
@@ -324,11 +328,12 @@ tg_status_t launch_pair(const void* A, const void* B, void* C, const tg_plan_t& 
     const tg::PersistentParams prm = persistent_params(pl, M, N, K, ep);
     int64_t pairs = pl.grid / 2;
     if (pairs > max_pairs) pairs = max_pairs;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    tg::set_dependent_launch(attr[1]);
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
@@ -336,7 +341,7 @@ tg_status_t launch_pair(const void* A, const void* B, void* C, const tg_plan_t& 
     cfg.dynamicSmemBytes = PairCfgT::kSmemBytes;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e =
         cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_pair<kPairStages, T, kPairBK>, tmA, tmB, tmC,
                            prm);
@@ -663,19 +668,21 @@ tg_status_t launch_sp24(const void* Ac, const void* E, const void* B, void* C, i
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    tg::set_dependent_launch(attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     cudaError_t e;
     if (pair) {
         const int64_t pairs = prm.num_tiles < ds->max_sp_pairs ? prm.num_tiles : ds->max_sp_pairs;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
         cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
         cfg.blockDim = dim3(PairCfg::kThreads);
         cfg.dynamicSmemBytes = PairCfg::kSmemBytes;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 2;
         e = cudaLaunchKernelEx(&cfg, tg::tg_gemm_sp24_pair<kSpPairStages, T>, tmA, tmB, tmE, tmC,
                                sp);
     } else {
@@ -980,12 +987,12 @@ tg_status_t tg_sync_status(void* stream) {
     }
     if (flags != 0) {
         // A kernel gave up early: let every queued kernel finish, then clear
-        // the split-K flags it may have left raised before anything reuses them.
+        // the split-K counters it may have left non-zero before anything reuses them.
         cudaDeviceSynchronize();
         const unsigned int zero = 0;
         cudaMemcpyToSymbol(tg::g_wait_timeout_flags, &zero, sizeof(zero));
-        tg::skinny_reset_flags(dev);
-        noalloc_reset_flags(dev);
+        tg::skinny_reset_counters(dev);
+        noalloc_reset_counters(dev);
         cudaGetLastError();
         return TG_ERR_TIMEOUT;
     }
@@ -1147,7 +1154,7 @@ extern "C" tg_status_t tg_gemm_f16_host(const void* A, const void* B, void* C, i
 // ====================================================================== no-allocation variant
 //
 // tg_gemm_f16_noalloc runs the skinny split-K kernel with its scratch (fp32
-// partial sums and the per-warp ready flags) in the file-scope array below
+// partial sums and the per-warp piece counters) in the file-scope array below
 // instead of a workspace obtained from cudaMalloc.  It serves callers that
 // cannot allocate device memory at call time.  The array is a fixed
 // TG_NOALLOC_SCRATCH_BYTES; every device that loads this library holds it
@@ -1161,9 +1168,10 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[TG_NOALLOC_SCRATCH_BYTES];
 
-// Flag words first (4 per CTA, 16 bytes), then the fp32 partial slots.
-constexpr int64_t kNoallocFlagBytes = 64 * 1024;
-constexpr int64_t kNoallocMaxCtas = kNoallocFlagBytes / 16;
+// Counter words first (4 per CTA, 16 bytes), then the fp32 partial slots
+// (two per CTA).
+constexpr int64_t kNoallocCounterBytes = 64 * 1024;
+constexpr int64_t kNoallocMaxCtas = kNoallocCounterBytes / 16;
 
 struct NoallocDeviceState {
     bool ready = false;
@@ -1173,11 +1181,11 @@ struct NoallocDeviceState {
 std::mutex g_noalloc_mutex;
 NoallocDeviceState g_noalloc[kMaxDevices];
 
-// After a timed-out launch: clear the flag words (the device is idle).
-void noalloc_reset_flags(int dev) {
+// After a timed-out launch: clear the counter words (the device is idle).
+void noalloc_reset_counters(int dev) {
     std::lock_guard<std::mutex> lk(g_noalloc_mutex);
     if (dev >= 0 && dev < kMaxDevices && g_noalloc[dev].ready)
-        cudaMemset(g_noalloc[dev].base, 0, kNoallocFlagBytes);
+        cudaMemset(g_noalloc[dev].base, 0, kNoallocCounterBytes);
 }
 
 }  // namespace
@@ -1206,7 +1214,7 @@ extern "C" tg_status_t tg_gemm_f16_noalloc(const void* A, const void* B, void* C
     std::memset(&pl, 0, sizeof(pl));
     tg::skinny_plan(M, N, K, ds->num_sms, &pl);
     if (pl.grid > kNoallocMaxCtas ||
-        kNoallocFlagBytes + pl.grid * tg::kSkSlotFloats * 4 > TG_NOALLOC_SCRATCH_BYTES)
+        kNoallocCounterBytes + 2 * pl.grid * tg::kSkSlotFloats * 4 > TG_NOALLOC_SCRATCH_BYTES)
         return TG_ERR_INVALID_VALUE;  // would need more scratch than the array holds
 
     tg::SkinnyParams prm;
@@ -1215,23 +1223,22 @@ extern "C" tg_status_t tg_gemm_f16_noalloc(const void* A, const void* B, void* C
         NoallocDeviceState& ns = g_noalloc[dev];
         if (!ns.ready) {
             // Once per device, with that device current: the array's device
-            // address, and the flag words cleared (each launch then leaves
-            // them at zero: the kernel's owners clear what they consume).
+            // address, and the counter words cleared (each launch then leaves
+            // them at zero: the warp that sums a tile zeroes its counter).
             void* p = nullptr;
             if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
                 cudaGetLastError();
                 return TG_ERR_LAUNCH;
             }
-            if (cudaMemsetAsync(p, 0, kNoallocFlagBytes, s) != cudaSuccess) {
+            if (cudaMemsetAsync(p, 0, kNoallocCounterBytes, s) != cudaSuccess) {
                 cudaGetLastError();
                 return TG_ERR_LAUNCH;
             }
             ns.base = static_cast<unsigned char*>(p);
             ns.ready = true;
         }
-        prm.flags = reinterpret_cast<uint32_t*>(ns.base);
-        prm.ws = reinterpret_cast<float*>(ns.base + kNoallocFlagBytes);
-        prm.epoch = 1;
+        prm.counters = reinterpret_cast<uint32_t*>(ns.base);
+        prm.ws = reinterpret_cast<float*>(ns.base + kNoallocCounterBytes);
     }
 
     const int64_t Mp = pl.mma_n;
