@@ -49,6 +49,40 @@ int main() {
         if (tg::unit_begin(G2, G2, U2) != U2) return fail("unit_begin overflow", U2, G2, 0);
         if (tg::unit_owner(U2 - 1, G2, U2) != G2 - 1) return fail("unit_owner overflow", U2, G2, 0);
     }
+    // pair work items: every (tile, k block) exactly once, pieces only in the
+    // last wave, at most kPairMaxSplit of them, each at least
+    // kPairMinPieceBlocks long, R·S <= P, and P <= pairs
+    for (int T = 1; T <= 700; T += (T < 160 ? 1 : 37)) {
+        for (int pairs : {1, 2, 7, 38, 74, 76}) {
+            for (int KB : {1, 7, 8, 16, 32, 33, 64}) {
+                int P = 0, S = 0;
+                tg::pair_launch_shape(T, pairs, KB, &P, &S);
+                if (P < 1 || P > pairs || S < 1 || S > tg::kPairMaxSplit)
+                    return fail("pair_launch_shape range", T, pairs, KB);
+                if (S > 1 && KB / S < tg::kPairMinPieceBlocks)
+                    return fail("pair piece length", T, pairs, KB);
+                const int W = T / P, R = T - W * P;
+                if (R * S > P) return fail("pair tail items", T, P, S);
+                std::vector<int> seen(static_cast<size_t>(T) * KB, 0);
+                for (int c = 0; c < P; ++c) {
+                    const int n = tg::pair_item_count(c, T, P, S);
+                    for (int i = 0; i < n; ++i) {
+                        int tile = -1, kb0 = -1, kb1 = -1;
+                        tg::pair_item(c, i, T, P, S, KB, &tile, &kb0, &kb1);
+                        if (tile < 0 || tile >= T || kb0 < 0 || kb1 > KB || kb0 >= kb1)
+                            return fail("pair_item range", T, c, i);
+                        if ((kb0 != 0 || kb1 != KB) && tile < W * P)
+                            return fail("pair piece outside the last wave", T, c, i);
+                        for (int kb = kb0; kb < kb1; ++kb)
+                            if (seen[static_cast<size_t>(tile) * KB + kb]++)
+                                return fail("pair_item duplicate", T, tile, kb);
+                    }
+                }
+                for (size_t u = 0; u < seen.size(); ++u)
+                    if (seen[u] != 1) return fail("pair_item missing", T, P, static_cast<long long>(u));
+            }
+        }
+    }
     std::printf("OK\n");
     return 0;
 }

@@ -54,7 +54,127 @@ struct PairCfg {
     static constexpr uint32_t kSmemBytes =
         1024 + STAGES * kStageBytes + kCBytes + kBarBytes;
     static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeded");
+    // a split tail tile's reduction borrows 48 KB of the ring per epilogue warp
+    static_assert(STAGES * kStageBytes >= 4 * 48 * 1024, "ring too small for the reduction");
 };
+
+// Partial slots of split tail tiles: per cluster, 8 warp regions (rank × lane
+// quarter) of 32 rows × 256 columns.  Inside a region, column group g (4
+// columns) of row `lane` is the float4 at ((g · 32) + lane) · 4, so each warp
+// store instruction covers 512 contiguous bytes and each 64-column chunk is
+// 8 KB of contiguous floats.
+constexpr int64_t kPairWarpFloats = 32 * 256;
+constexpr int64_t kPairSlotFloats = 8 * kPairWarpFloats;  // 256 KB
+constexpr uint32_t kPairChunkBytes = 64 * 32 * 4;         // one 64-column chunk of a region
+constexpr uint32_t kPairRedBytes = 48 * 1024;             // per epilogue warp, in the ring
+
+// Epilogue of one warp for a piece of a split tail tile (see tile_schedule.h).
+// A piece is always its cluster's last item, so the operand ring is idle and
+// the accumulator is not overwritten after its tmem_full.  The warp writes its
+// partial to the cluster's slot and adds one to the counter of (tail tile,
+// rank, quarter).  The warp that brings the counter to p.split sums the
+// tile's pieces in k order (piece 0 first): its own from tensor memory, the
+// others bulk-copied two chunks at a time into its 48 KB share of the ring
+// (red: its own barrier there).  It then applies the epilogue, stores C and
+// zeroes the counter.  Returns false if a bulk copy did not land in time.
+template <typename T>
+__device__ __forceinline__ bool pair_tail_piece(const PersistentParams& p, uint32_t taddr,
+                                                uint32_t tempty, int cluster_id, uint32_t rank,
+                                                int q, int lane, uint32_t red_buf,
+                                                uint32_t red_bar, uint32_t cbuf, int& buf,
+                                                const void* tmC, uint64_t c_policy, int row0,
+                                                int n0) {
+    const int64_t region = static_cast<int64_t>(rank * 4 + static_cast<uint32_t>(q)) *
+                           kPairWarpFloats;
+    float* const mine = p.ws + static_cast<int64_t>(cluster_id) * kPairSlotFloats + region;
+#pragma unroll 1
+    for (int j = 0; j < 4; ++j) {
+        uint32_t v[64];
+        tmem_ld_x64(taddr + static_cast<uint32_t>(64 * j), v);
+#pragma unroll
+        for (int g = 0; g < 16; ++g)
+            __stcg(reinterpret_cast<float4*>(mine + ((16 * j + g) * 32 + lane) * 4),
+                   make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                               __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])));
+    }
+    __threadfence();
+    __syncwarp();
+    const int S = p.split;
+    const int tail_tile = cluster_id / S;
+    const int own = cluster_id - tail_tile * S;  // this piece's place in k order
+    int last = 0;
+    if (lane == 0) {
+        uint32_t* cnt = p.counters + 8 * tail_tile + static_cast<int>(rank) * 4 + q;
+        const uint32_t before = atomic_add_acq_rel_gpu(cnt, 1u);
+        last = before + 1 == static_cast<uint32_t>(S) ? 1 : 0;
+        if (last) *cnt = 0u;  // zero again for the next launch
+    }
+    bool ok = true;
+    if (__shfl_sync(0xffffffffu, last, 0)) {
+        __threadfence();
+        const float* const first =
+            p.ws + static_cast<int64_t>(tail_tile) * S * kPairSlotFloats + region;
+#pragma unroll 1
+        for (int half = 0; half < 2 && ok; ++half) {
+            // the other pieces' chunks 2·half and 2·half + 1
+            if (lane == 0) {
+                fence_proxy_async_smem();  // earlier reads of the buffer come first
+                mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>(S - 1) * 2u *
+                                                   kPairChunkBytes);
+                int o = 0;
+                for (int s = 0; s < S; ++s) {
+                    if (s == own) continue;
+                    for (int jj = 0; jj < 2; ++jj)
+                        bulk_load(red_buf + static_cast<uint32_t>(2 * o + jj) * kPairChunkBytes,
+                                  first + s * kPairSlotFloats + (2 * half + jj) * 2048,
+                                  kPairChunkBytes, red_bar);
+                    ++o;
+                }
+                // copies in flight must land before anything else: no abort
+                ok = mbar_wait(red_bar, static_cast<uint32_t>(half), p.timeout_ns, nullptr);
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            mbar_wait(red_bar, static_cast<uint32_t>(half), p.timeout_ns, nullptr);  // lanes 1..31
+#pragma unroll 1
+            for (int jj = 0; jj < 2; ++jj) {
+                const int j = 2 * half + jj;
+                uint32_t v[64];
+                tmem_ld_x64(taddr + static_cast<uint32_t>(64 * j), v);
+                float x[64];
+                int o = 0;
+                for (int s = 0; s < S; ++s) {
+                    if (s == own) {
+#pragma unroll
+                        for (int t = 0; t < 64; ++t)
+                            x[t] = s == 0 ? __uint_as_float(v[t]) : x[t] + __uint_as_float(v[t]);
+                    } else {
+                        const uint32_t src = red_buf +
+                                             static_cast<uint32_t>(2 * o + jj) * kPairChunkBytes +
+                                             static_cast<uint32_t>(lane) * 16u;
+#pragma unroll
+                        for (int g = 0; g < 16; ++g) {
+                            const float4 a = ld_shared_f4(src + static_cast<uint32_t>(g) * 512u);
+                            x[4 * g] = s == 0 ? a.x : x[4 * g] + a.x;
+                            x[4 * g + 1] = s == 0 ? a.y : x[4 * g + 1] + a.y;
+                            x[4 * g + 2] = s == 0 ? a.z : x[4 * g + 2] + a.z;
+                            x[4 * g + 3] = s == 0 ? a.w : x[4 * g + 3] + a.w;
+                        }
+                        ++o;
+                    }
+                }
+                epilogue_math<T>(x, p.e, p.relu, row0 + lane, n0 + 64 * j, p.M, p.N);
+                epilogue_store<T>(x, cbuf, buf, tmC, c_policy, row0, n0 + 64 * j, p.M, p.N,
+                                  lane, p.out_f32 != 0);
+            }
+            __syncwarp();  // every lane is done reading the buffer
+        }
+    }
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(tempty);
+    return ok;
+}
 
 template <int STAGES, typename T = __half, int BK_ = 64>
 __global__ void __launch_bounds__(192, 1)
@@ -79,7 +199,8 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t bar_tfull = sBar + 16 * STAGES;
     const uint32_t bar_tempty = bar_tfull + 16;
     const uint32_t bar_drain = bar_tempty + 16;
-    const uint32_t slot_tmem = bar_drain + 8;
+    const uint32_t bar_red = bar_drain + 8;  // [4] split tail tiles: the epilogue warps' copies
+    const uint32_t slot_tmem = bar_red + 32;
     uint32_t* const tmem_slot_ptr = reinterpret_cast<uint32_t*>(base_ptr + (slot_tmem - base));
     volatile int* const abort_flag = reinterpret_cast<volatile int*>(tmem_slot_ptr + 1);
 
@@ -89,6 +210,7 @@ __global__ void __launch_bounds__(192, 1)
     const bool leader = rank == 0;
     const int cluster_id = static_cast<int>(blockIdx.x >> 1);
     const int nclusters = static_cast<int>(gridDim.x >> 1);
+    const int items = pair_item_count(cluster_id, p.num_tiles, nclusters, p.split);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -100,6 +222,7 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(bar_tempty + 8 * a, 8);
         }
         mbar_init(bar_drain, 1);
+        for (int e = 0; e < 4; ++e) mbar_init(bar_red + 8 * e, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -133,11 +256,14 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
             uint64_t last_issue = 0;
-            for (int tile = cluster_id; ok && tile < p.num_tiles; tile += nclusters) {
+            for (int i = 0; ok && i < items; ++i) {
+                int tile, kb0, kb1;
+                pair_item(cluster_id, i, p.num_tiles, nclusters, p.split, p.k_blocks, &tile, &kb0,
+                          &kb1);
                 const TileCoord tc = tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m);
                 const int ma = tc.m_blk * 256 + static_cast<int>(rank) * 128;
                 const int nb = tc.n_blk * 256 + static_cast<int>(rank) * 128;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.timeout_ns, abort_flag)) {
                         fail(kRoleProducer);
                         ok = false;
@@ -186,7 +312,10 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
-            for (int tile = cluster_id; ok && tile < p.num_tiles; tile += nclusters, ++it) {
+            for (; ok && it < items; ++it) {
+                int tile, kb0, kb1;
+                pair_item(cluster_id, it, p.num_tiles, nclusters, p.split, p.k_blocks, &tile,
+                          &kb0, &kb1);
                 const int acc = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
@@ -195,7 +324,7 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 256);
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(bar_full + 8 * stage, phase, p.timeout_ns, abort_flag)) {
                         fail(kRoleMma);
                         ok = false;
@@ -211,7 +340,8 @@ __global__ void __launch_bounds__(192, 1)
                         const uint64_t adesc =
                             smem_desc_sw128(a0 + 16384 * (k / 4) + 32 * (k % 4), 16, 1024);
                         const uint64_t bdesc = smem_desc_sw128(b0 + 2048 * k, kBBytes / 2, 1024);
-                        mma_f16_ss_pair(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+                        mma_f16_ss_pair(d_tmem, adesc, bdesc, idesc,
+                                        (kb != kb0 || k != 0) ? 1u : 0u);
                     }
                     mma_commit_pair_mc(bar_empty + 8 * stage, 0x3);
                     if (++stage == STAGES) {
@@ -234,7 +364,10 @@ __global__ void __launch_bounds__(192, 1)
         const uint64_t c_policy = policy_evict_first();  // C is written once, never reread
         int buf = 0;
         int it = 0;
-        for (int tile = cluster_id; tile < p.num_tiles; tile += nclusters, ++it) {
+        for (; it < items; ++it) {
+            int tile, kb0, kb1;
+            pair_item(cluster_id, it, p.num_tiles, nclusters, p.split, p.k_blocks, &tile, &kb0,
+                      &kb1);
             const TileCoord tc = tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m);
             const int row0 = tc.m_blk * 256 + static_cast<int>(rank) * 128 + 32 * q;
             const int n0 = tc.n_blk * 256;
@@ -249,6 +382,19 @@ __global__ void __launch_bounds__(192, 1)
                 break;
             }
             tc_fence_after_sync();
+            if (kb1 - kb0 < p.k_blocks) {
+                // A piece of a split tail tile: this warp's 32 rows × 256
+                // columns of fp32 partial go to the cluster's slot; the warp
+                // whose add completes the tile's count sums the slots.
+                const uint32_t e = static_cast<uint32_t>(warp - 2);
+                if (!pair_tail_piece<T>(p, tmem_base + lane_addr + static_cast<uint32_t>(acc * 256),
+                                        mapa_shared(bar_tempty + 8 * acc, 0), cluster_id, rank,
+                                        q, lane, sA + e * kPairRedBytes, bar_red + 8 * e, cbuf,
+                                        buf, &tmC, c_policy, row0, n0) &&
+                    lane == 0)
+                    fail(kRoleEpilogue);
+                continue;
+            }
 #pragma unroll 1
             for (int j = 0; j < 4; ++j) {
                 uint32_t v0[32], v1[32];

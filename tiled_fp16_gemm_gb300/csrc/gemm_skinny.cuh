@@ -181,16 +181,6 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
         : "memory");
 }
 
-// Returns the old value; orders this thread's earlier writes before the add
-// and its later reads after it, at GPU scope.
-__device__ __forceinline__ uint32_t atomic_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
-    uint32_t old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
-                 : "=r"(old)
-                 : "l"(p), "r"(v)
-                 : "memory");
-    return old;
-}
 
 // The kernel body shared by the fp16/bf16 kernel (QB = false: B^T tiles by
 // TMA) and the MXFP4 kernel (QB = true: B^T tiles decoded by warps 6..13).
@@ -807,39 +797,42 @@ inline cudaError_t skinny_mx_launch_kernel(const CUtensorMap& tmBq, const CUtens
                               tmS, prm);
 }
 
-struct SkinnyWorkspace {
+struct SplitkWorkspace {
     float* partials = nullptr;    // two slots per CTA
     uint32_t* counters = nullptr;  // four per CTA
     int64_t ctas = 0;
 };
 
-inline std::mutex& skinny_ws_mutex() {
+inline std::mutex& splitk_ws_mutex() {
     static std::mutex m;
     return m;
 }
 
-inline std::map<std::pair<int, cudaStream_t>, SkinnyWorkspace>& skinny_ws_map() {
-    static std::map<std::pair<int, cudaStream_t>, SkinnyWorkspace> m;
+inline std::map<std::pair<int, cudaStream_t>, SplitkWorkspace>& splitk_ws_map() {
+    static std::map<std::pair<int, cudaStream_t>, SplitkWorkspace> m;
     return m;
 }
 
 // After a launch gave up on a wait, some tiles' counters may never have
 // reached their piece count (and been zeroed): reset every workspace's
 // counters on this device (the device is idle).
-inline void skinny_reset_counters(int dev) {
-    std::lock_guard<std::mutex> lk(skinny_ws_mutex());
-    for (auto& kv : skinny_ws_map())
+inline void splitk_reset_counters(int dev) {
+    std::lock_guard<std::mutex> lk(splitk_ws_mutex());
+    for (auto& kv : splitk_ws_map())
         if (kv.first.first == dev && kv.second.counters != nullptr)
             cudaMemset(kv.second.counters, 0, 4 * kv.second.ctas * sizeof(uint32_t));
 }
 
 // The split-K workspace of (dev, stream) into prm (ws, counters); sized on
-// first use for the largest grid, so later calls never grow it.
-inline tg_status_t skinny_workspace(int dev, cudaStream_t stream, int64_t grid, int64_t max_ctas,
+// first use for the largest grid, so later calls never grow it.  The pair
+// kernel's split tail tiles use it too (one 256 KB slot per cluster, eight
+// counters per tail tile: within the same bytes for a grid of one CTA per
+// SM); launches on one stream are ordered, so they never share it at once.
+inline tg_status_t splitk_workspace(int dev, cudaStream_t stream, int64_t grid, int64_t max_ctas,
                                     SkinnyParams* prm) {
     {
-        std::lock_guard<std::mutex> lk(skinny_ws_mutex());
-        SkinnyWorkspace& ws = skinny_ws_map()[std::make_pair(dev, stream)];
+        std::lock_guard<std::mutex> lk(splitk_ws_mutex());
+        SplitkWorkspace& ws = splitk_ws_map()[std::make_pair(dev, stream)];
         if (ws.ctas < grid) {
             // First use on this stream: room for the largest grid (one CTA
             // per SM), so later calls, graph captures included, never grow it.
@@ -893,7 +886,7 @@ inline tg_status_t skinny_launch(const void* A, const void* B, void* C, const tg
         return TG_ERR_LAUNCH;
 
     SkinnyParams prm;
-    const tg_status_t wst = skinny_workspace(dev, stream, pl.grid, max_ctas, &prm);
+    const tg_status_t wst = splitk_workspace(dev, stream, pl.grid, max_ctas, &prm);
     if (wst != TG_OK) return wst;
     prm.M = static_cast<int32_t>(M);
     prm.N = static_cast<int32_t>(N);
@@ -939,7 +932,7 @@ inline tg_status_t skinny_mx_launch(const void* A, const void* Bq, const void* S
                 CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CU_TENSOR_MAP_SWIZZLE_128B))
         return TG_ERR_LAUNCH;
     SkinnyParams prm;
-    const tg_status_t wst = skinny_workspace(dev, stream, pl.grid, max_ctas, &prm);
+    const tg_status_t wst = splitk_workspace(dev, stream, pl.grid, max_ctas, &prm);
     if (wst != TG_OK) return wst;
     prm.M = static_cast<int32_t>(M);
     prm.N = static_cast<int32_t>(N);

@@ -93,14 +93,19 @@ void plan_pair(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* p) {
     p->tiles_n = ceil_div(N, 256);
     p->k_blocks = ceil_div(K, kPairBK);
     p->num_tiles = p->tiles_m * p->tiles_n;
-    const int64_t pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
-    p->grid = 2 * (p->num_tiles < pairs ? p->num_tiles : pairs);
+    const int32_t pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
+    int32_t P = 1, S = 1;
+    tg::pair_launch_shape(static_cast<int32_t>(p->num_tiles), pairs,
+                          static_cast<int32_t>(p->k_blocks), &P, &S);
+    p->grid = 2 * int64_t{P};
     p->threads = 192;
     p->group_m = static_cast<int32_t>(p->tiles_m < kPairGroupM ? p->tiles_m : kPairGroupM);
     p->smem_bytes = PairCfgT::kSmemBytes;
     p->ring_bytes = 2 * tg_ring_bytes(128, 128, kPairBK, kPairStages, 2);  // both CTAs
-    p->split_k = 1;
-    p->workspace_bytes = 0;
+    // pieces per tile of the last wave, and the partial slots and counters
+    // they use (tile_schedule.h)
+    p->split_k = S;
+    p->workspace_bytes = S > 1 ? int64_t{P} * tg::kPairSlotFloats * 4 + 8 * int64_t{P} * 4 : 0;
     p->cluster = 2;
 }
 
@@ -317,17 +322,34 @@ tg_status_t launch_persistent(const void* A, const void* B, void* C, const tg_pl
 
 // The pair kernel: clusters of two CTAs, at most as many pairs as the device
 // holds at once (the launch is persistent, so no pair waits for another).
+// The last, partial wave of tiles is split along k when that leaves fewer
+// pairs idle (tile_schedule.h); its partial sums use the stream's split-K
+// workspace, which is set up on the first pair launch on the stream whether
+// or not that launch splits, so a later launch inside a graph capture finds
+// it.  Without a workspace the wave is not split.
 template <typename T>
 tg_status_t launch_pair(const void* A, const void* B, void* C, const tg_plan_t& pl, int64_t M,
                         int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
-                        const tg::EpilogueSpec& ep, cudaStream_t stream, int max_pairs) {
+                        const tg::EpilogueSpec& ep, cudaStream_t stream, int dev,
+                        const DeviceState* ds) {
     CUtensorMap tmA, tmB, tmC;
     if (!encode_abc<T>(&tmA, &tmB, &tmC, A, B, C, M, N, K, lda, ldb, ldc, ep.out_f32 != 0,
                        kPairBK))
         return TG_ERR_LAUNCH;
-    const tg::PersistentParams prm = persistent_params(pl, M, N, K, ep);
-    int64_t pairs = pl.grid / 2;
-    if (pairs > max_pairs) pairs = max_pairs;
+    tg::PersistentParams prm = persistent_params(pl, M, N, K, ep);
+    int32_t pairs = ds->num_sms / 2 < ds->max_pairs ? ds->num_sms / 2 : ds->max_pairs;
+    int32_t P = 1, S = 1;
+    tg::pair_launch_shape(prm.num_tiles, pairs, prm.k_blocks, &P, &S);
+    tg::SkinnyParams wsp;
+    if (tg::splitk_workspace(dev, stream, ds->num_sms, ds->num_sms, &wsp) == TG_OK &&
+        int64_t{P} * tg::kPairSlotFloats <= 2 * int64_t{ds->num_sms} * tg::kSkSlotFloats &&
+        8 * P <= 4 * ds->num_sms) {
+        prm.ws = wsp.ws;
+        prm.counters = wsp.counters;
+    } else if (S > 1) {
+        tg::pair_launch_shape(prm.num_tiles, pairs, 0, &P, &S);  // no split
+    }
+    prm.split = S;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -336,7 +358,7 @@ tg_status_t launch_pair(const void* A, const void* B, void* C, const tg_plan_t& 
     tg::set_dependent_launch(attr[1]);
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * P));
     cfg.blockDim = dim3(PairCfgT::kThreads);
     cfg.dynamicSmemBytes = PairCfgT::kSmemBytes;
     cfg.stream = stream;
@@ -470,8 +492,7 @@ tg_status_t launch_planned(tg_plan_t pl, const void* A, const void* B, void* C, 
                     plan_persistent(M, N, K, ds->num_sms, kBigBN, kBigStages,
                                     tg::PersistentCfg<kBigBN, kBigStages>::kSmemBytes, &pl);
                 } else {
-                    return launch_pair<T>(A, B, C, pl, M, N, K, lda, ldb, ldc, ep, s,
-                                          ds->max_pairs);
+                    return launch_pair<T>(A, B, C, pl, M, N, K, lda, ldb, ldc, ep, s, dev, ds);
                 }
             }
             if (pl.bn == kBigBN)
@@ -991,7 +1012,7 @@ tg_status_t tg_sync_status(void* stream) {
         cudaDeviceSynchronize();
         const unsigned int zero = 0;
         cudaMemcpyToSymbol(tg::g_wait_timeout_flags, &zero, sizeof(zero));
-        tg::skinny_reset_counters(dev);
+        tg::splitk_reset_counters(dev);
         noalloc_reset_counters(dev);
         cudaGetLastError();
         return TG_ERR_TIMEOUT;

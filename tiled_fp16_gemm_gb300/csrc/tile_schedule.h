@@ -48,4 +48,53 @@ TG_HD int64_t unit_owner(int64_t u, int64_t num_ctas, int64_t total_units) {
     return ((u + 1) * num_ctas + total_units - 1) / total_units - 1;
 }
 
+// The pair kernel's work items.  With T tiles on P clusters, W = T / P full
+// waves are walked as above (cluster c takes tiles c, c + P, ...).  The
+// R = T - W·P tiles of the last, partial wave are cut into S pieces along k:
+// cluster c < R·S takes piece c % S (k blocks [KB·j/S, KB·(j+1)/S) for
+// j = c % S) of tile W·P + c / S.  S = 1 leaves the last wave whole.
+// Splitting a k range leaves fewer clusters idle in that wave; the pieces'
+// fp32 partials are summed in k order by whichever piece finishes last.
+constexpr int32_t kPairMaxSplit = 4;         // pieces per tail tile at most
+constexpr int32_t kPairMinPieceBlocks = 8;   // k blocks per piece at least
+
+// Clusters P to launch and pieces S per tail tile, for T tiles of KB k blocks
+// on at most `pairs` clusters.  Always R·S <= P.
+TG_HD void pair_launch_shape(int32_t T, int32_t pairs, int32_t KB, int32_t* P, int32_t* S) {
+    const int32_t R = T >= pairs ? T % pairs : T;
+    int32_t s = 1;
+    if (R > 0) {
+        s = pairs / R;
+        if (s > kPairMaxSplit) s = kPairMaxSplit;
+        const int32_t kmax = KB / kPairMinPieceBlocks;
+        if (s > kmax) s = kmax;
+        if (s < 1) s = 1;
+    }
+    *S = s;
+    *P = T >= pairs ? pairs : (T * s < pairs ? T * s : pairs);
+}
+
+// Number of work items of cluster c.
+TG_HD int32_t pair_item_count(int32_t c, int32_t T, int32_t P, int32_t S) {
+    const int32_t W = T / P;
+    const int32_t R = T - W * P;
+    return W + (c < R * S ? 1 : 0);
+}
+
+// Item i of cluster c: its tile and k-block range [kb0, kb1).
+TG_HD void pair_item(int32_t c, int32_t i, int32_t T, int32_t P, int32_t S, int32_t KB,
+                     int32_t* tile, int32_t* kb0, int32_t* kb1) {
+    const int32_t W = T / P;
+    if (i < W) {
+        *tile = c + i * P;
+        *kb0 = 0;
+        *kb1 = KB;
+    } else {
+        const int32_t j = c % S;
+        *tile = W * P + c / S;
+        *kb0 = KB * j / S;
+        *kb1 = KB * (j + 1) / S;
+    }
+}
+
 }  // namespace tg
