@@ -136,6 +136,16 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot_ptr;
+    if (warp == 0 && lane == 0 && static_cast<int>(blockIdx.x) < p.num_tiles) {
+        // the first ring's worth of this CTA's operand tiles into L2 while
+        // the previous kernel finishes
+        const TileCoord tc = tile_coord(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m);
+        for (int kb = 0; kb < STAGES && kb < p.k_blocks; ++kb) {
+            tma_prefetch_2d(&tmA, kb * BK, tc.m_blk * BM);
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_prefetch_2d(&tmB, tc.n_blk * BN + 64 * j, kb * BK);
+        }
+    }
     grid_dependency_wait();  // the previous kernel's writes are visible from here on
     grid_launch_dependents();
 

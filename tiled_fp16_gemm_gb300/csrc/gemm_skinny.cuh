@@ -264,6 +264,30 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot_ptr;
+    if (warp == 0 && lane == 0) {
+        // the first ring's worth of this CTA's units into L2 while the
+        // previous kernel finishes
+        int32_t t = static_cast<int32_t>(u_begin / KB);
+        int32_t kb = static_cast<int32_t>(u_begin - static_cast<int64_t>(t) * KB);
+        constexpr int kAhead = QB ? mx_raw_stages(MP_MAX) : kSkStages;
+        for (int i = 0; i < kAhead && u_begin + i < u_end; ++i) {
+            if constexpr (QB) {
+#pragma unroll
+                for (int h = 0; h < BK / 64; ++h)
+                    tma_prefetch_2d(tmB, kb * (BK / 2) + 32 * h, t * 128);
+                tma_prefetch_2d(tmS, t * 128, kb * (BK / 32));
+            } else {
+                tma_prefetch_2d(tmB, t * 128, kb * BK);
+                tma_prefetch_2d(tmB, t * 128 + 64, kb * BK);
+            }
+#pragma unroll
+            for (int h = 0; h < BK / 64; ++h) tma_prefetch_2d(tmA, kb * BK + 64 * h, 0);
+            if (++kb == static_cast<int32_t>(KB)) {
+                kb = 0;
+                ++t;
+            }
+        }
+    }
     grid_dependency_wait();  // the previous kernel's writes are visible from here on
     grid_launch_dependents();
 

@@ -154,6 +154,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
+// L2 prefetch of one box of a 2-D tensor map.  A prefetch only fills L2,
+// which every SM and TMA unit reads through, so it may be issued before
+// grid_dependency_wait(): the loads after the wait still see the previous
+// kernel's writes.
+__device__ __forceinline__ void tma_prefetch_2d(const void* desc, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(desc),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
