@@ -255,7 +255,15 @@ def test_plans(tg):
     assert s.kernel == tg.TG_KERNEL_SKINNY
     assert (s.mma_m, s.mma_n) == (128, 64) and s.tiles_n == 128
     assert (s.bk, s.k_blocks, s.stages) == (64, 128, 9)
-    assert s.grid == 152 and s.workspace_bytes > 0 and s.smem_bytes <= 232448
+    # 128 tiles: one CTA per whole tile (no partial sums)
+    assert s.grid == 128 and s.split_k == 1 and s.workspace_bytes > 0
+    assert s.smem_bytes <= 232448
+    # 224 tiles: two whole tiles per CTA; 64 tiles: two equal k pieces each;
+    # 86 tiles (no aligned grid reaches 0.7 of the SMs): balanced over 152
+    assert tg.tg_plan_f16(128, 28672, 4096, 152).grid == 112
+    h = tg.tg_plan_f16(64, 8192, 8192, 152)
+    assert h.grid == 128 and h.split_k == 2
+    assert tg.tg_plan_f16(64, 11008, 4096, 152).grid == 152
     w = tg.tg_plan_f16(128, 16384, 8192, 152)  # Mp = 128: 64-k units, 6 stages
     assert w.kernel == tg.TG_KERNEL_SKINNY and (w.bk, w.k_blocks, w.stages) == (64, 128, 6)
     assert w.smem_bytes <= 232448

@@ -695,9 +695,33 @@ inline bool skinny_applies(int64_t M, int64_t N, int64_t K) {
     return M >= 1 && M <= 128;
 }
 
+// A grid that cuts the units only at tile edges or at equal fractions of a
+// tile: T / d CTAs of d whole tiles each (d divides T), or T · s CTAs of one
+// 1/s k-range each, whichever is closer to num_sms; 0 if neither reaches
+// 0.7 num_sms or would give a CTA fewer than kSkMinUnitsPerCta units.  Each
+// CTA then streams whole tiles (no partial sums) or one equal piece of one.
+inline int64_t skinny_aligned_grid(int64_t T, int64_t KB, int32_t num_sms) {
+    int64_t best = 0;
+    for (int64_t d = 1; d <= T; ++d)
+        if (T % d == 0 && T / d <= num_sms) {
+            best = T / d;
+            break;
+        }
+    const int64_t s = T > 0 ? num_sms / T : 0;
+    if (s >= 2 && KB / s >= kSkMinUnitsPerCta && T * s > best) best = T * s;
+    if (10 * best < 7 * static_cast<int64_t>(num_sms)) return 0;
+    if (T * KB / best < kSkMinUnitsPerCta) return 0;
+    return best;
+}
+
 // Units of bk k (the fp16/bf16 kernel: SkinnyNarrow/Wide::kBK; MXFP4: kMxBK).
+// align: take skinny_aligned_grid when it applies.  The fp16/bf16 kernel is
+// bound by streaming B, and on 64×16384×8192 one CTA per whole tile (128
+// CTAs) measured 43.0 µs against 48.8 µs for 152 CTAs with pieces; on
+// 128×28672×4096 two whole tiles per CTA (112 CTAs) 47.0 against 53.4 µs.
+// The MXFP4 kernel is paced by its MMA thread, so it keeps every SM busy.
 inline void skinny_plan_bk(int64_t M, int64_t N, int64_t K, int32_t num_sms, int32_t bk,
-                           tg_plan_t* pl) {
+                           tg_plan_t* pl, bool align = false) {
     const int64_t Mp = (M + 15) / 16 * 16;
     const bool narrow = Mp <= 64;
     pl->kernel = TG_KERNEL_SKINNY;
@@ -715,6 +739,11 @@ inline void skinny_plan_bk(int64_t M, int64_t N, int64_t K, int32_t num_sms, int
     int64_t G = U / kSkMinUnitsPerCta;
     if (G < 1) G = 1;
     if (G > num_sms) G = num_sms;
+    int64_t aligned = 0;
+    if (align) {
+        aligned = skinny_aligned_grid(pl->tiles_n, pl->k_blocks, num_sms);
+        if (aligned > 0) G = aligned;
+    }
     pl->grid = G;
     pl->threads = narrow ? skinny_threads(SkinnyNarrow::kStages, 64, false)
                          : skinny_threads(SkinnyWide::kStages, 128, false);
@@ -722,9 +751,13 @@ inline void skinny_plan_bk(int64_t M, int64_t N, int64_t K, int32_t num_sms, int
     pl->smem_bytes = narrow ? SkinnyNarrow::kSmemBytes : SkinnyWide::kSmemBytes;
     pl->ring_bytes = narrow ? int64_t{SkinnyNarrow::kStages} * SkinnyNarrow::kStageBytes
                             : int64_t{SkinnyWide::kStages} * SkinnyWide::kStageBytes;
-    // most CTAs touching one tile: its k range over the shortest unit range, plus one
+    // most CTAs touching one tile: exact for an aligned grid; else its k range
+    // over the shortest unit range, plus one
     const int64_t shortest = U / G;
-    pl->split_k = shortest > 0 ? (pl->k_blocks + shortest - 1) / shortest + 1 : pl->k_blocks;
+    if (aligned > 0)
+        pl->split_k = G <= pl->tiles_n ? 1 : G / pl->tiles_n;
+    else
+        pl->split_k = shortest > 0 ? (pl->k_blocks + shortest - 1) / shortest + 1 : pl->k_blocks;
     if (pl->split_k > G) pl->split_k = G;
     pl->workspace_bytes = 2 * G * kSkSlotFloats * 4 + 4 * G * 4;
     pl->cluster = 1;
@@ -732,7 +765,7 @@ inline void skinny_plan_bk(int64_t M, int64_t N, int64_t K, int32_t num_sms, int
 
 inline void skinny_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* pl) {
     const bool narrow = (M + 15) / 16 * 16 <= 64;
-    skinny_plan_bk(M, N, K, num_sms, narrow ? SkinnyNarrow::kBK : SkinnyWide::kBK, pl);
+    skinny_plan_bk(M, N, K, num_sms, narrow ? SkinnyNarrow::kBK : SkinnyWide::kBK, pl, true);
 }
 
 // The MXFP4 kernel: the same units and split, its own rings and 448 threads.
