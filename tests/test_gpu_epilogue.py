@@ -161,9 +161,10 @@ VARIANTS = [  # (relu, bias, residual, out)
     (True, True, True, "f32"),
 ]
 # 512×512×4096 and 300×700×2048: the pair kernel splits its tiles along k
-# (4 and 2 pieces), so the epilogue runs on summed partials
+# (4 and 2 pieces), so the epilogue runs on summed partials; 64×4096×4096: the
+# skinny kernel's aligned grid (32 tiles in 4 equal k pieces)
 SHAPES = [(1, 1, 1), (129, 127, 1000), (300, 1000, 129), (64, 2048, 520), (257, 513, 65),
-          (512, 512, 4096), (300, 700, 2048)]
+          (512, 512, 4096), (300, 700, 2048), (64, 4096, 4096)]
 
 
 @pytest.mark.parametrize("fmt", ["f16", "bf16"])
