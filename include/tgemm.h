@@ -71,9 +71,13 @@ typedef enum {
  * That costs one extra read and write of the staged matrices.  C must not
  * overlap A or B (not checked).
  * Ownership: the caller owns A, B and C; the library keeps no reference past
- * the work it enqueued on `stream`.  The library owns a small split-K
- * workspace per (device, stream), allocated on first use and kept until
- * process exit.
+ * the work it enqueued on `stream`.  The library owns a split-K workspace
+ * per (device, stream): two 64 KB fp32 slots and four counter words per SM
+ * (about 20 MB on 152 SMs), allocated by the first call on that stream that
+ * runs the M <= 128 kernel or the CTA-pair kernel, and kept until process
+ * exit.  If it cannot be allocated, an M <= 128 call returns
+ * TG_ERR_NO_MEMORY and a pair-kernel call runs without splitting its last
+ * wave of tiles.
  * Errors: argument errors are returned before anything is enqueued.  Launch
  * failures return TG_ERR_LAUNCH.  A kernel that gives up on a bounded wait
  * records the fact on the device; tg_sync_status reports it.
@@ -82,11 +86,14 @@ typedef enum {
  * TGEMM_FORCE_CFG = pair256 | persistent256 | persistent128 | skinny
  * overrides it where the forced kernel applies, and TGEMM_GROUP_M sets the
  * raster group height (both for tests and tile sweeps).
- * CUDA graphs: once one call has run on a stream outside capture (the first
- * call per stream allocates that stream's split-K workspace), calls on that
- * stream can be captured; a graph holding an M <= 128 call uses the capturing
- * stream's workspace, so it must not run concurrently with other libtgemm
- * work on that stream.
+ * CUDA graphs: once a call that runs the M <= 128 kernel or the CTA-pair
+ * kernel has run on a stream outside capture (allocating that stream's
+ * split-K workspace), calls on that stream can be captured; a graph holding
+ * such a call uses the capturing stream's workspace, so it must not run
+ * concurrently with other libtgemm work on that stream.
+ * Kernels are launched with programmatic dependent launch: each may start its
+ * set-up while the previous kernel on the stream finishes, and waits for that
+ * kernel's completion before it reads or writes global memory.
  */
 tg_status_t tg_gemm_f16(const void* A, const void* B, void* C,
                         int64_t M, int64_t N, int64_t K,
@@ -290,8 +297,9 @@ typedef struct {
     int32_t group_m;      /* raster: tiles_m blocks walked per group            */
     int64_t smem_bytes;   /* dynamic shared memory per CTA                      */
     int64_t ring_bytes;   /* of which the operand ring                          */
-    int64_t split_k;      /* k-ranges per output tile (skinny: maximum)         */
-    int64_t workspace_bytes; /* device scratch needed (skinny split-K)          */
+    int64_t split_k;      /* k-ranges per output tile (skinny: maximum; CTA   */
+                          /* pairs: pieces per tile of the last wave)           */
+    int64_t workspace_bytes; /* device scratch used (split-K partial sums)      */
     int32_t cluster;      /* CTAs per cluster: 2 = tcgen05 CTA pair (256-row MMA) */
     int32_t reserved;
 } tg_plan_t;
