@@ -504,7 +504,7 @@ def run_ours(args, w, rank, world, local_rank):
                    "isolated_launch_ms_min": min(per6), "tflops": mw.flops / (k6 / 1e3) / 1e12}
             if mw.M <= 128:
                 gbs = mw.min_bytes / (k6 / 1e3) / 1e9
-                ent["kernel"] = "tg_gemm_mxfp4_skinny (codes decoded in shared memory)"
+                ent["kernel"] = "tg_gemm_mxfp4_skinny (codes decoded by converter warps into tensor memory)"
                 ent["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak,
                                    "unit": "GB/s", "frac": gbs / hbm_peak,
                                    "traffic": stored_traffic(f"mxfp4_skinny:{mname}"),
