@@ -300,7 +300,8 @@ typedef struct {
     int64_t split_k;      /* k-ranges per output tile (skinny: maximum; CTA   */
                           /* pairs: pieces per tile of the last wave)           */
     int64_t workspace_bytes; /* device scratch used (split-K partial sums)      */
-    int32_t cluster;      /* CTAs per cluster: 2 = tcgen05 CTA pair (256-row MMA) */
+    int32_t cluster;      /* CTAs per cluster: 2 = tcgen05 CTA pair (256-row MMA); */
+                          /* M <= 128: 4 = a tile's four k-pieces together     */
     int32_t reserved;
 } tg_plan_t;
 

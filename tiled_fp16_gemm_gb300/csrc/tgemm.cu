@@ -1284,7 +1284,7 @@ extern "C" tg_status_t tg_gemm_f16_noalloc(const void* A, const void* B, void* C
     prm.C = C;
     prm.ldc = ldc;
 
-    if (tg::skinny_launch_kernel<__half>(tmB, tmA, prm, pl.grid, s) != cudaSuccess) {
+    if (tg::skinny_launch_kernel<__half>(tmB, tmA, prm, pl.grid, s, pl.cluster) != cudaSuccess) {
         cudaGetLastError();
         return TG_ERR_LAUNCH;
     }
