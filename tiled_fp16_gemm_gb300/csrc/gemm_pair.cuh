@@ -22,6 +22,12 @@
 // A cluster barrier after set-up (barriers initialised, TMEM allocated) and
 // before exit (no peer still reads or signals this CTA) brackets the work.
 //
+// Work items (tile_schedule.h, pair_item): each pair walks its share of the
+// full waves of tiles; the tiles of a last, partial wave may be cut along k
+// into pieces run by otherwise idle pairs.  A piece's epilogue
+// (pair_tail_piece) writes an fp32 partial and counts itself in; the last
+// piece of a tile sums them in k order and stores C.
+//
 // Structure: producer warp / MMA warp / four epilogue warps as in the
 // one-CTA kernel (gemm_persistent.cuh), which follows the warp-specialised
 // TMA + mbarrier ring of "TileLang：比 Triton 低一层的 tile 语言", section
