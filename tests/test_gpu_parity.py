@@ -155,11 +155,12 @@ def test_ragged_shapes(tg, M, N, K, relu, forced):
     check(C, oracle.gemm(A, B, M, N, K, relu=relu), K, relu=relu, what=f"{M}x{N}x{K}")
 
 
-# (64, 4096, 4096): 32 tiles in 4 equal k pieces on 128 CTAs; (16, 14336, 4096): 112
-# CTAs of one whole tile each (the aligned grids); the rest split units evenly
+# (64, 4096, 4096) and (128, 4096, 8192): 32 tiles in 4 equal k pieces on 128 CTAs,
+# launched as clusters of a tile's 4 pieces; (16, 14336, 4096): 112 CTAs of one whole tile
+# each (the aligned grids); the rest split units evenly
 SKINNY = [(1, 300, 1000), (128, 4096, 333), (17, 129, 64), (64, 1000, 1000), (100, 8, 5000),
           (33, 2048, 4096), (64, 16384, 256), (128, 128, 8192), (5, 17, 13), (64, 4096, 4096),
-          (16, 14336, 4096)]
+          (16, 14336, 4096), (128, 4096, 8192)]
 
 
 @pytest.mark.parametrize("M,N,K", SKINNY, ids=[f"{m}x{n}x{k}" for m, n, k in SKINNY])
