@@ -765,6 +765,8 @@ inline void skinny_plan_bk(int64_t M, int64_t N, int64_t K, int32_t num_sms, int
     // 16.1 µs, 128×4096×14336 37.1 -> 33.8 µs, 32×4096×14336 24.8 -> 24.2 µs,
     // M = 1 and 16 unchanged.  Whole-tile grids took 0.5 % longer that way and
     // 2 or 3 pieces per tile gained nothing, so they launch without clusters.
+    // The launch drops the clusters if not all of them fit on the device at
+    // once (a second round of clusters would double the time).
     pl->cluster = (aligned > 0 && G == 4 * pl->tiles_n) ? 4 : 1;
 }
 

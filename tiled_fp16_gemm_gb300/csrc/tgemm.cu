@@ -118,6 +118,10 @@ struct DeviceState {
     bool attrs_set = false;
     int max_pairs = 0;  // CTA pairs of the pair kernel that fit on the device at once
     int max_sp_pairs = 0;  // the same for the 2:4 sparse pair kernel
+    // clusters of four CTAs of the skinny kernel (Mp <= 64, Mp <= 128) that
+    // fit at once; the planner's clusters of a tile's four k-pieces are used
+    // only when all of them do
+    int max_skinny_quads[2] = {0, 0};
 };
 
 std::mutex g_dev_mutex;
@@ -163,19 +167,19 @@ cudaError_t set_kernel_attributes() {
     return e;
 }
 
-// How many clusters of two CTAs of `kernel` can be resident together
-// (clusters must sit inside one GPC, so this can be below num_sms / 2);
+// How many clusters of `size` CTAs of `kernel` can be resident together
+// (clusters must sit inside one GPC, so this can be below num_sms / size);
 // 0 if the query fails.
 template <typename Kernel>
-int max_active_pairs(Kernel kernel, int threads, uint32_t smem, int num_sms) {
+int max_active_clusters(Kernel kernel, int threads, uint32_t smem, int num_sms, int size) {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(size);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * (num_sms / 2)));
+    cfg.gridDim = dim3(static_cast<unsigned>(size * (num_sms / size)));
     cfg.blockDim = dim3(static_cast<unsigned>(threads));
     cfg.dynamicSmemBytes = smem;
     cfg.attrs = attr;
@@ -217,11 +221,21 @@ tg_status_t current_device(int* dev, DeviceState** st) {
             cudaGetLastError();
             return TG_ERR_LAUNCH;
         }
-        s.max_pairs = max_active_pairs(tg::tg_gemm_f16_pair<kPairStages, __half, kPairBK>,
-                                       PairCfgT::kThreads, PairCfgT::kSmemBytes, s.num_sms);
-        s.max_sp_pairs = max_active_pairs(tg::tg_gemm_sp24_pair<kSpPairStages, __half>,
-                                          tg::SparsePairCfg<kSpPairStages>::kThreads,
-                                          tg::SparsePairCfg<kSpPairStages>::kSmemBytes, s.num_sms);
+        s.max_pairs = max_active_clusters(tg::tg_gemm_f16_pair<kPairStages, __half, kPairBK>,
+                                          PairCfgT::kThreads, PairCfgT::kSmemBytes, s.num_sms, 2);
+        s.max_sp_pairs = max_active_clusters(tg::tg_gemm_sp24_pair<kSpPairStages, __half>,
+                                             tg::SparsePairCfg<kSpPairStages>::kThreads,
+                                             tg::SparsePairCfg<kSpPairStages>::kSmemBytes,
+                                             s.num_sms, 2);
+        using NarrowCfg = tg::SkinnyNarrow;
+        using WideCfg = tg::SkinnyWide;
+        s.max_skinny_quads[0] = max_active_clusters(
+            tg::tg_gemm_f16_skinny<NarrowCfg::kStages, 64, __half, NarrowCfg::kBK>,
+            tg::skinny_threads(NarrowCfg::kStages, 64, false), NarrowCfg::kSmemBytes, s.num_sms,
+            4);
+        s.max_skinny_quads[1] = max_active_clusters(
+            tg::tg_gemm_f16_skinny<WideCfg::kStages, 128, __half, WideCfg::kBK>,
+            tg::skinny_threads(WideCfg::kStages, 128, false), WideCfg::kSmemBytes, s.num_sms, 4);
         s.attrs_set = true;
     }
     *dev = d;
@@ -503,6 +517,9 @@ tg_status_t launch_planned(tg_plan_t pl, const void* A, const void* B, void* C, 
         case TG_KERNEL_SKINNY: {
             const uint64_t timeout = g_timeout_ns.load();
             const int32_t inject = g_inject.exchange(0);
+            // clusters of a tile's four k-pieces only if all of them fit at once
+            if (pl.cluster == 4 && pl.grid / 4 > ds->max_skinny_quads[pl.mma_n > 64 ? 1 : 0])
+                pl.cluster = 1;
             return tg::skinny_launch<T>(A, B, C, pl, M, N, K, lda, ldb, ldc, ep, s, dev,
                                         ds->num_sms, timeout, inject, encode_2d);
         }
@@ -1284,7 +1301,9 @@ extern "C" tg_status_t tg_gemm_f16_noalloc(const void* A, const void* B, void* C
     prm.C = C;
     prm.ldc = ldc;
 
-    if (tg::skinny_launch_kernel<__half>(tmB, tmA, prm, pl.grid, s, pl.cluster) != cudaSuccess) {
+    const int32_t cluster =
+        pl.cluster == 4 && pl.grid / 4 <= ds->max_skinny_quads[Mp > 64 ? 1 : 0] ? 4 : 1;
+    if (tg::skinny_launch_kernel<__half>(tmB, tmA, prm, pl.grid, s, cluster) != cudaSuccess) {
         cudaGetLastError();
         return TG_ERR_LAUNCH;
     }
