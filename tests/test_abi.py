@@ -302,3 +302,26 @@ def test_schedule_bruteforce_cpp(tmp_path):
                     os.path.join(ROOT, "tests", "sched_check.cpp"), "-o", exe], check=True)
     r = subprocess.run([exe], capture_output=True, text=True)
     assert r.returncode == 0 and r.stdout.strip() == "OK", r.stdout
+
+
+def test_skinny_grid_invariants(tg):
+    """The M <= 128 planner over a sweep of shapes: at most one CTA per SM,
+    at least 8 units of work per CTA (unless the problem is smaller), an
+    aligned grid cuts only at tile edges or equal tile fractions, and the
+    cluster launch is asked for exactly when each tile has four k-pieces."""
+    for M in (1, 16, 64, 100, 128):
+        for N in (1, 128, 1000, 2048, 4096, 4864, 5120, 8192, 11008, 14336, 16384, 28672):
+            for K in (64, 1000, 4096, 8192, 14336):
+                p = tg.tg_plan_f16(M, N, K, 152)
+                assert p.kernel == tg.TG_KERNEL_SKINNY
+                T, KB, G = p.tiles_n, p.k_blocks, p.grid
+                U = T * KB
+                assert 1 <= G <= 152
+                assert G * 8 <= U or G == 1, (M, N, K, G, U)
+                assert p.cluster in (1, 4)
+                if p.cluster == 4:
+                    assert G == 4 * T and KB // 4 >= 8, (M, N, K)
+                if G < T and T % G == 0 and G * 10 >= 152 * 7:
+                    assert p.split_k == 1  # whole tiles per CTA
+                if G == T * (G // T) and G > T and G * 10 >= 152 * 7 and p.cluster == 4:
+                    assert p.split_k == 4
