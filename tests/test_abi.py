@@ -325,3 +325,26 @@ def test_skinny_grid_invariants(tg):
                     assert p.split_k == 1  # whole tiles per CTA
                 if G == T * (G // T) and G > T and G * 10 >= 152 * 7 and p.cluster == 4:
                     assert p.split_k == 4
+
+
+def test_pair_split_invariants(tg):
+    """The pair planner over a sweep of shapes: an even grid of at most 152
+    CTAs, and a last wave split into at most 4 k-pieces per tile, each at
+    least 8 blocks of 128 k, that fit the idle pairs."""
+    for M in (256, 1000, 2048, 2560, 4096, 8192):
+        for N in (256, 1000, 2048, 4096, 4864, 8192, 11008, 28672):
+            for K in (512, 1024, 4096, 8192, 16384):
+                p = tg.tg_plan_f16(M, N, K, 152)
+                if p.cluster != 2:
+                    continue
+                T, KB, G = p.num_tiles, p.k_blocks, p.grid
+                P = G // 2
+                assert G % 2 == 0 and 2 <= G <= 152
+                S = p.split_k
+                assert 1 <= S <= 4
+                R = T % P if T >= P else T
+                if S > 1:
+                    assert KB // S >= 8 and R * S <= P, (M, N, K, S)
+                    assert p.workspace_bytes > 0
+                else:
+                    assert P == min(T, 76)
