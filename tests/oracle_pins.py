@@ -669,4 +669,98 @@ def pin_sp24_integer_closed_form(o):
     assert np.array_equal(C.astype(np.float64), (A.astype(np.int64) @ Bi).astype(np.float64))
 
 
+def pin_sp24_sampled_matches_full(o):
+    """gemm_sp24_at (which decompresses only the rows it needs) equals the full
+    gemm_sp24 bit for bit, on rows given out of order, repeated, and leaving
+    rows out, with bias, residual (its own leading dimension) and both output
+    types."""
+    rng = np.random.default_rng(64)
+    M, N, K = 9, 11, 96
+    _, Ac, E = sp24_random(rng, M, K, lambda r: float(np.float16(r.normal(0, 1))))
+    Ac16 = _f16(Ac)
+    B = _f16(rng.normal(0, 1, (K, N)))
+    R = _f16(rng.normal(0, 1, (M, N + 3)))
+    bias = rng.normal(0, 1, N).astype(np.float32)
+    # rows 0, 2 and 7 never appear, so the row subset is not the identity
+    rows = np.array([8, 1, 8, 4, 3, 3, 6, 5, 1] + list(rng.choice([1, 3, 4, 5, 6, 8], 120)))
+    cols = rng.integers(0, N, rows.size)
+    for relu in (False, True):
+        for out_dtype in ("f16", "f32"):
+            C = o.gemm_sp24(Ac16, E, B, M, N, K, relu=relu, bias=bias, R=R, out_dtype=out_dtype)
+            v, _ = o.gemm_sp24_at(Ac16, E, B, K, rows, cols, relu=relu, bias=bias, R=R,
+                                  out_dtype=out_dtype)
+            v, C = np.asarray(v), np.asarray(C)
+            assert v.dtype == C.dtype, (out_dtype, v.dtype, C.dtype)
+            assert np.array_equal(v.view(np.uint8), np.ascontiguousarray(C[rows, cols]).view(np.uint8)), \
+                (relu, out_dtype)
+
+
+def pin_mx_sampled_matches_full(o):
+    """gemm_mxfp4_at equals the full gemm_mxfp4 bit for bit on scattered
+    elements, with ReLU, bias, residual and both output types (K != N, so a
+    swapped dimension cannot pass)."""
+    rng = np.random.default_rng(55)
+    M, N, K = 7, 13, 100
+    A = _f16(rng.normal(0, 1, (M, K)))
+    codes = rng.integers(0, 16, (K, N))
+    X = rng.integers(118, 132, ((K + 31) // 32, N)).astype(np.uint8)
+    Bq = _pack_codes(codes)
+    R = _f16(rng.normal(0, 1, (M, N + 5)))
+    bias = rng.normal(0, 1, N).astype(np.float32)
+    rows = rng.integers(0, M, 150)
+    cols = rng.integers(0, N, 150)
+    for relu in (False, True):
+        for out_dtype in ("f16", "f32"):
+            C = o.gemm_mxfp4(A, Bq, X, M, N, K, relu=relu, bias=bias, R=R, out_dtype=out_dtype)
+            v, _ = o.gemm_mxfp4_at(A, Bq, X, K, N, rows, cols, relu=relu, bias=bias, R=R,
+                                   out_dtype=out_dtype)
+            v, C = np.asarray(v), np.asarray(C)
+            assert v.dtype == C.dtype, (out_dtype, v.dtype, C.dtype)
+            assert np.array_equal(v.view(np.uint8), np.ascontiguousarray(C[rows, cols]).view(np.uint8)), \
+                (relu, out_dtype)
+
+
+# ---------------------------------------------------------------- tolerance spacings
+#
+# The parity tolerance is 2 spacings of the output format at the oracle value
+# plus 1e-3*sqrt(K).  The spacing functions are pinned to the formats
+# themselves: for every positive finite number x of the format below its
+# largest, the spacing at x is the distance to the next number up, read from
+# consecutive bit patterns (binary16 through numpy's decoder; bfloat16 as the
+# upper half of a binary32 pattern).  Hand-picked values cover zero, the
+# subnormal range, binade edges and the largest finite number.
+
+def _bf16_value(bits):
+    return (np.asarray(bits, dtype=np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def pin_spacing_f16_consecutive(o):
+    import oracle
+    h = np.arange(0, 0x7BFF, dtype=np.uint16)  # 0 .. next-to-largest finite
+    x = h.view(np.float16).astype(np.float64)
+    nxt = (h + 1).view(np.float16).astype(np.float64)
+    assert np.array_equal(oracle.ulp16(x), nxt - x)
+    assert np.array_equal(oracle.ulp16(-x), nxt - x)
+    hand = {0.0: 2.0 ** -24, 1.0: 2.0 ** -10, 1.999: 2.0 ** -10, 2.0: 2.0 ** -9,
+            65504.0: 32.0, 2.0 ** -14: 2.0 ** -24, 2.0 ** -15: 2.0 ** -24, -3.0: 2.0 ** -9}
+    got = oracle.ulp16(np.array(list(hand)))
+    assert list(got) == list(hand.values())
+
+
+def pin_spacing_bf16_consecutive(o):
+    import oracle
+    h = np.arange(0, 0x7F7F, dtype=np.uint32)  # 0 .. next-to-largest finite
+    x = _bf16_value(h)
+    nxt = _bf16_value(h + 1)
+    assert np.array_equal(oracle.ulp_bf16(x), nxt - x)
+    assert np.array_equal(oracle.ulp_bf16(-x), nxt - x)
+    bmax = float(_bf16_value(0x7F7F))  # largest finite bfloat16, (2 - 2^-7) * 2^127
+    assert bmax == (2.0 - 2.0 ** -7) * 2.0 ** 127
+    hand = {0.0: 2.0 ** -133, 1.0: 2.0 ** -7, 1.999: 2.0 ** -7, 2.0: 2.0 ** -6,
+            bmax: 2.0 ** 120, 2.0 ** -126: 2.0 ** -133, 2.0 ** -127: 2.0 ** -133,
+            -3.0: 2.0 ** -6}
+    got = oracle.ulp_bf16(np.array(list(hand)))
+    assert list(got) == list(hand.values())
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

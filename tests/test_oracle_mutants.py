@@ -1,11 +1,16 @@
-"""Plant plausible mistakes in a copy of the oracle's C source and check that
-the pins catch every one of them (no GPU).
+"""Plant plausible mistakes in a copy of the oracle and check that the pins
+catch every one of them (no GPU).
 
-Each mutant is a textual edit of ``oracle/tgemm_oracle.c`` compiled into a
-temporary library; the committed oracle is never modified.
+Each C mutant is a textual edit of ``oracle/tgemm_oracle.c`` compiled into a
+temporary library.  Each Python mutant is a textual edit of one function of
+``oracle/__init__.py``, compiled in that module's namespace and installed on a
+fresh ``Oracle`` (methods) or patched over the module attribute for the one
+test (the tolerance spacings).  The committed oracle is never modified.
 """
 
+import inspect
 import os
+import types
 
 import pytest
 
@@ -102,4 +107,49 @@ def test_mutant_is_caught(tmp_path, name, old, new):
         f.write(src.replace(old, new))
     lib = oracle.compile_source(path, os.path.join(str(tmp_path), f"lib{name}.so"))
     caught = _pin_catches(oracle.Oracle(lib))
+    assert caught, f"mutant {name} passed every pin"
+
+
+# Python-level parts of the oracle: (name, function, original text, replacement).
+# The spacing functions set the parity tolerance; the *_at functions produce
+# the expected values of the large sampled GPU tests.
+PY_MUTANTS = [
+    ("ulp_bf16_mantissa_8", "ulp_bf16", "e[nz] - 7.0", "e[nz] - 8.0"),
+    ("ulp_bf16_normal_from_2^-127", "ulp_bf16", "a >= 2.0 ** -126", "a >= 2.0 ** -127"),
+    ("ulp_bf16_subnormal_2^-134", "ulp_bf16", "np.full(a.shape, 2.0 ** -133)",
+     "np.full(a.shape, 2.0 ** -134)"),
+    ("ulp16_mantissa_11", "ulp16", "e[nz] - 10.0", "e[nz] - 11.0"),
+    ("ulp16_normal_from_2^-15", "ulp16", "a >= 2.0 ** -14", "a >= 2.0 ** -15"),
+    ("sp24_at_inverse_sorted", "_gemm_sp24_at", "gemm_ex_at(A, B, K, inv,",
+     "gemm_ex_at(A, B, K, np.sort(inv),"),
+    ("sp24_at_residual_not_subset", "_gemm_sp24_at", "np.asarray(R)[uniq]", "np.asarray(R)"),
+    ("sp24_at_metadata_not_subset", "_gemm_sp24_at", "np.asarray(E)[uniq]",
+     "np.asarray(E)[:uniq.size]"),
+    ("sp24_at_out_type_ignored", "_gemm_sp24_at", "out_dtype=out_dtype or in_dtype",
+     "out_dtype=in_dtype"),
+    ("mx_at_relu_dropped", "_gemm_mxfp4_at", "rows, cols, relu=relu,", "rows, cols, relu=False,"),
+    ("mx_at_bias_dropped", "_gemm_mxfp4_at", "bias=bias, R=R, in_dtype", "bias=None, R=R, in_dtype"),
+    ("mx_at_residual_dropped", "_gemm_mxfp4_at", "R=R, in_dtype", "R=None, in_dtype"),
+]
+
+_METHODS = {"_gemm_sp24_at": "gemm_sp24_at", "_gemm_mxfp4_at": "gemm_mxfp4_at"}
+
+
+def _mutated(fname, old, new):
+    src = inspect.getsource(getattr(oracle, fname))
+    assert src.count(old) >= 1, f"mutation site {old!r} not found in {fname}"
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), f"<mutant of {fname}>", "exec"), ns)
+    return ns[fname]
+
+
+@pytest.mark.parametrize("name,fname,old,new", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_python_mutant_is_caught(monkeypatch, name, fname, old, new):
+    fn = _mutated(fname, old, new)
+    o = oracle.Oracle(oracle.build())
+    if fname in _METHODS:
+        setattr(o, _METHODS[fname], types.MethodType(fn, o))
+    else:
+        monkeypatch.setattr(oracle, fname, fn)
+    caught = _pin_catches(o)
     assert caught, f"mutant {name} passed every pin"
