@@ -60,6 +60,8 @@ def parse_args(argv=None):
     p.add_argument("--no-epilogue", action="store_true")
     p.add_argument("--no-mxfp4", action="store_true")
     p.add_argument("--no-sp24", action="store_true")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the 256^3, 1024^3 ReLU and 4096^3 configs and the staged layout")
     p.add_argument("--sp24-workload", default="sp24_mlp_8192x28672x4096_relu",
                    choices=sorted(W.SP24_WORKLOADS))
     a = p.parse_args(argv)
@@ -231,6 +233,66 @@ def time_launches(launch, stream, steps: int, world: int, device):
     return total, total / steps, per, wall0, wall1
 
 
+def rotating_sets(set_bytes: int) -> int:
+    """Copies of one problem's operands to rotate through so that the copies
+    together span at least twice L2: each launch then reads operands that
+    the launches before it have evicted."""
+    return int(min(1024, max(1, -(-2 * L2_BYTES // max(set_bytes, 1)))))
+
+
+def host_issue_us(launch, n: int) -> float:
+    """Host time per call to enqueue `n` launches (no synchronisation inside)."""
+    import torch
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    for _ in range(n):
+        launch()
+    dt = time.perf_counter() - t
+    torch.cuda.synchronize()
+    return dt / n * 1e6
+
+
+def link_bound(h2d_bytes: int, d2h_bytes: int, device):
+    """Pinned host <-> device copy rates measured now, alone and with both
+    directions at once, and the shortest time in which a step can move its
+    bytes: no end-to-end step can be faster than its concurrent copies."""
+    import torch
+    hu = torch.empty(h2d_bytes, dtype=torch.uint8).pin_memory()
+    du = torch.empty(h2d_bytes, dtype=torch.uint8, device=device)
+    hd = torch.empty(d2h_bytes, dtype=torch.uint8).pin_memory()
+    dd = torch.empty(d2h_bytes, dtype=torch.uint8, device=device)
+    s_up, s_down = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    cur = torch.cuda.current_stream(device)
+
+    def timed(up: bool, down: bool) -> float:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record(cur)
+        s_up.wait_event(ev[0])
+        s_down.wait_event(ev[0])
+        if up:
+            with torch.cuda.stream(s_up):
+                du.copy_(hu, non_blocking=True)
+        if down:
+            with torch.cuda.stream(s_down):
+                hd.copy_(dd, non_blocking=True)
+        ev[1].record(s_up)
+        ev[2].record(s_down)
+        torch.cuda.synchronize()
+        return max(ev[0].elapsed_time(ev[1]), ev[0].elapsed_time(ev[2]))
+
+    best = {}
+    for key, up, down in (("up", True, False), ("down", False, True), ("both", True, True)):
+        timed(up, down)
+        best[key] = min(timed(up, down) for _ in range(3))
+    del hu, du, hd, dd
+    return {
+        "h2d_gbs_alone": h2d_bytes / (best["up"] / 1e3) / 1e9,
+        "d2h_gbs_alone": d2h_bytes / (best["down"] / 1e3) / 1e9,
+        "both_directions_ms": best["both"],
+        "how": "contiguous pinned copies of the step's bytes on two streams, best of 3",
+    }
+
+
 def cpu_oracle_rate(A, B, w, seconds: float):
     """Time the oracle on a row slab sized for about `seconds` of work.
     Returns (tflops, rows, elapsed_s, threads)."""
@@ -292,6 +354,59 @@ def config_block(w, gpus):
             "inputs": f"A {w.dist_a}, B {w.dist_b}, seed {w.seed}",
             "l2": f"inputs larger than L2 ({inb / 2**20:.0f} MiB of A+B vs {L2_BYTES // 2**20} MiB L2); no flush",
             "parallelism": "replicas" if gpus > 1 else "single GPU"}
+
+
+def time_config(tg, w, args, stream, world, device, nsm, tf_peak, peak_src):
+    """One of the square configs through tg_gemm_f16, timed like the main
+    workload (back-to-back launches between two events), its operands rotated
+    over copies spanning twice L2."""
+    import torch
+    from tiled_fp16_gemm_gb300 import workloads as W
+    A, B = W.workload_inputs(w)
+    sets = rotating_sets(w.min_bytes)
+    a = torch.from_numpy(A).to(device).unsqueeze(0).repeat(sets, 1, 1)
+    b = torch.from_numpy(B).to(device).unsqueeze(0).repeat(sets, 1, 1)
+    c = torch.empty((sets, w.M, w.N), dtype=torch.float16, device=device)
+    epi = tg.TG_EPI_RELU if w.relu else tg.TG_EPI_NONE
+    plan = tg.tg_plan_f16(w.M, w.N, w.K, nsm)
+    ctr = [0]
+
+    def launch():
+        i = ctr[0] % sets
+        ctr[0] += 1
+        st = tg.tg_gemm_f16(a[i].data_ptr(), b[i].data_ptr(), c[i].data_ptr(), w.M, w.N, w.K,
+                            w.K, w.N, w.N, epi, stream.cuda_stream)
+        if st != tg.TG_OK:
+            raise tg.TgemmError(st)
+
+    for _ in range(max(args.warmup, sets)):
+        launch()
+    tg.sync_status(stream)
+    n = max(200, args.steps) if w.flops < 1e11 else max(100, args.steps // 2)
+    _, k, per, _, _ = time_launches(launch, stream, n, world, device)
+    tg.sync_status(stream)
+    host_us = host_issue_us(launch, n)
+    tg.sync_status(stream)
+    tf = w.flops / (k / 1e3) / 1e12
+    if plan.cluster == 2:
+        kname = f"tg_gemm_f16_pair<{plan.stages} stages of {plan.bk} k>, split_k {plan.split_k}"
+    else:
+        kname = f"tg_gemm_f16_persistent<{plan.bn},{plan.stages}>"
+    del a, b, c
+    torch.cuda.empty_cache()
+    return {
+        "workload": w.name, "M": w.M, "N": w.N, "K": w.K, "epilogue": "relu" if w.relu else "none",
+        "kernel": kname, "grid": int(plan.grid), "tiles": int(plan.num_tiles),
+        "launches": n, "operand_sets": sets,
+        "l2": f"operands rotated over {sets} copies ({sets * w.min_bytes / 2**20:.0f} MiB)",
+        "kernel_ms_mean": k, "isolated_launch_ms_min": min(per),
+        "isolated_launch_ms_median": statistics.median(per),
+        "host_us_per_call": host_us,
+        "tflops": tf, "gbs": w.min_bytes / (k / 1e3) / 1e9,
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": tf_peak, "unit": "TFLOP/s",
+                     "frac": tf / tf_peak,
+                     "peak_source": f"{peak_src} dense bf16 burst (fp16 dense rate is the same)"},
+    }
 
 
 def run_ours(args, w, rank, world, local_rank):
@@ -365,6 +480,50 @@ def run_ours(args, w, rank, world, local_rank):
         "gpu_launches": args.steps,
         "clocks": clk,
     }
+
+    # ---- the other square configs (256^3, 1024^3 with ReLU, 4096^3), same
+    # method; operands rotate over enough copies that each launch reads them
+    # from HBM, not from what the previous launch left in L2
+    if not args.no_configs and w.name == MAIN_WORKLOAD:
+        out["configs"] = {}
+        for cname in ("gemm_256", "gemm_1024_relu", "gemm_4096"):
+            out["configs"][cname] = time_config(tg, W.WORKLOADS[cname], args, stream, world,
+                                                device, nsm, tf_peak, peak_src)
+        out["configs"][MAIN_WORKLOAD] = {"see": "top level (value, roofline)"}
+        out["configs"][SKINNY_WORKLOAD] = {"see": "skinny"}
+
+        # the main workload with A in a layout the tensor memory-access unit
+        # cannot address (lda = K + 1): A is first copied to an aligned
+        # staging buffer, then the same kernel runs
+        a_odd = torch.zeros((w.M, w.K + 1), dtype=torch.float16, device=device)
+        a_odd[:, :w.K] = a
+        c_odd = torch.empty_like(c)
+
+        def launch_odd():
+            st = tg.tg_gemm_f16(a_odd.data_ptr(), b.data_ptr(), c_odd.data_ptr(), w.M, w.N, w.K,
+                                w.K + 1, w.N, w.N, epi, stream.cuda_stream)
+            if st != tg.TG_OK:
+                raise tg.TgemmError(st)
+
+        for _ in range(args.warmup):
+            launch_odd()
+        launch()
+        tg.sync_status(stream)
+        same = bool(torch.equal(c_odd.view(torch.int16), c.view(torch.int16)))
+        n_odd = max(50, args.steps // 2)
+        _, k_odd, per_odd, _, _ = time_launches(launch_odd, stream, n_odd, world, device)
+        tg.sync_status(stream)
+        out["staged_layout"] = {
+            "workload": w.name, "lda": w.K + 1, "launches": n_odd,
+            "what": "A copied to an aligned staging buffer (tg_copy_matrix16), then the "
+                    "planned kernel",
+            "kernel_ms_mean": k_odd, "isolated_launch_ms_min": min(per_odd),
+            "tflops": flops / (k_odd / 1e3) / 1e12,
+            "vs_aligned": kernel_ms / k_odd,
+            "staging_bytes": 2 * 2 * w.M * w.K,
+            "same_bits_as_aligned": same,
+        }
+        del a_odd, c_odd
 
     # ---- skinny weight-streaming workload, same method
     if not args.no_skinny and w.name != SKINNY_WORKLOAD:
@@ -591,10 +750,18 @@ def run_ours(args, w, rank, world, local_rank):
         for _ in range(n3):
             tg.gemm_host(ha, hb, relu=w.relu, stream=stream)
         dt = max_over_ranks(time.perf_counter() - t, world, device)
-        out["e2e"] = {"value": world * flops * n3 / dt / 1e12, "unit": "TFLOP/s",
-                      "h2d_bytes_per_step": int(ha.numel() * 2 + hb.numel() * 2),
-                      "d2h_bytes_per_step": int(w.M * w.N * 2),
-                      "steps": n3, "call": "tiled_fp16_gemm_gb300.gemm_host"}
+        e2e_value = world * flops * n3 / dt / 1e12
+        h2d = int(ha.numel() * 2 + hb.numel() * 2)
+        d2h = int(w.M * w.N * 2)
+        out["e2e"] = {"value": e2e_value, "unit": "TFLOP/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "steps": n3, "call": "tiled_fp16_gemm_gb300.gemm_host",
+                      "ms_per_step": dt / n3 * 1e3}
+        del ha, hb
+        bound = link_bound(h2d, d2h, device)
+        bound["tflops_bound"] = flops / (bound["both_directions_ms"] / 1e3) / 1e12
+        bound["frac"] = (e2e_value / world) / bound["tflops_bound"]
+        out["e2e"]["bound"] = bound
 
     # ---- CPU oracle on this host (rank 0, N == 1 only)
     if not args.no_cpu and rank == 0 and world == 1:

@@ -103,6 +103,7 @@ __device__ __forceinline__ bool pair_tail_piece(const PersistentParams& p, uint3
                    make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
                                __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])));
     }
+    fence_proxy_async_global();  // the stores come before the reader's bulk copies of them
     __threadfence();
     __syncwarp();
     const int S = p.split;
@@ -118,6 +119,9 @@ __device__ __forceinline__ bool pair_tail_piece(const PersistentParams& p, uint3
     bool ok = true;
     if (__shfl_sync(0xffffffffu, last, 0)) {
         __threadfence();
+        // the other pieces' partials, observed through the acquire above, are
+        // read below by bulk copies (the async proxy)
+        if (lane == 0) fence_proxy_async_global();
         const float* const first =
             p.ws + static_cast<int64_t>(tail_tile) * S * kPairSlotFloats + region;
 #pragma unroll 1

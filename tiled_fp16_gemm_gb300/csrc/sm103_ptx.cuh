@@ -218,6 +218,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Order generic-proxy global-memory accesses before later async-proxy (bulk
+// copy) accesses of global memory.  Writers of data that another thread will
+// bulk-copy issue it after their stores; the reader issues it after the
+// acquire that observed those writes and before its bulk copies.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
