@@ -369,13 +369,15 @@ def time_config(tg, w, args, stream, world, device, nsm, tf_peak, peak_src):
     c = torch.empty((sets, w.M, w.N), dtype=torch.float16, device=device)
     epi = tg.TG_EPI_RELU if w.relu else tg.TG_EPI_NONE
     plan = tg.tg_plan_f16(w.M, w.N, w.K, nsm)
+    ptrs = [(a[i].data_ptr(), b[i].data_ptr(), c[i].data_ptr()) for i in range(sets)]
     ctr = [0]
+    fn = tg.library().tg_gemm_f16
+    sp = stream.cuda_stream
 
     def launch():
-        i = ctr[0] % sets
+        pa, pb, pc = ptrs[ctr[0] % sets]
         ctr[0] += 1
-        st = tg.tg_gemm_f16(a[i].data_ptr(), b[i].data_ptr(), c[i].data_ptr(), w.M, w.N, w.K,
-                            w.K, w.N, w.N, epi, stream.cuda_stream)
+        st = fn(pa, pb, pc, w.M, w.N, w.K, w.K, w.N, w.N, epi, sp)
         if st != tg.TG_OK:
             raise tg.TgemmError(st)
 

@@ -313,6 +313,31 @@ typedef struct {
 tg_status_t tg_plan_f16(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* plan);
 
 /*
+ * tg_plan_f16_limits — the same plan on a device that holds at most
+ * `max_pairs` CTA pairs of the pair kernel, and `max_quads_narrow` /
+ * `max_quads_wide` clusters of four skinny CTAs (M ≤ 64 / M ≤ 128), at once.
+ * Clusters must sit inside one GPC, so these can be below num_sms / 2 and
+ * num_sms / 4; tg_plan_f16 assumes they are not.  With the limits of the
+ * current device (tg_device_limits) the result is exactly the shape
+ * tg_gemm_f16 launches: pairs beyond max_pairs are never launched (none:
+ * one-CTA tiles), and a skinny grid whose clusters would not all fit at
+ * once launches without clusters.  Returns TG_ERR_INVALID_VALUE for
+ * negative limits or as tg_plan_f16.
+ */
+tg_status_t tg_plan_f16_limits(int64_t M, int64_t N, int64_t K, int32_t num_sms,
+                               int32_t max_pairs, int32_t max_quads_narrow,
+                               int32_t max_quads_wide, tg_plan_t* plan);
+
+/*
+ * tg_device_limits — the limits above for the current device (occupancy
+ * queries made once per device; needs a GB300).  Returns
+ * TG_ERR_UNSUPPORTED_DEVICE on any other device, TG_ERR_INVALID_VALUE for a
+ * NULL output.
+ */
+tg_status_t tg_device_limits(int32_t* num_sms, int32_t* max_pairs, int32_t* max_quads_narrow,
+                             int32_t* max_quads_wide);
+
+/*
  * tg_tile_coord — which (m block, n block) tile number `tile` of a plan maps
  * to; the persistent kernel walks tiles in this order (column-major inside
  * groups of plan->group_m row blocks, so consecutive CTAs share B panels in
@@ -342,6 +367,19 @@ void tg_debug_set_wait_timeout_ns(uint64_t ns);
  * kernel returns early with TG_ERR_TIMEOUT recorded.  mode 0: off.  The
  * setting applies to exactly one launch. */
 void tg_debug_inject(int32_t mode);
+
+/* The shape of the last tg_gemm_f16 / tg_gemm_bf16 / tg_gemm_ex launch made
+ * by the calling thread (tg_gemm_f16_noalloc's too): its plan, with grid,
+ * split_k and cluster as actually launched.  These differ from the plan only
+ * if the pair kernel's split-K workspace could not be allocated (the last
+ * wave then runs unsplit).  Returns TG_ERR_INVALID_VALUE for NULL. */
+tg_status_t tg_debug_last_launch(tg_plan_t* plan);
+
+/* Tensor maps served from the library's map cache (hits) and encoded anew
+ * (misses) since the library was loaded.  A map depends only on the
+ * address, extents, row stride, box and modes it encodes, and the cache is
+ * keyed by all of them, so a hit is always the map the call needs. */
+void tg_debug_map_cache_stats(uint64_t* hits, uint64_t* misses);
 
 /* ------------------------------------------------------------------------
  * Host buffers in and out.

@@ -348,3 +348,37 @@ def test_pair_split_invariants(tg):
                     assert p.workspace_bytes > 0
                 else:
                     assert P == min(T, 76)
+
+
+def test_plan_limits(tg):
+    """tg_plan_f16_limits: with the nominal limits it is tg_plan_f16; with
+    fewer resident pairs or four-CTA clusters it plans only what fits."""
+    for shape in [(8192, 28672, 4096), (4096, 4096, 4096), (2048, 2048, 4096),
+                  (1024, 1024, 1024), (64, 4096, 4096), (64, 16384, 8192), (7, 5, 3),
+                  (5, 5, 0)]:
+        a = tg.tg_plan_f16(*shape, 152)
+        b = tg.tg_plan_f16_limits(*shape, 152, 76, 38, 38)
+        assert bytes(a) == bytes(b), shape
+    # fewer pairs fit at once: the grid stays within them, the tail split follows
+    p = tg.tg_plan_f16_limits(8192, 28672, 4096, 152, 74, 38, 38)
+    assert p.cluster == 2 and p.grid <= 148 and p.grid % 2 == 0
+    R = p.num_tiles % (p.grid // 2)
+    assert p.split_k == 1 or R * p.split_k <= p.grid // 2
+    # limits above num_sms / 2 are clamped to it
+    assert bytes(tg.tg_plan_f16_limits(8192, 28672, 4096, 152, 99, 38, 38)) == \
+        bytes(tg.tg_plan_f16(8192, 28672, 4096, 152))
+    # no pair fits: one-CTA tiles
+    p = tg.tg_plan_f16_limits(8192, 28672, 4096, 152, 0, 38, 38)
+    assert p.kernel == tg.TG_KERNEL_PERSISTENT and p.cluster == 1
+    # a skinny grid of four-piece clusters: launched without clusters unless
+    # every cluster fits at once
+    s = tg.tg_plan_f16(64, 4096, 4096, 152)
+    assert s.cluster == 4 and s.grid == 128
+    s2 = tg.tg_plan_f16_limits(64, 4096, 4096, 152, 76, 31, 38)
+    assert s2.cluster == 1 and s2.grid == 128 and s2.split_k == s.split_k
+    assert tg.tg_plan_f16_limits(64, 4096, 4096, 152, 76, 32, 0).cluster == 4
+    w = tg.tg_plan_f16(128, 4096, 14336, 152)
+    assert w.cluster == 4
+    assert tg.tg_plan_f16_limits(128, 4096, 14336, 152, 76, 38, 31).cluster == 1
+    with pytest.raises(tg.TgemmError):
+        tg.tg_plan_f16_limits(5, 5, 5, 152, -1, 38, 38)

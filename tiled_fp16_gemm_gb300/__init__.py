@@ -41,7 +41,8 @@ EXPORTS = (
     "tg_gemm_f16", "tg_sync_status", "tg_status_string", "tg_version", "tg_plan_f16",
     "tg_tile_coord", "tg_ring_bytes", "tg_debug_set_wait_timeout_ns", "tg_debug_inject",
     "tg_gemm_f16_noalloc", "tg_gemm_bf16", "tg_gemm_ex", "tg_gemm_mxfp4", "tg_gemm_sp24",
-    "tg_gemm_f16_host",
+    "tg_gemm_f16_host", "tg_plan_f16_limits", "tg_device_limits", "tg_debug_last_launch",
+    "tg_debug_map_cache_stats",
 )
 
 #: bytes of the library's fixed scratch array used by tg_gemm_f16_noalloc
@@ -118,6 +119,15 @@ def _L():
     lib.tg_debug_set_wait_timeout_ns.restype = None
     lib.tg_debug_inject.argtypes = [ctypes.c_int32]
     lib.tg_debug_inject.restype = None
+    lib.tg_plan_f16_limits.argtypes = [_i64, _i64, _i64] + [ctypes.c_int32] * 4 + [
+        ctypes.POINTER(tg_plan_t)]
+    lib.tg_plan_f16_limits.restype = ctypes.c_int
+    lib.tg_device_limits.argtypes = [ctypes.POINTER(ctypes.c_int32)] * 4
+    lib.tg_device_limits.restype = ctypes.c_int
+    lib.tg_debug_last_launch.argtypes = [ctypes.POINTER(tg_plan_t)]
+    lib.tg_debug_last_launch.restype = ctypes.c_int
+    lib.tg_debug_map_cache_stats.argtypes = [ctypes.POINTER(ctypes.c_uint64)] * 2
+    lib.tg_debug_map_cache_stats.restype = None
     _lib = lib
     return lib
 
@@ -196,6 +206,40 @@ def tg_plan_f16(M: int, N: int, K: int, num_sms: int) -> tg_plan_t:
     if st != TG_OK:
         raise TgemmError(st, "tg_plan_f16")
     return plan
+
+
+def tg_plan_f16_limits(M: int, N: int, K: int, num_sms: int, max_pairs: int,
+                       max_quads_narrow: int, max_quads_wide: int) -> tg_plan_t:
+    plan = tg_plan_t()
+    st = _L().tg_plan_f16_limits(M, N, K, num_sms, max_pairs, max_quads_narrow, max_quads_wide,
+                                 ctypes.byref(plan))
+    if st != TG_OK:
+        raise TgemmError(st, "tg_plan_f16_limits")
+    return plan
+
+
+def tg_device_limits() -> tuple[int, int, int, int]:
+    """(num_sms, max_pairs, max_quads_narrow, max_quads_wide) of the current device."""
+    v = [ctypes.c_int32() for _ in range(4)]
+    st = _L().tg_device_limits(*[ctypes.byref(x) for x in v])
+    if st != TG_OK:
+        raise TgemmError(st, "tg_device_limits")
+    return tuple(x.value for x in v)
+
+
+def tg_debug_last_launch() -> tg_plan_t:
+    plan = tg_plan_t()
+    st = _L().tg_debug_last_launch(ctypes.byref(plan))
+    if st != TG_OK:
+        raise TgemmError(st, "tg_debug_last_launch")
+    return plan
+
+
+def tg_debug_map_cache_stats() -> tuple[int, int]:
+    """(hits, misses) of the library's tensor-map cache since it was loaded."""
+    h, m = ctypes.c_uint64(), ctypes.c_uint64()
+    _L().tg_debug_map_cache_stats(ctypes.byref(h), ctypes.byref(m))
+    return h.value, m.value
 
 
 def tg_tile_coord(plan: tg_plan_t, tile: int) -> tuple[int, int]:

@@ -391,74 +391,77 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            // fp16 B: A operand = B^T tile, MN-major in shared memory.  QB: A
-            // operand = decoded weights in tensor memory (K-major).
-            const uint32_t idesc =
-                idesc_f16_f32(128, p.Mp, /*a_mn=*/!QB, /*b_mn=*/false, Elem16<T>::kFmt);
-            int stage = 0;
-            uint32_t phase = 0;
-            int it = 0;
-            bool ok = true;
-            for (int64_t u = u_begin; ok && u < u_end; ++it) {
-                const int64_t t = u / KB;
-                const int64_t seg_end = (t + 1) * KB < u_end ? (t + 1) * KB : u_end;
-                const int acc = it & 1;
-                const uint32_t acc_phase = (it >> 1) & 1;
-                if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
-                    fail(kRoleMma);
+        // The whole warp runs the loop (warp-uniform control flow and
+        // operands); one elected lane issues each MMA and commit.  A wait
+        // counts as met only if every lane saw it met.
+        auto warp_wait = [&](uint32_t bar, uint32_t parity, const volatile int* ab) {
+            const bool r = mbar_wait(bar, parity, p.timeout_ns, ab);
+            return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
+        };
+        // fp16 B: A operand = B^T tile, MN-major in shared memory.  QB: A
+        // operand = decoded weights in tensor memory (K-major).
+        const uint32_t idesc =
+            idesc_f16_f32(128, p.Mp, /*a_mn=*/!QB, /*b_mn=*/false, Elem16<T>::kFmt);
+        int stage = 0;
+        uint32_t phase = 0;
+        int it = 0;
+        bool ok = true;
+        for (int64_t u = u_begin; ok && u < u_end; ++it) {
+            const int64_t t = u / KB;
+            const int64_t seg_end = (t + 1) * KB < u_end ? (t + 1) * KB : u_end;
+            const int acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            if (!warp_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag)) {
+                if (lane == 0) fail(kRoleMma);
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 128);
+            for (int64_t v = u; v < seg_end; ++v) {
+                // QB: B^T decoded into the operand stage, and (the
+                // converters waited for it) that stage's A tile landed
+                const bool got = warp_wait(QB ? bar_dec + 8 * stage : bar_full + 8 * stage,
+                                           phase, abort_flag);
+                if (!got) {
+                    if (lane == 0) fail(kRoleMma);
+                    ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 128);
-                for (int64_t v = u; v < seg_end; ++v) {
-                    // QB: B^T decoded into the operand stage, and (the
-                    // converters waited for it) that stage's A tile landed
-                    const bool got =
-                        QB ? mbar_wait(bar_dec + 8 * stage, phase, p.timeout_ns, abort_flag)
-                           : mbar_wait(bar_full + 8 * stage, phase, p.timeout_ns, abort_flag);
-                    if (!got) {
-                        fail(kRoleMma);
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint32_t b0 = sB + stage * kSkBBytes;
-                    const uint32_t a0 = sA + stage * kSkASlot;
+                const uint32_t b0 = sB + stage * kSkBBytes;
+                const uint32_t a0 = sA + stage * kSkASlot;
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        // A tile: 64-k boxes kABox apart, 32 B per 16 k inside one
-                        const uint64_t bdesc =
-                            smem_desc_sw128(a0 + kABox * (k / 4) + 32 * (k % 4), 16, 1024);
-                        const uint32_t acc_in = (v != u || k != 0) ? 1u : 0u;
-                        if constexpr (QB) {
-                            // 16 k = 8 columns of the operand stage
-                            const uint32_t a_tmem =
-                                tmem_base + kMxOpCol0 +
-                                static_cast<uint32_t>(kMxOpCols * stage + 8 * k);
-                            mx_mma_f16_ts(d_tmem, a_tmem, bdesc, idesc, acc_in);
-                        } else {
-                            // B^T: 16 k rows (2 KB) per step; the two 64-column
-                            // boxes kSkBBytes / 2 apart
-                            const uint64_t adesc =
-                                smem_desc_sw128(b0 + 2048 * k, kSkBBytes / 2, 1024);
-                            mma_f16_ss(d_tmem, adesc, bdesc, idesc, acc_in);
-                        }
-                    }
-                    mma_commit(bar_empty + 8 * stage);  // QB: the operand and A stages
-                    if (++stage == kSkStages) {
-                        stage = 0;
-                        phase ^= 1u;
+                for (int k = 0; k < BK / 16; ++k) {
+                    // A tile: 64-k boxes kABox apart, 32 B per 16 k inside one
+                    const uint64_t bdesc =
+                        smem_desc_sw128(a0 + kABox * (k / 4) + 32 * (k % 4), 16, 1024);
+                    const uint32_t acc_in = (v != u || k != 0) ? 1u : 0u;
+                    if constexpr (QB) {
+                        // 16 k = 8 columns of the operand stage
+                        const uint32_t a_tmem = tmem_base + kMxOpCol0 +
+                                                static_cast<uint32_t>(kMxOpCols * stage + 8 * k);
+                        mma_f16_ts_elect(d_tmem, a_tmem, bdesc, idesc, acc_in);
+                    } else {
+                        // B^T: 16 k rows (2 KB) per step; the two 64-column
+                        // boxes kSkBBytes / 2 apart
+                        const uint64_t adesc =
+                            smem_desc_sw128(b0 + 2048 * k, kSkBBytes / 2, 1024);
+                        mma_f16_ss_elect(d_tmem, adesc, bdesc, idesc, acc_in);
                     }
                 }
-                if (!ok) break;
-                if (!(p.inject == 1 && it == 0)) mma_commit(bar_tfull + 8 * acc);
-                u = seg_end;
+                mma_commit_elect(bar_empty + 8 * stage);  // QB: the operand and A stages
+                if (++stage == kSkStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
-            mma_commit(bar_drain);
-            if (!mbar_wait(bar_drain, 0, p.timeout_ns, nullptr))
-                atomicOr(&g_wait_timeout_flags, kRoleDrain);
+            if (!ok) break;
+            if (!(p.inject == 1 && it == 0)) mma_commit_elect(bar_tfull + 8 * acc);
+            u = seg_end;
         }
+        mma_commit_elect(bar_drain);
+        if (!warp_wait(bar_drain, 0, nullptr) && lane == 0)
+            atomicOr(&g_wait_timeout_flags, kRoleDrain);
     } else if (warp >= 2 && warp < 6) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
@@ -595,41 +598,56 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
             const uint32_t rphase = static_cast<uint32_t>((i / kRaw) & 1);
             int ok = 1;
             if (lane == 0) {
+                // the MMAs that read this operand stage have completed, and
+                // the unit's codes have landed
                 ok = mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.timeout_ns, abort_flag) ? 1
                                                                                             : 0;
                 if (ok)
                     ok = mbar_wait(bar_rfull + 8 * rstage, rphase, p.timeout_ns, abort_flag) ? 1
                                                                                              : 0;
-                // the unit's A tile: the MMA thread waits only for this warp's report
-                if (ok)
-                    ok = mbar_wait(bar_afull + 8 * stage, phase, p.timeout_ns, abort_flag) ? 1 : 0;
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
                 if (lane == 0) fail(kRoleConvert);
                 break;
             }
-            tc_fence_after_sync();  // the MMAs that read this operand stage have completed
-#pragma unroll 1
-            for (int h = 0; h < BK / 64; ++h) {  // the unit's 64-k halves
+            tc_fence_after_sync();
+            // The unit's codes and scales into registers, then the raw stage
+            // is free for the next load.
+            uint32_t w[BK / 64][8];
+            uint32_t X0[BK / 64], X1[BK / 64];
+#pragma unroll
+            for (int h = 0; h < BK / 64; ++h) {
                 const uint32_t row = sRaw + static_cast<uint32_t>(rstage) * kMxRawBytes +
                                      kMxCodeBox * static_cast<uint32_t>(h) + 32u * n_local;
                 const uint4 c0 = mx_ld_shared_v4(row + (swz32 << 4));
                 const uint4 c1 = mx_ld_shared_v4(row + ((swz32 ^ 1u) << 4));
                 const uint32_t scl = sScl + static_cast<uint32_t>(rstage) * kMxScaleBytes +
                                      256u * static_cast<uint32_t>(h) + n_local;
-                const uint32_t X0 = mx_ld_shared_u8(scl);
-                const uint32_t X1 = mx_ld_shared_u8(scl + 128u);
-                const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                X0[h] = mx_ld_shared_u8(scl);
+                X1[h] = mx_ld_shared_u8(scl + 128u);
+                w[h][0] = c0.x;
+                w[h][1] = c0.y;
+                w[h][2] = c0.z;
+                w[h][3] = c0.w;
+                w[h][4] = c1.x;
+                w[h][5] = c1.y;
+                w[h][6] = c1.z;
+                w[h][7] = c1.w;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_rempty + 8 * rstage);
+#pragma unroll
+            for (int h = 0; h < BK / 64; ++h) {  // the unit's 64-k halves
                 uint32_t d[32];
-                if (mx_fast_scale(X0) && mx_fast_scale(X1)) {
-                    const uint32_t f0 = mx_factor_bits(X0) * 0x10001u;  // both halves
-                    const uint32_t f1 = mx_factor_bits(X1) * 0x10001u;
+                if (mx_fast_scale(X0[h]) && mx_fast_scale(X1[h])) {
+                    const uint32_t f0 = mx_factor_bits(X0[h]) * 0x10001u;  // both halves
+                    const uint32_t f1 = mx_factor_bits(X1[h]) * 0x10001u;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const uint32_t f = j < 4 ? f0 : f1;  // words 0..3: k 0..31
                         const uint32_t fj[4] = {f, f, f, f};
-                        const uint4 o = mx_decode8_fast(w[j], fj);
+                        const uint4 o = mx_decode8_fast(w[h][j], fj);
                         d[4 * j] = o.x;
                         d[4 * j + 1] = o.y;
                         d[4 * j + 2] = o.z;
@@ -638,9 +656,9 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                 } else {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const uint32_t xb = j < 4 ? X0 : X1;
+                        const uint32_t xb = j < 4 ? X0[h] : X1[h];
                         const uint32_t x[8] = {xb, xb, xb, xb, xb, xb, xb, xb};
-                        const uint4 o = mx_decode8_exact(w[j], x);
+                        const uint4 o = mx_decode8_exact(w[h][j], x);
                         d[4 * j] = o.x;
                         d[4 * j + 1] = o.y;
                         d[4 * j + 2] = o.z;
@@ -653,12 +671,18 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                                d);
             }
             mx_tmem_wait_st();
+            // the unit's A tile (its load overlapped the decode): the MMA
+            // thread waits only for this warp's report
+            if (lane == 0)
+                ok = mbar_wait(bar_afull + 8 * stage, phase, p.timeout_ns, abort_flag) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) fail(kRoleConvert);
+                break;
+            }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(bar_rempty + 8 * rstage);
-                mbar_arrive(bar_dec + 8 * stage);
-            }
+            if (lane == 0) mbar_arrive(bar_dec + 8 * stage);
         }
     }
 

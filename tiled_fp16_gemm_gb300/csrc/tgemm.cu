@@ -80,8 +80,29 @@ constexpr int kPairGroupM = 16;
 // beside the epilogue's staging buffers).
 constexpr int kSpPairStages = 3;
 
-// 256×256 tiles on CTA pairs; grid = two CTAs per tile, at most num_sms.
-void plan_pair(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* p) {
+// What bounds a launch on one device: its SMs, the CTA pairs of the pair
+// kernel that fit on it at once, and the clusters of four skinny CTAs (Mp <=
+// 64, Mp <= 128) that do.  Clusters must sit inside one GPC, so the last
+// two can be below num_sms / 2 and num_sms / 4.
+struct PlanLimits {
+    int32_t num_sms;
+    int32_t pairs;
+    int32_t quads[2];
+};
+
+tg_status_t plan_limited(int64_t M, int64_t N, int64_t K, const PlanLimits& lim,
+                         tg_plan_t* plan);
+
+PlanLimits nominal_limits(int32_t num_sms) {
+    PlanLimits l;
+    l.num_sms = num_sms;
+    l.pairs = num_sms / 2;
+    l.quads[0] = l.quads[1] = num_sms / 4;
+    return l;
+}
+
+// 256×256 tiles on at most `pairs` CTA pairs (two CTAs per pair).
+void plan_pair(int64_t M, int64_t N, int64_t K, int32_t pairs, tg_plan_t* p) {
     p->kernel = TG_KERNEL_PERSISTENT;
     p->bm = 256;
     p->bn = 256;
@@ -93,7 +114,7 @@ void plan_pair(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* p) {
     p->tiles_n = ceil_div(N, 256);
     p->k_blocks = ceil_div(K, kPairBK);
     p->num_tiles = p->tiles_m * p->tiles_n;
-    const int32_t pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
+    if (pairs < 1) pairs = 1;
     int32_t P = 1, S = 1;
     tg::pair_launch_shape(static_cast<int32_t>(p->num_tiles), pairs,
                           static_cast<int32_t>(p->k_blocks), &P, &S);
@@ -126,6 +147,27 @@ struct DeviceState {
 
 std::mutex g_dev_mutex;
 DeviceState g_dev[kMaxDevices];
+
+PlanLimits device_limits(const DeviceState& ds) {
+    PlanLimits l;
+    l.num_sms = ds.num_sms;
+    l.pairs = ds.num_sms / 2 < ds.max_pairs ? ds.num_sms / 2 : ds.max_pairs;
+    l.quads[0] = ds.max_skinny_quads[0];
+    l.quads[1] = ds.max_skinny_quads[1];
+    return l;
+}
+
+// The shape of the last dense GEMM launch made by the calling thread
+// (tg_debug_last_launch): the plan it ran with, and the grid, pieces per
+// tile and cluster size it was actually launched with.
+thread_local tg_plan_t g_last_launch;
+
+void record_launch(const tg_plan_t& pl, int64_t grid, int64_t split, int32_t cluster) {
+    g_last_launch = pl;
+    g_last_launch.grid = grid;
+    g_last_launch.split_k = split;
+    g_last_launch.cluster = cluster;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -249,11 +291,72 @@ constexpr CUtensorMapDataType tensor_map_type() {
                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
+// Encoded tensor maps, keyed by everything the encoding depends on.  A map
+// holds only the address, extents, stride, box and modes it was made from
+// (no device or allocation state), so an entry stays valid for any later
+// call with the same key, whatever happened to the memory in between.  A
+// repeated call (same pointers, shape and leading dimensions) then skips the
+// encoding of its maps.  The table is direct-mapped: a colliding key
+// replaces the entry, so its size is fixed.
+struct MapKey {
+    const void* ptr;
+    uint64_t inner, outer, row_bytes;
+    uint32_t box_inner, box_outer;
+    int32_t dtype, swizzle;
+    bool operator==(const MapKey& o) const {
+        return ptr == o.ptr && inner == o.inner && outer == o.outer &&
+               row_bytes == o.row_bytes && box_inner == o.box_inner &&
+               box_outer == o.box_outer && dtype == o.dtype && swizzle == o.swizzle;
+    }
+};
+
+struct MapEntry {
+    bool used = false;
+    MapKey key{};
+    CUtensorMap map{};
+};
+
+constexpr int kMapCacheSlots = 1024;
+std::mutex g_map_mutex;
+MapEntry g_map_cache[kMapCacheSlots];
+std::atomic<uint64_t> g_map_hits{0}, g_map_misses{0};
+
+uint32_t map_slot(const MapKey& k) {
+    uint64_t h = reinterpret_cast<uintptr_t>(k.ptr) * 0x9E3779B97F4A7C15ull;
+    const uint64_t f[] = {k.inner, k.outer, k.row_bytes,
+                          (uint64_t{k.box_inner} << 32) | k.box_outer,
+                          (static_cast<uint64_t>(static_cast<uint32_t>(k.dtype)) << 32) |
+                              static_cast<uint32_t>(k.swizzle)};
+    for (uint64_t v : f) h = (h ^ v) * 0x100000001B3ull + (h >> 29);
+    return static_cast<uint32_t>((h ^ (h >> 32)) % kMapCacheSlots);
+}
+
 // 2-D tensor map: inner (contiguous) extent, outer extent, row stride in
-// bytes, box, swizzle, zero fill outside the tensor.
+// bytes, box, swizzle, zero fill outside the tensor.  Served from the cache
+// above when the same map was made before.
 bool encode_2d_sw(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                   CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle) {
+    MapKey key;
+    std::memset(&key, 0, sizeof(key));  // padding too: keys are compared field by field
+    key.ptr = ptr;
+    key.inner = inner;
+    key.outer = outer;
+    key.row_bytes = row_bytes;
+    key.box_inner = box_inner;
+    key.box_outer = box_outer;
+    key.dtype = static_cast<int32_t>(dtype);
+    key.swizzle = static_cast<int32_t>(swizzle);
+    const uint32_t slot = map_slot(key);
+    {
+        std::lock_guard<std::mutex> lk(g_map_mutex);
+        const MapEntry& e = g_map_cache[slot];
+        if (e.used && e.key == key) {
+            *map = e.map;
+            g_map_hits.fetch_add(1, std::memory_order_relaxed);
+            return true;
+        }
+    }
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[2] = {inner, outer};
@@ -263,7 +366,14 @@ bool encode_2d_sw(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t ou
     CUresult r = enc(map, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    if (r != CUDA_SUCCESS) return false;
+    g_map_misses.fetch_add(1, std::memory_order_relaxed);
+    std::lock_guard<std::mutex> lk(g_map_mutex);
+    MapEntry& e = g_map_cache[slot];
+    e.used = true;
+    e.key = key;
+    e.map = *map;
+    return true;
 }
 
 // The same with the 128-byte swizzle of every 16-bit operand tile.
@@ -325,6 +435,7 @@ tg_status_t launch_persistent(const void* A, const void* B, void* C, const tg_pl
     tg::set_dependent_launch(attr[0]);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    record_launch(pl, pl.grid, 1, 1);
     cudaError_t e =
         cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_persistent<BN, STAGES, T>, tmA, tmB, tmC, prm);
     if (e != cudaSuccess) {
@@ -351,9 +462,9 @@ tg_status_t launch_pair(const void* A, const void* B, void* C, const tg_plan_t& 
                        kPairBK))
         return TG_ERR_LAUNCH;
     tg::PersistentParams prm = persistent_params(pl, M, N, K, ep);
-    int32_t pairs = ds->num_sms / 2 < ds->max_pairs ? ds->num_sms / 2 : ds->max_pairs;
-    int32_t P = 1, S = 1;
-    tg::pair_launch_shape(prm.num_tiles, pairs, prm.k_blocks, &P, &S);
+    // the planner's shape: P pairs (within the pairs the device holds at
+    // once), tail tiles in S pieces
+    int32_t P = static_cast<int32_t>(pl.grid / 2), S = static_cast<int32_t>(pl.split_k);
     tg::SkinnyParams wsp;
     if (tg::splitk_workspace(dev, stream, ds->num_sms, ds->num_sms, &wsp) == TG_OK &&
         int64_t{P} * tg::kPairSlotFloats <= 2 * int64_t{ds->num_sms} * tg::kSkSlotFloats &&
@@ -361,9 +472,11 @@ tg_status_t launch_pair(const void* A, const void* B, void* C, const tg_plan_t& 
         prm.ws = wsp.ws;
         prm.counters = wsp.counters;
     } else if (S > 1) {
-        tg::pair_launch_shape(prm.num_tiles, pairs, 0, &P, &S);  // no split
+        // no workspace (out of memory): the same pairs, the last wave unsplit
+        tg::pair_launch_shape(prm.num_tiles, P, 0, &P, &S);
     }
     prm.split = S;
+    record_launch(pl, 2 * int64_t{P}, S, 2);
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -392,19 +505,26 @@ tg_status_t launch_pair(const void* A, const void* B, void* C, const tg_plan_t& 
 // overrides the planner's kernel choice (used by tests and tile sweeps);
 // ignored where the forced kernel does not apply (skinny needs M <= 128;
 // K == 0 always fills).
-void apply_forced_config(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* pl) {
+void apply_forced_config(int64_t M, int64_t N, int64_t K, const PlanLimits& lim,
+                         tg_plan_t* pl) {
     if (pl->kernel == TG_KERNEL_NONE || pl->kernel == TG_KERNEL_FILL) return;
+    const int32_t num_sms = lim.num_sms;
     const char* f = std::getenv("TGEMM_FORCE_CFG");
-    if (f != nullptr && std::strcmp(f, "pair256") == 0)
-        plan_pair(M, N, K, num_sms, pl);
+    if (f != nullptr && std::strcmp(f, "pair256") == 0 && lim.pairs >= 1)
+        plan_pair(M, N, K, lim.pairs, pl);
+    else if (f != nullptr && std::strcmp(f, "pair256") == 0)  // no pair fits: one-CTA tiles
+        plan_persistent(M, N, K, num_sms, kBigBN, kBigStages,
+                        tg::PersistentCfg<kBigBN, kBigStages>::kSmemBytes, pl);
     else if (f != nullptr && std::strcmp(f, "persistent256") == 0)
         plan_persistent(M, N, K, num_sms, kBigBN, kBigStages,
                         tg::PersistentCfg<kBigBN, kBigStages>::kSmemBytes, pl);
     else if (f != nullptr && std::strcmp(f, "persistent128") == 0)
         plan_persistent(M, N, K, num_sms, kMidBN, kMidStages,
                         tg::PersistentCfg<kMidBN, kMidStages>::kSmemBytes, pl);
-    else if (f != nullptr && std::strcmp(f, "skinny") == 0 && tg::skinny_applies(M, N, K))
+    else if (f != nullptr && std::strcmp(f, "skinny") == 0 && tg::skinny_applies(M, N, K)) {
         tg::skinny_plan(M, N, K, num_sms, pl);
+        if (pl->cluster == 4 && pl->grid / 4 > lim.quads[pl->mma_n > 64 ? 1 : 0]) pl->cluster = 1;
+    }
     // TGEMM_GROUP_M = row blocks per raster group of the persistent kernels
     // (for sweeps), clamped to [1, tiles_m].
     const char* g = std::getenv("TGEMM_GROUP_M");
@@ -501,14 +621,8 @@ tg_status_t launch_planned(tg_plan_t pl, const void* A, const void* B, void* C, 
                            const tg::EpilogueSpec& ep, cudaStream_t s, int dev, DeviceState* ds) {
     switch (pl.kernel) {
         case TG_KERNEL_PERSISTENT:
-            if (pl.cluster == 2) {
-                if (ds->max_pairs < 1) {  // cannot place a pair: one-CTA tiles instead
-                    plan_persistent(M, N, K, ds->num_sms, kBigBN, kBigStages,
-                                    tg::PersistentCfg<kBigBN, kBigStages>::kSmemBytes, &pl);
-                } else {
-                    return launch_pair<T>(A, B, C, pl, M, N, K, lda, ldb, ldc, ep, s, dev, ds);
-                }
-            }
+            if (pl.cluster == 2)
+                return launch_pair<T>(A, B, C, pl, M, N, K, lda, ldb, ldc, ep, s, dev, ds);
             if (pl.bn == kBigBN)
                 return launch_persistent<kBigBN, kBigStages, T>(A, B, C, pl, M, N, K, lda, ldb,
                                                                ldc, ep, s);
@@ -517,9 +631,7 @@ tg_status_t launch_planned(tg_plan_t pl, const void* A, const void* B, void* C, 
         case TG_KERNEL_SKINNY: {
             const uint64_t timeout = g_timeout_ns.load();
             const int32_t inject = g_inject.exchange(0);
-            // clusters of a tile's four k-pieces only if all of them fit at once
-            if (pl.cluster == 4 && pl.grid / 4 > ds->max_skinny_quads[pl.mma_n > 64 ? 1 : 0])
-                pl.cluster = 1;
+            record_launch(pl, pl.grid, pl.split_k, pl.cluster);
             return tg::skinny_launch<T>(A, B, C, pl, M, N, K, lda, ldb, ldc, ep, s, dev,
                                         ds->num_sms, timeout, inject, encode_2d);
         }
@@ -544,11 +656,13 @@ tg_status_t gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     tg_plan_t pl;
-    st = tg_plan_f16(M, N, K, ds->num_sms, &pl);
+    const PlanLimits lim = device_limits(*ds);
+    st = plan_limited(M, N, K, lim, &pl);
     if (st != TG_OK) return st;
-    apply_forced_config(M, N, K, ds->num_sms, &pl);
+    apply_forced_config(M, N, K, lim, &pl);
 
     if (pl.kernel == TG_KERNEL_FILL) {
+        record_launch(pl, pl.grid, pl.split_k, pl.cluster);
         if (ep.e.bias == nullptr && ep.e.resid == nullptr && !ep.out_f32) {
             // +0 has the same (all-zero) bits in fp16 and bf16; any ldc works
             tg::tg_fill_zero_f16<<<static_cast<unsigned>(pl.grid), 256, 0, s>>>(
@@ -737,20 +851,10 @@ tg_status_t launch_sp24(const void* Ac, const void* E, const void* B, void* C, i
     return TG_OK;
 }
 
-}  // namespace
-
-// ====================================================================== C ABI
-
-extern "C" {
-
-int64_t tg_ring_bytes(int32_t bm, int32_t bn, int32_t bk, int32_t stages, int32_t elem_bytes) {
-    if (bm <= 0 || bn <= 0 || bk <= 0 || stages <= 0 || elem_bytes <= 0) return -1;
-    const int64_t per_stage = (static_cast<int64_t>(bm) * bk + static_cast<int64_t>(bk) * bn) *
-                              elem_bytes;
-    return per_stage * stages;
-}
-
-tg_status_t tg_plan_f16(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* plan) {
+// The plan tg_gemm_f16 launches, within the limits of a device.
+tg_status_t plan_limited(int64_t M, int64_t N, int64_t K, const PlanLimits& lim,
+                         tg_plan_t* plan) {
+    const int32_t num_sms = lim.num_sms;
     if (plan == nullptr || num_sms < 1) return TG_ERR_INVALID_VALUE;
     if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
         return TG_ERR_INVALID_VALUE;
@@ -768,12 +872,16 @@ tg_status_t tg_plan_f16(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_pla
     }
     if (tg::skinny_applies(M, N, K)) {
         tg::skinny_plan(M, N, K, num_sms, plan);
+        // clusters of a tile's four k-pieces only if all of them fit at once
+        // (a second round of clusters would double the time)
+        if (plan->cluster == 4 && plan->grid / 4 > lim.quads[plan->mma_n > 64 ? 1 : 0])
+            plan->cluster = 1;
         return TG_OK;
     }
     // At least one full wave of 256×256 tiles on CTA pairs: the pair kernel.
     const int64_t tiles_pair = ceil_div(M, 256) * ceil_div(N, 256);
-    if (num_sms >= 2 && tiles_pair >= num_sms / 2) {
-        plan_pair(M, N, K, num_sms, plan);
+    if (lim.pairs >= 1 && tiles_pair >= lim.pairs) {
+        plan_pair(M, N, K, lim.pairs, plan);
         return TG_OK;
     }
     // Less than a wave of pair tiles, but more 128×128 tiles than SMs (one-CTA
@@ -784,8 +892,8 @@ tg_status_t tg_plan_f16(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_pla
     // 2048×2048×1024 14.1 µs against 16.4 µs.  With shorter K the pair kernel's
     // longer pipeline fill loses (2048×2048×256: 10.3 µs against 8.3 µs).
     const int64_t tiles128 = ceil_div(M, 128) * ceil_div(N, 128);
-    if (num_sms >= 2 && tiles128 > num_sms && K >= 1024) {
-        plan_pair(M, N, K, num_sms, plan);
+    if (lim.pairs >= 1 && tiles128 > num_sms && K >= 1024) {
+        plan_pair(M, N, K, lim.pairs, plan);
         return TG_OK;
     }
     const int64_t tiles256 = ceil_div(M, 128) * ceil_div(N, kBigBN);
@@ -802,6 +910,65 @@ tg_status_t tg_plan_f16(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_pla
     }
     return TG_OK;
 }
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+int64_t tg_ring_bytes(int32_t bm, int32_t bn, int32_t bk, int32_t stages, int32_t elem_bytes) {
+    if (bm <= 0 || bn <= 0 || bk <= 0 || stages <= 0 || elem_bytes <= 0) return -1;
+    const int64_t per_stage = (static_cast<int64_t>(bm) * bk + static_cast<int64_t>(bk) * bn) *
+                              elem_bytes;
+    return per_stage * stages;
+}
+
+tg_status_t tg_plan_f16(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* plan) {
+    if (num_sms < 1) return TG_ERR_INVALID_VALUE;
+    return plan_limited(M, N, K, nominal_limits(num_sms), plan);
+}
+
+tg_status_t tg_plan_f16_limits(int64_t M, int64_t N, int64_t K, int32_t num_sms,
+                               int32_t max_pairs, int32_t max_quads_narrow,
+                               int32_t max_quads_wide, tg_plan_t* plan) {
+    if (num_sms < 1 || max_pairs < 0 || max_quads_narrow < 0 || max_quads_wide < 0)
+        return TG_ERR_INVALID_VALUE;
+    PlanLimits l;
+    l.num_sms = num_sms;
+    l.pairs = max_pairs < num_sms / 2 ? max_pairs : num_sms / 2;
+    l.quads[0] = max_quads_narrow;
+    l.quads[1] = max_quads_wide;
+    return plan_limited(M, N, K, l, plan);
+}
+
+tg_status_t tg_device_limits(int32_t* num_sms, int32_t* max_pairs, int32_t* max_quads_narrow,
+                             int32_t* max_quads_wide) {
+    if (num_sms == nullptr || max_pairs == nullptr || max_quads_narrow == nullptr ||
+        max_quads_wide == nullptr)
+        return TG_ERR_INVALID_VALUE;
+    int dev = 0;
+    DeviceState* ds = nullptr;
+    const tg_status_t st = current_device(&dev, &ds);
+    if (st != TG_OK) return st;
+    *num_sms = ds->num_sms;
+    *max_pairs = ds->max_pairs;
+    *max_quads_narrow = ds->max_skinny_quads[0];
+    *max_quads_wide = ds->max_skinny_quads[1];
+    return TG_OK;
+}
+
+tg_status_t tg_debug_last_launch(tg_plan_t* plan) {
+    if (plan == nullptr) return TG_ERR_INVALID_VALUE;
+    *plan = g_last_launch;
+    return TG_OK;
+}
+
+void tg_debug_map_cache_stats(uint64_t* hits, uint64_t* misses) {
+    if (hits != nullptr) *hits = g_map_hits.load();
+    if (misses != nullptr) *misses = g_map_misses.load();
+}
+
 
 tg_status_t tg_tile_coord(const tg_plan_t* plan, int64_t tile, int64_t* m_blk, int64_t* n_blk) {
     if (plan == nullptr || m_blk == nullptr || n_blk == nullptr) return TG_ERR_INVALID_VALUE;
@@ -1249,8 +1416,8 @@ extern "C" tg_status_t tg_gemm_f16_noalloc(const void* A, const void* B, void* C
     }
 
     tg_plan_t pl;
-    std::memset(&pl, 0, sizeof(pl));
-    tg::skinny_plan(M, N, K, ds->num_sms, &pl);
+    if ((st = plan_limited(M, N, K, device_limits(*ds), &pl)) != TG_OK) return st;
+    if (pl.kernel != TG_KERNEL_SKINNY) return TG_ERR_INVALID_VALUE;
     if (pl.grid > kNoallocMaxCtas ||
         kNoallocCounterBytes + 2 * pl.grid * tg::kSkSlotFloats * 4 > TG_NOALLOC_SCRATCH_BYTES)
         return TG_ERR_INVALID_VALUE;  // would need more scratch than the array holds
@@ -1301,9 +1468,8 @@ extern "C" tg_status_t tg_gemm_f16_noalloc(const void* A, const void* B, void* C
     prm.C = C;
     prm.ldc = ldc;
 
-    const int32_t cluster =
-        pl.cluster == 4 && pl.grid / 4 <= ds->max_skinny_quads[Mp > 64 ? 1 : 0] ? 4 : 1;
-    if (tg::skinny_launch_kernel<__half>(tmB, tmA, prm, pl.grid, s, cluster) != cudaSuccess) {
+    record_launch(pl, pl.grid, pl.split_k, pl.cluster);
+    if (tg::skinny_launch_kernel<__half>(tmB, tmA, prm, pl.grid, s, pl.cluster) != cudaSuccess) {
         cudaGetLastError();
         return TG_ERR_LAUNCH;
     }
