@@ -78,61 +78,71 @@ struct SkinnyCfg {
 using SkinnyNarrow = SkinnyCfg<9, 64, 64>;
 using SkinnyWide = SkinnyCfg<6, 128, 64>;
 // MXFP4 B (M ≤ 128 weight streaming), units of kMxBK = 128 k.
-//   Raw ring (deep, four producer threads): per unit, two 128 n × 64 k tiles
-//     of packed codes (128 rows × 32 bytes each, TMA 32-byte swizzle) and
-//     their scales (4 rows × 128 bytes).  The codes are the HBM stream; ~130
-//     KB of them in flight per SM takes 16 stages.
-//   A ring (one producer thread): the unit's activation tile (from L2,
-//     re-read by every CTA).  Were it in the raw ring it would take most of
-//     each stage (16 KB against 8.5 KB) and cap the codes in flight.  It is
-//     indexed like the tensor-memory operand stages (4 of each), so the one
-//     MMA commit per unit frees both.
-//   Converters (two groups of four warps, one per tensor-memory lane
-//     quarter, alternate units): thread n owns weight column n of the tile,
-//     decodes its 128 k into fp16 and writes them with tcgen05.st straight
-//     into the operand stage (the weight tile is the A operand of the swapped
-//     product), so decoded weights never pass through shared memory.  A
-//     group also waits for the unit's A tile before it reports the operand
-//     decoded, so the MMA thread waits on one barrier per unit.
-//   Tensor memory: two accumulators (256 columns) and 4 operand stages of 64
-//     columns.
-// The MMA thread sets the pace (about 80 cycles per MMA issue, measured with
-// clock stamps); 128 k per unit spreads its per-unit wait, fence and commit
-// over 8 MMAs.  A raw stage is free once its group has decoded it; an
-// operand stage and its A stage once the MMAs that read them have completed.
+//   Raw ring (four producer threads): per unit, two 128 n × 64 k tiles of
+//     packed codes (128 rows × 32 bytes each, TMA 32-byte swizzle) and their
+//     scales (4 rows × 128 bytes).  The codes are the HBM stream; 8 stages
+//     (68 KB) keep enough of it in flight per SM.
+//   A ring (one producer thread, its own depth): the unit's activation tile
+//     (from L2, re-read by every CTA).  A stage is released by a commit of
+//     its own once the unit's MMAs have completed.  Tied to the operand
+//     stages, a 4-deep ring let each tile be requested only 4 units ahead,
+//     and its L2 round trip under the HBM stream then set the pace.
+//   Converters (kMxGroups groups of four warps, one per tensor-memory lane
+//     quarter, taking units in turn): thread n owns weight column n of the
+//     tile, loads its 128 k of codes and the unit's scales into registers
+//     (which frees the raw stage), decodes them into fp16 and writes them
+//     with tcgen05.st straight into the unit's operand stage (the weight
+//     tile is the A operand of the swapped product), so decoded weights
+//     never pass through shared memory.
+//   Tensor memory: two accumulators of MP_MAX columns, then operand stages
+//     of 64 columns in the rest (6 for Mp ≤ 64, 4 for Mp ≤ 128).
+// The MMA thread waits for the unit's operand stage (decoded) and its A
+// stage (landed), issues 8 MMAs and commits twice: the operand stage back to
+// the converters, the A stage back to its producer.
 constexpr int kMxBK = 128;                       // k per MXFP4 unit
 constexpr uint32_t kMxCodeBox = 128 * 32;        // one 64-k tile of codes
 constexpr uint32_t kMxRawBytes = (kMxBK / 64) * kMxCodeBox;
 constexpr uint32_t kMxScaleBytes = (kMxBK / 32) * 128;
 constexpr uint32_t kMxOpCols = kMxBK / 2;        // tensor-memory columns per operand stage
-constexpr int kMxConvWarps = 8;
-constexpr int kMxGroups = kMxConvWarps / 4;
+constexpr int kMxGroups = 3;
+constexpr int kMxConvWarps = 4 * kMxGroups;
+// Two MMA warps take a segment's units in turn, each into its own
+// accumulator; the epilogue adds the two (first warp's first).  One warp's
+// wait, issue and loop per unit took about twice the tensor pipe's 256
+// cycles of MMA work, and its MMA issue blocks until the pipe takes them, so
+// with one warp the pipe idled for the rest.
+constexpr int kMxMmaWarps = 2;
 constexpr uint32_t kMxTmemCols = 512;
-constexpr uint32_t kMxOpCol0 = 256;  // first tensor-memory column of the operand stages
-// Raw ring depth (codes + scales; as deep as shared memory allows beside 8
-// A stages of MP_MAX rows).
-__host__ __device__ constexpr int mx_raw_stages(int mp_max) { return mp_max <= 64 ? 16 : 8; }
+constexpr int kMxRawStages = 8;
+__host__ __device__ constexpr int mx_raw_stages(int mp_max) { return (void)mp_max, kMxRawStages; }
+// first tensor-memory column of the operand stages: after the accumulators
+// (one per MMA warp; a CTA's unit range spans at most a few tile segments,
+// so they are not double-buffered)
+__host__ __device__ constexpr uint32_t mx_op_col0(int mp_max) { return kMxMmaWarps * mp_max; }
+__host__ __device__ constexpr int mx_op_stages(int mp_max) {
+    return static_cast<int>((kMxTmemCols - mx_op_col0(mp_max)) / kMxOpCols);
+}
 constexpr uint32_t kMxBarBytes = 1024;
-template <int STAGES, int MP_MAX>
+template <int MP_MAX>
 struct SkinnyMxCfg {
-    static constexpr int kStages = STAGES;  // tensor-memory operand stages = A stages
-    static constexpr int kRawStages = mx_raw_stages(MP_MAX);
-    static constexpr int kAStages = STAGES;
+    static constexpr int kStages = mx_op_stages(MP_MAX);  // tensor-memory operand stages
+    static constexpr int kRawStages = kMxRawStages;
     static constexpr uint32_t kASlot = MP_MAX * kMxBK * 2;
+    static constexpr int kAStages = MP_MAX <= 64 ? 8 : 4;  // 128 KB of activation tiles
     static constexpr uint32_t kStageBytes = 0;  // no shared-memory operand ring
     static constexpr uint32_t kRawStageBytes = kMxRawBytes + kMxScaleBytes;
     static constexpr uint32_t kSmemBytes =
         1024 + kRawStages * kRawStageBytes + kAStages * kASlot + kMxBarBytes;
-    static_assert(kMxOpCol0 + kMxOpCols * STAGES <= kMxTmemCols,
+    static_assert(mx_op_col0(MP_MAX) + kMxOpCols * kStages <= kMxTmemCols,
                   "operand stages exceed tensor memory");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeded");
     // barriers: full/empty/dec per operand stage, rfull/rempty per raw stage,
-    // afull per A stage, two tfull, two tempty, drain, TMEM slot + flag
-    static_assert(8 * (3 * STAGES + 2 * kRawStages + kAStages) + 48 <= kMxBarBytes,
+    // afull/aempty per A stage, two tfull, two tempty, drain, TMEM slot + flag
+    static_assert(8 * (3 * kStages + 2 * kRawStages + 2 * kAStages) + 48 <= kMxBarBytes,
                   "barrier area too small");
 };
-using SkinnyMxNarrow = SkinnyMxCfg<4, 64>;
-using SkinnyMxWide = SkinnyMxCfg<4, 128>;
+using SkinnyMxNarrow = SkinnyMxCfg<64>;
+using SkinnyMxWide = SkinnyMxCfg<128>;
 constexpr unsigned int kRoleConvert = 16u;
 
 // Load issue is split over several producer threads (one per warp): one
@@ -145,10 +155,10 @@ __host__ __device__ constexpr int skinny_producers(int ring) {
     return ring % 4 == 0 ? 4 : (ring % 3 == 0 ? 3 : (ring % 2 == 0 ? 2 : 1));
 }
 // Threads of a skinny kernel: producer 0, MMA, 4 epilogue warps, the
-// converter warps (MXFP4), producers 1 .. count - 1, then (MXFP4) the
-// producer of the A ring.
+// converter warps and the second MMA warp (MXFP4), producers 1 .. count - 1,
+// then (MXFP4) the producer of the A ring.
 __host__ __device__ constexpr int skinny_threads(int stages, int mp_max, bool qb) {
-    return 32 * (6 + (qb ? kMxConvWarps + 1 : 0) +
+    return 32 * (6 + (qb ? kMxConvWarps + 2 : 0) +
                  skinny_producers(qb ? mx_raw_stages(mp_max) : stages) - 1);
 }
 constexpr uint32_t kSkTmemCols = 256;        // two accumulators of up to 128 columns
@@ -198,8 +208,15 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
     uint8_t* const base_ptr = smem_raw + (base - raw);
 
     constexpr int kRaw = QB ? mx_raw_stages(MP_MAX) : 0;  // raw ring depth (QB)
-    constexpr int kAS = QB ? kSkStages : 0;               // A ring depth (QB): the operand stages
+    constexpr int kAS = QB ? SkinnyMxCfg<MP_MAX>::kAStages : 0;  // A ring depth (QB)
     constexpr int kARing = QB ? kAS : kSkStages;          // A slots: own ring, or with B
+    // tensor-memory columns: accumulator stride, first operand-stage column (QB)
+    constexpr uint32_t kAccStride = QB ? static_cast<uint32_t>(MP_MAX) : 128u;
+    constexpr uint32_t kOpCol0 = QB ? mx_op_col0(MP_MAX) : 0u;
+    // MMA warps, and accumulator buffers per MMA warp (segments alternate
+    // over the buffers): accumulator (buffer b, warp m) is number b·kMW + m
+    constexpr int kMW = QB ? kMxMmaWarps : 1;
+    constexpr int kBufs = QB ? 1 : 2;
     constexpr int kBRing = QB ? 0 : kSkStages;            // B^T tiles in shared memory
     const uint32_t sB = base;                             // [kBRing] B^T tiles
     const uint32_t sA = sB + kBRing * kSkBBytes;          // [kARing] A tiles
@@ -213,7 +230,8 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
     const uint32_t bar_rfull = bar_dec + (QB ? 8 * kSkStages : 0);  // QB: [raw] landed
     const uint32_t bar_rempty = bar_rfull + 8 * kRaw;     // QB: [raw] decoded
     const uint32_t bar_afull = bar_rempty + 8 * kRaw;     // QB: [A stages] landed
-    const uint32_t bar_tfull = bar_afull + 8 * kAS;
+    const uint32_t bar_aempty = bar_afull + 8 * kAS;      // QB: [A stages] MMAs done
+    const uint32_t bar_tfull = bar_aempty + 8 * kAS;
     const uint32_t bar_tempty = bar_tfull + 16;
     const uint32_t bar_drain = bar_tempty + 16;
     const uint32_t slot_tmem = bar_drain + 8;
@@ -240,13 +258,16 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                 mbar_init(bar_rfull + 8 * r, 1);
                 mbar_init(bar_rempty + 8 * r, 4);  // the group's four warps
             }
-            for (int a = 0; a < kAS; ++a) mbar_init(bar_afull + 8 * a, 1);
+            for (int a = 0; a < kAS; ++a) {
+                mbar_init(bar_afull + 8 * a, 1);
+                mbar_init(bar_aempty + 8 * a, 1);
+            }
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(bar_tfull + 8 * a, 1);
+            mbar_init(bar_tfull + 8 * a, kMW);  // one commit per MMA warp
             mbar_init(bar_tempty + 8 * a, 4);
         }
-        mbar_init(bar_drain, 1);
+        mbar_init(bar_drain, kMW);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -301,7 +322,8 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
     constexpr int kRing = QB ? kRaw : kSkStages;
     constexpr int kProd = skinny_producers(kRing);
     static_assert(kRing % kProd == 0, "each ring stage must belong to one producer thread");
-    constexpr int kProdWarp1 = 6 + (QB ? kMxConvWarps : 0);  // warp of producer 1
+    constexpr int kMma2Warp = QB ? 6 + kMxConvWarps : -1;  // QB: the second MMA warp
+    constexpr int kProdWarp1 = 6 + (QB ? kMxConvWarps + 1 : 0);  // warp of producer 1
     constexpr int kAProdWarp = QB ? kProdWarp1 + kProd - 1 : -1;  // QB: A ring producer
     const int prod = warp == 0 ? 0
                      : (warp >= kProdWarp1 && warp < kProdWarp1 + kProd - 1 ? warp - kProdWarp1 + 1
@@ -368,8 +390,8 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
             for (int64_t i = 0; u_begin + i < u_end; ++i) {
                 const int stage = static_cast<int>(i % kAS);
                 const uint32_t phase = static_cast<uint32_t>((i / kAS) & 1);
-                // the MMAs of the unit kAS earlier (same operand stage) are done
-                if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.timeout_ns, abort_flag)) {
+                // the MMAs of the unit kAS earlier (same A stage) are done
+                if (!mbar_wait(bar_aempty + 8 * stage, phase ^ 1u, p.timeout_ns, abort_flag)) {
                     fail(kRoleProducer);
                     break;
                 }
@@ -389,37 +411,41 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                                    nullptr))
                         atomicOr(&g_wait_timeout_flags, kRoleDrain);
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == kMma2Warp) {
         // ------------------------------------------------------------ MMA issuer
         // The whole warp runs the loop (warp-uniform control flow and
         // operands); one elected lane issues each MMA and commit.  A wait
-        // counts as met only if every lane saw it met.
+        // counts as met only if every lane saw it met.  QB: MMA warp m takes
+        // the units u + m, u + m + kMW, ... of each segment [u, seg_end).
         auto warp_wait = [&](uint32_t bar, uint32_t parity, const volatile int* ab) {
             const bool r = mbar_wait(bar, parity, p.timeout_ns, ab);
             return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
         };
+        const int m = warp == 1 ? 0 : 1;
         // fp16 B: A operand = B^T tile, MN-major in shared memory.  QB: A
         // operand = decoded weights in tensor memory (K-major).
         const uint32_t idesc =
             idesc_f16_f32(128, p.Mp, /*a_mn=*/!QB, /*b_mn=*/false, Elem16<T>::kFmt);
-        int stage = 0;
-        uint32_t phase = 0;
         int it = 0;
         bool ok = true;
         for (int64_t u = u_begin; ok && u < u_end; ++it) {
             const int64_t t = u / KB;
             const int64_t seg_end = (t + 1) * KB < u_end ? (t + 1) * KB : u_end;
-            const int acc = it & 1;
-            const uint32_t acc_phase = (it >> 1) & 1;
-            if (!warp_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag)) {
+            const int buf = it % kBufs;
+            const uint32_t buf_phase = static_cast<uint32_t>((it / kBufs) & 1);
+            if (!warp_wait(bar_tempty + 8 * buf, buf_phase ^ 1u, abort_flag)) {
                 if (lane == 0) fail(kRoleMma);
                 break;
             }
             tc_fence_after_sync();
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 128);
-            for (int64_t v = u; v < seg_end; ++v) {
+            const uint32_t d_tmem =
+                tmem_base + static_cast<uint32_t>(buf * kMW + m) * kAccStride;
+            for (int64_t v = u + m; v < seg_end; v += kMW) {
+                const int64_t i = v - u_begin;  // local unit index
+                const int stage = static_cast<int>(i % kSkStages);
+                const uint32_t phase = static_cast<uint32_t>((i / kSkStages) & 1);
                 // QB: B^T decoded into the operand stage, and (the
-                // converters waited for it) that stage's A tile landed
+                // converters waited for it) the unit's A tile landed
                 const bool got = warp_wait(QB ? bar_dec + 8 * stage : bar_full + 8 * stage,
                                            phase, abort_flag);
                 if (!got) {
@@ -428,35 +454,33 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t b0 = sB + stage * kSkBBytes;
-                const uint32_t a0 = sA + stage * kSkASlot;
+                if constexpr (QB) {
+                    static_assert(BK == 128, "the unit issue below covers 128 k");
+                    const int astage = static_cast<int>(i % kAS);
+                    mx_unit_mma_elect<kABox / 16>(
+                        d_tmem, tmem_base + kOpCol0 + static_cast<uint32_t>(kMxOpCols * stage),
+                        smem_desc_sw128(sA + astage * kSkASlot, 16, 1024), idesc,
+                        v - u < kMW ? 1u : 0u, bar_empty + 8 * stage, bar_aempty + 8 * astage);
+                } else {
+                    const uint32_t b0 = sB + stage * kSkBBytes;
+                    const uint32_t a0 = sA + stage * kSkASlot;
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k) {
-                    // A tile: 64-k boxes kABox apart, 32 B per 16 k inside one
-                    const uint64_t bdesc =
-                        smem_desc_sw128(a0 + kABox * (k / 4) + 32 * (k % 4), 16, 1024);
-                    const uint32_t acc_in = (v != u || k != 0) ? 1u : 0u;
-                    if constexpr (QB) {
-                        // 16 k = 8 columns of the operand stage
-                        const uint32_t a_tmem = tmem_base + kMxOpCol0 +
-                                                static_cast<uint32_t>(kMxOpCols * stage + 8 * k);
-                        mma_f16_ts_elect(d_tmem, a_tmem, bdesc, idesc, acc_in);
-                    } else {
-                        // B^T: 16 k rows (2 KB) per step; the two 64-column
-                        // boxes kSkBBytes / 2 apart
+                    for (int k = 0; k < BK / 16; ++k) {
+                        // A tile: 64-k boxes kABox apart, 32 B per 16 k inside one
+                        const uint64_t bdesc =
+                            smem_desc_sw128(a0 + kABox * (k / 4) + 32 * (k % 4), 16, 1024);
+                        const uint32_t acc_in = (v != u || k != 0) ? 1u : 0u;
+                        // B^T: 16 k rows (2 KB) per step; the two 64-column boxes
+                        // kSkBBytes / 2 apart
                         const uint64_t adesc =
                             smem_desc_sw128(b0 + 2048 * k, kSkBBytes / 2, 1024);
                         mma_f16_ss_elect(d_tmem, adesc, bdesc, idesc, acc_in);
                     }
-                }
-                mma_commit_elect(bar_empty + 8 * stage);  // QB: the operand and A stages
-                if (++stage == kSkStages) {
-                    stage = 0;
-                    phase ^= 1u;
+                    mma_commit_elect(bar_empty + 8 * stage);
                 }
             }
             if (!ok) break;
-            if (!(p.inject == 1 && it == 0)) mma_commit_elect(bar_tfull + 8 * acc);
+            if (!(p.inject == 1 && it == 0)) mma_commit_elect(bar_tfull + 8 * buf);
             u = seg_end;
         }
         mma_commit_elect(bar_drain);
@@ -474,8 +498,8 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
             const int64_t kb0 = u - t * KB;
             const int64_t seg_end = (t + 1) * KB < u_end ? (t + 1) * KB : u_end;
             const int64_t kb1 = seg_end - t * KB;
-            const int acc = it & 1;
-            const uint32_t acc_phase = (it >> 1) & 1;
+            const int acc = it % kBufs;
+            const uint32_t acc_phase = static_cast<uint32_t>((it / kBufs) & 1);
             const int64_t n = t * 128 + n_local;
             int ok = 1;
             if (lane == 0)
@@ -486,7 +510,22 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                 break;
             }
             tc_fence_after_sync();
-            const uint32_t tacc = tmem_base + lane_addr + static_cast<uint32_t>(acc * 128);
+            const uint32_t tacc =
+                tmem_base + lane_addr + static_cast<uint32_t>(acc * kMW) * kAccStride;
+            // QB: the second MMA warp's accumulator holds units iff the
+            // segment has two or more
+            const bool two = kMW > 1 && seg_end - u >= 2;
+            // chunk c (16 m) of this thread's column: the accumulators' sum
+            auto load_acc = [&](int c, uint32_t (&r)[16]) {
+                tmem_ld_x16(tacc + 16 * c, r);
+                if (two) {
+                    uint32_t r2[16];
+                    tmem_ld_x16(tacc + kAccStride + 16 * c, r2);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+                }
+            };
 
             // The slots this warp sums, in k order (none: a FULL segment,
             // summed from tensor memory alone).
@@ -498,7 +537,7 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                 float* slot = p.ws + my_slot * kSkSlotFloats;
                 for (int c = 0; c < nchunks; ++c) {
                     uint32_t r[16];
-                    tmem_ld_x16(tacc + 16 * c, r);
+                    load_acc(c, r);
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         __stcg(slot + (16 * c + i) * 128 + n_local, __uint_as_float(r[i]));
@@ -532,7 +571,7 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                 float v[16];
                 if (c_last < 0) {
                     uint32_t r[16];
-                    tmem_ld_x16(tacc + 16 * c, r);
+                    load_acc(c, r);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
                 } else {
@@ -666,15 +705,18 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                     }
                 }
                 __syncwarp();
-                mx_tmem_st_x32(tmem_base + lane_addr + kMxOpCol0 +
+                mx_tmem_st_x32(tmem_base + lane_addr + kOpCol0 +
                                    static_cast<uint32_t>(kMxOpCols * stage + 32 * h),
                                d);
             }
             mx_tmem_wait_st();
             // the unit's A tile (its load overlapped the decode): the MMA
-            // thread waits only for this warp's report
+            // warp then waits on one barrier per unit
             if (lane == 0)
-                ok = mbar_wait(bar_afull + 8 * stage, phase, p.timeout_ns, abort_flag) ? 1 : 0;
+                ok = mbar_wait(bar_afull + 8 * static_cast<int>(i % kAS),
+                               static_cast<uint32_t>((i / kAS) & 1), p.timeout_ns, abort_flag)
+                         ? 1
+                         : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
                 if (lane == 0) fail(kRoleConvert);

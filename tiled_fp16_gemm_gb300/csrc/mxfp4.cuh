@@ -64,6 +64,47 @@ __device__ __forceinline__ void mx_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, 
         : "memory");
 }
 
+// The eight MMAs of one 128-k MXFP4 unit and its two release commits, issued
+// by one elected lane of a converged warp in one block: D (+)= W · Xᵀ with
+// the decoded weights W (128 n × 16 k per MMA) at tensor-memory columns
+// a_tmem + 8 k and the activation tile X in shared memory, its descriptor
+// b_desc advanced 32 bytes per 16 k inside a 64-k box and BOX16 (the box
+// size in 16-byte units) from one box to the next.  first != 0: the first
+// MMA overwrites D.  Fewer instructions per unit on the issuing warp, which
+// shares its scheduler with the decoding warps.
+template <uint32_t BOX16>
+__device__ __forceinline__ void mx_unit_mma_elect(uint32_t d_tmem, uint32_t a_tmem,
+                                                  uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t first, uint32_t bar_op,
+                                                  uint32_t bar_a) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b32 a;\n\t.reg .b64 b;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.eq.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 t, 0, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "add.u32 a, %1, 8;\n\tadd.u64 b, %2, 2;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+        "add.u32 a, %1, 16;\n\tadd.u64 b, %2, 4;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+        "add.u32 a, %1, 24;\n\tadd.u64 b, %2, 6;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+        "add.u32 a, %1, 32;\n\tadd.u64 b, %2, %7;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+        "add.u32 a, %1, 40;\n\tadd.u64 b, b, 2;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+        "add.u32 a, %1, 48;\n\tadd.u64 b, b, 2;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+        "add.u32 a, %1, 56;\n\tadd.u64 b, b, 2;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
+        "}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(first), "r"(bar_op), "r"(bar_a),
+        "n"(BOX16)
+        : "memory");
+}
+
 // This warp's 32 lanes (its lane quarter) × 32 consecutive 32-bit columns.
 __device__ __forceinline__ void mx_tmem_st_x32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
