@@ -104,8 +104,12 @@ constexpr uint32_t kMxCodeBox = 128 * 32;        // one 64-k tile of codes
 constexpr uint32_t kMxRawBytes = (kMxBK / 64) * kMxCodeBox;
 constexpr uint32_t kMxScaleBytes = (kMxBK / 32) * 128;
 constexpr uint32_t kMxOpCols = kMxBK / 2;        // tensor-memory columns per operand stage
+// Converter groups of four warps (one per tensor-memory lane quarter, both
+// 64-k halves of a unit each) or eight (two per quarter, one half each).
 constexpr int kMxGroups = 3;
-constexpr int kMxConvWarps = 4 * kMxGroups;
+constexpr int kMxGroupWarps = 4;
+constexpr int kMxHalvesPerWarp = 8 / kMxGroupWarps;
+constexpr int kMxConvWarps = kMxGroupWarps * kMxGroups;
 // Two MMA warps take a segment's units in turn, each into its own
 // accumulator; the epilogue adds the two (first warp's first).  One warp's
 // wait, issue and loop per unit took about twice the tensor pipe's 256
@@ -251,12 +255,12 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
         for (int s = 0; s < kSkStages; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
-            if (QB) mbar_init(bar_dec + 8 * s, 4);  // the four warps of one group
+            if (QB) mbar_init(bar_dec + 8 * s, kMxGroupWarps);  // the warps of one group
         }
         if (QB) {
             for (int r = 0; r < kRaw; ++r) {
                 mbar_init(bar_rfull + 8 * r, 1);
-                mbar_init(bar_rempty + 8 * r, 4);  // the group's four warps
+                mbar_init(bar_rempty + 8 * r, kMxGroupWarps);  // the group's warps
             }
             for (int a = 0; a < kAS; ++a) {
                 mbar_init(bar_afull + 8 * a, 1);
@@ -618,18 +622,22 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
     } else if constexpr (QB) {
         // ------------------------------------------------------------ converters (QB)
         // (warps 6 .. 6 + kMxConvWarps - 1)
-        // Warp cw = warp - 6 is in group g = cw / 4 and owns tensor-memory
-        // lane quarter q = warp % 4.  For each unit of local index i ≡ g (mod
-        // kMxGroups), thread l decodes column n = 32 q + l of the tile: its 64
-        // k codes (32 bytes: row n of the codes tile, 32-byte swizzle) with the
-        // two block scales of the unit, into 32 columns of fp16 pairs (lower k
-        // in the low half), stored to its lane of the unit's operand stage.
+        // Warp cw = warp - 6 is in group g = cw / kMxGroupWarps, owns
+        // tensor-memory lane quarter q = warp % 4 and decodes half hh =
+        // (cw % kMxGroupWarps) / 4 (k 64 hh .. 64 hh + 63) of each unit of
+        // local index i ≡ g (mod kMxGroups): thread l decodes column n = 32 q
+        // + l, its 64 k codes (32 bytes: row n of the codes tile, 32-byte
+        // swizzle) with the half's two block scales, into 32 columns of fp16
+        // pairs (lower k in the low half), stored to its lane of the unit's
+        // operand stage.
         const int cw = warp - 6;
-        const int g = cw / 4;
+        const int g = cw / kMxGroupWarps;
+        const uint32_t hh0 = static_cast<uint32_t>((cw % kMxGroupWarps) / 4 * kMxHalvesPerWarp);
         const uint32_t q = static_cast<uint32_t>(warp & 3);
         const uint32_t n_local = 32u * q + static_cast<uint32_t>(lane);
         const uint32_t swz32 = (n_local >> 2) & 1u;
         const uint32_t lane_addr = (32u * q) << 16;
+        static_assert(BK == 128 || !QB, "two 64-k halves per unit");
         for (int64_t i = g; u_begin + i < u_end; i += kMxGroups) {
             const int stage = static_cast<int>(i % kSkStages);
             const uint32_t phase = static_cast<uint32_t>((i / kSkStages) & 1);
@@ -651,18 +659,20 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                 break;
             }
             tc_fence_after_sync();
-            // The unit's codes and scales into registers, then the raw stage
-            // is free for the next load.
-            uint32_t w[BK / 64][8];
-            uint32_t X0[BK / 64], X1[BK / 64];
+            // This half's codes and scales into registers, then the raw
+            // stage is free for the next load (once the group's warps all
+            // have theirs).
+            uint32_t w[kMxHalvesPerWarp][8];
+            uint32_t X0[kMxHalvesPerWarp], X1[kMxHalvesPerWarp];
 #pragma unroll
-            for (int h = 0; h < BK / 64; ++h) {
+            for (int h = 0; h < kMxHalvesPerWarp; ++h) {
+                const uint32_t hh = hh0 + static_cast<uint32_t>(h);
                 const uint32_t row = sRaw + static_cast<uint32_t>(rstage) * kMxRawBytes +
-                                     kMxCodeBox * static_cast<uint32_t>(h) + 32u * n_local;
+                                     kMxCodeBox * hh + 32u * n_local;
                 const uint4 c0 = mx_ld_shared_v4(row + (swz32 << 4));
                 const uint4 c1 = mx_ld_shared_v4(row + ((swz32 ^ 1u) << 4));
                 const uint32_t scl = sScl + static_cast<uint32_t>(rstage) * kMxScaleBytes +
-                                     256u * static_cast<uint32_t>(h) + n_local;
+                                     256u * hh + n_local;
                 X0[h] = mx_ld_shared_u8(scl);
                 X1[h] = mx_ld_shared_u8(scl + 128u);
                 w[h][0] = c0.x;
@@ -677,7 +687,8 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_rempty + 8 * rstage);
 #pragma unroll
-            for (int h = 0; h < BK / 64; ++h) {  // the unit's 64-k halves
+            for (int h = 0; h < kMxHalvesPerWarp; ++h) {
+                const uint32_t hh = hh0 + static_cast<uint32_t>(h);
                 uint32_t d[32];
                 if (mx_fast_scale(X0[h]) && mx_fast_scale(X1[h])) {
                     const uint32_t f0 = mx_factor_bits(X0[h]) * 0x10001u;  // both halves
@@ -706,7 +717,7 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                 }
                 __syncwarp();
                 mx_tmem_st_x32(tmem_base + lane_addr + kOpCol0 +
-                                   static_cast<uint32_t>(kMxOpCols * stage + 32 * h),
+                                   static_cast<uint32_t>(kMxOpCols * stage) + 32u * hh,
                                d);
             }
             mx_tmem_wait_st();
@@ -843,7 +854,8 @@ inline void skinny_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_pla
 
 // The MXFP4 kernel: the same units and split, its own rings and 448 threads.
 inline void skinny_mx_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_plan_t* pl) {
-    skinny_plan_bk(M, N, K, num_sms, kMxBK, pl);
+    skinny_plan_bk(M, N, K, num_sms, kMxBK, pl, true);
+    pl->cluster = 1;  // the MXFP4 kernel launches without clusters
     const bool narrow = pl->bm <= 64;
     pl->stages = narrow ? SkinnyMxNarrow::kStages : SkinnyMxWide::kStages;
     pl->threads = narrow ? skinny_threads(SkinnyMxNarrow::kStages, 64, true)

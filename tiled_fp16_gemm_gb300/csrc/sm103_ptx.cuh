@@ -97,13 +97,33 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok;
 }
 
+// The same, suspending the thread until the phase completes or about
+// `hint_ns` nanoseconds have passed (the instruction's suspend-time hint).
+// A waiting warp then sleeps instead of re-issuing the test: the roles of a
+// kernel share their SM's schedulers, and waiting warps that kept polling
+// took issue slots from the working ones.
+__device__ __forceinline__ uint32_t mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                        uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok;
+}
+
+// Longest single suspension of a waiting thread; the give-up limit and the
+// abort flag are checked between suspensions.
+constexpr uint32_t kWaitSleepNs = 200000;
+
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                             const volatile int* abort_flag) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 16; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
         if (abort_flag != nullptr && *abort_flag) return false;
         if (globaltimer_ns() - t0 > timeout_ns) return false;
     }
