@@ -319,9 +319,17 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (even CTA)
-        if (leader && lane == 0) {
+        if (leader) {
+            // The whole warp runs the loop (warp-uniform control flow and
+            // operands); one elected lane issues each stage's MMAs and
+            // commit.  A wait counts as met only if every lane saw it met.
+            static_assert(BK == 128, "pair_stage_mma_elect issues 128 k per stage");
             constexpr uint32_t idesc =
                 idesc_f16_f32(256, 256, /*a_mn=*/false, /*b_mn=*/true, Elem16<T>::kFmt);
+            auto warp_wait = [&](uint32_t bar, uint32_t parity, const volatile int* ab) {
+                const bool r = mbar_wait(bar, parity, p.timeout_ns, ab);
+                return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
+            };
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
@@ -332,42 +340,37 @@ __global__ void __launch_bounds__(192, 1)
                           &kb0, &kb1);
                 const int acc = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
-                if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
-                    fail(kRoleMma);
+                if (!warp_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag)) {
+                    if (lane == 0) fail(kRoleMma);
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 256);
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait(bar_full + 8 * stage, phase, p.timeout_ns, abort_flag)) {
-                        fail(kRoleMma);
+                    if (!warp_wait(bar_full + 8 * stage, phase, abort_flag)) {
+                        if (lane == 0) fail(kRoleMma);
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a0 = sA + stage * kABytes;
-                    const uint32_t b0 = sB + stage * kBBytes;
-#pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        // A: 64-k boxes of 16 KB, 32 B per k16 inside one; B: 16
-                        // k rows (2 KB) per k16, the two column boxes kBBytes/2 apart
-                        const uint64_t adesc =
-                            smem_desc_sw128(a0 + 16384 * (k / 4) + 32 * (k % 4), 16, 1024);
-                        const uint64_t bdesc = smem_desc_sw128(b0 + 2048 * k, kBBytes / 2, 1024);
-                        mma_f16_ss_pair(d_tmem, adesc, bdesc, idesc,
-                                        (kb != kb0 || k != 0) ? 1u : 0u);
-                    }
-                    mma_commit_pair_mc(bar_empty + 8 * stage, 0x3);
+                    // A: 64-k boxes of 16 KB; B: the two column boxes kBBytes/2 apart
+                    pair_stage_mma_elect(d_tmem, smem_desc_sw128(sA + stage * kABytes, 16, 1024),
+                                         smem_desc_sw128(sB + stage * kBBytes, kBBytes / 2, 1024),
+                                         idesc, kb == kb0 ? 1u : 0u, bar_empty + 8 * stage);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                if (!(p.inject == 1 && it == 0)) mma_commit_pair_mc(bar_tfull + 8 * acc, 0x3);
+                if (!(p.inject == 1 && it == 0)) {
+                    __syncwarp();
+                    if (lane == 0) mma_commit_pair_mc(bar_tfull + 8 * acc, 0x3);
+                }
             }
-            mma_commit_pair_mc(bar_drain, 0x1);
-            if (!mbar_wait(bar_drain, 0, p.timeout_ns, nullptr))
+            __syncwarp();
+            if (lane == 0) mma_commit_pair_mc(bar_drain, 0x1);
+            if (!warp_wait(bar_drain, 0, nullptr) && lane == 0)
                 atomicOr(&g_wait_timeout_flags, kRoleDrain);
         }
     } else {

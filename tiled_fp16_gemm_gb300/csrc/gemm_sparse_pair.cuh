@@ -174,6 +174,39 @@ __device__ __forceinline__ void mma_f16_sp_pair(uint32_t d_tmem, uint64_t a_desc
         : "memory");
 }
 
+// One stage (128 dense-equivalent k) of the pair: four sparse MMAs of 256 ×
+// 256 × 32 and the two release commits (operand stage and metadata slot,
+// multicast to both CTAs), issued by one elected lane of a converged warp in
+// one block.  MMA k reads A 32 B further (ad + 2 k), B 4 KB further (bd +
+// 256 k) and metadata 16 columns further.  first != 0: the first MMA
+// overwrites D.  The issuing warp shares its scheduler with the metadata and
+// epilogue warps; the single block keeps its instruction count per stage low.
+__device__ __forceinline__ void sp_pair_stage_mma_elect(uint32_t d_tmem, uint64_t ad, uint64_t bd,
+                                                        uint32_t meta, uint32_t idesc,
+                                                        uint32_t first, uint32_t bar_stage,
+                                                        uint32_t bar_meta) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b32 m;\n\t.reg .b64 a, b;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.eq.b32 p, %5, 0;\n\t"
+        "setp.eq.b32 t, 0, 0;\n\t"
+        "@e tcgen05.mma.sp.cta_group::2.kind::f16 [%0], %1, %2, [%3], %4, p;\n\t"
+        "add.u64 a, %1, 2;\n\tadd.u64 b, %2, 256;\n\tadd.u32 m, %3, 16;\n\t"
+        "@e tcgen05.mma.sp.cta_group::2.kind::f16 [%0], a, b, [m], %4, t;\n\t"
+        "add.u64 a, %1, 4;\n\tadd.u64 b, %2, 512;\n\tadd.u32 m, %3, 32;\n\t"
+        "@e tcgen05.mma.sp.cta_group::2.kind::f16 [%0], a, b, [m], %4, t;\n\t"
+        "add.u64 a, %1, 6;\n\tadd.u64 b, %2, 768;\n\tadd.u32 m, %3, 48;\n\t"
+        "@e tcgen05.mma.sp.cta_group::2.kind::f16 [%0], a, b, [m], %4, t;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%6], %8;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%7], %8;\n\t"
+        "}" ::"r"(d_tmem),
+        "l"(ad), "l"(bd), "r"(meta), "r"(idesc), "r"(first), "r"(bar_stage), "r"(bar_meta),
+        "h"(static_cast<uint16_t>(0x3))
+        : "memory");
+}
+
 // Walks this cluster's (tile, k block) sequence: stage u is k block u % kb of
 // the cluster's tile u / kb (tiles cluster_id, cluster_id + nclusters, ...).
 // The tile's block coordinates (three integer divisions) are computed once
@@ -361,12 +394,17 @@ __global__ void __launch_bounds__(352, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (even CTA)
-        if (leader && lane == 0) {
+        if (leader) {
+            // The whole warp runs the loop (warp-uniform control flow and
+            // operands); one elected lane issues the MMAs and commits.  A
+            // wait counts as met only if every lane saw it met.
             // sparse (bit 2), selector 0; A K-major, B MN-major; 256 × 256 over the pair
             constexpr uint32_t idesc =
                 idesc_f16_f32(Cfg::BM, Cfg::BN, /*a_mn=*/false, /*b_mn=*/true,
                               Elem16<T>::kFmt) |
                 (1u << 2);
+            static_assert(Cfg::BK / 32 == 4 && Cfg::kMetaSliceCols == 16,
+                          "sp_pair_stage_mma_elect issues four MMAs 16 metadata columns apart");
             // Descriptors of stage 0; a stage or k step only moves the start
             // address, the descriptor's low 14 bits (address / 16, and every
             // address here is below 256 KB), so it is a plain add.
@@ -378,32 +416,26 @@ __global__ void __launch_bounds__(352, 1)
             int it = 0;
             bool ok = true;
             for (int tile = cluster_id; ok && tile < p.num_tiles; tile += nclusters, ++it) {
-                if (!mbar_wait_cluster(bar_tempty, (static_cast<uint32_t>(it) & 1u) ^ 1u,
-                                       p.timeout_ns, abort_flag)) {
-                    fail(kRoleMma);
+                const bool te = mbar_wait_cluster(bar_tempty, (static_cast<uint32_t>(it) & 1u) ^ 1u,
+                                                  p.timeout_ns, abort_flag);
+                if (!__all_sync(0xffffffffu, te ? 1 : 0)) {
+                    if (lane == 0) fail(kRoleMma);
                     break;
                 }
                 tc_fence_after_sync();
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait(bar_full + 8 * stage, phase, p.timeout_ns, abort_flag)) {
-                        fail(kRoleMma);
+                    const bool got = mbar_wait(bar_full + 8 * stage, phase, p.timeout_ns, abort_flag);
+                    if (!__all_sync(0xffffffffu, got ? 1 : 0)) {
+                        if (lane == 0) fail(kRoleMma);
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint64_t ad = adesc0 + static_cast<uint64_t>(stage) * kAStep;
-                    const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage) * kBStep;
-                    const uint32_t meta0 = tmem_base + Cfg::kMetaCol0 +
-                                           static_cast<uint32_t>(mslot) * Cfg::kMetaSlotCols;
-#pragma unroll
-                    for (int k = 0; k < Cfg::BK / 32; ++k) {
-                        // A: 16 kept values (32 B) per MMA; B: 32 k rows (4 KB)
-                        mma_f16_sp_pair(tmem_base, ad + 2 * k, bd + 256 * k,
-                                        meta0 + static_cast<uint32_t>(k) * Cfg::kMetaSliceCols,
-                                        idesc, (kb | k) != 0 ? 1u : 0u);
-                    }
-                    mma_commit_pair_mc(bar_empty + 8 * stage, 0x3);
-                    mma_commit_pair_mc(bar_mfree + 8 * mslot, 0x3);
+                    sp_pair_stage_mma_elect(
+                        tmem_base, adesc0 + static_cast<uint64_t>(stage) * kAStep,
+                        bdesc0 + static_cast<uint64_t>(stage) * kBStep,
+                        tmem_base + Cfg::kMetaCol0 + static_cast<uint32_t>(mslot) * Cfg::kMetaSlotCols,
+                        idesc, kb == 0 ? 1u : 0u, bar_empty + 8 * stage, bar_mfree + 8 * mslot);
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
@@ -411,10 +443,15 @@ __global__ void __launch_bounds__(352, 1)
                     if (++mslot == SM) mslot = 0;
                 }
                 if (!ok) break;
-                if (!(p.inject == 1 && it == 0)) mma_commit_pair_mc(bar_tfull, 0x3);
+                if (!(p.inject == 1 && it == 0)) {
+                    __syncwarp();
+                    if (lane == 0) mma_commit_pair_mc(bar_tfull, 0x3);
+                }
             }
-            mma_commit_pair_mc(bar_drain, 0x1);
-            if (!mbar_wait(bar_drain, 0, p.timeout_ns, nullptr))
+            __syncwarp();
+            if (lane == 0) mma_commit_pair_mc(bar_drain, 0x1);
+            const bool dr = mbar_wait(bar_drain, 0, p.timeout_ns, nullptr);
+            if (!__all_sync(0xffffffffu, dr ? 1 : 0) && lane == 0)
                 atomicOr(&g_wait_timeout_flags, kRoleDrain);
         }
     } else if (warp == 10) {

@@ -508,6 +508,43 @@ __device__ __forceinline__ void mma_f16_ss_pair(uint32_t d_tmem, uint64_t a_desc
         : "memory");
 }
 
+// One 128-k stage of the dense pair kernel: eight MMAs of 256 × 256 × 16
+// over the pair and the stage's release commit (multicast to both CTAs),
+// issued by one elected lane of a converged warp in one block.  MMA k reads
+// A at a_desc + 1024 (k / 4) + 2 (k % 4) (64-k boxes of 16 KB, 32 B per 16 k)
+// and B at b_desc + 128 k (16 k rows of 2 KB), in descriptor address units of
+// 16 bytes.  first != 0: the first MMA overwrites D.
+__device__ __forceinline__ void pair_stage_mma_elect(uint32_t d_tmem, uint64_t a_desc,
+                                                     uint64_t b_desc, uint32_t idesc,
+                                                     uint32_t first, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b64 a, b;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.eq.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 t, 0, 0;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "add.u64 a, %1, 2;\n\tadd.u64 b, %2, 128;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, t;\n\t"
+        "add.u64 a, %1, 4;\n\tadd.u64 b, %2, 256;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, t;\n\t"
+        "add.u64 a, %1, 6;\n\tadd.u64 b, %2, 384;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, t;\n\t"
+        "add.u64 a, %1, 1024;\n\tadd.u64 b, %2, 512;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, t;\n\t"
+        "add.u64 a, %1, 1026;\n\tadd.u64 b, %2, 640;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, t;\n\t"
+        "add.u64 a, %1, 1028;\n\tadd.u64 b, %2, 768;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, t;\n\t"
+        "add.u64 a, %1, 1030;\n\tadd.u64 b, %2, 896;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, t;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%5], %6;\n\t"
+        "}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(first), "r"(bar),
+        "h"(static_cast<uint16_t>(0x3))
+        : "memory");
+}
+
 // Arrive once on the mbarrier at shared::cta offset `bar` in every CTA of
 // `cta_mask` when this thread's earlier tcgen05 operations have completed.
 __device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
