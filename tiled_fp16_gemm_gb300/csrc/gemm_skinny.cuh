@@ -196,6 +196,25 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 
 
+// Columns [a, a + 16) and [b, b + 16) of this warp's lane quarter (two
+// accumulators) in one round trip: both loads, then one wait.
+__device__ __forceinline__ void tmem_ld2_x16(uint32_t a, uint32_t b, uint32_t (&r)[16],
+                                             uint32_t (&s)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(s[0]), "=r"(s[1]), "=r"(s[2]), "=r"(s[3]),
+          "=r"(s[4]), "=r"(s[5]), "=r"(s[6]), "=r"(s[7]), "=r"(s[8]), "=r"(s[9]), "=r"(s[10]),
+          "=r"(s[11]), "=r"(s[12]), "=r"(s[13]), "=r"(s[14]), "=r"(s[15])
+        : "r"(a), "r"(b)
+        : "memory");
+}
+
 // The kernel body shared by the fp16/bf16 kernel (QB = false: B^T tiles by
 // TMA) and the MXFP4 kernel (QB = true: B^T tiles decoded by warps 6..13).
 template <int STAGES, int MP_MAX, typename T, bool QB, int BK = 64>
@@ -294,7 +313,10 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
         // previous kernel finishes
         int32_t t = static_cast<int32_t>(u_begin / KB);
         int32_t kb = static_cast<int32_t>(u_begin - static_cast<int64_t>(t) * KB);
-        constexpr int kAhead = QB ? mx_raw_stages(MP_MAX) : kSkStages;
+        // (MXFP4: two units.  Prefetching the whole raw ring kept the TMA unit
+        // busy for about 3 us after the dependency wait, and the first loads
+        // queued behind it.)
+        constexpr int kAhead = QB ? 2 : kSkStages;
         for (int i = 0; i < kAhead && u_begin + i < u_end; ++i) {
             if constexpr (QB) {
 #pragma unroll
@@ -492,10 +514,21 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
             atomicOr(&g_wait_timeout_flags, kRoleDrain);
     } else if (warp >= 2 && warp < 6) {
         // ------------------------------------------------------------ epilogue
+        // The parameters it uses, in registers: read through the parameter
+        // reference, every store to C (which the compiler cannot prove
+        // apart from them) forced them to be read again, and a tile's
+        // epilogue took about 7000 cycles.
+        const int Mr = p.M, Nr = p.N, Mp = p.Mp, relu = p.relu, out_f32 = p.out_f32;
+        const int64_t ldc = p.ldc, ldr = p.e.ldr;
+        void* const Cv = p.C;
+        const float* const bias = p.e.bias;
+        const void* const resid = p.e.resid;
+        float* const ws = p.ws;
+        uint32_t* const counters = p.counters;
+        const uint64_t timeout_ns = p.timeout_ns;
         const int q = warp & 3;
         const int n_local = 32 * q + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
-        const int nchunks = p.Mp / 16;
         int it = 0;
         for (int64_t u = u_begin; u < u_end; ++it) {
             const int64_t t = u / KB;
@@ -507,7 +540,7 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
             const int64_t n = t * 128 + n_local;
             int ok = 1;
             if (lane == 0)
-                ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, p.timeout_ns, abort_flag) ? 1 : 0;
+                ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, timeout_ns, abort_flag) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
                 if (lane == 0) fail(kRoleEpilogue);
@@ -519,17 +552,30 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
             // QB: the second MMA warp's accumulator holds units iff the
             // segment has two or more
             const bool two = kMW > 1 && seg_end - u >= 2;
-            // chunk c (16 m) of this thread's column: the accumulators' sum
-            auto load_acc = [&](int c, uint32_t (&r)[16]) {
-                tmem_ld_x16(tacc + 16 * c, r);
-                if (two) {
-                    uint32_t r2[16];
-                    tmem_ld_x16(tacc + kAccStride + 16 * c, r2);
+            // Chunk c (32 m) of this thread's column: the accumulators' sum, in
+            // one tensor-memory round trip.  Rows past Mp read columns that
+            // are not this accumulator's (garbage, never stored).  A round
+            // trip per 16 m made the epilogue of a tile take about 7000 cycles.
+            // (With two accumulators the chunks are 16 m: 32 registers per
+            // load pair, within the MXFP4 kernel's register budget.)
+            constexpr int CW = kMW > 1 ? 16 : 32;
+            static_assert(kAccStride >= CW, "chunks stay inside the allocation");
+            auto load_acc = [&](int c, uint32_t (&r)[CW]) {
+                if constexpr (CW == 16) {
+                    if (two) {
+                        uint32_t r2[16];
+                        tmem_ld2_x16(tacc + 16 * c, tacc + kAccStride + 16 * c, r, r2);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+                        for (int i = 0; i < 16; ++i)
+                            r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+                    } else {
+                        tmem_ld_x16(tacc + 16 * c, r);
+                    }
+                } else {
+                    tmem_ld_x32(tacc + 32 * c, r);
                 }
             };
+            const int nchunksw = (Mp + CW - 1) / CW;
 
             // The slots this warp sums, in k order (none: a FULL segment,
             // summed from tensor memory alone).
@@ -538,13 +584,14 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                 // A piece of a split tile: its fp32 partial to this CTA's
                 // slot for it, layout [m][n_local].
                 const int64_t my_slot = 2 * static_cast<int64_t>(blockIdx.x) + (kb0 > 0 ? 0 : 1);
-                float* slot = p.ws + my_slot * kSkSlotFloats;
-                for (int c = 0; c < nchunks; ++c) {
-                    uint32_t r[16];
+                float* slot = ws + my_slot * kSkSlotFloats;
+                for (int c = 0; c < nchunksw; ++c) {
+                    uint32_t r[CW];
                     load_acc(c, r);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        __stcg(slot + (16 * c + i) * 128 + n_local, __uint_as_float(r[i]));
+                    for (int i = 0; i < CW; ++i)
+                        if (CW * c + i < Mp)
+                            __stcg(slot + (CW * c + i) * 128 + n_local, __uint_as_float(r[i]));
                 }
                 tc_fence_before_sync();
                 __threadfence();
@@ -557,7 +604,7 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                 int last = 0;
                 if (lane == 0) {
                     mbar_arrive(bar_tempty + 8 * acc);
-                    uint32_t* cnt = p.counters + 4 * c_head + q;
+                    uint32_t* cnt = counters + 4 * c_head + q;
                     const uint32_t before = atomic_add_acq_rel_gpu(cnt, 1u);
                     last = before + 1 == static_cast<uint32_t>(c_tail - c_head + 1) ? 1 : 0;
                     if (last) *cnt = 0u;  // zero again for the next launch
@@ -571,43 +618,44 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
             }
             // FULL, or the last piece of a split tile in: C[m][n] =
             // out(act(sum + bias[n]) + R[m][n]); this thread holds column n.
-            for (int c = 0; c < nchunks; ++c) {
-                float v[16];
+            for (int c = 0; c < nchunksw; ++c) {
+                float v[CW];
                 if (c_last < 0) {
-                    uint32_t r[16];
+                    uint32_t r[CW];
                     load_acc(c, r);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+                    for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]);
                 } else {
                     // the head's piece (its second slot), then the first
                     // pieces of CTAs c_head + 1 .. c_last: k order
-                    const float* h = p.ws + (2 * c_head + 1) * kSkSlotFloats;
+                    const float* h = ws + (2 * c_head + 1) * kSkSlotFloats;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = __ldcg(h + (16 * c + i) * 128 + n_local);
+                    for (int i = 0; i < CW; ++i)
+                        v[i] = CW * c + i < Mp ? __ldcg(h + (CW * c + i) * 128 + n_local) : 0.0f;
                     for (int64_t cc = c_head + 1; cc <= c_last; ++cc) {
-                        const float* slot = p.ws + 2 * cc * kSkSlotFloats;
+                        const float* slot = ws + 2 * cc * kSkSlotFloats;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            v[i] += __ldcg(slot + (16 * c + i) * 128 + n_local);
+                        for (int i = 0; i < CW; ++i)
+                            if (CW * c + i < Mp) v[i] += __ldcg(slot + (CW * c + i) * 128 + n_local);
                     }
                 }
-                if (n < p.N) {
-                    const float bias_n = p.e.bias != nullptr ? __ldg(p.e.bias + n) : 0.0f;
+                if (n < Nr) {
+                    const float bias_n = bias != nullptr ? __ldg(bias + n) : 0.0f;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int m = 16 * c + i;
-                        if (m < p.M) {
+                    for (int i = 0; i < CW; ++i) {
+                        const int m = CW * c + i;
+                        if (m < Mr) {
                             float x = v[i];
-                            if (p.e.bias != nullptr) x += bias_n;
-                            if (p.relu) x = relu_f32(x);
-                            if (p.e.resid != nullptr)
-                                x += Elem16<T>::to_float(static_cast<const T*>(
-                                    p.e.resid)[static_cast<int64_t>(m) * p.e.ldr + n]);
-                            const int64_t off = static_cast<int64_t>(m) * p.ldc + n;
-                            if (p.out_f32)
-                                static_cast<float*>(p.C)[off] = x;
+                            if (bias != nullptr) x += bias_n;
+                            if (relu) x = relu_f32(x);
+                            if (resid != nullptr)
+                                x += Elem16<T>::to_float(
+                                    static_cast<const T*>(resid)[static_cast<int64_t>(m) * ldr + n]);
+                            const int64_t off = static_cast<int64_t>(m) * ldc + n;
+                            if (out_f32)
+                                static_cast<float*>(Cv)[off] = x;
                             else
-                                static_cast<T*>(p.C)[off] = Elem16<T>::from_float(x);
+                                static_cast<T*>(Cv)[off] = Elem16<T>::from_float(x);
                         }
                     }
                 }
