@@ -175,6 +175,84 @@ class ClockSampler:
         }
 
 
+class NvmlSampler:
+    """SM clock, power and clock-event reasons of this process's GPU, read
+    through NVML (libnvidia-ml, ctypes) every `period_s` seconds on a thread
+    while work runs.  Reads only; changes no setting.  The GPU is found by its
+    PCI bus id, so the NVML index need not match the CUDA one."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device, period_s: float = 0.005):
+        import ctypes
+        import threading
+        self.period_s = period_s
+        self.samples = []
+        self._stop = threading.Event()
+        self._thread = None
+        self.ok = False
+        try:
+            import torch
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            pr = torch.cuda.get_device_properties(device)
+            bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) != 0:  # 1: SM clock
+                return
+            self.lib, self.h, self.max_mhz = lib, h, int(mx.value)
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _run(self):
+        import ctypes
+        mhz, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            t = time.time()
+            a = self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz))
+            b = self.lib.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(mw))
+            c = self.lib.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs))
+            if a == 0:
+                self.samples.append((t, int(mhz.value), mw.value / 1e3 if b == 0 else None,
+                                     int(rs.value) if c == 0 else 0))
+            time.sleep(self.period_s)
+
+    def start(self):
+        import threading
+        if not self.ok:
+            return
+        self.samples = []
+        self._stop.clear()
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+
+    def stop(self):
+        if self.ok and self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+
+    def window(self, t0: float, t1: float):
+        """Summary of the samples taken between wall times t0 and t1."""
+        if not self.ok:
+            return None
+        inside = [r for r in list(self.samples) if t0 <= r[0] <= t1]
+        if not inside:
+            return None
+        reasons = sorted({name for r in inside for bit, name in self.REASONS.items()
+                          if r[3] & bit})
+        pw = [r[2] for r in inside if r[2] is not None]
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_mhz_min": min(r[1] for r in inside), "sm_max_mhz": self.max_mhz,
+                "power_w_max": max(pw) if pw else None, "samples": len(inside),
+                "reasons": reasons, "source": f"NVML every {self.period_s * 1e3:.0f} ms"}
+
+
 def max_over_ranks(x: float, world: int, device=None) -> float:
     """Max of a per-rank float over all ranks (identity when world == 1)."""
     if world <= 1:
@@ -198,6 +276,8 @@ def barrier(world: int, device=None):
 # ------------------------------------------------------------------ timing
 
 PER_LAUNCH_SAMPLES = 20
+_NVML = None             # NvmlSampler running through the whole bench, if NVML loads
+LAST_LEG_CLOCKS = None   # its summary over the last timed region
 
 
 def time_launches(launch, stream, steps: int, world: int, device):
@@ -222,6 +302,8 @@ def time_launches(launch, stream, steps: int, world: int, device):
     barrier(world, device)
     wall1 = time.time()
     total = t_begin.elapsed_time(t_end)
+    global LAST_LEG_CLOCKS
+    LAST_LEG_CLOCKS = _NVML.window(wall0, wall1) if _NVML is not None else None
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(PER_LAUNCH_SAMPLES)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(PER_LAUNCH_SAMPLES)]
     for i in range(PER_LAUNCH_SAMPLES):
@@ -401,7 +483,7 @@ def time_config(tg, w, args, stream, world, device, nsm, tf_peak, peak_src):
         "kernel": kname, "grid": int(plan.grid), "tiles": int(plan.num_tiles),
         "launches": n, "operand_sets": sets,
         "l2": f"operands rotated over {sets} copies ({sets * w.min_bytes / 2**20:.0f} MiB)",
-        "kernel_ms_mean": k, "isolated_launch_ms_min": min(per),
+        "kernel_ms_mean": k, "isolated_launch_ms_min": min(per), "clocks": LAST_LEG_CLOCKS,
         "isolated_launch_ms_median": statistics.median(per),
         "host_us_per_call": host_us,
         "tflops": tf, "gbs": w.min_bytes / (k / 1e3) / 1e9,
@@ -440,10 +522,18 @@ def run_ours(args, w, rank, world, local_rank):
         launch()
     tg.sync_status(stream)
 
-    clocks = ClockSampler(local_rank)
-    clocks.start()
+    global _NVML
+    _NVML = NvmlSampler(device)
+    clocks = None if _NVML.ok else ClockSampler(local_rank)
+    if _NVML.ok:
+        _NVML.start()
+    else:
+        clocks.start()
     total_ms, _, per, wall0, wall1 = time_launches(launch, stream, args.steps, world, device)
-    clk = clocks.stop(wall0, wall1)
+    clk = _NVML.window(wall0, wall1) if _NVML.ok else None
+    if clk is None:
+        clk = clocks.stop(wall0, wall1) if clocks is not None else {
+            "sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock samples"]}
     tg.sync_status(stream)
     total_ms = max_over_ranks(total_ms, world, device)
 
@@ -520,6 +610,7 @@ def run_ours(args, w, rank, world, local_rank):
             "what": "A copied to an aligned staging buffer (tg_copy_matrix16), then the "
                     "planned kernel",
             "kernel_ms_mean": k_odd, "isolated_launch_ms_min": min(per_odd),
+            "clocks": LAST_LEG_CLOCKS,
             "tflops": flops / (k_odd / 1e3) / 1e12,
             "vs_aligned": kernel_ms / k_odd,
             "staging_bytes": 2 * 2 * w.M * w.K,
@@ -551,6 +642,7 @@ def run_ours(args, w, rank, world, local_rank):
         out["skinny"] = {
             "workload": ws.name, "launches": n2, "kernel_ms_mean": k2,
             "isolated_launch_ms_min": min(per2), "isolated_launch_ms_median": statistics.median(per2),
+            "clocks": LAST_LEG_CLOCKS,
             "tflops": ws.flops / (k2 / 1e3) / 1e12,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": gbs / hbm_peak,
@@ -587,6 +679,7 @@ def run_ours(args, w, rank, world, local_rank):
                      "frac": ach / hbm_peak}
         out["bf16"] = {"workload": w.name, "entry": "tg_gemm_bf16", "launches": n4,
                        "kernel_ms_mean": k4, "isolated_launch_ms_min": min(per4),
+                       "clocks": LAST_LEG_CLOCKS,
                        "tflops": flops / (k4 / 1e3) / 1e12, "roofline": roof4}
         del ab, bb, cb
 
@@ -621,6 +714,7 @@ def run_ours(args, w, rank, world, local_rank):
             extra = (w.M * w.N * 2 if r is not None else 0) + w.N * 4 + \
                 (w.M * w.N * 2 if odt == tg.TG_DTYPE_F32 else 0)
             ent = {"launches": n5, "kernel_ms_mean": k5, "isolated_launch_ms_min": min(per5),
+                   "clocks": LAST_LEG_CLOCKS,
                    "extra_bytes": extra, "vs_plain": kernel_ms / k5}
             if plan.kernel == tg.TG_KERNEL_PERSISTENT:
                 ach = flops / (k5 / 1e3) / 1e12
@@ -662,7 +756,8 @@ def run_ours(args, w, rank, world, local_rank):
             _, k6, per6, _, _ = time_launches(launch6, stream, n6, world, device)
             tg.sync_status(stream)
             ent = {"workload": mname, "launches": n6, "kernel_ms_mean": k6,
-                   "isolated_launch_ms_min": min(per6), "tflops": mw.flops / (k6 / 1e3) / 1e12}
+                   "isolated_launch_ms_min": min(per6), "tflops": mw.flops / (k6 / 1e3) / 1e12,
+                   "clocks": LAST_LEG_CLOCKS}
             if mw.M <= 128:
                 gbs = mw.min_bytes / (k6 / 1e3) / 1e9
                 ent["kernel"] = "tg_gemm_mxfp4_skinny (codes decoded by converter warps into tensor memory)"
@@ -709,6 +804,7 @@ def run_ours(args, w, rank, world, local_rank):
                     launch7()
                 tg.sync_status(stream)
                 _, mean, per, _, _ = time_launches(launch7, stream, n7, world, device)
+                sp_clocks[force] = LAST_LEG_CLOCKS
                 tg.sync_status(stream)
             finally:
                 os.environ.pop("TGEMM_FORCE_SP24", None)
@@ -717,6 +813,7 @@ def run_ours(args, w, rank, world, local_rank):
             return mean, min(per)
 
         n7 = max(20, args.steps // 10)
+        sp_clocks = {}
         k7, min7 = time_sp24(None)
         k7c, min7c = time_sp24("cta")
         tf7 = sw.flops / (k7 / 1e3) / 1e12
@@ -724,7 +821,7 @@ def run_ours(args, w, rank, world, local_rank):
         out["sp24"] = {
             "workload": sw.name, "entry": "tg_gemm_sp24", "launches": n7,
             "kernel": "tg_gemm_sp24_pair<3> (tcgen05.mma.sp cta_group::2, 256x256 tiles)",
-            "kernel_ms_mean": k7, "isolated_launch_ms_min": min7,
+            "kernel_ms_mean": k7, "isolated_launch_ms_min": min7, "clocks": sp_clocks.get(None),
             "tflops_dense_equivalent": tf7,
             "vs_dense_pair": kernel_ms / k7 if (sw.M, sw.N, sw.K) == (w.M, w.N, w.K) else None,
             "roofline": {"bound": "tensor", "achieved": tf7, "peak": sp_peak, "unit": "TFLOP/s",
@@ -764,6 +861,9 @@ def run_ours(args, w, rank, world, local_rank):
         bound["tflops_bound"] = flops / (bound["both_directions_ms"] / 1e3) / 1e12
         bound["frac"] = (e2e_value / world) / bound["tflops_bound"]
         out["e2e"]["bound"] = bound
+
+    if _NVML is not None:
+        _NVML.stop()
 
     # ---- CPU oracle on this host (rank 0, N == 1 only)
     if not args.no_cpu and rank == 0 and world == 1:

@@ -1,6 +1,6 @@
 """tg_gemm_f16_host (C = epi(A·B) with A, B, C in host memory, copies
 overlapped with the products block by block) against the oracle on a GB300:
-one column block and several with a ragged last one, host row strides with
+one column block, several with a ragged last one (up to six for wide C), host row strides with
 padding (odd ones included: the device copies are re-pitched), M <= 128 (the
 split-K kernel per block), K = 0, pageable host memory, and calls of
 different sizes back to back on one stream (the device copies grow)."""
@@ -62,6 +62,8 @@ CASES = [  # M, N, K, relu, (pad lda, pad ldb, pad ldc)
     (257, 4100, 96, True, (5, 3, 7)),        # odd host strides, ragged everything
     (64, 6000, 512, False, (8, 0, 16)),      # M <= 128: split-K kernel in every block
     (1, 2500, 33, True, (1, 1, 1)),
+    (200, 15000, 64, True, (0, 0, 0)),       # 1024, 2048, 4096, 7832 columns
+    (96, 29001, 72, False, (3, 5, 1)),       # six blocks, odd strides, a ragged last block
 ]
 
 
