@@ -315,6 +315,27 @@ def time_launches(launch, stream, steps: int, world: int, device):
     return total, total / steps, per, wall0, wall1
 
 
+def interleaved_ratio(launch_a, launch_b, stream, block: int, rounds: int) -> float:
+    """Time of `launch_a` over time of `launch_b`, from blocks of `block` back-to-back
+    launches of each taken in turn (`rounds` of each, each block between its own two
+    events), so both see the same clocks and temperature."""
+    import torch
+    ta = tb = 0.0
+    for _ in range(rounds):
+        for fn, which in ((launch_a, 0), (launch_b, 1)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(block):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if which == 0:
+                ta += e0.elapsed_time(e1)
+            else:
+                tb += e0.elapsed_time(e1)
+    return ta / tb
+
+
 def rotating_sets(set_bytes: int) -> int:
     """Copies of one problem's operands to rotate through so that the copies
     together span at least twice L2: each launch then reads operands that
@@ -715,7 +736,8 @@ def run_ours(args, w, rank, world, local_rank):
                 (w.M * w.N * 2 if odt == tg.TG_DTYPE_F32 else 0)
             ent = {"launches": n5, "kernel_ms_mean": k5, "isolated_launch_ms_min": min(per5),
                    "clocks": LAST_LEG_CLOCKS,
-                   "extra_bytes": extra, "vs_plain": kernel_ms / k5}
+                   "extra_bytes": extra, "vs_plain": kernel_ms / k5,
+                   "vs_plain_interleaved": interleaved_ratio(launch, launch5, stream, 10, 5)}
             if plan.kernel == tg.TG_KERNEL_PERSISTENT:
                 ach = flops / (k5 / 1e3) / 1e12
                 ent["roofline"] = {"bound": "tensor", "achieved": ach, "peak": tf_peak,

@@ -265,6 +265,10 @@ __global__ void __launch_bounds__(192, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer (both CTAs)
         if (lane == 0) {
+            // A panels are reread by every column block of their raster group
+            // (about 24 waves of tiles on the 8192-row MLP shape): keep them
+            // in L2 ahead of B tiles (reread within a wave) and C (evict-first).
+            const uint64_t a_policy = policy_evict_last();
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
@@ -287,8 +291,8 @@ __global__ void __launch_bounds__(192, 1)
                     const uint32_t fb = mapa_shared(bar_full + 8 * stage, 0);
 #pragma unroll
                     for (int i = 0; i < BK / 64; ++i)
-                        tma_load_2d_pair(sA + stage * kABytes + 16384 * i, &tmA, fb,
-                                         kb * BK + 64 * i, ma);
+                        tma_load_2d_pair_hint(sA + stage * kABytes + 16384 * i, &tmA, fb,
+                                              kb * BK + 64 * i, ma, a_policy);
                     tma_load_2d_pair(sB + stage * kBBytes, &tmB, fb, nb, kb * BK);
                     tma_load_2d_pair(sB + stage * kBBytes + kBBytes / 2, &tmB, fb, nb + 64,
                                      kb * BK);

@@ -157,6 +157,7 @@ __global__ void __launch_bounds__(192, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+            const uint64_t a_policy = policy_evict_last();
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;  // last load per stage
@@ -173,7 +174,9 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     const uint32_t full = bar_full + 8 * stage;
                     mbar_arrive_expect_tx(full, Cfg::kStageBytes);
-                    tma_load_2d(sA + stage * kABytes, &tmA, full, kb * BK, m0);
+                    // A panels are reread by every column block of the raster
+                    // group: kept in L2 ahead of B and C
+                    tma_load_2d_hint(sA + stage * kABytes, &tmA, full, kb * BK, m0, a_policy);
 #pragma unroll
                     for (int j = 0; j < BN / 64; ++j)
                         tma_load_2d(sB + stage * kBBytes + j * 8192, &tmB, full, n0 + 64 * j,
@@ -196,9 +199,17 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the loop (warp-uniform control flow and
+        // operands); one elected lane issues each stage's MMAs and commit.
+        // A wait counts as met only if every lane saw it met.
+        {
+            static_assert(BK == 64, "stage4_mma_ss_elect issues 64 k per stage");
             constexpr uint32_t idesc =
                 idesc_f16_f32(BM, BN, /*a_mn=*/false, /*b_mn=*/true, Elem16<T>::kFmt);
+            auto warp_wait = [&](uint32_t bar, uint32_t parity, const volatile int* ab) {
+                const bool r = mbar_wait(bar, parity, p.timeout_ns, ab);
+                return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
+            };
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
@@ -206,41 +217,40 @@ __global__ void __launch_bounds__(192, 1)
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
                 const int acc = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
-                if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
-                    fail(kRoleMma);
+                if (!warp_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag)) {
+                    if (lane == 0) fail(kRoleMma);
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait(bar_full + 8 * stage, phase, p.timeout_ns, abort_flag)) {
-                        fail(kRoleMma);
+                    if (!warp_wait(bar_full + 8 * stage, phase, abort_flag)) {
+                        if (lane == 0) fail(kRoleMma);
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a0 = sA + stage * kABytes;
-                    const uint32_t b0 = sB + stage * kBBytes;
-#pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        // A: K-major, +32 B per 16-element k slice inside the 128 B row.
-                        const uint64_t adesc = smem_desc_sw128(a0 + 32 * k, 16, 1024);
-                        // B: MN-major, 16 k-rows of 128 B per slice; 64-wide N chunks 8 KB apart.
-                        const uint64_t bdesc = smem_desc_sw128(b0 + 2048 * k, 8192, 1024);
-                        mma_f16_ss(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
-                    }
-                    mma_commit(bar_empty + 8 * stage);
+                    // A: K-major, +32 B per 16-element k slice inside the 128 B row.
+                    // B: MN-major, 16 k-rows of 128 B per slice; 64-wide N chunks 8 KB apart.
+                    stage4_mma_ss_elect<2, 128>(
+                        d_tmem, smem_desc_sw128(sA + stage * kABytes, 16, 1024),
+                        smem_desc_sw128(sB + stage * kBBytes, 8192, 1024), idesc,
+                        kb == 0 ? 1u : 0u, bar_empty + 8 * stage);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                if (!(p.inject == 1 && it == 0)) mma_commit(bar_tfull + 8 * acc);
+                if (!(p.inject == 1 && it == 0)) {
+                    __syncwarp();
+                    if (lane == 0) mma_commit(bar_tfull + 8 * acc);
+                }
             }
-            // Drain: all MMAs issued by this thread complete before TMEM is freed.
-            mma_commit(bar_drain);
-            if (!mbar_wait(bar_drain, 0, p.timeout_ns, nullptr))
+            // Drain: all MMAs issued by this warp complete before TMEM is freed.
+            __syncwarp();
+            if (lane == 0) mma_commit(bar_drain);
+            if (!warp_wait(bar_drain, 0, nullptr) && lane == 0)
                 atomicOr(&g_wait_timeout_flags, kRoleDrain);
         }
     } else {

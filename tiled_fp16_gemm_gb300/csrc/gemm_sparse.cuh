@@ -78,6 +78,32 @@ __device__ __forceinline__ void mma_f16_sp(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// One stage (128 dense-equivalent k) of the one-CTA sparse kernel: four
+// sparse MMAs of 128 × 128 × 32 and the stage's release commit, issued by one
+// elected lane of a converged warp in one block.  MMA k reads A 32 B further
+// (ad + 2 k), B 4 KB further (bd + 256 k) and metadata 16 columns further.
+// first != 0: the first MMA overwrites D.
+__device__ __forceinline__ void sp_stage_mma_elect(uint32_t d_tmem, uint64_t ad, uint64_t bd,
+                                                   uint32_t meta, uint32_t idesc, uint32_t first,
+                                                   uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b32 m;\n\t.reg .b64 a, b;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.eq.b32 p, %5, 0;\n\t"
+        "setp.eq.b32 t, 0, 0;\n\t"
+        "@e tcgen05.mma.sp.cta_group::1.kind::f16 [%0], %1, %2, [%3], %4, p;\n\t"
+        "add.u64 a, %1, 2;\n\tadd.u64 b, %2, 256;\n\tadd.u32 m, %3, 16;\n\t"
+        "@e tcgen05.mma.sp.cta_group::1.kind::f16 [%0], a, b, [m], %4, t;\n\t"
+        "add.u64 a, %1, 4;\n\tadd.u64 b, %2, 512;\n\tadd.u32 m, %3, 32;\n\t"
+        "@e tcgen05.mma.sp.cta_group::1.kind::f16 [%0], a, b, [m], %4, t;\n\t"
+        "add.u64 a, %1, 6;\n\tadd.u64 b, %2, 768;\n\tadd.u32 m, %3, 48;\n\t"
+        "@e tcgen05.mma.sp.cta_group::1.kind::f16 [%0], a, b, [m], %4, t;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
+        "}" ::"r"(d_tmem),
+        "l"(ad), "l"(bd), "r"(meta), "r"(idesc), "r"(first), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_x1(uint32_t taddr, uint32_t a) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(a)
                  : "memory");
@@ -203,12 +229,21 @@ __global__ void __launch_bounds__(320, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the loop (warp-uniform control flow and
+        // operands); one elected lane issues each stage's MMAs and commit.
+        // A wait counts as met only if every lane saw it met.
+        {
             // sparse (bit 2), selector 0; A K-major, B MN-major; 128 × 128
             constexpr uint32_t idesc =
                 idesc_f16_f32(Cfg::BM, Cfg::BN, /*a_mn=*/false, /*b_mn=*/true,
                               Elem16<T>::kFmt) |
                 (1u << 2);
+            static_assert(Cfg::BK / 32 == 4 && Cfg::kMetaSliceCols == 16,
+                          "sp_stage_mma_elect issues four MMAs 16 metadata columns apart");
+            auto warp_wait = [&](uint32_t bar, uint32_t parity, const volatile int* ab) {
+                const bool r = mbar_wait(bar, parity, p.timeout_ns, ab);
+                return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
+            };
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
@@ -216,44 +251,42 @@ __global__ void __launch_bounds__(320, 1)
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
                 const int acc = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
-                if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
-                    fail(kRoleMma);
+                if (!warp_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag)) {
+                    if (lane == 0) fail(kRoleMma);
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::BN);
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait(bar_full + 8 * stage, phase, p.timeout_ns, abort_flag) ||
-                        !mbar_wait(bar_meta + 8 * stage, phase, p.timeout_ns, abort_flag)) {
-                        fail(kRoleMma);
+                    if (!warp_wait(bar_full + 8 * stage, phase, abort_flag) ||
+                        !warp_wait(bar_meta + 8 * stage, phase, abort_flag)) {
+                        if (lane == 0) fail(kRoleMma);
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a0 = sA + stage * Cfg::kABytes;
-                    const uint32_t b0 = sB + stage * Cfg::kBBytes;
-#pragma unroll
-                    for (int k = 0; k < Cfg::BK / 32; ++k) {
-                        // A: 16 kept values (32 B) per 32 k; B: 32 k rows (4 KB) per MMA,
-                        // the two 64-column boxes 16 KB apart.
-                        const uint64_t adesc = smem_desc_sw128(a0 + 32 * k, 16, 1024);
-                        const uint64_t bdesc = smem_desc_sw128(b0 + 4096 * k, 16384, 1024);
-                        const uint32_t meta = tmem_base + Cfg::kMetaCol0 +
-                                              static_cast<uint32_t>(stage) * Cfg::kMetaStageCols +
-                                              static_cast<uint32_t>(k) * Cfg::kMetaSliceCols;
-                        mma_f16_sp(d_tmem, adesc, bdesc, meta, idesc, (kb | k) != 0 ? 1u : 0u);
-                    }
-                    mma_commit(bar_empty + 8 * stage);
+                    // A: 16 kept values (32 B) per 32 k; B: 32 k rows (4 KB) per MMA,
+                    // the two 64-column boxes 16 KB apart.
+                    sp_stage_mma_elect(
+                        d_tmem, smem_desc_sw128(sA + stage * Cfg::kABytes, 16, 1024),
+                        smem_desc_sw128(sB + stage * Cfg::kBBytes, 16384, 1024),
+                        tmem_base + Cfg::kMetaCol0 +
+                            static_cast<uint32_t>(stage) * Cfg::kMetaStageCols,
+                        idesc, kb == 0 ? 1u : 0u, bar_empty + 8 * stage);
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                if (!(p.inject == 1 && it == 0)) mma_commit(bar_tfull + 8 * acc);
+                if (!(p.inject == 1 && it == 0)) {
+                    __syncwarp();
+                    if (lane == 0) mma_commit(bar_tfull + 8 * acc);
+                }
             }
-            mma_commit(bar_drain);
-            if (!mbar_wait(bar_drain, 0, p.timeout_ns, nullptr))
+            __syncwarp();
+            if (lane == 0) mma_commit(bar_drain);
+            if (!warp_wait(bar_drain, 0, nullptr) && lane == 0)
                 atomicOr(&g_wait_timeout_flags, kRoleDrain);
         }
     } else if (warp < 6) {

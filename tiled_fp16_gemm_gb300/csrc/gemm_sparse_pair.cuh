@@ -323,6 +323,7 @@ __global__ void __launch_bounds__(352, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer of Ac and E (both CTAs)
         if (lane == 0) {
+            const uint64_t a_policy = policy_evict_last();
             uint32_t issued_mask = 0, issued_parity = 0;      // full[] phases armed here
             uint32_t e_issued_mask = 0, e_issued_parity = 0;  // efull[] phases armed here
             StageIter e_it(cluster_id, p, nclusters);
@@ -357,7 +358,10 @@ __global__ void __launch_bounds__(352, 1)
                 if (leader)
                     mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * (Cfg::kABytes + Cfg::kBBytes));
                 const uint32_t fb = mapa_shared(bar_full + 8 * stage, 0);
-                tma_load_2d_pair(sA + stage * Cfg::kABytes, &tmA, fb, it.kb * (Cfg::BK / 2), ma);
+                // kept values of A: reread by every column block of the raster
+                // group, so kept in L2 ahead of B and C
+                tma_load_2d_pair_hint(sA + stage * Cfg::kABytes, &tmA, fb, it.kb * (Cfg::BK / 2),
+                                      ma, a_policy);
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                 if (e_next < U) issue_e();

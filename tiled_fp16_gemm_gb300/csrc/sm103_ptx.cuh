@@ -482,6 +482,16 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* desc,
         : "memory");
 }
 
+// The same with an L2 eviction-priority hint (a createpolicy value).
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void* desc, uint32_t bar,
+                                                      int32_t x, int32_t y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
+        ".mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
                  "r"(ncols)
@@ -505,6 +515,32 @@ __device__ __forceinline__ void mma_f16_ss_pair(uint32_t d_tmem, uint64_t a_desc
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// One 64-k stage of a one-CTA kernel: four MMAs, A and B descriptors advanced
+// by A_STEP and B_STEP (16-byte units) per 16 k, and the stage's release
+// commit, issued by one elected lane of a converged warp in one block.
+// first != 0: the first MMA overwrites D.
+template <uint32_t A_STEP, uint32_t B_STEP>
+__device__ __forceinline__ void stage4_mma_ss_elect(uint32_t d_tmem, uint64_t a_desc,
+                                                    uint64_t b_desc, uint32_t idesc,
+                                                    uint32_t first, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b64 a, b;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.eq.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 t, 0, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "add.u64 a, %1, %6;\n\tadd.u64 b, %2, %7;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+        "add.u64 a, a, %6;\n\tadd.u64 b, b, %7;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+        "add.u64 a, a, %6;\n\tadd.u64 b, b, %7;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t"
+        "}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(first), "r"(bar), "n"(A_STEP), "n"(B_STEP)
         : "memory");
 }
 
