@@ -494,7 +494,8 @@ def time_config(tg, w, args, stream, world, device, nsm, tf_peak, peak_src):
     tg.sync_status(stream)
     tf = w.flops / (k / 1e3) / 1e12
     if plan.cluster == 2:
-        kname = f"tg_gemm_f16_pair<{plan.stages} stages of {plan.bk} k>, split_k {plan.split_k}"
+        kname = (f"tg_gemm_f16_pair<{plan.stages} stages of {plan.bk} k>, last wave in "
+                 f"{plan.split_k} k-pieces x {plan.split_n} column pieces per tile")
     else:
         kname = f"tg_gemm_f16_persistent<{plan.bn},{plan.stages}>"
     del a, b, c

@@ -76,8 +76,9 @@ typedef enum {
  * (about 20 MB on 152 SMs), allocated by the first call on that stream that
  * runs the M <= 128 kernel or the CTA-pair kernel, and kept until process
  * exit.  If it cannot be allocated, an M <= 128 call returns
- * TG_ERR_NO_MEMORY and a pair-kernel call runs without splitting its last
- * wave of tiles.
+ * TG_ERR_NO_MEMORY and a pair-kernel call runs without cutting its last
+ * wave of tiles into k-pieces (column halves, which need no workspace, are
+ * still used).
  * Errors: argument errors are returned before anything is enqueued.  Launch
  * failures return TG_ERR_LAUNCH.  A kernel that gives up on a bounded wait
  * records the fact on the device; tg_sync_status reports it.
@@ -302,7 +303,8 @@ typedef struct {
     int64_t workspace_bytes; /* device scratch used (split-K partial sums)      */
     int32_t cluster;      /* CTAs per cluster: 2 = tcgen05 CTA pair (256-row MMA); */
                           /* M <= 128: 4 = a tile's four k-pieces together     */
-    int32_t reserved;
+    int32_t split_n;      /* CTA pairs: column halves (1 or 2) per tile of the  */
+                          /* last wave; 0 for the other kernels                 */
 } tg_plan_t;
 
 /*
@@ -370,9 +372,10 @@ void tg_debug_inject(int32_t mode);
 
 /* The shape of the last tg_gemm_f16 / tg_gemm_bf16 / tg_gemm_ex launch made
  * by the calling thread (tg_gemm_f16_noalloc's too): its plan, with grid,
- * split_k and cluster as actually launched.  These differ from the plan only
- * if the pair kernel's split-K workspace could not be allocated (the last
- * wave then runs unsplit).  Returns TG_ERR_INVALID_VALUE for NULL. */
+ * split_k, cluster and split_n as actually launched.  These differ from the
+ * plan only if the pair kernel's split-K workspace could not be allocated
+ * (the last wave then runs without k-pieces).  Returns TG_ERR_INVALID_VALUE
+ * for NULL. */
 tg_status_t tg_debug_last_launch(tg_plan_t* plan);
 
 /* Tensor maps served from the library's map cache (hits) and encoded anew

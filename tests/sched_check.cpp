@@ -49,39 +49,61 @@ int main() {
         if (tg::unit_begin(G2, G2, U2) != U2) return fail("unit_begin overflow", U2, G2, 0);
         if (tg::unit_owner(U2 - 1, G2, U2) != G2 - 1) return fail("unit_owner overflow", U2, G2, 0);
     }
-    // pair work items: every (tile, k block) exactly once, pieces only in the
-    // last wave, at most kPairMaxSplit of them, each at least
-    // kPairMinPieceBlocks long, R·S <= P, and P <= pairs
+    // pair work items: every (tile, column half, k block) exactly once; cuts
+    // only in the last wave; either at most kPairMaxSplit k-pieces, each at
+    // least kPairMinPieceBlocks long, or two column halves over all of k;
+    // R·S·H <= P and P <= pairs; KB = 0 rules out k-pieces
     for (int T = 1; T <= 700; T += (T < 160 ? 1 : 37)) {
         for (int pairs : {1, 2, 7, 38, 74, 76}) {
-            for (int KB : {1, 7, 8, 16, 32, 33, 64}) {
-                int P = 0, S = 0;
-                tg::pair_launch_shape(T, pairs, KB, &P, &S);
-                if (P < 1 || P > pairs || S < 1 || S > tg::kPairMaxSplit)
+            for (int KB : {0, 1, 7, 8, 16, 32, 33, 64, 65, 96, 97, 128}) {
+                int P = 0, S = 0, H = 0;
+                tg::pair_launch_shape(T, pairs, KB, &P, &S, &H);
+                if (P < 1 || P > pairs || S < 1 || S > tg::kPairMaxSplit || H < 1 || H > 2)
                     return fail("pair_launch_shape range", T, pairs, KB);
+                if (S > 1 && H > 1) return fail("pair both cuts", T, pairs, KB);
                 if (S > 1 && KB / S < tg::kPairMinPieceBlocks)
                     return fail("pair piece length", T, pairs, KB);
                 const int W = T / P, R = T - W * P;
-                if (R * S > P) return fail("pair tail items", T, P, S);
-                std::vector<int> seen(static_cast<size_t>(T) * KB, 0);
+                if (R * S * H > P) return fail("pair tail items", T, P, S * H);
+                if (KB == 0) continue;
+                std::vector<int> seen(static_cast<size_t>(T) * 2 * KB, 0);
                 for (int c = 0; c < P; ++c) {
-                    const int n = tg::pair_item_count(c, T, P, S);
+                    const int n = tg::pair_item_count(c, T, P, S, H);
                     for (int i = 0; i < n; ++i) {
-                        int tile = -1, kb0 = -1, kb1 = -1;
-                        tg::pair_item(c, i, T, P, S, KB, &tile, &kb0, &kb1);
-                        if (tile < 0 || tile >= T || kb0 < 0 || kb1 > KB || kb0 >= kb1)
+                        int tile = -1, kb0 = -1, kb1 = -1, half = -2;
+                        tg::pair_item(c, i, T, P, S, H, KB, &tile, &kb0, &kb1, &half);
+                        if (tile < 0 || tile >= T || kb0 < 0 || kb1 > KB || kb0 >= kb1 ||
+                            half < -1 || half > 1)
                             return fail("pair_item range", T, c, i);
-                        if ((kb0 != 0 || kb1 != KB) && tile < W * P)
-                            return fail("pair piece outside the last wave", T, c, i);
-                        for (int kb = kb0; kb < kb1; ++kb)
-                            if (seen[static_cast<size_t>(tile) * KB + kb]++)
-                                return fail("pair_item duplicate", T, tile, kb);
+                        if ((kb0 != 0 || kb1 != KB || half >= 0) && tile < W * P)
+                            return fail("pair cut outside the last wave", T, c, i);
+                        if (half >= 0 && (kb0 != 0 || kb1 != KB))
+                            return fail("pair half with a k range", T, c, i);
+                        for (int h = 0; h < 2; ++h) {
+                            if (half >= 0 && h != half) continue;
+                            for (int kb = kb0; kb < kb1; ++kb)
+                                if (seen[(static_cast<size_t>(tile) * 2 + h) * KB + kb]++)
+                                    return fail("pair_item duplicate", T, tile, kb);
+                        }
                     }
                 }
                 for (size_t u = 0; u < seen.size(); ++u)
                     if (seen[u] != 1) return fail("pair_item missing", T, P, static_cast<long long>(u));
             }
         }
+    }
+    // the choice between the two cuts: column halves on the 4096^3 shape and
+    // the 8192x28672x4096 MLP shape (76 pairs), k-pieces once K is long
+    {
+        int P, S, H;
+        tg::pair_launch_shape(256, 76, 32, &P, &S, &H);
+        if (P != 76 || S != 1 || H != 2) return fail("4096^3 tail", P, S, H);
+        tg::pair_launch_shape(3584, 76, 32, &P, &S, &H);
+        if (P != 76 || S != 1 || H != 2) return fail("MLP tail", P, S, H);
+        tg::pair_launch_shape(4, 76, 128, &P, &S, &H);
+        if (P != 16 || S != 4 || H != 1) return fail("long-k tail", P, S, H);
+        tg::pair_launch_shape(80, 76, 32, &P, &S, &H);  // 4 tail tiles, k too short to pay
+        if (P != 76 || S != 1 || H != 2) return fail("short-k tail", P, S, H);
     }
     std::printf("OK\n");
     return 0;

@@ -329,8 +329,9 @@ def test_skinny_grid_invariants(tg):
 
 def test_pair_split_invariants(tg):
     """The pair planner over a sweep of shapes: an even grid of at most 152
-    CTAs, and a last wave split into at most 4 k-pieces per tile, each at
-    least 8 blocks of 128 k, that fit the idle pairs."""
+    CTAs, and a last wave cut either into two column halves per tile or into
+    at most 4 k-pieces per tile, each at least 8 blocks of 128 k, that fit
+    the idle pairs."""
     for M in (256, 1000, 2048, 2560, 4096, 8192):
         for N in (256, 1000, 2048, 4096, 4864, 8192, 11008, 28672):
             for K in (512, 1024, 4096, 8192, 16384):
@@ -340,14 +341,17 @@ def test_pair_split_invariants(tg):
                 T, KB, G = p.num_tiles, p.k_blocks, p.grid
                 P = G // 2
                 assert G % 2 == 0 and 2 <= G <= 152
-                S = p.split_k
-                assert 1 <= S <= 4
+                S, H = p.split_k, p.split_n
+                assert 1 <= S <= 4 and H in (1, 2) and (S == 1 or H == 1)
                 R = T % P if T >= P else T
                 if S > 1:
                     assert KB // S >= 8 and R * S <= P, (M, N, K, S)
                     assert p.workspace_bytes > 0
+                elif H > 1:
+                    assert 2 * R <= P and p.workspace_bytes == 0, (M, N, K)
                 else:
                     assert P == min(T, 76)
+                    assert R == 0 or 2 * R > P, (M, N, K)  # halves would have fit
 
 
 def test_plan_limits(tg):
@@ -363,7 +367,7 @@ def test_plan_limits(tg):
     p = tg.tg_plan_f16_limits(8192, 28672, 4096, 152, 74, 38, 38)
     assert p.cluster == 2 and p.grid <= 148 and p.grid % 2 == 0
     R = p.num_tiles % (p.grid // 2)
-    assert p.split_k == 1 or R * p.split_k <= p.grid // 2
+    assert R * p.split_k * p.split_n <= p.grid // 2
     # limits above num_sms / 2 are clamped to it
     assert bytes(tg.tg_plan_f16_limits(8192, 28672, 4096, 152, 99, 38, 38)) == \
         bytes(tg.tg_plan_f16(8192, 28672, 4096, 152))

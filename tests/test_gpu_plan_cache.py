@@ -31,8 +31,9 @@ def tg():
 
 
 SHAPES = [
-    (8192, 28672, 4096),   # pair kernel, full waves + split tail
-    (4096, 4096, 4096),    # pair kernel, last wave split in 2
+    (8192, 28672, 4096),   # pair kernel, full waves + tail in column halves
+    (4096, 4096, 4096),    # pair kernel, tail tiles in column halves
+    (512, 512, 16384),     # pair kernel below one wave, tiles in 4 k-pieces
     (2048, 2048, 4096),    # pair kernel below one wave
     (2048, 2048, 512),     # one-CTA 128x128 (short K)
     (1024, 1024, 1024),    # one-CTA 128x128
@@ -60,7 +61,7 @@ def test_launch_matches_plan(tg, monkeypatch, M, N, K):
     tg.sync_status()
     got = tg.tg_debug_last_launch()
     for f in ("kernel", "bm", "bn", "bk", "stages", "tiles_m", "tiles_n", "k_blocks",
-              "num_tiles", "grid", "split_k", "cluster"):
+              "num_tiles", "grid", "split_k", "cluster", "split_n"):
         assert getattr(got, f) == getattr(want, f), (f, getattr(got, f), getattr(want, f))
     del a, b, c
 

@@ -58,7 +58,7 @@ class tg_plan_t(ctypes.Structure):
         ("threads", ctypes.c_int32), ("group_m", ctypes.c_int32),
         ("smem_bytes", ctypes.c_int64), ("ring_bytes", ctypes.c_int64),
         ("split_k", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
-        ("cluster", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("cluster", ctypes.c_int32), ("split_n", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

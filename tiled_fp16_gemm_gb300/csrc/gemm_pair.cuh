@@ -23,10 +23,12 @@
 // before exit (no peer still reads or signals this CTA) brackets the work.
 //
 // Work items (tile_schedule.h, pair_item): each pair walks its share of the
-// full waves of tiles; the tiles of a last, partial wave may be cut along k
-// into pieces run by otherwise idle pairs.  A piece's epilogue
-// (pair_tail_piece) writes an fp32 partial and counts itself in; the last
-// piece of a tile sums them in k order and stores C.
+// full waves of tiles; the tiles of a last, partial wave may be shared out
+// to otherwise idle pairs, as column halves or as k-pieces.  A column half is
+// a 256×128 product over all of k: each CTA loads one 64-column box of B per
+// stage and the MMA takes N = 128.  A k-piece's epilogue (pair_tail_piece)
+// writes an fp32 partial and counts itself in; the last piece of a tile sums
+// them in k order and stores C.
 //
 // Structure: producer warp / MMA warp / four epilogue warps as in the
 // one-CTA kernel (gemm_persistent.cuh), which follows the warp-specialised
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(192, 1)
     const bool leader = rank == 0;
     const int cluster_id = static_cast<int>(blockIdx.x >> 1);
     const int nclusters = static_cast<int>(gridDim.x >> 1);
-    const int items = pair_item_count(cluster_id, p.num_tiles, nclusters, p.split);
+    const int items = pair_item_count(cluster_id, p.num_tiles, nclusters, p.split, p.split_n);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -275,27 +277,32 @@ __global__ void __launch_bounds__(192, 1)
             bool ok = true;
             uint64_t last_issue = 0;
             for (int i = 0; ok && i < items; ++i) {
-                int tile, kb0, kb1;
-                pair_item(cluster_id, i, p.num_tiles, nclusters, p.split, p.k_blocks, &tile, &kb0,
-                          &kb1);
+                int tile, kb0, kb1, half;
+                pair_item(cluster_id, i, p.num_tiles, nclusters, p.split, p.split_n, p.k_blocks,
+                          &tile, &kb0, &kb1, &half);
                 const TileCoord tc = tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m);
                 const int ma = tc.m_blk * 256 + static_cast<int>(rank) * 128;
-                const int nb = tc.n_blk * 256 + static_cast<int>(rank) * 128;
+                // this CTA's B columns: 128 of a whole tile, 64 of a column half
+                const int nb = half < 0 ? tc.n_blk * 256 + static_cast<int>(rank) * 128
+                                        : tc.n_blk * 256 + half * 128 + static_cast<int>(rank) * 64;
+                const uint32_t stage_tx =
+                    half < 0 ? 2 * Cfg::kStageBytes : 2 * (kABytes + kBBytes / 2);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.timeout_ns, abort_flag)) {
                         fail(kRoleProducer);
                         ok = false;
                         break;
                     }
-                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * Cfg::kStageBytes);
+                    if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, stage_tx);
                     const uint32_t fb = mapa_shared(bar_full + 8 * stage, 0);
 #pragma unroll
                     for (int i = 0; i < BK / 64; ++i)
                         tma_load_2d_pair_hint(sA + stage * kABytes + 16384 * i, &tmA, fb,
                                               kb * BK + 64 * i, ma, a_policy);
                     tma_load_2d_pair(sB + stage * kBBytes, &tmB, fb, nb, kb * BK);
-                    tma_load_2d_pair(sB + stage * kBBytes + kBBytes / 2, &tmB, fb, nb + 64,
-                                     kb * BK);
+                    if (half < 0)
+                        tma_load_2d_pair(sB + stage * kBBytes + kBBytes / 2, &tmB, fb, nb + 64,
+                                         kb * BK);
                     issued_mask |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -330,6 +337,9 @@ __global__ void __launch_bounds__(192, 1)
             static_assert(BK == 128, "pair_stage_mma_elect issues 128 k per stage");
             constexpr uint32_t idesc =
                 idesc_f16_f32(256, 256, /*a_mn=*/false, /*b_mn=*/true, Elem16<T>::kFmt);
+            // a column half: N = 128, 64 columns of B in each CTA
+            constexpr uint32_t idesc_half =
+                idesc_f16_f32(256, 128, /*a_mn=*/false, /*b_mn=*/true, Elem16<T>::kFmt);
             auto warp_wait = [&](uint32_t bar, uint32_t parity, const volatile int* ab) {
                 const bool r = mbar_wait(bar, parity, p.timeout_ns, ab);
                 return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
@@ -339,9 +349,10 @@ __global__ void __launch_bounds__(192, 1)
             int it = 0;
             bool ok = true;
             for (; ok && it < items; ++it) {
-                int tile, kb0, kb1;
-                pair_item(cluster_id, it, p.num_tiles, nclusters, p.split, p.k_blocks, &tile,
-                          &kb0, &kb1);
+                int tile, kb0, kb1, half;
+                pair_item(cluster_id, it, p.num_tiles, nclusters, p.split, p.split_n, p.k_blocks,
+                          &tile, &kb0, &kb1, &half);
+                const uint32_t id = half < 0 ? idesc : idesc_half;
                 const int acc = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!warp_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag)) {
@@ -360,7 +371,7 @@ __global__ void __launch_bounds__(192, 1)
                     // A: 64-k boxes of 16 KB; B: the two column boxes kBBytes/2 apart
                     pair_stage_mma_elect(d_tmem, smem_desc_sw128(sA + stage * kABytes, 16, 1024),
                                          smem_desc_sw128(sB + stage * kBBytes, kBBytes / 2, 1024),
-                                         idesc, kb == kb0 ? 1u : 0u, bar_empty + 8 * stage);
+                                         id, kb == kb0 ? 1u : 0u, bar_empty + 8 * stage);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -386,12 +397,13 @@ __global__ void __launch_bounds__(192, 1)
         int buf = 0;
         int it = 0;
         for (; it < items; ++it) {
-            int tile, kb0, kb1;
-            pair_item(cluster_id, it, p.num_tiles, nclusters, p.split, p.k_blocks, &tile, &kb0,
-                      &kb1);
+            int tile, kb0, kb1, half;
+            pair_item(cluster_id, it, p.num_tiles, nclusters, p.split, p.split_n, p.k_blocks,
+                      &tile, &kb0, &kb1, &half);
             const TileCoord tc = tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m);
             const int row0 = tc.m_blk * 256 + static_cast<int>(rank) * 128 + 32 * q;
-            const int n0 = tc.n_blk * 256;
+            const int n0 = tc.n_blk * 256 + (half < 0 ? 0 : 128 * half);
+            const int chunks = half < 0 ? 4 : 2;  // of 64 columns
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
             int ok = 1;
@@ -417,13 +429,13 @@ __global__ void __launch_bounds__(192, 1)
                 continue;
             }
 #pragma unroll 1
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < chunks; ++j) {
                 uint32_t v0[32], v1[32];
                 const uint32_t taddr =
                     tmem_base + lane_addr + static_cast<uint32_t>(acc * 256 + j * 64);
                 tmem_ld_x32(taddr, v0);
                 tmem_ld_x32(taddr + 32, v1);
-                if (j == 3) {
+                if (j == chunks - 1) {
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * acc, 0));

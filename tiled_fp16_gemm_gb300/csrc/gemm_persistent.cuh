@@ -48,10 +48,12 @@ struct PersistentParams {
     uint64_t timeout_ns;
     EpilogueArgs e;       // bias / residual (null: none)
     int32_t out_f32 = 0;  // 1: C is fp32 (tensor map with 32×32 boxes)
-    // Pair kernel only: pieces per tail tile (tile_schedule.h), and for
-    // split > 1 the partial slots (one per cluster) and the tail tiles'
-    // counters (eight per tile, zero between launches).
+    // Pair kernel only: k-pieces and column halves per tail tile
+    // (tile_schedule.h), and for split > 1 the partial slots (one per
+    // cluster) and the tail tiles' counters (eight per tile, zero between
+    // launches).
     int32_t split = 1;
+    int32_t split_n = 1;
     float* ws = nullptr;
     uint32_t* counters = nullptr;
 };

@@ -115,17 +115,18 @@ void plan_pair(int64_t M, int64_t N, int64_t K, int32_t pairs, tg_plan_t* p) {
     p->k_blocks = ceil_div(K, kPairBK);
     p->num_tiles = p->tiles_m * p->tiles_n;
     if (pairs < 1) pairs = 1;
-    int32_t P = 1, S = 1;
+    int32_t P = 1, S = 1, H = 1;
     tg::pair_launch_shape(static_cast<int32_t>(p->num_tiles), pairs,
-                          static_cast<int32_t>(p->k_blocks), &P, &S);
+                          static_cast<int32_t>(p->k_blocks), &P, &S, &H);
     p->grid = 2 * int64_t{P};
     p->threads = 192;
     p->group_m = static_cast<int32_t>(p->tiles_m < kPairGroupM ? p->tiles_m : kPairGroupM);
     p->smem_bytes = PairCfgT::kSmemBytes;
     p->ring_bytes = 2 * tg_ring_bytes(128, 128, kPairBK, kPairStages, 2);  // both CTAs
-    // pieces per tile of the last wave, and the partial slots and counters
-    // they use (tile_schedule.h)
+    // k-pieces or column halves per tile of the last wave, and the partial
+    // slots and counters k-pieces use (tile_schedule.h)
     p->split_k = S;
+    p->split_n = H;
     p->workspace_bytes = S > 1 ? int64_t{P} * tg::kPairSlotFloats * 4 + 8 * int64_t{P} * 4 : 0;
     p->cluster = 2;
 }
@@ -162,11 +163,13 @@ PlanLimits device_limits(const DeviceState& ds) {
 // tile and cluster size it was actually launched with.
 thread_local tg_plan_t g_last_launch;
 
-void record_launch(const tg_plan_t& pl, int64_t grid, int64_t split, int32_t cluster) {
+void record_launch(const tg_plan_t& pl, int64_t grid, int64_t split, int32_t cluster,
+                   int32_t split_n = -1) {
     g_last_launch = pl;
     g_last_launch.grid = grid;
     g_last_launch.split_k = split;
     g_last_launch.cluster = cluster;
+    if (split_n >= 0) g_last_launch.split_n = split_n;  // else as planned
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -463,8 +466,9 @@ tg_status_t launch_pair(const void* A, const void* B, void* C, const tg_plan_t& 
         return TG_ERR_LAUNCH;
     tg::PersistentParams prm = persistent_params(pl, M, N, K, ep);
     // the planner's shape: P pairs (within the pairs the device holds at
-    // once), tail tiles in S pieces
-    int32_t P = static_cast<int32_t>(pl.grid / 2), S = static_cast<int32_t>(pl.split_k);
+    // once), tail tiles in S k-pieces or H column halves
+    int32_t P = static_cast<int32_t>(pl.grid / 2), S = static_cast<int32_t>(pl.split_k),
+            H = static_cast<int32_t>(pl.split_n);
     tg::SkinnyParams wsp;
     if (tg::splitk_workspace(dev, stream, ds->num_sms, ds->num_sms, &wsp) == TG_OK &&
         int64_t{P} * tg::kPairSlotFloats <= 2 * int64_t{ds->num_sms} * tg::kSkSlotFloats &&
@@ -472,11 +476,13 @@ tg_status_t launch_pair(const void* A, const void* B, void* C, const tg_plan_t& 
         prm.ws = wsp.ws;
         prm.counters = wsp.counters;
     } else if (S > 1) {
-        // no workspace (out of memory): the same pairs, the last wave unsplit
-        tg::pair_launch_shape(prm.num_tiles, P, 0, &P, &S);
+        // no workspace (out of memory): the same pairs, no k-pieces (column
+        // halves need none)
+        tg::pair_launch_shape(prm.num_tiles, P, 0, &P, &S, &H);
     }
     prm.split = S;
-    record_launch(pl, 2 * int64_t{P}, S, 2);
+    prm.split_n = H;
+    record_launch(pl, 2 * int64_t{P}, S, 2, H);
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;

@@ -50,45 +50,69 @@ TG_HD int64_t unit_owner(int64_t u, int64_t num_ctas, int64_t total_units) {
 
 // The pair kernel's work items.  With T tiles on P clusters, W = T / P full
 // waves are walked as above (cluster c takes tiles c, c + P, ...).  The
-// R = T - W·P tiles of the last, partial wave are cut into S pieces along k:
-// cluster c < R·S takes piece c % S (k blocks [KB·j/S, KB·(j+1)/S) for
-// j = c % S) of tile W·P + c / S.  S = 1 leaves the last wave whole.
-// Splitting a k range leaves fewer clusters idle in that wave; the pieces'
-// fp32 partials are summed in k order by whichever piece finishes last.
+// R = T - W·P tiles of the last, partial wave may be shared out to otherwise
+// idle clusters in one of two ways:
+//  - H = 2 column halves: cluster c < 2R takes columns [128·(c % 2), +128)
+//    of tail tile W·P + c / 2 over every k block, a 256×128 product that
+//    needs no partial sums;
+//  - S k-pieces: cluster c < R·S takes piece c % S (k blocks
+//    [KB·j/S, KB·(j+1)/S) for j = c % S) of tile W·P + c / S; the pieces'
+//    fp32 partials are summed in k order by whichever piece finishes last.
+// S = H = 1 leaves the last wave whole.
 constexpr int32_t kPairMaxSplit = 4;         // pieces per tail tile at most
 constexpr int32_t kPairMinPieceBlocks = 8;   // k blocks per piece at least
+// k-pieces are used only where every piece is at least this many k blocks
+// longer than it would be short of a column half: a piece saves k time
+// against a half, but its partial sums cost a write and a read-back
+// (about 13 blocks' time on GB300; see the pair kernel's tail).
+constexpr int32_t kPairPieceGainBlocks = 16;
 
-// Clusters P to launch and pieces S per tail tile, for T tiles of KB k blocks
-// on at most `pairs` clusters.  Always R·S <= P.
-TG_HD void pair_launch_shape(int32_t T, int32_t pairs, int32_t KB, int32_t* P, int32_t* S) {
+// Clusters P to launch, k-pieces S and column halves H per tail tile, for T
+// tiles of KB k blocks on at most `pairs` clusters.  At most one of S and H
+// is above 1, and R·S·H <= P.  KB = 0 rules out k-pieces.
+TG_HD void pair_launch_shape(int32_t T, int32_t pairs, int32_t KB, int32_t* P, int32_t* S,
+                             int32_t* H) {
     const int32_t R = T >= pairs ? T % pairs : T;
-    int32_t s = 1;
+    int32_t s = 1, h = 1;
     if (R > 0) {
-        s = pairs / R;
-        if (s > kPairMaxSplit) s = kPairMaxSplit;
+        const int32_t fit = pairs / R;  // clusters per tail tile that are otherwise idle
+        int32_t k = fit < kPairMaxSplit ? fit : kPairMaxSplit;
         const int32_t kmax = KB / kPairMinPieceBlocks;
-        if (s > kmax) s = kmax;
-        if (s < 1) s = 1;
+        if (k > kmax) k = kmax;
+        // KB/k + gain < KB/2, i.e. (k - 2)·KB > 2·k·gain
+        if (k >= 3 && (k - 2) * KB > 2 * k * kPairPieceGainBlocks)
+            s = k;
+        else if (fit >= 2)
+            h = 2;
     }
     *S = s;
-    *P = T >= pairs ? pairs : (T * s < pairs ? T * s : pairs);
+    *H = h;
+    const int32_t items = T * s * h;
+    *P = T >= pairs ? pairs : (items < pairs ? items : pairs);
 }
 
 // Number of work items of cluster c.
-TG_HD int32_t pair_item_count(int32_t c, int32_t T, int32_t P, int32_t S) {
+TG_HD int32_t pair_item_count(int32_t c, int32_t T, int32_t P, int32_t S, int32_t H) {
     const int32_t W = T / P;
     const int32_t R = T - W * P;
-    return W + (c < R * S ? 1 : 0);
+    return W + (c < R * S * H ? 1 : 0);
 }
 
-// Item i of cluster c: its tile and k-block range [kb0, kb1).
-TG_HD void pair_item(int32_t c, int32_t i, int32_t T, int32_t P, int32_t S, int32_t KB,
-                     int32_t* tile, int32_t* kb0, int32_t* kb1) {
+// Item i of cluster c: its tile, k-block range [kb0, kb1) and column half
+// (-1: all 256 columns; 0 or 1: columns [128·half, 128·half + 128)).
+TG_HD void pair_item(int32_t c, int32_t i, int32_t T, int32_t P, int32_t S, int32_t H,
+                     int32_t KB, int32_t* tile, int32_t* kb0, int32_t* kb1, int32_t* half) {
     const int32_t W = T / P;
+    *half = -1;
     if (i < W) {
         *tile = c + i * P;
         *kb0 = 0;
         *kb1 = KB;
+    } else if (H > 1) {
+        *tile = W * P + c / H;
+        *kb0 = 0;
+        *kb1 = KB;
+        *half = c % H;
     } else {
         const int32_t j = c % S;
         *tile = W * P + c / S;
