@@ -104,6 +104,8 @@ int main() {
         if (P != 16 || S != 4 || H != 1) return fail("long-k tail", P, S, H);
         tg::pair_launch_shape(80, 76, 32, &P, &S, &H);  // 4 tail tiles, k too short to pay
         if (P != 76 || S != 1 || H != 2) return fail("short-k tail", P, S, H);
+        tg::pair_launch_shape(256, 76, 128, &P, &S, &H);  // 4096x4096x16384
+        if (P != 76 || S != 2 || H != 1) return fail("long-k two pieces", P, S, H);
     }
     std::printf("OK\n");
     return 0;

@@ -61,29 +61,43 @@ TG_HD int64_t unit_owner(int64_t u, int64_t num_ctas, int64_t total_units) {
 // S = H = 1 leaves the last wave whole.
 constexpr int32_t kPairMaxSplit = 4;         // pieces per tail tile at most
 constexpr int32_t kPairMinPieceBlocks = 8;   // k blocks per piece at least
-// k-pieces are used only where every piece is at least this many k blocks
-// longer than it would be short of a column half: a piece saves k time
-// against a half, but its partial sums cost a write and a read-back
-// (about 13 blocks' time on GB300; see the pair kernel's tail).
-constexpr int32_t kPairPieceGainBlocks = 16;
+// Choosing between the two, with times in 20ths of a whole tile's k block
+// (fitted to interleaved timings of six shapes on GB300, K 4096 to 16384):
+//  - a column half loads 1.5 times a whole tile's operand bytes per k block
+//    for half its tensor work and runs a k block in about 17/20 of a whole
+//    tile's time (both are bound by the SM's fill rate from L2);
+//  - S k-pieces run KB/S blocks each, then write and read back fp32 partial
+//    sums, which costs about 7 + 4.5·S blocks' time.
+// The cheapest of the two is taken; k-pieces need a workspace (KB = 0 rules
+// them out).
+constexpr int32_t kPairHalfBlockTime20 = 17;
+constexpr int32_t kPairPieceCost20 = 140;     // fixed part of the partial-sum cost
+constexpr int32_t kPairPieceCostPer20 = 90;   // and per piece
+
+TG_HD int32_t pair_piece_time20(int32_t KB, int32_t S) {
+    return 20 * KB / S + kPairPieceCost20 + kPairPieceCostPer20 * S;
+}
 
 // Clusters P to launch, k-pieces S and column halves H per tail tile, for T
 // tiles of KB k blocks on at most `pairs` clusters.  At most one of S and H
-// is above 1, and R·S·H <= P.  KB = 0 rules out k-pieces.
+// is above 1, and R·S·H <= P.
 TG_HD void pair_launch_shape(int32_t T, int32_t pairs, int32_t KB, int32_t* P, int32_t* S,
                              int32_t* H) {
     const int32_t R = T >= pairs ? T % pairs : T;
     int32_t s = 1, h = 1;
     if (R > 0) {
         const int32_t fit = pairs / R;  // clusters per tail tile that are otherwise idle
-        int32_t k = fit < kPairMaxSplit ? fit : kPairMaxSplit;
-        const int32_t kmax = KB / kPairMinPieceBlocks;
-        if (k > kmax) k = kmax;
-        // KB/k + gain < KB/2, i.e. (k - 2)·KB > 2·k·gain
-        if (k >= 3 && (k - 2) * KB > 2 * k * kPairPieceGainBlocks)
-            s = k;
-        else if (fit >= 2)
-            h = 2;
+        int32_t kmax = fit < kPairMaxSplit ? fit : kPairMaxSplit;
+        if (kmax > KB / kPairMinPieceBlocks) kmax = KB / kPairMinPieceBlocks;
+        int32_t best = fit >= 2 ? kPairHalfBlockTime20 * KB : 20 * KB;  // halves, or uncut
+        for (int32_t k = 2; k <= kmax; ++k) {
+            const int32_t t = pair_piece_time20(KB, k);
+            if (t < best) {
+                best = t;
+                s = k;
+            }
+        }
+        if (s == 1 && fit >= 2) h = 2;
     }
     *S = s;
     *H = h;
