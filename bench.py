@@ -62,6 +62,8 @@ def parse_args(argv=None):
     p.add_argument("--no-sp24", action="store_true")
     p.add_argument("--no-configs", action="store_true",
                    help="skip the 256^3, 1024^3 ReLU and 4096^3 configs and the staged layout")
+    p.add_argument("--no-library", action="store_true",
+                   help="skip the cuBLAS (torch.matmul) context timings")
     p.add_argument("--sp24-workload", default="sp24_mlp_8192x28672x4096_relu",
                    choices=sorted(W.SP24_WORKLOADS))
     a = p.parse_args(argv)
@@ -315,10 +317,10 @@ def time_launches(launch, stream, steps: int, world: int, device):
     return total, total / steps, per, wall0, wall1
 
 
-def interleaved_ratio(launch_a, launch_b, stream, block: int, rounds: int) -> float:
-    """Time of `launch_a` over time of `launch_b`, from blocks of `block` back-to-back
-    launches of each taken in turn (`rounds` of each, each block between its own two
-    events), so both see the same clocks and temperature."""
+def interleaved_times(launch_a, launch_b, stream, block: int, rounds: int):
+    """Mean ms per launch of `launch_a` and of `launch_b`, from blocks of `block`
+    back-to-back launches of each taken in turn (`rounds` of each, each block
+    between its own two events), so both see the same clocks and temperature."""
     import torch
     ta = tb = 0.0
     for _ in range(rounds):
@@ -333,7 +335,46 @@ def interleaved_ratio(launch_a, launch_b, stream, block: int, rounds: int) -> fl
                 ta += e0.elapsed_time(e1)
             else:
                 tb += e0.elapsed_time(e1)
+    return ta / (block * rounds), tb / (block * rounds)
+
+
+def interleaved_ratio(launch_a, launch_b, stream, block: int, rounds: int) -> float:
+    """Time of `launch_a` over time of `launch_b` (interleaved_times)."""
+    ta, tb = interleaved_times(launch_a, launch_b, stream, block, rounds)
     return ta / tb
+
+
+def library_context(launch_ours, a_sets, b_sets, stream, flops: float, relu: bool,
+                    min_bytes: float = 0.0):
+    """The same product through torch.matmul (cuBLAS, fp16, no epilogue) on the
+    same operand copies, timed in blocks interleaved with this library's
+    launches.  Context only: nothing of the library's path calls it."""
+    import torch
+    sets = len(a_sets)
+    outs = [torch.empty((a_sets[0].shape[0], b_sets[0].shape[1]), dtype=torch.float16,
+                        device=a_sets[0].device) for _ in range(sets)]
+    ctr = [0]
+
+    def launch_lib():
+        i = ctr[0] % sets
+        ctr[0] += 1
+        torch.matmul(a_sets[i], b_sets[i], out=outs[i])
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            launch_lib()
+        torch.cuda.synchronize()
+        one = flops / 1.8e15 * 1e3  # ms per launch, roughly
+        block = int(max(3, min(200, 5.0 / max(one, 1e-4))))
+        ours, lib = interleaved_times(launch_ours, launch_lib, stream, block, 4)
+    del outs
+    r = {"call": "torch.matmul (cuBLAS), fp16" + (", without the ReLU" if relu else ""),
+         "ms_mean": lib, "tflops": flops / (lib / 1e3) / 1e12,
+         "ours_ms_mean_interleaved": ours, "ours_over_library_time": ours / lib,
+         "how": f"4 blocks of {block} launches each, alternating with this library's"}
+    if min_bytes:
+        r["gbs"] = min_bytes / (lib / 1e3) / 1e9
+    return r
 
 
 def rotating_sets(set_bytes: int) -> int:
@@ -492,6 +533,11 @@ def time_config(tg, w, args, stream, world, device, nsm, tf_peak, peak_src):
     tg.sync_status(stream)
     host_us = host_issue_us(launch, n)
     tg.sync_status(stream)
+    lib = None
+    if not args.no_library:
+        lib = library_context(launch, [a[i] for i in range(sets)], [b[i] for i in range(sets)],
+                              stream, float(w.flops), w.relu)
+        tg.sync_status(stream)
     tf = w.flops / (k / 1e3) / 1e12
     if plan.cluster == 2:
         kname = (f"tg_gemm_f16_pair<{plan.stages} stages of {plan.bk} k>, last wave in "
@@ -512,6 +558,7 @@ def time_config(tg, w, args, stream, world, device, nsm, tf_peak, peak_src):
         "roofline": {"bound": "tensor", "achieved": tf, "peak": tf_peak, "unit": "TFLOP/s",
                      "frac": tf / tf_peak,
                      "peak_source": f"{peak_src} dense bf16 burst (fp16 dense rate is the same)"},
+        "library_context": lib,
     }
 
 
@@ -585,6 +632,10 @@ def run_ours(args, w, rank, world, local_rank):
     roof.update({"kernel": kname, "kernel_ms_mean": kernel_ms,
                  "isolated_launch_ms_min": min(per),
                  "isolated_launch_ms_median": statistics.median(per)})
+    lib_ctx = None
+    if not args.no_library:
+        lib_ctx = library_context(launch, [a], [b], stream, float(w.flops), w.relu)
+        tg.sync_status(stream)
     out = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -594,6 +645,8 @@ def run_ours(args, w, rank, world, local_rank):
         "gpu_launches": args.steps,
         "clocks": clk,
     }
+    if lib_ctx is not None:
+        out["library_context"] = lib_ctx
 
     # ---- the other square configs (256^3, 1024^3 with ReLU, 4096^3), same
     # method; operands rotate over enough copies that each launch reads them
@@ -671,6 +724,10 @@ def run_ours(args, w, rank, world, local_rank):
                          "traffic": stored_traffic(f"skinny:{ws.name}"),
                          "peak_source": f"{peak_src} copy bandwidth"},
         }
+        if not args.no_library:
+            out["skinny"]["library_context"] = library_context(
+                launch2, [a2], [b2], stream, float(ws.flops), False, float(ws.min_bytes))
+            tg.sync_status(stream)
         del a2, b2, c2
 
     # ---- bfloat16 variant on the same shape, same method
