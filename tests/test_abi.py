@@ -271,8 +271,10 @@ def test_plans(tg):
     assert small.kernel == tg.TG_KERNEL_SKINNY and small.mma_n == 16 and small.grid == 1
     assert tg.tg_plan_f16(0, 5, 3, 152).kernel == tg.TG_KERNEL_NONE
     assert tg.tg_plan_f16(5, 5, 0, 152).kernel == tg.TG_KERNEL_FILL
-    mid = tg.tg_plan_f16(1024, 1024, 1024, 152)
-    assert mid.kernel == tg.TG_KERNEL_PERSISTENT and mid.bn == 128 and mid.num_tiles == 64
+    mid = tg.tg_plan_f16(1024, 1024, 1024, 152)  # 64 tiles of 128x128 would fill < half
+    assert mid.kernel == tg.TG_KERNEL_PERSISTENT and mid.bn == 64 and mid.num_tiles == 128
+    wide = tg.tg_plan_f16(1536, 1024, 1024, 152)  # 96 tiles of 128x128: more than half
+    assert wide.kernel == tg.TG_KERNEL_PERSISTENT and wide.bn == 128 and wide.num_tiles == 96
     with pytest.raises(tg.TgemmError):
         tg.tg_plan_f16(-1, 5, 5, 152)
     with pytest.raises(tg.TgemmError):

@@ -59,7 +59,7 @@ def run(tg, A, B, M, N, K, relu=False):
     return bf16_bits_to_float(bits)
 
 
-CFGS = ["pair256", "persistent256", "persistent128", "skinny"]
+CFGS = ["pair256", "persistent256", "persistent128", "persistent64", "skinny"]
 # (64, 4096, 4096): the skinny kernel's four-piece aligned grid in clusters of 4;
 # (512, 512, 4096): the pair kernel's last wave split into k pieces
 SHAPES = [(1, 1, 1), (7, 7, 7), (129, 127, 1000), (200, 1000, 129), (300, 1000, 1000),

@@ -61,7 +61,8 @@ def _same(tg, step, make_bufs, steps=8):
 # (name, M, K=N, forced configuration): the pair kernel, the one-CTA kernel
 # with both tile widths, and the skinny kernel
 DENSE = [("pair", 2048, 2048, "pair256"), ("cta_bn256", 512, 1024, "persistent256"),
-         ("cta_bn128", 384, 768, "persistent128"), ("skinny", 64, 4096, None)]
+         ("cta_bn128", 384, 768, "persistent128"), ("cta_bn64", 384, 640, "persistent64"),
+         ("skinny", 64, 4096, None)]
 
 
 @pytest.mark.parametrize("name,M,K,cfg", DENSE, ids=[d[0] for d in DENSE])

@@ -43,7 +43,7 @@ def tg():
     return t
 
 
-CFGS = ["pair256", "persistent256", "persistent128", "skinny"]
+CFGS = ["pair256", "persistent256", "persistent128", "persistent64", "skinny"]
 TDT = {"f16": torch.float16, "bf16": torch.bfloat16}
 
 

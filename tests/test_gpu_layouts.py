@@ -45,7 +45,7 @@ LAYOUTS = [
     (1000, 200, 64, 64, 201, 200, 0, 1, 0),
     (512, 512, 256, 256, 512, 513, 0, 0, 0),
 ]
-CFGS = ["auto", "pair256", "persistent128", "skinny"]
+CFGS = ["auto", "pair256", "persistent128", "persistent64", "skinny"]
 
 
 @pytest.mark.parametrize("layout", LAYOUTS, ids=[f"{l[0]}x{l[1]}x{l[2]}" for l in LAYOUTS])

@@ -32,7 +32,7 @@ def tg():
     return t
 
 
-PATHS = [None, "pair256", "persistent256", "persistent128"]  # None: fused kernel for M <= 128
+PATHS = [None, "pair256", "persistent256", "persistent128", "persistent64"]  # None: fused kernel for M <= 128
 
 
 def dev(x: np.ndarray):

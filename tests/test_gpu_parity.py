@@ -61,7 +61,7 @@ def ld8(x):
 
 # ---------------------------------------------------------------- first: one tile
 
-CFGS = ["pair256", "persistent256", "persistent128", "skinny"]
+CFGS = ["pair256", "persistent256", "persistent128", "persistent64", "skinny"]
 
 
 @pytest.fixture(params=CFGS)

@@ -36,7 +36,8 @@ SHAPES = [
     (512, 512, 16384),     # pair kernel below one wave, tiles in 4 k-pieces
     (2048, 2048, 4096),    # pair kernel below one wave
     (2048, 2048, 512),     # one-CTA 128x128 (short K)
-    (1024, 1024, 1024),    # one-CTA 128x128
+    (1024, 1024, 1024),    # one-CTA 128x64
+    (1536, 1024, 1024),    # one-CTA 128x128
     (3000, 2000, 700),     # one-CTA, ragged
     (64, 16384, 8192),     # skinny, whole tiles
     (64, 4096, 4096),      # skinny, four-piece clusters

@@ -26,7 +26,8 @@ def tg():
 
 
 CASES = [("pair256", 512, 512, 256), ("persistent256", 256, 512, 256),
-         ("persistent128", 256, 256, 128), ("skinny", 64, 256, 1024)]
+         ("persistent128", 256, 256, 128), ("persistent64", 256, 128, 128),
+         ("skinny", 64, 256, 1024)]
 
 
 @pytest.mark.parametrize("cfg,M,N,K", CASES, ids=[c[0] for c in CASES])

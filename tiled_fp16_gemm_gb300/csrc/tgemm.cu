@@ -36,6 +36,9 @@ void noalloc_reset_counters(int dev);  // defined with the no-allocation entry p
 
 constexpr int kBigBN = 256, kBigStages = 4;
 constexpr int kMidBN = 128, kMidStages = 6;
+// 128×64 tiles for problems whose 128×128 tiles would fill at most half the
+// SMs: twice the CTAs, each loading 24 KB per 64-deep stage instead of 32 KB.
+constexpr int kSmallBN = 64, kSmallStages = 8;
 constexpr int kGroupM = 16;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -197,6 +200,10 @@ cudaError_t set_kernel_attributes() {
         e = cudaFuncSetAttribute(tg::tg_gemm_f16_persistent<kMidBN, kMidStages, T>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  tg::PersistentCfg<kMidBN, kMidStages>::kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tg::tg_gemm_f16_persistent<kSmallBN, kSmallStages, T>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tg::PersistentCfg<kSmallBN, kSmallStages>::kSmemBytes);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(tg::tg_gemm_f16_pair<kPairStages, T, kPairBK>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -507,7 +514,7 @@ tg_status_t launch_pair(const void* A, const void* B, void* C, const tg_plan_t& 
     return TG_OK;
 }
 
-// TGEMM_FORCE_CFG = pair256 | persistent256 | persistent128 | skinny
+// TGEMM_FORCE_CFG = pair256 | persistent256 | persistent128 | persistent64 | skinny
 // overrides the planner's kernel choice (used by tests and tile sweeps);
 // ignored where the forced kernel does not apply (skinny needs M <= 128;
 // K == 0 always fills).
@@ -527,6 +534,9 @@ void apply_forced_config(int64_t M, int64_t N, int64_t K, const PlanLimits& lim,
     else if (f != nullptr && std::strcmp(f, "persistent128") == 0)
         plan_persistent(M, N, K, num_sms, kMidBN, kMidStages,
                         tg::PersistentCfg<kMidBN, kMidStages>::kSmemBytes, pl);
+    else if (f != nullptr && std::strcmp(f, "persistent64") == 0)
+        plan_persistent(M, N, K, num_sms, kSmallBN, kSmallStages,
+                        tg::PersistentCfg<kSmallBN, kSmallStages>::kSmemBytes, pl);
     else if (f != nullptr && std::strcmp(f, "skinny") == 0 && tg::skinny_applies(M, N, K)) {
         tg::skinny_plan(M, N, K, num_sms, pl);
         if (pl->cluster == 4 && pl->grid / 4 > lim.quads[pl->mma_n > 64 ? 1 : 0]) pl->cluster = 1;
@@ -632,6 +642,9 @@ tg_status_t launch_planned(tg_plan_t pl, const void* A, const void* B, void* C, 
             if (pl.bn == kBigBN)
                 return launch_persistent<kBigBN, kBigStages, T>(A, B, C, pl, M, N, K, lda, ldb,
                                                                ldc, ep, s);
+            if (pl.bn == kSmallBN)
+                return launch_persistent<kSmallBN, kSmallStages, T>(A, B, C, pl, M, N, K, lda,
+                                                                   ldb, ldc, ep, s);
             return launch_persistent<kMidBN, kMidStages, T>(A, B, C, pl, M, N, K, lda, ldb, ldc,
                                                            ep, s);
         case TG_KERNEL_SKINNY: {
@@ -766,7 +779,8 @@ bool forced_dense_kernel() {
     const char* f = std::getenv("TGEMM_FORCE_CFG");
     return f != nullptr && (std::strcmp(f, "pair256") == 0 ||
                             std::strcmp(f, "persistent256") == 0 ||
-                            std::strcmp(f, "persistent128") == 0);
+                            std::strcmp(f, "persistent128") == 0 ||
+                            std::strcmp(f, "persistent64") == 0);
 }
 
 // 2:4 sparse A: tensor maps, kernel choice, tile plan and launch (operands in
@@ -900,6 +914,15 @@ tg_status_t plan_limited(int64_t M, int64_t N, int64_t K, const PlanLimits& lim,
     const int64_t tiles128 = ceil_div(M, 128) * ceil_div(N, 128);
     if (lim.pairs >= 1 && tiles128 > num_sms && K >= 1024) {
         plan_pair(M, N, K, lim.pairs, plan);
+        return TG_OK;
+    }
+    // 128×128 tiles would fill at most half the SMs: 128×64 tiles instead.
+    // Timed from CUDA graphs against 128×128 on GB300 (same bits): 256^3
+    // 3.89 -> 3.26 us, 512^3 5.32 -> 4.41, 1024^3 ReLU 7.32 -> 6.61,
+    // 1024×1024×4096 18.2 -> 15.9.
+    if (tiles128 * 2 <= num_sms) {
+        plan_persistent(M, N, K, num_sms, kSmallBN, kSmallStages,
+                        tg::PersistentCfg<kSmallBN, kSmallStages>::kSmemBytes, plan);
         return TG_OK;
     }
     const int64_t tiles256 = ceil_div(M, 128) * ceil_div(N, kBigBN);
