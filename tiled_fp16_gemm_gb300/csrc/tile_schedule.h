@@ -65,7 +65,8 @@ constexpr int32_t kPairMinPieceBlocks = 8;   // k blocks per piece at least
 // (fitted to interleaved timings of six shapes on GB300, K 4096 to 16384):
 //  - a column half loads 1.5 times a whole tile's operand bytes per k block
 //    for half its tensor work and runs a k block in about 17/20 of a whole
-//    tile's time (both are bound by the SM's fill rate from L2);
+//    tile's time (both turn their operand rings over at about the same
+//    bytes per cycle);
 //  - S k-pieces run KB/S blocks each, then write and read back fp32 partial
 //    sums, which costs about 7 + 4.5·S blocks' time.
 // The cheapest of the two is taken; k-pieces need a workspace (KB = 0 rules
