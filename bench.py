@@ -282,10 +282,17 @@ _NVML = None             # NvmlSampler running through the whole bench, if NVML 
 LAST_LEG_CLOCKS = None   # its summary over the last timed region
 
 
+# Idle time before each timed leg, so that a leg starts from an idle GPU as
+# the first one does and does not inherit the power state (clock cap) that
+# the legs before it left.
+LEG_IDLE_S = 1.0
+
+
 def time_launches(launch, stream, steps: int, world: int, device):
     """Time `steps` back-to-back launches on `stream` between two CUDA events,
     with no event between launches: consecutive launches overlap their
     start-up with the previous launch's tail, as in any stream of kernels.
+    The leg starts after LEG_IDLE_S of idle.
     Returns (total_ms, mean_ms = total_ms / steps, per_ms, wall0, wall1).
     per_ms holds PER_LAUNCH_SAMPLES further launches, each bracketed by its
     own events; those events serialise the launches, so per_ms is context
@@ -293,6 +300,8 @@ def time_launches(launch, stream, steps: int, world: int, device):
     import torch
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    time.sleep(LEG_IDLE_S)
     barrier(world, device)
     torch.cuda.synchronize()
     wall0 = time.time()
@@ -672,6 +681,7 @@ def run_ours(args, w, rank, world, local_rank):
         "roofline": roof,
         "gpu_launches": args.steps,
         "clocks": clk,
+        "leg_idle_s": LEG_IDLE_S,
     }
     if lib_ctx is not None:
         out["library_context"] = lib_ctx
