@@ -457,11 +457,12 @@ tg_status_t launch_persistent(const void* A, const void* B, void* C, const tg_pl
 
 // The pair kernel: clusters of two CTAs, at most as many pairs as the device
 // holds at once (the launch is persistent, so no pair waits for another).
-// The last, partial wave of tiles is split along k when that leaves fewer
-// pairs idle (tile_schedule.h); its partial sums use the stream's split-K
-// workspace, which is set up on the first pair launch on the stream whether
-// or not that launch splits, so a later launch inside a graph capture finds
-// it.  Without a workspace the wave is not split.
+// The last, partial wave of tiles is shared out to otherwise idle pairs as
+// column halves or k-pieces (tile_schedule.h).  k-pieces keep their partial
+// sums in the stream's split-K workspace, which is set up on the first pair
+// launch on the stream whether or not that launch uses it, so a later launch
+// inside a graph capture finds it.  Without a workspace only column halves
+// are used.
 template <typename T>
 tg_status_t launch_pair(const void* A, const void* B, void* C, const tg_plan_t& pl, int64_t M,
                         int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
