@@ -527,7 +527,10 @@ def config_block(w, gpus):
     return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
             "epilogue": "relu" if w.relu else "none",
             "inputs": f"A {w.dist_a}, B {w.dist_b}, seed {w.seed}",
-            "l2": f"inputs larger than L2 ({inb / 2**20:.0f} MiB of A+B vs {L2_BYTES // 2**20} MiB L2); no flush",
+            "l2": (f"inputs larger than L2 ({inb / 2**20:.0f} MiB of A+B vs "
+                   f"{L2_BYTES // 2**20} MiB L2); no flush" if inb > L2_BYTES else
+                   f"inputs fit in L2 ({inb / 2**20:.0f} MiB of A+B vs {L2_BYTES // 2**20} MiB "
+                   "L2) and stay there between launches"),
             "parallelism": "replicas" if gpus > 1 else "single GPU"}
 
 
