@@ -79,7 +79,10 @@ struct PersistentCfg {
                   "TMEM columns must be a power of two in [32, 512]");
 };
 
-template <int BN, int STAGES, typename T = __half>
+// EX = false: the plain epilogue only (no bias, no residual, 16-bit C); the
+// other epilogue paths are compiled out, which keeps the kernel's code small
+// for the latency-bound launches of small problems.
+template <int BN, int STAGES, typename T = __half, bool EX = true>
 __global__ void __launch_bounds__(192, 1)
     tg_gemm_f16_persistent(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
@@ -297,9 +300,10 @@ __global__ void __launch_bounds__(192, 1)
                     x[t] = __uint_as_float(v0[t]);
                     x[32 + t] = __uint_as_float(v1[t]);
                 }
-                epilogue_math<T>(x, p.e, p.relu, row0 + lane, n0 + 64 * j, p.M, p.N);
+                epilogue_math<T>(x, EX ? p.e : EpilogueArgs{}, p.relu, row0 + lane, n0 + 64 * j,
+                                 p.M, p.N);
                 epilogue_store<T>(x, cbuf, buf, &tmC, c_policy, row0, n0 + 64 * j, p.M, p.N, lane,
-                                  p.out_f32 != 0);
+                                  EX && p.out_f32 != 0);
             }
         }
         if (lane == 0) bulk_wait_group<0>();

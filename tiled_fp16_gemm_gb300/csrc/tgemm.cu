@@ -205,6 +205,14 @@ cudaError_t set_kernel_attributes() {
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  tg::PersistentCfg<kSmallBN, kSmallStages>::kSmemBytes);
     if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tg::tg_gemm_f16_persistent<kSmallBN, kSmallStages, T, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tg::PersistentCfg<kSmallBN, kSmallStages>::kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tg::tg_gemm_f16_persistent<kMidBN, kMidStages, T, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tg::PersistentCfg<kMidBN, kMidStages>::kSmemBytes);
+    if (e == cudaSuccess)
         e = cudaFuncSetAttribute(tg::tg_gemm_f16_pair<kPairStages, T, kPairBK>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PairCfgT::kSmemBytes);
@@ -446,8 +454,20 @@ tg_status_t launch_persistent(const void* A, const void* B, void* C, const tg_pl
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     record_launch(pl, pl.grid, 1, 1);
-    cudaError_t e =
-        cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_persistent<BN, STAGES, T>, tmA, tmB, tmC, prm);
+    // the plain epilogue: the variant with the others compiled out (BN <= 128)
+    const bool plain = ep.e.bias == nullptr && ep.e.resid == nullptr && ep.out_f32 == 0;
+    cudaError_t e = cudaErrorInvalidValue;
+    bool launched = false;
+    if constexpr (BN <= kMidBN) {
+        if (plain) {
+            e = cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_persistent<BN, STAGES, T, false>, tmA,
+                                   tmB, tmC, prm);
+            launched = true;
+        }
+    }
+    if (!launched)
+        e = cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_persistent<BN, STAGES, T, true>, tmA, tmB,
+                               tmC, prm);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return TG_ERR_LAUNCH;
