@@ -85,7 +85,7 @@ constexpr uint32_t kPairRedBytes = 48 * 1024;             // per epilogue warp, 
 // others bulk-copied two chunks at a time into its 48 KB share of the ring
 // (red: its own barrier there).  It then applies the epilogue, stores C and
 // zeroes the counter.  Returns false if a bulk copy did not land in time.
-template <typename T>
+template <typename T, bool EX>
 __device__ __forceinline__ bool pair_tail_piece(const PersistentParams& p, uint32_t taddr,
                                                 uint32_t tempty, int cluster_id, uint32_t rank,
                                                 int q, int lane, uint32_t red_buf,
@@ -175,9 +175,10 @@ __device__ __forceinline__ bool pair_tail_piece(const PersistentParams& p, uint3
                         ++o;
                     }
                 }
-                epilogue_math<T>(x, p.e, p.relu, row0 + lane, n0 + 64 * j, p.M, p.N);
+                epilogue_math<T>(x, EX ? p.e : EpilogueArgs{}, p.relu, row0 + lane, n0 + 64 * j,
+                                 p.M, p.N);
                 epilogue_store<T>(x, cbuf, buf, tmC, c_policy, row0, n0 + 64 * j, p.M, p.N,
-                                  lane, p.out_f32 != 0);
+                                  lane, EX && p.out_f32 != 0);
             }
             __syncwarp();  // every lane is done reading the buffer
         }
@@ -188,7 +189,9 @@ __device__ __forceinline__ bool pair_tail_piece(const PersistentParams& p, uint3
     return ok;
 }
 
-template <int STAGES, typename T = __half, int BK_ = 64>
+// EX = false: the plain epilogue only (no bias, no residual, 16-bit C); the
+// other epilogue paths are compiled out.
+template <int STAGES, typename T = __half, int BK_ = 64, bool EX = true>
 __global__ void __launch_bounds__(192, 1)
     tg_gemm_f16_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const PersistentParams p) {
@@ -420,7 +423,7 @@ __global__ void __launch_bounds__(192, 1)
                 // columns of fp32 partial go to the cluster's slot; the warp
                 // whose add completes the tile's count sums the slots.
                 const uint32_t e = static_cast<uint32_t>(warp - 2);
-                if (!pair_tail_piece<T>(p, tmem_base + lane_addr + static_cast<uint32_t>(acc * 256),
+                if (!pair_tail_piece<T, EX>(p, tmem_base + lane_addr + static_cast<uint32_t>(acc * 256),
                                         mapa_shared(bar_tempty + 8 * acc, 0), cluster_id, rank,
                                         q, lane, sA + e * kPairRedBytes, bar_red + 8 * e, cbuf,
                                         buf, &tmC, c_policy, row0, n0) &&
@@ -446,9 +449,10 @@ __global__ void __launch_bounds__(192, 1)
                     x[t] = __uint_as_float(v0[t]);
                     x[32 + t] = __uint_as_float(v1[t]);
                 }
-                epilogue_math<T>(x, p.e, p.relu, row0 + lane, n0 + 64 * j, p.M, p.N);
+                epilogue_math<T>(x, EX ? p.e : EpilogueArgs{}, p.relu, row0 + lane, n0 + 64 * j,
+                                 p.M, p.N);
                 epilogue_store<T>(x, cbuf, buf, &tmC, c_policy, row0, n0 + 64 * j, p.M, p.N, lane,
-                                  p.out_f32 != 0);
+                                  EX && p.out_f32 != 0);
             }
         }
         if (lane == 0) bulk_wait_group<0>();

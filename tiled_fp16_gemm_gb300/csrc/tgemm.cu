@@ -216,6 +216,10 @@ cudaError_t set_kernel_attributes() {
         e = cudaFuncSetAttribute(tg::tg_gemm_f16_pair<kPairStages, T, kPairBK>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PairCfgT::kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tg::tg_gemm_f16_pair<kPairStages, T, kPairBK, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PairCfgT::kSmemBytes);
     if (e == cudaSuccess) e = tg::skinny_set_attributes<T>();
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(tg::tg_gemm_sp24<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -526,8 +530,11 @@ tg_status_t launch_pair(const void* A, const void* B, void* C, const tg_plan_t& 
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     cudaError_t e =
-        cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_pair<kPairStages, T, kPairBK>, tmA, tmB, tmC,
-                           prm);
+        (ep.e.bias == nullptr && ep.e.resid == nullptr && ep.out_f32 == 0)
+            ? cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_pair<kPairStages, T, kPairBK, false>, tmA,
+                                 tmB, tmC, prm)
+            : cudaLaunchKernelEx(&cfg, tg::tg_gemm_f16_pair<kPairStages, T, kPairBK, true>, tmA,
+                                 tmB, tmC, prm);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return TG_ERR_LAUNCH;
