@@ -236,7 +236,9 @@ struct StageIter {
     }
 };
 
-template <int STAGES, typename T>
+// EX = false: the plain epilogue only (no bias, no residual, 16-bit C); the
+// other epilogue paths are compiled out.
+template <int STAGES, typename T, bool EX = true>
 __global__ void __launch_bounds__(352, 1)
     tg_gemm_sp24_pair(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
@@ -499,7 +501,8 @@ __global__ void __launch_bounds__(352, 1)
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
         const uint64_t c_policy = policy_evict_first();
         const uint32_t tempty_leader = mapa_shared(bar_tempty, 0);
-        const bool early_release = p.out_f32 == 0 && p.e.resid == nullptr;
+        const bool early_release = !EX || (p.out_f32 == 0 && p.e.resid == nullptr);
+        const EpilogueArgs epi_e = EX ? p.e : EpilogueArgs{};
         int buf = 0;
         int it = 0;
         for (int tile = cluster_id; tile < p.num_tiles; tile += nclusters, ++it) {
@@ -528,7 +531,7 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     uint32_t hp[32];
-                    epilogue_pack64<T>(tmem_base + lane_addr + static_cast<uint32_t>(64 * j), p.e,
+                    epilogue_pack64<T>(tmem_base + lane_addr + static_cast<uint32_t>(64 * j), epi_e,
                                        p.relu, n0 + 64 * j, p.N, hp);
                     const uint32_t rb = cbuf + static_cast<uint32_t>(j) * 4096u + row_off;
 #pragma unroll
@@ -537,8 +540,8 @@ __global__ void __launch_bounds__(352, 1)
                                      hp[4 * u], hp[4 * u + 1], hp[4 * u + 2], hp[4 * u + 3]);
                 }
                 uint32_t h2[32], h3[32];
-                epilogue_pack64<T>(tmem_base + lane_addr + 128u, p.e, p.relu, n0 + 128, p.N, h2);
-                epilogue_pack64<T>(tmem_base + lane_addr + 192u, p.e, p.relu, n0 + 192, p.N, h3);
+                epilogue_pack64<T>(tmem_base + lane_addr + 128u, epi_e, p.relu, n0 + 128, p.N, h2);
+                epilogue_pack64<T>(tmem_base + lane_addr + 192u, epi_e, p.relu, n0 + 192, p.N, h3);
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
@@ -577,9 +580,9 @@ __global__ void __launch_bounds__(352, 1)
                     x[t] = __uint_as_float(v0[t]);
                     x[32 + t] = __uint_as_float(v1[t]);
                 }
-                epilogue_math<T>(x, p.e, p.relu, row0 + lane, n0 + 64 * j, p.M, p.N);
+                epilogue_math<T>(x, epi_e, p.relu, row0 + lane, n0 + 64 * j, p.M, p.N);
                 epilogue_store<T>(x, cbuf, buf, &tmC, c_policy, row0, n0 + 64 * j, p.M, p.N, lane,
-                                  p.out_f32 != 0);
+                                  EX && p.out_f32 != 0);
             }
         }
         if (lane == 0) bulk_wait_group<0>();

@@ -228,6 +228,10 @@ cudaError_t set_kernel_attributes() {
         e = cudaFuncSetAttribute(tg::tg_gemm_sp24_pair<kSpPairStages, T>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  tg::SparsePairCfg<kSpPairStages>::kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tg::tg_gemm_sp24_pair<kSpPairStages, T, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tg::SparsePairCfg<kSpPairStages>::kSmemBytes);
     return e;
 }
 
@@ -883,8 +887,11 @@ tg_status_t launch_sp24(const void* Ac, const void* E, const void* B, void* C, i
         cfg.blockDim = dim3(PairCfg::kThreads);
         cfg.dynamicSmemBytes = PairCfg::kSmemBytes;
         cfg.numAttrs = 2;
-        e = cudaLaunchKernelEx(&cfg, tg::tg_gemm_sp24_pair<kSpPairStages, T>, tmA, tmB, tmE, tmC,
-                               sp);
+        e = (ep.e.bias == nullptr && ep.e.resid == nullptr && ep.out_f32 == 0)
+                ? cudaLaunchKernelEx(&cfg, tg::tg_gemm_sp24_pair<kSpPairStages, T, false>, tmA,
+                                     tmB, tmE, tmC, sp)
+                : cudaLaunchKernelEx(&cfg, tg::tg_gemm_sp24_pair<kSpPairStages, T, true>, tmA,
+                                     tmB, tmE, tmC, sp);
     } else {
         const int64_t grid = prm.num_tiles < ds->num_sms ? prm.num_tiles : ds->num_sms;
         cfg.gridDim = dim3(static_cast<unsigned>(grid));
