@@ -286,13 +286,14 @@ LAST_LEG_CLOCKS = None   # its summary over the last timed region
 # the first one does and does not inherit the power state (clock cap) that
 # the legs before it left.
 LEG_IDLE_S = 1.0
+LEG_REWARM = 3  # launches between the idle and the timed region
 
 
 def time_launches(launch, stream, steps: int, world: int, device):
     """Time `steps` back-to-back launches on `stream` between two CUDA events,
     with no event between launches: consecutive launches overlap their
     start-up with the previous launch's tail, as in any stream of kernels.
-    The leg starts after LEG_IDLE_S of idle.
+    The leg starts after LEG_IDLE_S of idle and LEG_REWARM untimed launches.
     Returns (total_ms, mean_ms = total_ms / steps, per_ms, wall0, wall1).
     per_ms holds PER_LAUNCH_SAMPLES further launches, each bracketed by its
     own events; those events serialise the launches, so per_ms is context
@@ -302,6 +303,8 @@ def time_launches(launch, stream, steps: int, world: int, device):
     t_end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     time.sleep(LEG_IDLE_S)
+    for _ in range(LEG_REWARM):  # clocks back up after the idle
+        launch()
     barrier(world, device)
     torch.cuda.synchronize()
     wall0 = time.time()
