@@ -160,9 +160,10 @@ VARIANTS = [  # (relu, bias, residual, out)
     (False, False, False, "f32"),
     (True, True, True, "f32"),
 ]
-# 512×512×4096 and 300×700×2048: the pair kernel splits its tiles along k
-# (4 and 2 pieces), so the epilogue runs on summed partials; 64×4096×4096: the
-# skinny kernel's aligned grid (32 tiles in 4 equal k pieces)
+# 512×512×4096 and 300×700×2048: the pair kernel runs its tail tiles as
+# column halves (256×128 products); 64×4096×4096: the skinny kernel's aligned
+# grid (32 tiles in 4 equal k pieces).  The pair kernel's k-pieces, whose
+# epilogue runs on summed fp32 partials, are test_epilogue_pair_k_pieces.
 SHAPES = [(1, 1, 1), (129, 127, 1000), (300, 1000, 129), (64, 2048, 520), (257, 513, 65),
           (512, 512, 4096), (300, 700, 2048), (64, 4096, 4096)]
 
@@ -193,6 +194,72 @@ def test_epilogue_every_kernel(tg, monkeypatch, cfg, M, N, K, fmt):
         else:
             check(got, decode(want, fmt) if fmt == "bf16" else want, K,
                   relu=relu and not use_r, fmt=fmt, what=what)
+
+
+@pytest.mark.parametrize("fmt", ["f16", "bf16"])
+def test_epilogue_pair_k_pieces(tg, monkeypatch, fmt):
+    """256×512×12288 on the pair kernel: 2 tiles, each cut into 4 k-pieces;
+    the last piece in applies every epilogue variant to the summed partials."""
+    monkeypatch.setenv("TGEMM_FORCE_CFG", "pair256")
+    M, N, K = 256, 512, 12288
+    A, B, bias, R, A64, B64, R64 = draw_case(M, N, K, fmt, 4321)
+    a, b = dev16(A, fmt), dev16(B, fmt)
+    bias_d = torch.from_numpy(bias).cuda()
+    r_d = dev16(R, fmt)
+    for relu, use_bias, use_r, out in VARIANTS:
+        out_t = "f32" if out == "f32" else fmt
+        c = out_buffer(M, N, out_t, fmt)
+        st = call_ex(tg, fmt, a, b, c, M, N, K, relu=relu, bias=bias_d if use_bias else None,
+                     resid=r_d if use_r else None, out=out_t)
+        assert st == tg.TG_OK, tg.tg_status_string(st)
+        assert tg.tg_sync_status(torch.cuda.current_stream().cuda_stream) == tg.TG_OK
+        launched = tg.tg_debug_last_launch()
+        if launched.grid == 16:  # all pairs resident: the planned cut
+            assert launched.split_k == 4 and launched.split_n == 1
+        got = host_out(c, out_t, fmt)
+        want = oracle.gemm_ex(A, B, M, N, K, relu=relu, bias=bias if use_bias else None,
+                              R=R if use_r else None, in_dtype=fmt, out_dtype=out_t)
+        what = f"pair k-pieces {fmt} relu={relu} bias={use_bias} R={use_r} out={out_t}"
+        if out_t == "f32":
+            T = abs_scale(A64, B64, bias if use_bias else None, R64 if use_r else None)
+            check_f32(got, want, K, T, what=what)
+        else:
+            check(got, decode(want, fmt) if fmt == "bf16" else want, K,
+                  relu=relu and not use_r, fmt=fmt, what=what)
+
+
+@pytest.mark.parametrize("cfg", ["pair256", "persistent128", "persistent64"])
+def test_plain_and_full_builds_interleaved(tg, monkeypatch, cfg):
+    """Plain epilogues (ReLU or none, 16-bit out) run a build of each kernel
+    with the other epilogue paths compiled out.  Calls of both builds queued
+    back to back on one stream (dependent launch between different kernels),
+    with one synchronisation at the end, each match the oracle."""
+    monkeypatch.setenv("TGEMM_FORCE_CFG", cfg)
+    M, N, K, fmt = 384, 640, 512, "f16"
+    A, B, bias, R, A64, B64, R64 = draw_case(M, N, K, fmt, 97)
+    a, b = dev16(A, fmt), dev16(B, fmt)
+    bias_d = torch.from_numpy(bias).cuda()
+    r_d = dev16(R, fmt)
+    plan = [(True, False, False, fmt), (False, True, True, fmt), (False, False, False, "f32"),
+            (False, False, False, fmt), (True, True, False, "f32"), (True, False, False, fmt)]
+    outs = []
+    for relu, use_bias, use_r, out_t in plan:
+        c = out_buffer(M, N, out_t, fmt)
+        st = call_ex(tg, fmt, a, b, c, M, N, K, relu=relu, bias=bias_d if use_bias else None,
+                     resid=r_d if use_r else None, out=out_t)
+        assert st == tg.TG_OK, tg.tg_status_string(st)
+        outs.append(c)
+    assert tg.tg_sync_status(torch.cuda.current_stream().cuda_stream) == tg.TG_OK
+    for (relu, use_bias, use_r, out_t), c in zip(plan, outs):
+        got = host_out(c, out_t, fmt)
+        want = oracle.gemm_ex(A, B, M, N, K, relu=relu, bias=bias if use_bias else None,
+                              R=R if use_r else None, in_dtype=fmt, out_dtype=out_t)
+        what = f"{cfg} interleaved relu={relu} bias={use_bias} R={use_r} out={out_t}"
+        if out_t == "f32":
+            T = abs_scale(A64, B64, bias if use_bias else None, R64 if use_r else None)
+            check_f32(got, want, K, T, what=what)
+        else:
+            check(got, want, K, relu=relu and not use_r, fmt=fmt, what=what)
 
 
 @pytest.mark.parametrize("cfg", CFGS)
