@@ -61,9 +61,11 @@ def run(tg, A, B, M, N, K, relu=False):
 
 CFGS = ["pair256", "persistent256", "persistent128", "persistent64", "skinny"]
 # (64, 4096, 4096): the skinny kernel's four-piece aligned grid in clusters of 4;
-# (512, 512, 4096): the pair kernel's last wave split into k pieces
+# (512, 512, 4096): the pair kernel's last wave in column halves;
+# (256, 512, 12288): its tiles in 4 k-pieces
 SHAPES = [(1, 1, 1), (7, 7, 7), (129, 127, 1000), (200, 1000, 129), (300, 1000, 1000),
-          (64, 2048, 4096), (257, 513, 65), (64, 4096, 4096), (512, 512, 4096)]
+          (64, 2048, 4096), (257, 513, 65), (64, 4096, 4096), (512, 512, 4096),
+          (256, 512, 12288)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES, ids=[f"{m}x{n}x{k}" for m, n, k in SHAPES])

@@ -3,7 +3,8 @@ serves a stale map (GPU).
 
 * For a sweep of shapes covering every dense kernel, tg_plan_f16_limits with
   the current device's limits equals what tg_gemm_f16 launched (kernel,
-  tiles, grid, k-pieces, cluster size), read back with tg_debug_last_launch.
+  tiles, grid, k-pieces, column halves, cluster size), read back with
+  tg_debug_last_launch.
 * Repeated calls reuse their tensor maps (cache hits, no new encodings); a
   changed pointer, a changed leading dimension and new contents behind the
   same pointers each give the oracle's product for the new operands.
