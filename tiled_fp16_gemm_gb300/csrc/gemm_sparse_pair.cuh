@@ -14,35 +14,36 @@
 // speed the L2 → SM bandwidth sets.
 //
 // Tensor memory (512 columns per CTA): one 256-column fp32 accumulator and,
-// from column 256, a ring of four metadata slots of 64 columns — each MMA's
-// metadata column on a 16-column boundary.  Each CTA's tensor memory holds
+// from column 256, one metadata slot of 64 columns per operand stage — each
+// MMA's metadata column on a 16-column boundary.  Each CTA's tensor memory holds
 // the metadata of its own 128 rows at the same column, in the lane layout of
 // the one-CTA kernel.  With one accumulator the epilogue's tensor-memory
 // reads of a tile are not overlapped with the next tile's MMAs (its global
 // stores are).
 //
-// The metadata path is kept off the operand ring's critical path and needs
-// no signal between the CTAs:
+// The metadata path is kept off the operand ring's critical path:
 //   * E boxes are loaded (plain TMA, local barrier) three stages ahead of
 //     the operands into their own 4-slot ring;
-//   * each CTA's metadata warps write stage u's words into metadata slot
-//     u % 4 once the MMAs of stage u - 4 have completed, then arrive on a
-//     local barrier;
-//   * each CTA's producer issues stage u's Ac load only after that local
-//     barrier, so the even CTA's full barrier — which counts both CTAs'
-//     bytes — completes only once both CTAs' metadata for the stage is in
-//     tensor memory.
+//   * tensor memory holds one metadata slot per operand stage: each CTA's
+//     metadata warps write stage u's words into slot u % STAGES once the
+//     MMAs of stage u - STAGES have completed (the stage's empty barrier),
+//     then arrive on the even CTA's full barrier of the stage (the odd CTA's
+//     warps with a relaxed remote arrive: tcgen05.wait::st has completed
+//     their writes);
+//   * so full[s] stands for the stage's operands and both CTAs' metadata,
+//     while the operand loads wait only for their ring slot and run the
+//     whole ring ahead of the MMAs.
 // A single thread issuing every TMA copy of a stage would take longer than
 // the stage's MMAs, so two threads (warps 0 and 10) share them: warp 0 the
-// Ac box and the E box kEAhead stages ahead, warp 10 the two B boxes (which
-// wait only for the stage's slot to be free).
+// Ac box and the E box kEAhead stages ahead, warp 10 the two B boxes.
 //
 // Synchronisation (all waits bounded):
-//   full[s]    even CTA: Ac and B bytes of both CTAs (pair TMA loads);
-//   empty[s]   each CTA: multicast commit after the MMAs of stage s;
+//   full[s]    even CTA: Ac and B bytes of both CTAs (pair TMA loads), the
+//              producer's arrive and the 8 metadata warps of the pair;
+//   empty[s]   each CTA: multicast commit after the MMAs of stage s (frees
+//              the operand slot and the metadata slot);
 //   efull[e]   each CTA: its own E box;
-//   mready[m]  each CTA: its 4 metadata warps wrote slot m;
-//   mfree[m]   each CTA: multicast commit after the MMAs that read slot m;
+//   efree[e]   each CTA: its 4 metadata warps read E slot e;
 //   tfull      each CTA: multicast commit at the end of a tile;
 //   tempty     even CTA: the 8 epilogue warps of the pair read the tile.
 // A cluster barrier after set-up and before exit brackets the work.
@@ -68,12 +69,14 @@ struct SparsePairCfg {
     static constexpr int kThreads = 352;
     static constexpr int kESlots = 4;   // E ring
     static constexpr int kEAhead = 3;   // E boxes issued this many stages ahead
-    static constexpr int kMSlots = 4;   // metadata ring in tensor memory
     static constexpr uint32_t kABytes = 128 * (BK / 2) * 2;  // 16 KB of kept values
     static constexpr uint32_t kBBytes = BK * 128 * 2;        // 32 KB: two 64-column boxes
     static constexpr uint32_t kEBytes = 128 * (BK / 32) * 4; // 2 KB of metadata
     static constexpr uint32_t kCBuf = 32 * 64 * 2;
-    static constexpr uint32_t kCBytes = 4 * 2 * kCBuf;
+    // staging buffers per epilogue warp: two, or one where a fourth operand
+    // stage takes the room (plain epilogue only)
+    static constexpr int kCBufs = STAGES >= 4 ? 1 : 2;
+    static constexpr uint32_t kCBytes = 4 * kCBufs * kCBuf;
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kMetaCol0 = BN;
     static constexpr uint32_t kMetaSlotCols = 64;
@@ -81,12 +84,14 @@ struct SparsePairCfg {
     static constexpr uint32_t kBarBytes = 256;
     static constexpr uint32_t kSmemBytes = 1024 + STAGES * (kABytes + kBBytes) +
                                            kESlots * kEBytes + kCBytes + kBarBytes;
-    static_assert(kMetaCol0 + kMetaSlotCols * kMSlots <= kTmemCols,
+    static_assert(kMetaCol0 + kMetaSlotCols * STAGES <= kTmemCols,
                   "metadata columns exceed tensor memory");
     // E slot (u + kEAhead) % kESlots was last read for stage u + kEAhead -
-    // kESlots <= u - 1, whose metadata the producer waited for at stage u - 1.
+    // kESlots <= u - 1, a read that follows the MMAs of stage u - 1 - STAGES;
+    // those completed before stage u's operand slot was free, so the
+    // producer's wait for the read (efree) is short.
     static_assert(kEAhead < kESlots, "E ring too shallow for the look-ahead");
-    static_assert(8 * (2 * STAGES + kESlots + 2 * kMSlots) + 32 <= kBarBytes,
+    static_assert(8 * (2 * STAGES + 2 * kESlots) + 32 <= kBarBytes,
                   "barrier area too small");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeded");
 };
@@ -120,9 +125,11 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 }
 
 // Arrive on an mbarrier of the peer CTA without release semantics (no memory
-// barrier): used where the signal only says "this thread has finished reading
-// tensor memory" — tcgen05.wait::ld completed those reads before the arrive
-// issues, and there are no writes whose visibility it would have to order.
+// barrier): used where the signal only says "this thread's tensor-memory
+// reads (or writes) are done" — tcgen05.wait::ld (wait::st) completed them
+// before the arrive issues, and there is no generic-proxy memory whose
+// visibility it would have to order.  A release arrive at cluster scope costs
+// a memory barrier of about 1500 cycles.
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
@@ -163,6 +170,27 @@ __device__ __forceinline__ void epilogue_pack64(uint32_t taddr, const EpilogueAr
     for (int t = 0; t < 32; ++t) h[t] = Elem16<T>::pack2(x[2 * t], x[2 * t + 1]);
 }
 
+// Stage and store one 64-column chunk of packed 16-bit pairs through this
+// warp's single 4 KB staging buffer, once the previous store has read it.
+__device__ __forceinline__ void epilogue_store_one_buffer(const uint32_t (&h)[32], uint32_t cbuf,
+                                                          const void* tmC, uint64_t policy,
+                                                          int row0, int col0, int M, int N,
+                                                          int lane) {
+    if (lane == 0) bulk_wait_group_read<0>();
+    __syncwarp();
+    const uint32_t row_addr = cbuf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        st_shared_v4(row_addr + ((static_cast<uint32_t>(c) ^ (lane & 7u)) << 4), h[4 * c],
+                     h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (row0 < M && col0 < N) tma_store_2d_hint(tmC, cbuf, col0, row0, policy);
+        bulk_commit_group();
+    }
+}
+
 __device__ __forceinline__ void mma_f16_sp_pair(uint32_t d_tmem, uint64_t a_desc,
                                                 uint64_t b_desc, uint32_t meta_tmem,
                                                 uint32_t idesc, uint32_t accumulate) {
@@ -175,16 +203,15 @@ __device__ __forceinline__ void mma_f16_sp_pair(uint32_t d_tmem, uint64_t a_desc
 }
 
 // One stage (128 dense-equivalent k) of the pair: four sparse MMAs of 256 ×
-// 256 × 32 and the two release commits (operand stage and metadata slot,
-// multicast to both CTAs), issued by one elected lane of a converged warp in
-// one block.  MMA k reads A 32 B further (ad + 2 k), B 4 KB further (bd +
+// 256 × 32 and the release commit of the stage (its operand and metadata
+// slots, multicast to both CTAs), issued by one elected lane of a converged
+// warp in one block.  MMA k reads A 32 B further (ad + 2 k), B 4 KB further (bd +
 // 256 k) and metadata 16 columns further.  first != 0: the first MMA
 // overwrites D.  The issuing warp shares its scheduler with the metadata and
 // epilogue warps; the single block keeps its instruction count per stage low.
 __device__ __forceinline__ void sp_pair_stage_mma_elect(uint32_t d_tmem, uint64_t ad, uint64_t bd,
                                                         uint32_t meta, uint32_t idesc,
-                                                        uint32_t first, uint32_t bar_stage,
-                                                        uint32_t bar_meta) {
+                                                        uint32_t first, uint32_t bar_stage) {
     asm volatile(
         "{\n\t.reg .pred e, p, t;\n\t.reg .b32 m;\n\t.reg .b64 a, b;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
@@ -198,11 +225,9 @@ __device__ __forceinline__ void sp_pair_stage_mma_elect(uint32_t d_tmem, uint64_
         "add.u64 a, %1, 6;\n\tadd.u64 b, %2, 768;\n\tadd.u32 m, %3, 48;\n\t"
         "@e tcgen05.mma.sp.cta_group::2.kind::f16 [%0], a, b, [m], %4, t;\n\t"
         "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%6], %8;\n\t"
-        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%7], %8;\n\t"
+        " [%6], %7;\n\t"
         "}" ::"r"(d_tmem),
-        "l"(ad), "l"(bd), "r"(meta), "r"(idesc), "r"(first), "r"(bar_stage), "r"(bar_meta),
+        "l"(ad), "l"(bd), "r"(meta), "r"(idesc), "r"(first), "r"(bar_stage),
         "h"(static_cast<uint16_t>(0x3))
         : "memory");
 }
@@ -245,9 +270,9 @@ __global__ void __launch_bounds__(352, 1)
                       const __grid_constant__ CUtensorMap tmE,
                       const __grid_constant__ CUtensorMap tmC, const SparseParams sp) {
     using Cfg = SparsePairCfg<STAGES>;
+    static_assert(Cfg::kCBufs == 2 || !EX, "one staging buffer per warp: plain epilogue only");
     constexpr int S = STAGES;
     constexpr int SE = Cfg::kESlots;
-    constexpr int SM = Cfg::kMSlots;
     const PersistentParams& p = sp.base;
 
     extern __shared__ uint8_t smem_raw[];
@@ -263,9 +288,8 @@ __global__ void __launch_bounds__(352, 1)
     const uint32_t bar_full = sBar;                  // [S]
     const uint32_t bar_empty = bar_full + 8 * S;     // [S]
     const uint32_t bar_efull = bar_empty + 8 * S;    // [SE]
-    const uint32_t bar_mready = bar_efull + 8 * SE;  // [SM]
-    const uint32_t bar_mfree = bar_mready + 8 * SM;  // [SM]
-    const uint32_t bar_tfull = bar_mfree + 8 * SM;
+    const uint32_t bar_efree = bar_efull + 8 * SE;   // [SE]
+    const uint32_t bar_tfull = bar_efree + 8 * SE;
     const uint32_t bar_tempty = bar_tfull + 8;
     const uint32_t bar_drain = bar_tempty + 8;
     const uint32_t slot_tmem = bar_drain + 8;
@@ -285,13 +309,12 @@ __global__ void __launch_bounds__(352, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_full + 8 * s, 1 + 8);  // producer + metadata warps (even CTA's)
             mbar_init(bar_empty + 8 * s, 1);
         }
-        for (int e = 0; e < SE; ++e) mbar_init(bar_efull + 8 * e, 1);
-        for (int m = 0; m < SM; ++m) {
-            mbar_init(bar_mready + 8 * m, 4);
-            mbar_init(bar_mfree + 8 * m, 1);
+        for (int e = 0; e < SE; ++e) {
+            mbar_init(bar_efull + 8 * e, 1);
+            mbar_init(bar_efree + 8 * e, 4);
         }
         mbar_init(bar_tfull, 1);
         mbar_init(bar_tempty, 8);
@@ -330,10 +353,14 @@ __global__ void __launch_bounds__(352, 1)
             uint32_t e_issued_mask = 0, e_issued_parity = 0;  // efull[] phases armed here
             StageIter e_it(cluster_id, p, nclusters);
             int e_next = 0;  // next stage whose E box is issued
-            auto issue_e = [&]() {
+            // E box of stage e_next into slot e_next % SE, once the metadata
+            // warps have read the slot's previous box (stage e_next - SE).
+            auto issue_e = [&]() -> bool {
                 const int ma = e_it.m_blk * Cfg::BM + static_cast<int>(rank) * 128;
                 const int slot = e_next % SE;
                 const uint32_t par = static_cast<uint32_t>(e_next / SE) & 1u;
+                if (!mbar_wait(bar_efree + 8 * slot, par ^ 1u, p.timeout_ns, abort_flag))
+                    return false;
                 const uint32_t eb = bar_efull + 8 * slot;
                 mbar_arrive_expect_tx(eb, Cfg::kEBytes);
                 tma_load_2d(sE + slot * Cfg::kEBytes, &tmE, eb, e_it.kb * (Cfg::BK / 32), ma);
@@ -341,21 +368,20 @@ __global__ void __launch_bounds__(352, 1)
                 e_issued_parity = (e_issued_parity & ~(1u << slot)) | (par << slot);
                 e_it.next();
                 ++e_next;
+                return true;
             };
+            // the first kEAhead slots are free: these waits return at once
             while (e_next < U && e_next < Cfg::kEAhead) issue_e();
             bool ok = true;
             StageIter it(cluster_id, p, nclusters);
-            int stage = 0, mslot = 0;
-            uint32_t phase = 0, mphase = 0;
+            int stage = 0;
+            uint32_t phase = 0;
             for (int u = 0; u < U; ++u, it.next()) {
-                if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.timeout_ns, abort_flag) ||
-                    !mbar_wait(bar_mready + 8 * mslot, mphase, p.timeout_ns, abort_flag)) {
+                if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, p.timeout_ns, abort_flag)) {
                     fail(kRoleProducer);
                     ok = false;
                     break;
                 }
-                // This CTA's metadata for stage u is in tensor memory: the
-                // loads below complete full[stage] only after it.
                 const int ma = it.m_blk * Cfg::BM + static_cast<int>(rank) * 128;
                 if (leader)
                     mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * (Cfg::kABytes + Cfg::kBBytes));
@@ -366,14 +392,14 @@ __global__ void __launch_bounds__(352, 1)
                                       ma, a_policy);
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                if (e_next < U) issue_e();
+                if (e_next < U && !issue_e()) {
+                    fail(kRoleProducer);
+                    ok = false;
+                    break;
+                }
                 if (++stage == S) {
                     stage = 0;
                     phase ^= 1u;
-                }
-                if (++mslot == SM) {
-                    mslot = 0;
-                    mphase ^= 1u;
                 }
             }
             if (ok) {
@@ -417,7 +443,7 @@ __global__ void __launch_bounds__(352, 1)
             const uint64_t adesc0 = smem_desc_sw128(sA, 16, 1024);
             const uint64_t bdesc0 = smem_desc_sw128(sB, 16384, 1024);
             constexpr uint64_t kAStep = Cfg::kABytes >> 4, kBStep = Cfg::kBBytes >> 4;
-            int stage = 0, mslot = 0;
+            int stage = 0;
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
@@ -430,7 +456,9 @@ __global__ void __launch_bounds__(352, 1)
                 }
                 tc_fence_after_sync();
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    const bool got = mbar_wait(bar_full + 8 * stage, phase, p.timeout_ns, abort_flag);
+                    // the stage's operands, and both CTAs' metadata for it
+                    const bool got =
+                        mbar_wait(bar_full + 8 * stage, phase, p.timeout_ns, abort_flag);
                     if (!__all_sync(0xffffffffu, got ? 1 : 0)) {
                         if (lane == 0) fail(kRoleMma);
                         ok = false;
@@ -440,13 +468,13 @@ __global__ void __launch_bounds__(352, 1)
                     sp_pair_stage_mma_elect(
                         tmem_base, adesc0 + static_cast<uint64_t>(stage) * kAStep,
                         bdesc0 + static_cast<uint64_t>(stage) * kBStep,
-                        tmem_base + Cfg::kMetaCol0 + static_cast<uint32_t>(mslot) * Cfg::kMetaSlotCols,
-                        idesc, kb == 0 ? 1u : 0u, bar_empty + 8 * stage, bar_mfree + 8 * mslot);
+                        tmem_base + Cfg::kMetaCol0 +
+                            static_cast<uint32_t>(stage) * Cfg::kMetaSlotCols,
+                        idesc, kb == 0 ? 1u : 0u, bar_empty + 8 * stage);
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
-                    if (++mslot == SM) mslot = 0;
                 }
                 if (!ok) break;
                 if (!(p.inject == 1 && it == 0)) {
@@ -497,7 +525,7 @@ __global__ void __launch_bounds__(352, 1)
     } else if (warp < 6) {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int q = warp & 3;
-        const uint32_t cbuf = sC + static_cast<uint32_t>((warp - 2) * 2) * Cfg::kCBuf;
+        const uint32_t cbuf = sC + static_cast<uint32_t>((warp - 2) * Cfg::kCBufs) * Cfg::kCBuf;
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
         const uint64_t c_policy = policy_evict_first();
         const uint32_t tempty_leader = mapa_shared(bar_tempty, 0);
@@ -519,7 +547,39 @@ __global__ void __launch_bounds__(352, 1)
                 break;
             }
             tc_fence_after_sync();
-            if (early_release) {
+            if constexpr (Cfg::kCBufs == 1) {
+                // One staging buffer: columns 0..63 go straight into it,
+                // 64..255 into registers, then the accumulator is released
+                // and the chunks are stored one after another.
+                if (lane == 0) bulk_wait_group_read<0>();  // the buffer is free
+                __syncwarp();
+                const uint32_t row_off = static_cast<uint32_t>(lane) * 128u;
+                {
+                    uint32_t hp[32];
+                    epilogue_pack64<T>(tmem_base + lane_addr, epi_e, p.relu, n0, p.N, hp);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        st_shared_v4(cbuf + row_off +
+                                         ((static_cast<uint32_t>(u) ^ (lane & 7u)) << 4),
+                                     hp[4 * u], hp[4 * u + 1], hp[4 * u + 2], hp[4 * u + 3]);
+                }
+                uint32_t h1[32], h2[32], h3[32];
+                epilogue_pack64<T>(tmem_base + lane_addr + 64u, epi_e, p.relu, n0 + 64, p.N, h1);
+                epilogue_pack64<T>(tmem_base + lane_addr + 128u, epi_e, p.relu, n0 + 128, p.N, h2);
+                epilogue_pack64<T>(tmem_base + lane_addr + 192u, epi_e, p.relu, n0 + 192, p.N, h3);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (row0 < p.M && n0 < p.N) tma_store_2d_hint(&tmC, cbuf, n0, row0, c_policy);
+                    bulk_commit_group();
+                }
+                epilogue_store_one_buffer(h1, cbuf, &tmC, c_policy, row0, n0 + 64, p.M, p.N, lane);
+                epilogue_store_one_buffer(h2, cbuf, &tmC, c_policy, row0, n0 + 128, p.M, p.N, lane);
+                epilogue_store_one_buffer(h3, cbuf, &tmC, c_policy, row0, n0 + 192, p.M, p.N, lane);
+            } else if (early_release) {
                 // 16-bit C without a residual: the row's 256 columns are read,
                 // finished and rounded before anything is stored — columns
                 // 0..127 straight into the two staging buffers (swizzled as
@@ -561,28 +621,28 @@ __global__ void __launch_bounds__(352, 1)
                                       lane);
                 epilogue_store_packed(h3, cbuf, buf, &tmC, c_policy, row0, n0 + 192, p.M, p.N,
                                       lane);
-                continue;
-            }
+            } else {
 #pragma unroll 1
-            for (int j = 0; j < Cfg::BN / 64; ++j) {
-                uint32_t v0[32], v1[32];
-                const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(j * 64);
-                tmem_ld_x32(taddr, v0);
-                tmem_ld_x32(taddr + 32, v1);
-                if (j == Cfg::BN / 64 - 1) {
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
-                }
-                float x[64];
+                for (int j = 0; j < Cfg::BN / 64; ++j) {
+                    uint32_t v0[32], v1[32];
+                    const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(j * 64);
+                    tmem_ld_x32(taddr, v0);
+                    tmem_ld_x32(taddr + 32, v1);
+                    if (j == Cfg::BN / 64 - 1) {
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
+                    }
+                    float x[64];
 #pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    x[t] = __uint_as_float(v0[t]);
-                    x[32 + t] = __uint_as_float(v1[t]);
+                    for (int t = 0; t < 32; ++t) {
+                        x[t] = __uint_as_float(v0[t]);
+                        x[32 + t] = __uint_as_float(v1[t]);
+                    }
+                    epilogue_math<T>(x, epi_e, p.relu, row0 + lane, n0 + 64 * j, p.M, p.N);
+                    epilogue_store<T>(x, cbuf, buf, &tmC, c_policy, row0, n0 + 64 * j, p.M,
+                                      p.N, lane, EX && p.out_f32 != 0);
                 }
-                epilogue_math<T>(x, epi_e, p.relu, row0 + lane, n0 + 64 * j, p.M, p.N);
-                epilogue_store<T>(x, cbuf, buf, &tmC, c_policy, row0, n0 + 64 * j, p.M, p.N, lane,
-                                  EX && p.out_f32 != 0);
             }
         }
         if (lane == 0) bulk_wait_group<0>();
@@ -599,14 +659,20 @@ __global__ void __launch_bounds__(352, 1)
         const uint32_t h = (L >> 3) & 1u;
         const uint32_t lane_addr = (32u * static_cast<uint32_t>(warp & 3)) << 16;
         constexpr uint32_t kNeutral = 0x4444u;  // positions (0, 1) in every group of a half
+        // The MMA thread reads these writes once the even CTA's full barrier
+        // of the stage has the pair's 8 arrivals (and the operand bytes).  A
+        // relaxed arrive suffices for the odd CTA: tcgen05.wait::st has
+        // completed the writes before it issues, and no other memory is
+        // handed over.
+        const uint32_t full_leader = mapa_shared(bar_full, 0);
         StageIter it(cluster_id, p, nclusters);
         int eslot = 0, mslot = 0;
-        uint32_t ephase = 0, mphase = 0;
+        uint32_t ephase = 0, mphase = 0;  // mslot: the stage's operand and metadata slot
         for (int u = 0; u < U; ++u, it.next()) {
             int got = 1;
             if (lane == 0)
                 got = (mbar_wait(bar_efull + 8 * eslot, ephase, p.timeout_ns, abort_flag) &&
-                       mbar_wait(bar_mfree + 8 * mslot, mphase ^ 1u, p.timeout_ns, abort_flag))
+                       mbar_wait(bar_empty + 8 * mslot, mphase ^ 1u, p.timeout_ns, abort_flag))
                           ? 1 : 0;
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) {
@@ -630,6 +696,8 @@ __global__ void __launch_bounds__(352, 1)
                 const uint32_t hi = (row1_in && word_in) ? (b[w] >> (16 * h)) & 0xFFFFu : kNeutral;
                 t[w] = lo | (hi << 16);
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_efree + 8 * eslot);  // the E slot is read
             const uint32_t col = tmem_base + lane_addr + Cfg::kMetaCol0 +
                                  static_cast<uint32_t>(mslot) * Cfg::kMetaSlotCols;
 #pragma unroll
@@ -637,12 +705,17 @@ __global__ void __launch_bounds__(352, 1)
             tmem_wait_st();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_mready + 8 * mslot);
+            if (lane == 0) {
+                if (leader)
+                    mbar_arrive(bar_full + 8 * mslot);
+                else
+                    mbar_arrive_cluster_relaxed(full_leader + 8u * static_cast<uint32_t>(mslot));
+            }
             if (++eslot == SE) {
                 eslot = 0;
                 ephase ^= 1u;
             }
-            if (++mslot == SM) {
+            if (++mslot == S) {
                 mslot = 0;
                 mphase ^= 1u;
             }

@@ -79,9 +79,11 @@ using PairCfgT = tg::PairCfg<kPairStages, kPairBK>;
 // 16: 1629, 32: 1552 TFLOP/s.
 constexpr int kPairGroupM = 16;
 
-// 2:4 sparse pair kernel: 3 stages of 50 KB per CTA (a fourth does not fit
-// beside the epilogue's staging buffers).
+// 2:4 sparse pair kernel: 48 KB of operands per stage and CTA.  The plain
+// build runs 4 stages with one staging buffer per epilogue warp; the full
+// build (bias, residual, fp32 C) keeps two buffers, which leaves room for 3.
 constexpr int kSpPairStages = 3;
+constexpr int kSpPairStagesPlain = 4;
 
 // What bounds a launch on one device: its SMs, the CTA pairs of the pair
 // kernel that fit on it at once, and the clusters of four skinny CTAs (Mp <=
@@ -229,9 +231,9 @@ cudaError_t set_kernel_attributes() {
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  tg::SparsePairCfg<kSpPairStages>::kSmemBytes);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(tg::tg_gemm_sp24_pair<kSpPairStages, T, false>,
+        e = cudaFuncSetAttribute(tg::tg_gemm_sp24_pair<kSpPairStagesPlain, T, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 tg::SparsePairCfg<kSpPairStages>::kSmemBytes);
+                                 tg::SparsePairCfg<kSpPairStagesPlain>::kSmemBytes);
     return e;
 }
 
@@ -295,6 +297,11 @@ tg_status_t current_device(int* dev, DeviceState** st) {
                                              tg::SparsePairCfg<kSpPairStages>::kThreads,
                                              tg::SparsePairCfg<kSpPairStages>::kSmemBytes,
                                              s.num_sms, 2);
+        const int plain_sp_pairs = max_active_clusters(
+            tg::tg_gemm_sp24_pair<kSpPairStagesPlain, __half, false>,
+            tg::SparsePairCfg<kSpPairStagesPlain>::kThreads,
+            tg::SparsePairCfg<kSpPairStagesPlain>::kSmemBytes, s.num_sms, 2);
+        if (plain_sp_pairs < s.max_sp_pairs) s.max_sp_pairs = plain_sp_pairs;
         using NarrowCfg = tg::SkinnyNarrow;
         using WideCfg = tg::SkinnyWide;
         s.max_skinny_quads[0] = max_active_clusters(
@@ -885,13 +892,16 @@ tg_status_t launch_sp24(const void* Ac, const void* E, const void* B, void* C, i
         attr[1].val.clusterDim.z = 1;
         cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
         cfg.blockDim = dim3(PairCfg::kThreads);
-        cfg.dynamicSmemBytes = PairCfg::kSmemBytes;
         cfg.numAttrs = 2;
-        e = (ep.e.bias == nullptr && ep.e.resid == nullptr && ep.out_f32 == 0)
-                ? cudaLaunchKernelEx(&cfg, tg::tg_gemm_sp24_pair<kSpPairStages, T, false>, tmA,
-                                     tmB, tmE, tmC, sp)
-                : cudaLaunchKernelEx(&cfg, tg::tg_gemm_sp24_pair<kSpPairStages, T, true>, tmA,
-                                     tmB, tmE, tmC, sp);
+        if (ep.e.bias == nullptr && ep.e.resid == nullptr && ep.out_f32 == 0) {
+            cfg.dynamicSmemBytes = tg::SparsePairCfg<kSpPairStagesPlain>::kSmemBytes;
+            e = cudaLaunchKernelEx(&cfg, tg::tg_gemm_sp24_pair<kSpPairStagesPlain, T, false>, tmA,
+                                   tmB, tmE, tmC, sp);
+        } else {
+            cfg.dynamicSmemBytes = PairCfg::kSmemBytes;
+            e = cudaLaunchKernelEx(&cfg, tg::tg_gemm_sp24_pair<kSpPairStages, T, true>, tmA, tmB,
+                                   tmE, tmC, sp);
+        }
     } else {
         const int64_t grid = prm.num_tiles < ds->num_sms ? prm.num_tiles : ds->num_sms;
         cfg.gridDim = dim3(static_cast<unsigned>(grid));
