@@ -149,6 +149,22 @@ def test_sp24_integers_exact(tg, kern, M, N, K):
     assert np.array_equal(got, want)
 
 
+@pytest.mark.parametrize("M,N,K", [(2560, 2304, 288), (2304, 2560, 544)])
+def test_sp24_ring_across_tiles_exact(tg, kern, M, N, K):
+    """More 256×256 tiles (90) than CTA pairs fit on the GPU, with 3 and 5
+    k blocks of 128: a cluster runs two tiles, and its operand and metadata
+    rings carry on from one tile into the next at a stage offset other than 0
+    (4-stage plain build, and 3-stage full build through the bias).  Integer
+    inputs: every sum is exact, so C equals the oracle bit for bit."""
+    Ac, E, B = case(M, N, K, "f16", 15 + K, integer=True)
+    got = run(tg, "f16", Ac, E, B, M, N, K)
+    assert np.array_equal(got, oracle.gemm_sp24(Ac, E, B, M, N, K).astype(np.float64))
+    bias = np.random.default_rng(16 + K).integers(-4, 5, N).astype(np.float32)
+    got = run(tg, "f16", Ac, E, B, M, N, K, relu=True, bias=bias)
+    want = oracle.gemm_sp24(Ac, E, B, M, N, K, relu=True, bias=bias)
+    assert np.array_equal(got, want.astype(np.float64))
+
+
 def test_sp24_metadata_padding(tg, kern):
     """Metadata words past K/32 in a padded row stride are never used."""
     M, N, K = 64, 128, 96
