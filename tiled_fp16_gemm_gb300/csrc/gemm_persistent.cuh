@@ -141,14 +141,22 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot_ptr;
-    if (warp == 0 && lane == 0 && static_cast<int>(blockIdx.x) < p.num_tiles) {
-        // the first ring's worth of this CTA's operand tiles into L2 while
-        // the previous kernel finishes
-        const TileCoord tc = tile_coord(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m);
-        for (int kb = 0; kb < STAGES && kb < p.k_blocks; ++kb) {
-            tma_prefetch_2d(&tmA, kb * BK, tc.m_blk * BM);
+    // Producer set-up that reads no data of the previous kernel (its cache
+    // policy, its first tile's block coordinates) is done before the
+    // dependency wait, with the first ring's worth of this CTA's operand
+    // tiles prefetched into L2 while the previous kernel finishes.
+    uint64_t a_policy = 0;
+    TileCoord tc_first{0, 0};
+    if (warp == 0 && lane == 0) {
+        a_policy = policy_evict_last();
+        if (static_cast<int>(blockIdx.x) < p.num_tiles) {
+            tc_first = tile_coord(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m);
+            for (int kb = 0; kb < STAGES && kb < p.k_blocks; ++kb) {
+                tma_prefetch_2d(&tmA, kb * BK, tc_first.m_blk * BM);
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_prefetch_2d(&tmB, tc.n_blk * BN + 64 * j, kb * BK);
+                for (int j = 0; j < BN / 64; ++j)
+                    tma_prefetch_2d(&tmB, tc_first.n_blk * BN + 64 * j, kb * BK);
+            }
         }
     }
     grid_dependency_wait();  // the previous kernel's writes are visible from here on
@@ -162,13 +170,14 @@ __global__ void __launch_bounds__(192, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            const uint64_t a_policy = policy_evict_last();
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_parity = 0;  // last load per stage
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-                const TileCoord tc = tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m);
+                const TileCoord tc = tile == static_cast<int>(blockIdx.x)
+                                         ? tc_first
+                                         : tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m);
                 const int m0 = tc.m_blk * BM;
                 const int n0 = tc.n_blk * BN;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {

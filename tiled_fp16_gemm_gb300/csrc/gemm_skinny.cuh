@@ -308,11 +308,40 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot_ptr;
+
+    // fp16 B: the operand ring (B^T + A per stage).  QB: the raw ring (codes +
+    // scales + A).
+    constexpr int kRing = QB ? kRaw : kSkStages;
+    constexpr int kProd = skinny_producers(kRing);
+    static_assert(kRing % kProd == 0, "each ring stage must belong to one producer thread");
+    constexpr int kMma2Warp = QB ? 6 + kMxConvWarps : -1;  // QB: the second MMA warp
+    constexpr int kProdWarp1 = 6 + (QB ? kMxConvWarps + 1 : 0);  // warp of producer 1
+    constexpr int kAProdWarp = QB ? kProdWarp1 + kProd - 1 : -1;  // QB: A ring producer
+    const int prod = warp == 0 ? 0
+                     : (warp >= kProdWarp1 && warp < kProdWarp1 + kProd - 1 ? warp - kProdWarp1 + 1
+                                                                             : -1);
+    // Producer set-up that reads no data of the previous kernel (cache
+    // policies, the first unit's tile and k block: a 64-bit division) is done
+    // before the dependency wait.
+    uint64_t keep_policy = 0, stream_policy = 0;
+    int32_t prod_t = 0, prod_kb = 0;  // producer thread: (tile, k block) of its first unit
+    int32_t a_kb = 0;                 // QB, A ring producer: its first k block
+    if (lane == 0 && (prod >= 0 || warp == kAProdWarp)) {
+        keep_policy = policy_evict_last();     // A: reread by every CTA
+        stream_policy = policy_evict_first();  // B: read exactly once
+        if (prod >= 0) {
+            const int64_t u0 = u_begin + prod;
+            prod_t = static_cast<int32_t>(u0 / KB);
+            prod_kb = static_cast<int32_t>(u0 - static_cast<int64_t>(prod_t) * KB);
+        } else {
+            a_kb = static_cast<int32_t>(u_begin % KB);
+        }
+    }
     if (warp == 0 && lane == 0) {
         // the first ring's worth of this CTA's units into L2 while the
-        // previous kernel finishes
-        int32_t t = static_cast<int32_t>(u_begin / KB);
-        int32_t kb = static_cast<int32_t>(u_begin - static_cast<int64_t>(t) * KB);
+        // previous kernel finishes (producer 0's first unit is u_begin)
+        int32_t t = prod_t;
+        int32_t kb = prod_kb;
         // (MXFP4: two units.  Prefetching the whole raw ring kept the TMA unit
         // busy for about 3 us after the dependency wait, and the first loads
         // queued behind it.)
@@ -343,30 +372,18 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
         *abort_flag = 1;
     };
 
-    // fp16 B: the operand ring (B^T + A per stage).  QB: the raw ring (codes +
-    // scales + A).
-    constexpr int kRing = QB ? kRaw : kSkStages;
-    constexpr int kProd = skinny_producers(kRing);
-    static_assert(kRing % kProd == 0, "each ring stage must belong to one producer thread");
-    constexpr int kMma2Warp = QB ? 6 + kMxConvWarps : -1;  // QB: the second MMA warp
-    constexpr int kProdWarp1 = 6 + (QB ? kMxConvWarps + 1 : 0);  // warp of producer 1
-    constexpr int kAProdWarp = QB ? kProdWarp1 + kProd - 1 : -1;  // QB: A ring producer
-    const int prod = warp == 0 ? 0
-                     : (warp >= kProdWarp1 && warp < kProdWarp1 + kProd - 1 ? warp - kProdWarp1 + 1
-                                                                             : -1);
     if (prod >= 0) {
         // ------------------------------------------------------------ producers
         if (lane == 0) {
-            const uint64_t keep = policy_evict_last();   // A: reread by every CTA
-            const uint64_t stream = policy_evict_first(); // B: read exactly once
+            const uint64_t keep = keep_policy;
+            const uint64_t stream = stream_policy;
             const uint32_t ring_full = QB ? bar_rfull : bar_full;
             const uint32_t ring_empty = QB ? bar_rempty : bar_empty;
             uint32_t issued_mask = 0, issued_parity = 0;
             // (tile, k block) of this producer's next unit, advanced by kProd
             // units per step (no division per unit)
-            const int64_t u0 = u_begin + prod;
-            int32_t t = static_cast<int32_t>(u0 / KB);
-            int32_t kb = static_cast<int32_t>(u0 - static_cast<int64_t>(t) * KB);
+            int32_t t = prod_t;
+            int32_t kb = prod_kb;
             for (int64_t i = prod; u_begin + i < u_end; i += kProd) {
                 const int stage = static_cast<int>(i % kRing);
                 const uint32_t phase = static_cast<uint32_t>((i / kRing) & 1);
@@ -410,9 +427,9 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
     } else if (warp == kAProdWarp) {
         // ------------------------------------------------------------ A ring producer (QB)
         if constexpr (QB) if (lane == 0) {
-            const uint64_t keep = policy_evict_last();  // A: reread by every CTA
+            const uint64_t keep = keep_policy;
             uint32_t issued_mask = 0, issued_parity = 0;
-            int32_t kb = static_cast<int32_t>(u_begin % KB);
+            int32_t kb = a_kb;
             for (int64_t i = 0; u_begin + i < u_end; ++i) {
                 const int stage = static_cast<int>(i % kAS);
                 const uint32_t phase = static_cast<uint32_t>((i / kAS) & 1);
