@@ -165,6 +165,17 @@ def test_sp24_ring_across_tiles_exact(tg, kern, M, N, K):
     assert np.array_equal(got, want.astype(np.float64))
 
 
+@pytest.mark.parametrize("M,N,K", [(512, 512, 8192), (1024, 1024, 1024), (256, 2048, 4096)])
+def test_sp24_planner_choice(tg, monkeypatch, M, N, K):
+    """The planner's own kernel (no override): long K below a wave takes the
+    CTA pairs (512×512×8192, 256×2048×4096), short K the one-CTA kernel (1024³)."""
+    monkeypatch.delenv("TGEMM_FORCE_SP24", raising=False)
+    Ac, E, B = case(M, N, K, "f16", 17 + M + K)
+    got = run(tg, "f16", Ac, E, B, M, N, K, relu=True)
+    check(got, oracle.gemm_sp24(Ac, E, B, M, N, K, relu=True), K, relu=True,
+          what=f"sp24 planned {M}x{N}x{K}")
+
+
 def test_sp24_metadata_padding(tg, kern):
     """Metadata words past K/32 in a padded row stride are never used."""
     M, N, K = 64, 128, 96
