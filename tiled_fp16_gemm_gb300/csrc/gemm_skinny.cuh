@@ -217,7 +217,9 @@ __device__ __forceinline__ void tmem_ld2_x16(uint32_t a, uint32_t b, uint32_t (&
 
 // The kernel body shared by the fp16/bf16 kernel (QB = false: B^T tiles by
 // TMA) and the MXFP4 kernel (QB = true: B^T tiles decoded by warps 6..13).
-template <int STAGES, int MP_MAX, typename T, bool QB, int BK = 64>
+// EX = false: the plain epilogue only (no bias, no residual, 16-bit C), with a
+// short store loop; the other epilogue paths are compiled out.
+template <int STAGES, int MP_MAX, typename T, bool QB, int BK = 64, bool EX = true>
 __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtensorMap* tmA,
                                             const CUtensorMap* tmS, const SkinnyParams& p) {
     static_assert(BK % 64 == 0 && (!QB || BK == kMxBK), "MXFP4 units are kMxBK");
@@ -656,7 +658,24 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
                             if (CW * c + i < Mp) v[i] += __ldcg(slot + (CW * c + i) * 128 + n_local);
                     }
                 }
-                if (n < Nr) {
+                if constexpr (!EX) {
+                    // Plain build: one row per step through a pointer.  (The
+                    // general body below, with its per-element branches and
+                    // offsets, is a few KB of code run once per chunk: it took
+                    // about 1500 cycles per chunk, with or without its loads
+                    // and stores.)
+                    if (n < Nr) {
+                        T* cp = static_cast<T*>(Cv) + static_cast<int64_t>(CW * c) * ldc + n;
+                        const int rows = Mr - CW * c;  // rows of this chunk inside C
+#pragma unroll
+                        for (int i = 0; i < CW; ++i) {
+                            float x = v[i];
+                            if (relu) x = relu_f32(x);
+                            if (i < rows) *cp = Elem16<T>::from_float(x);
+                            cp += ldc;
+                        }
+                    }
+                } else if (n < Nr) {
                     const float bias_n = bias != nullptr ? __ldg(bias + n) : 0.0f;
 #pragma unroll
                     for (int i = 0; i < CW; ++i) {
@@ -813,20 +832,20 @@ __device__ __forceinline__ void skinny_body(const CUtensorMap* tmB, const CUtens
     }
 }
 
-template <int STAGES, int MP_MAX, typename T = __half, int BK = 64>
+template <int STAGES, int MP_MAX, typename T = __half, int BK = 64, bool EX = true>
 __global__ void __launch_bounds__(skinny_threads(STAGES, MP_MAX, false), 1)
     tg_gemm_f16_skinny(const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmA, const SkinnyParams p) {
-    skinny_body<STAGES, MP_MAX, T, false, BK>(&tmB, &tmA, nullptr, p);
+    skinny_body<STAGES, MP_MAX, T, false, BK, EX>(&tmB, &tmA, nullptr, p);
 }
 
 // C = epi(A · Bdeq) with B in MXFP4 (mxfp4.cuh), M ≤ 128, A fp16.
-template <int STAGES, int MP_MAX>
+template <int STAGES, int MP_MAX, bool EX = true>
 __global__ void __launch_bounds__(skinny_threads(STAGES, MP_MAX, true), 1)
     tg_gemm_mxfp4_skinny(const __grid_constant__ CUtensorMap tmBq,
                          const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmS, const SkinnyParams p) {
-    skinny_body<STAGES, MP_MAX, __half, true, kMxBK>(&tmBq, &tmA, &tmS, p);
+    skinny_body<STAGES, MP_MAX, __half, true, kMxBK, EX>(&tmBq, &tmA, &tmS, p);
 }
 
 // ------------------------------------------------------------------ host side
@@ -933,25 +952,42 @@ inline void skinny_mx_plan(int64_t M, int64_t N, int64_t K, int32_t num_sms, tg_
                      int64_t{SkinnyMxWide::kAStages} * SkinnyMxWide::kASlot;
 }
 
-inline cudaError_t skinny_mx_set_attributes() {
-    cudaError_t e = cudaFuncSetAttribute(tg_gemm_mxfp4_skinny<SkinnyMxNarrow::kStages, 64>,
+template <bool EX>
+inline cudaError_t skinny_mx_set_attributes_ex() {
+    cudaError_t e = cudaFuncSetAttribute(tg_gemm_mxfp4_skinny<SkinnyMxNarrow::kStages, 64, EX>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SkinnyMxNarrow::kSmemBytes);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(tg_gemm_mxfp4_skinny<SkinnyMxWide::kStages, 128>,
+    return cudaFuncSetAttribute(tg_gemm_mxfp4_skinny<SkinnyMxWide::kStages, 128, EX>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 SkinnyMxWide::kSmemBytes);
 }
 
-template <typename T>
-inline cudaError_t skinny_set_attributes() {
+inline cudaError_t skinny_mx_set_attributes() {
+    const cudaError_t e = skinny_mx_set_attributes_ex<true>();
+    return e != cudaSuccess ? e : skinny_mx_set_attributes_ex<false>();
+}
+
+template <typename T, bool EX>
+inline cudaError_t skinny_set_attributes_ex() {
     cudaError_t e = cudaFuncSetAttribute(
-        tg_gemm_f16_skinny<SkinnyNarrow::kStages, 64, T, SkinnyNarrow::kBK>,
+        tg_gemm_f16_skinny<SkinnyNarrow::kStages, 64, T, SkinnyNarrow::kBK, EX>,
         cudaFuncAttributeMaxDynamicSharedMemorySize, SkinnyNarrow::kSmemBytes);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(tg_gemm_f16_skinny<SkinnyWide::kStages, 128, T, SkinnyWide::kBK>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                SkinnyWide::kSmemBytes);
+    return cudaFuncSetAttribute(
+        tg_gemm_f16_skinny<SkinnyWide::kStages, 128, T, SkinnyWide::kBK, EX>,
+        cudaFuncAttributeMaxDynamicSharedMemorySize, SkinnyWide::kSmemBytes);
+}
+
+template <typename T>
+inline cudaError_t skinny_set_attributes() {
+    const cudaError_t e = skinny_set_attributes_ex<T, true>();
+    return e != cudaSuccess ? e : skinny_set_attributes_ex<T, false>();
+}
+
+// The plain-epilogue build applies: no bias, no residual, 16-bit C.
+inline bool skinny_plain(const SkinnyParams& prm) {
+    return prm.e.bias == nullptr && prm.e.resid == nullptr && prm.out_f32 == 0;
 }
 
 // Launch of the instantiation whose A slots fit prm.Mp.
@@ -973,15 +1009,22 @@ inline cudaError_t skinny_launch_kernel(const CUtensorMap& tmB, const CUtensorMa
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = cluster > 1 && grid % cluster == 0 ? 2 : 1;
+    using N = SkinnyNarrow;
+    using Wd = SkinnyWide;
+    const bool plain = skinny_plain(prm);
     if (prm.Mp <= 64) {
-        cfg.dynamicSmemBytes = SkinnyNarrow::kSmemBytes;
-        return cudaLaunchKernelEx(
-            &cfg, tg_gemm_f16_skinny<SkinnyNarrow::kStages, 64, T, SkinnyNarrow::kBK>, tmB, tmA,
-            prm);
+        cfg.dynamicSmemBytes = N::kSmemBytes;
+        return plain ? cudaLaunchKernelEx(&cfg,
+                                          tg_gemm_f16_skinny<N::kStages, 64, T, N::kBK, false>,
+                                          tmB, tmA, prm)
+                     : cudaLaunchKernelEx(&cfg, tg_gemm_f16_skinny<N::kStages, 64, T, N::kBK>, tmB,
+                                          tmA, prm);
     }
-    cfg.dynamicSmemBytes = SkinnyWide::kSmemBytes;
-    return cudaLaunchKernelEx(
-        &cfg, tg_gemm_f16_skinny<SkinnyWide::kStages, 128, T, SkinnyWide::kBK>, tmB, tmA, prm);
+    cfg.dynamicSmemBytes = Wd::kSmemBytes;
+    return plain ? cudaLaunchKernelEx(&cfg, tg_gemm_f16_skinny<Wd::kStages, 128, T, Wd::kBK, false>,
+                                      tmB, tmA, prm)
+                 : cudaLaunchKernelEx(&cfg, tg_gemm_f16_skinny<Wd::kStages, 128, T, Wd::kBK>, tmB,
+                                      tmA, prm);
 }
 
 // Launch of the MXFP4 instantiation whose A slots fit prm.Mp.
@@ -998,14 +1041,20 @@ inline cudaError_t skinny_mx_launch_kernel(const CUtensorMap& tmBq, const CUtens
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    const bool plain = skinny_plain(prm);
     if (prm.Mp <= 64) {
         cfg.dynamicSmemBytes = SkinnyMxNarrow::kSmemBytes;
-        return cudaLaunchKernelEx(&cfg, tg_gemm_mxfp4_skinny<SkinnyMxNarrow::kStages, 64>, tmBq,
-                                  tmA, tmS, prm);
+        return plain ? cudaLaunchKernelEx(&cfg,
+                                          tg_gemm_mxfp4_skinny<SkinnyMxNarrow::kStages, 64, false>,
+                                          tmBq, tmA, tmS, prm)
+                     : cudaLaunchKernelEx(&cfg, tg_gemm_mxfp4_skinny<SkinnyMxNarrow::kStages, 64>,
+                                          tmBq, tmA, tmS, prm);
     }
     cfg.dynamicSmemBytes = SkinnyMxWide::kSmemBytes;
-    return cudaLaunchKernelEx(&cfg, tg_gemm_mxfp4_skinny<SkinnyMxWide::kStages, 128>, tmBq, tmA,
-                              tmS, prm);
+    return plain ? cudaLaunchKernelEx(&cfg, tg_gemm_mxfp4_skinny<SkinnyMxWide::kStages, 128, false>,
+                                      tmBq, tmA, tmS, prm)
+                 : cudaLaunchKernelEx(&cfg, tg_gemm_mxfp4_skinny<SkinnyMxWide::kStages, 128>, tmBq,
+                                      tmA, tmS, prm);
 }
 
 struct SplitkWorkspace {
