@@ -228,14 +228,16 @@ def test_epilogue_pair_k_pieces(tg, monkeypatch, fmt):
                   relu=relu and not use_r, fmt=fmt, what=what)
 
 
-@pytest.mark.parametrize("cfg", ["pair256", "persistent128", "persistent64"])
+@pytest.mark.parametrize("cfg", ["pair256", "persistent128", "persistent64", "skinny"])
 def test_plain_and_full_builds_interleaved(tg, monkeypatch, cfg):
     """Plain epilogues (ReLU or none, 16-bit out) run a build of each kernel
     with the other epilogue paths compiled out.  Calls of both builds queued
     back to back on one stream (dependent launch between different kernels),
-    with one synchronisation at the end, each match the oracle."""
+    with one synchronisation at the end, each match the oracle.  The skinny
+    case (96×640×4096) splits every tile into k-pieces, so both builds' fix-up
+    paths run."""
     monkeypatch.setenv("TGEMM_FORCE_CFG", cfg)
-    M, N, K, fmt = 384, 640, 512, "f16"
+    M, N, K, fmt = (96, 640, 4096, "f16") if cfg == "skinny" else (384, 640, 512, "f16")
     A, B, bias, R, A64, B64, R64 = draw_case(M, N, K, fmt, 97)
     a, b = dev16(A, fmt), dev16(B, fmt)
     bias_d = torch.from_numpy(bias).cuda()
