@@ -121,7 +121,9 @@ __device__ __forceinline__ uint4 ld_shared_v4_u32(uint32_t addr) {
     return v;
 }
 
-template <typename T>
+// EX = false: the plain epilogue only (no bias, no residual, 16-bit C); the
+// other epilogue paths are compiled out.
+template <typename T, bool EX = true>
 __global__ void __launch_bounds__(320, 1)
     tg_gemm_sp24(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmC,
@@ -295,6 +297,7 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t cbuf = sC + static_cast<uint32_t>((warp - 2) * 2) * Cfg::kCBuf;
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
         const uint64_t c_policy = policy_evict_first();
+        const EpilogueArgs epi_e = EX ? p.e : EpilogueArgs{};
         int buf = 0;
         int it = 0;
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
@@ -330,9 +333,9 @@ __global__ void __launch_bounds__(320, 1)
                     x[t] = __uint_as_float(v0[t]);
                     x[32 + t] = __uint_as_float(v1[t]);
                 }
-                epilogue_math<T>(x, p.e, p.relu, row0 + lane, n0 + 64 * j, p.M, p.N);
+                epilogue_math<T>(x, epi_e, p.relu, row0 + lane, n0 + 64 * j, p.M, p.N);
                 epilogue_store<T>(x, cbuf, buf, &tmC, c_policy, row0, n0 + 64 * j, p.M, p.N, lane,
-                                  p.out_f32 != 0);
+                                  EX && p.out_f32 != 0);
             }
         }
         if (lane == 0) bulk_wait_group<0>();

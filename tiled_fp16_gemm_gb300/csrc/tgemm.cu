@@ -227,6 +227,10 @@ cudaError_t set_kernel_attributes() {
         e = cudaFuncSetAttribute(tg::tg_gemm_sp24<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  tg::SparseCfg::kSmemBytes);
     if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tg::tg_gemm_sp24<T, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tg::SparseCfg::kSmemBytes);
+    if (e == cudaSuccess)
         e = cudaFuncSetAttribute(tg::tg_gemm_sp24_pair<kSpPairStages, T>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  tg::SparsePairCfg<kSpPairStages>::kSmemBytes);
@@ -912,7 +916,9 @@ tg_status_t launch_sp24(const void* Ac, const void* E, const void* B, void* C, i
         cfg.gridDim = dim3(static_cast<unsigned>(grid));
         cfg.blockDim = dim3(Cfg::kThreads);
         cfg.dynamicSmemBytes = Cfg::kSmemBytes;
-        e = cudaLaunchKernelEx(&cfg, tg::tg_gemm_sp24<T>, tmA, tmB, tmE, tmC, sp);
+        e = (ep.e.bias == nullptr && ep.e.resid == nullptr && ep.out_f32 == 0)
+                ? cudaLaunchKernelEx(&cfg, tg::tg_gemm_sp24<T, false>, tmA, tmB, tmE, tmC, sp)
+                : cudaLaunchKernelEx(&cfg, tg::tg_gemm_sp24<T>, tmA, tmB, tmE, tmC, sp);
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
