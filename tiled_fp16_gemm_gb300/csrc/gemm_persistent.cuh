@@ -359,28 +359,4 @@ __global__ void tg_epilogue_only(void* C, int64_t ldc, int32_t out_f32, Epilogue
     }
 }
 
-// Copy a rows×cols matrix of 2- or 4-byte elements between two row-major
-// layouts with any leading dimensions (used to move operands whose layout the
-// tensor memory-access unit cannot address into an aligned staging buffer,
-// and a result back out of one).  Each thread moves 8 consecutive elements
-// of a row with element-sized accesses; consecutive threads take consecutive
-// chunks, so every warp reads and writes contiguous runs.
-template <typename E>
-__global__ void tg_copy_matrix(const E* __restrict__ src, int64_t ld_src, E* __restrict__ dst,
-                               int64_t ld_dst, int64_t rows, int64_t cols) {
-    const int64_t chunks_per_row = (cols + 7) / 8;
-    const int64_t total = rows * chunks_per_row;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = i / chunks_per_row;
-        const int64_t c0 = (i - r * chunks_per_row) * 8;
-        const E* s = src + r * ld_src + c0;
-        E* d = dst + r * ld_dst + c0;
-        const int n = cols - c0 < 8 ? static_cast<int>(cols - c0) : 8;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (j < n) d[j] = s[j];
-    }
-}
-
 }  // namespace tg

@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "tgemm.h"
+#include "copy_matrix.cuh"
 #include "gemm_persistent.cuh"
 #include "gemm_pair.cuh"
 #include "gemm_sparse_pair.cuh"
@@ -659,8 +660,8 @@ tg_status_t staging_buffer(int dev, cudaStream_t s, size_t bytes, void** out) {
 // Copy a rows×cols matrix of `elem_bytes` (2 or 4) byte elements.
 tg_status_t copy_matrix(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows,
                         int64_t cols, int elem_bytes, int num_sms, cudaStream_t s) {
-    const int64_t chunks = rows * ((cols + 7) / 8);
-    const int64_t blocks = (chunks + 255) / 256;
+    const int64_t steps = rows * ((cols + 255) / 256);  // warp steps of 256 elements
+    const int64_t blocks = (steps + 7) / 8;             // 8 warps per block
     const unsigned grid = static_cast<unsigned>(blocks < 8 * num_sms ? blocks : 8 * num_sms);
     if (elem_bytes == 4)
         tg::tg_copy_matrix<uint32_t><<<grid, 256, 0, s>>>(static_cast<const uint32_t*>(src),
