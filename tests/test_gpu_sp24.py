@@ -149,7 +149,7 @@ def test_sp24_integers_exact(tg, kern, M, N, K):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("M,N,K", [(2560, 2304, 288), (2304, 2560, 544)])
+@pytest.mark.parametrize("M,N,K", [(2560, 2304, 288), (2304, 2560, 544), (2500, 2300, 288)])
 def test_sp24_ring_across_tiles_exact(tg, kern, M, N, K):
     """More 256×256 tiles (90) than CTA pairs fit on the GPU, with 3 and 5
     k blocks of 128: a cluster runs two tiles, and its operand and metadata
