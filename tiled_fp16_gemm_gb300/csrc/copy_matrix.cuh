@@ -3,6 +3,8 @@
 
 #include <cstdint>
 
+#include "sm103_ptx.cuh"
+
 namespace tg {
 
 // Copy a rows×cols matrix of E (2- or 4-byte elements) between two row
@@ -22,6 +24,8 @@ __global__ void tg_copy_matrix(const E* __restrict__ src, int64_t ld_src, E* __r
     const int64_t segs = (cols + kSeg - 1) / kSeg;
     const int64_t total = rows * segs;
     const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    grid_dependency_wait();  // (a plain launch: returns at once)
+    grid_launch_dependents();  // the next kernel may set up while this one copies
     for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
          w < total; w += nwarps) {
         const int64_t r = w / segs;

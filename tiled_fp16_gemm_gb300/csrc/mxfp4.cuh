@@ -27,6 +27,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "sm103_ptx.cuh"
+
 namespace tg {
 
 // Shared-memory accesses of the converter warps (32-bit shared addresses).
@@ -196,6 +198,8 @@ __global__ void __launch_bounds__(256)
     const int64_t tiles = tiles_n * ((K + 63) / 64);
     const int nl = threadIdx.x >> 2;  // decode: column n0 + nl, codes k0 + 16 kq .. + 15
     const int kq = threadIdx.x & 3;
+    grid_dependency_wait();  // (a plain launch: returns at once)
+    grid_launch_dependents();  // the GEMM on the decoded weights may set up meanwhile
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
         const int64_t n0 = (t % tiles_n) * 64;
         const int64_t k0 = (t / tiles_n) * 64;

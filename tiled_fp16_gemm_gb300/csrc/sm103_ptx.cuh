@@ -27,8 +27,10 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 // ------------------------------------------------------------------ dependent launch
 //
-// Every kernel of this library is launched with programmatic stream
-// serialisation allowed: its CTAs may be placed on SMs that the previous
+// Every GEMM kernel of this library is launched with programmatic stream
+// serialisation allowed (the staging copy and the MXFP4 dequantisation are
+// plain launches that release their dependents early; the K = 0 fills are
+// plain launches): its CTAs may be placed on SMs that the previous
 // kernel in the stream has already left, and run their set-up (barrier
 // initialisation, tensor-memory allocation, descriptor prefetch) while that
 // kernel's last CTAs finish.  grid_dependency_wait() then blocks until the

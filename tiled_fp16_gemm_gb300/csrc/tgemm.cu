@@ -663,15 +663,24 @@ tg_status_t copy_matrix(const void* src, int64_t ld_src, void* dst, int64_t ld_d
     const int64_t steps = rows * ((cols + 255) / 256);  // warp steps of 256 elements
     const int64_t blocks = (steps + 7) / 8;             // 8 warps per block
     const unsigned grid = static_cast<unsigned>(blocks < 8 * num_sms ? blocks : 8 * num_sms);
-    if (elem_bytes == 4)
-        tg::tg_copy_matrix<uint32_t><<<grid, 256, 0, s>>>(static_cast<const uint32_t*>(src),
-                                                          ld_src, static_cast<uint32_t*>(dst),
-                                                          ld_dst, rows, cols);
-    else
-        tg::tg_copy_matrix<uint16_t><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(src),
-                                                          ld_src, static_cast<uint16_t*>(dst),
-                                                          ld_dst, rows, cols);
-    return cudaGetLastError() == cudaSuccess ? TG_OK : TG_ERR_LAUNCH;
+    // A plain launch: it starts once the previous kernel has completed (as a
+    // dependent launch its many small CTAs sat on the SMs beside the previous
+    // GEMM and slowed it).  It lets the next kernel launch early.
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    const cudaError_t e =
+        elem_bytes == 4
+            ? cudaLaunchKernelEx(&cfg, tg::tg_copy_matrix<uint32_t>,
+                                 static_cast<const uint32_t*>(src), ld_src,
+                                 static_cast<uint32_t*>(dst), ld_dst, rows, cols)
+            : cudaLaunchKernelEx(&cfg, tg::tg_copy_matrix<uint16_t>,
+                                 static_cast<const uint16_t*>(src), ld_src,
+                                 static_cast<uint16_t*>(dst), ld_dst, rows, cols);
+    if (e != cudaSuccess) cudaGetLastError();
+    return e == cudaSuccess ? TG_OK : TG_ERR_LAUNCH;
 }
 
 // Launch the planned kernel for operands in the tensor memory-access layout.
@@ -1202,10 +1211,19 @@ tg_status_t tg_gemm_mxfp4(const void* A, const void* Bq, const void* Bscale, voi
     if (st != TG_OK) return st;
     const int64_t tiles = ((K + 63) / 64) * ((N + 63) / 64);  // 64 × 64 per block iteration
     const unsigned grid = static_cast<unsigned>(tiles < 8 * ds->num_sms ? tiles : 8 * ds->num_sms);
-    tg::tg_mxfp4_dequant_f16<<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(Bq), ldbq,
-                                                  static_cast<const uint8_t*>(Bscale), ldbs, K, N,
-                                                  static_cast<uint16_t*>(deq), ldd);
-    if (cudaGetLastError() != cudaSuccess) return TG_ERR_LAUNCH;
+    // A plain launch that lets the next kernel launch early (as a dependent
+    // launch it slowed the previous kernel, like the staging copy).
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    if (cudaLaunchKernelEx(&cfg, tg::tg_mxfp4_dequant_f16, static_cast<const uint8_t*>(Bq), ldbq,
+                           static_cast<const uint8_t*>(Bscale), ldbs, K, N,
+                           static_cast<uint16_t*>(deq), ldd) != cudaSuccess) {
+        cudaGetLastError();
+        return TG_ERR_LAUNCH;
+    }
     return gemm_impl<__half>(A, deq, C, M, N, K, lda, ldd, ldc, ep, stream);
 }
 
