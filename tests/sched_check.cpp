@@ -1,9 +1,11 @@
 // Host-side brute-force check of the scheduling arithmetic in tile_schedule.h
-// (compiled and run by test_host_logic.py with the system C++ compiler).
+// and of the 2:4 kernel choice in sparse_plan.h (compiled and run by
+// test_abi.py with the system C++ compiler).
 #include <cstdio>
 #include <cstdlib>
 #include <vector>
 
+#include "sparse_plan.h"
 #include "tile_schedule.h"
 
 static int fail(const char* what, long long a, long long b, long long c) {
@@ -107,6 +109,18 @@ int main() {
         tg::pair_launch_shape(256, 76, 128, &P, &S, &H);  // 4096x4096x16384
         if (P != 76 || S != 2 || H != 1) return fail("long-k two pieces", P, S, H);
     }
+    // the 2:4 kernel choice on 152 SMs with 76 resident pairs, at the shapes
+    // it was measured on (1: CTA pairs)
+    const long long sp[][4] = {{8192, 28672, 4096, 1}, {2048, 2048, 4096, 1}, {2048, 2048, 1024, 1},
+                               {512, 512, 8192, 1},    {1024, 1024, 4096, 1}, {256, 2048, 4096, 1},
+                               {256, 256, 16384, 1},   {1024, 2048, 2048, 1}, {1024, 1024, 2048, 0},
+                               {1024, 1024, 1024, 0},  {2048, 1024, 512, 0},  {512, 512, 512, 0},
+                               {128, 4096, 8192, 0},   {96, 160, 192, 0}};
+    for (auto& c : sp) {
+        const bool pair = tg::sp24_use_pairs(c[0], c[1], c[2], 76, 152);
+        if (pair != (c[3] == 1)) return fail("sp24 kernel choice", c[0], c[1], c[2]);
+    }
+    if (tg::sp24_use_pairs(8192, 28672, 4096, 0, 152)) return fail("sp24 no pairs", 0, 0, 0);
     std::printf("OK\n");
     return 0;
 }

@@ -20,6 +20,7 @@
 #include "gemm_sparse_pair.cuh"
 #include "gemm_skinny.cuh"
 #include "gemm_sparse.cuh"
+#include "sparse_plan.h"
 #include "tile_schedule.h"
 
 namespace {
@@ -837,17 +838,8 @@ bool forced_dense_kernel() {
 }
 
 // 2:4 sparse A: tensor maps, kernel choice, tile plan and launch (operands in
-// the tensor memory-access layout, checked by the caller).  The CTA-pair
-// kernel (256×256 tiles) runs once its tiles fill every resident pair at
-// least once, and also below that when K ≥ 1024 and one-CTA tiles would
-// occupy more than half the SMs (measured on GB300: 2048×2048×4096 22.7 µs
-// against 37.8 µs, 1536×1536×4096 20.8 against 22.7 µs, 2048×2048×1024 12.4
-// against 14.5 µs; a tie at K = 512), and for K ≥ 4096 with M > 128 whatever
-// the tile count: per k block a pair moves a 256×256 tile in less time than a
-// one-CTA kernel moves a 128×128 one (512×512×8192 28.2 against 32.3 µs,
-// 1024×1024×4096 17.0 against 17.9 µs).  Smaller problems take the one-CTA
-// kernel (128×128 tiles, four times the tiles in flight: 1024³ 7.1 against
-// 8.4 µs, 2048×1024×512 5.5 against 7.0 µs).
+// the tensor memory-access layout, checked by the caller).  The kernel is
+// tg::sp24_use_pairs' choice (sparse_plan.h).
 // TGEMM_FORCE_SP24 = pair | cta overrides the choice (tests and sweeps).  Both kernels take the same tensor maps: per CTA 128 rows of
 // Ac and E and 128 k of B per stage.
 template <typename T>
@@ -868,11 +860,8 @@ tg_status_t launch_sp24(const void* Ac, const void* E, const void* B, void* C, i
         !(ep.out_f32 ? encode_2d(&tmC, C, N, M, ldc * 4, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)
                      : encode_2d(&tmC, C, N, M, ldc * 2, 64, 32, dt)))
         return TG_ERR_LAUNCH;
-    const int64_t pair_tiles = ceil_div(M, PairCfg::BM) * ceil_div(N, PairCfg::BN);
-    const int64_t cta_tiles = ceil_div(M, Cfg::BM) * ceil_div(N, Cfg::BN);
-    bool pair = ds->max_sp_pairs >= 1 &&
-                (pair_tiles >= ds->max_sp_pairs || (K >= 1024 && 2 * cta_tiles > ds->num_sms) ||
-                 (K >= 4096 && M > 128));
+    static_assert(PairCfg::BN == 256 && Cfg::BN == 128, "the tile sizes sparse_plan.h assumes");
+    bool pair = tg::sp24_use_pairs(M, N, K, ds->max_sp_pairs, ds->num_sms);
     if (const char* f = std::getenv("TGEMM_FORCE_SP24")) {
         if (std::strcmp(f, "pair") == 0) pair = ds->max_sp_pairs >= 1;
         if (std::strcmp(f, "cta") == 0) pair = false;
